@@ -1,0 +1,433 @@
+"""Benchmark of the GB300 gated delta-net core.
+
+Headline workload (one step = one fused gdn_decode_step over the batch: conv +
+SiLU, split, q/k l2 norm, gates, the delta-rule update of the fp32 state in
+place, and the gated RMSNorm epilogue):
+  batched decode, B=64 sequences x 1 token, Hk=16, Hv=32, D=128, Tiled map,
+  negative-rate decay, bf16 activations ~N(0,1), fp32 state ~N(0,0.02)
+  (128 MiB), conv state bf16 ~N(0,0.1); 16 distinct input sets cycled.
+Metric: state GB/s = 2 * B * Hv * D^2 * 4 bytes / step time.
+
+A second block measures chunked prefill (one sequence of T=4096, Hk=16, Hv=32,
+D=128, Grouped, bf16 raw q/k/v/z/a/b, fused gated RMSNorm) in tokens/s.
+
+Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on
+the launching stream; a 512 MiB buffer is overwritten between timed steps so
+no step starts with the previous step's state in L2. Under torchrun each rank
+runs its own batch (weak scaling, no collective on the data path); the step
+time is the max over ranks.
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload instead (the CPU baseline).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import gdn_inputs as gi  # noqa: E402
+
+PROFILES = os.path.join(ROOT, "profiles")
+DECODE_WORKLOAD = ("batched decode B=64 x 1 token, Hk=16 Hv=32 D=128, Tiled, negative-rate, "
+                   "bf16 activations, fp32 state")
+PREFILL_WORKLOAD = "chunked prefill N=1 T=4096, Hk=16 Hv=32 D=128, Grouped, log-rate, bf16"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def _kernel_hash(*files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gated_delta_net_causal_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _profile_traffic(name: str, khash: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the kernel source as it is now (else None)."""
+    path = os.path.join(PROFILES, name)
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and not line.lstrip().startswith("#"):
+                k, v = line.split("=", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("kernel_hash") != khash:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier_max(value: float, ws: int) -> float:
+    if ws == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], device="cuda")
+    dist.barrier()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------- GPU arm
+
+def _decode_setup(batch: int, sets: int, rank: int):
+    import gated_delta_net_causal_gb300 as gdn
+    wl = gi.workload_batched_decode(batch=batch, sets=sets)
+    shape, w = wl["shape"], wl["weights"]
+    d = gdn.dims(16, 32, 128, map=shape.map, decay=shape.decay, io_dtype=torch.bfloat16)
+    dev = {k: getattr(w, k).cuda() for k in ("conv_w", "decay_param", "dt_bias", "norm_w")}
+    steps = [{"x": s.mixed_qkv.cuda(), "a": s.a.cuda(), "b": s.b.cuda(),
+              "z": s.z.cuda().view(batch, 32, 128)} for s in wl["steps"]]
+    host = [{"x": s.mixed_qkv.pin_memory(), "a": s.a.pin_memory(), "b": s.b.pin_memory(),
+             "z": s.z.pin_memory()} for s in wl["steps"]]
+    state = wl["state"].cuda()
+    cstate = wl["conv_state"].cuda()
+    out = torch.empty((batch, 32, 128), device="cuda", dtype=torch.bfloat16)
+    return gdn, d, dev, steps, host, state, cstate, out, shape
+
+
+def _decode_call(gdn, d, dev, inp, state, cstate, out):
+    gdn.gdn_decode_step(d, inp["x"], inp["a"], inp["b"], dev["decay_param"], dev["dt_bias"],
+                        dev["conv_w"], cstate, state, core_out=None, z=inp["z"],
+                        norm_w=dev["norm_w"], out=out)
+
+
+def run_gpu(args, ws, rank, local):
+    torch.cuda.set_device(local)
+    peaks = _peaks()
+    batch = args.batch
+    gdn, d, dev, steps, host, state, cstate, out, shape = _decode_setup(batch, 16, rank)
+    flush = torch.empty(512 * 1024 * 1024 // 4, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+    B, Hv, D, C = batch, 32, 128, shape.qkv_features
+    state_bytes = 2 * B * Hv * D * D * 4
+    other_bytes = (B * C * 2 + 2 * B * Hv * 2 + B * Hv * D * 2 + 2 * B * C * 3 * 2
+                   + B * Hv * D * 2 + C * 4 * 2 + 3 * Hv * 4 + D * 4)
+
+    for i in range(args.warmup):
+        _decode_call(gdn, d, dev, steps[i % 16], state, cstate, out)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        _decode_call(gdn, d, dev, steps[i % 16], state, cstate, out)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    times = [a.elapsed_time(b) * 1e-3 for a, b in ev]
+    t_step = sum(times) / len(times)
+    t_step = _barrier_max(t_step, ws)
+    ms_per_step = t_step * 1e3
+
+    # end to end through the C ABI with host buffers: H2D of the step's
+    # activations from pinned memory, the call, D2H of the gated output
+    out_host = torch.empty((B, Hv, D), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = min(args.steps, 64)
+    dbuf = {k: torch.empty_like(v, device="cuda") for k, v in host[0].items()}
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h = out_host.numel() * out_host.element_size()
+    torch.cuda.synchronize()
+    e2e_times = []
+    for i in range(e2e_steps):
+        flush.fill_(float(i))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k in dbuf:
+            dbuf[k].copy_(host[i % 16][k], non_blocking=True)
+        _decode_call(gdn, d, dev, {"x": dbuf["x"], "a": dbuf["a"], "b": dbuf["b"],
+                                   "z": dbuf["z"].view(B, Hv, D)}, state, cstate, out)
+        out_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_times.append(time.perf_counter() - t0)
+    t_e2e = _barrier_max(statistics.mean(e2e_times), ws)
+
+    # chunked prefill block
+    prefill = run_prefill(args, peaks, ws) if not args.no_prefill else None
+
+    if rank != 0:
+        return None
+    value = ws * state_bytes / t_step / 1e9
+    achieved = (state_bytes + other_bytes) / t_step / 1e9
+    khash = _kernel_hash("decode.cu", "gdn_common.cuh")
+    line = {
+        "metric": "GDN decode state GB/s (% HBM peak); chunked prefill tokens/s (% roofline)",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": DECODE_WORKLOAD, "batch_per_gpu": B, "global_batch": B * ws,
+                   "n_k_heads": 16, "n_v_heads": 32, "head_dim": 128,
+                   "state_bytes_per_step": state_bytes, "l2": "512 MiB buffer overwritten "
+                   "between timed steps (state 128 MiB)", "parallelism": f"replicas x{ws} "
+                   "(sequences sharded, no collective)"},
+        "seq_per_s": round(ws * B / t_step, 1),
+        "hbm_frac_state": round(value / ws / peaks["hbm_gbs"], 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": _profile_traffic("decode_step_b64.txt", khash),
+                     "peak_source": peaks["source"], "kernel": "decode_step_kernel<bf16,128>",
+                     "algorithmic_bytes_per_launch": state_bytes + other_bytes},
+        "e2e": {"value": round(ws * state_bytes / t_e2e / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(t_e2e * 1e3, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if prefill is not None:
+        line["prefill"] = prefill
+    if not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = cpu_baseline_decode(seconds=args.cpu_seconds)
+    return line
+
+
+def run_prefill(args, peaks, ws):
+    import gated_delta_net_causal_gb300 as gdn
+    T = 4096
+    wl = gi.workload_prefill(T, random_state=True)
+    shape, w = wl["shape"], wl["weights"]
+    d = gdn.dims(16, 32, 128, map=shape.map, decay=shape.decay, io_dtype=torch.bfloat16)
+    q, k, v = (wl[n].cuda().view(T, -1) for n in ("q", "k", "v"))
+    a, b, z = wl["a"].cuda(), wl["b"].cuda(), wl["z"].cuda()
+    dp, dt, nw = w.decay_param.cuda(), w.dt_bias.cuda(), w.norm_w.cuda()
+    cu = wl["cu_seqlens"].cuda()
+    s0 = wl["state"].cuda()
+    state = s0.clone()
+    out = torch.empty((T, 32, 128), device="cuda", dtype=torch.bfloat16)
+    flush = torch.empty(512 * 1024 * 1024 // 4, device="cuda", dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        gdn.gdn_prefill_chunked(d, cu, q, k, v, a, b, dp, dt, state, core_out=None, z=z,
+                                norm_w=nw, out=out)
+
+    for _ in range(3):
+        state.copy_(s0)
+        call()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 20))
+    times = []
+    for i in range(n):
+        state.copy_(s0)
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e-3)
+    t = _barrier_max(statistics.mean(times), ws)
+    Hk, Hv, D, Cc = 16, 32, 128, 64
+    flop_per_token = Hv * (6 * D * D + 6 * Cc * D + Cc * Cc / 3) + Hk * 4 * Cc * D
+    flops = flop_per_token * T
+    byts = T * (2 * Hk * D + 2 * Hv * D) * 2 + T * Hv * D * 2 + 2 * Hv * D * D * 4 + 4 * T * Hv * 2
+    return {"workload": PREFILL_WORKLOAD, "value": round(ws * T / t, 1), "unit": "tokens/s",
+            "ms_per_call": round(t * 1e3, 4), "calls": n,
+            "roofline": {"bound": "tensor", "achieved": round(flops / t / 1e12, 3),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(flops / t / 1e12 / peaks["bf16_tflops"], 5),
+                         "traffic": None, "peak_source": peaks["source"],
+                         "algorithmic_flops_per_call": flops,
+                         "hbm_frac": round(byts / t / 1e9 / peaks["hbm_gbs"], 4),
+                         "kernel": "prefill_cc_kernel<bf16,128,32>"}}
+
+
+# --------------------------------------------------------------- CPU oracle arm
+
+def cpu_baseline_decode(seconds: float = 15.0, threads: int = None):
+    """The oracle (as it stands) on a bounded sample of the decode workload:
+    repeated decode steps over a subset of the B=64 sequences, one sequence
+    per host thread (ctypes releases the GIL inside the C oracle)."""
+    import concurrent.futures as cf
+    import oracle
+    threads = threads or min(os.cpu_count() or 1, 64)
+    wl = gi.workload_batched_decode(batch=64, sets=2)
+    shape, w = wl["shape"], wl["weights"]
+    F = gi.as_f64
+    cw, dp, dt, nw = F(w.conv_w), F(w.decay_param), F(w.dt_bias), F(w.norm_w)
+    seqs = list(range(min(threads, 64)))
+    X = [F(s.mixed_qkv) for s in wl["steps"]]
+    A = [F(s.a) for s in wl["steps"]]
+    Bb = [F(s.b) for s in wl["steps"]]
+    Z = [F(s.z) for s in wl["steps"]]
+    cs = {b: F(wl["conv_state"])[b] for b in seqs}
+    S = {b: F(wl["state"])[b] for b in seqs}
+
+    def one(b, i):
+        _, _, cs[b], S[b] = oracle.segment(16, 32, 128, shape.map, shape.decay,
+                                           X[i % 2][b:b + 1], A[i % 2][b:b + 1],
+                                           Bb[i % 2][b:b + 1], Z[i % 2][b:b + 1], cw, dp, dt,
+                                           nw, cs[b], S[b])
+
+    oracle.lib()
+    done = 0
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=len(seqs)) as ex:
+        i = 0
+        while time.perf_counter() - t0 < seconds or i == 0:
+            list(ex.map(lambda b: one(b, i), seqs))
+            done += len(seqs)
+            i += 1
+    el = time.perf_counter() - t0
+    bytes_per_seq = 2 * 32 * 128 * 128 * 4
+    return {"value": round(done * bytes_per_seq / el / 1e9, 4), "unit": "GB/s",
+            "cores": len(seqs), "kind": "oracle",
+            "sample": f"{i} decode steps x {len(seqs)} of the 64 sequences (fp64 oracle, "
+                      f"one sequence per thread), {el:.1f} s"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    cb = cpu_baseline_decode(seconds=max(5.0, min(60.0, args.cpu_seconds)))
+    return {"impl": "reference",
+            "metric": "GDN decode state GB/s (% HBM peak); chunked prefill tokens/s (% roofline)",
+            "value": cb["value"], "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": DECODE_WORKLOAD, "global_batch": 64},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--batch", type=int, default=64)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
+    try:
+        if args.impl == "reference":
+            line = run_reference(args, ws, rank)
+        else:
+            line = run_gpu(args, ws, rank, local)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

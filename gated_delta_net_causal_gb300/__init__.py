@@ -1,0 +1,211 @@
+"""GB300 gated delta-net core: a thin Python binding over libgdn.so.
+
+Each function takes torch CUDA tensors, checks only what marshalling needs
+(device, dtype, contiguity), and calls the C-ABI entry point of the same name
+on the current torch CUDA stream. Every step of the computation runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback. If libgdn.so is
+missing the import of the library raises.
+
+The C ABI itself is declared in ``include/gdn.h``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+GDN_OK = 0
+GDN_MAP_GROUPED, GDN_MAP_TILED = 0, 1
+GDN_DECAY_LOG_RATE, GDN_DECAY_NEGATIVE_RATE = 0, 1
+GDN_F16, GDN_BF16, GDN_F32 = 0, 1, 2
+GDN_QK_PRENORMALIZED, GDN_GATES_PRECOMPUTED = 1, 2
+
+_TORCH_TO_GDN = {torch.float16: GDN_F16, torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}
+_GDN_TO_TORCH = {v: k for k, v in _TORCH_TO_GDN.items()}
+
+
+class GdnDims(ctypes.Structure):
+    _fields_ = [("n_k_heads", ctypes.c_int32), ("n_v_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("map", ctypes.c_int32),
+                ("decay", ctypes.c_int32), ("io_dtype", ctypes.c_int32),
+                ("l2_eps", ctypes.c_float), ("rms_eps", ctypes.c_float)]
+
+
+def dims(n_k_heads: int, n_v_heads: int, head_dim: int, map: int = GDN_MAP_GROUPED,
+         decay: int = GDN_DECAY_LOG_RATE, io_dtype=torch.bfloat16, l2_eps: float = 1e-6,
+         rms_eps: float = 1e-6) -> GdnDims:
+    dt = _TORCH_TO_GDN[io_dtype] if isinstance(io_dtype, torch.dtype) else int(io_dtype)
+    return GdnDims(n_k_heads, n_v_heads, head_dim, map, decay, dt, l2_eps, rms_eps)
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+_lib = None
+LIB_PATH = _build.LIB
+
+
+def library() -> ctypes.CDLL:
+    """Load libgdn.so (built by ``__graft_entry__.build()`` / ``_build.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                              "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        pd = ctypes.POINTER(GdnDims)
+        L.gdn_status_string.restype = ctypes.c_char_p
+        L.gdn_status_string.argtypes = [i32]
+        L.gdn_version.restype = i32
+        L.gdn_version.argtypes = []
+        L.gdn_qkv_features.restype = i64
+        L.gdn_qkv_features.argtypes = [pd]
+        L.gdn_conv_update.restype = ctypes.c_int
+        L.gdn_conv_update.argtypes = [pd, i32, vp, i64, vp, vp, vp, vp, vp]
+        L.gdn_decode_step.restype = ctypes.c_int
+        L.gdn_decode_step.argtypes = [pd, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.gdn_prefill_chunked.restype = ctypes.c_int
+        L.gdn_prefill_chunked.argtypes = [pd, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, vp, vp,
+                                          vp, i32, vp, vp, vp, vp, vp, vp]
+        L.gdn_gated_rmsnorm.restype = ctypes.c_int
+        L.gdn_gated_rmsnorm.argtypes = [pd, i64, vp, vp, vp, vp, vp]
+        L.gdn_device_error.restype = ctypes.c_int
+        L.gdn_device_error.argtypes = [ctypes.POINTER(i32), i32]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return library().gdn_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != GDN_OK:
+        raise GdnError(status, f"{what}: {status_string(status)}")
+
+
+def _ptr(t: Optional[torch.Tensor], name: str, dtype=None) -> Optional[int]:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream or None
+    return int(stream) or None
+
+
+def _io(d: GdnDims):
+    return _GDN_TO_TORCH[d.io_dtype]
+
+
+def gdn_conv_update(d: GdnDims, cu_seqlens: torch.Tensor, x: torch.Tensor, conv_w: torch.Tensor,
+                    conv_state: torch.Tensor, y: torch.Tensor, stream=None) -> torch.Tensor:
+    io = _io(d)
+    n = cu_seqlens.numel() - 1
+    total = x.shape[0] if x.dim() > 0 else 0
+    _check(library().gdn_conv_update(
+        ctypes.byref(d), n, _ptr(cu_seqlens, "cu_seqlens", torch.int32), total,
+        _ptr(x, "x", io), _ptr(conv_w, "conv_w", io), _ptr(conv_state, "conv_state", io),
+        _ptr(y, "y", io), _stream(stream)), "gdn_conv_update")
+    return y
+
+
+def gdn_decode_step(d: GdnDims, mixed_qkv, a, b, decay_param, dt_bias, conv_w, conv_state,
+                    state, core_out=None, z=None, norm_w=None, out=None, stream=None):
+    io = _io(d)
+    batch = mixed_qkv.shape[0]
+    f32 = torch.float32
+    _check(library().gdn_decode_step(
+        ctypes.byref(d), batch, _ptr(mixed_qkv, "mixed_qkv", io), _ptr(a, "a", io),
+        _ptr(b, "b", io), _ptr(decay_param, "decay_param", f32), _ptr(dt_bias, "dt_bias", f32),
+        _ptr(conv_w, "conv_w", io), _ptr(conv_state, "conv_state", io),
+        _ptr(state, "state", f32), _ptr(core_out, "core_out", f32), _ptr(z, "z", io),
+        _ptr(norm_w, "norm_w", f32), _ptr(out, "out", io), _stream(stream)), "gdn_decode_step")
+    return core_out, out
+
+
+def _token_stride(t: torch.Tensor, name: str) -> int:
+    if t.dim() < 2 or t.stride(-1) != 1:
+        raise ValueError(f"{name} must have a unit innermost stride")
+    return int(t.stride(0))
+
+
+def _base_ptr(t: torch.Tensor, name: str, dtype) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def gdn_prefill_chunked(d: GdnDims, cu_seqlens, q, k, v, a, b, decay_param, dt_bias, state,
+                        core_out=None, z=None, norm_w=None, out=None, flags: int = 0,
+                        stream=None):
+    """q, k: [T][Hk*D] (or views with a token stride, e.g. column slices of the
+    conv output); v: [T][Hv*D] likewise. With GDN_GATES_PRECOMPUTED a and b are
+    fp32 g and beta."""
+    io = _io(d)
+    f32 = torch.float32
+    gate_dt = f32 if (flags & GDN_GATES_PRECOMPUTED) else io
+    total = q.shape[0]
+    _check(library().gdn_prefill_chunked(
+        ctypes.byref(d), cu_seqlens.numel() - 1, _ptr(cu_seqlens, "cu_seqlens", torch.int32),
+        total, _base_ptr(q, "q", io), _token_stride(q, "q"), _base_ptr(k, "k", io),
+        _token_stride(k, "k"), _base_ptr(v, "v", io), _token_stride(v, "v"),
+        _ptr(a, "a", gate_dt), _ptr(b, "b", gate_dt), _ptr(decay_param, "decay_param", f32),
+        _ptr(dt_bias, "dt_bias", f32), int(flags), _ptr(state, "state", f32),
+        _ptr(core_out, "core_out", f32), _ptr(z, "z", io), _ptr(norm_w, "norm_w", f32),
+        _ptr(out, "out", io), _stream(stream)), "gdn_prefill_chunked")
+    return core_out, out
+
+
+def gdn_gated_rmsnorm(d: GdnDims, o, z, norm_w, y, stream=None):
+    io = _io(d)
+    rows = o.numel() // d.head_dim
+    _check(library().gdn_gated_rmsnorm(
+        ctypes.byref(d), rows, _ptr(o, "o", torch.float32), _ptr(z, "z", io),
+        _ptr(norm_w, "norm_w", torch.float32), _ptr(y, "y", io), _stream(stream)),
+        "gdn_gated_rmsnorm")
+    return y
+
+
+def gdn_device_error(clear: bool = True) -> int:
+    st = ctypes.c_int32(0)
+    _check(library().gdn_device_error(ctypes.byref(st), 1 if clear else 0), "gdn_device_error")
+    return st.value
+
+
+def gdn_qkv_features(d: GdnDims) -> int:
+    return int(library().gdn_qkv_features(ctypes.byref(d)))
+
+
+def gdn_version() -> int:
+    return int(library().gdn_version())
+
+
+__all__ = ["GdnDims", "GdnError", "dims", "library", "status_string", "gdn_conv_update",
+           "gdn_decode_step", "gdn_prefill_chunked", "gdn_gated_rmsnorm", "gdn_device_error",
+           "gdn_qkv_features", "gdn_version", "GDN_MAP_GROUPED", "GDN_MAP_TILED",
+           "GDN_DECAY_LOG_RATE", "GDN_DECAY_NEGATIVE_RATE", "GDN_F16", "GDN_BF16", "GDN_F32",
+           "GDN_QK_PRENORMALIZED", "GDN_GATES_PRECOMPUTED", "LIB_PATH"]

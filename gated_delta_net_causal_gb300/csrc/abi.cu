@@ -1,0 +1,330 @@
+// C ABI entry points: host-side validation, then one launcher call each.
+// Nothing is enqueued unless every check passes.
+#include <math.h>
+#include <stdint.h>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+using gdn::DecodeArgs;
+
+constexpr int64_t kMaxGridY = 65535;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t dtype_size(int32_t dt) {
+  switch (dt) {
+    case GDN_F16:
+    case GDN_BF16: return 2;
+    case GDN_F32: return 4;
+    default: return 0;
+  }
+}
+
+// a*b with overflow detection into *out; false on overflow or negative inputs
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > INT64_MAX / a) return false;
+  *out = a * b;
+  return true;
+}
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+Range range_of(const void* p, int64_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Range{lo, lo + (uintptr_t)(bytes > 0 ? bytes : 0)};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo; }
+
+gdn_status check_dims(const gdn_dims* d) {
+  if (d == nullptr) return GDN_ERR_INVALID_ARG;
+  if (d->n_k_heads < 1 || d->n_v_heads < 1) return GDN_ERR_INVALID_ARG;
+  if (d->n_v_heads % d->n_k_heads != 0) return GDN_ERR_INVALID_ARG;
+  if (d->map != GDN_MAP_GROUPED && d->map != GDN_MAP_TILED) return GDN_ERR_INVALID_ARG;
+  if (d->decay != GDN_DECAY_LOG_RATE && d->decay != GDN_DECAY_NEGATIVE_RATE)
+    return GDN_ERR_INVALID_ARG;
+  if (dtype_size(d->io_dtype) == 0) return GDN_ERR_INVALID_ARG;
+  if (!(d->l2_eps >= 0.f) || !isfinite(d->l2_eps)) return GDN_ERR_INVALID_ARG;
+  if (!(d->rms_eps >= 0.f) || !isfinite(d->rms_eps)) return GDN_ERR_INVALID_ARG;
+  if (d->head_dim < 1) return GDN_ERR_INVALID_ARG;
+  if (d->head_dim != 32 && d->head_dim != 64 && d->head_dim != 128) return GDN_ERR_UNSUPPORTED;
+  if (d->n_v_heads > kMaxGridY) return GDN_ERR_EXTENT;
+  const int64_t C = (2 * (int64_t)d->n_k_heads + d->n_v_heads) * d->head_dim;
+  if (C > INT32_MAX / 4) return GDN_ERR_EXTENT;
+  return GDN_OK;
+}
+
+int64_t qkv_features(const gdn_dims* d) {
+  return (2 * (int64_t)d->n_k_heads + d->n_v_heads) * d->head_dim;
+}
+
+gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_status_string(int32_t status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: null pointer, bad enum or bad dims";
+    case GDN_ERR_EXTENT: return "GDN_ERR_EXTENT: a size product exceeds the index or launch range";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: shape not implemented";
+    case GDN_ERR_ALIAS: return "GDN_ERR_ALIAS: an output overlaps an input";
+    case GDN_ERR_ALIGN: return "GDN_ERR_ALIGN: pointer or stride not 16-byte aligned";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: the CUDA runtime reported an error";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a device-side bounded wait gave up";
+    default: return "GDN_ERR_UNKNOWN";
+  }
+}
+
+int32_t gdn_version(void) { return 100; }
+
+int64_t gdn_qkv_features(const gdn_dims* dims) {
+  if (check_dims(dims) != GDN_OK) return -1;
+  return qkv_features(dims);
+}
+
+gdn_status gdn_conv_update(const gdn_dims* dims, int32_t num_seqs, const int32_t* cu_seqlens,
+                           int64_t total_tokens, const void* x, const void* conv_w,
+                           void* conv_state, void* y, void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
+  if (num_seqs == 0 && total_tokens > 0) return GDN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return GDN_OK;
+  if (cu_seqlens == nullptr || conv_w == nullptr || conv_state == nullptr) return GDN_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (x == nullptr || y == nullptr)) return GDN_ERR_INVALID_ARG;
+  const int64_t es = dtype_size(dims->io_dtype);
+  const int64_t C = qkv_features(dims);
+  int64_t xel = 0, xbytes = 0, sel = 0, sbytes = 0;
+  if (!mul_ok(total_tokens, C, &xel) || !mul_ok(xel, es, &xbytes)) return GDN_ERR_EXTENT;
+  if (!mul_ok((int64_t)num_seqs, C * 3, &sel) || !mul_ok(sel, es, &sbytes)) return GDN_ERR_EXTENT;
+  if ((total_tokens + 63) / 64 > INT32_MAX) return GDN_ERR_EXTENT;
+  if (!aligned16(cu_seqlens) || !aligned16(conv_w) || !aligned16(conv_state)) return GDN_ERR_ALIGN;
+  if (total_tokens > 0 && (!aligned16(x) || !aligned16(y))) return GDN_ERR_ALIGN;
+  if (total_tokens > 0) {
+    const Range ry = range_of(y, xbytes);
+    if (overlap(ry, range_of(x, xbytes)) || overlap(ry, range_of(conv_state, sbytes)) ||
+        overlap(ry, range_of(conv_w, C * 4 * es)))
+      return GDN_ERR_ALIAS;
+  }
+  if (overlap(range_of(conv_state, sbytes), range_of(x, xbytes)) ||
+      overlap(range_of(conv_state, sbytes), range_of(conv_w, C * 4 * es)))
+    return GDN_ERR_ALIAS;
+  gdn::ConvArgs a{};
+  a.cu_seqlens = cu_seqlens;
+  a.N = num_seqs;
+  a.T = total_tokens;
+  a.C = (int32_t)C;
+  a.x = x;
+  a.conv_w = conv_w;
+  a.conv_state = conv_state;
+  a.y = y;
+  return cuda_status(gdn::launch_conv(a, dims->io_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_decode_step(const gdn_dims* dims, int32_t batch, const void* mixed_qkv,
+                           const void* a, const void* b, const float* decay_param,
+                           const float* dt_bias, const void* conv_w, void* conv_state,
+                           float* state, float* core_out, const void* z, const float* norm_w,
+                           void* out, void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (batch < 0) return GDN_ERR_INVALID_ARG;
+  if (batch > kMaxGridY) return GDN_ERR_EXTENT;
+  const int rep = dims->n_v_heads / dims->n_k_heads;
+  if (rep > 8) return GDN_ERR_UNSUPPORTED;
+  if (batch == 0) return GDN_OK;
+  if (!mixed_qkv || !a || !b || !decay_param || !dt_bias || !conv_w || !conv_state || !state)
+    return GDN_ERR_INVALID_ARG;
+  if (core_out == nullptr && z == nullptr) return GDN_ERR_INVALID_ARG;
+  if (z != nullptr && (norm_w == nullptr || out == nullptr)) return GDN_ERR_INVALID_ARG;
+  const void* ptrs[] = {mixed_qkv, a, b, decay_param, dt_bias, conv_w, conv_state, state};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return GDN_ERR_ALIGN;
+  if ((core_out && !aligned16(core_out)) || (z && (!aligned16(z) || !aligned16(norm_w) || !aligned16(out))))
+    return GDN_ERR_ALIGN;
+  const int64_t es = dtype_size(dims->io_dtype);
+  const int64_t C = qkv_features(dims), Hv = dims->n_v_heads, D = dims->head_dim;
+  int64_t state_bytes = 0, tmp = 0;
+  if (!mul_ok((int64_t)batch * Hv, D * D * 4, &state_bytes)) return GDN_ERR_EXTENT;
+  if (!mul_ok((int64_t)batch, C * 3 * es, &tmp)) return GDN_ERR_EXTENT;
+  const int64_t conv_bytes = tmp;
+  const int64_t x_bytes = (int64_t)batch * C * es;
+  const int64_t o_bytes_f32 = (int64_t)batch * Hv * D * 4;
+  const int64_t o_bytes_io = (int64_t)batch * Hv * D * es;
+  const int64_t gate_bytes = (int64_t)batch * Hv * es;
+  const Range inputs[] = {range_of(mixed_qkv, x_bytes), range_of(a, gate_bytes),
+                          range_of(b, gate_bytes),      range_of(decay_param, Hv * 4),
+                          range_of(dt_bias, Hv * 4),    range_of(conv_w, C * 4 * es),
+                          range_of(z, z ? o_bytes_io : 0), range_of(norm_w, norm_w ? D * 4 : 0)};
+  const Range rs = range_of(state, state_bytes), rc = range_of(conv_state, conv_bytes);
+  const Range ro = range_of(core_out, core_out ? o_bytes_f32 : 0);
+  const Range ry = range_of(out, z ? o_bytes_io : 0);
+  for (const Range& in : inputs) {
+    if (overlap(rs, in) || overlap(rc, in) || overlap(ro, in) || overlap(ry, in)) return GDN_ERR_ALIAS;
+  }
+  if (overlap(rs, rc) || overlap(rs, ro) || overlap(rs, ry) || overlap(rc, ro) || overlap(rc, ry) ||
+      overlap(ro, ry))
+    return GDN_ERR_ALIAS;
+  DecodeArgs p{};
+  p.mixed_qkv = mixed_qkv;
+  p.a = a;
+  p.b = b;
+  p.decay_param = decay_param;
+  p.dt_bias = dt_bias;
+  p.conv_w = conv_w;
+  p.conv_state = conv_state;
+  p.state = state;
+  p.core_out = core_out;
+  p.z = z;
+  p.norm_w = norm_w;
+  p.out = out;
+  p.Hk = dims->n_k_heads;
+  p.Hv = dims->n_v_heads;
+  p.rep = rep;
+  p.map = dims->map;
+  p.decay = dims->decay;
+  p.C = (int32_t)C;
+  p.l2_eps = dims->l2_eps;
+  p.rms_eps = dims->rms_eps;
+  p.scale = 1.0f / sqrtf((float)D);
+  return cuda_status(gdn::launch_decode(p, dims->io_dtype, dims->head_dim, batch,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int32_t* cu_seqlens,
+                               int64_t total_tokens, const void* q, int64_t q_stride,
+                               const void* k, int64_t k_stride, const void* v, int64_t v_stride,
+                               const void* a, const void* b, const float* decay_param,
+                               const float* dt_bias, int32_t flags, float* state,
+                               float* core_out, const void* z, const float* norm_w, void* out,
+                               void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
+  if (num_seqs == 0 && total_tokens > 0) return GDN_ERR_INVALID_ARG;
+  if (num_seqs > kMaxGridY) return GDN_ERR_EXTENT;
+  if ((flags & ~(GDN_QK_PRENORMALIZED | GDN_GATES_PRECOMPUTED)) != 0) return GDN_ERR_INVALID_ARG;
+  if (num_seqs == 0) return GDN_OK;
+  const bool pregate = (flags & GDN_GATES_PRECOMPUTED) != 0;
+  if (!cu_seqlens || !state) return GDN_ERR_INVALID_ARG;
+  if (total_tokens > 0) {
+    if (!q || !k || !v || !a || !b) return GDN_ERR_INVALID_ARG;
+    if (!pregate && (!decay_param || !dt_bias)) return GDN_ERR_INVALID_ARG;
+    if (core_out == nullptr && z == nullptr) return GDN_ERR_INVALID_ARG;
+    if (z != nullptr && (norm_w == nullptr || out == nullptr)) return GDN_ERR_INVALID_ARG;
+  }
+  const int64_t es = dtype_size(dims->io_dtype);
+  const int64_t Hk = dims->n_k_heads, Hv = dims->n_v_heads, D = dims->head_dim;
+  if (q_stride < Hk * D || k_stride < Hk * D || v_stride < Hv * D) return GDN_ERR_INVALID_ARG;
+  if ((q_stride * es) % 16 || (k_stride * es) % 16 || (v_stride * es) % 16) return GDN_ERR_ALIGN;
+  int64_t tmp = 0, state_bytes = 0;
+  if (!mul_ok((int64_t)num_seqs * Hv, D * D * 4, &state_bytes)) return GDN_ERR_EXTENT;
+  if (!mul_ok(total_tokens, (q_stride > v_stride ? q_stride : v_stride) + k_stride, &tmp))
+    return GDN_ERR_EXTENT;
+  if (!mul_ok(total_tokens, Hv * D * 4, &tmp)) return GDN_ERR_EXTENT;
+  if (!aligned16(cu_seqlens) || !aligned16(state)) return GDN_ERR_ALIGN;
+  if (total_tokens > 0) {
+    const void* ptrs[] = {q, k, v, a, b};
+    for (const void* ptr : ptrs)
+      if (!aligned16(ptr)) return GDN_ERR_ALIGN;
+    if ((core_out && !aligned16(core_out)) || (z && (!aligned16(z) || !aligned16(norm_w) || !aligned16(out))))
+      return GDN_ERR_ALIGN;
+    if (!pregate && (!aligned16(decay_param) || !aligned16(dt_bias))) return GDN_ERR_ALIGN;
+  }
+  const int64_t T = total_tokens;
+  const int64_t gate_es = pregate ? 4 : es;
+  const Range inputs[] = {
+      range_of(q, T > 0 ? ((T - 1) * q_stride + Hk * D) * es : 0),
+      range_of(k, T > 0 ? ((T - 1) * k_stride + Hk * D) * es : 0),
+      range_of(v, T > 0 ? ((T - 1) * v_stride + Hv * D) * es : 0),
+      range_of(a, T * Hv * gate_es),
+      range_of(b, T * Hv * gate_es),
+      range_of(z, z ? T * Hv * D * es : 0),
+      range_of(cu_seqlens, ((int64_t)num_seqs + 1) * 4)};
+  const Range rs = range_of(state, state_bytes);
+  const Range ro = range_of(core_out, core_out ? T * Hv * D * 4 : 0);
+  const Range ry = range_of(out, z ? T * Hv * D * es : 0);
+  for (const Range& in : inputs) {
+    if (overlap(rs, in) || overlap(ro, in) || overlap(ry, in)) return GDN_ERR_ALIAS;
+  }
+  if (overlap(rs, ro) || overlap(rs, ry) || overlap(ro, ry)) return GDN_ERR_ALIAS;
+  gdn::PrefillArgs p{};
+  p.cu_seqlens = cu_seqlens;
+  p.N = num_seqs;
+  p.T = total_tokens;
+  p.q = q;
+  p.q_stride = q_stride;
+  p.k = k;
+  p.k_stride = k_stride;
+  p.v = v;
+  p.v_stride = v_stride;
+  p.a = a;
+  p.b = b;
+  p.decay_param = decay_param;
+  p.dt_bias = dt_bias;
+  p.flags = flags;
+  p.state = state;
+  p.core_out = core_out;
+  p.z = z;
+  p.norm_w = norm_w;
+  p.out = out;
+  p.Hk = (int32_t)Hk;
+  p.Hv = (int32_t)Hv;
+  p.rep = (int32_t)(Hv / Hk);
+  p.map = dims->map;
+  p.decay = dims->decay;
+  p.l2_eps = dims->l2_eps;
+  p.rms_eps = dims->rms_eps;
+  p.scale = 1.0f / sqrtf((float)D);
+  return cuda_status(gdn::launch_prefill(p, dims->io_dtype, dims->head_dim,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, int64_t rows, const float* o, const void* z,
+                             const float* norm_w, void* y, void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (rows < 0) return GDN_ERR_INVALID_ARG;
+  if (rows == 0) return GDN_OK;
+  if (!o || !z || !norm_w || !y) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(z) || !aligned16(norm_w) || !aligned16(y)) return GDN_ERR_ALIGN;
+  const int64_t es = dtype_size(dims->io_dtype), D = dims->head_dim;
+  int64_t el = 0;
+  if (!mul_ok(rows, D * 4, &el)) return GDN_ERR_EXTENT;
+  if ((rows + 7) / 8 > INT32_MAX) return GDN_ERR_EXTENT;
+  const Range ry = range_of(y, rows * D * es);
+  if (overlap(ry, range_of(o, rows * D * 4)) || overlap(ry, range_of(z, rows * D * es)) ||
+      overlap(ry, range_of(norm_w, D * 4)))
+    return GDN_ERR_ALIAS;
+  gdn::RmsNormArgs p{};
+  p.rows = rows;
+  p.o = o;
+  p.z = z;
+  p.norm_w = norm_w;
+  p.y = y;
+  p.eps = dims->rms_eps;
+  return cuda_status(
+      gdn::launch_rmsnorm(p, dims->io_dtype, dims->head_dim, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_device_error(int32_t* status, int32_t clear) {
+  if (status == nullptr) return GDN_ERR_INVALID_ARG;
+  *status = GDN_OK;
+  cudaError_t (*readers[])(int32_t*, bool) = {gdn::read_error_decode, gdn::read_error_conv,
+                                               gdn::read_error_rmsnorm, gdn::read_error_prefill};
+  for (auto rd : readers) {
+    int32_t v = 0;
+    if (rd(&v, clear != 0) != cudaSuccess) return GDN_ERR_CUDA;
+    if (v != GDN_OK && *status == GDN_OK) *status = v;
+  }
+  return GDN_OK;
+}
+
+}  // extern "C"

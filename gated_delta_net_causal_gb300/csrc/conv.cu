@@ -1,0 +1,160 @@
+// Causal depthwise conv1d (kernel 4) + SiLU over packed variable-length
+// sequences, with a rolling 3-wide conv state per sequence
+// (ferrum-kernels gated_delta_attention_tests.rs, `cpu_segment` conv loop and
+// conv-state update; libmir-metal decode/mod.rs `convolve`).
+//
+// Two launches on the caller's stream:
+//  1. conv_fwd_kernel: y for every token. A thread owns 16 bytes of channels
+//     (8 for f16/bf16, 4 for f32) and 8 consecutive tokens; it loads the 11
+//     input rows its window needs once and reads the OLD conv state only for
+//     the (at most three) taps that fall before its sequence's first token.
+//  2. conv_state_kernel: the new conv state (last three raw inputs of each
+//     sequence). Running it after (1) in stream order is what makes the in-place
+//     state update race-free: (1) never sees a half-updated state.
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+
+constexpr int kConvTPT = 8;    // tokens per thread
+constexpr int kConvCV = 32;    // channel vectors per block
+constexpr int kConvTG = 8;     // token groups per block
+
+__device__ __forceinline__ int64_t clamp_cu(const int32_t* cu, int n, int64_t T) {
+  int64_t v = cu[n];
+  return v < 0 ? 0 : (v > T ? T : v);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kConvCV* kConvTG) conv_fwd_kernel(const ConvArgs p) {
+  constexpr int VEC = 16 / (int)sizeof(T);
+  const int cv = threadIdx.x % kConvCV, tg = threadIdx.x / kConvCV;
+  const int64_t c0 = ((int64_t)blockIdx.y * kConvCV + cv) * VEC;
+  const int64_t t0 = ((int64_t)blockIdx.x * kConvTG + tg) * kConvTPT;
+  const int64_t T_ = p.T, C = p.C;
+  if (c0 >= C || t0 >= T_) return;
+  const T* x = static_cast<const T*>(p.x);
+  const T* st = static_cast<const T*>(p.conv_state);
+  T* y = static_cast<T*>(p.y);
+
+  // weights of these VEC channels, [VEC][4]
+  float wf[VEC][4];
+  {
+    const T* wp = static_cast<const T*>(p.conv_w) + c0 * 4;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) wf[e][j] = to_f32(wp[e * 4 + j]);
+  }
+
+  // window rows tau = t0-3 .. t0+TPT-1
+  constexpr int NR = kConvTPT + 3;
+  float xv[NR][VEC];
+#pragma unroll
+  for (int u = 0; u < NR; ++u) {
+    const int64_t tau = t0 - 3 + u;
+    if (tau >= 0 && tau < T_) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(x + tau * C + c0);
+      const T* rv = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) xv[u][e] = to_f32(rv[e]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) xv[u][e] = 0.f;
+    }
+  }
+
+  // sequence owning t0: the last n with cu[n] <= t0
+  int lo = 0, hi = p.N - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (clamp_cu(p.cu_seqlens, mid, T_) <= t0) lo = mid;
+    else hi = mid - 1;
+  }
+  int n = lo;
+
+#pragma unroll
+  for (int jj = 0; jj < kConvTPT; ++jj) {
+    const int64_t t = t0 + jj;
+    if (t >= T_) break;
+    while (n + 1 < p.N && clamp_cu(p.cu_seqlens, n + 1, T_) <= t) ++n;
+    int64_t s = clamp_cu(p.cu_seqlens, n, T_);
+    if (s > t) s = t;
+    float acc[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t tau = t + j - 3;
+      if (tau >= s) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] += wf[e][j] * xv[jj + j][e];
+      } else {
+        // tap before the sequence start: old conv state slot 3 + (tau - s)
+        const int slot = 3 + (int)(tau - s);
+        const T* sp = st + ((int64_t)n * C + c0) * 3 + slot;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] += wf[e][j] * to_f32(sp[e * 3]);
+      }
+    }
+    uint4 packed;
+    T* pv = reinterpret_cast<T*>(&packed);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) pv[e] = from_f32<T>(silu_f(acc[e]));
+    *reinterpret_cast<uint4*>(y + t * C + c0) = packed;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) conv_state_kernel(const ConvArgs p) {
+  const int n = blockIdx.x;
+  const int64_t c = (int64_t)blockIdx.y * 256 + threadIdx.x;
+  if (c >= p.C) return;
+  const int64_t T_ = p.T, C = p.C;
+  const int64_t s = clamp_cu(p.cu_seqlens, n, T_);
+  int64_t e = clamp_cu(p.cu_seqlens, n + 1, T_);
+  if (e < s) e = s;
+  const int64_t L = e - s;
+  T* sp = static_cast<T*>(p.conv_state) + ((int64_t)n * C + c) * 3;
+  const T* x = static_cast<const T*>(p.x);
+  const T old[3] = {sp[0], sp[1], sp[2]};
+  T nw[3];
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    const int64_t tau = L + q - 3;
+    nw[q] = tau >= 0 ? x[(s + tau) * C + c] : old[3 + tau];
+  }
+#pragma unroll
+  for (int q = 0; q < 3; ++q) sp[q] = nw[q];
+}
+
+template <typename T>
+static cudaError_t launch_conv_t(const ConvArgs& p, cudaStream_t stream) {
+  constexpr int VEC = 16 / (int)sizeof(T);
+  if (p.T > 0) {
+    const int64_t gx = (p.T + kConvTG * kConvTPT - 1) / (kConvTG * kConvTPT);
+    const int64_t gy = (p.C / VEC + kConvCV - 1) / kConvCV;
+    conv_fwd_kernel<T><<<dim3((unsigned)gx, (unsigned)gy), kConvCV * kConvTG, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (p.N > 0) {
+    const int64_t gy = (p.C + 255) / 256;
+    conv_state_kernel<T><<<dim3((unsigned)p.N, (unsigned)gy), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_conv(const ConvArgs& p, int32_t dtype, cudaStream_t stream) {
+  switch (dtype) {
+    case GDN_F16: return launch_conv_t<__half>(p, stream);
+    case GDN_BF16: return launch_conv_t<__nv_bfloat16>(p, stream);
+    case GDN_F32: return launch_conv_t<float>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gdn
+
+GDN_DEFINE_ERROR_READER(conv)

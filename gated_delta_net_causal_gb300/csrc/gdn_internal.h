@@ -1,0 +1,103 @@
+// Host-side interface between the C ABI (abi.cu) and the kernel translation
+// units. Arguments arrive here already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+struct DecodeArgs {
+  const void* mixed_qkv;
+  const void* a;
+  const void* b;
+  const float* decay_param;
+  const float* dt_bias;
+  const void* conv_w;
+  void* conv_state;
+  float* state;
+  float* core_out;
+  const void* z;
+  const float* norm_w;
+  void* out;
+  int32_t Hk, Hv, rep, map, decay, C;
+  float l2_eps, rms_eps, scale;
+};
+
+struct ConvArgs {
+  const int32_t* cu_seqlens;
+  int32_t N;
+  int64_t T;
+  int32_t C;
+  const void* x;
+  const void* conv_w;
+  void* conv_state;
+  void* y;
+};
+
+struct RmsNormArgs {
+  int64_t rows;
+  const float* o;
+  const void* z;
+  const float* norm_w;
+  void* y;
+  float eps;
+};
+
+struct PrefillArgs {
+  const int32_t* cu_seqlens;
+  int32_t N;
+  int64_t T;
+  const void* q;
+  int64_t q_stride;
+  const void* k;
+  int64_t k_stride;
+  const void* v;
+  int64_t v_stride;
+  const void* a;
+  const void* b;
+  const float* decay_param;
+  const float* dt_bias;
+  int32_t flags;
+  float* state;
+  float* core_out;
+  const void* z;
+  const float* norm_w;
+  void* out;
+  int32_t Hk, Hv, rep, map, decay;
+  float l2_eps, rms_eps, scale;
+};
+
+// Each launcher dispatches on (io dtype, head_dim) and returns the launch
+// status (cudaSuccess when everything was enqueued).
+cudaError_t launch_decode(const DecodeArgs& p, int32_t dtype, int32_t D, int32_t batch,
+                          cudaStream_t stream);
+cudaError_t launch_conv(const ConvArgs& p, int32_t dtype, cudaStream_t stream);
+cudaError_t launch_rmsnorm(const RmsNormArgs& p, int32_t dtype, int32_t D, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs& p, int32_t dtype, int32_t D, cudaStream_t stream);
+
+// Device error words, one per kernel translation unit.
+cudaError_t read_error_decode(int32_t* status, bool clear);
+cudaError_t read_error_conv(int32_t* status, bool clear);
+cudaError_t read_error_rmsnorm(int32_t* status, bool clear);
+cudaError_t read_error_prefill(int32_t* status, bool clear);
+
+}  // namespace gdn
+
+// Defines the per-translation-unit device error word reader.
+#define GDN_DEFINE_ERROR_READER(NAME)                                                  \
+  namespace gdn {                                                                      \
+  cudaError_t read_error_##NAME(int32_t* status, bool clear) {                         \
+    int32_t v = 0;                                                                     \
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));               \
+    if (e != cudaSuccess) return e;                                                    \
+    *status = v;                                                                       \
+    if (clear && v != 0) {                                                             \
+      const int32_t zero = 0;                                                          \
+      e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));                     \
+    }                                                                                  \
+    return e;                                                                          \
+  }                                                                                    \
+  }

@@ -1,0 +1,202 @@
+/*
+ * gdn.h -- C ABI of the GB300 gated delta-net core library (libgdn.so).
+ *
+ * The library computes the gated delta-net linear-attention core (the
+ * Qwen3-Next / Qwen3.5 recurrence) on one sm_103a GPU:
+ *
+ *   per token, per V head h reading K head kh (Grouped: kh = h / (Hv/Hk),
+ *   Tiled: kh = h % Hk), with the state S[h][j][i] (value row j, key col i):
+ *       S  *= exp(g_h)
+ *       pred = S k            d = beta_h (v - pred)
+ *       S  += d k^T           o = S q / sqrt(D)
+ *   -- ferrox-core 0.24.0 src/gdn.rs, module docs (the six-line formula),
+ *      `HeadMap`, `delta_step`; ferrum-kernels gated_delta_attention_tests.rs
+ *      `cpu_segment`.
+ *
+ * Conventions shared by every call:
+ *  - Every pointer is a DEVICE pointer the caller owns (allocated with
+ *    cudaMalloc or by a framework allocator); the library never allocates,
+ *    frees or retains one past the call. All work is enqueued on `stream`
+ *    (a cudaStream_t; NULL = the legacy default stream) and is asynchronous.
+ *  - Arguments are validated on the host before anything is enqueued; on an
+ *    error nothing is launched and the status says why. A failed launch
+ *    returns GDN_ERR_CUDA.
+ *  - Tensors are dense row-major with the innermost dimension last, and every
+ *    pointer must be 16-byte aligned.
+ *  - io dtype (gdn_dims.io_dtype) is the storage type of the activations,
+ *    the conv weight and the conv state; the delta state, core outputs,
+ *    decay parameters, dt_bias and the norm weight are always fp32.
+ *  - Supported shapes: head_dim (Dk = Dv = D) in {32, 64, 128};
+ *    n_v_heads a multiple of n_k_heads; conv kernel width 4 (3-wide state).
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1, /* null pointer, bad enum, bad dims */
+  GDN_ERR_EXTENT = 2,      /* a size product overflows the launch/index range */
+  GDN_ERR_UNSUPPORTED = 3, /* valid but not implemented (e.g. head_dim 80) */
+  GDN_ERR_ALIAS = 4,       /* an output overlaps an input it must not */
+  GDN_ERR_ALIGN = 5,       /* pointer or stride not 16-byte aligned */
+  GDN_ERR_CUDA = 6,        /* the CUDA runtime reported an error */
+  GDN_ERR_TIMEOUT = 7      /* a device-side bounded wait gave up */
+} gdn_status;
+
+/* V head -> K head map (gdn.rs `HeadMap`; enum values as the Metal test's
+ * params use them: 0 = grouped, 1 = interleaved/tiled). */
+typedef enum gdn_head_map { GDN_MAP_GROUPED = 0, GDN_MAP_TILED = 1 } gdn_head_map;
+
+/* Decay parameterisation (gated_delta_attention_tests.rs, `cpu_segment`
+ * gate lines): LOG_RATE: rate_h = -exp(decay_param[h]) (decay_param = A_log);
+ * NEGATIVE_RATE: rate_h = decay_param[h] (already negative).
+ * Then g = rate_h * softplus(a + dt_bias[h]), beta = sigmoid(b). */
+typedef enum gdn_decay { GDN_DECAY_LOG_RATE = 0, GDN_DECAY_NEGATIVE_RATE = 1 } gdn_decay;
+
+typedef enum gdn_dtype { GDN_F16 = 0, GDN_BF16 = 1, GDN_F32 = 2 } gdn_dtype;
+
+/* gdn_prefill_chunked flags */
+enum {
+  GDN_QK_PRENORMALIZED = 1, /* q and k are already l2-normalised: skip it */
+  GDN_GATES_PRECOMPUTED = 2 /* a holds g and b holds beta, both fp32 [T][Hv] */
+};
+
+typedef struct gdn_dims {
+  int32_t n_k_heads; /* Hk >= 1 */
+  int32_t n_v_heads; /* Hv, a multiple of Hk */
+  int32_t head_dim;  /* D = Dk = Dv in {32, 64, 128} */
+  int32_t map;       /* gdn_head_map */
+  int32_t decay;     /* gdn_decay */
+  int32_t io_dtype;  /* gdn_dtype */
+  float l2_eps;      /* q/k normalisation: x * (sum x^2 + l2_eps)^(-1/2); 1e-6 */
+  float rms_eps;     /* gated RMSNorm: o * (mean o^2 + rms_eps)^(-1/2); 1e-6 */
+} gdn_dims;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* gdn_status_string(int32_t status);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int32_t gdn_version(void);
+
+/* Channels of the packed pre-conv activation: C = 2*Hk*D + Hv*D, laid out
+ * [q (Hk*D) | k (Hk*D) | v (Hv*D)] (gated_delta_attention_tests.rs
+ * `cpu_segment` split; libmir-metal decode/mod.rs `split_qkv`). -1 if dims
+ * is invalid. */
+int64_t gdn_qkv_features(const gdn_dims* dims);
+
+/*
+ * Causal depthwise conv1d (kernel 4) + SiLU over a packed batch of
+ * variable-length sequences, with a rolling 3-wide conv state per sequence.
+ * -- gated_delta_attention_tests.rs `cpu_segment` conv loop and conv-state
+ *    update; libmir-metal decode/mod.rs `convolve`.
+ *
+ *   y[t][c] = silu( sum_{j=0..3} conv_w[c][j] * xh[t+j-3][c] ),
+ *   xh[tau] = x[tau] inside the sequence, conv_state[n][c][3+tau'] for the
+ *   three positions before its first token (tau' = -3..-1, oldest first).
+ *   Afterwards conv_state[n][c][0..2] holds the last three raw inputs of
+ *   sequence n (a bit copy; older entries shift in when the sequence has
+ *   fewer than three tokens).
+ *
+ * num_seqs    N >= 0 sequences.
+ * cu_seqlens  device int32 [N+1], cu[0] = 0, non-decreasing, cu[N] =
+ *             total_tokens; sequence n owns tokens [cu[n], cu[n+1]). Values
+ *             outside [0, total_tokens] are clamped on the device.
+ * x           [total_tokens][C] io dtype (C = gdn_qkv_features).
+ * conv_w      [C][4] io dtype; tap 3 multiplies the current token; no bias.
+ * conv_state  [N][C][3] io dtype, updated in place.
+ * y           [total_tokens][C] io dtype; must not overlap x or conv_state.
+ */
+gdn_status gdn_conv_update(const gdn_dims* dims, int32_t num_seqs, const int32_t* cu_seqlens,
+                           int64_t total_tokens, const void* x, const void* conv_w,
+                           void* conv_state, void* y, void* stream);
+
+/*
+ * One decode token for each of `batch` sequences, fully fused: conv + SiLU
+ * on the packed pre-conv activation, split q|k|v, l2-normalise q and k per
+ * K head (q also scaled by 1/sqrt(D)), gates, the delta-rule step on the
+ * fp32 state in place, and optionally the gated RMSNorm of the output.
+ * -- gdn.rs `delta_step` (the step), gated_delta_attention_tests.rs
+ *    `cpu_segment` (conv, norm, gates, gated norm), libmir-metal
+ *    decode/mod.rs `build` (one decode layer: convolve, split, recurrence,
+ *    rms_norm, gate).
+ *
+ * batch        B >= 0 sequences (one token each), B <= 65535.
+ * mixed_qkv    [B][C] io dtype, pre-conv.
+ * a, b         [B][Hv] io dtype: raw decay input (a) and raw beta input (b).
+ * decay_param  [Hv] fp32: A_log (LOG_RATE) or the negative rate.
+ * dt_bias      [Hv] fp32.
+ * conv_w       [C][4] io dtype.
+ * conv_state   [B][C][3] io dtype, in place.
+ * state        [B][Hv][D][D] fp32 S[b][h][j][i], in place.
+ * core_out     [B][Hv][D] fp32 core output o, or NULL.
+ * z            [B][Hv][D] io dtype output-gate input, or NULL (no norm).
+ * norm_w       [D] fp32 RMSNorm weight (shared by all heads); needed with z.
+ * out          [B][Hv][D] io dtype gated-RMSNorm output; needed with z.
+ * At least one of core_out and (z, out) must be given. Hv/Hk <= 8.
+ */
+gdn_status gdn_decode_step(const gdn_dims* dims, int32_t batch, const void* mixed_qkv,
+                           const void* a, const void* b, const float* decay_param,
+                           const float* dt_bias, const void* conv_w, void* conv_state,
+                           float* state, float* core_out, const void* z, const float* norm_w,
+                           void* out, void* stream);
+
+/*
+ * Chunked prefill: the same recurrence as gdn_decode_step summed chunk-wise
+ * (chunk 64, UT/WY form) over a packed batch of variable-length sequences,
+ * each continuing from its own fp32 state (in place). q, k, v are the
+ * post-conv activations (e.g. slices of gdn_conv_update's y).
+ * -- gdn.rs module docs ("the same recurrence in a different summation
+ *    order"); gated_delta_attention_tests.rs `run_chunked_core` (the six
+ *    chunk stages: K gram, (I+A)^-1, U/W, QK^T, carry, output) and
+ *    `chunked_c64_matches_recurrent_oracle_and_non_aligned_state_continuity`.
+ *
+ * cu_seqlens   device int32 [N+1] as for gdn_conv_update.
+ * q, k         token t, K head kh, column i at q[t*q_stride + kh*D + i]
+ *              (io dtype); strides in elements, multiples of 8.
+ * v            token t, V head h, column j at v[t*v_stride + h*D + j].
+ * a, b         [T][Hv] io dtype raw gate inputs, or with
+ *              GDN_GATES_PRECOMPUTED fp32 g and beta.
+ * decay_param, dt_bias  [Hv] fp32 (ignored with GDN_GATES_PRECOMPUTED).
+ * flags        GDN_QK_PRENORMALIZED | GDN_GATES_PRECOMPUTED.
+ * state        [N][Hv][D][D] fp32, in place (initial state = its contents).
+ * core_out     [T][Hv][D] fp32 core output, or NULL.
+ * z, norm_w, out  optional fused gated RMSNorm as in gdn_decode_step.
+ */
+gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int32_t* cu_seqlens,
+                               int64_t total_tokens, const void* q, int64_t q_stride,
+                               const void* k, int64_t k_stride, const void* v, int64_t v_stride,
+                               const void* a, const void* b, const float* decay_param,
+                               const float* dt_bias, int32_t flags, float* state,
+                               float* core_out, const void* z, const float* norm_w, void* out,
+                               void* stream);
+
+/*
+ * Gated RMSNorm over rows of D: y = o * (mean_j o_j^2 + rms_eps)^(-1/2)
+ * * norm_w[j] * silu(z[j]), computed in fp32 and rounded once to io dtype.
+ * -- gated_delta_attention_tests.rs `cpu_segment` output loop.
+ *
+ * rows   >= 0 (e.g. T * Hv).
+ * o      [rows][D] fp32;  z [rows][D] io dtype;  norm_w [D] fp32;
+ * y      [rows][D] io dtype, must not overlap o or z.
+ */
+gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, int64_t rows, const float* o, const void* z,
+                             const float* norm_w, void* y, void* stream);
+
+/*
+ * Device-side error word: kernels whose bounded waits give up record a
+ * status here instead of hanging. Reads it (synchronising the device) into
+ * *status and, when clear != 0, resets it to GDN_OK.
+ */
+gdn_status gdn_device_error(int32_t* status, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,141 @@
+"""Host-side checks of the C-ABI library that need no GPU: it loads, exports
+every function include/gdn.h declares, and rejects bad arguments on the host
+before anything is launched."""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import gated_delta_net_causal_gb300 as gdn
+from gated_delta_net_causal_gb300 import _build
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+# fake device addresses are only safe where no launch can happen at all
+no_device = pytest.mark.skipif(torch.cuda.is_available(),
+                               reason="fake-pointer validation runs only without a GPU")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return gdn.library()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_four_calls():
+    names = _declared()
+    for n in ("gdn_conv_update", "gdn_decode_step", "gdn_prefill_chunked", "gdn_gated_rmsnorm"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    for s in range(8):
+        assert gdn.status_string(s).startswith("GDN_")
+    assert gdn.status_string(99) == "GDN_ERR_UNKNOWN"
+    assert gdn.gdn_version() >= 100
+
+
+def test_qkv_features(lib):
+    assert gdn.gdn_qkv_features(gdn.dims(16, 32, 128)) == 8192
+    assert gdn.gdn_qkv_features(gdn.dims(16, 48, 128)) == 10240
+    assert gdn.gdn_qkv_features(gdn.dims(16, 64, 128)) == 12288
+    assert gdn.gdn_qkv_features(gdn.dims(3, 4, 128)) == -1  # Hv not a multiple of Hk
+
+
+VP = ctypes.c_void_p
+
+
+def _decode(lib, d, batch=1, ptrs=None, core=True):
+    p = dict(x=0x10000, a=0x20000, b=0x30000, dp=0x40000, dt=0x50000, w=0x60000,
+             cs=0x1000000, st=0x10000000, core=0x70000000 if core else None, z=None, nw=None,
+             out=None)
+    if ptrs:
+        p.update(ptrs)
+    return lib.gdn_decode_step(ctypes.byref(d) if d is not None else None, batch,
+                               *[VP(p[k]) if p[k] is not None else None for k in
+                                 ("x", "a", "b", "dp", "dt", "w", "cs", "st", "core", "z", "nw",
+                                  "out")], None)
+
+
+@no_device
+def test_decode_rejects_bad_arguments(lib):
+    ok = gdn.dims(16, 32, 128)
+    assert _decode(lib, None) == 1  # no dims
+    assert _decode(lib, gdn.dims(3, 4, 128)) == 1  # Hv % Hk
+    assert _decode(lib, gdn.dims(16, 32, 80)) == 3  # head_dim 80 unsupported
+    assert _decode(lib, gdn.dims(16, 32, 128, map=7)) == 1
+    assert _decode(lib, gdn.dims(16, 32, 128, decay=5)) == 1
+    assert _decode(lib, gdn.dims(1, 16, 128)) == 3  # 16 V heads per K head > 8
+    assert _decode(lib, ok, batch=-1) == 1
+    assert _decode(lib, ok, batch=70000) == 2  # grid y limit
+    assert _decode(lib, ok, batch=0) == 0  # nothing to do, nothing launched
+    assert _decode(lib, ok, ptrs={"x": None}) == 1
+    assert _decode(lib, ok, core=False) == 1  # neither core_out nor z
+    assert _decode(lib, ok, ptrs={"a": 0x20008}) == 5  # misaligned
+    # the state overlapping the conv state
+    assert _decode(lib, ok, ptrs={"st": 0x1000000 + 64}) == 4
+    # the core output overlapping an input
+    assert _decode(lib, ok, ptrs={"core": 0x10000}) == 4
+
+
+@no_device
+def test_conv_and_prefill_and_norm_reject_bad_arguments(lib):
+    d = gdn.dims(2, 4, 32)
+    f = lib.gdn_conv_update
+    assert f(ctypes.byref(d), -1, VP(0x100), 0, None, None, None, None, None) == 1
+    assert f(ctypes.byref(d), 0, None, 5, None, None, None, None, None) == 1  # tokens, no seqs
+    assert f(ctypes.byref(d), 0, None, 0, None, None, None, None, None) == 0
+    assert f(ctypes.byref(d), 1, VP(0x100), 4, VP(0x1000), VP(0x9000), VP(0xa000),
+             VP(0x1000 + 16), None) == 4  # y overlaps x
+    assert f(ctypes.byref(d), 1, VP(0x104), 4, VP(0x1000), VP(0x9000), VP(0xa000),
+             VP(0x100000), None) == 5  # cu_seqlens misaligned
+    assert f(ctypes.byref(d), 1, VP(0x100), 2 ** 62, VP(0x1000), VP(0x9000), VP(0xa000),
+             VP(0x100000), None) == 2  # extent overflow
+
+    pf = lib.gdn_prefill_chunked
+    base = [ctypes.byref(d), 1, VP(0x100), 10, VP(0x1000), 128, VP(0x2000), 128, VP(0x3000), 128,
+            VP(0x4000), VP(0x5000), VP(0x6000), VP(0x7000), 0, VP(0x100000), VP(0x200000), None,
+            None, None, None]
+    args = list(base)
+    args[5] = 8  # q stride below Hk*D
+    assert pf(*args) == 1
+    args = list(base)
+    args[5] = 68  # q stride not a multiple of 16 bytes
+    assert pf(*args) == 5
+    args = list(base)
+    args[14] = 8  # unknown flag
+    assert pf(*args) == 1
+    args = list(base)
+    args[16] = VP(0x100000)  # core_out aliases the state
+    assert pf(*args) == 4
+    args = list(base)
+    args[15] = VP(0x1000)  # state overlaps q
+    assert pf(*args) == 4
+
+    rn = lib.gdn_gated_rmsnorm
+    assert rn(ctypes.byref(d), -1, None, None, None, None, None) == 1
+    assert rn(ctypes.byref(d), 0, None, None, None, None, None) == 0
+    assert rn(ctypes.byref(d), 4, VP(0x1000), VP(0x2000), VP(0x3000), VP(0x1000), None) == 4
+    assert rn(ctypes.byref(d), 4, VP(0x1004), VP(0x2000), VP(0x3000), VP(0x9000), None) == 5
+
+
+def test_binding_fails_loudly_on_cpu_tensors(lib):
+    d = gdn.dims(2, 4, 32, io_dtype=torch.float32)
+    t = torch.zeros(4, 8)
+    with pytest.raises(ValueError):
+        gdn.gdn_gated_rmsnorm(d, t, t, torch.zeros(32), t)

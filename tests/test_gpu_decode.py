@@ -1,0 +1,142 @@
+"""GPU parity of gdn_decode_step (through the C ABI) against the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import gdn_inputs as gi
+import oracle
+from tests.gpu_helpers import (DECODE_OUT_ABS, DECODE_STATE_REL, DecodeRunner, F64, assert_abs,
+                               assert_gated, assert_state_rel, decode_reference)
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_steps(shape, batch, steps, seed, with_norm=True, core=True):
+    g = gi.rng(seed)
+    w = gi.layer_weights(g, shape)
+    cs0 = gi.conv_state(g, shape, batch, std=0.1)
+    S0 = gi.delta_state(g, shape, batch, std=0.05)
+    run = DecodeRunner(shape, w, cs0, S0)
+    cs, S = F64(cs0), F64(S0)
+    for step in range(steps):
+        x = gi.step_inputs(g, shape, batch)
+        core_out, out = run.step(x, core=core, norm=with_norm)
+        torch.cuda.synchronize()
+        rc, ry, cs, S = decode_reference(shape, w, x, cs, S, with_norm=with_norm)
+        tag = f"{shape} step {step}"
+        if core:
+            assert_abs(core_out, rc, DECODE_OUT_ABS, tag + " core")
+        if with_norm:
+            assert_gated(out, ry, rc, x.z, w.norm_w, shape.dtype, tag + " gated norm",
+                         core_gpu=core_out)
+        assert_state_rel(run.state, S, DECODE_STATE_REL, tag + " state")
+        assert np.array_equal(F64(run.conv_state.cpu()), cs), tag + " conv state (bitwise)"
+    assert run.gdn.gdn_device_error() == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("hk,hv,d", [(2, 4, 32), (2, 4, 64), (1, 2, 128), (4, 8, 128),
+                                     (2, 2, 128), (1, 8, 128)])
+@pytest.mark.parametrize("mp,dec", [(gi.GROUPED, gi.LOG_RATE), (gi.TILED, gi.NEGATIVE_RATE)])
+def test_decode_small_shapes(dtype, hk, hv, d, mp, dec):
+    shape = gi.Shape(hk, hv, d, map=mp, decay=dec, dtype=dtype)
+    _check_steps(shape, batch=3, steps=3, seed=1000 + hk * 100 + hv * 10 + d + mp)
+
+
+def test_decode_core_only_and_norm_only():
+    shape = gi.Shape(2, 4, 128, map=gi.TILED, decay=gi.LOG_RATE, dtype="bf16")
+    _check_steps(shape, batch=2, steps=2, seed=77, with_norm=False, core=True)
+    _check_steps(shape, batch=2, steps=2, seed=78, with_norm=True, core=False)
+
+
+def test_decode_batch_zero_is_a_no_op():
+    shape = gi.Shape(2, 4, 128)
+    g = gi.rng(3)
+    w = gi.layer_weights(g, shape)
+    run = DecodeRunner(shape, w, gi.conv_state(g, shape, 1), gi.delta_state(g, shape, 1))
+    x = gi.step_inputs(g, shape, 0)
+    before = run.state.clone()
+    run.step(x)
+    torch.cuda.synchronize()
+    assert torch.equal(before, run.state)
+
+
+def _permute_heads(shape, t, axis):
+    """Reorder the V-head axis from grouped order to tiled order: grouped head
+    kh*rep + r  ->  tiled head kh + r*Hk."""
+    Hk, Hv = shape.n_k_heads, shape.n_v_heads
+    rep = Hv // Hk
+    perm = np.empty(Hv, dtype=np.int64)
+    for kh in range(Hk):
+        for r in range(rep):
+            perm[kh + r * Hk] = kh * rep + r
+    idx = torch.as_tensor(perm)
+    return t.index_select(axis, idx), perm
+
+
+def test_head_maps_are_a_pure_reindexing():
+    """A grouped run and a tiled run on the same data, with every V-head
+    indexed tensor permuted between the two orders, agree bit for bit."""
+    Hk, Hv, D, B = 4, 8, 128, 3
+    sg = gi.Shape(Hk, Hv, D, map=gi.GROUPED, decay=gi.LOG_RATE, dtype="bf16")
+    st = gi.Shape(Hk, Hv, D, map=gi.TILED, decay=gi.LOG_RATE, dtype="bf16")
+    g = gi.rng(91)
+    w = gi.layer_weights(g, sg)
+    x = gi.step_inputs(g, sg, B)
+    cs = gi.conv_state(g, sg, B)
+    S = gi.delta_state(g, sg, B)
+    C, qk = sg.qkv_features, 2 * Hk * D
+    # tiled copies: permute v channels, conv rows of v, gates, params, state, z
+    def perm_v_channels(t, axis):
+        head = t.narrow(axis, qk, Hv * D)
+        shp = list(head.shape)
+        shp[axis:axis + 1] = [Hv, D]
+        ph, _ = _permute_heads(sg, head.reshape(shp), axis)
+        return torch.cat([t.narrow(axis, 0, qk), ph.reshape(head.shape)], axis)
+    wt = gi.Weights(conv_w=perm_v_channels(w.conv_w, 0),
+                    decay_param=_permute_heads(sg, w.decay_param, 0)[0],
+                    dt_bias=_permute_heads(sg, w.dt_bias, 0)[0], norm_w=w.norm_w)
+    xt = gi.StepInputs(mixed_qkv=perm_v_channels(x.mixed_qkv, 1),
+                       a=_permute_heads(sg, x.a, 1)[0], b=_permute_heads(sg, x.b, 1)[0],
+                       z=_permute_heads(sg, x.z.view(B, Hv, D), 1)[0].reshape(B, Hv * D))
+    cst = perm_v_channels(cs, 1)
+    Sg = _permute_heads(sg, S, 1)[0]
+    rg = DecodeRunner(sg, w, cs, S)
+    rt = DecodeRunner(st, wt, cst, Sg)
+    og, yg = rg.step(x)
+    ot, yt = rt.step(xt)
+    torch.cuda.synchronize()
+    assert torch.equal(_permute_heads(sg, og.cpu(), 1)[0], ot.cpu())
+    assert torch.equal(_permute_heads(sg, yg.cpu(), 1)[0], yt.cpu())
+    assert torch.equal(_permute_heads(sg, rg.state.cpu(), 1)[0], rt.state.cpu())
+    assert torch.equal(perm_v_channels(rg.conv_state.cpu(), 1), rt.conv_state.cpu())
+
+
+def test_decode_tagged_heads_read_the_mapped_k_head():
+    """With zero conv state, conv weight taps (0,0,0,w3) and inputs chosen per
+    K head, every V head's output depends only on which K head it read; the
+    outputs must match the oracle's exactly-indexed result for both maps."""
+    for mp in (gi.GROUPED, gi.TILED):
+        shape = gi.Shape(4, 8, 128, map=mp, decay=gi.LOG_RATE, dtype="f32")
+        g = gi.rng(5)
+        w = gi.layer_weights(g, shape)
+        C = shape.qkv_features
+        cw = torch.zeros(C, 4)
+        cw[:, 3] = 1.0
+        w.conv_w = cw
+        x = gi.step_inputs(g, shape, 1)
+        xm = torch.zeros_like(x.mixed_qkv)
+        D, Hk = 128, 4
+        for kh in range(Hk):
+            xm[0, kh * D + kh] = 3.0  # q of K head kh: one-hot at column kh
+            xm[0, Hk * D + kh * D + kh] = 3.0  # k likewise
+        xm[0, 2 * Hk * D:] = x.mixed_qkv[0, 2 * Hk * D:]
+        x.mixed_qkv = xm
+        cs = torch.zeros(1, C, 3)
+        S = gi.delta_state(g, shape, 1)
+        run = DecodeRunner(shape, w, cs, S)
+        core, _ = run.step(x, norm=False)
+        torch.cuda.synchronize()
+        rc, _, _, _ = decode_reference(shape, w, x, F64(cs), F64(S), with_norm=False)
+        assert_abs(core, rc, DECODE_OUT_ABS, f"tagged heads map={mp}")

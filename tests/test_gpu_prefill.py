@@ -1,0 +1,190 @@
+"""GPU parity of gdn_prefill_chunked (through the C ABI) against the oracle's
+token-by-token recurrence."""
+
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_net_causal_gb300 as gdn
+import gdn_inputs as gi
+import oracle
+from tests.gpu_helpers import (CHUNK_OUT_ABS, CHUNK_STATE_ABS, F64, assert_abs, assert_lowp,
+                               cuda)
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = 73.25
+
+
+def _guarded_state(S: torch.Tensor):
+    """Device state followed by 16 sentinel floats that no call may touch."""
+    n = S.numel()
+    buf = torch.full((n + 16,), SENTINEL, device="cuda", dtype=torch.float32)
+    buf[:n].copy_(S.reshape(-1).to("cuda"))
+    return buf, buf[:n].view(S.shape)
+
+
+def _unit_rows(x: np.ndarray) -> np.ndarray:
+    """Input preparation for the pre-normalised form: rows scaled to unit
+    length the way the Metal chunk test prepares its q and k."""
+    x = x.astype(np.float32)
+    inv = 1.0 / np.sqrt((x * x).sum(-1, keepdims=True, dtype=np.float32) + np.float32(1e-6))
+    return (x * inv).astype(np.float32)
+
+
+def _page_chunk_inputs(T, Hk, Hv, D):
+    """The deterministic fill of the Metal chunk test: sin-valued q, k, v,
+    g = -0.008 - |sin(0.017 i)| 0.025, beta = 0.2 + |sin(0.013 i)| 0.6."""
+    q = _unit_rows(gi.sin_values(T * Hk * D, 0.019, 0.4).reshape(T, Hk, D))
+    k = _unit_rows(gi.sin_values(T * Hk * D, 0.031, 0.35).reshape(T, Hk, D))
+    v = gi.sin_values(T * Hv * D, 0.023, 0.2).astype(np.float32).reshape(T, Hv, D)
+    i = np.arange(T * Hv, dtype=np.float32)
+    g = (np.float32(-0.008) - np.abs(np.sin(i * np.float32(0.017))) * np.float32(0.025))
+    beta = np.float32(0.2) + np.abs(np.sin(i * np.float32(0.013))) * np.float32(0.6)
+    S0 = gi.sin_values(Hv * D * D, 0.011, 0.025).astype(np.float32).reshape(1, Hv, D, D)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t(q), t(k), t(v), t(g.reshape(T, Hv)), t(beta.reshape(T, Hv)), t(S0)
+
+
+def _run_prefill(d, cu, q, k, v, a, b, state, flags, dp=None, dt=None, z=None, nw=None):
+    T = q.shape[0]
+    Hv, D = d.n_v_heads, d.head_dim
+    core = torch.full((T, Hv, D), float("nan"), device="cuda")
+    out = None
+    if z is not None:
+        out = torch.full((T, Hv, D), float("nan"), device="cuda", dtype=z.dtype)
+    gdn.gdn_prefill_chunked(d, cuda(cu), cuda(q).reshape(T, -1), cuda(k).reshape(T, -1),
+                            cuda(v).reshape(T, -1), cuda(a), cuda(b),
+                            None if dp is None else cuda(dp), None if dt is None else cuda(dt),
+                            state, core_out=core, z=z, norm_w=nw, out=out, flags=flags)
+    torch.cuda.synchronize()
+    return core, out
+
+
+@pytest.mark.parametrize("hk,hv,d", [(2, 4, 32), (2, 4, 128), (2, 2, 128)])
+@pytest.mark.parametrize("mp", [gi.GROUPED, gi.TILED])
+def test_page_chunk_case_and_split_continuity(hk, hv, d, mp):
+    """T = 145 (2 x 64 + 17), split at 73, with the state's sentinel tail
+    untouched (the Metal chunk test's shapes and fill)."""
+    T = 145
+    q, k, v, g, beta, S0 = _page_chunk_inputs(T, hk, hv, d)
+    dims = gdn.dims(hk, hv, d, map=mp, io_dtype=torch.float32)
+    flags = gdn.GDN_QK_PRENORMALIZED | gdn.GDN_GATES_PRECOMPUTED
+    ro, rS = oracle.delta(F64(q), F64(k), F64(v), F64(g), F64(beta), F64(S0)[0], mp)
+
+    buf, state = _guarded_state(S0)
+    core, _ = _run_prefill(dims, gi.cu_seqlens([T]), q, k, v, g, beta, state, flags)
+    assert_abs(core.cpu(), ro, CHUNK_OUT_ABS, "chunk/full output")
+    assert_abs(state.cpu()[0], rS, CHUNK_STATE_ABS, "chunk/full state")
+    assert torch.all(buf[-16:] == SENTINEL)
+
+    sp = 73
+    buf2, st2 = _guarded_state(S0)
+    c1, _ = _run_prefill(dims, gi.cu_seqlens([sp]), q[:sp], k[:sp], v[:sp], g[:sp], beta[:sp],
+                         st2, flags)
+    assert torch.all(buf2[-16:] == SENTINEL)
+    c2, _ = _run_prefill(dims, gi.cu_seqlens([T - sp]), q[sp:], k[sp:], v[sp:], g[sp:],
+                         beta[sp:], st2, flags)
+    assert torch.all(buf2[-16:] == SENTINEL)
+    assert_abs(torch.cat([c1, c2]).cpu(), F64(core.cpu()), CHUNK_OUT_ABS, "chunk split output")
+    assert_abs(st2.cpu(), F64(state.cpu()), CHUNK_STATE_ABS, "chunk split state")
+    assert_abs(torch.cat([c1, c2]).cpu(), ro, CHUNK_OUT_ABS, "chunk split output vs oracle")
+
+
+def _raw_case(seed, shape, lengths):
+    g = gi.rng(seed)
+    Hk, Hv, D = shape.n_k_heads, shape.n_v_heads, shape.head_dim
+    T = int(sum(lengths))
+    w = gi.layer_weights(g, shape)
+    q = gi.to_dtype(gi.normal(g, (T, Hk, D), 1.0), shape.dtype)
+    k = gi.to_dtype(gi.normal(g, (T, Hk, D), 1.0), shape.dtype)
+    v = gi.to_dtype(gi.normal(g, (T, Hv, D), 1.0), shape.dtype)
+    z = gi.to_dtype(gi.normal(g, (T, Hv, D), 1.0), shape.dtype)
+    a = gi.to_dtype(gi.normal(g, (T, Hv), 1.0), shape.dtype)
+    b = gi.to_dtype(gi.normal(g, (T, Hv), 1.0), shape.dtype)
+    S0 = gi.delta_state(g, shape, len(lengths), std=0.02)
+    return w, q, k, v, z, a, b, S0
+
+
+def _oracle_prefill(shape, w, q, k, v, a, b, S0, cu):
+    gg, bb = oracle.gates(F64(a), F64(b), F64(w.decay_param), F64(w.dt_bias), shape.decay)
+    return oracle.prefill_core(shape.n_k_heads, shape.n_v_heads, shape.head_dim, shape.map,
+                               F64(q), F64(k), F64(v), gg, bb, F64(S0), cu.numpy(), l2_eps=1e-6)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("mp,dec", [(gi.GROUPED, gi.LOG_RATE), (gi.TILED, gi.NEGATIVE_RATE)])
+def test_varlen_raw_inputs_with_fused_norm(dtype, d, mp, dec):
+    lengths = [1, 63, 64, 65, 130, 0, 7]
+    shape = gi.Shape(2, 4, d, map=mp, decay=dec, dtype=dtype)
+    w, q, k, v, z, a, b, S0 = _raw_case(500 + d, shape, lengths)
+    cu = gi.cu_seqlens(lengths)
+    dims = gdn.dims(2, 4, d, map=mp, decay=dec, io_dtype=gi.DTYPES[dtype])
+    state = cuda(S0)
+    core, out = _run_prefill(dims, cu, q, k, v, a, b, state, 0, dp=w.decay_param, dt=w.dt_bias,
+                             z=cuda(z), nw=cuda(w.norm_w))
+    ro, rS = _oracle_prefill(shape, w, q, k, v, a, b, S0, cu)
+    assert_abs(core.cpu(), ro, CHUNK_OUT_ABS, "varlen output")
+    assert_abs(state.cpu(), rS, CHUNK_STATE_ABS, "varlen state")
+    # the empty sequence keeps its state bit for bit
+    assert torch.equal(state.cpu()[5], S0[5])
+    # the fused norm against the oracle's norm of the kernel's own core output
+    ry = oracle.gated_rmsnorm(F64(core.cpu()), F64(z), F64(w.norm_w), 1e-6)
+    assert_lowp(out.cpu(), ry, dtype, "fused gated norm")
+
+
+def test_prefill_reads_strided_conv_output():
+    """q, k, v passed as column slices of one [T][C] buffer (the conv output)."""
+    shape = gi.Shape(2, 4, 64, map=gi.TILED, dtype="bf16")
+    lengths = [70, 5]
+    T = sum(lengths)
+    g = gi.rng(808)
+    w = gi.layer_weights(g, shape)
+    y = gi.to_dtype(gi.normal(g, (T, shape.qkv_features), 1.0), "bf16")
+    a = gi.to_dtype(gi.normal(g, (T, 4), 1.0), "bf16")
+    b = gi.to_dtype(gi.normal(g, (T, 4), 1.0), "bf16")
+    S0 = gi.delta_state(g, shape, 2)
+    qk = 2 * 64
+    yd = cuda(y)
+    dims = gdn.dims(2, 4, 64, map=gi.TILED, io_dtype=torch.bfloat16)
+    state = cuda(S0)
+    core = torch.empty((T, 4, 64), device="cuda")
+    cu = gi.cu_seqlens(lengths)
+    gdn.gdn_prefill_chunked(dims, cuda(cu), yd[:, :qk], yd[:, qk:2 * qk], yd[:, 2 * qk:], cuda(a),
+                            cuda(b), cuda(w.decay_param), cuda(w.dt_bias), state, core_out=core)
+    torch.cuda.synchronize()
+    q = y[:, :qk].reshape(T, 2, 64)
+    k = y[:, qk:2 * qk].reshape(T, 2, 64)
+    v = y[:, 2 * qk:].reshape(T, 4, 64)
+    ro, rS = _oracle_prefill(shape, w, q, k, v, a, b, S0, cu)
+    assert_abs(core.cpu(), ro, CHUNK_OUT_ABS, "strided output")
+    assert_abs(state.cpu(), rS, CHUNK_STATE_ABS, "strided state")
+
+
+@pytest.mark.parametrize("random_state", [False, True])
+def test_prefill_t4096_sampled_heads(random_state):
+    """One sequence of 4096 tokens (Hk=16, Hv=32, D=128, Grouped, bf16 raw
+    inputs) at full size on the GPU; the oracle recomputes sampled heads."""
+    wl = gi.workload_prefill(4096, random_state=random_state)
+    shape, w = wl["shape"], wl["weights"]
+    dims = gdn.dims(16, 32, 128, map=shape.map, decay=shape.decay, io_dtype=torch.bfloat16)
+    state = cuda(wl["state"])
+    T = 4096
+    core, out = _run_prefill(dims, wl["cu_seqlens"], wl["q"], wl["k"], wl["v"], wl["a"],
+                             wl["b"], state, 0, dp=w.decay_param, dt=w.dt_bias,
+                             z=cuda(wl["z"]), nw=cuda(w.norm_w))
+    gg, bb = oracle.gates(F64(wl["a"]), F64(wl["b"]), F64(w.decay_param), F64(w.dt_bias),
+                          shape.decay)
+    q = oracle.l2norm(F64(wl["q"]))
+    k = oracle.l2norm(F64(wl["k"]))
+    v = F64(wl["v"])
+    S0 = F64(wl["state"])[0]
+    for h in (0, 13, 31):
+        kh = oracle.k_head(shape.map, h, 16, 32)
+        ro, rS = oracle.delta(q[:, kh:kh + 1], k[:, kh:kh + 1], v[:, h:h + 1], gg[:, h:h + 1],
+                              bb[:, h:h + 1], S0[h:h + 1], 0)
+        assert_abs(core.cpu()[:, h:h + 1], ro, CHUNK_OUT_ABS, f"T=4096 head {h} output")
+        assert_abs(state.cpu()[0, h:h + 1], rS, CHUNK_STATE_ABS, f"T=4096 head {h} state")
+    ry = oracle.gated_rmsnorm(F64(core.cpu()[:64]), F64(wl["z"][:64]), F64(w.norm_w), 1e-6)
+    assert_lowp(out.cpu()[:64], ry, "bf16", "T=4096 fused norm")
