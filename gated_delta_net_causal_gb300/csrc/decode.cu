@@ -10,16 +10,18 @@
 // reductions run side by side instead of one after the other.
 //
 // One CTA per (sequence, V head): it streams that head's D x D fp32 state
-// (64 KB at D=128) into shared memory with eight 1-D bulk copies issued up
-// front (all 64 KB in flight while the prologue computes the conv, norms and
-// gates), updates it row group by row group and writes each 2 KB row group
-// back with a bulk store as soon as it is done.
+// (64 KB at D=128) into shared memory with eight 1-D bulk copies issued first
+// thing, so the whole head is in flight while the prologue computes the conv,
+// norms and gates; every global load of the prologue is issued in one round.
+// Each row group is then updated in registers and written straight back to
+// global memory with coalesced 16-byte stores.
 //
 // Conv state ownership: the q/k channels of K head kh are read by every V
 // head mapped to kh (Hv/Hk CTAs). Those CTAs form one thread-block cluster;
 // each reads the old conv state, arrives on the cluster barrier, and only the
-// cluster's rank-0 CTA writes the new q/k conv state after waiting on it. The
-// v channels belong to one head and are written by its own CTA.
+// cluster's rank-0 CTA writes the new q/k conv state after waiting on it (from
+// values it kept in registers). The v channels belong to one head and are
+// written by its own CTA.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 
@@ -37,13 +39,13 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_step_kernel(const Decod
   constexpr int NCHUNK = 8;               // bulk loads per head
   constexpr int ROWS_PER_CHUNK = D / NCHUNK;
   constexpr uint32_t CHUNK_BYTES = ROWS_PER_CHUNK * D * 4;
-  constexpr uint32_t GROUP_BYTES = RPW * D * 4;
-  static_assert(GROUP_BYTES % 16 == 0 && CHUNK_BYTES % 16 == 0, "bulk copy granularity");
+  constexpr int NITEM = (3 * D + NT - 1) / NT;  // conv channels per thread
+  static_assert(CHUNK_BYTES % 16 == 0, "bulk copy granularity");
+  static_assert(2 * D <= NT, "each thread owns at most one q/k channel");
 
   extern __shared__ __align__(128) float sS[];  // D x D state tile
   __shared__ float sq[D], sk[D], sv[D], so[D];
   __shared__ float sred[3][NW];
-  __shared__ float sgate[5];  // alpha, beta, kq, inv_q*scale, inv_k
   __shared__ __align__(8) uint64_t bars[NCHUNK];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -65,39 +67,68 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_step_kernel(const Decod
     }
   }
 
-  // ---- prologue: conv + SiLU for the q, k channels of kh and v channels of h
+  // ---- prologue, one round of global loads: gate scalars and conv inputs
+  const int gi = bseq * p.Hv + h;
+  const float a_raw = to_f32(static_cast<const T*>(p.a)[gi]);
+  const float b_raw = to_f32(static_cast<const T*>(p.b)[gi]);
+  const float dparam = p.decay_param[h], dtb = p.dt_bias[h];
+
   const size_t C = (size_t)p.C;
   const T* xrow = static_cast<const T*>(p.mixed_qkv) + (size_t)bseq * C;
   T* cstate = static_cast<T*>(p.conv_state) + (size_t)bseq * C * 3;
   const T* w = static_cast<const T*>(p.conv_w);
   const int qk_f = p.Hk * D;
-  for (int idx = tid; idx < 3 * D; idx += NT) {
-    const int which = idx / D, i = idx - which * D;
-    const int c = which == 0 ? kh * D + i : which == 1 ? qk_f + kh * D + i : 2 * qk_f + h * D + i;
-    const T s0 = cstate[(size_t)c * 3 + 0], s1 = cstate[(size_t)c * 3 + 1],
-            s2 = cstate[(size_t)c * 3 + 2], xt = xrow[c];
-    const T* wc = w + (size_t)c * 4;
-    float acc = to_f32(wc[0]) * to_f32(s0);
-    acc += to_f32(wc[1]) * to_f32(s1);
-    acc += to_f32(wc[2]) * to_f32(s2);
-    acc += to_f32(wc[3]) * to_f32(xt);
-    const float y = silu_f(acc);
-    if (which == 0) {
-      sq[i] = y;
-    } else if (which == 1) {
-      sk[i] = y;
-    } else {
-      sv[i] = y;
-      cstate[(size_t)c * 3 + 0] = s1;  // v channels: this CTA is the only reader
-      cstate[(size_t)c * 3 + 1] = s2;
-      cstate[(size_t)c * 3 + 2] = xt;
+  T cs0[NITEM], cs1[NITEM], cs2[NITEM], cx[NITEM], cw[NITEM][4];
+  int chan[NITEM];
+#pragma unroll
+  for (int it = 0; it < NITEM; ++it) {
+    const int idx = tid + it * NT;
+    chan[it] = -1;
+    if (idx < 3 * D) {
+      const int which = idx / D, i = idx - which * D;
+      const int c = which == 0 ? kh * D + i : which == 1 ? qk_f + kh * D + i : 2 * qk_f + h * D + i;
+      chan[it] = c;
+      cs0[it] = cstate[(size_t)c * 3 + 0];
+      cs1[it] = cstate[(size_t)c * 3 + 1];
+      cs2[it] = cstate[(size_t)c * 3 + 2];
+      cx[it] = xrow[c];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) cw[it][j] = w[(size_t)c * 4 + j];
+    }
+  }
+  int qk_c = -1;
+  T qk_s1 = T(), qk_s2 = T(), qk_x = T();
+#pragma unroll
+  for (int it = 0; it < NITEM; ++it) {
+    const int idx = tid + it * NT;
+    if (idx < 3 * D) {
+      const int which = idx / D, i = idx - which * D;
+      float acc = to_f32(cw[it][0]) * to_f32(cs0[it]);
+      acc += to_f32(cw[it][1]) * to_f32(cs1[it]);
+      acc += to_f32(cw[it][2]) * to_f32(cs2[it]);
+      acc += to_f32(cw[it][3]) * to_f32(cx[it]);
+      const float y = silu_f(acc);
+      if (which == 2) {
+        sv[i] = y;
+        T* cp = cstate + (size_t)chan[it] * 3;  // v channels: this CTA is the only reader
+        cp[0] = cs1[it];
+        cp[1] = cs2[it];
+        cp[2] = cx[it];
+      } else {
+        (which == 0 ? sq : sk)[i] = y;
+        qk_c = chan[it];
+        qk_s1 = cs1[it];
+        qk_s2 = cs2[it];
+        qk_x = cx[it];
+      }
     }
   }
   // every CTA of the cluster has read the old q/k conv state after this
   cluster_arrive_release();
   __syncthreads();
 
-  // ---- l2 norms of q and k and the k.q product, block-reduced
+  // ---- l2 norms of q and k and the k.q product, block-reduced; every thread
+  // then forms the same scalars itself
   {
     float qq = 0.f, kk = 0.f, qk = 0.f;
     for (int i = tid; i < D; i += NT) {
@@ -116,40 +147,30 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_step_kernel(const Decod
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    float qq = 0.f, kk = 0.f, qk = 0.f;
+  float qq = 0.f, kk = 0.f, qkr = 0.f;
 #pragma unroll
-    for (int i = 0; i < NW; ++i) {
-      qq += sred[0][i];
-      kk += sred[1][i];
-      qk += sred[2][i];
-    }
-    const float inv_q = 1.f / sqrtf(qq + p.l2_eps);
-    const float inv_k = 1.f / sqrtf(kk + p.l2_eps);
-    const int gi = bseq * p.Hv + h;
-    const float a_raw = to_f32(static_cast<const T*>(p.a)[gi]);
-    const float b_raw = to_f32(static_cast<const T*>(p.b)[gi]);
-    const float g = gate_g(p.decay, p.decay_param[h], p.dt_bias[h], a_raw);
-    sgate[0] = expf(g);
-    sgate[1] = sigmoid_f(b_raw);
-    sgate[2] = qk * inv_q * inv_k * p.scale;
-    sgate[3] = inv_q * p.scale;
-    sgate[4] = inv_k;
+  for (int i = 0; i < NW; ++i) {
+    qq += sred[0][i];
+    kk += sred[1][i];
+    qkr += sred[2][i];
   }
-  __syncthreads();
+  const float inv_q = 1.f / sqrtf(qq + p.l2_eps);
+  const float inv_k = 1.f / sqrtf(kk + p.l2_eps);
+  const float kq = qkr * inv_q * inv_k * p.scale;
+  const float alpha = expf(gate_g(p.decay, dparam, dtb, a_raw));
+  const float beta = sigmoid_f(b_raw);
 
   // ---- the state pass
-  const float alpha = sgate[0], beta = sgate[1], kq = sgate[2];
   const int sub = lane % LPR, rq = lane / LPR;
   float kr[16], qr[16];
   {
-    const float sqs = sgate[3], sks = sgate[4];
+    const float sqs = inv_q * p.scale;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int col = 4 * sub + 4 * LPR * m + e;
-        kr[4 * m + e] = sk[col] * sks;
+        kr[4 * m + e] = sk[col] * inv_k;
         qr[4 * m + e] = sq[col] * sqs;
       }
     }
@@ -162,10 +183,11 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_step_kernel(const Decod
       break;
     }
     const int row = row0 + rq;
-    float* srow = sS + row * D;
+    const float* srow = sS + row * D;
     float4 s4[4];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) s4[m] = *reinterpret_cast<const float4*>(srow + 4 * sub + 4 * LPR * m);
+    for (int m = 0; m < 4; ++m)
+      s4[m] = *reinterpret_cast<const float4*>(srow + 4 * sub + 4 * LPR * m);
     float pk = 0.f, pq = 0.f;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -182,6 +204,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_step_kernel(const Decod
     pq = group_sum<LPR>(pq);
     const float d = beta * (sv[row] - alpha * pk);
     const float o = fmaf(alpha, pq, d * kq);
+    float* grow = gS + (size_t)row * D;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       float4 n4;
@@ -189,15 +212,9 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_step_kernel(const Decod
       n4.y = fmaf(d, kr[4 * m + 1], alpha * s4[m].y);
       n4.z = fmaf(d, kr[4 * m + 2], alpha * s4[m].z);
       n4.w = fmaf(d, kr[4 * m + 3], alpha * s4[m].w);
-      *reinterpret_cast<float4*>(srow + 4 * sub + 4 * LPR * m) = n4;
+      __stcs(reinterpret_cast<float4*>(grow + 4 * sub + 4 * LPR * m), n4);
     }
     if (sub == 0) so[row] = o;
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      bulk_store(gS + row0 * D, sS + row0 * D, GROUP_BYTES);
-      bulk_commit();
-    }
   }
   const bool all_ok = __syncthreads_and(ok) != 0;
 
@@ -229,17 +246,12 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_step_kernel(const Decod
   // ---- q/k conv state: written once per (sequence, K head), after every
   // CTA of the cluster has read the old values.
   cluster_wait_acquire();
-  if (r == 0) {
-    for (int idx = tid; idx < 2 * D; idx += NT) {
-      const int which = idx / D, i = idx - which * D;
-      const size_t c = which == 0 ? (size_t)kh * D + i : (size_t)qk_f + kh * D + i;
-      const T s1 = cstate[c * 3 + 1], s2 = cstate[c * 3 + 2], xt = xrow[c];
-      cstate[c * 3 + 0] = s1;
-      cstate[c * 3 + 1] = s2;
-      cstate[c * 3 + 2] = xt;
-    }
+  if (r == 0 && qk_c >= 0) {
+    T* cp = cstate + (size_t)qk_c * 3;
+    cp[0] = qk_s1;
+    cp[1] = qk_s2;
+    cp[2] = qk_x;
   }
-  if (lane == 0) bulk_wait_read_all();
 }
 
 template <typename T, int D>
