@@ -9,279 +9,431 @@
 // (the one-pass read-out identity gdn.rs notes as exact), so the two
 // reductions run side by side instead of one after the other.
 //
-// One CTA per (sequence, V head): it streams that head's D x D fp32 state
-// (64 KB at D=128) into shared memory with eight 1-D bulk copies issued first
-// thing, so the whole head is in flight while the prologue computes the conv,
-// norms and gates; every global load of the prologue is issued in one round.
-// Each row group is then updated in registers and written straight back to
-// global memory with coalesced 16-byte stores.
+// Structure: a persistent kernel, one CTA per SM. A work item is one
+// (sequence, K head) pair with all Hv/Hk V heads that read that K head, so
+// the CTA that reads a K head's old q/k conv state is also the only one that
+// writes the new one (no cross-CTA ordering). Items go to CTAs round-robin.
 //
-// Conv state ownership: the q/k channels of K head kh are read by every V
-// head mapped to kh (Hv/Hk CTAs). Those CTAs form one thread-block cluster;
-// each reads the old conv state, arrives on the cluster barrier, and only the
-// cluster's rank-0 CTA writes the new q/k conv state after waiting on it (from
-// values it kept in registers). The v channels belong to one head and are
-// written by its own CTA.
+// Inside a CTA, one producer warp streams the state rows of its items, in
+// order, through a ring of shared-memory slots with 1-D bulk copies (each
+// slot has a "full" mbarrier completed by the copy's byte count and an
+// "empty" mbarrier the consumer warps arrive on). The ring spans item
+// boundaries, so while the consumer warps compute the next item's conv,
+// norms and gates, its state is already streaming in. The eight consumer
+// warps update rows in registers (a quarter-warp per 512-byte row) and write
+// them back to global memory with coalesced 16-byte stores.
+//
+// Every wait is bounded; a wait that gives up records GDN_ERR_TIMEOUT and
+// raises a CTA-wide abort flag, after which no warp waits again, so the
+// kernel always runs to its end.
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 
 namespace gdn {
 
-constexpr int kDecodeThreads = 256;
+constexpr int kDecCW = 8;                      // consumer warps
+constexpr int kDecThreads = 32 * (kDecCW + 1);  // + one producer warp
+constexpr int kDecMaxStages = 16;              // ring slots (upper bound)
+constexpr int kDecRingBytes = 192 * 1024;      // shared-memory ring
+constexpr int kDecRPL = 2;                     // rows each lane updates per pass
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kDecodeThreads) decode_step_kernel(const DecodeArgs p) {
-  constexpr int NT = kDecodeThreads;
-  constexpr int NW = NT / 32;
-  constexpr int LPR = D / 16;             // lanes per state row (16 floats per lane)
-  constexpr int RPW = 32 / LPR;           // rows per warp pass
-  constexpr int NGROUPS = D / RPW;        // row groups of RPW rows
-  constexpr int NCHUNK = 8;               // bulk loads per head
-  constexpr int ROWS_PER_CHUNK = D / NCHUNK;
-  constexpr uint32_t CHUNK_BYTES = ROWS_PER_CHUNK * D * 4;
-  constexpr int NITEM = (3 * D + NT - 1) / NT;  // conv channels per thread
-  static_assert(CHUNK_BYTES % 16 == 0, "bulk copy granularity");
-  static_assert(2 * D <= NT, "each thread owns at most one q/k channel");
+template <int D>
+struct DecGeom {
+  static constexpr int LPR = D / 16;                       // lanes per row
+  static constexpr int RPW = 32 / LPR;                     // rows per warp, per row slot
+  static constexpr int WROWS = RPW * kDecRPL;              // rows per warp pass
+  static constexpr int CHUNK_ROWS = WROWS * kDecCW < D ? WROWS * kDecCW : D;
+  static constexpr int CPH = D / CHUNK_ROWS;               // chunks per head
+  static constexpr uint32_t SLOT_BYTES = CHUNK_ROWS * D * 4;
+  static constexpr int SLOT_FLOATS = CHUNK_ROWS * D;
+  static constexpr int STAGES_RAW = kDecRingBytes / (int)SLOT_BYTES;
+  static constexpr int STAGES = STAGES_RAW < kDecMaxStages ? STAGES_RAW : kDecMaxStages;
+  static constexpr int RING_BYTES = STAGES * (int)SLOT_BYTES;
+};
 
-  extern __shared__ __align__(128) float sS[];  // D x D state tile
-  __shared__ float sq[D], sk[D], sv[D], so[D];
-  __shared__ float sred[3][NW];
-  __shared__ __align__(8) uint64_t bars[NCHUNK];
+// Bounded wait that also gives up as soon as another warp has aborted.
+__device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (*abort_flag) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  record_device_error(GDN_ERR_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kDecCW * 32) : "memory");
+}
+
+template <typename T, int D, int REPMAX>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_step_kernel(const DecodeArgs p, const int num_items) {
+  using G = DecGeom<D>;
+  constexpr int LPR = G::LPR, RPW = G::RPW;
+  constexpr int kDecStages = G::STAGES;
+  constexpr int kDecMaxRep = REPMAX;
+  constexpr int NC = kDecCW * 32;
+  static_assert(2 * D <= NC, "each consumer thread owns at most one q/k channel");
+
+  extern __shared__ __align__(128) float ring[];
+  // per-item buffers written before an item's first barrier are doubled
+  // (by item parity) so a fast warp may start the next item while slow warps
+  // finish this one
+  __shared__ float sq[2][D], sk[2][D], sv[2][kDecMaxRep][D], so[kDecMaxRep][D];
+  __shared__ float sred[3][kDecCW];
+  __shared__ float sgate[2][kDecMaxRep][2];
+  __shared__ float snw[D];
+  __shared__ __align__(8) uint64_t full_bar[kDecMaxStages], empty_bar[kDecMaxStages];
+  __shared__ int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int bseq = blockIdx.y;
-  const int kh = blockIdx.x / p.rep;
-  const int r = blockIdx.x - kh * p.rep;
-  const int h = p.map == GDN_MAP_TILED ? kh + r * p.Hk : blockIdx.x;
-  float* gS = p.state + ((size_t)bseq * p.Hv + h) * (size_t)(D * D);
+  const int rep = p.rep, Hk = p.Hk, Hv = p.Hv;
 
   if (tid == 0) {
-#pragma unroll
-    for (int c = 0; c < NCHUNK; ++c) mbar_init(&bars[c], 1);
+    for (int s = 0; s < kDecStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kDecCW);
+    }
+    s_abort = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
-#pragma unroll
-    for (int c = 0; c < NCHUNK; ++c) {
-      mbar_arrive_expect_tx(&bars[c], CHUNK_BYTES);
-      bulk_load(sS + c * ROWS_PER_CHUNK * D, gS + c * ROWS_PER_CHUNK * D, CHUNK_BYTES, &bars[c]);
+  }
+  __syncthreads();
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == kDecCW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t k = 0;
+      for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+        const int b = item / Hk, kh = item - (item / Hk) * Hk;
+        for (int r = 0; r < rep; ++r) {
+          const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+          const float* gS = p.state + ((size_t)b * Hv + h) * (size_t)(D * D);
+          for (int c = 0; c < G::CPH; ++c, ++k) {
+            const int slot = (int)(k % kDecStages);
+            if (k >= (uint32_t)kDecStages &&
+                !dec_wait(&empty_bar[slot], ((k / kDecStages) - 1) & 1, abort_flag))
+              return;
+            mbar_arrive_expect_tx(&full_bar[slot], G::SLOT_BYTES);
+            bulk_load(ring + slot * G::SLOT_FLOATS, gS + (size_t)c * G::SLOT_FLOATS,
+                      G::SLOT_BYTES, &full_bar[slot]);
+          }
+        }
+      }
     }
+    return;
   }
 
-  // ---- prologue, one round of global loads: gate scalars and conv inputs
-  const int gi = bseq * p.Hv + h;
-  const float a_raw = to_f32(static_cast<const T*>(p.a)[gi]);
-  const float b_raw = to_f32(static_cast<const T*>(p.b)[gi]);
-  const float dparam = p.decay_param[h], dtb = p.dt_bias[h];
-
+  // -------------------------------------------------------------- consumers
   const size_t C = (size_t)p.C;
-  const T* xrow = static_cast<const T*>(p.mixed_qkv) + (size_t)bseq * C;
-  T* cstate = static_cast<T*>(p.conv_state) + (size_t)bseq * C * 3;
+  const int qk_f = Hk * D;
   const T* w = static_cast<const T*>(p.conv_w);
-  const int qk_f = p.Hk * D;
-  T cs0[NITEM], cs1[NITEM], cs2[NITEM], cx[NITEM], cw[NITEM][4];
-  int chan[NITEM];
+  const int sub = lane % LPR, rq = lane / LPR;
+  // Prefetch registers: the conv inputs and gate scalars of the NEXT item
+  // are loaded while the current one is processed, so an item's prologue
+  // never waits on global memory.
+  constexpr int NIT = ((2 + kDecMaxRep) * D + NC - 1) / NC;
+  T pcs0[NIT], pcs1[NIT], pcs2[NIT], pcx[NIT], pcw[NIT][4];
+  int pchan[NIT];
+  float pga = 0.f, pgb = 0.f, pgp = 0.f, pgd = 0.f;
+  constexpr int PER = D / 32;  // output elements per lane (warp r writes head r)
+  T pz[PER];
+  if (p.z != nullptr)
+    for (int j = tid; j < D; j += NC) snw[j] = p.norm_w[j];
+  auto prefetch = [&](int item) {
+    const int b = item / Hk, kh = item - (item / Hk) * Hk;
+    const T* xrow = static_cast<const T*>(p.mixed_qkv) + (size_t)b * C;
+    const T* cst = static_cast<const T*>(p.conv_state) + (size_t)b * C * 3;
+    const int nch = (2 + rep) * D;
 #pragma unroll
-  for (int it = 0; it < NITEM; ++it) {
-    const int idx = tid + it * NT;
-    chan[it] = -1;
-    if (idx < 3 * D) {
-      const int which = idx / D, i = idx - which * D;
-      const int c = which == 0 ? kh * D + i : which == 1 ? qk_f + kh * D + i : 2 * qk_f + h * D + i;
-      chan[it] = c;
-      cs0[it] = cstate[(size_t)c * 3 + 0];
-      cs1[it] = cstate[(size_t)c * 3 + 1];
-      cs2[it] = cstate[(size_t)c * 3 + 2];
-      cx[it] = xrow[c];
+    for (int it = 0; it < NIT; ++it) {
+      const int idx = tid + it * NC;
+      pchan[it] = -1;
+      if (item < num_items && idx < nch) {
+        const int which = idx / D, i = idx - which * D;
+        int c;
+        if (which < 2) {
+          c = which * qk_f + kh * D + i;
+        } else {
+          const int r = which - 2;
+          const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+          c = 2 * qk_f + h * D + i;
+        }
+        pchan[it] = c;
+        const T* cp = cst + (size_t)c * 3;
+        pcs0[it] = cp[0];
+        pcs1[it] = cp[1];
+        pcs2[it] = cp[2];
+        pcx[it] = xrow[c];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) cw[it][j] = w[(size_t)c * 4 + j];
+        for (int j = 0; j < 4; ++j) pcw[it][j] = w[(size_t)c * 4 + j];
+      } else {
+        pcs0[it] = pcs1[it] = pcs2[it] = pcx[it] = T();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pcw[it][j] = T();
+      }
     }
-  }
-  int qk_c = -1;
-  T qk_s1 = T(), qk_s2 = T(), qk_x = T();
+    if (item < num_items && tid < rep) {
+      const int h = p.map == GDN_MAP_TILED ? kh + tid * Hk : kh * rep + tid;
+      const int gi = b * Hv + h;
+      pga = to_f32(static_cast<const T*>(p.a)[gi]);
+      pgb = to_f32(static_cast<const T*>(p.b)[gi]);
+      pgp = p.decay_param[h];
+      pgd = p.dt_bias[h];
+    }
+    if (item < num_items && p.z != nullptr && warp < rep) {
+      const int h = p.map == GDN_MAP_TILED ? kh + warp * Hk : kh * rep + warp;
+      const T* zr = static_cast<const T*>(p.z) + ((size_t)b * Hv + h) * D + lane * PER;
 #pragma unroll
-  for (int it = 0; it < NITEM; ++it) {
-    const int idx = tid + it * NT;
-    if (idx < 3 * D) {
+      for (int e = 0; e < PER; ++e) pz[e] = zr[e];
+    }
+  };
+  prefetch(blockIdx.x);
+
+  uint32_t k = 0;
+  for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+    const int b = item / Hk, kh = item - (item / Hk) * Hk;
+    T* cstate = static_cast<T*>(p.conv_state) + (size_t)b * C * 3;
+    const int buf = ((item - (int)blockIdx.x) / (int)gridDim.x) & 1;
+    T cs1[NIT], cs2[NIT], cx[NIT];
+    int chan[NIT];
+    float y[NIT];
+    T zc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) zc[e] = pz[e];
+    // conv + SiLU for this item from the prefetched registers: channels
+    // [q of kh | k of kh | v of each head]
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+      chan[it] = pchan[it];
+      cs1[it] = pcs1[it];
+      cs2[it] = pcs2[it];
+      cx[it] = pcx[it];
+      float acc = to_f32(pcw[it][0]) * to_f32(pcs0[it]);
+      acc += to_f32(pcw[it][1]) * to_f32(pcs1[it]);
+      acc += to_f32(pcw[it][2]) * to_f32(pcs2[it]);
+      acc += to_f32(pcw[it][3]) * to_f32(pcx[it]);
+      y[it] = silu_f(acc);
+    }
+    if (tid < rep) {
+      sgate[buf][tid][0] = expf(gate_g(p.decay, pgp, pgd, pga));
+      sgate[buf][tid][1] = sigmoid_f(pgb);
+    }
+    prefetch(item + gridDim.x);
+    int qk_c = -1;
+    T qk_s1 = T(), qk_s2 = T(), qk_x = T();
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+      if (chan[it] < 0) continue;
+      const int idx = tid + it * NC;
       const int which = idx / D, i = idx - which * D;
-      float acc = to_f32(cw[it][0]) * to_f32(cs0[it]);
-      acc += to_f32(cw[it][1]) * to_f32(cs1[it]);
-      acc += to_f32(cw[it][2]) * to_f32(cs2[it]);
-      acc += to_f32(cw[it][3]) * to_f32(cx[it]);
-      const float y = silu_f(acc);
-      if (which == 2) {
-        sv[i] = y;
-        T* cp = cstate + (size_t)chan[it] * 3;  // v channels: this CTA is the only reader
+      if (which >= 2) {
+        sv[buf][which - 2][i] = y[it];
+        T* cp = cstate + (size_t)chan[it] * 3;  // this CTA alone reads and writes these channels
         cp[0] = cs1[it];
         cp[1] = cs2[it];
         cp[2] = cx[it];
       } else {
-        (which == 0 ? sq : sk)[i] = y;
+        (which == 0 ? sq[buf] : sk[buf])[i] = y[it];
         qk_c = chan[it];
         qk_s1 = cs1[it];
         qk_s2 = cs2[it];
         qk_x = cx[it];
       }
     }
-  }
-  // every CTA of the cluster has read the old q/k conv state after this
-  cluster_arrive_release();
-  __syncthreads();
+    consumer_sync();
 
-  // ---- l2 norms of q and k and the k.q product, block-reduced; every thread
-  // then forms the same scalars itself
-  {
-    float qq = 0.f, kk = 0.f, qk = 0.f;
-    for (int i = tid; i < D; i += NT) {
-      const float qv = sq[i], kv = sk[i];
-      qq += qv * qv;
-      kk += kv * kv;
-      qk += qv * kv;
-    }
-    qq = group_sum<32>(qq);
-    kk = group_sum<32>(kk);
-    qk = group_sum<32>(qk);
-    if (lane == 0) {
-      sred[0][warp] = qq;
-      sred[1][warp] = kk;
-      sred[2][warp] = qk;
-    }
-  }
-  __syncthreads();
-  float qq = 0.f, kk = 0.f, qkr = 0.f;
-#pragma unroll
-  for (int i = 0; i < NW; ++i) {
-    qq += sred[0][i];
-    kk += sred[1][i];
-    qkr += sred[2][i];
-  }
-  const float inv_q = 1.f / sqrtf(qq + p.l2_eps);
-  const float inv_k = 1.f / sqrtf(kk + p.l2_eps);
-  const float kq = qkr * inv_q * inv_k * p.scale;
-  const float alpha = expf(gate_g(p.decay, dparam, dtb, a_raw));
-  const float beta = sigmoid_f(b_raw);
-
-  // ---- the state pass
-  const int sub = lane % LPR, rq = lane / LPR;
-  float kr[16], qr[16];
-  {
-    const float sqs = inv_q * p.scale;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int col = 4 * sub + 4 * LPR * m + e;
-        kr[4 * m + e] = sk[col] * inv_k;
-        qr[4 * m + e] = sq[col] * sqs;
+    // l2 norms of q and k and k.q
+    {
+      float qq = 0.f, kk = 0.f, qk = 0.f;
+      for (int i = tid; i < D; i += NC) {
+        const float qv = sq[buf][i], kv = sk[buf][i];
+        qq += qv * qv;
+        kk += kv * kv;
+        qk += qv * kv;
+      }
+      qq = group_sum<32>(qq);
+      kk = group_sum<32>(kk);
+      qk = group_sum<32>(qk);
+      if (lane == 0) {
+        sred[0][warp] = qq;
+        sred[1][warp] = kk;
+        sred[2][warp] = qk;
       }
     }
-  }
-  bool ok = true;
-  for (int grp = warp; grp < NGROUPS; grp += NW) {
-    const int row0 = grp * RPW;
-    if (!mbar_wait(&bars[row0 / ROWS_PER_CHUNK], 0)) {
-      ok = false;
-      break;
-    }
-    const int row = row0 + rq;
-    const float* srow = sS + row * D;
-    float4 s4[4];
+    consumer_sync();
+    float qq = 0.f, kk = 0.f, qkr = 0.f;
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
-      s4[m] = *reinterpret_cast<const float4*>(srow + 4 * sub + 4 * LPR * m);
-    float pk = 0.f, pq = 0.f;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      pk = fmaf(s4[m].x, kr[4 * m + 0], pk);
-      pq = fmaf(s4[m].x, qr[4 * m + 0], pq);
-      pk = fmaf(s4[m].y, kr[4 * m + 1], pk);
-      pq = fmaf(s4[m].y, qr[4 * m + 1], pq);
-      pk = fmaf(s4[m].z, kr[4 * m + 2], pk);
-      pq = fmaf(s4[m].z, qr[4 * m + 2], pq);
-      pk = fmaf(s4[m].w, kr[4 * m + 3], pk);
-      pq = fmaf(s4[m].w, qr[4 * m + 3], pq);
+    for (int i = 0; i < kDecCW; ++i) {
+      qq += sred[0][i];
+      kk += sred[1][i];
+      qkr += sred[2][i];
     }
-    pk = group_sum<LPR>(pk);
-    pq = group_sum<LPR>(pq);
-    const float d = beta * (sv[row] - alpha * pk);
-    const float o = fmaf(alpha, pq, d * kq);
-    float* grow = gS + (size_t)row * D;
+    const float inv_q = 1.f / sqrtf(qq + p.l2_eps);
+    const float inv_k = 1.f / sqrtf(kk + p.l2_eps);
+    const float kq = qkr * inv_q * inv_k * p.scale;
+    float kr[16], qr[16];
+    {
+      const float sqs = inv_q * p.scale;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      float4 n4;
-      n4.x = fmaf(d, kr[4 * m + 0], alpha * s4[m].x);
-      n4.y = fmaf(d, kr[4 * m + 1], alpha * s4[m].y);
-      n4.z = fmaf(d, kr[4 * m + 2], alpha * s4[m].z);
-      n4.w = fmaf(d, kr[4 * m + 3], alpha * s4[m].w);
-      __stcs(reinterpret_cast<float4*>(grow + 4 * sub + 4 * LPR * m), n4);
-    }
-    if (sub == 0) so[row] = o;
-  }
-  const bool all_ok = __syncthreads_and(ok) != 0;
-
-  // ---- outputs
-  const size_t obase = ((size_t)bseq * p.Hv + h) * D;
-  if (all_ok) {
-    if (p.core_out != nullptr) {
-      for (int j = tid; j < D; j += NT) p.core_out[obase + j] = so[j];
-    }
-    if (p.z != nullptr) {
-      float ss = 0.f;
-      for (int j = tid; j < D; j += NT) ss += so[j] * so[j];
-      ss = group_sum<32>(ss);
-      if (lane == 0) sred[0][warp] = ss;
-      __syncthreads();
-      float tot = 0.f;
+      for (int m = 0; m < 4; ++m) {
 #pragma unroll
-      for (int i = 0; i < NW; ++i) tot += sred[0][i];
-      const float inv = 1.f / sqrtf(tot / (float)D + p.rms_eps);
-      const T* zr = static_cast<const T*>(p.z) + obase;
-      T* outr = static_cast<T*>(p.out) + obase;
-      for (int j = tid; j < D; j += NT) {
-        const float y = so[j] * inv * p.norm_w[j] * silu_f(to_f32(zr[j]));
-        outr[j] = from_f32<T>(y);
+        for (int e = 0; e < 4; ++e) {
+          const int col = 4 * sub + 4 * LPR * m + e;
+          kr[4 * m + e] = sk[buf][col] * inv_k;
+          qr[4 * m + e] = sq[buf][col] * sqs;
+        }
       }
     }
-  }
 
-  // ---- q/k conv state: written once per (sequence, K head), after every
-  // CTA of the cluster has read the old values.
-  cluster_wait_acquire();
-  if (r == 0 && qk_c >= 0) {
-    T* cp = cstate + (size_t)qk_c * 3;
-    cp[0] = qk_s1;
-    cp[1] = qk_s2;
-    cp[2] = qk_x;
+    // the state pass over the item's heads, chunk by chunk from the ring
+    for (int r = 0; r < rep; ++r) {
+      const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+      float* gS = p.state + ((size_t)b * Hv + h) * (size_t)(D * D);
+      const float alpha = sgate[buf][r][0], beta = sgate[buf][r][1];
+      for (int c = 0; c < G::CPH; ++c, ++k) {
+        const int slot = (int)(k % kDecStages);
+        const bool ready = dec_wait(&full_bar[slot], (k / kDecStages) & 1, abort_flag);
+        if (ready && warp * G::WROWS < G::CHUNK_ROWS) {
+          float4 s4[kDecRPL][4];
+          int rowv[kDecRPL];
+#pragma unroll
+          for (int u = 0; u < kDecRPL; ++u) {
+            const int rl = warp * G::WROWS + u * RPW + rq;  // row within the chunk
+            rowv[u] = c * G::CHUNK_ROWS + rl;
+            const float* srow = ring + slot * G::SLOT_FLOATS + rl * D;
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+              s4[u][m] = *reinterpret_cast<const float4*>(srow + 4 * sub + 4 * LPR * m);
+          }
+          float pk[kDecRPL], pq[kDecRPL];
+#pragma unroll
+          for (int u = 0; u < kDecRPL; ++u) {
+            float pk4[4], pq4[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              pk4[m] = s4[u][m].x * kr[4 * m + 0];
+              pq4[m] = s4[u][m].x * qr[4 * m + 0];
+              pk4[m] = fmaf(s4[u][m].y, kr[4 * m + 1], pk4[m]);
+              pq4[m] = fmaf(s4[u][m].y, qr[4 * m + 1], pq4[m]);
+              pk4[m] = fmaf(s4[u][m].z, kr[4 * m + 2], pk4[m]);
+              pq4[m] = fmaf(s4[u][m].z, qr[4 * m + 2], pq4[m]);
+              pk4[m] = fmaf(s4[u][m].w, kr[4 * m + 3], pk4[m]);
+              pq4[m] = fmaf(s4[u][m].w, qr[4 * m + 3], pq4[m]);
+            }
+            pk[u] = (pk4[0] + pk4[1]) + (pk4[2] + pk4[3]);
+            pq[u] = (pq4[0] + pq4[1]) + (pq4[2] + pq4[3]);
+          }
+#pragma unroll
+          for (int o = LPR / 2; o > 0; o >>= 1) {
+#pragma unroll
+            for (int u = 0; u < kDecRPL; ++u) {
+              pk[u] += __shfl_xor_sync(0xffffffffu, pk[u], o);
+              pq[u] += __shfl_xor_sync(0xffffffffu, pq[u], o);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kDecRPL; ++u) {
+            const int row = rowv[u];
+            const float d = beta * (sv[buf][r][row] - alpha * pk[u]);
+            const float o = fmaf(alpha, pq[u], d * kq);
+            float* grow = gS + (size_t)row * D;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              float4 n4;
+              n4.x = fmaf(d, kr[4 * m + 0], alpha * s4[u][m].x);
+              n4.y = fmaf(d, kr[4 * m + 1], alpha * s4[u][m].y);
+              n4.z = fmaf(d, kr[4 * m + 2], alpha * s4[u][m].z);
+              n4.w = fmaf(d, kr[4 * m + 3], alpha * s4[u][m].w);
+              __stcs(reinterpret_cast<float4*>(grow + 4 * sub + 4 * LPR * m), n4);
+            }
+            if (sub == 0) so[r][row] = o;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+      }
+    }
+    consumer_sync();
+
+    // outputs: warp r finishes head r (core output and/or gated norm)
+    const bool live = !*abort_flag;
+    if (warp < rep && live) {
+      const int r = warp;
+      const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+      const size_t obase = ((size_t)b * Hv + h) * D + lane * PER;
+      float ov[PER];
+#pragma unroll
+      for (int e = 0; e < PER; ++e) ov[e] = so[r][lane * PER + e];
+      if (p.core_out != nullptr) {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) p.core_out[obase + e] = ov[e];
+      }
+      if (p.z != nullptr) {
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) ss += ov[e] * ov[e];
+        ss = group_sum<32>(ss);
+        const float inv = 1.f / sqrtf(ss / (float)D + p.rms_eps);
+        T* outr = static_cast<T*>(p.out) + obase;
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+          outr[e] = from_f32<T>(ov[e] * inv * snw[lane * PER + e] * silu_f(to_f32(zc[e])));
+      }
+    }
+    // new q/k conv state: this CTA read the old values itself, in the prologue
+    if (qk_c >= 0 && live) {
+      T* cp = cstate + (size_t)qk_c * 3;
+      cp[0] = qk_s1;
+      cp[1] = qk_s2;
+      cp[2] = qk_x;
+    }
   }
 }
 
-template <typename T, int D>
+static int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <typename T, int D, int REPMAX>
 static cudaError_t launch_decode_t(const DecodeArgs& p, int32_t batch, cudaStream_t stream) {
-  auto kern = decode_step_kernel<T, D>;
-  const int smem = D * D * (int)sizeof(float);
+  auto kern = decode_step_kernel<T, D, REPMAX>;
+  const int smem = DecGeom<D>::RING_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.Hv, (unsigned)batch, 1);
-  cfg.blockDim = dim3(kDecodeThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)p.rep;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  const int items = batch * p.Hk;
+  const int grid = items < sm_count() ? items : sm_count();
+  kern<<<grid, kDecThreads, smem, stream>>>(p, items);
+  return cudaGetLastError();
+}
+
+// The per-item register and shared buffers are sized for REPMAX V heads per
+// K head: 2, 4 or 8.
+template <typename T, int D>
+static cudaError_t launch_decode_r(const DecodeArgs& p, int32_t batch, cudaStream_t stream) {
+  if (p.rep <= 2) return launch_decode_t<T, D, 2>(p, batch, stream);
+  if (p.rep <= 4) return launch_decode_t<T, D, 4>(p, batch, stream);
+  return launch_decode_t<T, D, 8>(p, batch, stream);
 }
 
 template <typename T>
 static cudaError_t launch_decode_d(const DecodeArgs& p, int32_t D, int32_t batch,
                                    cudaStream_t stream) {
   switch (D) {
-    case 32: return launch_decode_t<T, 32>(p, batch, stream);
-    case 64: return launch_decode_t<T, 64>(p, batch, stream);
-    case 128: return launch_decode_t<T, 128>(p, batch, stream);
+    case 32: return launch_decode_r<T, 32>(p, batch, stream);
+    case 64: return launch_decode_r<T, 64>(p, batch, stream);
+    case 128: return launch_decode_r<T, 128>(p, batch, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,0 +1,171 @@
+// Tensor-core (tcgen05 / TMEM) and TMA building blocks for sm_103a, as inline
+// PTX. Layout conventions used throughout:
+//
+//  * Shared-memory operand tiles are K-major with the 128-byte swizzle: a tile
+//    of R rows is stored as ceil(K*elem/128) "K atoms"; atom a holds bytes
+//    [128a, 128a+128) of every row, rows 128 B apart, and inside each 8-row
+//    group (1024 B) the 16-byte chunk j of row r sits at chunk (j ^ (r & 7)).
+//    Tiles start on a 1024-byte boundary. This is the layout a TMA load with
+//    CU_TENSOR_MAP_SWIZZLE_128B writes for a box whose inner extent is 128 B.
+//  * One MMA instruction consumes 32 bytes of K (16 bf16/f16, 8 tf32), so the
+//    descriptor of k-step s starts (s / 4) atoms and (s % 4) * 32 B in.
+//  * TMEM addresses are (lane << 16) | column.
+#pragma once
+
+#include <stdint.h>
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+namespace tc {
+
+// ------------------------------------------------------------ descriptors
+
+// Byte offset of element (r, k) in a K-major SW128 tile of `rows` rows whose
+// elements are `esize` bytes.
+__host__ __device__ __forceinline__ uint32_t sw128_offset(int r, int k, int rows, int esize) {
+  const int kb = k * esize;               // byte position along K
+  const int atom = kb >> 7;               // 128-byte K atom
+  const int chunk = (kb >> 4) & 7;        // 16-byte chunk inside the atom
+  const int within = kb & 15;
+  return (uint32_t)(atom * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 +
+                    ((chunk ^ (r & 7)) << 4) + within);
+}
+
+// Shared-memory matrix descriptor for a K-major SW128 tile (Blackwell form:
+// start >> 4 in bits 0-13, leading offset 16-29 (unused here), stride offset
+// 32-45 = 1024 B between 8-row groups, version 1 in bits 46-47, layout type
+// SWIZZLE_128B (2) in bits 61-63).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;                 // leading byte offset (ignored for SW128 K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  d |= (uint64_t)2 << 61;                 // SWIZZLE_128B
+  return d;
+}
+
+// Descriptor of k-step `s` (32 bytes of K each) of a K-major SW128 tile.
+__device__ __forceinline__ uint64_t sdesc_kstep(uint32_t tile_addr, int rows, int s) {
+  return sdesc_sw128(tile_addr + (uint32_t)((s >> 2) * rows * 128 + (s & 3) * 32));
+}
+
+enum : uint32_t { kF16 = 0, kBF16 = 1, kTF32 = 2 };
+
+// Instruction descriptor for kind::f16 / kind::tf32 with fp32 accumulation,
+// both operands K-major: D format (bits 4-5) = F32, A/B formats in bits 7-9 /
+// 10-12, N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ __forceinline__ uint32_t idesc(uint32_t ab_format, int M, int N) {
+  uint32_t d = 0;
+  d |= 1u << 4;
+  d |= ab_format << 7;
+  d |= ab_format << 10;
+  d |= (uint32_t)(N >> 3) << 17;
+  d |= (uint32_t)(M >> 4) << 24;
+  return d;
+}
+
+// ------------------------------------------------------------------ TMEM
+
+// Allocates `ncols` TMEM columns (power of two >= 32) for the CTA; the base
+// address is written to *dst (shared). Executed by one full warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ------------------------------------------------------------------- MMA
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one instruction (K = 32 bytes).
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                        bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"((uint32_t)accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                         bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"((uint32_t)accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every tcgen05 operation this thread issued so far has
+// completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+// -------------------------------------------------------------- TMEM I/O
+// 32x32b shape: thread t of the warp reads/writes lane (quadrant base + t),
+// consecutive 32-bit columns.
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------------- TMA
+// 2-D tiled load of box (x = inner coordinate, y = row) into shared memory,
+// completing `bytes` on the mbarrier.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+}  // namespace tc
+}  // namespace gdn
