@@ -23,7 +23,7 @@ GDN_OK = 0
 GDN_MAP_GROUPED, GDN_MAP_TILED = 0, 1
 GDN_DECAY_LOG_RATE, GDN_DECAY_NEGATIVE_RATE = 0, 1
 GDN_F16, GDN_BF16, GDN_F32 = 0, 1, 2
-GDN_QK_PRENORMALIZED, GDN_GATES_PRECOMPUTED = 1, 2
+GDN_QK_PRENORMALIZED, GDN_GATES_PRECOMPUTED, GDN_PREFILL_CUDA_CORES = 1, 2, 4
 
 _TORCH_TO_GDN = {torch.float16: GDN_F16, torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}
 _GDN_TO_TORCH = {v: k for k, v in _TORCH_TO_GDN.items()}
@@ -208,4 +208,4 @@ __all__ = ["GdnDims", "GdnError", "dims", "library", "status_string", "gdn_conv_
            "gdn_decode_step", "gdn_prefill_chunked", "gdn_gated_rmsnorm", "gdn_device_error",
            "gdn_qkv_features", "gdn_version", "GDN_MAP_GROUPED", "GDN_MAP_TILED",
            "GDN_DECAY_LOG_RATE", "GDN_DECAY_NEGATIVE_RATE", "GDN_F16", "GDN_BF16", "GDN_F32",
-           "GDN_QK_PRENORMALIZED", "GDN_GATES_PRECOMPUTED", "LIB_PATH"]
+           "GDN_QK_PRENORMALIZED", "GDN_GATES_PRECOMPUTED", "GDN_PREFILL_CUDA_CORES", "LIB_PATH"]

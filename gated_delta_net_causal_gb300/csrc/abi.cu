@@ -210,7 +210,8 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int
   if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
   if (num_seqs == 0 && total_tokens > 0) return GDN_ERR_INVALID_ARG;
   if (num_seqs > kMaxGridY) return GDN_ERR_EXTENT;
-  if ((flags & ~(GDN_QK_PRENORMALIZED | GDN_GATES_PRECOMPUTED)) != 0) return GDN_ERR_INVALID_ARG;
+  if ((flags & ~(GDN_QK_PRENORMALIZED | GDN_GATES_PRECOMPUTED | GDN_PREFILL_CUDA_CORES)) != 0)
+    return GDN_ERR_INVALID_ARG;
   if (num_seqs == 0) return GDN_OK;
   const bool pregate = (flags & GDN_GATES_PRECOMPUTED) != 0;
   if (!cu_seqlens || !state) return GDN_ERR_INVALID_ARG;
@@ -318,7 +319,8 @@ gdn_status gdn_device_error(int32_t* status, int32_t clear) {
   if (status == nullptr) return GDN_ERR_INVALID_ARG;
   *status = GDN_OK;
   cudaError_t (*readers[])(int32_t*, bool) = {gdn::read_error_decode, gdn::read_error_conv,
-                                               gdn::read_error_rmsnorm, gdn::read_error_prefill};
+                                               gdn::read_error_rmsnorm, gdn::read_error_prefill,
+                                               gdn::read_error_prefill_tc};
   for (auto rd : readers) {
     int32_t v = 0;
     if (rd(&v, clear != 0) != cudaSuccess) return GDN_ERR_CUDA;

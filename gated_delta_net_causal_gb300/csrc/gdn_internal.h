@@ -77,12 +77,16 @@ cudaError_t launch_decode(const DecodeArgs& p, int32_t dtype, int32_t D, int32_t
 cudaError_t launch_conv(const ConvArgs& p, int32_t dtype, cudaStream_t stream);
 cudaError_t launch_rmsnorm(const RmsNormArgs& p, int32_t dtype, int32_t D, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& p, int32_t dtype, int32_t D, cudaStream_t stream);
+// tensor-core chunked prefill (head_dim 128, f16/bf16 activations)
+bool prefill_tc_supported(const PrefillArgs& p, int32_t dtype, int32_t D);
+cudaError_t launch_prefill_tc(const PrefillArgs& p, int32_t dtype, cudaStream_t stream);
 
 // Device error words, one per kernel translation unit.
 cudaError_t read_error_decode(int32_t* status, bool clear);
 cudaError_t read_error_conv(int32_t* status, bool clear);
 cudaError_t read_error_rmsnorm(int32_t* status, bool clear);
 cudaError_t read_error_prefill(int32_t* status, bool clear);
+cudaError_t read_error_prefill_tc(int32_t* status, bool clear);
 
 }  // namespace gdn
 

@@ -317,6 +317,8 @@ static cudaError_t launch_prefill_d(const PrefillArgs& p, int32_t D, cudaStream_
 }
 
 cudaError_t launch_prefill(const PrefillArgs& p, int32_t dtype, int32_t D, cudaStream_t stream) {
+  if ((p.flags & GDN_PREFILL_CUDA_CORES) == 0 && prefill_tc_supported(p, dtype, D))
+    return launch_prefill_tc(p, dtype, stream);
   switch (dtype) {
     case GDN_F16: return launch_prefill_d<__half>(p, D, stream);
     case GDN_BF16: return launch_prefill_d<__nv_bfloat16>(p, D, stream);

@@ -66,6 +66,14 @@ __host__ __device__ __forceinline__ uint32_t idesc(uint32_t ab_format, int M, in
   return d;
 }
 
+// fp32 -> tf32 with round-to-nearest (ties away); the tensor cores would
+// otherwise drop the low 13 mantissa bits of an fp32 operand (truncation).
+__device__ __forceinline__ float tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
 // ------------------------------------------------------------------ TMEM
 
 // Allocates `ncols` TMEM columns (power of two >= 32) for the CTA; the base

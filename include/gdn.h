@@ -63,8 +63,10 @@ typedef enum gdn_dtype { GDN_F16 = 0, GDN_BF16 = 1, GDN_F32 = 2 } gdn_dtype;
 
 /* gdn_prefill_chunked flags */
 enum {
-  GDN_QK_PRENORMALIZED = 1, /* q and k are already l2-normalised: skip it */
-  GDN_GATES_PRECOMPUTED = 2 /* a holds g and b holds beta, both fp32 [T][Hv] */
+  GDN_QK_PRENORMALIZED = 1,  /* q and k are already l2-normalised: skip it */
+  GDN_GATES_PRECOMPUTED = 2, /* a holds g and b holds beta, both fp32 [T][Hv] */
+  GDN_PREFILL_CUDA_CORES = 4 /* use the fp32 CUDA-core chunk kernel even where the
+                                tensor-core one applies (head_dim 128, f16/bf16) */
 };
 
 typedef struct gdn_dims {
@@ -163,7 +165,11 @@ gdn_status gdn_decode_step(const gdn_dims* dims, int32_t batch, const void* mixe
  * a, b         [T][Hv] io dtype raw gate inputs, or with
  *              GDN_GATES_PRECOMPUTED fp32 g and beta.
  * decay_param, dt_bias  [Hv] fp32 (ignored with GDN_GATES_PRECOMPUTED).
- * flags        GDN_QK_PRENORMALIZED | GDN_GATES_PRECOMPUTED.
+ * flags        GDN_QK_PRENORMALIZED | GDN_GATES_PRECOMPUTED | GDN_PREFILL_CUDA_CORES.
+ *              Head_dim 128 with f16/bf16 activations runs on the tensor cores
+ *              (bf16/f16 K K^T and Q K^T, tf32 for every product with the
+ *              state or with the triangular inverse); other shapes, fp32
+ *              activations or GDN_PREFILL_CUDA_CORES use fp32 CUDA cores.
  * state        [N][Hv][D][D] fp32, in place (initial state = its contents).
  * core_out     [T][Hv][D] fp32 core output, or NULL.
  * z, norm_w, out  optional fused gated RMSNorm as in gdn_decode_step.

@@ -61,14 +61,18 @@ def _run_prefill(d, cu, q, k, v, a, b, state, flags, dp=None, dt=None, z=None, n
     return core, out
 
 
+@pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("hk,hv,d", [(2, 4, 32), (2, 4, 128), (2, 2, 128)])
 @pytest.mark.parametrize("mp", [gi.GROUPED, gi.TILED])
-def test_page_chunk_case_and_split_continuity(hk, hv, d, mp):
+def test_page_chunk_case_and_split_continuity(hk, hv, d, mp, io):
     """T = 145 (2 x 64 + 17), split at 73, with the state's sentinel tail
-    untouched (the Metal chunk test's shapes and fill)."""
+    untouched (the Metal chunk test's shapes and fill). fp32 activations run
+    the CUDA-core kernel; bf16 at head_dim 128 the tensor-core one."""
     T = 145
     q, k, v, g, beta, S0 = _page_chunk_inputs(T, hk, hv, d)
-    dims = gdn.dims(hk, hv, d, map=mp, io_dtype=torch.float32)
+    if io == "bf16":
+        q, k, v = (x.to(torch.bfloat16) for x in (q, k, v))
+    dims = gdn.dims(hk, hv, d, map=mp, io_dtype=gi.DTYPES[io])
     flags = gdn.GDN_QK_PRENORMALIZED | gdn.GDN_GATES_PRECOMPUTED
     ro, rS = oracle.delta(F64(q), F64(k), F64(v), F64(g), F64(beta), F64(S0)[0], mp)
 
@@ -132,6 +136,29 @@ def test_varlen_raw_inputs_with_fused_norm(dtype, d, mp, dec):
     # the fused norm against the oracle's norm of the kernel's own core output
     ry = oracle.gated_rmsnorm(F64(core.cpu()), F64(z), F64(w.norm_w), 1e-6)
     assert_lowp(out.cpu(), ry, dtype, "fused gated norm")
+
+
+@pytest.mark.parametrize("lengths", [[64], [1], [200, 0, 63], [129, 65, 1, 300]])
+def test_tensor_core_kernel_matches_cuda_core_kernel(lengths):
+    """The two chunk kernels on the same bf16 inputs (head_dim 128): both
+    within the chunk bounds of the oracle, and of each other."""
+    shape = gi.Shape(2, 8, 128, map=gi.TILED, decay=gi.LOG_RATE, dtype="bf16")
+    w, q, k, v, z, a, b, S0 = _raw_case(900 + len(lengths), shape, lengths)
+    cu = gi.cu_seqlens(lengths)
+    dims = gdn.dims(2, 8, 128, map=gi.TILED, io_dtype=torch.bfloat16)
+    st_tc, st_cc = cuda(S0), cuda(S0)
+    c_tc, o_tc = _run_prefill(dims, cu, q, k, v, a, b, st_tc, 0, dp=w.decay_param,
+                              dt=w.dt_bias, z=cuda(z), nw=cuda(w.norm_w))
+    c_cc, o_cc = _run_prefill(dims, cu, q, k, v, a, b, st_cc, gdn.GDN_PREFILL_CUDA_CORES,
+                              dp=w.decay_param, dt=w.dt_bias, z=cuda(z), nw=cuda(w.norm_w))
+    ro, rS = _oracle_prefill(shape, w, q, k, v, a, b, S0, cu)
+    assert_abs(c_tc.cpu(), ro, CHUNK_OUT_ABS, "tensor-core output")
+    assert_abs(st_tc.cpu(), rS, CHUNK_STATE_ABS, "tensor-core state")
+    assert_abs(c_cc.cpu(), ro, CHUNK_OUT_ABS, "cuda-core output")
+    assert_abs(c_tc.cpu(), F64(c_cc.cpu()), CHUNK_OUT_ABS, "tensor core vs cuda core")
+    ry = oracle.gated_rmsnorm(F64(c_tc.cpu()), F64(z), F64(w.norm_w), 1e-6)
+    assert_lowp(o_tc.cpu(), ry, "bf16", "tensor-core fused norm")
+    assert gdn.gdn_device_error() == 0
 
 
 def test_prefill_reads_strided_conv_output():
