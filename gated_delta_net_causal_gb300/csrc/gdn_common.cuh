@@ -170,6 +170,15 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t smem_addr, uint32_t
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_addr), "r"(rank));
   return out;
 }
+// Asynchronous 4-byte store into another CTA's shared memory that completes
+// 4 transaction bytes on that CTA's mbarrier (both addresses from mapa).
+__device__ __forceinline__ void st_async_cluster_f32(uint32_t remote_addr, float v,
+                                                     uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
+      "r"(__float_as_uint(v)), "r"(remote_bar)
+      : "memory");
+}
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");

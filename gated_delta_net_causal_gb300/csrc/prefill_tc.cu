@@ -55,7 +55,8 @@ constexpr uint32_t OFF_KBF = 0;          // k chunk, bf16 [64][128] SW128 (2 ato
 constexpr uint32_t OFF_QBF = 16384;      // q chunk, bf16 [64][128]
 constexpr uint32_t OFF_KT = 32768;       // fp32 [128 i][64 s] (k transposed)
 constexpr uint32_t OFF_SB = 65536;       // io dtype [32 j][128 i] state copy for Q S0^T
-constexpr uint32_t OFF_TAL = 73728;      // fp32 [64][64] low part of Tm diag(beta)
+constexpr uint32_t OFF_TAL = 73728;      // fp32 [64][64] low part of Tm diag(beta); the next
+                                         // chunk's v lands here (row-major, 4 KB) after (D)
 constexpr uint32_t OFF_DTLL = 90112;     // fp32 [32 j][64 s] low part of (dl invk Dm)^T
 constexpr uint32_t OFF_VT = 98304;       // fp32 [32 j][64 s] (v transposed); later O staging
 constexpr uint32_t OFF_TA = 106496;      // fp32 [64][64] Tm, then hi part of Tm diag(beta)
@@ -63,7 +64,7 @@ constexpr uint32_t OFF_TB = 122880;      // fp32 [64][64] A, then Tm diag(beta G
 constexpr uint32_t OFF_PM = 139264;      // fp32 [64][64]
 constexpr uint32_t OFF_W = 155648;       // fp32 [64][128]
 constexpr uint32_t OFF_SOP = 188416;     // fp32 [32 j][128 i] state operand
-constexpr uint32_t OFF_DT = 204800;      // fp32 [32 j][64 s] Dm^T; the v chunk lands here first
+constexpr uint32_t OFF_DT = 204800;      // fp32 [32 j][64 s] Dm^T; block-inverse scratch in (C)
 constexpr uint32_t OFF_DTL = 212992;     // fp32 [32 j][64 s] hi part of (dl invk Dm)^T
 constexpr uint32_t SMEM_TILES = 221184;
 constexpr uint32_t SMEM_DYN = SMEM_TILES + 1024;
@@ -97,9 +98,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ float sg[kTcC], sbeta[kTcC], sc[kTcC], sgam[kTcC], sdl[kTcC], sinvk[kTcC],
       sinvq[kTcC];
-  __shared__ float snorm[2][kTcC];
+  // per-row partial sums of squares of the output, from every slice of the
+  // head (indexed by cluster rank), double-buffered by chunk parity
+  __shared__ float snorm[2][kTcNSL][kTcC];
   __shared__ uint32_t s_tmem;
-  __shared__ __align__(8) uint64_t bar_tma, bar_gp, bar_uw, bar_sq, bar_od;
+  __shared__ float sinv[kTcC];
+  __shared__ __align__(8) uint64_t bar_k, bar_q, bar_v, bar_gp, bar_uw, bar_sq, bar_od;
+  __shared__ __align__(8) uint64_t bar_norm[2];
 
   constexpr uint32_t kFmt = std::is_same<T, __half>::value ? tc::kF16 : tc::kBF16;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -119,11 +124,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(&bar_tma, 1);
+    mbar_init(&bar_k, 1);
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_v, 1);
     mbar_init(&bar_gp, 1);
     mbar_init(&bar_uw, 1);
     mbar_init(&bar_sq, 1);
     mbar_init(&bar_od, 1);
+    mbar_init(&bar_norm[0], 1);
+    mbar_init(&bar_norm[1], 1);
+    // armed for the first two chunks; each later use is re-armed right after
+    // the previous one is consumed
+    mbar_arrive_expect_tx(&bar_norm[0], (kTcNSL - 1) * kTcC * 4);
+    mbar_arrive_expect_tx(&bar_norm[1], (kTcNSL - 1) * kTcC * 4);
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -144,6 +157,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  // every CTA of the cluster has initialised its barriers before any peer
+  // stores into its shared memory
+  cluster_arrive_release();
+  cluster_wait_acquire();
   const uint32_t tb = s_tmem;
   const uint32_t tq = tb + ((uint32_t)(32 * qd) << 16);  // this warp's TMEM quadrant
 
@@ -155,44 +172,90 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  a_w = smem_u32(sm + OFF_W), a_sop = smem_u32(sm + OFF_SOP),
                  a_dt = smem_u32(sm + OFF_DT), a_dtl = smem_u32(sm + OFF_DTL);
 
+  // TMA issue helpers: each of k, q, v has its own barrier, completing once
+  // per chunk, so the next chunk's tile is requested as soon as the current
+  // one has been consumed
+  auto issue_k = [&](int64_t c) {
+    mbar_arrive_expect_tx(&bar_k, 16384u);
+    tc::tma_load_2d(sm + OFF_KBF, &tm_k, kh * kTcD, (int)c, &bar_k);
+    tc::tma_load_2d(sm + OFF_KBF + 8192, &tm_k, kh * kTcD + 64, (int)c, &bar_k);
+  };
+  auto issue_q = [&](int64_t c) {
+    mbar_arrive_expect_tx(&bar_q, 16384u);
+    tc::tma_load_2d(sm + OFF_QBF, &tm_q, kh * kTcD, (int)c, &bar_q);
+    tc::tma_load_2d(sm + OFF_QBF + 8192, &tm_q, kh * kTcD + 64, (int)c, &bar_q);
+  };
+  auto issue_v = [&](int64_t c) {
+    mbar_arrive_expect_tx(&bar_v, 4096u);
+    tc::tma_load_2d(sm + OFF_TAL, &tm_v, h * kTcD + j0, (int)c, &bar_v);
+  };
+  if (tid == 0 && seq_s < seq_e) {
+    issue_k(seq_s);
+    issue_q(seq_s);
+    issue_v(seq_s);
+  }
+  // raw gate inputs of the next chunk, prefetched into registers (tid < 64)
+  float ga_next = 0.f, gb_next = 0.f;
+  auto load_gates = [&](int64_t c) {
+    ga_next = 0.f;
+    gb_next = 0.f;
+    if (tid < kTcC && c + tid < seq_e) {
+      const int64_t gi = (c + tid) * p.Hv + h;
+      if (pregate) {
+        ga_next = static_cast<const float*>(p.a)[gi];
+        gb_next = static_cast<const float*>(p.b)[gi];
+      } else {
+        ga_next = to_f32(static_cast<const T*>(p.a)[gi]);
+        gb_next = to_f32(static_cast<const T*>(p.b)[gi]);
+      }
+    }
+  };
+  load_gates(seq_s);
+  const float nw_j = fused_norm ? p.norm_w[j0 + (tid & 31)] : 0.f;
+  const float gparam = pregate ? 0.f : p.decay_param[h];
+  const float gdtb = pregate ? 0.f : p.dt_bias[h];
+  const uint32_t my_rank = cluster_ctarank();
+
   int chunk = 0;
   for (int64_t c0 = seq_s; c0 < seq_e; c0 += kTcC, ++chunk) {
     const int L = (int)((seq_e - c0) < kTcC ? (seq_e - c0) : kTcC);
     const uint32_t par = (uint32_t)(chunk & 1);
+    const int64_t c1 = c0 + kTcC;  // next chunk start
+    const bool has_next = c1 < seq_e;
 
-    // ---- (A) TMA: k, q (SW128, MMA layout) and this slice of v; gates
-    if (tid == 0) {
-      mbar_arrive_expect_tx(&bar_tma, 16384u + 16384u + 4096u);
-      tc::tma_load_2d(sm + OFF_KBF, &tm_k, kh * kTcD, (int)c0, &bar_tma);
-      tc::tma_load_2d(sm + OFF_KBF + 8192, &tm_k, kh * kTcD + 64, (int)c0, &bar_tma);
-      tc::tma_load_2d(sm + OFF_QBF, &tm_q, kh * kTcD, (int)c0, &bar_tma);
-      tc::tma_load_2d(sm + OFF_QBF + 8192, &tm_q, kh * kTcD + 64, (int)c0, &bar_tma);
-      tc::tma_load_2d(sm + OFF_DT, &tm_v, h * kTcD + j0, (int)c0, &bar_tma);
-    }
+    // ---- (A) gates of this chunk (from the prefetched raw inputs)
     if (tid < kTcC) {
       float g = 0.f, bt = 0.f;
       if (tid < L) {
-        const int64_t gi = (c0 + tid) * p.Hv + h;
         if (pregate) {
-          g = static_cast<const float*>(p.a)[gi];
-          bt = static_cast<const float*>(p.b)[gi];
+          g = ga_next;
+          bt = gb_next;
         } else {
-          g = gate_g(p.decay, p.decay_param[h], p.dt_bias[h], to_f32(static_cast<const T*>(p.a)[gi]));
-          bt = sigmoid_f(to_f32(static_cast<const T*>(p.b)[gi]));
+          g = gate_g(p.decay, gparam, gdtb, ga_next);
+          bt = sigmoid_f(gb_next);
         }
       }
       sg[tid] = g;
       sbeta[tid] = bt;
     }
+    if (has_next) load_gates(c1);
     __syncthreads();
-    if (tid == 0) {
-      float run = 0.f;
-      for (int t = 0; t < kTcC; ++t) {
-        run += sg[t];
-        sc[t] = run;
+    if (warp < 2) {
+      // inclusive prefix sum of g over the 64 tokens: two warp scans, then the
+      // second half adds the first half's total
+      float v = sg[tid];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
       }
+      sc[tid] = v;
     }
-    tc_wait(&bar_tma, par);
+    __syncthreads();
+    if (warp == 1) sc[tid] += sc[31];
+    tc_wait(&bar_k, par);
+    tc_wait(&bar_q, par);
+    tc_wait(&bar_v, par);
     __syncthreads();
 
     // ---- (B) K K^T and Q K^T on the tensor cores, straight from the TMA tiles
@@ -213,42 +276,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       sgam[tid] = expf(sc[tid]);
       sdl[tid] = tid < L ? expf(sc[L - 1] - sc[tid]) : 0.f;
     }
-    // row norms of k and q (raw bf16 tiles)
-    for (int t = warp; t < kTcC; t += kTcThreads / 32) {
+    // row norms of k and q and the K^T copy, 16 bytes at a time: four threads
+    // per token row, each taking four 8-element chunks of k and of q
+    {
+      const int srow = tid >> 2, part = tid & 3;
       float kk = 0.f, qq = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 4 * lane + e;
-        const float kv = to_f32(*reinterpret_cast<const T*>(sm + OFF_KBF + tc::sw128_offset(t, i, 64, 2)));
-        const float qv = to_f32(*reinterpret_cast<const T*>(sm + OFF_QBF + tc::sw128_offset(t, i, 64, 2)));
-        kk += kv * kv;
-        qq += qv * qv;
+      for (int m = 0; m < 4; ++m) {
+        const int c16 = part + 4 * m;  // 16-byte chunk of the 256-byte row
+        const uint32_t off = (uint32_t)((c16 >> 3) * (64 * 128) + (srow >> 3) * 1024 +
+                                        (srow & 7) * 128 + (((c16 & 7) ^ (srow & 7)) << 4));
+        const uint4 kr = *reinterpret_cast<const uint4*>(sm + OFF_KBF + off);
+        const uint4 qr = *reinterpret_cast<const uint4*>(sm + OFF_QBF + off);
+        const T* kv = reinterpret_cast<const T*>(&kr);
+        const T* qv = reinterpret_cast<const T*>(&qr);
+        const int i0 = 8 * c16;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float kf = to_f32(kv[e]), qf = to_f32(qv[e]);
+          kk = fmaf(kf, kf, kk);
+          qq = fmaf(qf, qf, qq);
+          *f32at(sm, OFF_KT, i0 + e, srow, kTcD) = srow < L ? kf : 0.f;
+        }
       }
-      kk = group_sum<32>(kk);
-      qq = group_sum<32>(qq);
-      if (lane == 0) {
-        const bool live = t < L;
-        sinvk[t] = live ? (prenorm ? 1.f : 1.f / sqrtf(kk + p.l2_eps)) : 0.f;
-        sinvq[t] = live ? (prenorm ? 1.f : 1.f / sqrtf(qq + p.l2_eps)) * p.scale : 0.f;
+      kk += __shfl_xor_sync(0xffffffffu, kk, 1);
+      kk += __shfl_xor_sync(0xffffffffu, kk, 2);
+      qq += __shfl_xor_sync(0xffffffffu, qq, 1);
+      qq += __shfl_xor_sync(0xffffffffu, qq, 2);
+      if (part == 0) {
+        const bool live = srow < L;
+        sinvk[srow] = live ? (prenorm ? 1.f : 1.f / sqrtf(kk + p.l2_eps)) : 0.f;
+        sinvq[srow] = live ? (prenorm ? 1.f : 1.f / sqrtf(qq + p.l2_eps)) * p.scale : 0.f;
       }
-    }
-    // fp32 operand copies (exact: raw 16-bit values): K^T [i][s], V^T [j][s];
-    // rows past the end of the sequence are zero
-    for (int e = tid; e < kTcC * kTcD; e += kTcThreads) {
-      const int s = e / kTcD, i = e - (e / kTcD) * kTcD;
-      const float kv = to_f32(*reinterpret_cast<const T*>(sm + OFF_KBF + tc::sw128_offset(s, i, 64, 2)));
-      *f32at(sm, OFF_KT, i, s, kTcD) = s < L ? kv : 0.f;
-    }
-    for (int e = tid; e < kTcC * kTcNS; e += kTcThreads) {
-      const int s = e / kTcNS, j = e - (e / kTcNS) * kTcNS;
-      const float vv = to_f32(reinterpret_cast<const T*>(sm + OFF_DT)[s * kTcNS + j]);
-      *f32at(sm, OFF_VT, j, s, kTcNS) = s < L ? vv : 0.f;
+      // V^T from the row-major staging copy: 8 values of one token row each
+      const uint4 vr = *reinterpret_cast<const uint4*>(sm + OFF_TAL + (srow * kTcNS + 8 * part) * 2);
+      const T* vv = reinterpret_cast<const T*>(&vr);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        *f32at(sm, OFF_VT, 8 * part + e, srow, kTcNS) = srow < L ? to_f32(vv[e]) : 0.f;
     }
     __syncthreads();
     tc_wait(&bar_gp, par);
     tc::fence_after_sync();
 
-    // ---- (C) A (into TB), PM, and Tm = (I + A)^{-1} (into TA)
+    // ---- (C) A and PM from the tensor-core grams; Tm = (I + A)^{-1}
+    // A and Tm are kept row-major (plain fp32 [64][64]) in the W tile's space,
+    // which is free until (E); block products go through the Dm tiles' space.
+    float* Ap = reinterpret_cast<float*>(sm + OFF_W);
+    float* Tp = reinterpret_cast<float*>(sm + OFF_W + 16384);
+    float* Xp = reinterpret_cast<float*>(sm + OFF_DT);
     {
       float gv[32], pv[32];
       tc::tmem_ld16(tq + TM_G + 32 * hh, *reinterpret_cast<float(*)[16]>(gv));
@@ -259,38 +335,73 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane < 16) {
         const int t = 16 * qd + lane;
         const bool live = t < L;
-        const float ct = sc[t], bt = sbeta[t], ikt = sinvk[t], iqt = sinvq[t];
+        constexpr float kLog2e = 1.4426950408889634f;
+        const float ct = sc[t] * kLog2e, bt = sbeta[t], ikt = sinvk[t], iqt = sinvq[t];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int s = 32 * hh + e;
-          const float dec = expf(ct - sc[s]);
+          const float dec = exp2f(ct - sc[s] * kLog2e);  // e^{c_t - c_s} <= 1 for s <= t
           const float ks = sinvk[s];
-          *f32at(sm, OFF_TB, t, s, kTcC) = (live && s < t) ? bt * dec * gv[e] * ikt * ks : 0.f;
+          Ap[t * kTcC + s] = (live && s < t) ? bt * dec * gv[e] * ikt * ks : 0.f;
           *f32at(sm, OFF_PM, t, s, kTcC) = (live && s <= t) ? tc::tf32_rna(dec * pv[e] * iqt * ks) : 0.f;
-          *f32at(sm, OFF_TA, t, s, kTcC) = (s == t) ? 1.f : 0.f;
         }
       }
     }
-    tc::fence_before_sync();
     __syncthreads();
-    // forward substitution, one row per step:
-    //   Tm[t][s] = -A[t][s] - sum_{s<r<t} A[t][r] Tm[r][s]
-    for (int t = 1; t < L; ++t) {
-      const int s = tid >> 2, part = tid & 3;
-      float acc = 0.f;
-      if (s < t) {
-        for (int r = s + 1 + part; r < t; r += 4)
-          acc = fmaf(*f32at(sm, OFF_TB, t, r, kTcC), *f32at(sm, OFF_TA, r, s, kTcC), acc);
+    if (tid == 0 && has_next) issue_k(c1);  // K K^T, Q K^T done; the K copy is made
+    // diagonal 16x16 blocks: warp b inverts block b by forward substitution,
+    // lane l holding column 16b + l in registers
+    if (warp < 4) {
+      const int b0 = 16 * warp, l = lane & 15;
+      float x[16];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) x[m] = (m == l) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 1; m < 16; ++m) {
+        const float* arow = Ap + (b0 + m) * kTcC + b0;
+        float acc = 0.f;
+#pragma unroll
+        for (int r = 0; r < m; ++r) acc = fmaf(arow[r], x[r], acc);
+        if (m > l) x[m] = -acc;
       }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      if (s < t && part == 0) *f32at(sm, OFF_TA, t, s, kTcC) = -*f32at(sm, OFF_TB, t, s, kTcC) - acc;
+      if (lane < 16) {
+#pragma unroll
+        for (int m = 0; m < 16; ++m) Tp[(b0 + m) * kTcC + b0 + l] = x[m];
+      }
+    }
+    __syncthreads();
+    // off-diagonal blocks, one block diagonal at a time:
+    //   T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
+    for (int d = 1; d < 4; ++d) {
+      const int nblk = 4 - d;
+      for (int e = tid; e < nblk * 256; e += kTcThreads) {
+        const int jb = e >> 8, rr = (e >> 4) & 15, cc = e & 15, ib = jb + d;
+        float acc = 0.f;
+        for (int kb = jb; kb < ib; ++kb) {
+          const float* arow = Ap + (16 * ib + rr) * kTcC + 16 * kb;
+          const float* tcol = Tp + (16 * kb) * kTcC + 16 * jb + cc;
+#pragma unroll
+          for (int m = 0; m < 16; ++m) acc = fmaf(arow[m], tcol[m * kTcC], acc);
+        }
+        Xp[e] = acc;
+      }
+      __syncthreads();
+      for (int e = tid; e < nblk * 256; e += kTcThreads) {
+        const int jb = e >> 8, rr = (e >> 4) & 15, cc = e & 15, ib = jb + d;
+        const float* trow = Tp + (16 * ib + rr) * kTcC + 16 * ib;
+        const float* xcol = Xp + (jb << 8) + cc;
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc = (m <= rr) ? fmaf(trow[m], xcol[m << 4], acc) : acc;
+        Tp[(16 * ib + rr) * kTcC + 16 * jb + cc] = -acc;
+      }
       __syncthreads();
     }
-    // TA/TAL = hi/lo of Tm diag(beta); TB = Tm diag(beta G invk)
+    // TA/TAL = hi/lo of Tm diag(beta); TB = Tm diag(beta G invk); zero above
+    // the diagonal
     for (int e = tid; e < kTcC * kTcC; e += kTcThreads) {
       const int t = e / kTcC, s = e - (e / kTcC) * kTcC;
-      const float tv = *f32at(sm, OFF_TA, t, s, kTcC);
+      const float tv = s <= t ? Tp[e] : 0.f;
       const float ta = tv * sbeta[s];
       const float hi = tc::tf32_rna(ta);
       *f32at(sm, OFF_TA, t, s, kTcC) = hi;
@@ -321,6 +432,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     tc_wait(&bar_uw, par);
     tc::fence_after_sync();
+    if (tid == 0 && has_next) issue_v(c1);  // the low part of Tm diag(beta) has been read
 
     // ---- (E) W to shared memory as the A operand of W S0^T
     {
@@ -356,6 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     tc_wait(&bar_sq, par);
     tc::fence_after_sync();
+    if (tid == 0 && has_next) issue_q(c1);  // Q S0^T done
 
     // ---- (G) Dm = U - W S0^T (transposed, twice scaled); inter-chunk output
     float oi[16];
@@ -402,6 +515,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      ids, true);
       tc::mma_commit(&bar_od);
     }
+    // z for this thread's output elements (row e / 32, column tid % 32), loaded
+    // while the last MMAs of the chunk run
+    T zpre[kTcC * kTcNS / kTcThreads];
+    if (fused_norm) {
+      const T* zg = static_cast<const T*>(p.z);
+#pragma unroll
+      for (int m = 0; m < kTcC * kTcNS / kTcThreads; ++m) {
+        const int e = tid + kTcThreads * m;
+        const int t = e / kTcNS;
+        zpre[m] = t < L ? zg[((c0 + t) * p.Hv + h) * kTcD + j0 + (e % kTcNS)] : T();
+      }
+    }
     tc_wait(&bar_od, par);
     tc::fence_after_sync();
 
@@ -439,24 +564,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (fused_norm) {
         const int buf = chunk & 1;
+        // partial sums of squares of this slice's 32 columns, per row, sent to
+        // every CTA of the cluster (own slot written locally); each CTA waits
+        // for its three peers' 64 x 4 bytes on its own mbarrier
         for (int t = warp; t < kTcC; t += kTcThreads / 32) {
           float v = ostage[t * kTcNS + lane];
           v = group_sum<32>(v * v);
-          if (lane == 0) snorm[buf][t] = v;
+          if (lane < kTcNSL) {
+            const uint32_t slot = smem_u32(&snorm[buf][my_rank][t]);
+            if ((uint32_t)lane == my_rank) {
+              snorm[buf][my_rank][t] = v;
+            } else {
+              st_async_cluster_f32(map_shared_rank(slot, lane), v,
+                                   map_shared_rank(smem_u32(&bar_norm[buf]), lane));
+            }
+          }
         }
-        cluster_arrive_release();
-        cluster_wait_acquire();
-        const T* zg = static_cast<const T*>(p.z);
-        T* og = static_cast<T*>(p.out);
-        for (int e = tid; e < L * kTcNS; e += kTcThreads) {
-          const int t = e / kTcNS, j = e - (e / kTcNS) * kTcNS;
-          const uint32_t addr = smem_u32(&snorm[buf][t]);
+        tc_wait(&bar_norm[buf], (uint32_t)((chunk >> 1) & 1));
+        __syncthreads();
+        if (tid < kTcC) {
           float tot = 0.f;
 #pragma unroll
-          for (int r = 0; r < kTcNSL; ++r) tot += ld_shared_cluster_f32(map_shared_rank(addr, r));
-          const float inv = 1.f / sqrtf(tot / (float)kTcD + p.rms_eps);
-          const int64_t oi2 = ((c0 + t) * p.Hv + h) * kTcD + j0 + j;
-          og[oi2] = from_f32<T>(ostage[e] * inv * p.norm_w[j0 + j] * silu_f(to_f32(zg[oi2])));
+          for (int r = 0; r < kTcNSL; ++r) tot += snorm[buf][r][tid];
+          sinv[tid] = 1.f / sqrtf(tot / (float)kTcD + p.rms_eps);
+        }
+        __syncthreads();
+        if (tid == 0) mbar_arrive_expect_tx(&bar_norm[buf], (kTcNSL - 1) * kTcC * 4);
+        T* og = static_cast<T*>(p.out);
+#pragma unroll
+        for (int m = 0; m < kTcC * kTcNS / kTcThreads; ++m) {
+          const int e = tid + kTcThreads * m;
+          const int t = e / kTcNS;
+          if (t < L) {
+            const int64_t oi2 = ((c0 + t) * p.Hv + h) * kTcD + j0 + (e % kTcNS);
+            og[oi2] = from_f32<T>(ostage[e] * sinv[t] * nw_j * silu_f(to_f32(zpre[m])));
+          }
         }
       }
     }
