@@ -9,7 +9,9 @@ place, and the gated RMSNorm epilogue):
 Metric: state GB/s = 2 * B * Hv * D^2 * 4 bytes / step time.
 
 A second block measures chunked prefill (one sequence of T=4096, Hk=16, Hv=32,
-D=128, Grouped, bf16 raw q/k/v/z/a/b, fused gated RMSNorm) in tokens/s.
+D=128, Grouped, bf16 raw q/k/v/z/a/b, fused gated RMSNorm) in tokens/s, and a
+third the whole path on the varlen workload (conv update over 8 packed
+sequences, chunked prefill with the fused norm, 16 decode steps) in tokens/s.
 
 Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on
 the launching stream; a 512 MiB buffer is overwritten between timed steps so
@@ -196,12 +198,12 @@ def run_gpu(args, ws, rank, local):
     other_bytes = (B * C * 2 + 2 * B * Hv * 2 + B * Hv * D * 2 + 2 * B * C * 3 * 2
                    + B * Hv * D * 2 + C * 4 * 2 + 3 * Hv * 4 + D * 4)
 
+    clocks = ClockSampler(local)
+    clocks.start()
     for i in range(args.warmup):
         _decode_call(gdn, d, dev, steps[i % 16], state, cstate, out)
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local)
-    clocks.start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     if ws > 1:
@@ -216,7 +218,6 @@ def run_gpu(args, ws, rank, local):
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
-    clk = clocks.stop()
     times = [a.elapsed_time(b) * 1e-3 for a, b in ev]
     t_step = sum(times) / len(times)
     t_step = _barrier_max(t_step, ws)
@@ -244,8 +245,12 @@ def run_gpu(args, ws, rank, local):
         e2e_times.append(time.perf_counter() - t0)
     t_e2e = _barrier_max(statistics.mean(e2e_times), ws)
 
-    # chunked prefill block
+    # chunked prefill block and the varlen whole-path block
     prefill = run_prefill(args, peaks, ws) if not args.no_prefill else None
+    varlen = run_varlen(args, ws) if not args.no_prefill else None
+    clk = clocks.stop()
+    if clk is not None:
+        clk["window"] = "decode warm-up through the prefill blocks (brackets the timed steps)"
 
     if rank != 0:
         return None
@@ -285,6 +290,8 @@ def run_gpu(args, ws, rank, local):
     }
     if prefill is not None:
         line["prefill"] = prefill
+    if varlen is not None:
+        line["varlen_path"] = varlen
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = cpu_baseline_decode(seconds=args.cpu_seconds)
     return line
@@ -335,10 +342,74 @@ def run_prefill(args, peaks, ws):
             "roofline": {"bound": "tensor", "achieved": round(flops / t / 1e12, 3),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(flops / t / 1e12 / peaks["bf16_tflops"], 5),
-                         "traffic": None, "peak_source": peaks["source"],
+                         "traffic": _profile_traffic("prefill_tc_t4096.txt",
+                                                     _kernel_hash("prefill_tc.cu", "tc_common.cuh",
+                                                                  "gdn_common.cuh")),
+                         "traffic_unit": "bytes per launch",
+                         "peak_source": peaks["source"],
                          "algorithmic_flops_per_call": flops,
+                         "algorithmic_bytes_per_call": byts,
                          "hbm_frac": round(byts / t / 1e9 / peaks["hbm_gbs"], 4),
-                         "kernel": "prefill_cc_kernel<bf16,128,32>"}}
+                         "kernel": "prefill_tc_kernel<bf16>"}}
+
+
+def run_varlen(args, ws):
+    """The whole hot path on the varlen workload: conv update over 8 packed
+    sequences (lengths U[512,8192] as drawn, 34,482 tokens), chunked prefill
+    with the fused gated norm continuing from their states, then 16 batched
+    decode steps. Inputs are drawn on the device (same shapes and laws as the
+    parity test's host-drawn ones)."""
+    import gated_delta_net_causal_gb300 as gdn
+    lengths = gi.varlen_lengths(gi.SEED_BASE + 5, 8, 512, 8192)
+    N, T = len(lengths), int(sum(lengths))
+    Hk, Hv, D = 16, 64, 128
+    C = (2 * Hk + Hv) * D
+    gen = torch.Generator(device="cuda").manual_seed(gi.SEED_BASE + 5)
+    bf = torch.bfloat16
+
+    def rn(*shape, std=1.0, dtype=bf):
+        return (torch.randn(shape, device="cuda", generator=gen) * std).to(dtype)
+    x, a, b, z = rn(T, C), rn(T, Hv), rn(T, Hv), rn(T, Hv, D)
+    dec = [(rn(N, C), rn(N, Hv), rn(N, Hv), rn(N, Hv, D)) for _ in range(16)]
+    conv_w = rn(C, 4, std=0.16)
+    dp = torch.log(torch.rand(Hv, device="cuda", generator=gen) * 15 + 1)
+    dt = torch.rand(Hv, device="cuda", generator=gen) - 0.5
+    nw = (0.82 + 0.013 * torch.arange(D, device="cuda")).float()
+    cs0, s0 = rn(N, C, 3, std=0.1), rn(N, Hv, D, D, std=0.02, dtype=torch.float32)
+    cu = gi.cu_seqlens(lengths).cuda()
+    d = gdn.dims(Hk, Hv, D, map=gdn.GDN_MAP_TILED, decay=gdn.GDN_DECAY_LOG_RATE, io_dtype=bf)
+    y = torch.empty_like(x)
+    out = torch.empty((T, Hv, D), device="cuda", dtype=bf)
+    dout = torch.empty((N, Hv, D), device="cuda", dtype=bf)
+    cs, st = cs0.clone(), s0.clone()
+    qk = Hk * D
+    stream = torch.cuda.current_stream()
+
+    def path():
+        gdn.gdn_conv_update(d, cu, x, conv_w, cs, y)
+        gdn.gdn_prefill_chunked(d, cu, y[:, :qk], y[:, qk:2 * qk], y[:, 2 * qk:], a, b, dp, dt,
+                                st, z=z, norm_w=nw, out=out)
+        for (xd, ad, bd, zd) in dec:
+            gdn.gdn_decode_step(d, xd, ad, bd, dp, dt, conv_w, cs, st, z=zd, norm_w=nw, out=dout)
+
+    path()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(3):
+        cs.copy_(cs0)
+        st.copy_(s0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        path()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e-3)
+    t = _barrier_max(statistics.mean(times), ws)
+    tokens = T + 16 * N
+    return {"workload": "varlen: 8 sequences (34,482 tokens) conv update + chunked prefill with "
+                        "fused norm + 16 decode steps, Hk=16 Hv=64 D=128, Tiled, bf16",
+            "value": round(ws * tokens / t, 1), "unit": "tokens/s", "ms_per_pass": round(t * 1e3, 4),
+            "launches_per_pass": 2 + 1 + 16}
 
 
 # --------------------------------------------------------------- CPU oracle arm

@@ -5,9 +5,10 @@
 //
 // Two launches on the caller's stream:
 //  1. conv_fwd_kernel: y for every token. A thread owns 16 bytes of channels
-//     (8 for f16/bf16, 4 for f32) and 8 consecutive tokens; it loads the 11
-//     input rows its window needs once and reads the OLD conv state only for
-//     the (at most three) taps that fall before its sequence's first token.
+//     (8 for f16/bf16, 4 for f32) and 4 consecutive tokens; it loads the 7
+//     input rows its window needs once (16-byte vectors) and reads the OLD conv
+//     state only for the (at most three) taps that fall before its sequence's
+//     first token.
 //  2. conv_state_kernel: the new conv state (last three raw inputs of each
 //     sequence). Running it after (1) in stream order is what makes the in-place
 //     state update race-free: (1) never sees a half-updated state.
@@ -16,13 +17,27 @@
 
 namespace gdn {
 
-constexpr int kConvTPT = 8;    // tokens per thread
+constexpr int kConvTPT = 4;    // tokens per thread
 constexpr int kConvCV = 32;    // channel vectors per block
 constexpr int kConvTG = 8;     // token groups per block
 
 __device__ __forceinline__ int64_t clamp_cu(const int32_t* cu, int n, int64_t T) {
   int64_t v = cu[n];
   return v < 0 ? 0 : (v > T ? T : v);
+}
+
+// silu with the fast exponential and reciprocal: the result is rounded to the
+// 16-bit activation type (or compared at fp32 tolerance), far above their
+// ~2^-21 relative error.
+__device__ __forceinline__ float silu_fast(float x) {
+  return x * __frcp_rn(1.f + __expf(-x));
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& raw, float (&out)[16 / sizeof(T)]) {
+  const T* v = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+  for (int e = 0; e < (int)(16 / sizeof(T)); ++e) out[e] = to_f32(v[e]);
 }
 
 template <typename T>
@@ -37,32 +52,22 @@ __global__ void __launch_bounds__(kConvCV* kConvTG) conv_fwd_kernel(const ConvAr
   const T* st = static_cast<const T*>(p.conv_state);
   T* y = static_cast<T*>(p.y);
 
-  // weights of these VEC channels, [VEC][4]
-  float wf[VEC][4];
-  {
-    const T* wp = static_cast<const T*>(p.conv_w) + c0 * 4;
-#pragma unroll
-    for (int e = 0; e < VEC; ++e)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) wf[e][j] = to_f32(wp[e * 4 + j]);
-  }
-
-  // window rows tau = t0-3 .. t0+TPT-1
+  // window rows tau = t0-3 .. t0+TPT-1, kept packed until used
   constexpr int NR = kConvTPT + 3;
-  float xv[NR][VEC];
+  uint4 xr[NR];
 #pragma unroll
   for (int u = 0; u < NR; ++u) {
     const int64_t tau = t0 - 3 + u;
-    if (tau >= 0 && tau < T_) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(x + tau * C + c0);
-      const T* rv = reinterpret_cast<const T*>(&raw);
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) xv[u][e] = to_f32(rv[e]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) xv[u][e] = 0.f;
-    }
+    xr[u] = (tau >= 0 && tau < T_) ? *reinterpret_cast<const uint4*>(x + tau * C + c0)
+                                    : make_uint4(0, 0, 0, 0);
   }
+  // weights of these VEC channels, [VEC][4] contiguous: VEC*4 elements
+  constexpr int WV = VEC * 4 * (int)sizeof(T) / 16;  // 16-byte vectors of weights
+  uint4 wr[WV];
+  const uint4* wp = reinterpret_cast<const uint4*>(static_cast<const T*>(p.conv_w) + c0 * 4);
+#pragma unroll
+  for (int i = 0; i < WV; ++i) wr[i] = wp[i];
+  const T* wv = reinterpret_cast<const T*>(wr);
 
   // sequence owning t0: the last n with cu[n] <= t0
   int lo = 0, hi = p.N - 1;
@@ -86,21 +91,23 @@ __global__ void __launch_bounds__(kConvCV* kConvTG) conv_fwd_kernel(const ConvAr
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int64_t tau = t + j - 3;
+      float xv[VEC];
       if (tau >= s) {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) acc[e] += wf[e][j] * xv[jj + j][e];
+        unpack16<T>(xr[jj + j], xv);
       } else {
         // tap before the sequence start: old conv state slot 3 + (tau - s)
         const int slot = 3 + (int)(tau - s);
         const T* sp = st + ((int64_t)n * C + c0) * 3 + slot;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) acc[e] += wf[e][j] * to_f32(sp[e * 3]);
+        for (int e = 0; e < VEC; ++e) xv[e] = to_f32(sp[e * 3]);
       }
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] = fmaf(to_f32(wv[e * 4 + j]), xv[e], acc[e]);
     }
     uint4 packed;
     T* pv = reinterpret_cast<T*>(&packed);
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) pv[e] = from_f32<T>(silu_f(acc[e]));
+    for (int e = 0; e < VEC; ++e) pv[e] = from_f32<T>(silu_fast(acc[e]));
     *reinterpret_cast<uint4*>(y + t * C + c0) = packed;
   }
 }
