@@ -310,12 +310,13 @@ def run_prefill(args, peaks, ws):
     s0 = wl["state"].cuda()
     state = s0.clone()
     out = torch.empty((T, 32, 128), device="cuda", dtype=torch.bfloat16)
+    wsb = torch.empty(gdn.gdn_prefill_workspace_size(d, 1, T), device="cuda", dtype=torch.uint8)
     flush = torch.empty(512 * 1024 * 1024 // 4, device="cuda", dtype=torch.float32)
     stream = torch.cuda.current_stream()
 
     def call():
         gdn.gdn_prefill_chunked(d, cu, q, k, v, a, b, dp, dt, state, core_out=None, z=z,
-                                norm_w=nw, out=out)
+                                norm_w=nw, out=out, workspace=wsb)
 
     for _ in range(3):
         state.copy_(s0)
@@ -338,19 +339,20 @@ def run_prefill(args, peaks, ws):
     flops = flop_per_token * T
     byts = T * (2 * Hk * D + 2 * Hv * D) * 2 + T * Hv * D * 2 + 2 * Hv * D * D * 4 + 4 * T * Hv * 2
     return {"workload": PREFILL_WORKLOAD, "value": round(ws * T / t, 1), "unit": "tokens/s",
-            "ms_per_call": round(t * 1e3, 4), "calls": n,
+            "ms_per_call": round(t * 1e3, 4), "calls": n, "launches_per_call": 3,
             "roofline": {"bound": "tensor", "achieved": round(flops / t / 1e12, 3),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(flops / t / 1e12 / peaks["bf16_tflops"], 5),
-                         "traffic": _profile_traffic("prefill_tc_t4096.txt",
-                                                     _kernel_hash("prefill_tc.cu", "tc_common.cuh",
+                         "traffic": _profile_traffic("prefill_cp_t4096.txt",
+                                                     _kernel_hash("prefill_cp.cu", "tc_common.cuh",
                                                                   "gdn_common.cuh")),
-                         "traffic_unit": "bytes per launch",
+                         "traffic_unit": "bytes per call (all three launches)",
                          "peak_source": peaks["source"],
                          "algorithmic_flops_per_call": flops,
                          "algorithmic_bytes_per_call": byts,
                          "hbm_frac": round(byts / t / 1e9 / peaks["hbm_gbs"], 4),
-                         "kernel": "prefill_tc_kernel<bf16>"}}
+                         "timed": "the whole call (chunk index, prep, carry launches)",
+                         "kernel": "cp_prep_kernel + cp_chain_kernel"}}
 
 
 def run_varlen(args, ws):
@@ -383,12 +385,13 @@ def run_varlen(args, ws):
     dout = torch.empty((N, Hv, D), device="cuda", dtype=bf)
     cs, st = cs0.clone(), s0.clone()
     qk = Hk * D
+    wsb = torch.empty(gdn.gdn_prefill_workspace_size(d, N, T), device="cuda", dtype=torch.uint8)
     stream = torch.cuda.current_stream()
 
     def path():
         gdn.gdn_conv_update(d, cu, x, conv_w, cs, y)
         gdn.gdn_prefill_chunked(d, cu, y[:, :qk], y[:, qk:2 * qk], y[:, 2 * qk:], a, b, dp, dt,
-                                st, z=z, norm_w=nw, out=out)
+                                st, z=z, norm_w=nw, out=out, workspace=wsb)
         for (xd, ad, bd, zd) in dec:
             gdn.gdn_decode_step(d, xd, ad, bd, dp, dt, conv_w, cs, st, z=zd, norm_w=nw, out=dout)
 
@@ -409,7 +412,7 @@ def run_varlen(args, ws):
     return {"workload": "varlen: 8 sequences (34,482 tokens) conv update + chunked prefill with "
                         "fused norm + 16 decode steps, Hk=16 Hv=64 D=128, Tiled, bf16",
             "value": round(ws * tokens / t, 1), "unit": "tokens/s", "ms_per_pass": round(t * 1e3, 4),
-            "launches_per_pass": 2 + 1 + 16}
+            "launches_per_pass": 2 + 3 + 16}
 
 
 # --------------------------------------------------------------- CPU oracle arm

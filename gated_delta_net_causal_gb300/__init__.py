@@ -75,7 +75,9 @@ def library() -> ctypes.CDLL:
         L.gdn_decode_step.argtypes = [pd, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.gdn_prefill_chunked.restype = ctypes.c_int
         L.gdn_prefill_chunked.argtypes = [pd, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, vp, vp,
-                                          vp, i32, vp, vp, vp, vp, vp, vp]
+                                          vp, i32, vp, vp, vp, vp, vp, vp, i64, vp]
+        L.gdn_prefill_workspace_size.restype = ctypes.c_int
+        L.gdn_prefill_workspace_size.argtypes = [pd, i32, i64, i32, ctypes.POINTER(i64)]
         L.gdn_gated_rmsnorm.restype = ctypes.c_int
         L.gdn_gated_rmsnorm.argtypes = [pd, i64, vp, vp, vp, vp, vp]
         L.gdn_device_error.restype = ctypes.c_int
@@ -159,24 +161,55 @@ def _base_ptr(t: torch.Tensor, name: str, dtype) -> int:
     return t.data_ptr()
 
 
+def gdn_prefill_workspace_size(d: GdnDims, num_seqs: int, total_tokens: int,
+                               flags: int = 0) -> int:
+    n = ctypes.c_int64(0)
+    _check(library().gdn_prefill_workspace_size(ctypes.byref(d), int(num_seqs), int(total_tokens),
+                                                int(flags), ctypes.byref(n)),
+           "gdn_prefill_workspace_size")
+    return n.value
+
+
 def gdn_prefill_chunked(d: GdnDims, cu_seqlens, q, k, v, a, b, decay_param, dt_bias, state,
                         core_out=None, z=None, norm_w=None, out=None, flags: int = 0,
-                        stream=None):
+                        workspace="auto", stream=None):
     """q, k: [T][Hk*D] (or views with a token stride, e.g. column slices of the
     conv output); v: [T][Hv*D] likewise. With GDN_GATES_PRECOMPUTED a and b are
-    fp32 g and beta."""
+    fp32 g and beta.
+
+    workspace: "auto" allocates the scratch the library asks for (a torch
+    CUDA byte tensor, only when a workspace path applies); None passes no
+    workspace (the single-pass kernels); or a CUDA uint8 tensor of at least
+    gdn_prefill_workspace_size bytes."""
     io = _io(d)
     f32 = torch.float32
     gate_dt = f32 if (flags & GDN_GATES_PRECOMPUTED) else io
     total = q.shape[0]
+    n = cu_seqlens.numel() - 1
+    ws_ptr, ws_bytes = None, 0
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto', None or a CUDA tensor")
+        need = gdn_prefill_workspace_size(d, n, total, flags)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            if isinstance(stream, torch.cuda.Stream):
+                # freed when this call returns: keep it from being reused
+                # before the kernels on that stream are done with it
+                workspace.record_stream(stream)
+        else:
+            workspace = None
+    if workspace is not None:
+        ws_ptr = _ptr(workspace, "workspace", torch.uint8)
+        ws_bytes = workspace.numel()
     _check(library().gdn_prefill_chunked(
-        ctypes.byref(d), cu_seqlens.numel() - 1, _ptr(cu_seqlens, "cu_seqlens", torch.int32),
+        ctypes.byref(d), n, _ptr(cu_seqlens, "cu_seqlens", torch.int32),
         total, _base_ptr(q, "q", io), _token_stride(q, "q"), _base_ptr(k, "k", io),
         _token_stride(k, "k"), _base_ptr(v, "v", io), _token_stride(v, "v"),
         _ptr(a, "a", gate_dt), _ptr(b, "b", gate_dt), _ptr(decay_param, "decay_param", f32),
         _ptr(dt_bias, "dt_bias", f32), int(flags), _ptr(state, "state", f32),
         _ptr(core_out, "core_out", f32), _ptr(z, "z", io), _ptr(norm_w, "norm_w", f32),
-        _ptr(out, "out", io), _stream(stream)), "gdn_prefill_chunked")
+        _ptr(out, "out", io), ws_ptr, ws_bytes, _stream(stream)), "gdn_prefill_chunked")
     return core_out, out
 
 
@@ -205,7 +238,7 @@ def gdn_version() -> int:
 
 
 __all__ = ["GdnDims", "GdnError", "dims", "library", "status_string", "gdn_conv_update",
-           "gdn_decode_step", "gdn_prefill_chunked", "gdn_gated_rmsnorm", "gdn_device_error",
+           "gdn_decode_step", "gdn_prefill_chunked", "gdn_prefill_workspace_size", "gdn_gated_rmsnorm", "gdn_device_error",
            "gdn_qkv_features", "gdn_version", "GDN_MAP_GROUPED", "GDN_MAP_TILED",
            "GDN_DECAY_LOG_RATE", "GDN_DECAY_NEGATIVE_RATE", "GDN_F16", "GDN_BF16", "GDN_F32",
            "GDN_QK_PRENORMALIZED", "GDN_GATES_PRECOMPUTED", "GDN_PREFILL_CUDA_CORES", "LIB_PATH"]

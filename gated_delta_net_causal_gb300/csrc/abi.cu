@@ -82,7 +82,7 @@ const char* gdn_status_string(int32_t status) {
   }
 }
 
-int32_t gdn_version(void) { return 100; }
+int32_t gdn_version(void) { return 200; }
 
 int64_t gdn_qkv_features(const gdn_dims* dims) {
   if (check_dims(dims) != GDN_OK) return -1;
@@ -204,7 +204,7 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int
                                const void* a, const void* b, const float* decay_param,
                                const float* dt_bias, int32_t flags, float* state,
                                float* core_out, const void* z, const float* norm_w, void* out,
-                               void* stream) {
+                               void* workspace, int64_t workspace_bytes, void* stream) {
   gdn_status st = check_dims(dims);
   if (st != GDN_OK) return st;
   if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
@@ -256,6 +256,22 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int
     if (overlap(rs, in) || overlap(ro, in) || overlap(ry, in)) return GDN_ERR_ALIAS;
   }
   if (overlap(rs, ro) || overlap(rs, ry) || overlap(ro, ry)) return GDN_ERR_ALIAS;
+  int64_t ws_need = 0;
+  st = gdn_prefill_workspace_size(dims, num_seqs, total_tokens, flags, &ws_need);
+  if (st != GDN_OK) return st;
+  const bool use_ws = workspace != nullptr && ws_need > 0 && total_tokens > 0;
+  if (use_ws) {
+    if (workspace_bytes < ws_need) return GDN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGN;
+    const Range rw = range_of(workspace, ws_need);
+    for (const Range& in : inputs)
+      if (overlap(rw, in)) return GDN_ERR_ALIAS;
+    if (overlap(rw, rs) || overlap(rw, ro) || overlap(rw, ry) ||
+        overlap(rw, range_of(decay_param, pregate ? 0 : Hv * 4)) ||
+        overlap(rw, range_of(dt_bias, pregate ? 0 : Hv * 4)) ||
+        overlap(rw, range_of(norm_w, z ? D * 4 : 0)))
+      return GDN_ERR_ALIAS;
+  }
   gdn::PrefillArgs p{};
   p.cu_seqlens = cu_seqlens;
   p.N = num_seqs;
@@ -284,8 +300,34 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int
   p.l2_eps = dims->l2_eps;
   p.rms_eps = dims->rms_eps;
   p.scale = 1.0f / sqrtf((float)D);
+  if (use_ws && gdn::prefill_cp_supported(p, dims->io_dtype, dims->head_dim))
+    return cuda_status(gdn::launch_prefill_cp(p, workspace, static_cast<cudaStream_t>(stream)));
   return cuda_status(gdn::launch_prefill(p, dims->io_dtype, dims->head_dim,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
+                                      int64_t total_tokens, int32_t flags, int64_t* bytes) {
+  if (bytes == nullptr) return GDN_ERR_INVALID_ARG;
+  *bytes = 0;
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
+  if (num_seqs > kMaxGridY) return GDN_ERR_EXTENT;
+  if ((flags & ~(GDN_QK_PRENORMALIZED | GDN_GATES_PRECOMPUTED | GDN_PREFILL_CUDA_CORES)) != 0)
+    return GDN_ERR_INVALID_ARG;
+  if (dims->head_dim != 128 || dims->io_dtype != GDN_BF16 || (flags & GDN_PREFILL_CUDA_CORES) ||
+      num_seqs == 0 || total_tokens == 0)
+    return GDN_OK;
+  // (T + 63 N) / 64 chunk slots of 25 KB per V head and 16 KB per K head,
+  // plus the chunk index
+  int64_t tmp = 0;
+  if (!mul_ok(total_tokens + 63 * (int64_t)num_seqs,
+              (int64_t)dims->n_v_heads * 400 + (int64_t)dims->n_k_heads * 256 + 400, &tmp))
+    return GDN_ERR_EXTENT;
+  *bytes = gdn::prefill_cp_workspace_bytes(num_seqs, total_tokens, dims->n_k_heads,
+                                           dims->n_v_heads);
+  return GDN_OK;
 }
 
 gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, int64_t rows, const float* o, const void* z,
@@ -320,7 +362,8 @@ gdn_status gdn_device_error(int32_t* status, int32_t clear) {
   *status = GDN_OK;
   cudaError_t (*readers[])(int32_t*, bool) = {gdn::read_error_decode, gdn::read_error_conv,
                                                gdn::read_error_rmsnorm, gdn::read_error_prefill,
-                                               gdn::read_error_prefill_tc};
+                                               gdn::read_error_prefill_tc,
+                                               gdn::read_error_prefill_cp};
   for (auto rd : readers) {
     int32_t v = 0;
     if (rd(&v, clear != 0) != cudaSuccess) return GDN_ERR_CUDA;

@@ -80,6 +80,10 @@ cudaError_t launch_prefill(const PrefillArgs& p, int32_t dtype, int32_t D, cudaS
 // tensor-core chunked prefill (head_dim 128, f16/bf16 activations)
 bool prefill_tc_supported(const PrefillArgs& p, int32_t dtype, int32_t D);
 cudaError_t launch_prefill_tc(const PrefillArgs& p, int32_t dtype, cudaStream_t stream);
+// chunk-parallel tensor-core prefill (head_dim 128, bf16) over a workspace
+int64_t prefill_cp_workspace_bytes(int32_t N, int64_t T, int32_t Hk, int32_t Hv);
+bool prefill_cp_supported(const PrefillArgs& p, int32_t dtype, int32_t D);
+cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_t stream);
 
 // Device error words, one per kernel translation unit.
 cudaError_t read_error_decode(int32_t* status, bool clear);
@@ -87,6 +91,7 @@ cudaError_t read_error_conv(int32_t* status, bool clear);
 cudaError_t read_error_rmsnorm(int32_t* status, bool clear);
 cudaError_t read_error_prefill(int32_t* status, bool clear);
 cudaError_t read_error_prefill_tc(int32_t* status, bool clear);
+cudaError_t read_error_prefill_cp(int32_t* status, bool clear);
 
 }  // namespace gdn
 

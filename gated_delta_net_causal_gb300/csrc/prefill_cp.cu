@@ -1,0 +1,1043 @@
+// Chunk-parallel prefill on the 5th-generation tensor cores: head_dim 128,
+// bf16 activations, chunk 64, three launches over a caller-provided
+// workspace.
+//
+// The chunk algebra is the one of the single-pass kernel (the recurrence of
+// ferrox-core gdn.rs summed chunk-wise; the stages of ferrum-kernels
+// gated_delta_attention_tests.rs `run_chunked_core`), split by what depends on
+// the state. Within a chunk of L tokens from state S (rows j = value, columns
+// i = key), with c the chunk-local cumulative decay, G_t = e^{c_t}, raw k, q
+// and their l2 scales rk_t, rq_t (rq includes 1/sqrt(D)):
+//
+//   state-free, every chunk at once (cp_prep_kernel, one CTA per chunk and
+//   K head, looping over the V heads that read it):
+//     A   = beta_t e^{c_t-c_s} rk_t rk_s (k_t . k_s)            (s < t)
+//     Tb  = (I + A)^{-1} diag(beta)                              -> hi + lo bf16
+//     P   = e^{c_t-c_s} rq_t rk_s (q_t . k_s)                    (s <= t) -> bf16
+//     ak_t = G_t rk_t,  dk_t = e^{c_{L-1}-c_t} rk_t,  gq_t = G_t rq_t,  G_{L-1}
+//   the carry, one CTA per (V head, sequence), chunk after chunk
+//   (cp_chain_kernel; the state lives in TMEM as an fp32 accumulator):
+//     KS^T = S K^T                  R^T[j][s] = v_s[j] - ak_s KS^T[j][s]
+//     Dm^T = R^T Tb^T               (the chunk's delta-rule corrections d_t)
+//     S    = G_{L-1} S + (Dm diag(dk))^T K
+//     O^T  = S Q^T diag(gq) + Dm^T P^T, then the gated RMSNorm over j.
+//
+// Every product that carries the state forward (S K^T, R Tb^T, Dm^T K) keeps
+// fp32 accuracy on bf16 tensor cores by splitting the fp32 factor as
+// x = hi + lo (two bf16 values, about 16 significant bits together): S and
+// Dm' are split, raw k is exact in bf16, and R Tb^T uses hi*hi + hi*lo +
+// lo*hi. The two output products (S Q^T, Dm P^T) use the hi parts only.
+//
+// Because the carry CTA owns all 128 value rows of its head, the gated
+// RMSNorm of each output row is a reduction inside the CTA: no cluster.
+#include <cuda.h>
+#include <string.h>
+
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+#include "tc_common.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kC = 64;   // chunk
+constexpr int kD = 128;  // head_dim
+constexpr int kPrepThreads = 256;
+constexpr int kChainThreads = 384;  // warps 0-3: carry, warps 4-11: output
+constexpr int kAStride = kC + 1;    // padded row pitch of the fp32 A matrix
+
+// ---------------------------------------------------------------- workspace
+
+struct CpWork {
+  int32_t* cs;         // [N+1] first chunk slot of each sequence
+  __nv_bfloat16* tw;   // [3][G*Hv*64][64]: Tb hi, Tb lo, P (row-major per slot)
+  __nv_bfloat16* kt;   // [G*Hk*128][64]: raw k transposed, rows t >= L zero
+  float* vec;          // [G*Hv][4][64]: ak, dk, gq, {G_{L-1}, 0...}
+  int64_t G;           // chunk slots
+};
+
+struct CpLayout {
+  int64_t G;
+  size_t off_tm, off_kt, off_vec, total;
+};
+
+CpLayout cp_layout(int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
+  CpLayout l{};
+  // sum over sequences of ceil(len/64) <= (T + 63 N) / 64
+  l.G = T > 0 ? (T + 63 * (int64_t)N) / kC : 0;
+  l.off_tm = ((size_t)4 * ((size_t)N + 1) + 1023) / 1024 * 1024;
+  l.off_kt = l.off_tm + (size_t)3 * l.G * Hv * kC * kC * 2;
+  l.off_vec = l.off_kt + (size_t)l.G * Hk * kD * kC * 2;
+  l.total = l.off_vec + (size_t)l.G * Hv * 4 * kC * 4;
+  return l;
+}
+
+__device__ __forceinline__ void seq_range(const PrefillArgs& p, int n, int64_t& s, int64_t& e) {
+  int64_t a = p.cu_seqlens[n], b = p.cu_seqlens[n + 1];
+  a = a < 0 ? 0 : (a > p.T ? p.T : a);
+  b = b < 0 ? 0 : (b > p.T ? p.T : b);
+  s = a;
+  e = b < a ? a : b;
+}
+
+// named barrier with an OR-reduced predicate over `count` threads
+__device__ __forceinline__ bool bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void bar_named(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Byte offset of 16-byte chunk c (along K) of row r in a K-major SW128 bf16
+// tile of `rows` rows (64 elements per atom).
+__device__ __forceinline__ uint32_t sw_chunk(int r, int c, int rows) {
+  return (uint32_t)((c >> 3) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 +
+                    (((c & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 8 fp32 values -> their bf16 hi parts and the bf16 rounding of the remainders
+__device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * m], x[2 * m + 1]);
+    h[m] = *reinterpret_cast<const uint32_t*>(&hv);
+    l[m] = pack_bf16(x[2 * m] - __low2float(hv), x[2 * m + 1] - __high2float(hv));
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// ------------------------------------------------------------ chunk index
+
+// cs[n] = sum_{m<n} ceil(len_m / 64), cs[N] = total (clamped to G + 1 so a
+// cu_seqlens that overlaps itself is caught, not overflowed). One block of
+// 1024 threads.
+__global__ void __launch_bounds__(1024) cp_index_kernel(const PrefillArgs p, const CpWork w) {
+  __shared__ int64_t swarp[32];
+  __shared__ int64_t scarry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) scarry = 0;
+  __syncthreads();
+  for (int base = 0; base < p.N; base += 1024) {
+    const int n = base + tid;
+    int64_t cnt = 0;
+    if (n < p.N) {
+      int64_t s, e;
+      seq_range(p, n, s, e);
+      cnt = (e - s + kC - 1) / kC;
+    }
+    int64_t v = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    if (lane == 31) swarp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int64_t x = swarp[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t u = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += u;
+      }
+      swarp[lane] = x;
+    }
+    __syncthreads();
+    const int64_t excl = scarry + (warp > 0 ? swarp[warp - 1] : 0) + v - cnt;
+    if (n < p.N) w.cs[n] = (int32_t)(excl < w.G + 1 ? excl : w.G + 1);
+    __syncthreads();
+    if (tid == 1023) scarry = excl + cnt;
+    __syncthreads();
+  }
+  if (tid == 0) w.cs[p.N] = (int32_t)(scarry < w.G + 1 ? scarry : w.G + 1);
+}
+
+// ------------------------------------------------------------------ prep
+
+constexpr uint32_t P_OFF_K = 0;        // bf16 [64][128] SW128 (TMA)
+constexpr uint32_t P_OFF_Q = 16384;    // bf16 [64][128] SW128 (TMA)
+constexpr uint32_t P_OFF_A = 32768;    // fp32 [64][65]
+constexpr uint32_t P_OFF_T = 49408;    // fp32 [64][64] Tm
+constexpr uint32_t P_OFF_X = 65792;    // fp32 [768] block-product scratch
+constexpr uint32_t P_SMEM = 68864 + 1024;
+
+__global__ void __launch_bounds__(kPrepThreads, 2)
+    cp_prep_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ float sg[kC], sbeta[kC], sc[kC], sgam[kC], sinvk[kC], sinvq[kC];
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(8) uint64_t bar_ld, bar_gp;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int qd = warp & 3, hh = warp >> 2;
+  const int64_t g = blockIdx.x;
+  const int kh = blockIdx.y;
+  const int64_t total = w.cs[p.N] < w.G ? w.cs[p.N] : w.G;
+  if (g >= total) return;
+  // the sequence owning slot g: the last n with cs[n] <= g
+  int lo = 0, hi = p.N - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (w.cs[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  const int n = lo;
+  int64_t seq_s, seq_e;
+  seq_range(p, n, seq_s, seq_e);
+  const int64_t c0 = seq_s + (int64_t)kC * (g - w.cs[n]);
+  const int L = (int)((seq_e - c0) < kC ? (seq_e - c0) : kC);
+  const bool prenorm = (p.flags & GDN_QK_PRENORMALIZED) != 0;
+  const bool pregate = (p.flags & GDN_GATES_PRECOMPUTED) != 0;
+
+  if (warp == 0) {
+    tc::tmem_alloc(&s_tmem, 128);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar_ld, 1);
+    mbar_init(&bar_gp, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar_ld, 32768u);
+    tc::tma_load_2d(sm + P_OFF_K, &tm_k, kh * kD, (int)c0, &bar_ld);
+    tc::tma_load_2d(sm + P_OFF_K + 8192, &tm_k, kh * kD + 64, (int)c0, &bar_ld);
+    tc::tma_load_2d(sm + P_OFF_Q, &tm_q, kh * kD, (int)c0, &bar_ld);
+    tc::tma_load_2d(sm + P_OFF_Q + 8192, &tm_q, kh * kD + 64, (int)c0, &bar_ld);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tb = s_tmem;
+  const uint32_t tq = tb + ((uint32_t)(32 * qd) << 16);
+  const uint32_t a_k = smem_u32(sm + P_OFF_K), a_q = smem_u32(sm + P_OFF_Q);
+
+  bool to = !mbar_wait(&bar_ld, 0);
+  if (tid == 0 && !to) {
+    tc::fence_after_sync();
+    const uint32_t id = tc::idesc(tc::kBF16, 64, 64);
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      tc::mma_f16(tb, tc::sdesc_kstep(a_k, 64, s), tc::sdesc_kstep(a_k, 64, s), id, s > 0);
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      tc::mma_f16(tb + 64, tc::sdesc_kstep(a_q, 64, s), tc::sdesc_kstep(a_k, 64, s), id, s > 0);
+    tc::mma_commit(&bar_gp);
+  }
+  // l2 scales of k and q rows, four threads per row, 16 bytes at a time
+  {
+    const int srow = tid >> 2, part = tid & 3;
+    float kk = 0.f, qq = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int c16 = part + 4 * m;
+      const uint32_t off = sw_chunk(srow, c16, 64);
+      const uint4 kr = *reinterpret_cast<const uint4*>(sm + P_OFF_K + off);
+      const uint4 qr = *reinterpret_cast<const uint4*>(sm + P_OFF_Q + off);
+      const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&kr);
+      const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&qr);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float kf = __bfloat162float(kv[e]), qf = __bfloat162float(qv[e]);
+        kk = fmaf(kf, kf, kk);
+        qq = fmaf(qf, qf, qq);
+      }
+    }
+    kk += __shfl_xor_sync(0xffffffffu, kk, 1);
+    kk += __shfl_xor_sync(0xffffffffu, kk, 2);
+    qq += __shfl_xor_sync(0xffffffffu, qq, 1);
+    qq += __shfl_xor_sync(0xffffffffu, qq, 2);
+    if (part == 0) {
+      const bool live = srow < L;
+      sinvk[srow] = live ? (prenorm ? 1.f : 1.f / sqrtf(kk + p.l2_eps)) : 0.f;
+      sinvq[srow] = live ? (prenorm ? 1.f : 1.f / sqrtf(qq + p.l2_eps)) * p.scale : 0.f;
+    }
+  }
+  // K^T of this chunk and K head for the carry's state update: thread pair
+  // (i, half) gathers 32 rows t of column i
+  {
+    const int i = tid >> 1, th = tid & 1;
+    const uint32_t col = (uint32_t)((i >> 6) * 8192 + (i & 7) * 2);
+    const int ic = (i & 63) >> 3;
+    uint32_t wv[16];
+#pragma unroll
+    for (int t2 = 0; t2 < 16; ++t2) {
+      uint32_t pr = 0;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int t = 32 * th + 2 * t2 + q;
+        const uint32_t off = col + (uint32_t)((t >> 3) * 1024 + (t & 7) * 128 + ((ic ^ (t & 7)) << 4));
+        const uint32_t x = *reinterpret_cast<const unsigned short*>(sm + P_OFF_K + off);
+        pr |= (t < L ? x : 0u) << (16 * q);
+      }
+      wv[t2] = pr;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(w.kt + ((g * p.Hk + kh) * kD + i) * kC + 32 * th);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dst[c] = make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
+  }
+  if (!to) to = !mbar_wait(&bar_gp, 0);
+  if (__syncthreads_or(to)) {
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tb, 128);
+    return;
+  }
+  tc::fence_after_sync();
+  // the grams of this K head, once for all its V heads (rows of the M=64
+  // accumulator live in lanes 16 qd + 0..15 of quadrant qd)
+  float gv[32], pv[32];
+  tc::tmem_ld16(tq + 32 * hh, *reinterpret_cast<float(*)[16]>(gv));
+  tc::tmem_ld16(tq + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(gv + 16));
+  tc::tmem_ld16(tq + 64 + 32 * hh, *reinterpret_cast<float(*)[16]>(pv));
+  tc::tmem_ld16(tq + 64 + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(pv + 16));
+  tc::tmem_wait_ld();
+
+  float* Ap = reinterpret_cast<float*>(sm + P_OFF_A);
+  float* Tp = reinterpret_cast<float*>(sm + P_OFF_T);
+  float* Xp = reinterpret_cast<float*>(sm + P_OFF_X);
+  const size_t HvG = (size_t)w.G * p.Hv;
+  for (int r = 0; r < p.rep; ++r) {
+    const int h = p.map == GDN_MAP_GROUPED ? kh * p.rep + r : kh + r * p.Hk;
+    const size_t slot = (size_t)g * p.Hv + h;
+    // gates of this V head
+    if (tid < kC) {
+      float gt = 0.f, bt = 0.f;
+      if (tid < L) {
+        const int64_t gi = (c0 + tid) * p.Hv + h;
+        if (pregate) {
+          gt = static_cast<const float*>(p.a)[gi];
+          bt = static_cast<const float*>(p.b)[gi];
+        } else {
+          gt = gate_g(p.decay, p.decay_param[h], p.dt_bias[h],
+                      __bfloat162float(static_cast<const __nv_bfloat16*>(p.a)[gi]));
+          bt = sigmoid_f(__bfloat162float(static_cast<const __nv_bfloat16*>(p.b)[gi]));
+        }
+      }
+      sg[tid] = gt;
+      sbeta[tid] = bt;
+    }
+    __syncthreads();
+    if (warp < 2) {
+      float v = sg[tid];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      sc[tid] = v;
+    }
+    __syncthreads();
+    if (warp == 1) sc[tid] += sc[31];
+    __syncthreads();
+    if (tid < kC) sgam[tid] = expf(sc[tid]);
+    // A (padded rows) and P (bf16, straight to the workspace)
+    if (lane < 16) {
+      const int t = 16 * qd + lane;
+      const bool live = t < L;
+      constexpr float kLog2e = 1.4426950408889634f;
+      const float ct = sc[t] * kLog2e, bt = sbeta[t], ikt = sinvk[t], iqt = sinvq[t];
+      float pr[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int s = 32 * hh + e;
+        const float dec = exp2f(ct - sc[s] * kLog2e);  // e^{c_t - c_s} <= 1 for s <= t
+        const float ks = sinvk[s];
+        Ap[t * kAStride + s] = (live && s < t) ? bt * dec * gv[e] * ikt * ks : 0.f;
+        pr[e] = (live && s <= t) ? dec * pv[e] * iqt * ks : 0.f;
+      }
+      uint4* dst = reinterpret_cast<uint4*>(w.tw + ((2 * HvG + slot) * kC + t) * kC + 32 * hh);
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        dst[m] = make_uint4(pack_bf16(pr[8 * m], pr[8 * m + 1]), pack_bf16(pr[8 * m + 2], pr[8 * m + 3]),
+                            pack_bf16(pr[8 * m + 4], pr[8 * m + 5]),
+                            pack_bf16(pr[8 * m + 6], pr[8 * m + 7]));
+    }
+    __syncthreads();
+    // (I + A)^{-1}: diagonal 16x16 blocks by forward substitution (warp b,
+    // lane l holds column l of block b), then the off-diagonal blocks one
+    // block diagonal at a time: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
+    if (warp < 4) {
+      const int b0 = 16 * warp, l = lane & 15;
+      float x[16];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) x[m] = (m == l) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 1; m < 16; ++m) {
+        const float* arow = Ap + (b0 + m) * kAStride + b0;
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < m; ++q) acc = fmaf(arow[q], x[q], acc);
+        if (m > l) x[m] = -acc;
+      }
+      if (lane < 16) {
+#pragma unroll
+        for (int m = 0; m < 16; ++m) Tp[(b0 + m) * kC + b0 + l] = x[m];
+      }
+    }
+    __syncthreads();
+    for (int d = 1; d < 4; ++d) {
+      const int nblk = 4 - d;
+      for (int e = tid; e < nblk * 256; e += kPrepThreads) {
+        const int jb = e >> 8, rr = (e >> 4) & 15, cc = e & 15, ib = jb + d;
+        float acc = 0.f;
+        for (int kb = jb; kb < ib; ++kb) {
+          const float* arow = Ap + (16 * ib + rr) * kAStride + 16 * kb;
+          const float* tcol = Tp + (16 * kb) * kC + 16 * jb + cc;
+#pragma unroll
+          for (int m = 0; m < 16; ++m) acc = fmaf(arow[m], tcol[m * kC], acc);
+        }
+        Xp[e] = acc;
+      }
+      __syncthreads();
+      for (int e = tid; e < nblk * 256; e += kPrepThreads) {
+        const int jb = e >> 8, rr = (e >> 4) & 15, cc = e & 15, ib = jb + d;
+        const float* trow = Tp + (16 * ib + rr) * kC + 16 * ib;
+        const float* xcol = Xp + (jb << 8) + cc;
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) acc = (m <= rr) ? fmaf(trow[m], xcol[m << 4], acc) : acc;
+        Tp[(16 * ib + rr) * kC + 16 * jb + cc] = -acc;
+      }
+      __syncthreads();
+    }
+    // Tb = Tm diag(beta) as hi + lo bf16, zero above the diagonal; 16
+    // consecutive elements of one row per thread
+    {
+      const int e0 = 16 * tid, t = e0 >> 6, s0 = e0 & 63;
+      float x[16];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const int s = s0 + m;
+        x[m] = s <= t ? Tp[t * kC + s] * sbeta[s] : 0.f;
+      }
+      uint4 h0, l0, h1, l1;
+      split8(x, h0, l0);
+      split8(x + 8, h1, l1);
+      uint4* dh = reinterpret_cast<uint4*>(w.tw + slot * (kC * kC) + e0);
+      uint4* dl = reinterpret_cast<uint4*>(w.tw + (HvG + slot) * (kC * kC) + e0);
+      dh[0] = h0;
+      dh[1] = h1;
+      dl[0] = l0;
+      dl[1] = l1;
+    }
+    if (tid < kC) {
+      const int t = tid;
+      const bool live = t < L;
+      float* vv = w.vec + slot * (4 * kC);
+      vv[t] = live ? sgam[t] * sinvk[t] : 0.f;
+      vv[kC + t] = live ? expf(sc[L - 1] - sc[t]) * sinvk[t] : 0.f;
+      vv[2 * kC + t] = live ? sgam[t] * sinvq[t] : 0.f;
+      vv[3 * kC + t] = t == 0 ? sgam[L - 1] : 0.f;
+    }
+    __syncthreads();  // gate arrays, A and Tm are rewritten for the next V head
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tb, 128);
+}
+
+// ----------------------------------------------------------------- carry
+
+constexpr uint32_t C_OFF_SHI = 0;        // bf16 [128 j][128 i] SW128, hi part of S
+constexpr uint32_t C_OFF_SLO = 32768;    // lo part of S
+constexpr uint32_t C_OFF_K = 65536;      // bf16 [64 t][128 i] SW128 (TMA)
+constexpr uint32_t C_OFF_Q = 81920;      // bf16 [64 t][128 i] SW128 (TMA)
+constexpr uint32_t C_OFF_KT = 98304;     // bf16 [128 i][64 t] SW128 (TMA, k transposed by prep)
+constexpr uint32_t C_OFF_RHI = 114688;   // bf16 [128 j][64 s]: R^T hi, later (dk Dm)^T hi
+constexpr uint32_t C_OFF_RLO = 131072;   // lo parts of the same
+constexpr uint32_t C_OFF_DMH = 147456;   // bf16 [128 j][64 s]: Dm^T
+constexpr uint32_t C_OFF_TMH = 163840;   // bf16 [64 t][64 s] SW128 (TMA): Tb hi
+constexpr uint32_t C_OFF_TML = 172032;   // Tb lo
+constexpr uint32_t C_OFF_P = 180224;     // P
+constexpr uint32_t C_OFF_V = 188416;     // bf16 [64 s][128 j] row-major (TMA)
+constexpr uint32_t C_OFF_VEC = 204800;   // fp32 [2][4][64] (bulk copy), by chunk parity
+constexpr uint32_t C_OFF_Z = 206848;     // bf16 [64 t][128 j] row-major: z (TMA), then out
+constexpr uint32_t C_SMEM = 223232 + 1024;
+
+// TMEM columns
+constexpr uint32_t TM_S = 0, TM_KS = 128, TM_DM = 192, TM_OQ = 256, TM_OP = 320, TM_COLS = 512;
+// (TM_OQ, TM_OP) + 128 * (chunk & 1): output accumulators, double-buffered
+
+// Loads are issued by thread 0 as soon as the buffer's last reader is known
+// to be done (every MMA a commit covers has completed):
+//   K    after S K^T (bar_m1)             Q      after R Tb^T (bar_m3; covers S Q^T)
+//   V    after R is written               Tb     after R Tb^T (bar_m3)
+//   P,KT after the chunk's Dm P^T (bar_of) vec    two chunks ahead, by parity
+__global__ void __launch_bounds__(kChainThreads, 1)
+    cp_chain_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_z,
+                    const __grid_constant__ CUtensorMap tm_kt) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t bar_k, bar_q, bar_v, bar_tm, bar_p, bar_m1, bar_m3, bar_m5;
+  __shared__ __align__(8) uint64_t bar_vec[2], bar_of[2], bar_oe[2], bar_fin, bar_z;
+  __shared__ uint32_t s_tmem;
+  __shared__ float spart[4][kC];
+  __shared__ float sinv[kC];
+  __shared__ float sgq[2][kC];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x, n = blockIdx.y;
+  const int kh = k_head_of(p.map, h, p.Hk, p.rep);
+  const int64_t kb = w.cs[n], ke = w.cs[n + 1];
+  if (ke <= kb) return;  // empty sequence: the state is left as it is
+  if (ke > w.G) {
+    if (tid == 0) record_device_error(GDN_ERR_INVALID_ARG);
+    return;
+  }
+  const int nch = (int)(ke - kb);
+  int64_t seq_s, seq_e;
+  seq_range(p, n, seq_s, seq_e);
+  const bool fused = p.z != nullptr;
+  const size_t HvG = (size_t)w.G * p.Hv;
+
+  if (warp == 0) {
+    tc::tmem_alloc(&s_tmem, TM_COLS);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar_k, 1);
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_v, 1);
+    mbar_init(&bar_tm, 1);
+    mbar_init(&bar_p, 1);
+    mbar_init(&bar_m1, 1);
+    mbar_init(&bar_m3, 1);
+    mbar_init(&bar_m5, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_vec[b], 1);
+      mbar_init(&bar_of[b], 1);
+      mbar_init(&bar_oe[b], kChainThreads - 128);
+    }
+    mbar_init(&bar_fin, 1);
+    mbar_init(&bar_z, 1);
+    fence_mbar_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tb = s_tmem;
+
+  // thread 0's loads; the counts let the exit path wait for copies in flight
+  uint32_t n_k = 0, n_q = 0, n_v = 0, n_tm = 0, n_p = 0, n_vec0 = 0, n_vec1 = 0;
+  auto chunk_c0 = [&](int k) { return seq_s + (int64_t)kC * k; };
+  auto slot_of = [&](int k) { return (size_t)(kb + k) * p.Hv + h; };
+  auto load_k = [&](int k) {
+    ++n_k;
+    mbar_arrive_expect_tx(&bar_k, 16384u);
+    tc::tma_load_2d(sm + C_OFF_K, &tm_k, kh * kD, (int)chunk_c0(k), &bar_k);
+    tc::tma_load_2d(sm + C_OFF_K + 8192, &tm_k, kh * kD + 64, (int)chunk_c0(k), &bar_k);
+  };
+  auto load_q = [&](int k) {
+    ++n_q;
+    mbar_arrive_expect_tx(&bar_q, 16384u);
+    tc::tma_load_2d(sm + C_OFF_Q, &tm_q, kh * kD, (int)chunk_c0(k), &bar_q);
+    tc::tma_load_2d(sm + C_OFF_Q + 8192, &tm_q, kh * kD + 64, (int)chunk_c0(k), &bar_q);
+  };
+  auto load_v = [&](int k) {
+    ++n_v;
+    mbar_arrive_expect_tx(&bar_v, 16384u);
+    tc::tma_load_2d(sm + C_OFF_V, &tm_v, h * kD, (int)chunk_c0(k), &bar_v);
+  };
+  auto load_tm = [&](int k) {
+    const size_t slot = slot_of(k);
+    ++n_tm;
+    mbar_arrive_expect_tx(&bar_tm, 16384u);
+    tc::tma_load_2d(sm + C_OFF_TMH, &tm_w, 0, (int)(slot * kC), &bar_tm);
+    tc::tma_load_2d(sm + C_OFF_TML, &tm_w, 0, (int)((HvG + slot) * kC), &bar_tm);
+  };
+  auto load_pk = [&](int k) {
+    ++n_p;
+    mbar_arrive_expect_tx(&bar_p, 8192u + 16384u);
+    tc::tma_load_2d(sm + C_OFF_P, &tm_w, 0, (int)((2 * HvG + slot_of(k)) * kC), &bar_p);
+    tc::tma_load_2d(sm + C_OFF_KT, &tm_kt, 0, (int)(((kb + k) * p.Hk + kh) * kD), &bar_p);
+  };
+  auto load_vec = [&](int k) {
+    uint64_t* bar = &bar_vec[k & 1];
+    if (k & 1) ++n_vec1; else ++n_vec0;
+    mbar_arrive_expect_tx(bar, 1024u);
+    bulk_load(sm + C_OFF_VEC + (k & 1) * 1024, w.vec + slot_of(k) * (4 * kC), 1024u, bar);
+  };
+  if (tid == 0) {
+    load_k(0);
+    load_q(0);
+    load_v(0);
+    load_tm(0);
+    load_pk(0);
+    load_vec(0);
+    if (nch > 1) load_vec(1);
+  }
+
+  if (tid < 128) {
+    // ============================ carry group: thread j owns value row j
+    const int j = tid;
+    const uint32_t tl = tb + ((uint32_t)(32 * warp) << 16);
+    const uint32_t id64 = tc::idesc(tc::kBF16, 128, 64), id128 = tc::idesc(tc::kBF16, 128, 128);
+    const uint64_t d_shi = tc::sdesc_sw128(smem_u32(sm + C_OFF_SHI)),
+                   d_slo = tc::sdesc_sw128(smem_u32(sm + C_OFF_SLO)),
+                   d_k = tc::sdesc_sw128(smem_u32(sm + C_OFF_K)),
+                   d_q = tc::sdesc_sw128(smem_u32(sm + C_OFF_Q)),
+                   d_kt = tc::sdesc_sw128(smem_u32(sm + C_OFF_KT)),
+                   d_rhi = tc::sdesc_sw128(smem_u32(sm + C_OFF_RHI)),
+                   d_rlo = tc::sdesc_sw128(smem_u32(sm + C_OFF_RLO)),
+                   d_dmh = tc::sdesc_sw128(smem_u32(sm + C_OFF_DMH)),
+                   d_tmh = tc::sdesc_sw128(smem_u32(sm + C_OFF_TMH)),
+                   d_tml = tc::sdesc_sw128(smem_u32(sm + C_OFF_TML)),
+                   d_p = tc::sdesc_sw128(smem_u32(sm + C_OFF_P));
+    float* gS = p.state + (((size_t)n * p.Hv + h) * kD + j) * kD;
+    bool to = !mbar_wait(&bar_vec[0], 0);
+    {
+      // S0 -> hi/lo operand copies; TMEM <- G_{L-1} S0 of the first chunk
+      const float gl = reinterpret_cast<const float*>(sm + C_OFF_VEC)[3 * kC];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float v[kC];
+        const float4* src = reinterpret_cast<const float4*>(gS + 64 * hf);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float4 f = src[m];
+          v[4 * m] = f.x;
+          v[4 * m + 1] = f.y;
+          v[4 * m + 2] = f.z;
+          v[4 * m + 3] = f.w;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 hi, lo;
+          split8(v + 8 * c, hi, lo);
+          *reinterpret_cast<uint4*>(sm + C_OFF_SHI + sw_chunk(j, 8 * hf + c, 128)) = hi;
+          *reinterpret_cast<uint4*>(sm + C_OFF_SLO + sw_chunk(j, 8 * hf + c, 128)) = lo;
+        }
+#pragma unroll
+        for (int e = 0; e < kC; ++e) v[e] *= gl;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          tc::tmem_st16(tl + TM_S + 64 * hf + 16 * m, *reinterpret_cast<const float(*)[16]>(v + 16 * m));
+      }
+      tc::tmem_wait_st();
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+    }
+
+    for (int k = 0; k < nch; ++k) {
+      const uint32_t ph = (uint32_t)(k & 1);
+      const int64_t c0 = chunk_c0(k);
+      const int L = (int)((seq_e - c0) < kC ? (seq_e - c0) : kC);
+      const float* vec = reinterpret_cast<const float*>(sm + C_OFF_VEC + (k & 1) * 1024);
+      const uint32_t ob = 128u * (uint32_t)(k & 1);
+      const bool more = k + 1 < nch;
+
+      // (1) KS^T = S K^T (hi + lo); then, for the output only, S_hi Q^T
+      if (tid == 0) {
+        to |= !mbar_wait(&bar_k, ph);
+        if (k >= 2) to |= !mbar_wait(&bar_oe[k & 1], (uint32_t)(((k >> 1) - 1) & 1));
+      }
+      if (bar_or(1, 128, to)) break;
+      if (tid == 0) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int s = 0; s < 8; ++s)
+            tc::mma_f16(tb + TM_KS, tc::sdesc_at(part ? d_slo : d_shi, 128, s),
+                        tc::sdesc_at(d_k, 64, s), id64, (part | s) != 0);
+        tc::mma_commit(&bar_m1);
+        to |= !mbar_wait(&bar_q, ph);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          tc::mma_f16(tb + TM_OQ + ob, tc::sdesc_at(d_shi, 128, s), tc::sdesc_at(d_q, 64, s), id64,
+                      s > 0);
+      }
+
+      // (2) R^T = V^T - diag(ak) KS^T  (columns s >= L are zero)
+      to |= !mbar_wait(&bar_m1, ph);
+      to |= !mbar_wait(&bar_v, ph);
+      to |= !mbar_wait(&bar_vec[k & 1], (uint32_t)((k >> 1) & 1));
+      if (bar_or(1, 128, to)) break;
+      tc::fence_after_sync();
+      if (tid == 0 && more) load_k(k + 1);
+      {
+        const __nv_bfloat16* vt = reinterpret_cast<const __nv_bfloat16*>(sm + C_OFF_V) + j;
+        float ks[kC];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          tc::tmem_ld16(tl + TM_KS + 16 * m, *reinterpret_cast<float(*)[16]>(ks + 16 * m));
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          float r[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 a4 = reinterpret_cast<const float4*>(vec)[4 * m + e4];
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int e = 4 * e4 + u, s = 16 * m + e;
+              const float x = __bfloat162float(vt[s * kD]) - av[u] * ks[s];
+              r[e] = s < L ? x : 0.f;
+            }
+          }
+          uint4 h0, l0, h1, l1;
+          split8(r, h0, l0);
+          split8(r + 8, h1, l1);
+          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, 2 * m, 128)) = h0;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, 2 * m + 1, 128)) = h1;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, 2 * m, 128)) = l0;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, 2 * m + 1, 128)) = l1;
+        }
+      }
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      bar_named(1, 128);
+
+      // (3) Dm^T = R^T Tb^T  (hi*hi + hi*lo + lo*hi)
+      if (tid == 0) {
+        if (more) load_v(k + 1);
+        to |= !mbar_wait(&bar_tm, ph);
+        tc::fence_after_sync();
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          tc::mma_f16(tb + TM_DM, tc::sdesc_at(d_rhi, 128, s), tc::sdesc_at(d_tmh, 64, s), id64,
+                      s > 0);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          tc::mma_f16(tb + TM_DM, tc::sdesc_at(d_rhi, 128, s), tc::sdesc_at(d_tml, 64, s), id64, true);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          tc::mma_f16(tb + TM_DM, tc::sdesc_at(d_rlo, 128, s), tc::sdesc_at(d_tmh, 64, s), id64, true);
+        tc::mma_commit(&bar_m3);
+      }
+
+      // (4) Dm' = diag(dk) Dm (hi + lo, over R's buffers) and Dm_hi
+      to |= !mbar_wait(&bar_m3, ph);
+      tc::fence_after_sync();
+      if (tid == 0 && more) {
+        load_q(k + 1);   // S_hi Q^T was issued before R Tb^T
+        load_tm(k + 1);
+      }
+      {
+        float dm[kC];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          tc::tmem_ld16(tl + TM_DM + 16 * m, *reinterpret_cast<float(*)[16]>(dm + 16 * m));
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          float x[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 d4 = reinterpret_cast<const float4*>(vec + kC)[4 * m + e4];
+            x[4 * e4] = d4.x * dm[16 * m + 4 * e4];
+            x[4 * e4 + 1] = d4.y * dm[16 * m + 4 * e4 + 1];
+            x[4 * e4 + 2] = d4.z * dm[16 * m + 4 * e4 + 2];
+            x[4 * e4 + 3] = d4.w * dm[16 * m + 4 * e4 + 3];
+          }
+          uint4 h0, l0, h1, l1;
+          split8(x, h0, l0);
+          split8(x + 8, h1, l1);
+          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, 2 * m, 128)) = h0;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, 2 * m + 1, 128)) = h1;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, 2 * m, 128)) = l0;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, 2 * m + 1, 128)) = l1;
+          const float* d = dm + 16 * m;
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            *reinterpret_cast<uint4*>(sm + C_OFF_DMH + sw_chunk(j, 2 * m + c, 128)) =
+                make_uint4(pack_bf16(d[8 * c], d[8 * c + 1]), pack_bf16(d[8 * c + 2], d[8 * c + 3]),
+                           pack_bf16(d[8 * c + 4], d[8 * c + 5]), pack_bf16(d[8 * c + 6], d[8 * c + 7]));
+        }
+      }
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      if (bar_or(1, 128, to)) break;
+
+      // (5) S += Dm'^T K (hi + lo) on the pre-decayed accumulator; then, for
+      // the output only, Dm^T P^T
+      if (tid == 0) {
+        if (k + 2 < nch) load_vec(k + 2);  // this parity's vector block is consumed
+        to |= !mbar_wait(&bar_p, ph);
+        tc::fence_after_sync();
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            tc::mma_f16(tb + TM_S, tc::sdesc_at(part ? d_rlo : d_rhi, 128, s),
+                        tc::sdesc_at(d_kt, 128, s), id128, true);
+        tc::mma_commit(&bar_m5);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          tc::mma_f16(tb + TM_OP + ob, tc::sdesc_at(d_dmh, 128, s), tc::sdesc_at(d_p, 64, s), id64,
+                      s > 0);
+        tc::mma_commit(&bar_of[k & 1]);  // S_hi Q^T and Dm^T P^T of this chunk
+      }
+
+      // (6) the new state: operand copies, decay of the next chunk applied in
+      // TMEM; after the last chunk, back to global memory
+      to |= !mbar_wait(&bar_m5, ph);
+      tc::fence_after_sync();
+      float gl = 1.f;
+      if (more) {
+        to |= !mbar_wait(&bar_vec[(k + 1) & 1], (uint32_t)(((k + 1) >> 1) & 1));
+        gl = reinterpret_cast<const float*>(sm + C_OFF_VEC + ((k + 1) & 1) * 1024)[3 * kC];
+      }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float v[kC];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          tc::tmem_ld16(tl + TM_S + 64 * hf + 16 * m, *reinterpret_cast<float(*)[16]>(v + 16 * m));
+        tc::tmem_wait_ld();
+        if (!more) {
+          float4* dst = reinterpret_cast<float4*>(gS + 64 * hf);
+#pragma unroll
+          for (int m = 0; m < 16; ++m)
+            dst[m] = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 hi, lo;
+            split8(v + 8 * c, hi, lo);
+            *reinterpret_cast<uint4*>(sm + C_OFF_SHI + sw_chunk(j, 8 * hf + c, 128)) = hi;
+            *reinterpret_cast<uint4*>(sm + C_OFF_SLO + sw_chunk(j, 8 * hf + c, 128)) = lo;
+          }
+#pragma unroll
+          for (int e = 0; e < kC; ++e) v[e] *= gl;
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            tc::tmem_st16(tl + TM_S + 64 * hf + 16 * m, *reinterpret_cast<const float(*)[16]>(v + 16 * m));
+        }
+      }
+      tc::tmem_wait_st();
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      if (tid == 0 && more) {
+        // P and K^T of this chunk are free once its Dm^T P^T has completed
+        to |= !mbar_wait(&bar_of[k & 1], (uint32_t)((k >> 1) & 1));
+        load_pk(k + 1);
+      }
+    }
+  } else {
+    // ============================ output group: 8 warps; thread (j, half)
+    // owns output column j = 32 (warp % 4) + lane for the 32 rows of its half.
+    // O = diag(gq) OQ + OP from TMEM; with the fused norm, the per-row sums of
+    // squares are reduce-scattered across lanes, z arrives by TMA into a
+    // row-major tile that the gated result then overwrites in place, and each
+    // live row leaves as one 256-byte bulk store.
+    constexpr int kOut = kChainThreads - 128;
+    const int u = tid - 128, q4 = warp & 3, half = (warp - 4) >> 2;
+    const int j = 32 * q4 + lane, t0 = 32 * half;
+    const uint32_t tl = tb + ((uint32_t)(32 * q4) << 16);
+    const float nwj = fused ? p.norm_w[j] : 0.f;
+    __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(sm + C_OFF_Z);
+    uint32_t n_z = 0;
+    bool stored = false;
+    auto load_z = [&](int k) {
+      ++n_z;
+      mbar_arrive_expect_tx(&bar_z, 16384u);
+      tc::tma_load_2d(sm + C_OFF_Z, &tm_z, h * kD, (int)chunk_c0(k), &bar_z);
+    };
+    if (fused && u == 0) load_z(0);
+    for (int k = 0; k < nch; ++k) {
+      const int64_t c0 = chunk_c0(k);
+      const int L = (int)((seq_e - c0) < kC ? (seq_e - c0) : kC);
+      const uint32_t ob = 128u * (uint32_t)(k & 1) + (uint32_t)t0;
+      const float* gq = sgq[k & 1] + t0;
+      if (u < kC) sgq[k & 1][u] = __ldg(w.vec + slot_of(k) * (4 * kC) + 2 * kC + u);
+      bool to = !mbar_wait(&bar_of[k & 1], (uint32_t)((k >> 1) & 1));
+      if (bar_or(2, kOut, to)) break;
+      tc::fence_after_sync();
+      // pass 1: core output and per-row squares
+      float sq[32];
+      {
+        float a[2][16], b[2][16];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          tc::tmem_ld16(tl + TM_OQ + ob + 16 * m, a[m]);
+          tc::tmem_ld16(tl + TM_OP + ob + 16 * m, b[m]);
+        }
+        tc::tmem_wait_ld();
+        float o[32];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            o[16 * m + e] = fmaf(gq[16 * m + e], a[m][e], b[m][e]);
+            sq[16 * m + e] = o[16 * m + e] * o[16 * m + e];
+          }
+        if (p.core_out != nullptr) {
+          float* cg = p.core_out + ((c0 + t0) * p.Hv + h) * kD + j;
+          const int64_t cstr = (int64_t)p.Hv * kD;
+          if (L == kC) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) cg[e * cstr] = o[e];
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (t0 + e < L) cg[e * cstr] = o[e];
+          }
+        }
+      }
+      if (!fused) {
+        tc::fence_before_sync();
+        mbar_arrive(&bar_oe[k & 1]);
+        continue;
+      }
+      // five halving exchanges: lane l ends with the sum of row t0 + l
+#pragma unroll
+      for (int st = 0; st < 5; ++st) {
+        const int m = 16 >> st, hv = 16 >> st;
+        const bool up = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < hv; ++i) {
+          const float send = up ? sq[i] : sq[i + hv];
+          const float keep = up ? sq[i + hv] : sq[i];
+          sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+      spart[q4][t0 + lane] = sq[0];
+      bar_named(2, kOut);
+      if (u < kC)
+        sinv[u] = 1.f / sqrtf((spart[0][u] + spart[1][u] + spart[2][u] + spart[3][u]) / (float)kD +
+                              p.rms_eps);
+      to = !mbar_wait(&bar_z, (uint32_t)(k & 1));
+      bar_named(2, kOut);
+      // pass 2: the gated result over z, in place (rows >= L hold finite
+      // values that are never stored)
+      {
+        float a[2][16], b[2][16];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          tc::tmem_ld16(tl + TM_OQ + ob + 16 * m, a[m]);
+          tc::tmem_ld16(tl + TM_OP + ob + 16 * m, b[m]);
+        }
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int t = t0 + 16 * m + e;
+            const float o = fmaf(gq[16 * m + e], a[m][e], b[m][e]);
+            const float zf = __bfloat162float(zb[t * kD + j]);
+            const float gate = __fdividef(zf, 1.f + __expf(-zf));
+            zb[t * kD + j] = __float2bfloat16_rn(o * sinv[t] * nwj * gate);
+          }
+      }
+      tc::fence_before_sync();
+      mbar_arrive(&bar_oe[k & 1]);  // this chunk's output accumulators are free
+      fence_proxy_async_smem();
+      bar_named(2, kOut);
+      if (u < L) {
+        bulk_store(static_cast<__nv_bfloat16*>(p.out) + ((c0 + u) * p.Hv + h) * kD, zb + u * kD,
+                   (uint32_t)(kD * 2));
+        bulk_commit();
+        bulk_wait_read_all();
+        stored = true;
+      }
+      if (bar_or(2, kOut, to)) break;  // every row has left the staging tile
+      if (u == 0 && k + 1 < nch) load_z(k + 1);
+    }
+    if (stored) bulk_wait_all();
+    if (u == 0 && n_z) mbar_wait(&bar_z, (n_z - 1) & 1);
+  }
+
+  // drain: every copy and MMA this CTA issued has completed before it exits
+  // and TMEM is released (all of these have completed already unless a
+  // bounded wait gave up)
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid == 0) {
+    tc::fence_after_sync();
+    tc::mma_commit(&bar_fin);
+    mbar_wait(&bar_fin, 0);
+    if (n_k) mbar_wait(&bar_k, (n_k - 1) & 1);
+    if (n_q) mbar_wait(&bar_q, (n_q - 1) & 1);
+    if (n_v) mbar_wait(&bar_v, (n_v - 1) & 1);
+    if (n_tm) mbar_wait(&bar_tm, (n_tm - 1) & 1);
+    if (n_p) mbar_wait(&bar_p, (n_p - 1) & 1);
+    if (n_vec0) mbar_wait(&bar_vec[0], (n_vec0 - 1) & 1);
+    if (n_vec1) mbar_wait(&bar_vec[1], (n_vec1 - 1) & 1);
+    tc::fence_before_sync();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tb, TM_COLS);
+  }
+}
+
+}  // namespace
+
+int64_t prefill_cp_workspace_bytes(int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
+  return (int64_t)cp_layout(N, T, Hk, Hv).total;
+}
+
+bool prefill_cp_supported(const PrefillArgs& p, int32_t dtype, int32_t D) {
+  if (D != kD || dtype != GDN_BF16) return false;
+  if (p.T >= ((int64_t)1 << 31)) return false;  // TMA row coordinates are int32
+  const CpLayout l = cp_layout(p.N, p.T, p.Hk, p.Hv);
+  if ((double)l.G * p.Hv * kC * 3 >= 2147483647.0) return false;
+  if ((double)l.G * p.Hk * kD >= 2147483647.0) return false;
+  return tc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_t stream) {
+  if (p.N == 0 || p.T == 0) return cudaSuccess;
+  const CpLayout l = cp_layout(p.N, p.T, p.Hk, p.Hv);
+  CpWork w{};
+  w.cs = static_cast<int32_t*>(workspace);
+  w.tw = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(workspace) + l.off_tm);
+  w.kt = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(workspace) + l.off_kt);
+  w.vec = reinterpret_cast<float*>(static_cast<char*>(workspace) + l.off_vec);
+  w.G = l.G;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap mq, mk, mv, mw, mz, mkt;
+  memset(&mz, 0, sizeof(mz));
+  const int64_t qkc = (int64_t)p.Hk * kD, vc = (int64_t)p.Hv * kD;
+  if (!tc::make_map_2d(&mq, p.q, p.T, qkc, p.q_stride, 2, bf, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::make_map_2d(&mk, p.k, p.T, qkc, p.k_stride, 2, bf, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::make_map_2d(&mv, p.v, p.T, vc, p.v_stride, 2, bf, kD, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !tc::make_map_2d(&mw, w.tw, 3 * l.G * p.Hv * kC, kC, kC, 2, bf, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!tc::make_map_2d(&mkt, w.kt, l.G * p.Hk * kD, kC, kC, 2, bf, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (p.z != nullptr &&
+      !tc::make_map_2d(&mz, p.z, p.T, vc, vc, 2, bf, kD, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  cp_index_kernel<<<1, 1024, 0, stream>>>(p, w);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(cp_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+  if (e != cudaSuccess) return e;
+  cp_prep_kernel<<<dim3((unsigned)l.G, (unsigned)p.Hk), kPrepThreads, P_SMEM, stream>>>(p, w, mq, mk);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(cp_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
+  if (e != cudaSuccess) return e;
+  cp_chain_kernel<<<dim3((unsigned)p.Hv, (unsigned)p.N), kChainThreads, C_SMEM, stream>>>(p, w, mq, mk,
+                                                                                         mv, mw, mz, mkt);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn
+
+GDN_DEFINE_ERROR_READER(prefill_cp)

@@ -617,50 +617,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) tc::tmem_dealloc(tb, TM_COLS);
 }
 
-// ------------------------------------------------------------ tensor maps
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
-// 2-D map over rows of `cols` elements spaced `stride` elements apart.
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t stride,
-              CUtensorMapDataType dt, uint32_t box_cols, uint32_t box_rows,
-              CUtensorMapSwizzle sw) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
-  const cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename T>
 cudaError_t launch_tc_t(const PrefillArgs& p, cudaStream_t stream) {
   const CUtensorMapDataType dt =
       std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap mq, mk, mv;
   const int64_t qkc = (int64_t)p.Hk * kTcD, vc = (int64_t)p.Hv * kTcD;
-  if (!make_map(&mq, p.q, p.T, qkc, p.q_stride, dt, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&mk, p.k, p.T, qkc, p.k_stride, dt, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&mv, p.v, p.T, vc, p.v_stride, dt, kTcNS, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+  if (!tc::make_map_2d(&mq, p.q, p.T, qkc, p.q_stride, 2, dt, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::make_map_2d(&mk, p.k, p.T, qkc, p.k_stride, 2, dt, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::make_map_2d(&mv, p.v, p.T, vc, p.v_stride, 2, dt, kTcNS, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   auto kern = prefill_tc_kernel<T>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_DYN);
@@ -685,7 +650,7 @@ cudaError_t launch_tc_t(const PrefillArgs& p, cudaStream_t stream) {
 bool prefill_tc_supported(const PrefillArgs& p, int32_t dtype, int32_t D) {
   if (D != kTcD || (dtype != GDN_BF16 && dtype != GDN_F16)) return false;
   if (p.T >= ((int64_t)1 << 31)) return false;  // TMA row coordinate is int32
-  return encode_fn() != nullptr;
+  return tc::encode_fn() != nullptr;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& p, int32_t dtype, cudaStream_t stream) {

@@ -12,6 +12,8 @@
 //  * TMEM addresses are (lane << 16) | column.
 #pragma once
 
+#include <cuda.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "gdn_common.cuh"
@@ -49,6 +51,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr) {
 // Descriptor of k-step `s` (32 bytes of K each) of a K-major SW128 tile.
 __device__ __forceinline__ uint64_t sdesc_kstep(uint32_t tile_addr, int rows, int s) {
   return sdesc_sw128(tile_addr + (uint32_t)((s >> 2) * rows * 128 + (s & 3) * 32));
+}
+
+// Descriptor of k-step `s` advanced from a tile's base descriptor (the start
+// address field is linear; shared addresses stay below 256 KB).
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t base, int rows, int s) {
+  return base + (uint64_t)(((s >> 2) * rows * 128 + (s & 3) * 32) >> 4);
 }
 
 enum : uint32_t { kF16 = 0, kBF16 = 1, kTF32 = 2 };
@@ -173,6 +181,45 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, in
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
       "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+// ------------------------------------------------------- host: tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (no
+// link-time dependency on libcuda); nullptr if the driver lacks it.
+inline EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D map over `rows` rows of `cols` elements of `esize` bytes, rows
+// `stride` elements apart; boxes of box_cols x box_rows. Out-of-range box
+// elements read as zero.
+inline bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
+                        int64_t stride, uint32_t esize, CUtensorMapDataType dt, uint32_t box_cols,
+                        uint32_t box_rows, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
+  const cuuint64_t strides[1] = {(cuuint64_t)stride * esize};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace tc

@@ -65,7 +65,7 @@ typedef enum gdn_dtype { GDN_F16 = 0, GDN_BF16 = 1, GDN_F32 = 2 } gdn_dtype;
 enum {
   GDN_QK_PRENORMALIZED = 1,  /* q and k are already l2-normalised: skip it */
   GDN_GATES_PRECOMPUTED = 2, /* a holds g and b holds beta, both fp32 [T][Hv] */
-  GDN_PREFILL_CUDA_CORES = 4 /* use the fp32 CUDA-core chunk kernel even where the
+  GDN_PREFILL_CUDA_CORES = 4 /* use the fp32 CUDA-core chunk kernel even where a
                                 tensor-core one applies (head_dim 128, f16/bf16) */
 };
 
@@ -166,13 +166,26 @@ gdn_status gdn_decode_step(const gdn_dims* dims, int32_t batch, const void* mixe
  *              GDN_GATES_PRECOMPUTED fp32 g and beta.
  * decay_param, dt_bias  [Hv] fp32 (ignored with GDN_GATES_PRECOMPUTED).
  * flags        GDN_QK_PRENORMALIZED | GDN_GATES_PRECOMPUTED | GDN_PREFILL_CUDA_CORES.
- *              Head_dim 128 with f16/bf16 activations runs on the tensor cores
- *              (bf16/f16 K K^T and Q K^T, tf32 for every product with the
- *              state or with the triangular inverse); other shapes, fp32
- *              activations or GDN_PREFILL_CUDA_CORES use fp32 CUDA cores.
  * state        [N][Hv][D][D] fp32, in place (initial state = its contents).
  * core_out     [T][Hv][D] fp32 core output, or NULL.
  * z, norm_w, out  optional fused gated RMSNorm as in gdn_decode_step.
+ * workspace    device scratch of at least gdn_prefill_workspace_size bytes,
+ *              256-byte aligned, owned by the caller, not overlapping any
+ *              other argument; its contents need no initialisation and are
+ *              garbage afterwards. May be NULL (workspace_bytes ignored).
+ *
+ * Which kernels run (all on the given stream):
+ *  - head_dim 128, bf16, a workspace: the chunk-parallel tensor-core path.
+ *    Every chunk's state-free factors (the K and QK grams, (I+A)^-1 diag(beta),
+ *    the masked decayed QK^T) are computed at once into the workspace, then
+ *    one CTA per (V head, sequence) carries the state through its chunks with
+ *    the fp32 state as a TMEM accumulator; products that carry the state use
+ *    bf16 hi+lo splits of their fp32 factors.
+ *  - head_dim 128, f16/bf16, no workspace (or f16): a single-pass tensor-core
+ *    kernel (one cluster of four CTAs per V head and sequence, every chunk
+ *    stage in sequence; tf32 hi+lo splits for the state-carrying products).
+ *  - other head dims, fp32 activations, or GDN_PREFILL_CUDA_CORES: fp32 CUDA
+ *    cores.
  */
 gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int32_t* cu_seqlens,
                                int64_t total_tokens, const void* q, int64_t q_stride,
@@ -180,7 +193,18 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int
                                const void* a, const void* b, const float* decay_param,
                                const float* dt_bias, int32_t flags, float* state,
                                float* core_out, const void* z, const float* norm_w, void* out,
-                               void* stream);
+                               void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of workspace gdn_prefill_chunked can use for these sizes and flags
+ * (0 when no workspace path applies: head_dim != 128, io dtype not bf16, or
+ * GDN_PREFILL_CUDA_CORES): per 64-token chunk slot ((T + 63 N) / 64 of
+ * them) 25 KB per V head and 16 KB per K head, plus 4 (N + 1) bytes rounded
+ * up to 1 KB. Writes the size to *bytes; GDN_ERR_INVALID_ARG /
+ * GDN_ERR_EXTENT for invalid dims or sizes.
+ */
+gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
+                                      int64_t total_tokens, int32_t flags, int64_t* bytes);
 
 /*
  * Gated RMSNorm over rows of D: y = o * (mean_j o_j^2 + rms_eps)^(-1/2)

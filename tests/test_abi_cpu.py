@@ -50,6 +50,24 @@ def test_status_strings_and_version(lib):
     assert gdn.gdn_version() >= 100
 
 
+def test_prefill_workspace_size(lib):
+    d = gdn.dims(16, 32, 128, io_dtype=torch.bfloat16)
+    # (T + 63 N) / 64 chunk slots x (Hv x 25 KB + Hk x 16 KB), after the 1 KB index
+    per_slot = 32 * 25600 + 16 * 16384
+    assert gdn.gdn_prefill_workspace_size(d, 1, 4096) == 1024 + 64 * per_slot
+    assert gdn.gdn_prefill_workspace_size(d, 8, 34482) == 1024 + (34482 + 63 * 8) // 64 * per_slot
+    assert gdn.gdn_prefill_workspace_size(d, 1, 0) == 0
+    assert gdn.gdn_prefill_workspace_size(d, 1, 4096, gdn.GDN_PREFILL_CUDA_CORES) == 0
+    assert gdn.gdn_prefill_workspace_size(gdn.dims(16, 32, 64, io_dtype=torch.bfloat16), 1,
+                                          4096) == 0
+    assert gdn.gdn_prefill_workspace_size(gdn.dims(16, 32, 128, io_dtype=torch.float16), 1,
+                                          4096) == 0
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_prefill_workspace_size(d, -1, 10)
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_prefill_workspace_size(d, 1, 10, 64)  # unknown flag
+
+
 def test_qkv_features(lib):
     assert gdn.gdn_qkv_features(gdn.dims(16, 32, 128)) == 8192
     assert gdn.gdn_qkv_features(gdn.dims(16, 48, 128)) == 10240
@@ -110,7 +128,7 @@ def test_conv_and_prefill_and_norm_reject_bad_arguments(lib):
     pf = lib.gdn_prefill_chunked
     base = [ctypes.byref(d), 1, VP(0x100), 10, VP(0x1000), 128, VP(0x2000), 128, VP(0x3000), 128,
             VP(0x4000), VP(0x5000), VP(0x6000), VP(0x7000), 0, VP(0x100000), VP(0x200000), None,
-            None, None, None]
+            None, None, None, 0, None]
     args = list(base)
     args[5] = 8  # q stride below Hk*D
     assert pf(*args) == 1
@@ -126,6 +144,18 @@ def test_conv_and_prefill_and_norm_reject_bad_arguments(lib):
     args = list(base)
     args[15] = VP(0x1000)  # state overlaps q
     assert pf(*args) == 4
+
+    # workspace: too small, misaligned, overlapping an input (bf16, D=128)
+    d2 = gdn.dims(2, 4, 128, io_dtype=torch.bfloat16)
+    need = ctypes.c_int64(0)
+    assert lib.gdn_prefill_workspace_size(ctypes.byref(d2), 1, 10, 0, ctypes.byref(need)) == 0
+    assert need.value > 0
+    wbase = [ctypes.byref(d2), 1, VP(0x100), 10, VP(0x10000), 256, VP(0x20000), 256,
+             VP(0x30000), 512, VP(0x40000), VP(0x50000), VP(0x60000), VP(0x70000), 0,
+             VP(0x1000000), VP(0x2000000), None, None, None]
+    assert pf(*wbase, VP(0x4000000), need.value - 1, None) == 1  # too small
+    assert pf(*wbase, VP(0x4000010), need.value, None) == 5  # not 256-byte aligned
+    assert pf(*wbase, VP(0x30000), need.value, None) == 4  # overlaps v
 
     rn = lib.gdn_gated_rmsnorm
     assert rn(ctypes.byref(d), -1, None, None, None, None, None) == 1

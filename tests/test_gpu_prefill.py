@@ -46,7 +46,13 @@ def _page_chunk_inputs(T, Hk, Hv, D):
     return t(q), t(k), t(v), t(g.reshape(T, Hv)), t(beta.reshape(T, Hv)), t(S0)
 
 
-def _run_prefill(d, cu, q, k, v, a, b, state, flags, dp=None, dt=None, z=None, nw=None):
+# workspace argument per path: the chunk-parallel kernels (a workspace) or the
+# single-pass kernel (none); both are tensor-core paths for bf16 at D=128
+PATHS = {"parallel": "auto", "single": None}
+
+
+def _run_prefill(d, cu, q, k, v, a, b, state, flags, dp=None, dt=None, z=None, nw=None,
+                 workspace="auto"):
     T = q.shape[0]
     Hv, D = d.n_v_heads, d.head_dim
     core = torch.full((T, Hv, D), float("nan"), device="cuda")
@@ -56,18 +62,24 @@ def _run_prefill(d, cu, q, k, v, a, b, state, flags, dp=None, dt=None, z=None, n
     gdn.gdn_prefill_chunked(d, cuda(cu), cuda(q).reshape(T, -1), cuda(k).reshape(T, -1),
                             cuda(v).reshape(T, -1), cuda(a), cuda(b),
                             None if dp is None else cuda(dp), None if dt is None else cuda(dt),
-                            state, core_out=core, z=z, norm_w=nw, out=out, flags=flags)
+                            state, core_out=core, z=z, norm_w=nw, out=out, flags=flags,
+                            workspace=workspace)
     torch.cuda.synchronize()
     return core, out
 
 
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 @pytest.mark.parametrize("hk,hv,d", [(2, 4, 32), (2, 4, 128), (2, 2, 128)])
 @pytest.mark.parametrize("mp", [gi.GROUPED, gi.TILED])
-def test_page_chunk_case_and_split_continuity(hk, hv, d, mp, io):
+def test_page_chunk_case_and_split_continuity(hk, hv, d, mp, io, path):
     """T = 145 (2 x 64 + 17), split at 73, with the state's sentinel tail
     untouched (the Metal chunk test's shapes and fill). fp32 activations run
-    the CUDA-core kernel; bf16 at head_dim 128 the tensor-core one."""
+    the CUDA-core kernel; bf16 at head_dim 128 a tensor-core one (chunk-
+    parallel with a workspace, single-pass without)."""
+    if path == "single" and not (io == "bf16" and d == 128):
+        pytest.skip("the workspace only selects a kernel for bf16 at head_dim 128")
+    ws = PATHS[path]
     T = 145
     q, k, v, g, beta, S0 = _page_chunk_inputs(T, hk, hv, d)
     if io == "bf16":
@@ -77,7 +89,7 @@ def test_page_chunk_case_and_split_continuity(hk, hv, d, mp, io):
     ro, rS = oracle.delta(F64(q), F64(k), F64(v), F64(g), F64(beta), F64(S0)[0], mp)
 
     buf, state = _guarded_state(S0)
-    core, _ = _run_prefill(dims, gi.cu_seqlens([T]), q, k, v, g, beta, state, flags)
+    core, _ = _run_prefill(dims, gi.cu_seqlens([T]), q, k, v, g, beta, state, flags, workspace=ws)
     assert_abs(core.cpu(), ro, CHUNK_OUT_ABS, "chunk/full output")
     assert_abs(state.cpu()[0], rS, CHUNK_STATE_ABS, "chunk/full state")
     assert torch.all(buf[-16:] == SENTINEL)
@@ -85,10 +97,10 @@ def test_page_chunk_case_and_split_continuity(hk, hv, d, mp, io):
     sp = 73
     buf2, st2 = _guarded_state(S0)
     c1, _ = _run_prefill(dims, gi.cu_seqlens([sp]), q[:sp], k[:sp], v[:sp], g[:sp], beta[:sp],
-                         st2, flags)
+                         st2, flags, workspace=ws)
     assert torch.all(buf2[-16:] == SENTINEL)
     c2, _ = _run_prefill(dims, gi.cu_seqlens([T - sp]), q[sp:], k[sp:], v[sp:], g[sp:],
-                         beta[sp:], st2, flags)
+                         beta[sp:], st2, flags, workspace=ws)
     assert torch.all(buf2[-16:] == SENTINEL)
     assert_abs(torch.cat([c1, c2]).cpu(), F64(core.cpu()), CHUNK_OUT_ABS, "chunk split output")
     assert_abs(st2.cpu(), F64(state.cpu()), CHUNK_STATE_ABS, "chunk split state")
@@ -116,10 +128,13 @@ def _oracle_prefill(shape, w, q, k, v, a, b, S0, cu):
                                F64(q), F64(k), F64(v), gg, bb, F64(S0), cu.numpy(), l2_eps=1e-6)
 
 
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("mp,dec", [(gi.GROUPED, gi.LOG_RATE), (gi.TILED, gi.NEGATIVE_RATE)])
-def test_varlen_raw_inputs_with_fused_norm(dtype, d, mp, dec):
+def test_varlen_raw_inputs_with_fused_norm(dtype, d, mp, dec, path):
+    if path == "single" and not (dtype == "bf16" and d == 128):
+        pytest.skip("the workspace only selects a kernel for bf16 at head_dim 128")
     lengths = [1, 63, 64, 65, 130, 0, 7]
     shape = gi.Shape(2, 4, d, map=mp, decay=dec, dtype=dtype)
     w, q, k, v, z, a, b, S0 = _raw_case(500 + d, shape, lengths)
@@ -127,7 +142,7 @@ def test_varlen_raw_inputs_with_fused_norm(dtype, d, mp, dec):
     dims = gdn.dims(2, 4, d, map=mp, decay=dec, io_dtype=gi.DTYPES[dtype])
     state = cuda(S0)
     core, out = _run_prefill(dims, cu, q, k, v, a, b, state, 0, dp=w.decay_param, dt=w.dt_bias,
-                             z=cuda(z), nw=cuda(w.norm_w))
+                             z=cuda(z), nw=cuda(w.norm_w), workspace=PATHS[path])
     ro, rS = _oracle_prefill(shape, w, q, k, v, a, b, S0, cu)
     assert_abs(core.cpu(), ro, CHUNK_OUT_ABS, "varlen output")
     assert_abs(state.cpu(), rS, CHUNK_STATE_ABS, "varlen state")
@@ -139,26 +154,70 @@ def test_varlen_raw_inputs_with_fused_norm(dtype, d, mp, dec):
 
 
 @pytest.mark.parametrize("lengths", [[64], [1], [200, 0, 63], [129, 65, 1, 300]])
-def test_tensor_core_kernel_matches_cuda_core_kernel(lengths):
-    """The two chunk kernels on the same bf16 inputs (head_dim 128): both
-    within the chunk bounds of the oracle, and of each other."""
+def test_tensor_core_kernels_match_cuda_core_kernel(lengths):
+    """The three chunk kernels on the same bf16 inputs (head_dim 128): the
+    chunk-parallel and single-pass tensor-core ones and the fp32 CUDA-core
+    one, each within the chunk bounds of the oracle and of each other."""
     shape = gi.Shape(2, 8, 128, map=gi.TILED, decay=gi.LOG_RATE, dtype="bf16")
     w, q, k, v, z, a, b, S0 = _raw_case(900 + len(lengths), shape, lengths)
     cu = gi.cu_seqlens(lengths)
     dims = gdn.dims(2, 8, 128, map=gi.TILED, io_dtype=torch.bfloat16)
-    st_tc, st_cc = cuda(S0), cuda(S0)
-    c_tc, o_tc = _run_prefill(dims, cu, q, k, v, a, b, st_tc, 0, dp=w.decay_param,
-                              dt=w.dt_bias, z=cuda(z), nw=cuda(w.norm_w))
-    c_cc, o_cc = _run_prefill(dims, cu, q, k, v, a, b, st_cc, gdn.GDN_PREFILL_CUDA_CORES,
-                              dp=w.decay_param, dt=w.dt_bias, z=cuda(z), nw=cuda(w.norm_w))
     ro, rS = _oracle_prefill(shape, w, q, k, v, a, b, S0, cu)
-    assert_abs(c_tc.cpu(), ro, CHUNK_OUT_ABS, "tensor-core output")
-    assert_abs(st_tc.cpu(), rS, CHUNK_STATE_ABS, "tensor-core state")
-    assert_abs(c_cc.cpu(), ro, CHUNK_OUT_ABS, "cuda-core output")
-    assert_abs(c_tc.cpu(), F64(c_cc.cpu()), CHUNK_OUT_ABS, "tensor core vs cuda core")
-    ry = oracle.gated_rmsnorm(F64(c_tc.cpu()), F64(z), F64(w.norm_w), 1e-6)
-    assert_lowp(o_tc.cpu(), ry, "bf16", "tensor-core fused norm")
+    runs = {}
+    for name, flags, ws in (("parallel", 0, "auto"), ("single", 0, None),
+                            ("cuda cores", gdn.GDN_PREFILL_CUDA_CORES, None)):
+        st = cuda(S0)
+        c, o = _run_prefill(dims, cu, q, k, v, a, b, st, flags, dp=w.decay_param, dt=w.dt_bias,
+                            z=cuda(z), nw=cuda(w.norm_w), workspace=ws)
+        assert_abs(c.cpu(), ro, CHUNK_OUT_ABS, f"{name} output")
+        assert_abs(st.cpu(), rS, CHUNK_STATE_ABS, f"{name} state")
+        ry = oracle.gated_rmsnorm(F64(c.cpu()), F64(z), F64(w.norm_w), 1e-6)
+        assert_lowp(o.cpu(), ry, "bf16", f"{name} fused norm")
+        runs[name] = c.cpu()
+    assert_abs(runs["parallel"], F64(runs["cuda cores"]), CHUNK_OUT_ABS, "parallel vs cuda cores")
+    assert_abs(runs["single"], F64(runs["cuda cores"]), CHUNK_OUT_ABS, "single vs cuda cores")
     assert gdn.gdn_device_error() == 0
+
+
+def test_many_short_sequences_chunk_index():
+    """1100 sequences of 0..3 tokens and a few long ones (the chunk index is
+    a scan over sequences in blocks of 1024): states of empty sequences stay
+    bit for bit, every other one matches the oracle."""
+    rng = gi.rng(4242)
+    lengths = [int(x) for x in rng.integers(0, 4, size=1100)]
+    lengths[7], lengths[1030], lengths[1099] = 130, 64, 65
+    shape = gi.Shape(1, 1, 128, map=gi.GROUPED, decay=gi.LOG_RATE, dtype="bf16")
+    w, q, k, v, z, a, b, S0 = _raw_case(4243, shape, lengths)
+    cu = gi.cu_seqlens(lengths)
+    dims = gdn.dims(1, 1, 128, io_dtype=torch.bfloat16)
+    state = cuda(S0)
+    core, out = _run_prefill(dims, cu, q, k, v, a, b, state, 0, dp=w.decay_param,
+                             dt=w.dt_bias, z=cuda(z), nw=cuda(w.norm_w))
+    ro, rS = _oracle_prefill(shape, w, q, k, v, a, b, S0, cu)
+    assert_abs(core.cpu(), ro, CHUNK_OUT_ABS, "many sequences output")
+    assert_abs(state.cpu(), rS, CHUNK_STATE_ABS, "many sequences state")
+    sc = state.cpu()
+    for n, l in enumerate(lengths):
+        if l == 0:
+            assert torch.equal(sc[n], S0[n]), n
+    assert gdn.gdn_device_error() == 0
+
+
+def test_workspace_size_and_too_small_workspace():
+    d = gdn.dims(16, 32, 128, io_dtype=torch.bfloat16)
+    n = gdn.gdn_prefill_workspace_size(d, 1, 4096)
+    # 64 chunk slots x (32 V heads x 25 KB + 16 K heads x 16 KB) + the 1 KB index
+    assert n == 1024 + 64 * (32 * (3 * 8192 + 1024) + 16 * 16384)
+    assert gdn.gdn_prefill_workspace_size(d, 1, 4096, gdn.GDN_PREFILL_CUDA_CORES) == 0
+    assert gdn.gdn_prefill_workspace_size(gdn.dims(16, 32, 128, io_dtype=torch.float16), 1,
+                                          4096) == 0
+    assert gdn.gdn_prefill_workspace_size(gdn.dims(2, 4, 64), 1, 4096) == 0
+    shape = gi.Shape(2, 4, 128, dtype="bf16")
+    w, q, k, v, z, a, b, S0 = _raw_case(31, shape, [100])
+    small = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gdn.GdnError):
+        _run_prefill(gdn.dims(2, 4, 128), gi.cu_seqlens([100]), q, k, v, a, b, cuda(S0), 0,
+                     dp=w.decay_param, dt=w.dt_bias, workspace=small)
 
 
 def test_prefill_reads_strided_conv_output():
@@ -189,8 +248,9 @@ def test_prefill_reads_strided_conv_output():
     assert_abs(state.cpu(), rS, CHUNK_STATE_ABS, "strided state")
 
 
+@pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("random_state", [False, True])
-def test_prefill_t4096_sampled_heads(random_state):
+def test_prefill_t4096_sampled_heads(random_state, path):
     """One sequence of 4096 tokens (Hk=16, Hv=32, D=128, Grouped, bf16 raw
     inputs) at full size on the GPU; the oracle recomputes sampled heads."""
     wl = gi.workload_prefill(4096, random_state=random_state)
@@ -200,7 +260,7 @@ def test_prefill_t4096_sampled_heads(random_state):
     T = 4096
     core, out = _run_prefill(dims, wl["cu_seqlens"], wl["q"], wl["k"], wl["v"], wl["a"],
                              wl["b"], state, 0, dp=w.decay_param, dt=w.dt_bias,
-                             z=cuda(wl["z"]), nw=cuda(w.norm_w))
+                             z=cuda(wl["z"]), nw=cuda(w.norm_w), workspace=PATHS[path])
     gg, bb = oracle.gates(F64(wl["a"]), F64(wl["b"]), F64(w.decay_param), F64(w.dt_bias),
                           shape.decay)
     q = oracle.l2norm(F64(wl["q"]))
