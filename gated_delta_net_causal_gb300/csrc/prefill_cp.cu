@@ -44,7 +44,8 @@ namespace {
 constexpr int kC = 64;   // chunk
 constexpr int kD = 128;  // head_dim
 constexpr int kPrepThreads = 256;
-constexpr int kChainThreads = 384;  // warps 0-3: carry, warps 4-11: output
+constexpr int kCarryThreads = 256;  // warps 0-7: the state carry (two threads per value row)
+constexpr int kChainThreads = 512;  // warps 8-15: output and gated norm
 constexpr int kAStride = kC + 1;    // padded row pitch of the fp32 A matrix
 
 // ---------------------------------------------------------------- workspace
@@ -457,8 +458,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 
 constexpr uint32_t C_OFF_SHI = 0;        // bf16 [128 j][128 i] SW128, hi part of S
 constexpr uint32_t C_OFF_SLO = 32768;    // lo part of S
-constexpr uint32_t C_OFF_K = 65536;      // bf16 [64 t][128 i] SW128 (TMA)
-constexpr uint32_t C_OFF_Q = 81920;      // bf16 [64 t][128 i] SW128 (TMA)
+constexpr uint32_t C_OFF_KQ = 65536;     // bf16 [128][128 i] SW128 (TMA): rows 0-63 k, 64-127 q
 constexpr uint32_t C_OFF_KT = 98304;     // bf16 [128 i][64 t] SW128 (TMA, k transposed by prep)
 constexpr uint32_t C_OFF_RHI = 114688;   // bf16 [128 j][64 s]: R^T hi, later (dk Dm)^T hi
 constexpr uint32_t C_OFF_RLO = 131072;   // lo parts of the same
@@ -471,15 +471,15 @@ constexpr uint32_t C_OFF_VEC = 204800;   // fp32 [2][4][64] (bulk copy), by chun
 constexpr uint32_t C_OFF_Z = 206848;     // bf16 [64 t][128 j] row-major: z (TMA), then out
 constexpr uint32_t C_SMEM = 223232 + 1024;
 
-// TMEM columns
-constexpr uint32_t TM_S = 0, TM_KS = 128, TM_DM = 192, TM_OQ = 256, TM_OP = 320, TM_COLS = 512;
-// (TM_OQ, TM_OP) + 128 * (chunk & 1): output accumulators, double-buffered
+// TMEM columns, by chunk parity b: [KS | OQ] at TM_KQ + 128 b (S [k; q]^T as one
+// N = 128 accumulator; Dm^T later reuses the KS half) and OP at TM_OP + 64 b
+constexpr uint32_t TM_S = 0, TM_OP = 128, TM_KQ = 256, TM_COLS = 512;
 
 // Loads are issued by thread 0 as soon as the buffer's last reader is known
 // to be done (every MMA a commit covers has completed):
-//   K    after S K^T (bar_m1)             Q      after R Tb^T (bar_m3; covers S Q^T)
-//   V    after R is written               Tb     after R Tb^T (bar_m3)
-//   P,KT after the chunk's Dm P^T (bar_of) vec    two chunks ahead, by parity
+//   K, Q after S [k; q]^T (bar_m1)         V      after R is written
+//   Tb   after R Tb^T (bar_m3)             P, KT  after the chunk's Dm P^T (bar_of)
+//   vec  two chunks ahead, by parity
 __global__ void __launch_bounds__(kChainThreads, 1)
     cp_chain_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -487,7 +487,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
                     const __grid_constant__ CUtensorMap tm_kt) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) uint64_t bar_k, bar_q, bar_v, bar_tm, bar_p, bar_m1, bar_m3, bar_m5;
+  __shared__ __align__(8) uint64_t bar_kq, bar_v, bar_tm, bar_p, bar_m1, bar_m3, bar_m5;
   __shared__ __align__(8) uint64_t bar_vec[2], bar_of[2], bar_oe[2], bar_fin, bar_z;
   __shared__ uint32_t s_tmem;
   __shared__ float spart[4][kC];
@@ -514,8 +514,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(&bar_k, 1);
-    mbar_init(&bar_q, 1);
+    mbar_init(&bar_kq, 1);
     mbar_init(&bar_v, 1);
     mbar_init(&bar_tm, 1);
     mbar_init(&bar_p, 1);
@@ -525,7 +524,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_vec[b], 1);
       mbar_init(&bar_of[b], 1);
-      mbar_init(&bar_oe[b], kChainThreads - 128);
+      mbar_init(&bar_oe[b], kChainThreads - kCarryThreads);
     }
     mbar_init(&bar_fin, 1);
     mbar_init(&bar_z, 1);
@@ -537,20 +536,17 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   const uint32_t tb = s_tmem;
 
   // thread 0's loads; the counts let the exit path wait for copies in flight
-  uint32_t n_k = 0, n_q = 0, n_v = 0, n_tm = 0, n_p = 0, n_vec0 = 0, n_vec1 = 0;
+  uint32_t n_kq = 0, n_v = 0, n_tm = 0, n_p = 0, n_vec0 = 0, n_vec1 = 0;
   auto chunk_c0 = [&](int k) { return seq_s + (int64_t)kC * k; };
   auto slot_of = [&](int k) { return (size_t)(kb + k) * p.Hv + h; };
-  auto load_k = [&](int k) {
-    ++n_k;
-    mbar_arrive_expect_tx(&bar_k, 16384u);
-    tc::tma_load_2d(sm + C_OFF_K, &tm_k, kh * kD, (int)chunk_c0(k), &bar_k);
-    tc::tma_load_2d(sm + C_OFF_K + 8192, &tm_k, kh * kD + 64, (int)chunk_c0(k), &bar_k);
-  };
-  auto load_q = [&](int k) {
-    ++n_q;
-    mbar_arrive_expect_tx(&bar_q, 16384u);
-    tc::tma_load_2d(sm + C_OFF_Q, &tm_q, kh * kD, (int)chunk_c0(k), &bar_q);
-    tc::tma_load_2d(sm + C_OFF_Q + 8192, &tm_q, kh * kD + 64, (int)chunk_c0(k), &bar_q);
+  auto load_kq = [&](int k) {
+    const int y = (int)chunk_c0(k);
+    ++n_kq;
+    mbar_arrive_expect_tx(&bar_kq, 32768u);
+    tc::tma_load_2d(sm + C_OFF_KQ, &tm_k, kh * kD, y, &bar_kq);
+    tc::tma_load_2d(sm + C_OFF_KQ + 16384, &tm_k, kh * kD + 64, y, &bar_kq);
+    tc::tma_load_2d(sm + C_OFF_KQ + 8192, &tm_q, kh * kD, y, &bar_kq);
+    tc::tma_load_2d(sm + C_OFF_KQ + 24576, &tm_q, kh * kD + 64, y, &bar_kq);
   };
   auto load_v = [&](int k) {
     ++n_v;
@@ -577,8 +573,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     bulk_load(sm + C_OFF_VEC + (k & 1) * 1024, w.vec + slot_of(k) * (4 * kC), 1024u, bar);
   };
   if (tid == 0) {
-    load_k(0);
-    load_q(0);
+    load_kq(0);
     load_v(0);
     load_tm(0);
     load_pk(0);
@@ -586,15 +581,15 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     if (nch > 1) load_vec(1);
   }
 
-  if (tid < 128) {
-    // ============================ carry group: thread j owns value row j
-    const int j = tid;
-    const uint32_t tl = tb + ((uint32_t)(32 * warp) << 16);
+  if (tid < kCarryThreads) {
+    // ============================ carry group: thread (j, ch) owns value row j
+    // and half ch of the columns of each per-row phase
+    const int j = tid & 127, ch = tid >> 7;
+    const uint32_t tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
     const uint32_t id64 = tc::idesc(tc::kBF16, 128, 64), id128 = tc::idesc(tc::kBF16, 128, 128);
     const uint64_t d_shi = tc::sdesc_sw128(smem_u32(sm + C_OFF_SHI)),
                    d_slo = tc::sdesc_sw128(smem_u32(sm + C_OFF_SLO)),
-                   d_k = tc::sdesc_sw128(smem_u32(sm + C_OFF_K)),
-                   d_q = tc::sdesc_sw128(smem_u32(sm + C_OFF_Q)),
+                   d_kq = tc::sdesc_sw128(smem_u32(sm + C_OFF_KQ)),
                    d_kt = tc::sdesc_sw128(smem_u32(sm + C_OFF_KT)),
                    d_rhi = tc::sdesc_sw128(smem_u32(sm + C_OFF_RHI)),
                    d_rlo = tc::sdesc_sw128(smem_u32(sm + C_OFF_RLO)),
@@ -602,36 +597,33 @@ __global__ void __launch_bounds__(kChainThreads, 1)
                    d_tmh = tc::sdesc_sw128(smem_u32(sm + C_OFF_TMH)),
                    d_tml = tc::sdesc_sw128(smem_u32(sm + C_OFF_TML)),
                    d_p = tc::sdesc_sw128(smem_u32(sm + C_OFF_P));
-    float* gS = p.state + (((size_t)n * p.Hv + h) * kD + j) * kD;
+    float* gS = p.state + (((size_t)n * p.Hv + h) * kD + j) * kD + 64 * ch;
     bool to = !mbar_wait(&bar_vec[0], 0);
     {
       // S0 -> hi/lo operand copies; TMEM <- G_{L-1} S0 of the first chunk
       const float gl = reinterpret_cast<const float*>(sm + C_OFF_VEC)[3 * kC];
+      float v[kC];
+      const float4* src = reinterpret_cast<const float4*>(gS);
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float v[kC];
-        const float4* src = reinterpret_cast<const float4*>(gS + 64 * hf);
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float4 f = src[m];
-          v[4 * m] = f.x;
-          v[4 * m + 1] = f.y;
-          v[4 * m + 2] = f.z;
-          v[4 * m + 3] = f.w;
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 hi, lo;
-          split8(v + 8 * c, hi, lo);
-          *reinterpret_cast<uint4*>(sm + C_OFF_SHI + sw_chunk(j, 8 * hf + c, 128)) = hi;
-          *reinterpret_cast<uint4*>(sm + C_OFF_SLO + sw_chunk(j, 8 * hf + c, 128)) = lo;
-        }
-#pragma unroll
-        for (int e = 0; e < kC; ++e) v[e] *= gl;
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-          tc::tmem_st16(tl + TM_S + 64 * hf + 16 * m, *reinterpret_cast<const float(*)[16]>(v + 16 * m));
+      for (int m = 0; m < 16; ++m) {
+        const float4 f = src[m];
+        v[4 * m] = f.x;
+        v[4 * m + 1] = f.y;
+        v[4 * m + 2] = f.z;
+        v[4 * m + 3] = f.w;
       }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 hi, lo;
+        split8(v + 8 * c, hi, lo);
+        *reinterpret_cast<uint4*>(sm + C_OFF_SHI + sw_chunk(j, 8 * ch + c, 128)) = hi;
+        *reinterpret_cast<uint4*>(sm + C_OFF_SLO + sw_chunk(j, 8 * ch + c, 128)) = lo;
+      }
+#pragma unroll
+      for (int e = 0; e < kC; ++e) v[e] *= gl;
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        tc::tmem_st16(tl + TM_S + 64 * ch + 16 * m, *reinterpret_cast<const float(*)[16]>(v + 16 * m));
       tc::tmem_wait_st();
       fence_proxy_async_smem();
       tc::fence_before_sync();
@@ -642,109 +634,103 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       const int64_t c0 = chunk_c0(k);
       const int L = (int)((seq_e - c0) < kC ? (seq_e - c0) : kC);
       const float* vec = reinterpret_cast<const float*>(sm + C_OFF_VEC + (k & 1) * 1024);
-      const uint32_t ob = 128u * (uint32_t)(k & 1);
+      const uint32_t kq = TM_KQ + 128u * (uint32_t)(k & 1);  // [KS | OQ], later [DM | OQ]
       const bool more = k + 1 < nch;
 
-      // (1) KS^T = S K^T (hi + lo); then, for the output only, S_hi Q^T
+      // (1) [KS | OQ]^T = S_hi [k; q]^T + S_lo k^T (one N=128 accumulator)
       if (tid == 0) {
-        to |= !mbar_wait(&bar_k, ph);
+        to |= !mbar_wait(&bar_kq, ph);
         if (k >= 2) to |= !mbar_wait(&bar_oe[k & 1], (uint32_t)(((k >> 1) - 1) & 1));
       }
-      if (bar_or(1, 128, to)) break;
+      if (bar_or(1, kCarryThreads, to)) break;
       if (tid == 0) {
         tc::fence_after_sync();
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int s = 0; s < 8; ++s)
-            tc::mma_f16(tb + TM_KS, tc::sdesc_at(part ? d_slo : d_shi, 128, s),
-                        tc::sdesc_at(d_k, 64, s), id64, (part | s) != 0);
-        tc::mma_commit(&bar_m1);
-        to |= !mbar_wait(&bar_q, ph);
+        for (int s = 0; s < 8; ++s)
+          tc::mma_f16(tb + kq, tc::sdesc_at(d_shi, 128, s), tc::sdesc_at(d_kq, 128, s), id128, s > 0);
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          tc::mma_f16(tb + TM_OQ + ob, tc::sdesc_at(d_shi, 128, s), tc::sdesc_at(d_q, 64, s), id64,
-                      s > 0);
+          tc::mma_f16(tb + kq, tc::sdesc_at(d_slo, 128, s), tc::sdesc_at(d_kq, 128, s), id64, true);
+        tc::mma_commit(&bar_m1);
       }
 
-      // (2) R^T = V^T - diag(ak) KS^T  (columns s >= L are zero)
+      // (2) R^T = V^T - diag(ak) KS^T  (columns s >= L are zero); this
+      // thread's 32 columns s
       to |= !mbar_wait(&bar_m1, ph);
       to |= !mbar_wait(&bar_v, ph);
       to |= !mbar_wait(&bar_vec[k & 1], (uint32_t)((k >> 1) & 1));
-      if (bar_or(1, 128, to)) break;
+      if (bar_or(1, kCarryThreads, to)) break;
       tc::fence_after_sync();
-      if (tid == 0 && more) load_k(k + 1);
+      if (tid == 0 && more) load_kq(k + 1);
       {
         const __nv_bfloat16* vt = reinterpret_cast<const __nv_bfloat16*>(sm + C_OFF_V) + j;
-        float ks[kC];
+        float ks[32];
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-          tc::tmem_ld16(tl + TM_KS + 16 * m, *reinterpret_cast<float(*)[16]>(ks + 16 * m));
+        for (int m = 0; m < 2; ++m)
+          tc::tmem_ld16(tl + kq + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(ks + 16 * m));
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < 2; ++m) {
           float r[16];
 #pragma unroll
           for (int e4 = 0; e4 < 4; ++e4) {
-            const float4 a4 = reinterpret_cast<const float4*>(vec)[4 * m + e4];
+            const float4 a4 = reinterpret_cast<const float4*>(vec)[8 * ch + 4 * m + e4];
             const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const int e = 4 * e4 + u, s = 16 * m + e;
-              const float x = __bfloat162float(vt[s * kD]) - av[u] * ks[s];
+              const int e = 4 * e4 + u, s = 32 * ch + 16 * m + e;
+              const float x = __bfloat162float(vt[s * kD]) - av[u] * ks[16 * m + e];
               r[e] = s < L ? x : 0.f;
             }
           }
           uint4 h0, l0, h1, l1;
           split8(r, h0, l0);
           split8(r + 8, h1, l1);
-          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, 2 * m, 128)) = h0;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, 2 * m + 1, 128)) = h1;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, 2 * m, 128)) = l0;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, 2 * m + 1, 128)) = l1;
+          const int c = 4 * ch + 2 * m;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, c, 128)) = h0;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, c + 1, 128)) = h1;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, c, 128)) = l0;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, c + 1, 128)) = l1;
         }
       }
       fence_proxy_async_smem();
       tc::fence_before_sync();
-      bar_named(1, 128);
+      bar_named(1, kCarryThreads);
 
-      // (3) Dm^T = R^T Tb^T  (hi*hi + hi*lo + lo*hi)
+      // (3) Dm^T = R^T Tb^T  (hi*hi + hi*lo + lo*hi), over KS
       if (tid == 0) {
         if (more) load_v(k + 1);
         to |= !mbar_wait(&bar_tm, ph);
         tc::fence_after_sync();
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          tc::mma_f16(tb + TM_DM, tc::sdesc_at(d_rhi, 128, s), tc::sdesc_at(d_tmh, 64, s), id64,
-                      s > 0);
+          tc::mma_f16(tb + kq, tc::sdesc_at(d_rhi, 128, s), tc::sdesc_at(d_tmh, 64, s), id64, s > 0);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          tc::mma_f16(tb + TM_DM, tc::sdesc_at(d_rhi, 128, s), tc::sdesc_at(d_tml, 64, s), id64, true);
+          tc::mma_f16(tb + kq, tc::sdesc_at(d_rhi, 128, s), tc::sdesc_at(d_tml, 64, s), id64, true);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          tc::mma_f16(tb + TM_DM, tc::sdesc_at(d_rlo, 128, s), tc::sdesc_at(d_tmh, 64, s), id64, true);
+          tc::mma_f16(tb + kq, tc::sdesc_at(d_rlo, 128, s), tc::sdesc_at(d_tmh, 64, s), id64, true);
         tc::mma_commit(&bar_m3);
       }
 
-      // (4) Dm' = diag(dk) Dm (hi + lo, over R's buffers) and Dm_hi
+      // (4) Dm' = diag(dk) Dm (hi + lo, over R's buffers) and Dm_hi; this
+      // thread's 32 rows t
       to |= !mbar_wait(&bar_m3, ph);
       tc::fence_after_sync();
-      if (tid == 0 && more) {
-        load_q(k + 1);   // S_hi Q^T was issued before R Tb^T
-        load_tm(k + 1);
-      }
+      if (tid == 0 && more) load_tm(k + 1);
       {
-        float dm[kC];
+        float dm[32];
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-          tc::tmem_ld16(tl + TM_DM + 16 * m, *reinterpret_cast<float(*)[16]>(dm + 16 * m));
+        for (int m = 0; m < 2; ++m)
+          tc::tmem_ld16(tl + kq + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(dm + 16 * m));
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < 2; ++m) {
           float x[16];
 #pragma unroll
           for (int e4 = 0; e4 < 4; ++e4) {
-            const float4 d4 = reinterpret_cast<const float4*>(vec + kC)[4 * m + e4];
+            const float4 d4 = reinterpret_cast<const float4*>(vec + kC)[8 * ch + 4 * m + e4];
             x[4 * e4] = d4.x * dm[16 * m + 4 * e4];
             x[4 * e4 + 1] = d4.y * dm[16 * m + 4 * e4 + 1];
             x[4 * e4 + 2] = d4.z * dm[16 * m + 4 * e4 + 2];
@@ -753,21 +739,23 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           uint4 h0, l0, h1, l1;
           split8(x, h0, l0);
           split8(x + 8, h1, l1);
-          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, 2 * m, 128)) = h0;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, 2 * m + 1, 128)) = h1;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, 2 * m, 128)) = l0;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, 2 * m + 1, 128)) = l1;
+          const int c = 4 * ch + 2 * m;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, c, 128)) = h0;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, c + 1, 128)) = h1;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, c, 128)) = l0;
+          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, c + 1, 128)) = l1;
           const float* d = dm + 16 * m;
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-            *reinterpret_cast<uint4*>(sm + C_OFF_DMH + sw_chunk(j, 2 * m + c, 128)) =
-                make_uint4(pack_bf16(d[8 * c], d[8 * c + 1]), pack_bf16(d[8 * c + 2], d[8 * c + 3]),
-                           pack_bf16(d[8 * c + 4], d[8 * c + 5]), pack_bf16(d[8 * c + 6], d[8 * c + 7]));
+          for (int cc = 0; cc < 2; ++cc)
+            *reinterpret_cast<uint4*>(sm + C_OFF_DMH + sw_chunk(j, c + cc, 128)) =
+                make_uint4(pack_bf16(d[8 * cc], d[8 * cc + 1]), pack_bf16(d[8 * cc + 2], d[8 * cc + 3]),
+                           pack_bf16(d[8 * cc + 4], d[8 * cc + 5]),
+                           pack_bf16(d[8 * cc + 6], d[8 * cc + 7]));
         }
       }
       fence_proxy_async_smem();
       tc::fence_before_sync();
-      if (bar_or(1, 128, to)) break;
+      if (bar_or(1, kCarryThreads, to)) break;
 
       // (5) S += Dm'^T K (hi + lo) on the pre-decayed accumulator; then, for
       // the output only, Dm^T P^T
@@ -784,13 +772,13 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         tc::mma_commit(&bar_m5);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          tc::mma_f16(tb + TM_OP + ob, tc::sdesc_at(d_dmh, 128, s), tc::sdesc_at(d_p, 64, s), id64,
-                      s > 0);
+          tc::mma_f16(tb + TM_OP + 64u * (uint32_t)(k & 1), tc::sdesc_at(d_dmh, 128, s),
+                      tc::sdesc_at(d_p, 64, s), id64, s > 0);
         tc::mma_commit(&bar_of[k & 1]);  // S_hi Q^T and Dm^T P^T of this chunk
       }
 
       // (6) the new state: operand copies, decay of the next chunk applied in
-      // TMEM; after the last chunk, back to global memory
+      // TMEM; after the last chunk, back to global memory (columns 64 ch..)
       to |= !mbar_wait(&bar_m5, ph);
       tc::fence_after_sync();
       float gl = 1.f;
@@ -798,15 +786,14 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         to |= !mbar_wait(&bar_vec[(k + 1) & 1], (uint32_t)(((k + 1) >> 1) & 1));
         gl = reinterpret_cast<const float*>(sm + C_OFF_VEC + ((k + 1) & 1) * 1024)[3 * kC];
       }
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+      {
         float v[kC];
 #pragma unroll
         for (int m = 0; m < 4; ++m)
-          tc::tmem_ld16(tl + TM_S + 64 * hf + 16 * m, *reinterpret_cast<float(*)[16]>(v + 16 * m));
+          tc::tmem_ld16(tl + TM_S + 64 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(v + 16 * m));
         tc::tmem_wait_ld();
         if (!more) {
-          float4* dst = reinterpret_cast<float4*>(gS + 64 * hf);
+          float4* dst = reinterpret_cast<float4*>(gS);
 #pragma unroll
           for (int m = 0; m < 16; ++m)
             dst[m] = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
@@ -815,14 +802,14 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           for (int c = 0; c < 8; ++c) {
             uint4 hi, lo;
             split8(v + 8 * c, hi, lo);
-            *reinterpret_cast<uint4*>(sm + C_OFF_SHI + sw_chunk(j, 8 * hf + c, 128)) = hi;
-            *reinterpret_cast<uint4*>(sm + C_OFF_SLO + sw_chunk(j, 8 * hf + c, 128)) = lo;
+            *reinterpret_cast<uint4*>(sm + C_OFF_SHI + sw_chunk(j, 8 * ch + c, 128)) = hi;
+            *reinterpret_cast<uint4*>(sm + C_OFF_SLO + sw_chunk(j, 8 * ch + c, 128)) = lo;
           }
 #pragma unroll
           for (int e = 0; e < kC; ++e) v[e] *= gl;
 #pragma unroll
           for (int m = 0; m < 4; ++m)
-            tc::tmem_st16(tl + TM_S + 64 * hf + 16 * m, *reinterpret_cast<const float(*)[16]>(v + 16 * m));
+            tc::tmem_st16(tl + TM_S + 64 * ch + 16 * m, *reinterpret_cast<const float(*)[16]>(v + 16 * m));
         }
       }
       tc::tmem_wait_st();
@@ -841,8 +828,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     // squares are reduce-scattered across lanes, z arrives by TMA into a
     // row-major tile that the gated result then overwrites in place, and each
     // live row leaves as one 256-byte bulk store.
-    constexpr int kOut = kChainThreads - 128;
-    const int u = tid - 128, q4 = warp & 3, half = (warp - 4) >> 2;
+    constexpr int kOut = kChainThreads - kCarryThreads;
+    const int u = tid - kCarryThreads, q4 = warp & 3, half = (warp - 8) >> 2;
     const int j = 32 * q4 + lane, t0 = 32 * half;
     const uint32_t tl = tb + ((uint32_t)(32 * q4) << 16);
     const float nwj = fused ? p.norm_w[j] : 0.f;
@@ -858,7 +845,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     for (int k = 0; k < nch; ++k) {
       const int64_t c0 = chunk_c0(k);
       const int L = (int)((seq_e - c0) < kC ? (seq_e - c0) : kC);
-      const uint32_t ob = 128u * (uint32_t)(k & 1) + (uint32_t)t0;
+      const uint32_t oq = TM_KQ + 128u * (uint32_t)(k & 1) + 64u + (uint32_t)t0;
+      const uint32_t op = TM_OP + 64u * (uint32_t)(k & 1) + (uint32_t)t0;
       const float* gq = sgq[k & 1] + t0;
       if (u < kC) sgq[k & 1][u] = __ldg(w.vec + slot_of(k) * (4 * kC) + 2 * kC + u);
       bool to = !mbar_wait(&bar_of[k & 1], (uint32_t)((k >> 1) & 1));
@@ -870,8 +858,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         float a[2][16], b[2][16];
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-          tc::tmem_ld16(tl + TM_OQ + ob + 16 * m, a[m]);
-          tc::tmem_ld16(tl + TM_OP + ob + 16 * m, b[m]);
+          tc::tmem_ld16(tl + oq + 16 * m, a[m]);
+          tc::tmem_ld16(tl + op + 16 * m, b[m]);
         }
         tc::tmem_wait_ld();
         float o[32];
@@ -925,8 +913,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         float a[2][16], b[2][16];
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-          tc::tmem_ld16(tl + TM_OQ + ob + 16 * m, a[m]);
-          tc::tmem_ld16(tl + TM_OP + ob + 16 * m, b[m]);
+          tc::tmem_ld16(tl + oq + 16 * m, a[m]);
+          tc::tmem_ld16(tl + op + 16 * m, b[m]);
         }
         tc::tmem_wait_ld();
 #pragma unroll
@@ -967,8 +955,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     tc::fence_after_sync();
     tc::mma_commit(&bar_fin);
     mbar_wait(&bar_fin, 0);
-    if (n_k) mbar_wait(&bar_k, (n_k - 1) & 1);
-    if (n_q) mbar_wait(&bar_q, (n_q - 1) & 1);
+    if (n_kq) mbar_wait(&bar_kq, (n_kq - 1) & 1);
     if (n_v) mbar_wait(&bar_v, (n_v - 1) & 1);
     if (n_tm) mbar_wait(&bar_tm, (n_tm - 1) & 1);
     if (n_p) mbar_wait(&bar_p, (n_p - 1) & 1);
