@@ -76,6 +76,9 @@ def library() -> ctypes.CDLL:
         L.gdn_prefill_chunked.restype = ctypes.c_int
         L.gdn_prefill_chunked.argtypes = [pd, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, vp, vp,
                                           vp, i32, vp, vp, vp, vp, vp, vp, i64, vp]
+        L.gdn_prefill_chunked_static.restype = ctypes.c_int
+        L.gdn_prefill_chunked_static.argtypes = [pd, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp,
+                                                 vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]
         L.gdn_prefill_workspace_size.restype = ctypes.c_int
         L.gdn_prefill_workspace_size.argtypes = [pd, i32, i64, i32, ctypes.POINTER(i64)]
         L.gdn_gated_rmsnorm.restype = ctypes.c_int
@@ -213,6 +216,28 @@ def gdn_prefill_chunked(d: GdnDims, cu_seqlens, q, k, v, a, b, decay_param, dt_b
     return core_out, out
 
 
+GDN_STATIC_SCRATCH_BYTES = 96 << 20
+
+
+def gdn_prefill_chunked_static(d: GdnDims, cu_seqlens, q, k, v, a, b, decay_param, dt_bias,
+                               state, core_out=None, z=None, norm_w=None, out=None,
+                               flags: int = 0, stream=None):
+    """gdn_prefill_chunked over the library's static device scratch (no
+    workspace, no allocation). Calls must not overlap in time on one device."""
+    io = _io(d)
+    f32 = torch.float32
+    gate_dt = f32 if (flags & GDN_GATES_PRECOMPUTED) else io
+    _check(library().gdn_prefill_chunked_static(
+        ctypes.byref(d), cu_seqlens.numel() - 1, _ptr(cu_seqlens, "cu_seqlens", torch.int32),
+        q.shape[0], _base_ptr(q, "q", io), _token_stride(q, "q"), _base_ptr(k, "k", io),
+        _token_stride(k, "k"), _base_ptr(v, "v", io), _token_stride(v, "v"),
+        _ptr(a, "a", gate_dt), _ptr(b, "b", gate_dt), _ptr(decay_param, "decay_param", f32),
+        _ptr(dt_bias, "dt_bias", f32), int(flags), _ptr(state, "state", f32),
+        _ptr(core_out, "core_out", f32), _ptr(z, "z", io), _ptr(norm_w, "norm_w", f32),
+        _ptr(out, "out", io), _stream(stream)), "gdn_prefill_chunked_static")
+    return core_out, out
+
+
 def gdn_gated_rmsnorm(d: GdnDims, o, z, norm_w, y, stream=None):
     io = _io(d)
     rows = o.numel() // d.head_dim
@@ -238,7 +263,8 @@ def gdn_version() -> int:
 
 
 __all__ = ["GdnDims", "GdnError", "dims", "library", "status_string", "gdn_conv_update",
-           "gdn_decode_step", "gdn_prefill_chunked", "gdn_prefill_workspace_size", "gdn_gated_rmsnorm", "gdn_device_error",
+           "gdn_decode_step", "gdn_prefill_chunked", "gdn_prefill_workspace_size",
+           "gdn_prefill_chunked_static", "GDN_STATIC_SCRATCH_BYTES", "gdn_gated_rmsnorm", "gdn_device_error",
            "gdn_qkv_features", "gdn_version", "GDN_MAP_GROUPED", "GDN_MAP_TILED",
            "GDN_DECAY_LOG_RATE", "GDN_DECAY_NEGATIVE_RATE", "GDN_F16", "GDN_BF16", "GDN_F32",
            "GDN_QK_PRENORMALIZED", "GDN_GATES_PRECOMPUTED", "GDN_PREFILL_CUDA_CORES", "LIB_PATH"]

@@ -206,6 +206,39 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int
 gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
                                       int64_t total_tokens, int32_t flags, int64_t* bytes);
 
+/* Size of the static device scratch behind gdn_prefill_chunked_static. */
+#define GDN_STATIC_SCRATCH_BYTES (96u << 20)
+
+/*
+ * gdn_prefill_chunked without a workspace argument that still takes the
+ * chunk-parallel path: it runs over a scratch buffer of
+ * GDN_STATIC_SCRATCH_BYTES that the library reserves statically on each
+ * device (when the library's kernels first load there), so the call
+ * allocates nothing. The pages have no counterpart to this call; it serves
+ * callers that cannot hand out device memory.
+ *
+ * Arguments, results and errors are those of gdn_prefill_chunked, plus:
+ *  - GDN_ERR_EXTENT, checked first, when gdn_prefill_workspace_size for
+ *    these sizes exceeds GDN_STATIC_SCRATCH_BYTES (e.g. more than about
+ *    5,900 tokens at Hk=16, Hv=32; 3,400 at Hk=16, Hv=64);
+ *  - where no workspace path applies (f16, head_dim != 128,
+ *    GDN_PREFILL_CUDA_CORES) it is gdn_prefill_chunked with workspace NULL.
+ *
+ * Races: the scratch is one buffer per device shared by every call of this
+ * function. Two calls whose executions can overlap in time (on different
+ * streams without an event between them, or issued from host threads
+ * without ordering) write it concurrently and corrupt each other's output
+ * and state. Issue them on one stream or order them with events.
+ */
+gdn_status gdn_prefill_chunked_static(const gdn_dims* dims, int32_t num_seqs,
+                                      const int32_t* cu_seqlens, int64_t total_tokens,
+                                      const void* q, int64_t q_stride, const void* k,
+                                      int64_t k_stride, const void* v, int64_t v_stride,
+                                      const void* a, const void* b, const float* decay_param,
+                                      const float* dt_bias, int32_t flags, float* state,
+                                      float* core_out, const void* z, const float* norm_w,
+                                      void* out, void* stream);
+
 /*
  * Gated RMSNorm over rows of D: y = o * (mean_j o_j^2 + rms_eps)^(-1/2)
  * * norm_w[j] * silu(z[j]), computed in fp32 and rounded once to io dtype.
