@@ -317,7 +317,7 @@ gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
   if ((flags & ~(GDN_QK_PRENORMALIZED | GDN_GATES_PRECOMPUTED | GDN_PREFILL_CUDA_CORES)) != 0)
     return GDN_ERR_INVALID_ARG;
   if (dims->head_dim != 128 || dims->io_dtype != GDN_BF16 || (flags & GDN_PREFILL_CUDA_CORES) ||
-      num_seqs == 0 || total_tokens == 0)
+      dims->n_v_heads > 8 * dims->n_k_heads || num_seqs == 0 || total_tokens == 0)
     return GDN_OK;
   // (T + 63 N) / 64 chunk slots of 25 KB per V head and 16 KB per K head,
   // plus the chunk index

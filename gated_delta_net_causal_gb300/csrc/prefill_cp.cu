@@ -47,6 +47,7 @@ constexpr int kPrepThreads = 256;
 constexpr int kCarryThreads = 256;  // warps 0-7: the state carry (two threads per value row)
 constexpr int kChainThreads = 512;  // warps 8-15: output and gated norm
 constexpr int kAStride = kC + 1;    // padded row pitch of the fp32 A matrix
+constexpr int kMaxRep = 8;          // V heads per K head on this path
 
 // ---------------------------------------------------------------- workspace
 
@@ -185,6 +186,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ float sg[kC], sbeta[kC], sc[kC], sgam[kC], sinvk[kC], sinvq[kC];
+  __shared__ float sga[kMaxRep][kC], sgb[kMaxRep][kC];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t bar_ld, bar_gp;
 
@@ -221,6 +223,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     tc::tma_load_2d(sm + P_OFF_K + 8192, &tm_k, kh * kD + 64, (int)c0, &bar_ld);
     tc::tma_load_2d(sm + P_OFF_Q, &tm_q, kh * kD, (int)c0, &bar_ld);
     tc::tma_load_2d(sm + P_OFF_Q + 8192, &tm_q, kh * kD + 64, (int)c0, &bar_ld);
+  }
+  // raw gate inputs of every V head reading this K head, fetched while the
+  // k and q tiles are in flight
+  for (int e = tid; e < p.rep * kC; e += kPrepThreads) {
+    const int r = e >> 6, t = e & 63;
+    const int h = p.map == GDN_MAP_GROUPED ? kh * p.rep + r : kh + r * p.Hk;
+    float ga = 0.f, gb = 0.f;
+    if (t < L) {
+      const int64_t gi = (c0 + t) * p.Hv + h;
+      if (pregate) {
+        ga = static_cast<const float*>(p.a)[gi];
+        gb = static_cast<const float*>(p.b)[gi];
+      } else {
+        ga = __bfloat162float(static_cast<const __nv_bfloat16*>(p.a)[gi]);
+        gb = __bfloat162float(static_cast<const __nv_bfloat16*>(p.b)[gi]);
+      }
+    }
+    sga[r][t] = ga;
+    sgb[r][t] = gb;
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -321,14 +342,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     if (tid < kC) {
       float gt = 0.f, bt = 0.f;
       if (tid < L) {
-        const int64_t gi = (c0 + tid) * p.Hv + h;
         if (pregate) {
-          gt = static_cast<const float*>(p.a)[gi];
-          bt = static_cast<const float*>(p.b)[gi];
+          gt = sga[r][tid];
+          bt = sgb[r][tid];
         } else {
-          gt = gate_g(p.decay, p.decay_param[h], p.dt_bias[h],
-                      __bfloat162float(static_cast<const __nv_bfloat16*>(p.a)[gi]));
-          bt = sigmoid_f(__bfloat162float(static_cast<const __nv_bfloat16*>(p.b)[gi]));
+          gt = gate_g(p.decay, p.decay_param[h], p.dt_bias[h], sga[r][tid]);
+          bt = sigmoid_f(sgb[r][tid]);
         }
       }
       sg[tid] = gt;
@@ -421,12 +440,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     // Tb = Tm diag(beta) as hi + lo bf16, zero above the diagonal; 16
     // consecutive elements of one row per thread
     {
-      const int e0 = 16 * tid, t = e0 >> 6, s0 = e0 & 63;
+      const int e0 = 16 * tid, tr = e0 >> 6, u0 = e0 & 63;
       float x[16];
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
-        const int s = s0 + m;
-        x[m] = s <= t ? Tp[t * kC + s] * sbeta[s] : 0.f;
+        const int s = u0 + m;
+        x[m] = s <= tr ? Tp[tr * kC + s] * sbeta[s] : 0.f;
       }
       uint4 h0, l0, h1, l1;
       split8(x, h0, l0);
@@ -456,30 +475,35 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 
 // ----------------------------------------------------------------- carry
 
-constexpr uint32_t C_OFF_SHI = 0;        // bf16 [128 j][128 i] SW128, hi part of S
-constexpr uint32_t C_OFF_SLO = 32768;    // lo part of S
-constexpr uint32_t C_OFF_KQ = 65536;     // bf16 [128][128 i] SW128 (TMA): rows 0-63 k, 64-127 q
-constexpr uint32_t C_OFF_KT = 98304;     // bf16 [128 i][64 t] SW128 (TMA, k transposed by prep)
-constexpr uint32_t C_OFF_RHI = 114688;   // bf16 [128 j][64 s]: R^T hi, later (dk Dm)^T hi
-constexpr uint32_t C_OFF_RLO = 131072;   // lo parts of the same
-constexpr uint32_t C_OFF_DMH = 147456;   // bf16 [128 j][64 s]: Dm^T
-constexpr uint32_t C_OFF_TMH = 163840;   // bf16 [64 t][64 s] SW128 (TMA): Tb hi
-constexpr uint32_t C_OFF_TML = 172032;   // Tb lo
-constexpr uint32_t C_OFF_P = 180224;     // P
-constexpr uint32_t C_OFF_V = 188416;     // bf16 [64 s][128 j] row-major (TMA)
-constexpr uint32_t C_OFF_VEC = 204800;   // fp32 [2][4][64] (bulk copy), by chunk parity
-constexpr uint32_t C_OFF_Z = 206848;     // bf16 [64 t][128 j] row-major: z (TMA), then out
-constexpr uint32_t C_SMEM = 223232 + 1024;
+// shared memory (byte offsets from a 1024-aligned base)
+constexpr uint32_t C_OFF_KQ = 0;         // bf16 [128][128 i] SW128 (TMA): rows 0-63 k, 64-127 q
+constexpr uint32_t C_OFF_KT = 32768;     // bf16 [128 i][64 t] SW128 (TMA, k transposed by prep)
+constexpr uint32_t C_OFF_TMH = 49152;    // bf16 [64 t][64 s] SW128 (TMA): Tb hi
+constexpr uint32_t C_OFF_TML = 57344;    // Tb lo
+constexpr uint32_t C_OFF_P = 65536;      // P
+constexpr uint32_t C_OFF_V = 73728;      // bf16 [64 s][128 j] row-major (TMA)
+constexpr uint32_t C_OFF_VEC = 90112;    // fp32 [2][4][64] (bulk copy), by chunk parity
+constexpr uint32_t C_OFF_Z = 92160;      // bf16 [2][64 t][128 j] row-major: z (TMA), then out
+constexpr uint32_t C_SMEM = 124928 + 1024;
 
-// TMEM columns, by chunk parity b: [KS | OQ] at TM_KQ + 128 b (S [k; q]^T as one
-// N = 128 accumulator; Dm^T later reuses the KS half) and OP at TM_OP + 64 b
-constexpr uint32_t TM_S = 0, TM_OP = 128, TM_KQ = 256, TM_COLS = 512;
+// TMEM columns. The A operands of the MMAs live in TMEM as packed bf16 pairs
+// (row j in lane j, K elements 2c, 2c+1 in column c).
+constexpr uint32_t TM_S = 0;      // fp32 S (128): the state accumulator
+constexpr uint32_t TM_SHI = 128;  // bf16 hi part of S (64); (dk Dm)^T hi during the update
+constexpr uint32_t TM_SLO = 192;  // lo part (64); (dk Dm)^T lo during the update
+constexpr uint32_t TM_RHI = 256;  // bf16 R^T hi (32); Dm^T (hi only) once R Tb^T is done
+constexpr uint32_t TM_RLO = 288;  // R^T lo (32)
+constexpr uint32_t TM_KQ = 320;   // fp32 [KS | OQ] (128); Dm^T later takes the KS half
+constexpr uint32_t TM_OP = 448;   // fp32 Dm^T P^T (64)
+constexpr uint32_t TM_COLS = 512;
 
 // Loads are issued by thread 0 as soon as the buffer's last reader is known
 // to be done (every MMA a commit covers has completed):
-//   K, Q after S [k; q]^T (bar_m1)         V      after R is written
-//   Tb   after R Tb^T (bar_m3)             P, KT  after the chunk's Dm P^T (bar_of)
-//   vec  two chunks ahead, by parity
+//   K, Q after S [k; q]^T (bar_m1)     V   after R is written
+//   Tb   after R Tb^T (bar_m3)         P   after Dm^T P^T (bar_of)
+//   K^T  after the update (bar_m5)     vec two chunks ahead, by parity
+// The output group reads [KS | OQ] and OP of chunk k; thread 0 waits for it
+// (bar_oe) before chunk k+1 writes them.
 __global__ void __launch_bounds__(kChainThreads, 1)
     cp_chain_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -487,8 +511,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
                     const __grid_constant__ CUtensorMap tm_kt) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) uint64_t bar_kq, bar_v, bar_tm, bar_p, bar_m1, bar_m3, bar_m5;
-  __shared__ __align__(8) uint64_t bar_vec[2], bar_of[2], bar_oe[2], bar_fin, bar_z;
+  __shared__ __align__(8) uint64_t bar_kq, bar_v, bar_tb, bar_p, bar_kt, bar_m1, bar_m3, bar_m5;
+  __shared__ __align__(8) uint64_t bar_vec[2], bar_of, bar_oe, bar_fin, bar_z[2];
   __shared__ uint32_t s_tmem;
   __shared__ float spart[4][kC];
   __shared__ float sinv[kC];
@@ -516,18 +540,19 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   if (tid == 0) {
     mbar_init(&bar_kq, 1);
     mbar_init(&bar_v, 1);
-    mbar_init(&bar_tm, 1);
+    mbar_init(&bar_tb, 1);
     mbar_init(&bar_p, 1);
+    mbar_init(&bar_kt, 1);
     mbar_init(&bar_m1, 1);
     mbar_init(&bar_m3, 1);
     mbar_init(&bar_m5, 1);
+    mbar_init(&bar_of, 1);
+    mbar_init(&bar_oe, kChainThreads - kCarryThreads);
+    mbar_init(&bar_fin, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bar_vec[b], 1);
-      mbar_init(&bar_of[b], 1);
-      mbar_init(&bar_oe[b], kChainThreads - kCarryThreads);
+      mbar_init(&bar_z[b], 1);
     }
-    mbar_init(&bar_fin, 1);
-    mbar_init(&bar_z, 1);
     fence_mbar_init();
   }
   tc::fence_before_sync();
@@ -536,7 +561,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   const uint32_t tb = s_tmem;
 
   // thread 0's loads; the counts let the exit path wait for copies in flight
-  uint32_t n_kq = 0, n_v = 0, n_tm = 0, n_p = 0, n_vec0 = 0, n_vec1 = 0;
+  uint32_t n_kq = 0, n_v = 0, n_tb = 0, n_p = 0, n_kt = 0, n_vec0 = 0, n_vec1 = 0;
   auto chunk_c0 = [&](int k) { return seq_s + (int64_t)kC * k; };
   auto slot_of = [&](int k) { return (size_t)(kb + k) * p.Hv + h; };
   auto load_kq = [&](int k) {
@@ -553,18 +578,22 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     mbar_arrive_expect_tx(&bar_v, 16384u);
     tc::tma_load_2d(sm + C_OFF_V, &tm_v, h * kD, (int)chunk_c0(k), &bar_v);
   };
-  auto load_tm = [&](int k) {
+  auto load_tb = [&](int k) {
     const size_t slot = slot_of(k);
-    ++n_tm;
-    mbar_arrive_expect_tx(&bar_tm, 16384u);
-    tc::tma_load_2d(sm + C_OFF_TMH, &tm_w, 0, (int)(slot * kC), &bar_tm);
-    tc::tma_load_2d(sm + C_OFF_TML, &tm_w, 0, (int)((HvG + slot) * kC), &bar_tm);
+    ++n_tb;
+    mbar_arrive_expect_tx(&bar_tb, 16384u);
+    tc::tma_load_2d(sm + C_OFF_TMH, &tm_w, 0, (int)(slot * kC), &bar_tb);
+    tc::tma_load_2d(sm + C_OFF_TML, &tm_w, 0, (int)((HvG + slot) * kC), &bar_tb);
   };
-  auto load_pk = [&](int k) {
+  auto load_p = [&](int k) {
     ++n_p;
-    mbar_arrive_expect_tx(&bar_p, 8192u + 16384u);
+    mbar_arrive_expect_tx(&bar_p, 8192u);
     tc::tma_load_2d(sm + C_OFF_P, &tm_w, 0, (int)((2 * HvG + slot_of(k)) * kC), &bar_p);
-    tc::tma_load_2d(sm + C_OFF_KT, &tm_kt, 0, (int)(((kb + k) * p.Hk + kh) * kD), &bar_p);
+  };
+  auto load_kt = [&](int k) {
+    ++n_kt;
+    mbar_arrive_expect_tx(&bar_kt, 16384u);
+    tc::tma_load_2d(sm + C_OFF_KT, &tm_kt, 0, (int)(((kb + k) * p.Hk + kh) * kD), &bar_kt);
   };
   auto load_vec = [&](int k) {
     uint64_t* bar = &bar_vec[k & 1];
@@ -575,33 +604,51 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   if (tid == 0) {
     load_kq(0);
     load_v(0);
-    load_tm(0);
-    load_pk(0);
+    load_tb(0);
+    load_p(0);
+    load_kt(0);
     load_vec(0);
     if (nch > 1) load_vec(1);
   }
 
   if (tid < kCarryThreads) {
     // ============================ carry group: thread (j, ch) owns value row j
-    // and half ch of the columns of each per-row phase
+    // (TMEM lane j) and half ch of the columns of each per-row phase
     const int j = tid & 127, ch = tid >> 7;
     const uint32_t tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
     const uint32_t id64 = tc::idesc(tc::kBF16, 128, 64), id128 = tc::idesc(tc::kBF16, 128, 128);
-    const uint64_t d_shi = tc::sdesc_sw128(smem_u32(sm + C_OFF_SHI)),
-                   d_slo = tc::sdesc_sw128(smem_u32(sm + C_OFF_SLO)),
-                   d_kq = tc::sdesc_sw128(smem_u32(sm + C_OFF_KQ)),
+    const uint64_t d_kq = tc::sdesc_sw128(smem_u32(sm + C_OFF_KQ)),
                    d_kt = tc::sdesc_sw128(smem_u32(sm + C_OFF_KT)),
-                   d_rhi = tc::sdesc_sw128(smem_u32(sm + C_OFF_RHI)),
-                   d_rlo = tc::sdesc_sw128(smem_u32(sm + C_OFF_RLO)),
-                   d_dmh = tc::sdesc_sw128(smem_u32(sm + C_OFF_DMH)),
                    d_tmh = tc::sdesc_sw128(smem_u32(sm + C_OFF_TMH)),
                    d_tml = tc::sdesc_sw128(smem_u32(sm + C_OFF_TML)),
                    d_p = tc::sdesc_sw128(smem_u32(sm + C_OFF_P));
     float* gS = p.state + (((size_t)n * p.Hv + h) * kD + j) * kD + 64 * ch;
+
+    // 64 fp32 state values (this thread's half row) -> hi/lo A operands in
+    // TMEM, then the accumulator rescaled by gl
+    auto store_state = [&](float (&v)[kC], float gl) {
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t hw[16], lw[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float a0 = v[32 * hf + 2 * m], a1 = v[32 * hf + 2 * m + 1];
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(a0, a1);
+          hw[m] = *reinterpret_cast<const uint32_t*>(&hv);
+          lw[m] = pack_bf16(a0 - __low2float(hv), a1 - __high2float(hv));
+        }
+        tc::tmem_st16u(tl + TM_SHI + 32 * ch + 16 * hf, hw);
+        tc::tmem_st16u(tl + TM_SLO + 32 * ch + 16 * hf, lw);
+      }
+#pragma unroll
+      for (int e = 0; e < kC; ++e) v[e] *= gl;
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        tc::tmem_st16(tl + TM_S + 64 * ch + 16 * m, *reinterpret_cast<const float(*)[16]>(v + 16 * m));
+    };
+
     bool to = !mbar_wait(&bar_vec[0], 0);
     {
-      // S0 -> hi/lo operand copies; TMEM <- G_{L-1} S0 of the first chunk
-      const float gl = reinterpret_cast<const float*>(sm + C_OFF_VEC)[3 * kC];
       float v[kC];
       const float4* src = reinterpret_cast<const float4*>(gS);
 #pragma unroll
@@ -612,20 +659,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         v[4 * m + 2] = f.z;
         v[4 * m + 3] = f.w;
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 hi, lo;
-        split8(v + 8 * c, hi, lo);
-        *reinterpret_cast<uint4*>(sm + C_OFF_SHI + sw_chunk(j, 8 * ch + c, 128)) = hi;
-        *reinterpret_cast<uint4*>(sm + C_OFF_SLO + sw_chunk(j, 8 * ch + c, 128)) = lo;
-      }
-#pragma unroll
-      for (int e = 0; e < kC; ++e) v[e] *= gl;
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        tc::tmem_st16(tl + TM_S + 64 * ch + 16 * m, *reinterpret_cast<const float(*)[16]>(v + 16 * m));
+      store_state(v, reinterpret_cast<const float*>(sm + C_OFF_VEC)[3 * kC]);
       tc::tmem_wait_st();
-      fence_proxy_async_smem();
       tc::fence_before_sync();
     }
 
@@ -634,28 +669,27 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       const int64_t c0 = chunk_c0(k);
       const int L = (int)((seq_e - c0) < kC ? (seq_e - c0) : kC);
       const float* vec = reinterpret_cast<const float*>(sm + C_OFF_VEC + (k & 1) * 1024);
-      const uint32_t kq = TM_KQ + 128u * (uint32_t)(k & 1);  // [KS | OQ], later [DM | OQ]
       const bool more = k + 1 < nch;
 
       // (1) [KS | OQ]^T = S_hi [k; q]^T + S_lo k^T (one N=128 accumulator)
       if (tid == 0) {
         to |= !mbar_wait(&bar_kq, ph);
-        if (k >= 2) to |= !mbar_wait(&bar_oe[k & 1], (uint32_t)(((k >> 1) - 1) & 1));
+        if (k >= 1) to |= !mbar_wait(&bar_oe, (uint32_t)((k - 1) & 1));
       }
       if (bar_or(1, kCarryThreads, to)) break;
       if (tid == 0) {
         tc::fence_after_sync();
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          tc::mma_f16(tb + kq, tc::sdesc_at(d_shi, 128, s), tc::sdesc_at(d_kq, 128, s), id128, s > 0);
+          tc::mma_f16_ts(tb + TM_KQ, tb + TM_SHI + 8 * s, tc::sdesc_at(d_kq, 128, s), id128, s > 0);
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          tc::mma_f16(tb + kq, tc::sdesc_at(d_slo, 128, s), tc::sdesc_at(d_kq, 128, s), id64, true);
+          tc::mma_f16_ts(tb + TM_KQ, tb + TM_SLO + 8 * s, tc::sdesc_at(d_kq, 128, s), id64, true);
         tc::mma_commit(&bar_m1);
       }
 
-      // (2) R^T = V^T - diag(ak) KS^T  (columns s >= L are zero); this
-      // thread's 32 columns s
+      // (2) R^T = V^T - diag(ak) KS^T (columns s >= L zero); this thread's
+      // 32 columns s = 32 ch ..
       to |= !mbar_wait(&bar_m1, ph);
       to |= !mbar_wait(&bar_v, ph);
       to |= !mbar_wait(&bar_vec[k & 1], (uint32_t)((k >> 1) & 1));
@@ -667,93 +701,82 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         float ks[32];
 #pragma unroll
         for (int m = 0; m < 2; ++m)
-          tc::tmem_ld16(tl + kq + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(ks + 16 * m));
+          tc::tmem_ld16(tl + TM_KQ + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(ks + 16 * m));
         tc::tmem_wait_ld();
+        uint32_t hw[16], lw[16];
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          float r[16];
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 a4 = reinterpret_cast<const float4*>(vec)[8 * ch + e4];
+          const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+          float r[4];
 #pragma unroll
-          for (int e4 = 0; e4 < 4; ++e4) {
-            const float4 a4 = reinterpret_cast<const float4*>(vec)[8 * ch + 4 * m + e4];
-            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int e = 4 * e4 + u, s = 32 * ch + 16 * m + e;
-              const float x = __bfloat162float(vt[s * kD]) - av[u] * ks[16 * m + e];
-              r[e] = s < L ? x : 0.f;
-            }
+          for (int u = 0; u < 4; ++u) {
+            const int e = 4 * e4 + u, s = 32 * ch + e;
+            const float x = __bfloat162float(vt[s * kD]) - av[u] * ks[e];
+            r[u] = s < L ? x : 0.f;
           }
-          uint4 h0, l0, h1, l1;
-          split8(r, h0, l0);
-          split8(r + 8, h1, l1);
-          const int c = 4 * ch + 2 * m;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, c, 128)) = h0;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, c + 1, 128)) = h1;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, c, 128)) = l0;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, c + 1, 128)) = l1;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(r[2 * u], r[2 * u + 1]);
+            hw[2 * e4 + u] = *reinterpret_cast<const uint32_t*>(&hv);
+            lw[2 * e4 + u] = pack_bf16(r[2 * u] - __low2float(hv), r[2 * u + 1] - __high2float(hv));
+          }
         }
+        tc::tmem_st16u(tl + TM_RHI + 16 * ch, hw);
+        tc::tmem_st16u(tl + TM_RLO + 16 * ch, lw);
+        tc::tmem_wait_st();
       }
-      fence_proxy_async_smem();
       tc::fence_before_sync();
       bar_named(1, kCarryThreads);
 
       // (3) Dm^T = R^T Tb^T  (hi*hi + hi*lo + lo*hi), over KS
       if (tid == 0) {
         if (more) load_v(k + 1);
-        to |= !mbar_wait(&bar_tm, ph);
+        to |= !mbar_wait(&bar_tb, ph);
         tc::fence_after_sync();
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          tc::mma_f16(tb + kq, tc::sdesc_at(d_rhi, 128, s), tc::sdesc_at(d_tmh, 64, s), id64, s > 0);
+          tc::mma_f16_ts(tb + TM_KQ, tb + TM_RHI + 8 * s, tc::sdesc_at(d_tmh, 64, s), id64, s > 0);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          tc::mma_f16(tb + kq, tc::sdesc_at(d_rhi, 128, s), tc::sdesc_at(d_tml, 64, s), id64, true);
+          tc::mma_f16_ts(tb + TM_KQ, tb + TM_RHI + 8 * s, tc::sdesc_at(d_tml, 64, s), id64, true);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          tc::mma_f16(tb + kq, tc::sdesc_at(d_rlo, 128, s), tc::sdesc_at(d_tmh, 64, s), id64, true);
+          tc::mma_f16_ts(tb + TM_KQ, tb + TM_RLO + 8 * s, tc::sdesc_at(d_tmh, 64, s), id64, true);
         tc::mma_commit(&bar_m3);
       }
 
-      // (4) Dm' = diag(dk) Dm (hi + lo, over R's buffers) and Dm_hi; this
-      // thread's 32 rows t
+      // (4) Dm' = diag(dk) Dm as hi + lo A operands (into the S operand
+      // columns, free until the new state is copied) and Dm_hi for the output
+      // (into R's columns); this thread's 32 rows t
       to |= !mbar_wait(&bar_m3, ph);
       tc::fence_after_sync();
-      if (tid == 0 && more) load_tm(k + 1);
+      if (tid == 0 && more) load_tb(k + 1);
       {
         float dm[32];
 #pragma unroll
         for (int m = 0; m < 2; ++m)
-          tc::tmem_ld16(tl + kq + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(dm + 16 * m));
+          tc::tmem_ld16(tl + TM_KQ + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(dm + 16 * m));
         tc::tmem_wait_ld();
+        uint32_t hw[16], lw[16], dw[16];
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          float x[16];
+        for (int m = 0; m < 16; ++m) dw[m] = pack_bf16(dm[2 * m], dm[2 * m + 1]);
+        tc::tmem_st16u(tl + TM_RHI + 16 * ch, dw);
 #pragma unroll
-          for (int e4 = 0; e4 < 4; ++e4) {
-            const float4 d4 = reinterpret_cast<const float4*>(vec + kC)[8 * ch + 4 * m + e4];
-            x[4 * e4] = d4.x * dm[16 * m + 4 * e4];
-            x[4 * e4 + 1] = d4.y * dm[16 * m + 4 * e4 + 1];
-            x[4 * e4 + 2] = d4.z * dm[16 * m + 4 * e4 + 2];
-            x[4 * e4 + 3] = d4.w * dm[16 * m + 4 * e4 + 3];
-          }
-          uint4 h0, l0, h1, l1;
-          split8(x, h0, l0);
-          split8(x + 8, h1, l1);
-          const int c = 4 * ch + 2 * m;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, c, 128)) = h0;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RHI + sw_chunk(j, c + 1, 128)) = h1;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, c, 128)) = l0;
-          *reinterpret_cast<uint4*>(sm + C_OFF_RLO + sw_chunk(j, c + 1, 128)) = l1;
-          const float* d = dm + 16 * m;
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc)
-            *reinterpret_cast<uint4*>(sm + C_OFF_DMH + sw_chunk(j, c + cc, 128)) =
-                make_uint4(pack_bf16(d[8 * cc], d[8 * cc + 1]), pack_bf16(d[8 * cc + 2], d[8 * cc + 3]),
-                           pack_bf16(d[8 * cc + 4], d[8 * cc + 5]),
-                           pack_bf16(d[8 * cc + 6], d[8 * cc + 7]));
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 d4 = reinterpret_cast<const float4*>(vec + kC)[8 * ch + e4];
+          const float x0 = d4.x * dm[4 * e4], x1 = d4.y * dm[4 * e4 + 1];
+          const float x2 = d4.z * dm[4 * e4 + 2], x3 = d4.w * dm[4 * e4 + 3];
+          const __nv_bfloat162 h01 = __floats2bfloat162_rn(x0, x1), h23 = __floats2bfloat162_rn(x2, x3);
+          hw[2 * e4] = *reinterpret_cast<const uint32_t*>(&h01);
+          hw[2 * e4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+          lw[2 * e4] = pack_bf16(x0 - __low2float(h01), x1 - __high2float(h01));
+          lw[2 * e4 + 1] = pack_bf16(x2 - __low2float(h23), x3 - __high2float(h23));
         }
+        tc::tmem_st16u(tl + TM_SHI + 16 * ch, hw);
+        tc::tmem_st16u(tl + TM_SLO + 16 * ch, lw);
+        tc::tmem_wait_st();
       }
-      fence_proxy_async_smem();
       tc::fence_before_sync();
       if (bar_or(1, kCarryThreads, to)) break;
 
@@ -761,31 +784,27 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       // the output only, Dm^T P^T
       if (tid == 0) {
         if (k + 2 < nch) load_vec(k + 2);  // this parity's vector block is consumed
+        to |= !mbar_wait(&bar_kt, ph);
         to |= !mbar_wait(&bar_p, ph);
         tc::fence_after_sync();
 #pragma unroll
         for (int part = 0; part < 2; ++part)
 #pragma unroll
           for (int s = 0; s < 4; ++s)
-            tc::mma_f16(tb + TM_S, tc::sdesc_at(part ? d_rlo : d_rhi, 128, s),
-                        tc::sdesc_at(d_kt, 128, s), id128, true);
+            tc::mma_f16_ts(tb + TM_S, tb + (part ? TM_SLO : TM_SHI) + 8 * s,
+                           tc::sdesc_at(d_kt, 128, s), id128, true);
         tc::mma_commit(&bar_m5);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          tc::mma_f16(tb + TM_OP + 64u * (uint32_t)(k & 1), tc::sdesc_at(d_dmh, 128, s),
-                      tc::sdesc_at(d_p, 64, s), id64, s > 0);
-        tc::mma_commit(&bar_of[k & 1]);  // S_hi Q^T and Dm^T P^T of this chunk
+          tc::mma_f16_ts(tb + TM_OP, tb + TM_RHI + 8 * s, tc::sdesc_at(d_p, 64, s), id64, s > 0);
+        tc::mma_commit(&bar_of);  // OQ and OP of this chunk
       }
 
-      // (6) the new state: operand copies, decay of the next chunk applied in
-      // TMEM; after the last chunk, back to global memory (columns 64 ch..)
+      // (6) the new state: operand copies and the next chunk's decay in TMEM;
+      // after the last chunk, back to global memory
       to |= !mbar_wait(&bar_m5, ph);
       tc::fence_after_sync();
-      float gl = 1.f;
-      if (more) {
-        to |= !mbar_wait(&bar_vec[(k + 1) & 1], (uint32_t)(((k + 1) >> 1) & 1));
-        gl = reinterpret_cast<const float*>(sm + C_OFF_VEC + ((k + 1) & 1) * 1024)[3 * kC];
-      }
+      if (tid == 0 && more) load_kt(k + 1);
       {
         float v[kC];
 #pragma unroll
@@ -798,97 +817,89 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           for (int m = 0; m < 16; ++m)
             dst[m] = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
         } else {
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 hi, lo;
-            split8(v + 8 * c, hi, lo);
-            *reinterpret_cast<uint4*>(sm + C_OFF_SHI + sw_chunk(j, 8 * ch + c, 128)) = hi;
-            *reinterpret_cast<uint4*>(sm + C_OFF_SLO + sw_chunk(j, 8 * ch + c, 128)) = lo;
-          }
-#pragma unroll
-          for (int e = 0; e < kC; ++e) v[e] *= gl;
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-            tc::tmem_st16(tl + TM_S + 64 * ch + 16 * m, *reinterpret_cast<const float(*)[16]>(v + 16 * m));
+          to |= !mbar_wait(&bar_vec[(k + 1) & 1], (uint32_t)(((k + 1) >> 1) & 1));
+          store_state(v, reinterpret_cast<const float*>(sm + C_OFF_VEC + ((k + 1) & 1) * 1024)[3 * kC]);
+          tc::tmem_wait_st();
         }
       }
-      tc::tmem_wait_st();
-      fence_proxy_async_smem();
       tc::fence_before_sync();
       if (tid == 0 && more) {
-        // P and K^T of this chunk are free once its Dm^T P^T has completed
-        to |= !mbar_wait(&bar_of[k & 1], (uint32_t)((k >> 1) & 1));
-        load_pk(k + 1);
+        // P of this chunk is free once Dm^T P^T has completed
+        to |= !mbar_wait(&bar_of, ph);
+        load_p(k + 1);
       }
     }
   } else {
     // ============================ output group: 8 warps; thread (j, half)
     // owns output column j = 32 (warp % 4) + lane for the 32 rows of its half.
-    // O = diag(gq) OQ + OP from TMEM; with the fused norm, the per-row sums of
-    // squares are reduce-scattered across lanes, z arrives by TMA into a
-    // row-major tile that the gated result then overwrites in place, and each
-    // live row leaves as one 256-byte bulk store.
+    // O = diag(gq) OQ + OP is read from TMEM once (then TMEM is released to
+    // the next chunk); with the fused norm, the per-row sums of squares are
+    // reduce-scattered across lanes, z arrives by TMA into a row-major tile
+    // (two, by chunk parity) that the gated result overwrites in place, and
+    // each live row leaves as one 256-byte bulk store.
     constexpr int kOut = kChainThreads - kCarryThreads;
     const int u = tid - kCarryThreads, q4 = warp & 3, half = (warp - 8) >> 2;
     const int j = 32 * q4 + lane, t0 = 32 * half;
     const uint32_t tl = tb + ((uint32_t)(32 * q4) << 16);
     const float nwj = fused ? p.norm_w[j] : 0.f;
-    __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(sm + C_OFF_Z);
-    uint32_t n_z = 0;
+    uint32_t n_z0 = 0, n_z1 = 0;
     bool stored = false;
     auto load_z = [&](int k) {
-      ++n_z;
-      mbar_arrive_expect_tx(&bar_z, 16384u);
-      tc::tma_load_2d(sm + C_OFF_Z, &tm_z, h * kD, (int)chunk_c0(k), &bar_z);
+      if (k & 1) ++n_z1; else ++n_z0;
+      mbar_arrive_expect_tx(&bar_z[k & 1], 16384u);
+      tc::tma_load_2d(sm + C_OFF_Z + (k & 1) * 16384, &tm_z, h * kD, (int)chunk_c0(k), &bar_z[k & 1]);
     };
-    if (fused && u == 0) load_z(0);
+    if (fused && u == 0) {
+      load_z(0);
+      if (nch > 1) load_z(1);
+    }
+    bool to = false;  // a bounded wait gave up (agreed on at the next barrier)
     for (int k = 0; k < nch; ++k) {
       const int64_t c0 = chunk_c0(k);
       const int L = (int)((seq_e - c0) < kC ? (seq_e - c0) : kC);
-      const uint32_t oq = TM_KQ + 128u * (uint32_t)(k & 1) + 64u + (uint32_t)t0;
-      const uint32_t op = TM_OP + 64u * (uint32_t)(k & 1) + (uint32_t)t0;
       const float* gq = sgq[k & 1] + t0;
+      __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(sm + C_OFF_Z + (k & 1) * 16384);
       if (u < kC) sgq[k & 1][u] = __ldg(w.vec + slot_of(k) * (4 * kC) + 2 * kC + u);
-      bool to = !mbar_wait(&bar_of[k & 1], (uint32_t)((k >> 1) & 1));
+      to |= !mbar_wait(&bar_of, (uint32_t)(k & 1));
       if (bar_or(2, kOut, to)) break;
       tc::fence_after_sync();
-      // pass 1: core output and per-row squares
-      float sq[32];
+      float o[32];
       {
         float a[2][16], b[2][16];
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-          tc::tmem_ld16(tl + oq + 16 * m, a[m]);
-          tc::tmem_ld16(tl + op + 16 * m, b[m]);
+          tc::tmem_ld16(tl + TM_KQ + 64 + t0 + 16 * m, a[m]);
+          tc::tmem_ld16(tl + TM_OP + t0 + 16 * m, b[m]);
         }
         tc::tmem_wait_ld();
-        float o[32];
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            o[16 * m + e] = fmaf(gq[16 * m + e], a[m][e], b[m][e]);
-            sq[16 * m + e] = o[16 * m + e] * o[16 * m + e];
-          }
-        if (p.core_out != nullptr) {
-          float* cg = p.core_out + ((c0 + t0) * p.Hv + h) * kD + j;
-          const int64_t cstr = (int64_t)p.Hv * kD;
-          if (L == kC) {
+          for (int e = 0; e < 16; ++e) o[16 * m + e] = fmaf(gq[16 * m + e], a[m][e], b[m][e]);
+      }
+      tc::fence_before_sync();
+      mbar_arrive(&bar_oe);  // this chunk's output accumulators are free
+      if (p.core_out != nullptr) {
+        float* cg = p.core_out + ((c0 + t0) * p.Hv + h) * kD + j;
+        const int64_t cstr = (int64_t)p.Hv * kD;
+        if (L == kC) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) cg[e * cstr] = o[e];
-          } else {
+          for (int e = 0; e < 32; ++e) cg[e * cstr] = o[e];
+        } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (t0 + e < L) cg[e * cstr] = o[e];
-          }
+          for (int e = 0; e < 32; ++e)
+            if (t0 + e < L) cg[e * cstr] = o[e];
         }
       }
-      if (!fused) {
-        tc::fence_before_sync();
-        mbar_arrive(&bar_oe[k & 1]);
-        continue;
-      }
+      if (!fused) continue;
+      // the bulk stores of two chunks ago have read their tile: reload it
+      if (stored) bulk_wait_read_all();
+      if (bar_or(2, kOut, to)) break;
+      if (u == 0 && k >= 1 && k + 1 < nch) load_z(k + 1);
       // five halving exchanges: lane l ends with the sum of row t0 + l
+      float sq[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) sq[e] = o[e] * o[e];
 #pragma unroll
       for (int st = 0; st < 5; ++st) {
         const int m = 16 >> st, hv = 16 >> st;
@@ -905,45 +916,31 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       if (u < kC)
         sinv[u] = 1.f / sqrtf((spart[0][u] + spart[1][u] + spart[2][u] + spart[3][u]) / (float)kD +
                               p.rms_eps);
-      to = !mbar_wait(&bar_z, (uint32_t)(k & 1));
+      to |= !mbar_wait(&bar_z[k & 1], (uint32_t)((k >> 1) & 1));
       bar_named(2, kOut);
-      // pass 2: the gated result over z, in place (rows >= L hold finite
-      // values that are never stored)
-      {
-        float a[2][16], b[2][16];
+      // the gated result over z, in place (rows >= L hold finite values that
+      // are never stored)
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          tc::tmem_ld16(tl + oq + 16 * m, a[m]);
-          tc::tmem_ld16(tl + op + 16 * m, b[m]);
-        }
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int t = t0 + 16 * m + e;
-            const float o = fmaf(gq[16 * m + e], a[m][e], b[m][e]);
-            const float zf = __bfloat162float(zb[t * kD + j]);
-            const float gate = __fdividef(zf, 1.f + __expf(-zf));
-            zb[t * kD + j] = __float2bfloat16_rn(o * sinv[t] * nwj * gate);
-          }
+      for (int e = 0; e < 32; ++e) {
+        const int t = t0 + e;
+        const float zf = __bfloat162float(zb[t * kD + j]);
+        const float gate = __fdividef(zf, 1.f + __expf(-zf));
+        zb[t * kD + j] = __float2bfloat16_rn(o[e] * sinv[t] * nwj * gate);
       }
-      tc::fence_before_sync();
-      mbar_arrive(&bar_oe[k & 1]);  // this chunk's output accumulators are free
       fence_proxy_async_smem();
       bar_named(2, kOut);
       if (u < L) {
         bulk_store(static_cast<__nv_bfloat16*>(p.out) + ((c0 + u) * p.Hv + h) * kD, zb + u * kD,
                    (uint32_t)(kD * 2));
         bulk_commit();
-        bulk_wait_read_all();
         stored = true;
       }
-      if (bar_or(2, kOut, to)) break;  // every row has left the staging tile
-      if (u == 0 && k + 1 < nch) load_z(k + 1);
     }
     if (stored) bulk_wait_all();
-    if (u == 0 && n_z) mbar_wait(&bar_z, (n_z - 1) & 1);
+    if (u == 0) {
+      if (n_z0) mbar_wait(&bar_z[0], (n_z0 - 1) & 1);
+      if (n_z1) mbar_wait(&bar_z[1], (n_z1 - 1) & 1);
+    }
   }
 
   // drain: every copy and MMA this CTA issued has completed before it exits
@@ -957,8 +954,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     mbar_wait(&bar_fin, 0);
     if (n_kq) mbar_wait(&bar_kq, (n_kq - 1) & 1);
     if (n_v) mbar_wait(&bar_v, (n_v - 1) & 1);
-    if (n_tm) mbar_wait(&bar_tm, (n_tm - 1) & 1);
+    if (n_tb) mbar_wait(&bar_tb, (n_tb - 1) & 1);
     if (n_p) mbar_wait(&bar_p, (n_p - 1) & 1);
+    if (n_kt) mbar_wait(&bar_kt, (n_kt - 1) & 1);
     if (n_vec0) mbar_wait(&bar_vec[0], (n_vec0 - 1) & 1);
     if (n_vec1) mbar_wait(&bar_vec[1], (n_vec1 - 1) & 1);
     tc::fence_before_sync();
@@ -977,7 +975,7 @@ int64_t prefill_cp_workspace_bytes(int32_t N, int64_t T, int32_t Hk, int32_t Hv)
 }
 
 bool prefill_cp_supported(const PrefillArgs& p, int32_t dtype, int32_t D) {
-  if (D != kD || dtype != GDN_BF16) return false;
+  if (D != kD || dtype != GDN_BF16 || p.rep > kMaxRep) return false;
   if (p.T >= ((int64_t)1 << 31)) return false;  // TMA row coordinates are int32
   const CpLayout l = cp_layout(p.N, p.T, p.Hk, p.Hv);
   if ((double)l.G * p.Hv * kC * 3 >= 2147483647.0) return false;

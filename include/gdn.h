@@ -175,7 +175,8 @@ gdn_status gdn_decode_step(const gdn_dims* dims, int32_t batch, const void* mixe
  *              garbage afterwards. May be NULL (workspace_bytes ignored).
  *
  * Which kernels run (all on the given stream):
- *  - head_dim 128, bf16, a workspace: the chunk-parallel tensor-core path.
+ *  - head_dim 128, bf16, Hv/Hk <= 8, a workspace: the chunk-parallel
+ *    tensor-core path.
  *    Every chunk's state-free factors (the K and QK grams, (I+A)^-1 diag(beta),
  *    the masked decayed QK^T) are computed at once into the workspace, then
  *    one CTA per (V head, sequence) carries the state through its chunks with
@@ -197,8 +198,8 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int
 
 /*
  * Bytes of workspace gdn_prefill_chunked can use for these sizes and flags
- * (0 when no workspace path applies: head_dim != 128, io dtype not bf16, or
- * GDN_PREFILL_CUDA_CORES): per 64-token chunk slot ((T + 63 N) / 64 of
+ * (0 when no workspace path applies: head_dim != 128, io dtype not bf16,
+ * more than 8 V heads per K head, or GDN_PREFILL_CUDA_CORES): per 64-token chunk slot ((T + 63 N) / 64 of
  * them) 25 KB per V head and 16 KB per K head, plus 4 (N + 1) bytes rounded
  * up to 1 KB. Writes the size to *bytes; GDN_ERR_INVALID_ARG /
  * GDN_ERR_EXTENT for invalid dims or sizes.
