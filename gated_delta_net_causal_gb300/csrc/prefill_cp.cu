@@ -173,14 +173,13 @@ __global__ void __launch_bounds__(1024) cp_index_kernel(const PrefillArgs p, con
 
 // ------------------------------------------------------------------ prep
 
-constexpr uint32_t P_OFF_K = 0;        // bf16 [64][128] SW128 (TMA)
-constexpr uint32_t P_OFF_Q = 16384;    // bf16 [64][128] SW128 (TMA)
+constexpr uint32_t P_OFF_KQ = 0;       // bf16 [128][128 i] SW128 (TMA): rows 0-63 k, 64-127 q
 constexpr uint32_t P_OFF_A = 32768;    // fp32 [64][65]
 constexpr uint32_t P_OFF_T = 49408;    // fp32 [64][64] Tm
 constexpr uint32_t P_OFF_X = 65792;    // fp32 [768] block-product scratch
 constexpr uint32_t P_SMEM = 68864 + 1024;
 
-__global__ void __launch_bounds__(kPrepThreads, 2)
+__global__ void __launch_bounds__(kPrepThreads, 3)
     cp_prep_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -191,7 +190,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   __shared__ __align__(8) uint64_t bar_ld, bar_gp;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int qd = warp & 3, hh = warp >> 2;
+  const int qd = warp & 3;
   const int64_t g = blockIdx.x;
   const int kh = blockIdx.y;
   const int64_t total = w.cs[p.N] < w.G ? w.cs[p.N] : w.G;
@@ -211,7 +210,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   const bool pregate = (p.flags & GDN_GATES_PRECOMPUTED) != 0;
 
   if (warp == 0) {
-    tc::tmem_alloc(&s_tmem, 128);
+    tc::tmem_alloc(&s_tmem, 64);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
@@ -219,10 +218,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     mbar_init(&bar_gp, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(&bar_ld, 32768u);
-    tc::tma_load_2d(sm + P_OFF_K, &tm_k, kh * kD, (int)c0, &bar_ld);
-    tc::tma_load_2d(sm + P_OFF_K + 8192, &tm_k, kh * kD + 64, (int)c0, &bar_ld);
-    tc::tma_load_2d(sm + P_OFF_Q, &tm_q, kh * kD, (int)c0, &bar_ld);
-    tc::tma_load_2d(sm + P_OFF_Q + 8192, &tm_q, kh * kD + 64, (int)c0, &bar_ld);
+    tc::tma_load_2d(sm + P_OFF_KQ, &tm_k, kh * kD, (int)c0, &bar_ld);
+    tc::tma_load_2d(sm + P_OFF_KQ + 16384, &tm_k, kh * kD + 64, (int)c0, &bar_ld);
+    tc::tma_load_2d(sm + P_OFF_KQ + 8192, &tm_q, kh * kD, (int)c0, &bar_ld);
+    tc::tma_load_2d(sm + P_OFF_KQ + 24576, &tm_q, kh * kD + 64, (int)c0, &bar_ld);
   }
   // raw gate inputs of every V head reading this K head, fetched while the
   // k and q tiles are in flight
@@ -248,18 +247,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   tc::fence_after_sync();
   const uint32_t tb = s_tmem;
   const uint32_t tq = tb + ((uint32_t)(32 * qd) << 16);
-  const uint32_t a_k = smem_u32(sm + P_OFF_K), a_q = smem_u32(sm + P_OFF_Q);
+  const uint64_t d_kq = tc::sdesc_sw128(smem_u32(sm + P_OFF_KQ));
 
   bool to = !mbar_wait(&bar_ld, 0);
   if (tid == 0 && !to) {
     tc::fence_after_sync();
-    const uint32_t id = tc::idesc(tc::kBF16, 64, 64);
+    // [k; q] k^T as one M=128 accumulator: rows 0-63 K K^T, rows 64-127 Q K^T
+    const uint32_t id = tc::idesc(tc::kBF16, 128, 64);
 #pragma unroll
     for (int s = 0; s < 8; ++s)
-      tc::mma_f16(tb, tc::sdesc_kstep(a_k, 64, s), tc::sdesc_kstep(a_k, 64, s), id, s > 0);
-#pragma unroll
-    for (int s = 0; s < 8; ++s)
-      tc::mma_f16(tb + 64, tc::sdesc_kstep(a_q, 64, s), tc::sdesc_kstep(a_k, 64, s), id, s > 0);
+      tc::mma_f16(tb, tc::sdesc_at(d_kq, 128, s), tc::sdesc_at(d_kq, 128, s), id, s > 0);
     tc::mma_commit(&bar_gp);
   }
   // l2 scales of k and q rows, four threads per row, 16 bytes at a time
@@ -269,9 +266,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int c16 = part + 4 * m;
-      const uint32_t off = sw_chunk(srow, c16, 64);
-      const uint4 kr = *reinterpret_cast<const uint4*>(sm + P_OFF_K + off);
-      const uint4 qr = *reinterpret_cast<const uint4*>(sm + P_OFF_Q + off);
+      const uint4 kr = *reinterpret_cast<const uint4*>(sm + P_OFF_KQ + sw_chunk(srow, c16, 128));
+      const uint4 qr = *reinterpret_cast<const uint4*>(sm + P_OFF_KQ + sw_chunk(64 + srow, c16, 128));
       const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&kr);
       const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&qr);
 #pragma unroll
@@ -295,7 +291,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   // (i, half) gathers 32 rows t of column i
   {
     const int i = tid >> 1, th = tid & 1;
-    const uint32_t col = (uint32_t)((i >> 6) * 8192 + (i & 7) * 2);
+    const uint32_t col = (uint32_t)((i >> 6) * 16384 + (i & 7) * 2);
     const int ic = (i & 63) >> 3;
     uint32_t wv[16];
 #pragma unroll
@@ -305,7 +301,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       for (int q = 0; q < 2; ++q) {
         const int t = 32 * th + 2 * t2 + q;
         const uint32_t off = col + (uint32_t)((t >> 3) * 1024 + (t & 7) * 128 + ((ic ^ (t & 7)) << 4));
-        const uint32_t x = *reinterpret_cast<const unsigned short*>(sm + P_OFF_K + off);
+        const uint32_t x = *reinterpret_cast<const unsigned short*>(sm + P_OFF_KQ + off);
         pr |= (t < L ? x : 0u) << (16 * q);
       }
       wv[t2] = pr;
@@ -318,18 +314,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   if (__syncthreads_or(to)) {
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tb, 128);
+    if (warp == 0) tc::tmem_dealloc(tb, 64);
     return;
   }
   tc::fence_after_sync();
-  // the grams of this K head, once for all its V heads (rows of the M=64
-  // accumulator live in lanes 16 qd + 0..15 of quadrant qd)
-  float gv[32], pv[32];
-  tc::tmem_ld16(tq + 32 * hh, *reinterpret_cast<float(*)[16]>(gv));
-  tc::tmem_ld16(tq + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(gv + 16));
-  tc::tmem_ld16(tq + 64 + 32 * hh, *reinterpret_cast<float(*)[16]>(pv));
-  tc::tmem_ld16(tq + 64 + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(pv + 16));
-  tc::tmem_wait_ld();
 
   float* Ap = reinterpret_cast<float*>(sm + P_OFF_A);
   float* Tp = reinterpret_cast<float*>(sm + P_OFF_T);
@@ -367,27 +355,45 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     if (warp == 1) sc[tid] += sc[31];
     __syncthreads();
     if (tid < kC) sgam[tid] = expf(sc[tid]);
-    // A (padded rows) and P (bf16, straight to the workspace)
-    if (lane < 16) {
-      const int t = 16 * qd + lane;
+    // A (padded rows) and P (bf16, straight to the workspace) from the grams
+    // of this K head, read again for each V head: thread (row, half) takes
+    // 32 columns of row `row` of the M=128 accumulator (lane = row), A for
+    // rows 0-63 and P for rows 64-127
+    {
+      const int row = tid & 127, hc = tid >> 7;
+      float gv[32];
+      tc::tmem_ld16(tq + 32 * hc, *reinterpret_cast<float(*)[16]>(gv));
+      tc::tmem_ld16(tq + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(gv + 16));
+      tc::tmem_wait_ld();
+      const bool is_a = row < kC;  // warp-uniform
+      const int t = is_a ? row : row - kC;
       const bool live = t < L;
       constexpr float kLog2e = 1.4426950408889634f;
-      const float ct = sc[t] * kLog2e, bt = sbeta[t], ikt = sinvk[t], iqt = sinvq[t];
-      float pr[32];
+      const float ct = sc[t] * kLog2e;
+      if (is_a) {
+        const float bk = sbeta[t] * sinvk[t];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int s = 32 * hh + e;
-        const float dec = exp2f(ct - sc[s] * kLog2e);  // e^{c_t - c_s} <= 1 for s <= t
-        const float ks = sinvk[s];
-        Ap[t * kAStride + s] = (live && s < t) ? bt * dec * gv[e] * ikt * ks : 0.f;
-        pr[e] = (live && s <= t) ? dec * pv[e] * iqt * ks : 0.f;
+        for (int e = 0; e < 32; ++e) {
+          const int s = 32 * hc + e;
+          const float dec = exp2f(ct - sc[s] * kLog2e);  // e^{c_t - c_s} <= 1 for s <= t
+          Ap[t * kAStride + s] = (live && s < t) ? bk * dec * gv[e] * sinvk[s] : 0.f;
+        }
+      } else {
+        const float iqt = sinvq[t];
+        float pr[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int s = 32 * hc + e;
+          const float dec = exp2f(ct - sc[s] * kLog2e);
+          pr[e] = (live && s <= t) ? dec * gv[e] * iqt * sinvk[s] : 0.f;
+        }
+        uint4* dst = reinterpret_cast<uint4*>(w.tw + ((2 * HvG + slot) * kC + t) * kC + 32 * hc);
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          dst[m] = make_uint4(pack_bf16(pr[8 * m], pr[8 * m + 1]), pack_bf16(pr[8 * m + 2], pr[8 * m + 3]),
+                              pack_bf16(pr[8 * m + 4], pr[8 * m + 5]),
+                              pack_bf16(pr[8 * m + 6], pr[8 * m + 7]));
       }
-      uint4* dst = reinterpret_cast<uint4*>(w.tw + ((2 * HvG + slot) * kC + t) * kC + 32 * hh);
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        dst[m] = make_uint4(pack_bf16(pr[8 * m], pr[8 * m + 1]), pack_bf16(pr[8 * m + 2], pr[8 * m + 3]),
-                            pack_bf16(pr[8 * m + 4], pr[8 * m + 5]),
-                            pack_bf16(pr[8 * m + 6], pr[8 * m + 7]));
     }
     __syncthreads();
     // (I + A)^{-1}: diagonal 16x16 blocks by forward substitution (warp b,
@@ -412,28 +418,51 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       }
     }
     __syncthreads();
+    // off-diagonal blocks, one block diagonal d at a time, 64 threads per
+    // block and a 2 x 2 output tile per thread:
+    //   X = sum_{kb=jb}^{ib-1} A_{ib,kb} T_{kb,jb},  T_{ib,jb} = -T_{ib,ib} X
     for (int d = 1; d < 4; ++d) {
       const int nblk = 4 - d;
-      for (int e = tid; e < nblk * 256; e += kPrepThreads) {
-        const int jb = e >> 8, rr = (e >> 4) & 15, cc = e & 15, ib = jb + d;
-        float acc = 0.f;
-        for (int kb = jb; kb < ib; ++kb) {
-          const float* arow = Ap + (16 * ib + rr) * kAStride + 16 * kb;
-          const float* tcol = Tp + (16 * kb) * kC + 16 * jb + cc;
+      const int jb = tid >> 6, q = tid & 63, r0 = (q >> 3) * 2, c0 = (q & 7) * 2, ib = jb + d;
+      const bool act = tid < nblk * 64;
+      if (act) {
+        const float* a0 = Ap + (16 * ib + r0) * kAStride + 16 * jb;
+        const float* a1 = a0 + kAStride;
+        const float* tc0 = Tp + (16 * jb) * kC + 16 * jb + c0;
+        float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+        for (int kk = 0; kk < 16 * d; kk += 16) {
 #pragma unroll
-          for (int m = 0; m < 16; ++m) acc = fmaf(arow[m], tcol[m * kC], acc);
+          for (int k = 0; k < 16; ++k) {
+            const float2 tv = *reinterpret_cast<const float2*>(tc0 + (kk + k) * kC);
+            const float av0 = a0[kk + k], av1 = a1[kk + k];
+            x00 = fmaf(av0, tv.x, x00);
+            x01 = fmaf(av0, tv.y, x01);
+            x10 = fmaf(av1, tv.x, x10);
+            x11 = fmaf(av1, tv.y, x11);
+          }
         }
-        Xp[e] = acc;
+        float* xb = Xp + (jb << 8) + r0 * 16 + c0;
+        *reinterpret_cast<float2*>(xb) = make_float2(x00, x01);
+        *reinterpret_cast<float2*>(xb + 16) = make_float2(x10, x11);
       }
       __syncthreads();
-      for (int e = tid; e < nblk * 256; e += kPrepThreads) {
-        const int jb = e >> 8, rr = (e >> 4) & 15, cc = e & 15, ib = jb + d;
-        const float* trow = Tp + (16 * ib + rr) * kC + 16 * ib;
-        const float* xcol = Xp + (jb << 8) + cc;
-        float acc = 0.f;
+      if (act) {
+        const float* t0 = Tp + (16 * ib + r0) * kC + 16 * ib;
+        const float* t1 = t0 + kC;
+        const float* xb = Xp + (jb << 8) + c0;
+        float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc = (m <= rr) ? fmaf(trow[m], xcol[m << 4], acc) : acc;
-        Tp[(16 * ib + rr) * kC + 16 * jb + cc] = -acc;
+        for (int m = 0; m < 16; ++m) {
+          const float2 xv = *reinterpret_cast<const float2*>(xb + m * 16);
+          const float tv0 = m <= r0 ? t0[m] : 0.f, tv1 = m <= r0 + 1 ? t1[m] : 0.f;
+          y00 = fmaf(tv0, xv.x, y00);
+          y01 = fmaf(tv0, xv.y, y01);
+          y10 = fmaf(tv1, xv.x, y10);
+          y11 = fmaf(tv1, xv.y, y11);
+        }
+        float* tout = Tp + (16 * ib + r0) * kC + 16 * jb + c0;
+        *reinterpret_cast<float2*>(tout) = make_float2(-y00, -y01);
+        *reinterpret_cast<float2*>(tout + kC) = make_float2(-y10, -y11);
       }
       __syncthreads();
     }
@@ -470,7 +499,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tb, 128);
+  if (warp == 0) tc::tmem_dealloc(tb, 64);
 }
 
 // ----------------------------------------------------------------- carry
