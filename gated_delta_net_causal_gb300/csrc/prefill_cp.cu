@@ -506,14 +506,15 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
 
 // shared memory (byte offsets from a 1024-aligned base)
 constexpr uint32_t C_OFF_KQ = 0;         // bf16 [128][128 i] SW128 (TMA): rows 0-63 k, 64-127 q
-constexpr uint32_t C_OFF_KT = 32768;     // bf16 [128 i][64 t] SW128 (TMA, k transposed by prep)
-constexpr uint32_t C_OFF_TMH = 49152;    // bf16 [64 t][64 s] SW128 (TMA): Tb hi
-constexpr uint32_t C_OFF_TML = 57344;    // Tb lo
-constexpr uint32_t C_OFF_P = 65536;      // P
-constexpr uint32_t C_OFF_V = 73728;      // bf16 [64 s][128 j] row-major (TMA)
-constexpr uint32_t C_OFF_VEC = 90112;    // fp32 [2][4][64] (bulk copy), by chunk parity
-constexpr uint32_t C_OFF_Z = 92160;      // bf16 [2][64 t][128 j] row-major: z (TMA), then out
-constexpr uint32_t C_SMEM = 124928 + 1024;
+constexpr uint32_t C_OFF_KT = 32768;     // bf16 [2][128 i][64 t] SW128 (TMA, k transposed by prep)
+constexpr uint32_t C_OFF_TMH = 65536;    // bf16 [64 t][64 s] SW128 (TMA): Tb hi
+constexpr uint32_t C_OFF_TML = 73728;    // Tb lo
+constexpr uint32_t C_OFF_P = 81920;      // bf16 [2][64 t][64 s] SW128 (TMA): P
+constexpr uint32_t C_OFF_V = 98304;      // bf16 [64 s][128 j] row-major (TMA)
+constexpr uint32_t C_OFF_VEC = 114688;   // fp32 [2][4][64] (bulk copy), by chunk parity
+constexpr uint32_t C_OFF_Z = 116736;     // bf16 [2][64 t][128 j] row-major: z (TMA), then out
+constexpr uint32_t C_SMEM = 149504 + 1024;
+// K^T and P are double-buffered by chunk parity and loaded a chunk ahead
 
 // TMEM columns. The A operands of the MMAs live in TMEM as packed bf16 pairs
 // (row j in lane j, K elements 2c, 2c+1 in column c).
@@ -529,8 +530,9 @@ constexpr uint32_t TM_COLS = 512;
 // Loads are issued by thread 0 as soon as the buffer's last reader is known
 // to be done (every MMA a commit covers has completed):
 //   K, Q after S [k; q]^T (bar_m1)     V   after R is written
-//   Tb   after R Tb^T (bar_m3)         P   after Dm^T P^T (bar_of)
-//   K^T  after the update (bar_m5)     vec two chunks ahead, by parity
+//   Tb   after R Tb^T (bar_m3)         vec two chunks ahead, by parity
+//   P, K^T of chunk k+1 into the buffers of chunk k-1 once S [k; q]^T has
+//   completed (its commit covers chunk k-1's update and Dm^T P^T)
 // The output group reads [KS | OQ] and OP of chunk k; thread 0 waits for it
 // (bar_oe) before chunk k+1 writes them.
 __global__ void __launch_bounds__(kChainThreads, 1)
@@ -540,7 +542,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
                     const __grid_constant__ CUtensorMap tm_kt) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) uint64_t bar_kq, bar_v, bar_tb, bar_p, bar_kt, bar_m1, bar_m3, bar_m5;
+  __shared__ __align__(8) uint64_t bar_kq, bar_v, bar_tb, bar_p[2], bar_kt[2], bar_m1, bar_m3, bar_m5;
   __shared__ __align__(8) uint64_t bar_vec[2], bar_of, bar_oe, bar_fin, bar_z[2];
   __shared__ uint32_t s_tmem;
   __shared__ float spart[4][kC];
@@ -570,8 +572,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     mbar_init(&bar_kq, 1);
     mbar_init(&bar_v, 1);
     mbar_init(&bar_tb, 1);
-    mbar_init(&bar_p, 1);
-    mbar_init(&bar_kt, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_p[b], 1);
+      mbar_init(&bar_kt[b], 1);
+    }
     mbar_init(&bar_m1, 1);
     mbar_init(&bar_m3, 1);
     mbar_init(&bar_m5, 1);
@@ -590,7 +594,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   const uint32_t tb = s_tmem;
 
   // thread 0's loads; the counts let the exit path wait for copies in flight
-  uint32_t n_kq = 0, n_v = 0, n_tb = 0, n_p = 0, n_kt = 0, n_vec0 = 0, n_vec1 = 0;
+  uint32_t n_kq = 0, n_v = 0, n_tb = 0, n_pk0 = 0, n_pk1 = 0, n_vec0 = 0, n_vec1 = 0;
   auto chunk_c0 = [&](int k) { return seq_s + (int64_t)kC * k; };
   auto slot_of = [&](int k) { return (size_t)(kb + k) * p.Hv + h; };
   auto load_kq = [&](int k) {
@@ -614,15 +618,14 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     tc::tma_load_2d(sm + C_OFF_TMH, &tm_w, 0, (int)(slot * kC), &bar_tb);
     tc::tma_load_2d(sm + C_OFF_TML, &tm_w, 0, (int)((HvG + slot) * kC), &bar_tb);
   };
-  auto load_p = [&](int k) {
-    ++n_p;
-    mbar_arrive_expect_tx(&bar_p, 8192u);
-    tc::tma_load_2d(sm + C_OFF_P, &tm_w, 0, (int)((2 * HvG + slot_of(k)) * kC), &bar_p);
-  };
-  auto load_kt = [&](int k) {
-    ++n_kt;
-    mbar_arrive_expect_tx(&bar_kt, 16384u);
-    tc::tma_load_2d(sm + C_OFF_KT, &tm_kt, 0, (int)(((kb + k) * p.Hk + kh) * kD), &bar_kt);
+  auto load_pk = [&](int k) {
+    const int b = k & 1;
+    if (b) ++n_pk1; else ++n_pk0;
+    mbar_arrive_expect_tx(&bar_p[b], 8192u);
+    tc::tma_load_2d(sm + C_OFF_P + b * 8192, &tm_w, 0, (int)((2 * HvG + slot_of(k)) * kC), &bar_p[b]);
+    mbar_arrive_expect_tx(&bar_kt[b], 16384u);
+    tc::tma_load_2d(sm + C_OFF_KT + b * 16384, &tm_kt, 0, (int)(((kb + k) * p.Hk + kh) * kD),
+                    &bar_kt[b]);
   };
   auto load_vec = [&](int k) {
     uint64_t* bar = &bar_vec[k & 1];
@@ -634,8 +637,8 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     load_kq(0);
     load_v(0);
     load_tb(0);
-    load_p(0);
-    load_kt(0);
+    load_pk(0);
+    if (nch > 1) load_pk(1);
     load_vec(0);
     if (nch > 1) load_vec(1);
   }
@@ -724,7 +727,10 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       to |= !mbar_wait(&bar_vec[k & 1], (uint32_t)((k >> 1) & 1));
       if (bar_or(1, kCarryThreads, to)) break;
       tc::fence_after_sync();
-      if (tid == 0 && more) load_kq(k + 1);
+      if (tid == 0 && more) {
+        load_kq(k + 1);
+        if (k >= 1) load_pk(k + 1);  // into chunk k-1's buffers
+      }
       {
         const __nv_bfloat16* vt = reinterpret_cast<const __nv_bfloat16*>(sm + C_OFF_V) + j;
         float ks[32];
@@ -813,19 +819,20 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       // the output only, Dm^T P^T
       if (tid == 0) {
         if (k + 2 < nch) load_vec(k + 2);  // this parity's vector block is consumed
-        to |= !mbar_wait(&bar_kt, ph);
-        to |= !mbar_wait(&bar_p, ph);
+        to |= !mbar_wait(&bar_kt[k & 1], (uint32_t)((k >> 1) & 1));
+        to |= !mbar_wait(&bar_p[k & 1], (uint32_t)((k >> 1) & 1));
         tc::fence_after_sync();
 #pragma unroll
         for (int part = 0; part < 2; ++part)
 #pragma unroll
           for (int s = 0; s < 4; ++s)
             tc::mma_f16_ts(tb + TM_S, tb + (part ? TM_SLO : TM_SHI) + 8 * s,
-                           tc::sdesc_at(d_kt, 128, s), id128, true);
+                           tc::sdesc_at(d_kt + (uint64_t)((k & 1) * 16384 >> 4), 128, s), id128, true);
         tc::mma_commit(&bar_m5);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          tc::mma_f16_ts(tb + TM_OP, tb + TM_RHI + 8 * s, tc::sdesc_at(d_p, 64, s), id64, s > 0);
+          tc::mma_f16_ts(tb + TM_OP, tb + TM_RHI + 8 * s,
+                         tc::sdesc_at(d_p + (uint64_t)((k & 1) * 8192 >> 4), 64, s), id64, s > 0);
         tc::mma_commit(&bar_of);  // OQ and OP of this chunk
       }
 
@@ -833,7 +840,6 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       // after the last chunk, back to global memory
       to |= !mbar_wait(&bar_m5, ph);
       tc::fence_after_sync();
-      if (tid == 0 && more) load_kt(k + 1);
       {
         float v[kC];
 #pragma unroll
@@ -852,11 +858,7 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         }
       }
       tc::fence_before_sync();
-      if (tid == 0 && more) {
-        // P of this chunk is free once Dm^T P^T has completed
-        to |= !mbar_wait(&bar_of, ph);
-        load_p(k + 1);
-      }
+
     }
   } else {
     // ============================ output group: 8 warps; thread (j, half)
@@ -984,8 +986,14 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     if (n_kq) mbar_wait(&bar_kq, (n_kq - 1) & 1);
     if (n_v) mbar_wait(&bar_v, (n_v - 1) & 1);
     if (n_tb) mbar_wait(&bar_tb, (n_tb - 1) & 1);
-    if (n_p) mbar_wait(&bar_p, (n_p - 1) & 1);
-    if (n_kt) mbar_wait(&bar_kt, (n_kt - 1) & 1);
+    if (n_pk0) {
+      mbar_wait(&bar_p[0], (n_pk0 - 1) & 1);
+      mbar_wait(&bar_kt[0], (n_pk0 - 1) & 1);
+    }
+    if (n_pk1) {
+      mbar_wait(&bar_p[1], (n_pk1 - 1) & 1);
+      mbar_wait(&bar_kt[1], (n_pk1 - 1) & 1);
+    }
     if (n_vec0) mbar_wait(&bar_vec[0], (n_vec0 - 1) & 1);
     if (n_vec1) mbar_wait(&bar_vec[1], (n_vec1 - 1) & 1);
     tc::fence_before_sync();
