@@ -507,44 +507,82 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
 // shared memory (byte offsets from a 1024-aligned base)
 constexpr uint32_t C_OFF_KQ = 0;         // bf16 [128][128 i] SW128 (TMA): rows 0-63 k, 64-127 q
 constexpr uint32_t C_OFF_KT = 32768;     // bf16 [2][128 i][64 t] SW128 (TMA, k transposed by prep)
-constexpr uint32_t C_OFF_TMH = 65536;    // bf16 [64 t][64 s] SW128 (TMA): Tb hi
-constexpr uint32_t C_OFF_TML = 73728;    // Tb lo
-constexpr uint32_t C_OFF_P = 81920;      // bf16 [2][64 t][64 s] SW128 (TMA): P
-constexpr uint32_t C_OFF_V = 98304;      // bf16 [64 s][128 j] row-major (TMA)
-constexpr uint32_t C_OFF_VEC = 114688;   // fp32 [2][4][64] (bulk copy), by chunk parity
-constexpr uint32_t C_OFF_Z = 116736;     // bf16 [2][64 t][128 j] row-major: z (TMA), then out
-constexpr uint32_t C_SMEM = 149504 + 1024;
-// K^T and P are double-buffered by chunk parity and loaded a chunk ahead
+constexpr uint32_t C_OFF_TB = 65536;     // bf16 [2][128][64 s] SW128 (TMA): rows 0-63 Tb hi, 64-127 lo
+constexpr uint32_t C_OFF_P = 98304;      // bf16 [2][64 t][64 s] SW128 (TMA): P
+constexpr uint32_t C_OFF_V = 114688;     // bf16 [64 s][128 j] row-major (TMA)
+constexpr uint32_t C_OFF_VEC = 131072;   // fp32 [2][4][64] (bulk copy), by chunk parity
+constexpr uint32_t C_OFF_Z = 133120;     // bf16 [2][64 t][128 j] row-major: z (TMA), then out
+constexpr uint32_t C_SMEM = 165888 + 1024;
+// K^T, Tb and P are double-buffered by chunk parity and loaded a chunk ahead,
+// together with k and q, on one barrier per parity
+constexpr uint32_t kInBytes = 32768 + 16384 + 16384 + 8192;
 
-// TMEM columns. The A operands of the MMAs live in TMEM as packed bf16 pairs
-// (row j in lane j, K elements 2c, 2c+1 in column c).
+// TMEM columns. A operands of the MMAs live in TMEM as packed bf16 pairs
+// (row j in lane j, K elements 2c, 2c+1 in column c). Each region is
+// rewritten only after every reader of its previous contents is known to be
+// done (an MMA commit or a wait on the reading threads' barrier).
 constexpr uint32_t TM_S = 0;      // fp32 S (128): the state accumulator
-constexpr uint32_t TM_SHI = 128;  // bf16 hi part of S (64); (dk Dm)^T hi during the update
-constexpr uint32_t TM_SLO = 192;  // lo part (64); (dk Dm)^T lo during the update
-constexpr uint32_t TM_RHI = 256;  // bf16 R^T hi (32); Dm^T (hi only) once R Tb^T is done
-constexpr uint32_t TM_RLO = 288;  // R^T lo (32)
-constexpr uint32_t TM_KQ = 320;   // fp32 [KS | OQ] (128); Dm^T later takes the KS half
-constexpr uint32_t TM_OP = 448;   // fp32 Dm^T P^T (64)
+constexpr uint32_t TM_X = 128;    // S hi (64) | S lo (64); fp32 [R_hi Tb^T | R_hi Tb_lo^T] after (3)
+constexpr uint32_t TM_XLO = 192;
+constexpr uint32_t TM_Z = 256;    // R^T hi (32) | lo (32); (dk Dm)^T hi | lo after (4)
+constexpr uint32_t TM_ZLO = 288;
+constexpr uint32_t TM_Y = 320;    // fp32 [KS | OQ] (128); Dm^T P^T over the KS half
+constexpr uint32_t TM_W = 448;    // Dm^T hi (32), A operand of Dm^T P^T
 constexpr uint32_t TM_COLS = 512;
 
-// Loads are issued by thread 0 as soon as the buffer's last reader is known
-// to be done (every MMA a commit covers has completed):
-//   K, Q after S [k; q]^T (bar_m1)     V   after R is written
-//   Tb   after R Tb^T (bar_m3)         vec two chunks ahead, by parity
-//   P, K^T of chunk k+1 into the buffers of chunk k-1 once S [k; q]^T has
-//   completed (its commit covers chunk k-1's update and Dm^T P^T)
-// The output group reads [KS | OQ] and OP of chunk k; thread 0 waits for it
-// (bar_oe) before chunk k+1 writes them.
-__global__ void __launch_bounds__(kChainThreads, 1)
+constexpr int kIssueWarp = 16;                 // every MMA (a converged warp, one elected lane)
+constexpr int kLoadWarp = 17;                  // the carry's TMA loads (lane 0)
+constexpr int kOutThreads = 256;               // warps 8-15
+constexpr int kChainAll = kChainThreads + 64;  // + the issue and load warps
+
+// Bounded wait that gives up at once when another role has given up.
+__device__ __forceinline__ bool chain_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+  }
+  record_device_error(GDN_ERR_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+// A carry warp hands one K slice of an A operand it wrote to the issue warp.
+__device__ __forceinline__ void slice_done(uint64_t* bar, int lane) {
+  tc::tmem_wait_st();
+  tc::fence_before_sync();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+// Per chunk k (the issue warp's order; the carry warps hand over each K slice
+// of an operand as soon as it is in TMEM, so the MMAs on slice s run while
+// slice s+1 is computed):
+//   (1) [KS | OQ] = S_hi [k; q]^T + S_lo k^T, K = i in two slices (bar_sc)
+//   (2) R^T = V^T - diag(ak) KS^T -> hi/lo, K = s in two slices (bar_r)
+//   (3) [R_hi Tb^T | R_hi Tb_lo^T] (+ R_lo Tb^T onto the first half)
+//   (4) Dm^T = sum of the halves; (dk Dm)^T hi/lo and Dm^T hi (bar_d)
+//   (5) S += (dk Dm)^T K (hi, lo), on the accumulator pre-scaled by G_{L-1};
+//       Dm^T P^T over the KS half, for the output only
+//   (6) the new state: hi/lo copies (next chunk's (1)), accumulator rescaled
+// The load warp issues a buffer's next load once its last reader is done:
+//   K, Q, and Tb, P, K^T of chunk k+1 (into the buffers of chunk k-1), all on
+//   bar_in[(k+1) & 1], after (1) completes (its commit covers chunk k-1's
+//   (3) and (5));  V after every slice of (2);  vec two chunks ahead after
+//   every slice of (4)
+// The output group reads OQ after (1) and Dm^T P^T after (5), then releases
+// the [KS | OQ] columns (bar_oe) for chunk k+1's (1).
+__global__ void __launch_bounds__(kChainAll, 1)
     cp_chain_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_z,
-                    const __grid_constant__ CUtensorMap tm_kt) {
+                    const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_o) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) uint64_t bar_kq, bar_v, bar_tb, bar_p[2], bar_kt[2], bar_m1, bar_m3, bar_m5;
+  __shared__ __align__(8) uint64_t bar_in[2], bar_v, bar_m1, bar_m3, bar_m5;
   __shared__ __align__(8) uint64_t bar_vec[2], bar_of, bar_oe, bar_fin, bar_z[2];
+  __shared__ __align__(8) uint64_t bar_sc[2], bar_r[2], bar_d[2];
   __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
   __shared__ float spart[4][kC];
   __shared__ float sinv[kC];
   __shared__ float sgq[2][kC];
@@ -569,108 +607,192 @@ __global__ void __launch_bounds__(kChainThreads, 1)
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(&bar_kq, 1);
     mbar_init(&bar_v, 1);
-    mbar_init(&bar_tb, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar_p[b], 1);
-      mbar_init(&bar_kt[b], 1);
+      mbar_init(&bar_in[b], 1);
+      mbar_init(&bar_vec[b], 1);
+      mbar_init(&bar_z[b], 1);
+      mbar_init(&bar_sc[b], kCarryThreads / 32);
+      mbar_init(&bar_r[b], kCarryThreads / 32);
+      mbar_init(&bar_d[b], kCarryThreads / 32);
     }
     mbar_init(&bar_m1, 1);
     mbar_init(&bar_m3, 1);
     mbar_init(&bar_m5, 1);
     mbar_init(&bar_of, 1);
-    mbar_init(&bar_oe, kChainThreads - kCarryThreads);
+    mbar_init(&bar_oe, kOutThreads);
     mbar_init(&bar_fin, 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar_vec[b], 1);
-      mbar_init(&bar_z[b], 1);
-    }
+    s_abort = 0;
     fence_mbar_init();
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tb = s_tmem;
-
-  // thread 0's loads; the counts let the exit path wait for copies in flight
-  uint32_t n_kq = 0, n_v = 0, n_tb = 0, n_pk0 = 0, n_pk1 = 0, n_vec0 = 0, n_vec1 = 0;
+  volatile int* abort_flag = &s_abort;
   auto chunk_c0 = [&](int k) { return seq_s + (int64_t)kC * k; };
   auto slot_of = [&](int k) { return (size_t)(kb + k) * p.Hv + h; };
-  auto load_kq = [&](int k) {
-    const int y = (int)chunk_c0(k);
-    ++n_kq;
-    mbar_arrive_expect_tx(&bar_kq, 32768u);
-    tc::tma_load_2d(sm + C_OFF_KQ, &tm_k, kh * kD, y, &bar_kq);
-    tc::tma_load_2d(sm + C_OFF_KQ + 16384, &tm_k, kh * kD + 64, y, &bar_kq);
-    tc::tma_load_2d(sm + C_OFF_KQ + 8192, &tm_q, kh * kD, y, &bar_kq);
-    tc::tma_load_2d(sm + C_OFF_KQ + 24576, &tm_q, kh * kD + 64, y, &bar_kq);
-  };
-  auto load_v = [&](int k) {
-    ++n_v;
-    mbar_arrive_expect_tx(&bar_v, 16384u);
-    tc::tma_load_2d(sm + C_OFF_V, &tm_v, h * kD, (int)chunk_c0(k), &bar_v);
-  };
-  auto load_tb = [&](int k) {
-    const size_t slot = slot_of(k);
-    ++n_tb;
-    mbar_arrive_expect_tx(&bar_tb, 16384u);
-    tc::tma_load_2d(sm + C_OFF_TMH, &tm_w, 0, (int)(slot * kC), &bar_tb);
-    tc::tma_load_2d(sm + C_OFF_TML, &tm_w, 0, (int)((HvG + slot) * kC), &bar_tb);
-  };
-  auto load_pk = [&](int k) {
-    const int b = k & 1;
-    if (b) ++n_pk1; else ++n_pk0;
-    mbar_arrive_expect_tx(&bar_p[b], 8192u);
-    tc::tma_load_2d(sm + C_OFF_P + b * 8192, &tm_w, 0, (int)((2 * HvG + slot_of(k)) * kC), &bar_p[b]);
-    mbar_arrive_expect_tx(&bar_kt[b], 16384u);
-    tc::tma_load_2d(sm + C_OFF_KT + b * 16384, &tm_kt, 0, (int)(((kb + k) * p.Hk + kh) * kD),
-                    &bar_kt[b]);
-  };
-  auto load_vec = [&](int k) {
-    uint64_t* bar = &bar_vec[k & 1];
-    if (k & 1) ++n_vec1; else ++n_vec0;
-    mbar_arrive_expect_tx(bar, 1024u);
-    bulk_load(sm + C_OFF_VEC + (k & 1) * 1024, w.vec + slot_of(k) * (4 * kC), 1024u, bar);
-  };
-  if (tid == 0) {
-    load_kq(0);
-    load_v(0);
-    load_tb(0);
-    load_pk(0);
-    if (nch > 1) load_pk(1);
-    load_vec(0);
-    if (nch > 1) load_vec(1);
-  }
 
-  if (tid < kCarryThreads) {
+  // the load warp's loads; the counts let the exit path wait for copies in
+  // flight
+  uint32_t n_in0 = 0, n_in1 = 0, n_v = 0, n_vec0 = 0, n_vec1 = 0;
+  const bool loader = warp == kLoadWarp && lane == 0;
+
+  if (loader) {
+    // the MMA operands of chunk k on bar_in[k & 1]: the expected bytes are
+    // posted once per phase, the copies may land before or after
+    auto arm_in = [&](int k) {
+      if (k & 1) ++n_in1; else ++n_in0;
+      mbar_arrive_expect_tx(&bar_in[k & 1], kInBytes);
+    };
+    auto load_kq = [&](int k) {
+      uint64_t* bar = &bar_in[k & 1];
+      const int y = (int)chunk_c0(k);
+      tc::tma_load_2d(sm + C_OFF_KQ, &tm_k, kh * kD, y, bar);
+      tc::tma_load_2d(sm + C_OFF_KQ + 16384, &tm_k, kh * kD + 64, y, bar);
+      tc::tma_load_2d(sm + C_OFF_KQ + 8192, &tm_q, kh * kD, y, bar);
+      tc::tma_load_2d(sm + C_OFF_KQ + 24576, &tm_q, kh * kD + 64, y, bar);
+    };
+    auto load_tbpk = [&](int k) {
+      uint64_t* bar = &bar_in[k & 1];
+      const int b = k & 1;
+      const size_t slot = slot_of(k);
+      tc::tma_load_2d(sm + C_OFF_TB + b * 16384, &tm_w, 0, (int)(slot * kC), bar);
+      tc::tma_load_2d(sm + C_OFF_TB + b * 16384 + 8192, &tm_w, 0, (int)((HvG + slot) * kC), bar);
+      tc::tma_load_2d(sm + C_OFF_P + b * 8192, &tm_w, 0, (int)((2 * HvG + slot) * kC), bar);
+      tc::tma_load_2d(sm + C_OFF_KT + b * 16384, &tm_kt, 0, (int)(((kb + k) * p.Hk + kh) * kD), bar);
+    };
+    auto load_v = [&](int k) {
+      ++n_v;
+      mbar_arrive_expect_tx(&bar_v, 16384u);
+      tc::tma_load_2d(sm + C_OFF_V, &tm_v, h * kD, (int)chunk_c0(k), &bar_v);
+    };
+    auto load_vec = [&](int k) {
+      uint64_t* bar = &bar_vec[k & 1];
+      if (k & 1) ++n_vec1; else ++n_vec0;
+      mbar_arrive_expect_tx(bar, 1024u);
+      bulk_load(sm + C_OFF_VEC + (k & 1) * 1024, w.vec + slot_of(k) * (4 * kC), 1024u, bar);
+    };
+    arm_in(0);
+    load_kq(0);
+    load_tbpk(0);
+    load_v(0);
+    load_vec(0);
+    if (nch > 1) {
+      arm_in(1);
+      load_tbpk(1);
+      load_vec(1);
+    }
+    for (int k = 0; k < nch; ++k) {
+      const uint32_t ph = (uint32_t)(k & 1);
+      const bool more = k + 1 < nch;
+      if (!chain_wait(&bar_m1, ph, abort_flag)) break;
+      if (more) {
+        if (k >= 1) {
+          arm_in(k + 1);
+          load_tbpk(k + 1);  // into chunk k-1's buffers
+        }
+        load_kq(k + 1);
+      }
+      if (!chain_wait(&bar_r[1], ph, abort_flag)) break;
+      if (more) load_v(k + 1);  // every slice of (2) has read V
+      if (!chain_wait(&bar_d[1], ph, abort_flag)) break;
+      if (k + 2 < nch) load_vec(k + 2);  // every slice of (4) has read these vectors
+    }
+  } else if (warp == kIssueWarp) {
+    const uint32_t id64 = tc::idesc(tc::kBF16, 128, 64), id128 = tc::idesc(tc::kBF16, 128, 128);
+    const uint64_t d_kq = tc::sdesc_sw128(smem_u32(sm + C_OFF_KQ)),
+                   d_kt = tc::sdesc_sw128(smem_u32(sm + C_OFF_KT)),
+                   d_tb = tc::sdesc_sw128(smem_u32(sm + C_OFF_TB)),
+                   d_p = tc::sdesc_sw128(smem_u32(sm + C_OFF_P));
+    for (int k = 0; k < nch; ++k) {
+      const uint32_t ph = (uint32_t)(k & 1);
+      bool ok = chain_wait(&bar_in[k & 1], (uint32_t)((k >> 1) & 1), abort_flag);
+      if (ok && k >= 1) ok = chain_wait(&bar_oe, (uint32_t)((k - 1) & 1), abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      // (1) slice s of the state copies covers k-steps 2s, 2s+1, 4+2s, 5+2s
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        ok = __all_sync(0xffffffffu, chain_wait(&bar_sc[s], ph, abort_flag));
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int ks = 2 * s + (e & 1) + 4 * (e >> 1);
+          tc::mma_f16_ts_elect(tb + TM_Y, tb + TM_X + 8 * ks, tc::sdesc_at(d_kq, 128, ks), id128, ks > 0);
+          tc::mma_f16_ts_elect(tb + TM_Y, tb + TM_XLO + 8 * ks, tc::sdesc_at(d_kq, 128, ks), id64, true);
+        }
+      }
+      if (!ok) break;
+      tc::mma_commit_elect(&bar_m1);
+      // (3) slice s of R covers k-steps s and 2 + s; B = [Tb hi; Tb lo]
+      // (N=128) for R hi, Tb hi (N=64) for R lo
+      const uint64_t dtb = d_tb + (uint64_t)((k & 1) * 16384 >> 4);
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        ok = __all_sync(0xffffffffu, chain_wait(&bar_r[s], ph, abort_flag));
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int ks = s + 2 * e;
+          tc::mma_f16_ts_elect(tb + TM_X, tb + TM_Z + 8 * ks, tc::sdesc_at(dtb, 128, ks), id128, ks > 0);
+          tc::mma_f16_ts_elect(tb + TM_X, tb + TM_ZLO + 8 * ks, tc::sdesc_at(dtb, 64, ks), id64, true);
+        }
+      }
+      if (!ok) break;
+      tc::mma_commit_elect(&bar_m3);
+      // (5) slice s of Dm covers k-steps s and 2 + s
+      const uint64_t dkt = d_kt + (uint64_t)((k & 1) * 16384 >> 4);
+      const uint64_t dp = d_p + (uint64_t)((k & 1) * 8192 >> 4);
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        ok = __all_sync(0xffffffffu, chain_wait(&bar_d[s], ph, abort_flag));
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int ks = s + 2 * e;
+          tc::mma_f16_ts_elect(tb + TM_S, tb + TM_Z + 8 * ks, tc::sdesc_at(dkt, 128, ks), id128, true);
+          tc::mma_f16_ts_elect(tb + TM_S, tb + TM_ZLO + 8 * ks, tc::sdesc_at(dkt, 128, ks), id128, true);
+        }
+        if (s == 0) {
+          tc::mma_f16_ts_elect(tb + TM_Y, tb + TM_W, tc::sdesc_at(dp, 64, 0), id64, false);
+          tc::mma_f16_ts_elect(tb + TM_Y, tb + TM_W + 16, tc::sdesc_at(dp, 64, 2), id64, true);
+        }
+      }
+      if (!ok) break;
+      tc::mma_commit_elect(&bar_m5);
+      tc::mma_f16_ts_elect(tb + TM_Y, tb + TM_W + 8, tc::sdesc_at(dp, 64, 1), id64, true);
+      tc::mma_f16_ts_elect(tb + TM_Y, tb + TM_W + 24, tc::sdesc_at(dp, 64, 3), id64, true);
+      tc::mma_commit_elect(&bar_of);  // OQ and Dm^T P^T of this chunk
+    }
+  } else if (tid < kCarryThreads) {
     // ============================ carry group: thread (j, ch) owns value row j
     // (TMEM lane j) and half ch of the columns of each per-row phase
     const int j = tid & 127, ch = tid >> 7;
     const uint32_t tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
-    const uint32_t id64 = tc::idesc(tc::kBF16, 128, 64), id128 = tc::idesc(tc::kBF16, 128, 128);
-    const uint64_t d_kq = tc::sdesc_sw128(smem_u32(sm + C_OFF_KQ)),
-                   d_kt = tc::sdesc_sw128(smem_u32(sm + C_OFF_KT)),
-                   d_tmh = tc::sdesc_sw128(smem_u32(sm + C_OFF_TMH)),
-                   d_tml = tc::sdesc_sw128(smem_u32(sm + C_OFF_TML)),
-                   d_p = tc::sdesc_sw128(smem_u32(sm + C_OFF_P));
     float* gS = p.state + (((size_t)n * p.Hv + h) * kD + j) * kD + 64 * ch;
 
     // 64 fp32 state values (this thread's half row) -> hi/lo A operands in
-    // TMEM, then the accumulator rescaled by gl
+    // TMEM, one 32-wide K slice at a time, then the accumulator rescaled by gl
     auto store_state = [&](float (&v)[kC], float gl) {
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t hw[16], lw[16];
+      for (int s = 0; s < 2; ++s) {
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float a0 = v[32 * hf + 2 * m], a1 = v[32 * hf + 2 * m + 1];
-          const __nv_bfloat162 hv = __floats2bfloat162_rn(a0, a1);
-          hw[m] = *reinterpret_cast<const uint32_t*>(&hv);
-          lw[m] = pack_bf16(a0 - __low2float(hv), a1 - __high2float(hv));
+        for (int q = 0; q < 2; ++q) {
+          uint32_t hw[8], lw[8];
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            const float a0 = v[32 * s + 16 * q + 2 * m], a1 = v[32 * s + 16 * q + 2 * m + 1];
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(a0, a1);
+            hw[m] = *reinterpret_cast<const uint32_t*>(&hv);
+            lw[m] = pack_bf16(a0 - __low2float(hv), a1 - __high2float(hv));
+          }
+          tc::tmem_st8u(tl + TM_X + 32 * ch + 16 * s + 8 * q, hw);
+          tc::tmem_st8u(tl + TM_XLO + 32 * ch + 16 * s + 8 * q, lw);
         }
-        tc::tmem_st16u(tl + TM_SHI + 32 * ch + 16 * hf, hw);
-        tc::tmem_st16u(tl + TM_SLO + 32 * ch + 16 * hf, lw);
+        slice_done(&bar_sc[s], lane);
       }
 #pragma unroll
       for (int e = 0; e < kC; ++e) v[e] *= gl;
@@ -679,8 +801,9 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         tc::tmem_st16(tl + TM_S + 64 * ch + 16 * m, *reinterpret_cast<const float(*)[16]>(v + 16 * m));
     };
 
-    bool to = !mbar_wait(&bar_vec[0], 0);
-    {
+    bool to = !chain_wait(&bar_vec[0], 0, abort_flag);
+    to = __any_sync(0xffffffffu, to);
+    if (!to) {
       float v[kC];
       const float4* src = reinterpret_cast<const float4*>(gS);
 #pragma unroll
@@ -692,153 +815,104 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         v[4 * m + 3] = f.w;
       }
       store_state(v, reinterpret_cast<const float*>(sm + C_OFF_VEC)[3 * kC]);
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
     }
 
-    for (int k = 0; k < nch; ++k) {
+    for (int k = 0; k < nch && !to; ++k) {
       const uint32_t ph = (uint32_t)(k & 1);
       const int64_t c0 = chunk_c0(k);
       const int L = (int)((seq_e - c0) < kC ? (seq_e - c0) : kC);
       const float* vec = reinterpret_cast<const float*>(sm + C_OFF_VEC + (k & 1) * 1024);
       const bool more = k + 1 < nch;
 
-      // (1) [KS | OQ]^T = S_hi [k; q]^T + S_lo k^T (one N=128 accumulator)
-      if (tid == 0) {
-        to |= !mbar_wait(&bar_kq, ph);
-        if (k >= 1) to |= !mbar_wait(&bar_oe, (uint32_t)((k - 1) & 1));
-      }
-      if (bar_or(1, kCarryThreads, to)) break;
-      if (tid == 0) {
-        tc::fence_after_sync();
-#pragma unroll
-        for (int s = 0; s < 8; ++s)
-          tc::mma_f16_ts(tb + TM_KQ, tb + TM_SHI + 8 * s, tc::sdesc_at(d_kq, 128, s), id128, s > 0);
-#pragma unroll
-        for (int s = 0; s < 8; ++s)
-          tc::mma_f16_ts(tb + TM_KQ, tb + TM_SLO + 8 * s, tc::sdesc_at(d_kq, 128, s), id64, true);
-        tc::mma_commit(&bar_m1);
-      }
-
       // (2) R^T = V^T - diag(ak) KS^T (columns s >= L zero); this thread's
-      // 32 columns s = 32 ch ..
-      to |= !mbar_wait(&bar_m1, ph);
-      to |= !mbar_wait(&bar_v, ph);
-      to |= !mbar_wait(&bar_vec[k & 1], (uint32_t)((k >> 1) & 1));
-      if (bar_or(1, kCarryThreads, to)) break;
+      // 32 columns s = 32 ch .., two slices of 16
+      // (V and the vectors landed long before (1) completes: checked first)
+      to = !chain_wait(&bar_v, ph, abort_flag) ||
+           !chain_wait(&bar_vec[k & 1], (uint32_t)((k >> 1) & 1), abort_flag) ||
+           !chain_wait(&bar_m1, ph, abort_flag);
+      if (__any_sync(0xffffffffu, to)) break;
       tc::fence_after_sync();
-      if (tid == 0 && more) {
-        load_kq(k + 1);
-        if (k >= 1) load_pk(k + 1);  // into chunk k-1's buffers
-      }
       {
         const __nv_bfloat16* vt = reinterpret_cast<const __nv_bfloat16*>(sm + C_OFF_V) + j;
         float ks[32];
 #pragma unroll
         for (int m = 0; m < 2; ++m)
-          tc::tmem_ld16(tl + TM_KQ + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(ks + 16 * m));
+          tc::tmem_ld16(tl + TM_Y + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(ks + 16 * m));
         tc::tmem_wait_ld();
-        uint32_t hw[16], lw[16];
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 a4 = reinterpret_cast<const float4*>(vec)[8 * ch + e4];
-          const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-          float r[4];
+        for (int s = 0; s < 2; ++s) {
+          uint32_t hw[8], lw[8];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int e = 4 * e4 + u, s = 32 * ch + e;
-            const float x = __bfloat162float(vt[s * kD]) - av[u] * ks[e];
-            r[u] = s < L ? x : 0.f;
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 a4 = reinterpret_cast<const float4*>(vec)[8 * ch + 4 * s + e4];
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+            float r[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int e = 16 * s + 4 * e4 + u, t = 32 * ch + e;
+              const float x = __bfloat162float(vt[t * kD]) - av[u] * ks[e];
+              r[u] = t < L ? x : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const __nv_bfloat162 hv = __floats2bfloat162_rn(r[2 * u], r[2 * u + 1]);
+              hw[2 * e4 + u] = *reinterpret_cast<const uint32_t*>(&hv);
+              lw[2 * e4 + u] = pack_bf16(r[2 * u] - __low2float(hv), r[2 * u + 1] - __high2float(hv));
+            }
           }
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const __nv_bfloat162 hv = __floats2bfloat162_rn(r[2 * u], r[2 * u + 1]);
-            hw[2 * e4 + u] = *reinterpret_cast<const uint32_t*>(&hv);
-            lw[2 * e4 + u] = pack_bf16(r[2 * u] - __low2float(hv), r[2 * u + 1] - __high2float(hv));
-          }
+          tc::tmem_st8u(tl + TM_Z + 16 * ch + 8 * s, hw);
+          tc::tmem_st8u(tl + TM_ZLO + 16 * ch + 8 * s, lw);
+          slice_done(&bar_r[s], lane);
         }
-        tc::tmem_st16u(tl + TM_RHI + 16 * ch, hw);
-        tc::tmem_st16u(tl + TM_RLO + 16 * ch, lw);
-        tc::tmem_wait_st();
-      }
-      tc::fence_before_sync();
-      bar_named(1, kCarryThreads);
-
-      // (3) Dm^T = R^T Tb^T  (hi*hi + hi*lo + lo*hi), over KS
-      if (tid == 0) {
-        if (more) load_v(k + 1);
-        to |= !mbar_wait(&bar_tb, ph);
-        tc::fence_after_sync();
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          tc::mma_f16_ts(tb + TM_KQ, tb + TM_RHI + 8 * s, tc::sdesc_at(d_tmh, 64, s), id64, s > 0);
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          tc::mma_f16_ts(tb + TM_KQ, tb + TM_RHI + 8 * s, tc::sdesc_at(d_tml, 64, s), id64, true);
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          tc::mma_f16_ts(tb + TM_KQ, tb + TM_RLO + 8 * s, tc::sdesc_at(d_tmh, 64, s), id64, true);
-        tc::mma_commit(&bar_m3);
       }
 
-      // (4) Dm' = diag(dk) Dm as hi + lo A operands (into the S operand
-      // columns, free until the new state is copied) and Dm_hi for the output
-      // (into R's columns); this thread's 32 rows t
-      to |= !mbar_wait(&bar_m3, ph);
+      // (4) Dm^T = [R Tb^T halves summed]; (dk Dm)^T hi/lo into R's columns
+      // and Dm^T hi for the output; this thread's 32 columns t, two slices
+      to = !chain_wait(&bar_m3, ph, abort_flag);
+      if (__any_sync(0xffffffffu, to)) break;
       tc::fence_after_sync();
-      if (tid == 0 && more) load_tb(k + 1);
       {
         float dm[32];
+        {
+          float db[32];
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
-          tc::tmem_ld16(tl + TM_KQ + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(dm + 16 * m));
-        tc::tmem_wait_ld();
-        uint32_t hw[16], lw[16], dw[16];
+          for (int m = 0; m < 2; ++m) {
+            tc::tmem_ld16(tl + TM_X + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(dm + 16 * m));
+            tc::tmem_ld16(tl + TM_XLO + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(db + 16 * m));
+          }
+          tc::tmem_wait_ld();
 #pragma unroll
-        for (int m = 0; m < 16; ++m) dw[m] = pack_bf16(dm[2 * m], dm[2 * m + 1]);
-        tc::tmem_st16u(tl + TM_RHI + 16 * ch, dw);
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 d4 = reinterpret_cast<const float4*>(vec + kC)[8 * ch + e4];
-          const float x0 = d4.x * dm[4 * e4], x1 = d4.y * dm[4 * e4 + 1];
-          const float x2 = d4.z * dm[4 * e4 + 2], x3 = d4.w * dm[4 * e4 + 3];
-          const __nv_bfloat162 h01 = __floats2bfloat162_rn(x0, x1), h23 = __floats2bfloat162_rn(x2, x3);
-          hw[2 * e4] = *reinterpret_cast<const uint32_t*>(&h01);
-          hw[2 * e4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
-          lw[2 * e4] = pack_bf16(x0 - __low2float(h01), x1 - __high2float(h01));
-          lw[2 * e4 + 1] = pack_bf16(x2 - __low2float(h23), x3 - __high2float(h23));
+          for (int e = 0; e < 32; ++e) dm[e] += db[e];
         }
-        tc::tmem_st16u(tl + TM_SHI + 16 * ch, hw);
-        tc::tmem_st16u(tl + TM_SLO + 16 * ch, lw);
-        tc::tmem_wait_st();
-      }
-      tc::fence_before_sync();
-      if (bar_or(1, kCarryThreads, to)) break;
-
-      // (5) S += Dm'^T K (hi + lo) on the pre-decayed accumulator; then, for
-      // the output only, Dm^T P^T
-      if (tid == 0) {
-        if (k + 2 < nch) load_vec(k + 2);  // this parity's vector block is consumed
-        to |= !mbar_wait(&bar_kt[k & 1], (uint32_t)((k >> 1) & 1));
-        to |= !mbar_wait(&bar_p[k & 1], (uint32_t)((k >> 1) & 1));
-        tc::fence_after_sync();
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
+        for (int s = 0; s < 2; ++s) {
+          uint32_t hw[8], lw[8], dw[8];
 #pragma unroll
-          for (int s = 0; s < 4; ++s)
-            tc::mma_f16_ts(tb + TM_S, tb + (part ? TM_SLO : TM_SHI) + 8 * s,
-                           tc::sdesc_at(d_kt + (uint64_t)((k & 1) * 16384 >> 4), 128, s), id128, true);
-        tc::mma_commit(&bar_m5);
+          for (int m = 0; m < 8; ++m) dw[m] = pack_bf16(dm[16 * s + 2 * m], dm[16 * s + 2 * m + 1]);
+          tc::tmem_st8u(tl + TM_W + 16 * ch + 8 * s, dw);
 #pragma unroll
-        for (int s = 0; s < 4; ++s)
-          tc::mma_f16_ts(tb + TM_OP, tb + TM_RHI + 8 * s,
-                         tc::sdesc_at(d_p + (uint64_t)((k & 1) * 8192 >> 4), 64, s), id64, s > 0);
-        tc::mma_commit(&bar_of);  // OQ and OP of this chunk
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 d4 = reinterpret_cast<const float4*>(vec + kC)[8 * ch + 4 * s + e4];
+            const int e = 16 * s + 4 * e4;
+            const float x0 = d4.x * dm[e], x1 = d4.y * dm[e + 1];
+            const float x2 = d4.z * dm[e + 2], x3 = d4.w * dm[e + 3];
+            const __nv_bfloat162 h01 = __floats2bfloat162_rn(x0, x1), h23 = __floats2bfloat162_rn(x2, x3);
+            hw[2 * e4] = *reinterpret_cast<const uint32_t*>(&h01);
+            hw[2 * e4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+            lw[2 * e4] = pack_bf16(x0 - __low2float(h01), x1 - __high2float(h01));
+            lw[2 * e4 + 1] = pack_bf16(x2 - __low2float(h23), x3 - __high2float(h23));
+          }
+          tc::tmem_st8u(tl + TM_Z + 16 * ch + 8 * s, hw);
+          tc::tmem_st8u(tl + TM_ZLO + 16 * ch + 8 * s, lw);
+          slice_done(&bar_d[s], lane);
+        }
       }
 
       // (6) the new state: operand copies and the next chunk's decay in TMEM;
       // after the last chunk, back to global memory
-      to |= !mbar_wait(&bar_m5, ph);
+      to = more && !chain_wait(&bar_vec[(k + 1) & 1], (uint32_t)(((k + 1) >> 1) & 1), abort_flag);
+      to = to || !chain_wait(&bar_m5, ph, abort_flag);
+      if (__any_sync(0xffffffffu, to)) break;
       tc::fence_after_sync();
       {
         float v[kC];
@@ -852,23 +926,20 @@ __global__ void __launch_bounds__(kChainThreads, 1)
           for (int m = 0; m < 16; ++m)
             dst[m] = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
         } else {
-          to |= !mbar_wait(&bar_vec[(k + 1) & 1], (uint32_t)(((k + 1) >> 1) & 1));
           store_state(v, reinterpret_cast<const float*>(sm + C_OFF_VEC + ((k + 1) & 1) * 1024)[3 * kC]);
-          tc::tmem_wait_st();
         }
       }
-      tc::fence_before_sync();
-
     }
-  } else {
+    tc::tmem_wait_st();
+    tc::fence_before_sync();
+  } else if (tid < kChainThreads) {
     // ============================ output group: 8 warps; thread (j, half)
     // owns output column j = 32 (warp % 4) + lane for the 32 rows of its half.
-    // O = diag(gq) OQ + OP is read from TMEM once (then TMEM is released to
-    // the next chunk); with the fused norm, the per-row sums of squares are
-    // reduce-scattered across lanes, z arrives by TMA into a row-major tile
-    // (two, by chunk parity) that the gated result overwrites in place, and
-    // each live row leaves as one 256-byte bulk store.
-    constexpr int kOut = kChainThreads - kCarryThreads;
+    // OQ is read once (1) completes and Dm^T P^T once (5) completes; then
+    // TMEM is released to the next chunk. With the fused norm, the per-row
+    // sums of squares are reduce-scattered across lanes, z arrives by TMA into
+    // a row-major tile (two, by chunk parity) that the gated result overwrites
+    // in place, and each live row leaves as one 256-byte bulk store.
     const int u = tid - kCarryThreads, q4 = warp & 3, half = (warp - 8) >> 2;
     const int j = 32 * q4 + lane, t0 = 32 * half;
     const uint32_t tl = tb + ((uint32_t)(32 * q4) << 16);
@@ -891,25 +962,27 @@ __global__ void __launch_bounds__(kChainThreads, 1)
       const float* gq = sgq[k & 1] + t0;
       __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(sm + C_OFF_Z + (k & 1) * 16384);
       if (u < kC) sgq[k & 1][u] = __ldg(w.vec + slot_of(k) * (4 * kC) + 2 * kC + u);
-      to |= !mbar_wait(&bar_of, (uint32_t)(k & 1));
-      if (bar_or(2, kOut, to)) break;
-      tc::fence_after_sync();
-      float o[32];
-      {
-        float a[2][16], b[2][16];
+      float a[2][16], b[2][16];
+      to |= !chain_wait(&bar_m1, (uint32_t)(k & 1), abort_flag);
+      if (!__any_sync(0xffffffffu, to)) {
+        tc::fence_after_sync();
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          tc::tmem_ld16(tl + TM_KQ + 64 + t0 + 16 * m, a[m]);
-          tc::tmem_ld16(tl + TM_OP + t0 + 16 * m, b[m]);
-        }
+        for (int m = 0; m < 2; ++m) tc::tmem_ld16(tl + TM_Y + 64 + t0 + 16 * m, a[m]);
         tc::tmem_wait_ld();
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[16 * m + e] = fmaf(gq[16 * m + e], a[m][e], b[m][e]);
       }
+      to |= !chain_wait(&bar_of, (uint32_t)(k & 1), abort_flag);
+      if (bar_or(2, kOutThreads, to)) break;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int m = 0; m < 2; ++m) tc::tmem_ld16(tl + TM_Y + t0 + 16 * m, b[m]);
+      tc::tmem_wait_ld();
       tc::fence_before_sync();
       mbar_arrive(&bar_oe);  // this chunk's output accumulators are free
+      float o[32];
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[16 * m + e] = fmaf(gq[16 * m + e], a[m][e], b[m][e]);
       if (p.core_out != nullptr) {
         float* cg = p.core_out + ((c0 + t0) * p.Hv + h) * kD + j;
         const int64_t cstr = (int64_t)p.Hv * kD;
@@ -923,16 +996,20 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         }
       }
       if (!fused) continue;
-      // the bulk stores of two chunks ago have read their tile: reload it
-      if (stored) bulk_wait_read_all();
-      if (bar_or(2, kOut, to)) break;
-      if (u == 0 && k >= 1 && k + 1 < nch) load_z(k + 1);
-      // five halving exchanges: lane l ends with the sum of row t0 + l
-      float sq[32];
+      // five halving exchanges: lane l ends with the sum of row t0 + l (the
+      // first one squares on the fly)
+      float sq[16];
+      {
+        const bool up = (lane & 16) != 0;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) sq[e] = o[e] * o[e];
+        for (int i = 0; i < 16; ++i) {
+          const float send = up ? o[i] * o[i] : o[i + 16] * o[i + 16];
+          const float keep = up ? o[i + 16] * o[i + 16] : o[i] * o[i];
+          sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+      }
 #pragma unroll
-      for (int st = 0; st < 5; ++st) {
+      for (int st = 1; st < 5; ++st) {
         const int m = 16 >> st, hv = 16 >> st;
         const bool up = (lane & m) != 0;
 #pragma unroll
@@ -943,24 +1020,48 @@ __global__ void __launch_bounds__(kChainThreads, 1)
         }
       }
       spart[q4][t0 + lane] = sq[0];
-      bar_named(2, kOut);
+      bar_named(2, kOutThreads);
       if (u < kC)
         sinv[u] = 1.f / sqrtf((spart[0][u] + spart[1][u] + spart[2][u] + spart[3][u]) / (float)kD +
                               p.rms_eps);
-      to |= !mbar_wait(&bar_z[k & 1], (uint32_t)((k >> 1) & 1));
-      bar_named(2, kOut);
+      // z of chunk k+1 into the tile chunk k-1 was stored from. Only a
+      // sequence's last chunk can be partial, so chunk k-1 was full and left
+      // as thread 0's one tile store: its own wait covers the reload.
+      if (u == 0 && k >= 1 && k + 1 < nch) {
+        bulk_wait_read_all();
+        load_z(k + 1);
+      }
+      to |= !chain_wait(&bar_z[k & 1], (uint32_t)((k >> 1) & 1), abort_flag);
+      bar_named(2, kOutThreads);
       // the gated result over z, in place (rows >= L hold finite values that
-      // are never stored)
+      // are never stored), 16 rows at a time: all loads, then the math, then
+      // all stores
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int t = t0 + e;
-        const float zf = __bfloat162float(zb[t * kD + j]);
-        const float gate = __fdividef(zf, 1.f + __expf(-zf));
-        zb[t * kD + j] = __float2bfloat16_rn(o[e] * sinv[t] * nwj * gate);
+      for (int hf = 0; hf < 2; ++hf) {
+        float zf[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) zf[e] = __bfloat162float(zb[(t0 + 16 * hf + e) * kD + j]);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int t = t0 + 16 * hf + e;
+          const float gate = __fdividef(zf[e], 1.f + __expf(-zf[e]));
+          zf[e] = o[16 * hf + e] * sinv[t] * nwj * gate;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) zb[(t0 + 16 * hf + e) * kD + j] = __float2bfloat16_rn(zf[e]);
       }
       fence_proxy_async_smem();
-      bar_named(2, kOut);
-      if (u < L) {
+      bar_named(2, kOutThreads);
+      if (L == kC) {
+        // a full chunk leaves as one tile
+        if (u == 0) {
+          tc::tma_store_2d(&tm_o, h * kD, (int)c0, zb);
+          bulk_commit();
+          stored = true;
+        }
+      } else if (u < L) {
+        // the sequence's last chunk: row by row, so no row of the next
+        // sequence is written
         bulk_store(static_cast<__nv_bfloat16*>(p.out) + ((c0 + u) * p.Hv + h) * kD, zb + u * kD,
                    (uint32_t)(kD * 2));
         bulk_commit();
@@ -979,24 +1080,18 @@ __global__ void __launch_bounds__(kChainThreads, 1)
   // bounded wait gave up)
   tc::fence_before_sync();
   __syncthreads();
-  if (tid == 0) {
+  if (warp == kIssueWarp) {
     tc::fence_after_sync();
-    tc::mma_commit(&bar_fin);
+    tc::mma_commit_elect(&bar_fin);
     mbar_wait(&bar_fin, 0);
-    if (n_kq) mbar_wait(&bar_kq, (n_kq - 1) & 1);
+    tc::fence_before_sync();
+  }
+  if (loader) {
+    if (n_in0) mbar_wait(&bar_in[0], (n_in0 - 1) & 1);
+    if (n_in1) mbar_wait(&bar_in[1], (n_in1 - 1) & 1);
     if (n_v) mbar_wait(&bar_v, (n_v - 1) & 1);
-    if (n_tb) mbar_wait(&bar_tb, (n_tb - 1) & 1);
-    if (n_pk0) {
-      mbar_wait(&bar_p[0], (n_pk0 - 1) & 1);
-      mbar_wait(&bar_kt[0], (n_pk0 - 1) & 1);
-    }
-    if (n_pk1) {
-      mbar_wait(&bar_p[1], (n_pk1 - 1) & 1);
-      mbar_wait(&bar_kt[1], (n_pk1 - 1) & 1);
-    }
     if (n_vec0) mbar_wait(&bar_vec[0], (n_vec0 - 1) & 1);
     if (n_vec1) mbar_wait(&bar_vec[1], (n_vec1 - 1) & 1);
-    tc::fence_before_sync();
   }
   __syncthreads();
   if (warp == 0) {
@@ -1030,8 +1125,9 @@ cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_
   w.vec = reinterpret_cast<float*>(static_cast<char*>(workspace) + l.off_vec);
   w.G = l.G;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  CUtensorMap mq, mk, mv, mw, mz, mkt;
+  CUtensorMap mq, mk, mv, mw, mz, mkt, mo;
   memset(&mz, 0, sizeof(mz));
+  memset(&mo, 0, sizeof(mo));
   const int64_t qkc = (int64_t)p.Hk * kD, vc = (int64_t)p.Hv * kD;
   if (!tc::make_map_2d(&mq, p.q, p.T, qkc, p.q_stride, 2, bf, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc::make_map_2d(&mk, p.k, p.T, qkc, p.k_stride, 2, bf, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -1043,7 +1139,8 @@ cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_
                        CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (p.z != nullptr &&
-      !tc::make_map_2d(&mz, p.z, p.T, vc, vc, 2, bf, kD, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+      (!tc::make_map_2d(&mz, p.z, p.T, vc, vc, 2, bf, kD, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+       !tc::make_map_2d(&mo, p.out, p.T, vc, vc, 2, bf, kD, 64, CU_TENSOR_MAP_SWIZZLE_NONE)))
     return cudaErrorInvalidValue;
   cp_index_kernel<<<1, 1024, 0, stream>>>(p, w);
   cudaError_t e = cudaGetLastError();
@@ -1055,8 +1152,8 @@ cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(cp_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
-  cp_chain_kernel<<<dim3((unsigned)p.Hv, (unsigned)p.N), kChainThreads, C_SMEM, stream>>>(p, w, mq, mk,
-                                                                                         mv, mw, mz, mkt);
+  cp_chain_kernel<<<dim3((unsigned)p.Hv, (unsigned)p.N), kChainAll, C_SMEM, stream>>>(p, w, mq, mk,
+                                                                                         mv, mw, mz, mkt, mo);
   return cudaGetLastError();
 }
 
