@@ -173,19 +173,24 @@ __global__ void __launch_bounds__(1024) cp_index_kernel(const PrefillArgs p, con
 
 // ------------------------------------------------------------------ prep
 
+// The k and q tile is dead once the grams have completed and K^T and the l2
+// scales are taken from it; the per-V-head matrices then reuse its space.
 constexpr uint32_t P_OFF_KQ = 0;       // bf16 [128][128 i] SW128 (TMA): rows 0-63 k, 64-127 q
-constexpr uint32_t P_OFF_A = 32768;    // fp32 [64][65]
-constexpr uint32_t P_OFF_T = 49408;    // fp32 [64][64] Tm
-constexpr uint32_t P_OFF_X = 65792;    // fp32 [768] block-product scratch
-constexpr uint32_t P_SMEM = 68864 + 1024;
+constexpr uint32_t P_OFF_A = 0;        // fp32 [64][65]
+constexpr uint32_t P_OFF_T = 16640;    // fp32 [64][64] Tm
+constexpr uint32_t P_OFF_X = 33024;    // fp32 [768] block-product scratch
+constexpr uint32_t P_SMEM = 36096 + 1024;
 
-__global__ void __launch_bounds__(kPrepThreads, 3)
+__global__ void __launch_bounds__(kPrepThreads, 4)
     cp_prep_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ float sg[kC], sbeta[kC], sc[kC], sgam[kC], sinvk[kC], sinvq[kC];
-  __shared__ float sga[kMaxRep][kC], sgb[kMaxRep][kC];
+  __shared__ float sinvk[kC], sinvq[kC];
+  // raw gate inputs, then per V head: beta, the chunk-local cumulative decay
+  // c and G = e^c
+  __shared__ float sga[kMaxRep][kC], sgb[kMaxRep][kC], sbeta[kMaxRep][kC], sc[kMaxRep][kC],
+      sgam[kMaxRep][kC];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t bar_ld, bar_gp;
 
@@ -319,6 +324,44 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
   }
   tc::fence_after_sync();
 
+  // the gates of every V head reading this K head at once: two warps per
+  // head (32 tokens each) take g and beta and scan g; then the second half
+  // adds the first half's total, and G = e^c
+  for (int r0 = 0; r0 < p.rep; r0 += kPrepThreads / kC) {
+    const int r = r0 + (warp >> 1), t = 32 * (warp & 1) + lane;
+    if (r < p.rep) {
+      const int h = p.map == GDN_MAP_GROUPED ? kh * p.rep + r : kh + r * p.Hk;
+      float gt = 0.f, bt = 0.f;
+      if (t < L) {
+        if (pregate) {
+          gt = sga[r][t];
+          bt = sgb[r][t];
+        } else {
+          gt = gate_g(p.decay, p.decay_param[h], p.dt_bias[h], sga[r][t]);
+          bt = sigmoid_f(sgb[r][t]);
+        }
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, gt, o);
+        if (lane >= o) gt += u;
+      }
+      sc[r][t] = gt;
+      sbeta[r][t] = bt;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < p.rep * kC; e += kPrepThreads) {
+    const int r = e >> 6, t = e & 63;
+    if (t >= 32) sc[r][t] += sc[r][31];
+  }
+  __syncthreads();
+  for (int e = tid; e < p.rep * kC; e += kPrepThreads) {
+    const int r = e >> 6, t = e & 63;
+    sgam[r][t] = expf(sc[r][t]);
+  }
+  __syncthreads();
+
   float* Ap = reinterpret_cast<float*>(sm + P_OFF_A);
   float* Tp = reinterpret_cast<float*>(sm + P_OFF_T);
   float* Xp = reinterpret_cast<float*>(sm + P_OFF_X);
@@ -326,35 +369,6 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
   for (int r = 0; r < p.rep; ++r) {
     const int h = p.map == GDN_MAP_GROUPED ? kh * p.rep + r : kh + r * p.Hk;
     const size_t slot = (size_t)g * p.Hv + h;
-    // gates of this V head
-    if (tid < kC) {
-      float gt = 0.f, bt = 0.f;
-      if (tid < L) {
-        if (pregate) {
-          gt = sga[r][tid];
-          bt = sgb[r][tid];
-        } else {
-          gt = gate_g(p.decay, p.decay_param[h], p.dt_bias[h], sga[r][tid]);
-          bt = sigmoid_f(sgb[r][tid]);
-        }
-      }
-      sg[tid] = gt;
-      sbeta[tid] = bt;
-    }
-    __syncthreads();
-    if (warp < 2) {
-      float v = sg[tid];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
-      }
-      sc[tid] = v;
-    }
-    __syncthreads();
-    if (warp == 1) sc[tid] += sc[31];
-    __syncthreads();
-    if (tid < kC) sgam[tid] = expf(sc[tid]);
     // A (padded rows) and P (bf16, straight to the workspace) from the grams
     // of this K head, read again for each V head: thread (row, half) takes
     // 32 columns of row `row` of the M=128 accumulator (lane = row), A for
@@ -369,13 +383,13 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
       const int t = is_a ? row : row - kC;
       const bool live = t < L;
       constexpr float kLog2e = 1.4426950408889634f;
-      const float ct = sc[t] * kLog2e;
+      const float ct = sc[r][t] * kLog2e;
       if (is_a) {
-        const float bk = sbeta[t] * sinvk[t];
+        const float bk = sbeta[r][t] * sinvk[t];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int s = 32 * hc + e;
-          const float dec = exp2f(ct - sc[s] * kLog2e);  // e^{c_t - c_s} <= 1 for s <= t
+          const float dec = exp2f(ct - sc[r][s] * kLog2e);  // e^{c_t - c_s} <= 1 for s <= t
           Ap[t * kAStride + s] = (live && s < t) ? bk * dec * gv[e] * sinvk[s] : 0.f;
         }
       } else {
@@ -384,7 +398,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int s = 32 * hc + e;
-          const float dec = exp2f(ct - sc[s] * kLog2e);
+          const float dec = exp2f(ct - sc[r][s] * kLog2e);
           pr[e] = (live && s <= t) ? dec * gv[e] * iqt * sinvk[s] : 0.f;
         }
         uint4* dst = reinterpret_cast<uint4*>(w.tw + ((2 * HvG + slot) * kC + t) * kC + 32 * hc);
@@ -474,7 +488,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
         const int s = u0 + m;
-        x[m] = s <= tr ? Tp[tr * kC + s] * sbeta[s] : 0.f;
+        x[m] = s <= tr ? Tp[tr * kC + s] * sbeta[r][s] : 0.f;
       }
       uint4 h0, l0, h1, l1;
       split8(x, h0, l0);
@@ -490,12 +504,12 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
       const int t = tid;
       const bool live = t < L;
       float* vv = w.vec + slot * (4 * kC);
-      vv[t] = live ? sgam[t] * sinvk[t] : 0.f;
-      vv[kC + t] = live ? expf(sc[L - 1] - sc[t]) * sinvk[t] : 0.f;
-      vv[2 * kC + t] = live ? sgam[t] * sinvq[t] : 0.f;
-      vv[3 * kC + t] = t == 0 ? sgam[L - 1] : 0.f;
+      vv[t] = live ? sgam[r][t] * sinvk[t] : 0.f;
+      vv[kC + t] = live ? expf(sc[r][L - 1] - sc[r][t]) * sinvk[t] : 0.f;
+      vv[2 * kC + t] = live ? sgam[r][t] * sinvq[t] : 0.f;
+      vv[3 * kC + t] = t == 0 ? sgam[r][L - 1] : 0.f;
     }
-    __syncthreads();  // gate arrays, A and Tm are rewritten for the next V head
+    __syncthreads();  // A and Tm are rewritten for the next V head
   }
   tc::fence_before_sync();
   __syncthreads();
