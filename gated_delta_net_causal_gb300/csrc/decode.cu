@@ -21,7 +21,11 @@
 // boundaries, so while the consumer warps compute the next item's conv,
 // norms and gates, its state is already streaming in. The eight consumer
 // warps update rows in registers (a quarter-warp per 512-byte row) and write
-// them back to global memory with coalesced 16-byte stores.
+// them back to global memory with coalesced 16-byte stores. Per item there
+// is one barrier among the consumer warps (the item's q, k, v and gates are
+// in shared memory); each warp takes the l2 norms itself, and an item's
+// outputs are written after the next item's barrier, by when every warp has
+// finished its state pass, so they overlap the next item's stream.
 //
 // Every wait is bounded; a wait that gives up records GDN_ERR_TIMEOUT and
 // raises a CTA-wide abort flag, after which no warp waits again, so the
@@ -77,11 +81,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   static_assert(2 * D <= NC, "each consumer thread owns at most one q/k channel");
 
   extern __shared__ __align__(128) float ring[];
-  // per-item buffers written before an item's first barrier are doubled
-  // (by item parity) so a fast warp may start the next item while slow warps
-  // finish this one
-  __shared__ float sq[2][D], sk[2][D], sv[2][kDecMaxRep][D], so[kDecMaxRep][D];
-  __shared__ float sred[3][kDecCW];
+  // per-item buffers are doubled (by item parity): a fast warp may start the
+  // next item while slow warps finish this one, and an item's outputs are
+  // written during the next item
+  __shared__ float sq[2][D], sk[2][D], sv[2][kDecMaxRep][D], so[2][kDecMaxRep][D];
   __shared__ float sgate[2][kDecMaxRep][2];
   __shared__ float snw[D];
   __shared__ __align__(8) uint64_t full_bar[kDecMaxStages], empty_bar[kDecMaxStages];
@@ -192,7 +195,41 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   };
   prefetch(blockIdx.x);
 
+  // Outputs of an item (core output and/or gated norm, warp r < rep taking
+  // head r) are written after every warp has finished its state pass, i.e.
+  // past the next item's first barrier, so they overlap the next item's
+  // stream instead of holding every warp at a barrier of their own.
+  auto write_outputs = [&](int it, int pb, const T (&zz)[PER]) {
+    if (warp >= rep || *abort_flag) return;
+    const int b = it / Hk, kh = it - (it / Hk) * Hk;
+    const int r = warp;
+    const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+    const size_t obase = ((size_t)b * Hv + h) * D + lane * PER;
+    float ov[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) ov[e] = so[pb][r][lane * PER + e];
+    if (p.core_out != nullptr) {
+#pragma unroll
+      for (int e = 0; e < PER; ++e) p.core_out[obase + e] = ov[e];
+    }
+    if (p.z != nullptr) {
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) ss += ov[e] * ov[e];
+      ss = group_sum<32>(ss);
+      const float inv = 1.f / sqrtf(ss / (float)D + p.rms_eps);
+      T* outr = static_cast<T*>(p.out) + obase;
+#pragma unroll
+      for (int e = 0; e < PER; ++e)
+        outr[e] = from_f32<T>(ov[e] * inv * snw[lane * PER + e] * silu_f(to_f32(zz[e])));
+    }
+  };
+
   uint32_t k = 0;
+  int prev_item = -1, prev_buf = 0;
+  T zp[PER];  // z of the previous item, for its outputs
+#pragma unroll
+  for (int e = 0; e < PER; ++e) zp[e] = T();
   for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
     const int b = item / Hk, kh = item - (item / Hk) * Hk;
     T* cstate = static_cast<T*>(p.conv_state) + (size_t)b * C * 3;
@@ -243,34 +280,27 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         qk_x = cx[it];
       }
     }
+    // this item's q, k, v and gates are in shared memory, and every warp has
+    // finished the previous item's state pass
     consumer_sync();
+    if (prev_item >= 0) write_outputs(prev_item, prev_buf, zp);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) zp[e] = zc[e];
+    prev_item = item;
+    prev_buf = buf;
 
-    // l2 norms of q and k and k.q
-    {
-      float qq = 0.f, kk = 0.f, qk = 0.f;
-      for (int i = tid; i < D; i += NC) {
-        const float qv = sq[buf][i], kv = sk[buf][i];
-        qq += qv * qv;
-        kk += kv * kv;
-        qk += qv * kv;
-      }
-      qq = group_sum<32>(qq);
-      kk = group_sum<32>(kk);
-      qk = group_sum<32>(qk);
-      if (lane == 0) {
-        sred[0][warp] = qq;
-        sred[1][warp] = kk;
-        sred[2][warp] = qk;
-      }
-    }
-    consumer_sync();
+    // l2 norms of q and k and k.q, each warp over all D (no second barrier)
     float qq = 0.f, kk = 0.f, qkr = 0.f;
 #pragma unroll
-    for (int i = 0; i < kDecCW; ++i) {
-      qq += sred[0][i];
-      kk += sred[1][i];
-      qkr += sred[2][i];
+    for (int i = lane; i < D; i += 32) {
+      const float qv = sq[buf][i], kv = sk[buf][i];
+      qq = fmaf(qv, qv, qq);
+      kk = fmaf(kv, kv, kk);
+      qkr = fmaf(qv, kv, qkr);
     }
+    qq = group_sum<32>(qq);
+    kk = group_sum<32>(kk);
+    qkr = group_sum<32>(qkr);
     const float inv_q = 1.f / sqrtf(qq + p.l2_eps);
     const float inv_k = 1.f / sqrtf(kk + p.l2_eps);
     const float kq = qkr * inv_q * inv_k * p.scale;
@@ -349,48 +379,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
               n4.w = fmaf(d, kr[4 * m + 3], alpha * s4[u][m].w);
               __stcs(reinterpret_cast<float4*>(grow + 4 * sub + 4 * LPR * m), n4);
             }
-            if (sub == 0) so[r][row] = o;
+            if (sub == 0) so[buf][r][row] = o;
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[slot]);
       }
     }
-    consumer_sync();
 
-    // outputs: warp r finishes head r (core output and/or gated norm)
-    const bool live = !*abort_flag;
-    if (warp < rep && live) {
-      const int r = warp;
-      const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
-      const size_t obase = ((size_t)b * Hv + h) * D + lane * PER;
-      float ov[PER];
-#pragma unroll
-      for (int e = 0; e < PER; ++e) ov[e] = so[r][lane * PER + e];
-      if (p.core_out != nullptr) {
-#pragma unroll
-        for (int e = 0; e < PER; ++e) p.core_out[obase + e] = ov[e];
-      }
-      if (p.z != nullptr) {
-        float ss = 0.f;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) ss += ov[e] * ov[e];
-        ss = group_sum<32>(ss);
-        const float inv = 1.f / sqrtf(ss / (float)D + p.rms_eps);
-        T* outr = static_cast<T*>(p.out) + obase;
-#pragma unroll
-        for (int e = 0; e < PER; ++e)
-          outr[e] = from_f32<T>(ov[e] * inv * snw[lane * PER + e] * silu_f(to_f32(zc[e])));
-      }
-    }
     // new q/k conv state: this CTA read the old values itself, in the prologue
-    if (qk_c >= 0 && live) {
+    if (qk_c >= 0 && !*abort_flag) {
       T* cp = cstate + (size_t)qk_c * 3;
       cp[0] = qk_s1;
       cp[1] = qk_s2;
       cp[2] = qk_x;
     }
   }
+  // every warp has finished the last item's state pass: its outputs
+  consumer_sync();
+  if (prev_item >= 0) write_outputs(prev_item, prev_buf, zp);
 }
 
 static int sm_count() {
