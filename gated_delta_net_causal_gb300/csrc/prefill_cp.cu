@@ -177,9 +177,8 @@ __global__ void __launch_bounds__(1024) cp_index_kernel(const PrefillArgs p, con
 // scales are taken from it; the per-V-head matrices then reuse its space.
 constexpr uint32_t P_OFF_KQ = 0;       // bf16 [128][128 i] SW128 (TMA): rows 0-63 k, 64-127 q
 constexpr uint32_t P_OFF_A = 0;        // fp32 [64][65]
-constexpr uint32_t P_OFF_T = 16640;    // fp32 [64][64] Tm
-constexpr uint32_t P_OFF_X = 33024;    // fp32 [768] block-product scratch
-constexpr uint32_t P_SMEM = 36096 + 1024;
+constexpr uint32_t P_OFF_T = 16640;    // fp32 [64][64] Tm (products in its upper triangle)
+constexpr uint32_t P_SMEM = 33024 + 1024;
 
 __global__ void __launch_bounds__(kPrepThreads, 4)
     cp_prep_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
@@ -364,7 +363,6 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
 
   float* Ap = reinterpret_cast<float*>(sm + P_OFF_A);
   float* Tp = reinterpret_cast<float*>(sm + P_OFF_T);
-  float* Xp = reinterpret_cast<float*>(sm + P_OFF_X);
   const size_t HvG = (size_t)w.G * p.Hv;
   for (int r = 0; r < p.rep; ++r) {
     const int h = p.map == GDN_MAP_GROUPED ? kh * p.rep + r : kh + r * p.Hk;
@@ -411,8 +409,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
     }
     __syncthreads();
     // (I + A)^{-1}: diagonal 16x16 blocks by forward substitution (warp b,
-    // lane l holds column l of block b), then the off-diagonal blocks one
-    // block diagonal at a time: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
+    // lane l holds column l of block b; zeros above the diagonal written)
     if (warp < 4) {
       const int b0 = 16 * warp, l = lane & 15;
       float x[16];
@@ -430,54 +427,81 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
 #pragma unroll
         for (int m = 0; m < 16; ++m) Tp[(b0 + m) * kC + b0 + l] = x[m];
       }
+    } else {
+      // zeros above the diagonal in the two 32x32 diagonal blocks too (rows
+      // 0-15 x columns 16-31 and rows 32-47 x columns 48-63), so the doubling
+      // below runs fixed-length loops over whole blocks
+      const int e = tid - 128, zr = e >> 3, zc = (e & 7) * 2;
+      *reinterpret_cast<float2*>(Tp + zr * kC + 16 + zc) = make_float2(0.f, 0.f);
+      *reinterpret_cast<float2*>(Tp + (32 + zr) * kC + 48 + zc) = make_float2(0.f, 0.f);
     }
     __syncthreads();
-    // off-diagonal blocks, one block diagonal d at a time, 64 threads per
-    // block and a 2 x 2 output tile per thread:
-    //   X = sum_{kb=jb}^{ib-1} A_{ib,kb} T_{kb,jb},  T_{ib,jb} = -T_{ib,ib} X
-    for (int d = 1; d < 4; ++d) {
-      const int nblk = 4 - d;
-      const int jb = tid >> 6, q = tid & 63, r0 = (q >> 3) * 2, c0 = (q & 7) * 2, ib = jb + d;
-      const bool act = tid < nblk * 64;
-      if (act) {
-        const float* a0 = Ap + (16 * ib + r0) * kAStride + 16 * jb;
-        const float* a1 = a0 + kAStride;
-        const float* tc0 = Tp + (16 * jb) * kC + 16 * jb + c0;
-        float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
-        for (int kk = 0; kk < 16 * d; kk += 16) {
+    // The rest by doubling, T = [[T1, 0], [-T2 A21 T1, T2]] for the lower
+    // triangular blocks: first both 32x32 diagonal blocks from their 16x16
+    // ones, then the whole 64x64 from the two 32x32. Each product X = A21 T1
+    // is kept in the (otherwise unused) upper-right 32x32 block of Tm before
+    // -T2 X is formed; the loops run over whole blocks, the zeros above the
+    // diagonal of T1 and T2 masking what a triangular loop would skip.
+    {
+      // 16 -> 32: block B's rows 16-31 x columns 0-15, one row and two
+      // columns per thread; X at Tm[r][32 + 16 B + c]
+      const int B = tid >> 7, u = tid & 127, r = u >> 3, c = (u & 7) * 2, o = 32 * B;
+      const float* arow = Ap + (o + 16 + r) * kAStride + o;
+      float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 tv = *reinterpret_cast<const float2*>(tc0 + (kk + k) * kC);
-            const float av0 = a0[kk + k], av1 = a1[kk + k];
-            x00 = fmaf(av0, tv.x, x00);
-            x01 = fmaf(av0, tv.y, x01);
-            x10 = fmaf(av1, tv.x, x10);
-            x11 = fmaf(av1, tv.y, x11);
-          }
-        }
-        float* xb = Xp + (jb << 8) + r0 * 16 + c0;
-        *reinterpret_cast<float2*>(xb) = make_float2(x00, x01);
-        *reinterpret_cast<float2*>(xb + 16) = make_float2(x10, x11);
+      for (int q = 0; q < 16; ++q) {
+        const float2 tv = *reinterpret_cast<const float2*>(Tp + (o + q) * kC + o + c);
+        const float av = arow[q];
+        x0 = fmaf(av, tv.x, x0);
+        x1 = fmaf(av, tv.y, x1);
       }
+      *reinterpret_cast<float2*>(Tp + r * kC + 32 + 16 * B + c) = make_float2(x0, x1);
       __syncthreads();
-      if (act) {
-        const float* t0 = Tp + (16 * ib + r0) * kC + 16 * ib;
-        const float* t1 = t0 + kC;
-        const float* xb = Xp + (jb << 8) + c0;
-        float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+      const float* trow = Tp + (o + 16 + r) * kC + o + 16;
+      float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float2 xv = *reinterpret_cast<const float2*>(xb + m * 16);
-          const float tv0 = m <= r0 ? t0[m] : 0.f, tv1 = m <= r0 + 1 ? t1[m] : 0.f;
-          y00 = fmaf(tv0, xv.x, y00);
-          y01 = fmaf(tv0, xv.y, y01);
-          y10 = fmaf(tv1, xv.x, y10);
-          y11 = fmaf(tv1, xv.y, y11);
-        }
-        float* tout = Tp + (16 * ib + r0) * kC + 16 * jb + c0;
-        *reinterpret_cast<float2*>(tout) = make_float2(-y00, -y01);
-        *reinterpret_cast<float2*>(tout + kC) = make_float2(-y10, -y11);
+      for (int q = 0; q < 16; ++q) {
+        const float2 xv = *reinterpret_cast<const float2*>(Tp + q * kC + 32 + 16 * B + c);
+        const float tv = trow[q];
+        y0 = fmaf(tv, xv.x, y0);
+        y1 = fmaf(tv, xv.y, y1);
       }
+      *reinterpret_cast<float2*>(Tp + (o + 16 + r) * kC + o + c) = make_float2(-y0, -y1);
+      __syncthreads();
+    }
+    {
+      // 32 -> 64: rows 32-63 x columns 0-31, a 2 x 2 tile per thread; X at
+      // Tm[r][32 + c]
+      const int r0 = (tid >> 4) * 2, c0 = (tid & 15) * 2;
+      const float* a0 = Ap + (32 + r0) * kAStride;
+      const float* a1 = a0 + kAStride;
+      float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const float2 tv = *reinterpret_cast<const float2*>(Tp + q * kC + c0);
+        const float av0 = a0[q], av1 = a1[q];
+        x00 = fmaf(av0, tv.x, x00);
+        x01 = fmaf(av0, tv.y, x01);
+        x10 = fmaf(av1, tv.x, x10);
+        x11 = fmaf(av1, tv.y, x11);
+      }
+      *reinterpret_cast<float2*>(Tp + r0 * kC + 32 + c0) = make_float2(x00, x01);
+      *reinterpret_cast<float2*>(Tp + (r0 + 1) * kC + 32 + c0) = make_float2(x10, x11);
+      __syncthreads();
+      const float* t0 = Tp + (32 + r0) * kC + 32;
+      const float* t1 = t0 + kC;
+      float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const float2 xv = *reinterpret_cast<const float2*>(Tp + q * kC + 32 + c0);
+        const float tv0 = t0[q], tv1 = t1[q];
+        y00 = fmaf(tv0, xv.x, y00);
+        y01 = fmaf(tv0, xv.y, y01);
+        y10 = fmaf(tv1, xv.x, y10);
+        y11 = fmaf(tv1, xv.y, y11);
+      }
+      *reinterpret_cast<float2*>(Tp + (32 + r0) * kC + c0) = make_float2(-y00, -y01);
+      *reinterpret_cast<float2*>(Tp + (32 + r0 + 1) * kC + c0) = make_float2(-y10, -y11);
       __syncthreads();
     }
     // Tb = Tm diag(beta) as hi + lo bf16, zero above the diagonal; 16
