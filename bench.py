@@ -276,6 +276,7 @@ def run_gpu(args, ws, rank, local):
     # chunked prefill block and the varlen whole-path block
     prefill = run_prefill(args, peaks, ws) if not args.no_prefill else None
     varlen = run_varlen(args, ws) if not args.no_prefill else None
+    multilayer = run_multilayer(args, ws, peaks) if not args.no_multilayer else None
     clk = clocks.stop()
     if clk is not None:
         clk["window"] = "decode warm-up through the prefill blocks (brackets the timed steps)"
@@ -324,6 +325,8 @@ def run_gpu(args, ws, rank, local):
         line["prefill"] = prefill
     if varlen is not None:
         line["varlen_path"] = varlen
+    if multilayer is not None:
+        line["multilayer_decode"] = multilayer
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = cpu_baseline_decode(seconds=args.cpu_seconds)
     return line
@@ -447,6 +450,63 @@ def run_varlen(args, ws):
             "launches_per_pass": 2 + 3 + 16}
 
 
+def run_multilayer(args, ws, peaks):
+    """Large-batch multi-layer decode: 48 layers back to back on one stream,
+    each one token per sequence for B=128 sequences (Hk=16, Hv=48, D=128,
+    Grouped, log-rate decay with A_log = ln U[1,16] and dt_bias ~ U(-0.5,
+    0.5), bf16 activations ~N(0,1), fp32 states ~N(0,0.02)). Every layer has
+    its own state (384 MiB; 18 GiB for the 48), conv state, weights and
+    activations, so no layer finds its state in L2; one step = all 48 layers,
+    timed with CUDA events on the launching stream."""
+    import gated_delta_net_causal_gb300 as gdn
+    nl, B, Hk, Hv, D = 48, 128, 16, 48, 128
+    C = (2 * Hk + Hv) * D
+    gen = torch.Generator(device="cuda").manual_seed(gi.SEED_BASE + 2)
+    bf = torch.bfloat16
+
+    def rn(*shape, std=1.0, dtype=bf):
+        return (torch.randn(shape, device="cuda", generator=gen) * std).to(dtype)
+    d = gdn.dims(Hk, Hv, D, map=gdn.GDN_MAP_GROUPED, decay=gdn.GDN_DECAY_LOG_RATE, io_dtype=bf)
+    nw = (0.82 + 0.013 * torch.arange(D, device="cuda")).float()
+    layers = []
+    for _ in range(nl):
+        layers.append({
+            "state": rn(B, Hv, D, D, std=0.02, dtype=torch.float32), "cs": rn(B, C, 3, std=0.1),
+            "w": rn(C, 4, std=0.16),
+            "dp": torch.log(torch.rand(Hv, device="cuda", generator=gen) * 15 + 1),
+            "dt": torch.rand(Hv, device="cuda", generator=gen) - 0.5,
+            "x": rn(B, C), "a": rn(B, Hv), "b": rn(B, Hv), "z": rn(B, Hv, D),
+            "out": torch.empty((B, Hv, D), device="cuda", dtype=bf)})
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for L in layers:
+            gdn.gdn_decode_step(d, L["x"], L["a"], L["b"], L["dp"], L["dt"], L["w"], L["cs"],
+                                L["state"], z=L["z"], norm_w=nw, out=L["out"])
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = 5
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t = _barrier_max(statistics.mean(a.elapsed_time(b) * 1e-3 for a, b in ev), ws)
+    state_bytes = 2 * nl * B * Hv * D * D * 4
+    gbs = ws * state_bytes / t / 1e9
+    del layers
+    torch.cuda.empty_cache()
+    return {"workload": "multi-layer decode: 48 layers x B=128 x 1 token back to back, Hk=16 "
+                        "Hv=48 D=128, Grouped, log-rate, bf16 activations, fp32 states (18 GiB)",
+            "value": round(gbs, 2), "unit": "GB/s", "metric": "decode state GB/s",
+            "ms_per_step": round(t * 1e3, 4), "hbm_frac_state": round(gbs / ws / peaks["hbm_gbs"], 4),
+            "us_per_layer": round(t * 1e6 / nl, 2), "launches_per_step": nl,
+            "l2": "inputs larger than L2 (each layer's state 384 MiB)"}
+
+
 # --------------------------------------------------------------- CPU oracle arm
 
 def cpu_baseline_decode(seconds: float = 15.0, threads: int = None):
@@ -515,6 +575,7 @@ def main():
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-multilayer", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
