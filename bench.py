@@ -350,6 +350,7 @@ def run_gpu(args, ws, rank, local):
     prefill = run_prefill(args, peaks, ws) if not args.no_prefill else None
     varlen = run_varlen(args, ws) if not args.no_prefill else None
     multilayer = run_multilayer(args, ws, peaks) if not args.no_multilayer else None
+    slot_dec = run_slot_decode(args, ws, peaks) if not args.no_multilayer else None
     clk = clocks.stop()
     if clk is not None:
         clk["window"] = "decode warm-up through the prefill blocks (brackets the timed steps)"
@@ -417,6 +418,8 @@ def run_gpu(args, ws, rank, local):
         line["varlen_path"] = varlen
     if multilayer is not None:
         line["multilayer_decode"] = multilayer
+    if slot_dec is not None:
+        line["slot_decode"] = slot_dec
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = cpu_baseline_decode(seconds=args.cpu_seconds)
     return line
@@ -609,6 +612,63 @@ def run_multilayer(args, ws, peaks):
             "timing": "one step = the 48 layer launches as one CUDA graph replay between two "
                       "CUDA events; mean of 5 steps after 2 eager steps and one replay",
             "l2": "inputs larger than L2 (each layer's state 384 MiB)"}
+
+
+def run_slot_decode(args, ws, peaks):
+    """The batched-decode shape (B=64, Hk=16, Hv=32, D=128, Tiled,
+    negative-rate, bf16) through gdn_decode_step_slots: the 64 rows name
+    slots of a pool of 256 states (fp32 ~N(0, 0.02), 512 MiB). Four slot
+    tables, one seeded permutation of the pool cut in four, are cycled step
+    by step, so a step's states were last touched four steps earlier (inputs
+    larger than L2). Timed like the headline: the K steps as one CUDA graph."""
+    import gated_delta_net_causal_gb300 as gdn
+    B, P, Hv, D = 64, 256, 32, 128
+    gdn_, d, dev, steps, host, state, cstate, out, shape = _decode_setup(B, 16, 0)
+    del host, state, cstate
+    gen = torch.Generator(device="cuda").manual_seed(gi.SEED_BASE + 6)
+    pool = torch.randn((P, Hv, D, D), device="cuda", generator=gen) * 0.02
+    cpool = (torch.randn((P, shape.qkv_features, 3), device="cuda", generator=gen) * 0.1).to(
+        torch.bfloat16)
+    perm = torch.randperm(P, device="cuda", generator=gen).to(torch.int32)
+    tables = [perm[i * B:(i + 1) * B].contiguous() for i in range(P // B)]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        inp = steps[i % 16]
+        gdn.gdn_decode_step_slots(d, tables[i % len(tables)], inp["x"], inp["a"], inp["b"],
+                                  dev["decay_param"], dev["dt_bias"], dev["conv_w"], cpool, pool,
+                                  z=inp["z"], norm_w=dev["norm_w"], out=out)
+
+    for i in range(max(args.warmup, 4)):
+        step(i)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(args.steps):
+                step(i)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t = _barrier_max(ev0.elapsed_time(ev1) * 1e-3 / args.steps, ws)
+    del graph, pool, cpool
+    torch.cuda.empty_cache()
+    state_bytes = 2 * B * Hv * D * D * 4
+    gbs = ws * state_bytes / t / 1e9
+    return {"workload": "batched decode through a state-slot table: B=64 rows in a pool of 256 "
+                        "slots, Hk=16 Hv=32 D=128, Tiled, negative-rate, bf16",
+            "value": round(gbs, 2), "unit": "GB/s", "metric": "decode state GB/s",
+            "ms_per_step": round(t * 1e3, 5),
+            "hbm_frac_state": round(gbs / ws / peaks["hbm_gbs"], 4),
+            "l2": "inputs larger than L2: four disjoint slot tables of 64 cycled (512 MiB pool)",
+            "timing": f"the {args.steps} consecutive steps as one CUDA graph replay"}
 
 
 # --------------------------------------------------------------- CPU oracle arm

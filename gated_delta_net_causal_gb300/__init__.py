@@ -73,6 +73,9 @@ def library() -> ctypes.CDLL:
         L.gdn_conv_update.argtypes = [pd, i32, vp, i64, vp, vp, vp, vp, vp]
         L.gdn_decode_step.restype = ctypes.c_int
         L.gdn_decode_step.argtypes = [pd, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.gdn_decode_step_slots.restype = ctypes.c_int
+        L.gdn_decode_step_slots.argtypes = [pd, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                            vp, vp, vp, vp]
         L.gdn_prefill_chunked.restype = ctypes.c_int
         L.gdn_prefill_chunked.argtypes = [pd, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, vp, vp,
                                           vp, i32, vp, vp, vp, vp, vp, vp, i64, vp]
@@ -147,6 +150,30 @@ def gdn_decode_step(d: GdnDims, mixed_qkv, a, b, decay_param, dt_bias, conv_w, c
         _ptr(conv_w, "conv_w", io), _ptr(conv_state, "conv_state", io),
         _ptr(state, "state", f32), _ptr(core_out, "core_out", f32), _ptr(z, "z", io),
         _ptr(norm_w, "norm_w", f32), _ptr(out, "out", io), _stream(stream)), "gdn_decode_step")
+    return core_out, out
+
+
+def gdn_decode_step_slots(d: GdnDims, state_slots, mixed_qkv, a, b, decay_param, dt_bias, conv_w,
+                          conv_state, state, core_out=None, z=None, norm_w=None, out=None,
+                          stream=None):
+    """gdn_decode_step where batch row b works on state[state_slots[b]] and
+    conv_state[state_slots[b]] of a pool (state [P][Hv][D][D], conv_state
+    [P][C][3]); a negative slot marks a padded row."""
+    io = _io(d)
+    batch = mixed_qkv.shape[0]
+    if state_slots.numel() != batch:
+        raise ValueError("state_slots must hold one entry per batch row")
+    if conv_state.shape[0] != state.shape[0]:
+        raise ValueError("state and conv_state must hold the same number of slots")
+    f32 = torch.float32
+    _check(library().gdn_decode_step_slots(
+        ctypes.byref(d), batch, _ptr(state_slots, "state_slots", torch.int32), state.shape[0],
+        _ptr(mixed_qkv, "mixed_qkv", io), _ptr(a, "a", io), _ptr(b, "b", io),
+        _ptr(decay_param, "decay_param", f32), _ptr(dt_bias, "dt_bias", f32),
+        _ptr(conv_w, "conv_w", io), _ptr(conv_state, "conv_state", io),
+        _ptr(state, "state", f32), _ptr(core_out, "core_out", f32), _ptr(z, "z", io),
+        _ptr(norm_w, "norm_w", f32), _ptr(out, "out", io), _stream(stream)),
+        "gdn_decode_step_slots")
     return core_out, out
 
 
@@ -263,7 +290,7 @@ def gdn_version() -> int:
 
 
 __all__ = ["GdnDims", "GdnError", "dims", "library", "status_string", "gdn_conv_update",
-           "gdn_decode_step", "gdn_prefill_chunked", "gdn_prefill_workspace_size",
+           "gdn_decode_step", "gdn_decode_step_slots", "gdn_prefill_chunked", "gdn_prefill_workspace_size",
            "gdn_prefill_chunked_static", "GDN_STATIC_SCRATCH_BYTES", "gdn_gated_rmsnorm", "gdn_device_error",
            "gdn_qkv_features", "gdn_version", "GDN_MAP_GROUPED", "GDN_MAP_TILED",
            "GDN_DECAY_LOG_RATE", "GDN_DECAY_NEGATIVE_RATE", "GDN_F16", "GDN_BF16", "GDN_F32",

@@ -64,6 +64,82 @@ int64_t qkv_features(const gdn_dims* d) {
 
 gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
 
+// Shared by gdn_decode_step (slots == nullptr: row b owns slot b, num_slots
+// = batch) and gdn_decode_step_slots.
+gdn_status decode_impl(const gdn_dims* dims, int32_t batch, const int32_t* slots,
+                       int32_t num_slots, const void* mixed_qkv, const void* a, const void* b,
+                       const float* decay_param, const float* dt_bias, const void* conv_w,
+                       void* conv_state, float* state, float* core_out, const void* z,
+                       const float* norm_w, void* out, void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (batch < 0 || num_slots < 0) return GDN_ERR_INVALID_ARG;
+  if (batch > kMaxGridY) return GDN_ERR_EXTENT;
+  const int rep = dims->n_v_heads / dims->n_k_heads;
+  if (rep > 8) return GDN_ERR_UNSUPPORTED;
+  if (batch == 0) return GDN_OK;
+  if (!mixed_qkv || !a || !b || !decay_param || !dt_bias || !conv_w || !conv_state || !state)
+    return GDN_ERR_INVALID_ARG;
+  if (slots != nullptr && !aligned16(slots)) return GDN_ERR_ALIGN;
+  if (core_out == nullptr && z == nullptr) return GDN_ERR_INVALID_ARG;
+  if (z != nullptr && (norm_w == nullptr || out == nullptr)) return GDN_ERR_INVALID_ARG;
+  const void* ptrs[] = {mixed_qkv, a, b, decay_param, dt_bias, conv_w, conv_state, state};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return GDN_ERR_ALIGN;
+  if ((core_out && !aligned16(core_out)) || (z && (!aligned16(z) || !aligned16(norm_w) || !aligned16(out))))
+    return GDN_ERR_ALIGN;
+  const int64_t es = dtype_size(dims->io_dtype);
+  const int64_t C = qkv_features(dims), Hv = dims->n_v_heads, D = dims->head_dim;
+  int64_t state_bytes = 0, tmp = 0;
+  if (!mul_ok((int64_t)num_slots * Hv, D * D * 4, &state_bytes)) return GDN_ERR_EXTENT;
+  if (!mul_ok((int64_t)num_slots, C * 3 * es, &tmp)) return GDN_ERR_EXTENT;
+  const int64_t conv_bytes = tmp;
+  const int64_t x_bytes = (int64_t)batch * C * es;
+  const int64_t o_bytes_f32 = (int64_t)batch * Hv * D * 4;
+  const int64_t o_bytes_io = (int64_t)batch * Hv * D * es;
+  const int64_t gate_bytes = (int64_t)batch * Hv * es;
+  const Range inputs[] = {range_of(mixed_qkv, x_bytes), range_of(a, gate_bytes),
+                          range_of(b, gate_bytes),      range_of(decay_param, Hv * 4),
+                          range_of(dt_bias, Hv * 4),    range_of(conv_w, C * 4 * es),
+                          range_of(z, z ? o_bytes_io : 0), range_of(norm_w, norm_w ? D * 4 : 0),
+                          range_of(slots, slots ? (int64_t)batch * 4 : 0)};
+  const Range rs = range_of(state, state_bytes), rc = range_of(conv_state, conv_bytes);
+  const Range ro = range_of(core_out, core_out ? o_bytes_f32 : 0);
+  const Range ry = range_of(out, z ? o_bytes_io : 0);
+  for (const Range& in : inputs) {
+    if (overlap(rs, in) || overlap(rc, in) || overlap(ro, in) || overlap(ry, in)) return GDN_ERR_ALIAS;
+  }
+  if (overlap(rs, rc) || overlap(rs, ro) || overlap(rs, ry) || overlap(rc, ro) || overlap(rc, ry) ||
+      overlap(ro, ry))
+    return GDN_ERR_ALIAS;
+  DecodeArgs p{};
+  p.mixed_qkv = mixed_qkv;
+  p.a = a;
+  p.b = b;
+  p.decay_param = decay_param;
+  p.dt_bias = dt_bias;
+  p.conv_w = conv_w;
+  p.conv_state = conv_state;
+  p.state = state;
+  p.core_out = core_out;
+  p.z = z;
+  p.norm_w = norm_w;
+  p.out = out;
+  p.slots = slots;
+  p.num_slots = num_slots;
+  p.Hk = dims->n_k_heads;
+  p.Hv = dims->n_v_heads;
+  p.rep = rep;
+  p.map = dims->map;
+  p.decay = dims->decay;
+  p.C = (int32_t)C;
+  p.l2_eps = dims->l2_eps;
+  p.rms_eps = dims->rms_eps;
+  p.scale = 1.0f / sqrtf((float)D);
+  return cuda_status(gdn::launch_decode(p, dims->io_dtype, dims->head_dim, batch,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -133,69 +209,19 @@ gdn_status gdn_decode_step(const gdn_dims* dims, int32_t batch, const void* mixe
                            const float* dt_bias, const void* conv_w, void* conv_state,
                            float* state, float* core_out, const void* z, const float* norm_w,
                            void* out, void* stream) {
-  gdn_status st = check_dims(dims);
-  if (st != GDN_OK) return st;
-  if (batch < 0) return GDN_ERR_INVALID_ARG;
-  if (batch > kMaxGridY) return GDN_ERR_EXTENT;
-  const int rep = dims->n_v_heads / dims->n_k_heads;
-  if (rep > 8) return GDN_ERR_UNSUPPORTED;
-  if (batch == 0) return GDN_OK;
-  if (!mixed_qkv || !a || !b || !decay_param || !dt_bias || !conv_w || !conv_state || !state)
-    return GDN_ERR_INVALID_ARG;
-  if (core_out == nullptr && z == nullptr) return GDN_ERR_INVALID_ARG;
-  if (z != nullptr && (norm_w == nullptr || out == nullptr)) return GDN_ERR_INVALID_ARG;
-  const void* ptrs[] = {mixed_qkv, a, b, decay_param, dt_bias, conv_w, conv_state, state};
-  for (const void* q : ptrs)
-    if (!aligned16(q)) return GDN_ERR_ALIGN;
-  if ((core_out && !aligned16(core_out)) || (z && (!aligned16(z) || !aligned16(norm_w) || !aligned16(out))))
-    return GDN_ERR_ALIGN;
-  const int64_t es = dtype_size(dims->io_dtype);
-  const int64_t C = qkv_features(dims), Hv = dims->n_v_heads, D = dims->head_dim;
-  int64_t state_bytes = 0, tmp = 0;
-  if (!mul_ok((int64_t)batch * Hv, D * D * 4, &state_bytes)) return GDN_ERR_EXTENT;
-  if (!mul_ok((int64_t)batch, C * 3 * es, &tmp)) return GDN_ERR_EXTENT;
-  const int64_t conv_bytes = tmp;
-  const int64_t x_bytes = (int64_t)batch * C * es;
-  const int64_t o_bytes_f32 = (int64_t)batch * Hv * D * 4;
-  const int64_t o_bytes_io = (int64_t)batch * Hv * D * es;
-  const int64_t gate_bytes = (int64_t)batch * Hv * es;
-  const Range inputs[] = {range_of(mixed_qkv, x_bytes), range_of(a, gate_bytes),
-                          range_of(b, gate_bytes),      range_of(decay_param, Hv * 4),
-                          range_of(dt_bias, Hv * 4),    range_of(conv_w, C * 4 * es),
-                          range_of(z, z ? o_bytes_io : 0), range_of(norm_w, norm_w ? D * 4 : 0)};
-  const Range rs = range_of(state, state_bytes), rc = range_of(conv_state, conv_bytes);
-  const Range ro = range_of(core_out, core_out ? o_bytes_f32 : 0);
-  const Range ry = range_of(out, z ? o_bytes_io : 0);
-  for (const Range& in : inputs) {
-    if (overlap(rs, in) || overlap(rc, in) || overlap(ro, in) || overlap(ry, in)) return GDN_ERR_ALIAS;
-  }
-  if (overlap(rs, rc) || overlap(rs, ro) || overlap(rs, ry) || overlap(rc, ro) || overlap(rc, ry) ||
-      overlap(ro, ry))
-    return GDN_ERR_ALIAS;
-  DecodeArgs p{};
-  p.mixed_qkv = mixed_qkv;
-  p.a = a;
-  p.b = b;
-  p.decay_param = decay_param;
-  p.dt_bias = dt_bias;
-  p.conv_w = conv_w;
-  p.conv_state = conv_state;
-  p.state = state;
-  p.core_out = core_out;
-  p.z = z;
-  p.norm_w = norm_w;
-  p.out = out;
-  p.Hk = dims->n_k_heads;
-  p.Hv = dims->n_v_heads;
-  p.rep = rep;
-  p.map = dims->map;
-  p.decay = dims->decay;
-  p.C = (int32_t)C;
-  p.l2_eps = dims->l2_eps;
-  p.rms_eps = dims->rms_eps;
-  p.scale = 1.0f / sqrtf((float)D);
-  return cuda_status(gdn::launch_decode(p, dims->io_dtype, dims->head_dim, batch,
-                                        static_cast<cudaStream_t>(stream)));
+  return decode_impl(dims, batch, nullptr, batch, mixed_qkv, a, b, decay_param, dt_bias, conv_w,
+                     conv_state, state, core_out, z, norm_w, out, stream);
+}
+
+gdn_status gdn_decode_step_slots(const gdn_dims* dims, int32_t batch, const int32_t* state_slots,
+                                 int32_t num_slots, const void* mixed_qkv, const void* a,
+                                 const void* b, const float* decay_param, const float* dt_bias,
+                                 const void* conv_w, void* conv_state, float* state,
+                                 float* core_out, const void* z, const float* norm_w, void* out,
+                                 void* stream) {
+  if (state_slots == nullptr) return GDN_ERR_INVALID_ARG;
+  return decode_impl(dims, batch, state_slots, num_slots, mixed_qkv, a, b, decay_param, dt_bias,
+                     conv_w, conv_state, state, core_out, z, norm_w, out, stream);
 }
 
 gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int32_t* cu_seqlens,

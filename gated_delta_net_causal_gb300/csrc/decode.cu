@@ -27,6 +27,13 @@
 // outputs are written after the next item's barrier, by when every warp has
 // finished its state pass, so they overlap the next item's stream.
 //
+// With a state-slot table, batch row b works on state[slots[b]] and
+// conv_state[slots[b]] of a larger pool (every other tensor is still indexed
+// by b). The producer and the consumers look the slot up themselves and skip
+// a padded row (negative slot) or an out-of-range one alike, so their ring
+// positions stay in step; such a row touches neither state and gets zero
+// core outputs.
+//
 // Every wait is bounded; a wait that gives up records GDN_ERR_TIMEOUT and
 // raises a CTA-wide abort flag, after which no warp waits again, so the
 // kernel always runs to its end.
@@ -70,7 +77,7 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kDecCW * 32) : "memory");
 }
 
-template <typename T, int D, int REPMAX>
+template <typename T, int D, int REPMAX, bool SLOTS>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_step_kernel(const DecodeArgs p, const int num_items) {
   using G = DecGeom<D>;
@@ -105,15 +112,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
   volatile int* abort_flag = &s_abort;
 
+  // state slot of batch row b, or -1 for a padded or out-of-range row (the
+  // plain call is compiled without the table: slot b, never -1)
+  auto slot_of = [&](int b) -> int {
+    if (!SLOTS) return b;
+    const int s = __ldg(p.slots + b);
+    return (s >= 0 && s < p.num_slots) ? s : -1;
+  };
+
   if (warp == kDecCW) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t k = 0;
       for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
         const int b = item / Hk, kh = item - (item / Hk) * Hk;
+        const int sb = slot_of(b);
+        if (SLOTS && sb < 0) continue;
         for (int r = 0; r < rep; ++r) {
           const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
-          const float* gS = p.state + ((size_t)b * Hv + h) * (size_t)(D * D);
+          const float* gS = p.state + ((size_t)sb * Hv + h) * (size_t)(D * D);
           for (int c = 0; c < G::CPH; ++c, ++k) {
             const int slot = (int)(k % kDecStages);
             if (k >= (uint32_t)kDecStages &&
@@ -147,14 +164,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     for (int j = tid; j < D; j += NC) snw[j] = p.norm_w[j];
   auto prefetch = [&](int item) {
     const int b = item / Hk, kh = item - (item / Hk) * Hk;
+    const int sb = SLOTS ? (item < num_items ? slot_of(b) : -1) : b;
     const T* xrow = static_cast<const T*>(p.mixed_qkv) + (size_t)b * C;
-    const T* cst = static_cast<const T*>(p.conv_state) + (size_t)b * C * 3;
+    const T* cst = static_cast<const T*>(p.conv_state) + (size_t)(SLOTS && sb < 0 ? 0 : sb) * C * 3;
     const int nch = (2 + rep) * D;
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
       const int idx = tid + it * NC;
       pchan[it] = -1;
-      if (item < num_items && idx < nch) {
+      if (item < num_items && (!SLOTS || sb >= 0) && idx < nch) {
         const int which = idx / D, i = idx - which * D;
         int c;
         if (which < 2) {
@@ -232,7 +250,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   for (int e = 0; e < PER; ++e) zp[e] = T();
   for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
     const int b = item / Hk, kh = item - (item / Hk) * Hk;
-    T* cstate = static_cast<T*>(p.conv_state) + (size_t)b * C * 3;
+    const int sb = slot_of(b);  // the producer skipped this row's state too if < 0
+    if (SLOTS && sb < 0 && tid == 0 && kh == 0 && __ldg(p.slots + b) >= p.num_slots)
+      record_device_error(GDN_ERR_EXTENT);
+    T* cstate = static_cast<T*>(p.conv_state) + (size_t)(SLOTS && sb < 0 ? 0 : sb) * C * 3;
     const int buf = ((item - (int)blockIdx.x) / (int)gridDim.x) & 1;
     T cs1[NIT], cs2[NIT], cx[NIT];
     int chan[NIT];
@@ -318,10 +339,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
     }
 
+    // a row without a state slot: zero core outputs, no state pass (its
+    // conv channels were never loaded, so no conv state is written either)
+    if (SLOTS && sb < 0) {
+      for (int j = tid; j < rep * D; j += NC) so[buf][j / D][j - (j / D) * D] = 0.f;
+      continue;
+    }
+
     // the state pass over the item's heads, chunk by chunk from the ring
     for (int r = 0; r < rep; ++r) {
       const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
-      float* gS = p.state + ((size_t)b * Hv + h) * (size_t)(D * D);
+      float* gS = p.state + ((size_t)sb * Hv + h) * (size_t)(D * D);
       const float alpha = sgate[buf][r][0], beta = sgate[buf][r][1];
       for (int c = 0; c < G::CPH; ++c, ++k) {
         const int slot = (int)(k % kDecStages);
@@ -415,7 +443,8 @@ static int sm_count() {
 
 template <typename T, int D, int REPMAX>
 static cudaError_t launch_decode_t(const DecodeArgs& p, int32_t batch, cudaStream_t stream) {
-  auto kern = decode_step_kernel<T, D, REPMAX>;
+  auto kern = p.slots != nullptr ? decode_step_kernel<T, D, REPMAX, true>
+                                 : decode_step_kernel<T, D, REPMAX, false>;
   const int smem = DecGeom<D>::RING_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

@@ -22,6 +22,10 @@ struct DecodeArgs {
   const void* z;
   const float* norm_w;
   void* out;
+  // state-slot table: batch row b reads and writes state[slots[b]] and
+  // conv_state[slots[b]] (slots == nullptr: slot b); num_slots bounds it
+  const int32_t* slots;
+  int32_t num_slots;
   int32_t Hk, Hv, rep, map, decay, C;
   float l2_eps, rms_eps, scale;
 };

@@ -149,6 +149,36 @@ gdn_status gdn_decode_step(const gdn_dims* dims, int32_t batch, const void* mixe
                            void* out, void* stream);
 
 /*
+ * gdn_decode_step over a pool of state slots: batch row b reads and updates
+ * state[state_slots[b]] and conv_state[state_slots[b]] of a pool of
+ * num_slots sequences, so a serving loop can batch whichever sequences are
+ * live without gathering their states. The pages declare a batch submodule
+ * of the decode layer (libmir-metal decode/mod.rs, `mod batch`) without
+ * showing it; this indirection is this library's own reading of it.
+ *
+ * state_slots  device int32 [B]. A negative entry marks a padded row: it
+ *              touches no state or conv state, its core_out row is zero and
+ *              its out row is the gated norm of a zero row (zero for finite
+ *              z). An entry >= num_slots is treated the same and also
+ *              records GDN_ERR_EXTENT in the device error word
+ *              (gdn_device_error). Two rows naming the same slot is a caller
+ *              error: both update that state at once and the result is
+ *              unspecified (no fault).
+ * num_slots    P >= 0 slots in the pool.
+ * conv_state   [P][C][3] io dtype, in place.
+ * state        [P][Hv][D][D] fp32, in place.
+ * Every other argument is indexed by the batch row, exactly as in
+ * gdn_decode_step, with the same errors; state_slots NULL is
+ * GDN_ERR_INVALID_ARG.
+ */
+gdn_status gdn_decode_step_slots(const gdn_dims* dims, int32_t batch, const int32_t* state_slots,
+                                 int32_t num_slots, const void* mixed_qkv, const void* a,
+                                 const void* b, const float* decay_param, const float* dt_bias,
+                                 const void* conv_w, void* conv_state, float* state,
+                                 float* core_out, const void* z, const float* norm_w, void* out,
+                                 void* stream);
+
+/*
  * Chunked prefill: the same recurrence as gdn_decode_step summed chunk-wise
  * (chunk 64, UT/WY form) over a packed batch of variable-length sequences,
  * each continuing from its own fp32 state (in place). q, k, v are the

@@ -111,6 +111,32 @@ def test_decode_rejects_bad_arguments(lib):
     assert _decode(lib, ok, ptrs={"core": 0x10000}) == 4
 
 
+def _decode_slots(lib, d, batch=2, num_slots=4, ptrs=None):
+    p = dict(sl=0x80000, x=0x10000, a=0x20000, b=0x30000, dp=0x40000, dt=0x50000, w=0x60000,
+             cs=0x1000000, st=0x10000000, core=0x70000000, z=None, nw=None, out=None)
+    if ptrs:
+        p.update(ptrs)
+    v = [VP(p[k]) if p[k] is not None else None for k in
+         ("x", "a", "b", "dp", "dt", "w", "cs", "st", "core", "z", "nw", "out")]
+    return lib.gdn_decode_step_slots(ctypes.byref(d), batch,
+                                     VP(p["sl"]) if p["sl"] is not None else None, num_slots,
+                                     *v, None)
+
+
+@no_device
+def test_decode_slots_rejects_bad_arguments(lib):
+    ok = gdn.dims(16, 32, 128)
+    assert _decode_slots(lib, ok, ptrs={"sl": None}) == 1  # no slot table
+    assert _decode_slots(lib, ok, num_slots=-1) == 1
+    assert _decode_slots(lib, ok, ptrs={"sl": 0x80004}) == 5  # misaligned table
+    assert _decode_slots(lib, ok, batch=0) == 0  # nothing to do, nothing launched
+    # the pool's size, not the batch, decides the state's extent: 4 slots of
+    # 2 MiB reach past a conv state placed 4 MiB after the state's start
+    assert _decode_slots(lib, ok, ptrs={"cs": 0x10000000 + (4 << 20)}) == 4
+    # the slot table is an input: the core output must not overlap it
+    assert _decode_slots(lib, ok, ptrs={"core": 0x80000}) == 4
+
+
 @no_device
 def test_conv_and_prefill_and_norm_reject_bad_arguments(lib):
     d = gdn.dims(2, 4, 32)
