@@ -351,6 +351,7 @@ def run_gpu(args, ws, rank, local):
     varlen = run_varlen(args, ws) if not args.no_prefill else None
     multilayer = run_multilayer(args, ws, peaks) if not args.no_multilayer else None
     slot_dec = run_slot_decode(args, ws, peaks) if not args.no_multilayer else None
+    multi_dec = run_multi_decode(args, ws, peaks) if not args.no_multilayer else None
     clk = clocks.stop()
     if clk is not None:
         clk["window"] = "decode warm-up through the prefill blocks (brackets the timed steps)"
@@ -420,6 +421,8 @@ def run_gpu(args, ws, rank, local):
         line["multilayer_decode"] = multilayer
     if slot_dec is not None:
         line["slot_decode"] = slot_dec
+    if multi_dec is not None:
+        line["multi_token_decode"] = multi_dec
     if not args.no_cpu_baseline and ws == 1:
         line["cpu_baseline"] = cpu_baseline_decode(seconds=args.cpu_seconds)
     return line
@@ -612,6 +615,103 @@ def run_multilayer(args, ws, peaks):
             "timing": "one step = the 48 layer launches as one CUDA graph replay between two "
                       "CUDA events; mean of 5 steps after 2 eager steps and one replay",
             "l2": "inputs larger than L2 (each layer's state 384 MiB)"}
+
+
+def run_multi_decode(args, ws, peaks, T=4):
+    """The batched-decode shape (B=64, Hk=16, Hv=32, D=128, Tiled,
+    negative-rate, bf16) with T=4 tokens per sequence and call
+    (gdn_decode_multi: each state read and written once per call). Four state
+    sets cycled, the K calls as one CUDA graph, as in the headline. Beside it,
+    the route without the call: gdn_conv_update over the B*T tokens then
+    gdn_prefill_chunked over B sequences of T tokens (chunk-parallel path,
+    workspace allocated once), timed the same way."""
+    import gated_delta_net_causal_gb300 as gdn
+    B, Hk, Hv, D = 64, 16, 32, 128
+    _, d, dev, steps, host, state, cstate, out1, shape = _decode_setup(B, 16, 0)
+    del host
+    C = shape.qkv_features
+    gen = torch.Generator(device="cuda").manual_seed(gi.SEED_BASE + 7)
+    bf = torch.bfloat16
+
+    def rn(*sh, std=1.0):
+        return (torch.randn(sh, device="cuda", generator=gen) * std).to(bf)
+    inputs = [{"x": rn(B, T, C), "a": rn(B, T, Hv), "b": rn(B, T, Hv), "z": rn(B, T, Hv, D)}
+              for _ in range(4)]
+    nsets = max(4, -(-512 * 2**20 // state.nbytes))
+    states = [state] + [state.clone() for _ in range(nsets - 1)]
+    cstates = [cstate] + [cstate.clone() for _ in range(nsets - 1)]
+    out = torch.empty((B, T, Hv, D), device="cuda", dtype=bf)
+    stream = torch.cuda.current_stream()
+
+    def mstep(i):
+        x = inputs[i % 4]
+        gdn.gdn_decode_multi(d, x["x"], x["a"], x["b"], dev["decay_param"], dev["dt_bias"],
+                             dev["conv_w"], cstates[i % nsets], states[i % nsets], z=x["z"],
+                             norm_w=dev["norm_w"], out=out)
+
+    # the prefill route over the same tokens: packed [B*T] rows, cu_seqlens of T
+    cu = torch.arange(0, B * T + 1, T, device="cuda", dtype=torch.int32)
+    y = torch.empty((B * T, C), device="cuda", dtype=bf)
+    wsb = torch.empty(gdn.gdn_prefill_workspace_size(d, B, B * T), device="cuda",
+                      dtype=torch.uint8)
+    qk = Hk * D
+
+    def pstep(i):
+        x = inputs[i % 4]
+        cs, st = cstates[i % nsets], states[i % nsets]
+        gdn.gdn_conv_update(d, cu, x["x"].view(B * T, C), dev["conv_w"], cs, y)
+        gdn.gdn_prefill_chunked(d, cu, y[:, :qk], y[:, qk:2 * qk], y[:, 2 * qk:],
+                                x["a"].view(B * T, Hv), x["b"].view(B * T, Hv),
+                                dev["decay_param"], dev["dt_bias"], st, z=x["z"].view(B * T, Hv, D),
+                                norm_w=dev["norm_w"], out=out.view(B * T, Hv, D), workspace=wsb)
+
+    def timed(fn, graphed=True):
+        for i in range(max(args.warmup, 4)):
+            fn(i)
+        torch.cuda.synchronize()
+        if not graphed:
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for i in range(args.steps):
+                fn(i)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            return _barrier_max(ev0.elapsed_time(ev1) * 1e-3 / args.steps, ws)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for i in range(args.steps):
+                    fn(i)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        del graph
+        return _barrier_max(ev0.elapsed_time(ev1) * 1e-3 / args.steps, ws)
+
+    t_multi = timed(mstep)
+    t_pref = timed(pstep, graphed=False)
+    del states, cstates, inputs, wsb
+    torch.cuda.empty_cache()
+    state_bytes = 2 * B * Hv * D * D * 4
+    return {"workload": f"multi-token decode: B=64 sequences x {T} tokens per call, Hk=16 Hv=32 "
+                        "D=128, Tiled, negative-rate, bf16",
+            "value": round(ws * B * T / t_multi, 1), "unit": "tokens/s",
+            "ms_per_call": round(t_multi * 1e3, 5),
+            "state_gbs": round(ws * state_bytes / t_multi / 1e9, 2),
+            "hbm_frac_state": round(state_bytes / t_multi / 1e9 / peaks["hbm_gbs"], 4),
+            "via_conv_and_prefill_ms": round(t_pref * 1e3, 5),
+            "via_conv_and_prefill_timing": "gdn_conv_update + gdn_prefill_chunked per call, "
+                                           "issued eagerly back to back (five launches)",
+            "l2": f"inputs larger than L2: {nsets} state sets cycled",
+            "timing": f"the {args.steps} consecutive calls as one CUDA graph replay"}
 
 
 def run_slot_decode(args, ws, peaks):

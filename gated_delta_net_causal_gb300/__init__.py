@@ -73,6 +73,9 @@ def library() -> ctypes.CDLL:
         L.gdn_conv_update.argtypes = [pd, i32, vp, i64, vp, vp, vp, vp, vp]
         L.gdn_decode_step.restype = ctypes.c_int
         L.gdn_decode_step.argtypes = [pd, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.gdn_decode_multi.restype = ctypes.c_int
+        L.gdn_decode_multi.argtypes = [pd, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                       vp, vp]
         L.gdn_decode_step_slots.restype = ctypes.c_int
         L.gdn_decode_step_slots.argtypes = [pd, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                             vp, vp, vp, vp]
@@ -150,6 +153,24 @@ def gdn_decode_step(d: GdnDims, mixed_qkv, a, b, decay_param, dt_bias, conv_w, c
         _ptr(conv_w, "conv_w", io), _ptr(conv_state, "conv_state", io),
         _ptr(state, "state", f32), _ptr(core_out, "core_out", f32), _ptr(z, "z", io),
         _ptr(norm_w, "norm_w", f32), _ptr(out, "out", io), _stream(stream)), "gdn_decode_step")
+    return core_out, out
+
+
+def gdn_decode_multi(d: GdnDims, mixed_qkv, a, b, decay_param, dt_bias, conv_w, conv_state,
+                     state, core_out=None, z=None, norm_w=None, out=None, stream=None):
+    """T consecutive tokens per sequence: mixed_qkv [B][T][C], a and b
+    [B][T][Hv], z / core_out / out [B][T][Hv][D]."""
+    io = _io(d)
+    if mixed_qkv.dim() != 3:
+        raise ValueError("mixed_qkv must be [B][T][C]")
+    batch, tokens = mixed_qkv.shape[0], mixed_qkv.shape[1]
+    f32 = torch.float32
+    _check(library().gdn_decode_multi(
+        ctypes.byref(d), batch, tokens, _ptr(mixed_qkv, "mixed_qkv", io), _ptr(a, "a", io),
+        _ptr(b, "b", io), _ptr(decay_param, "decay_param", f32), _ptr(dt_bias, "dt_bias", f32),
+        _ptr(conv_w, "conv_w", io), _ptr(conv_state, "conv_state", io),
+        _ptr(state, "state", f32), _ptr(core_out, "core_out", f32), _ptr(z, "z", io),
+        _ptr(norm_w, "norm_w", f32), _ptr(out, "out", io), _stream(stream)), "gdn_decode_multi")
     return core_out, out
 
 
@@ -290,7 +311,7 @@ def gdn_version() -> int:
 
 
 __all__ = ["GdnDims", "GdnError", "dims", "library", "status_string", "gdn_conv_update",
-           "gdn_decode_step", "gdn_decode_step_slots", "gdn_prefill_chunked", "gdn_prefill_workspace_size",
+           "gdn_decode_step", "gdn_decode_multi", "gdn_decode_step_slots", "gdn_prefill_chunked", "gdn_prefill_workspace_size",
            "gdn_prefill_chunked_static", "GDN_STATIC_SCRATCH_BYTES", "gdn_gated_rmsnorm", "gdn_device_error",
            "gdn_qkv_features", "gdn_version", "GDN_MAP_GROUPED", "GDN_MAP_TILED",
            "GDN_DECAY_LOG_RATE", "GDN_DECAY_NEGATIVE_RATE", "GDN_F16", "GDN_BF16", "GDN_F32",

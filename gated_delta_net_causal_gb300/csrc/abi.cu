@@ -66,14 +66,15 @@ gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_E
 
 // Shared by gdn_decode_step (slots == nullptr: row b owns slot b, num_slots
 // = batch) and gdn_decode_step_slots.
-gdn_status decode_impl(const gdn_dims* dims, int32_t batch, const int32_t* slots,
+gdn_status decode_impl(const gdn_dims* dims, int32_t batch, int32_t tokens, const int32_t* slots,
                        int32_t num_slots, const void* mixed_qkv, const void* a, const void* b,
                        const float* decay_param, const float* dt_bias, const void* conv_w,
                        void* conv_state, float* state, float* core_out, const void* z,
                        const float* norm_w, void* out, void* stream) {
   gdn_status st = check_dims(dims);
   if (st != GDN_OK) return st;
-  if (batch < 0 || num_slots < 0) return GDN_ERR_INVALID_ARG;
+  if (batch < 0 || num_slots < 0 || tokens < 1) return GDN_ERR_INVALID_ARG;
+  if (tokens > 8 || (tokens > 1 && slots != nullptr)) return GDN_ERR_UNSUPPORTED;
   if (batch > kMaxGridY) return GDN_ERR_EXTENT;
   const int rep = dims->n_v_heads / dims->n_k_heads;
   if (rep > 8) return GDN_ERR_UNSUPPORTED;
@@ -94,10 +95,11 @@ gdn_status decode_impl(const gdn_dims* dims, int32_t batch, const int32_t* slots
   if (!mul_ok((int64_t)num_slots * Hv, D * D * 4, &state_bytes)) return GDN_ERR_EXTENT;
   if (!mul_ok((int64_t)num_slots, C * 3 * es, &tmp)) return GDN_ERR_EXTENT;
   const int64_t conv_bytes = tmp;
-  const int64_t x_bytes = (int64_t)batch * C * es;
-  const int64_t o_bytes_f32 = (int64_t)batch * Hv * D * 4;
-  const int64_t o_bytes_io = (int64_t)batch * Hv * D * es;
-  const int64_t gate_bytes = (int64_t)batch * Hv * es;
+  const int64_t rows = (int64_t)batch * tokens;
+  const int64_t x_bytes = rows * C * es;
+  const int64_t o_bytes_f32 = rows * Hv * D * 4;
+  const int64_t o_bytes_io = rows * Hv * D * es;
+  const int64_t gate_bytes = rows * Hv * es;
   const Range inputs[] = {range_of(mixed_qkv, x_bytes), range_of(a, gate_bytes),
                           range_of(b, gate_bytes),      range_of(decay_param, Hv * 4),
                           range_of(dt_bias, Hv * 4),    range_of(conv_w, C * 4 * es),
@@ -127,6 +129,7 @@ gdn_status decode_impl(const gdn_dims* dims, int32_t batch, const int32_t* slots
   p.out = out;
   p.slots = slots;
   p.num_slots = num_slots;
+  p.tokens = tokens;
   p.Hk = dims->n_k_heads;
   p.Hv = dims->n_v_heads;
   p.rep = rep;
@@ -136,6 +139,9 @@ gdn_status decode_impl(const gdn_dims* dims, int32_t batch, const int32_t* slots
   p.l2_eps = dims->l2_eps;
   p.rms_eps = dims->rms_eps;
   p.scale = 1.0f / sqrtf((float)D);
+  if (tokens > 1)
+    return cuda_status(gdn::launch_decode_multi(p, dims->io_dtype, dims->head_dim, batch,
+                                                static_cast<cudaStream_t>(stream)));
   return cuda_status(gdn::launch_decode(p, dims->io_dtype, dims->head_dim, batch,
                                         static_cast<cudaStream_t>(stream)));
 }
@@ -209,8 +215,17 @@ gdn_status gdn_decode_step(const gdn_dims* dims, int32_t batch, const void* mixe
                            const float* dt_bias, const void* conv_w, void* conv_state,
                            float* state, float* core_out, const void* z, const float* norm_w,
                            void* out, void* stream) {
-  return decode_impl(dims, batch, nullptr, batch, mixed_qkv, a, b, decay_param, dt_bias, conv_w,
-                     conv_state, state, core_out, z, norm_w, out, stream);
+  return decode_impl(dims, batch, 1, nullptr, batch, mixed_qkv, a, b, decay_param, dt_bias,
+                     conv_w, conv_state, state, core_out, z, norm_w, out, stream);
+}
+
+gdn_status gdn_decode_multi(const gdn_dims* dims, int32_t batch, int32_t tokens,
+                            const void* mixed_qkv, const void* a, const void* b,
+                            const float* decay_param, const float* dt_bias, const void* conv_w,
+                            void* conv_state, float* state, float* core_out, const void* z,
+                            const float* norm_w, void* out, void* stream) {
+  return decode_impl(dims, batch, tokens, nullptr, batch, mixed_qkv, a, b, decay_param, dt_bias,
+                     conv_w, conv_state, state, core_out, z, norm_w, out, stream);
 }
 
 gdn_status gdn_decode_step_slots(const gdn_dims* dims, int32_t batch, const int32_t* state_slots,
@@ -220,8 +235,8 @@ gdn_status gdn_decode_step_slots(const gdn_dims* dims, int32_t batch, const int3
                                  float* core_out, const void* z, const float* norm_w, void* out,
                                  void* stream) {
   if (state_slots == nullptr) return GDN_ERR_INVALID_ARG;
-  return decode_impl(dims, batch, state_slots, num_slots, mixed_qkv, a, b, decay_param, dt_bias,
-                     conv_w, conv_state, state, core_out, z, norm_w, out, stream);
+  return decode_impl(dims, batch, 1, state_slots, num_slots, mixed_qkv, a, b, decay_param,
+                     dt_bias, conv_w, conv_state, state, core_out, z, norm_w, out, stream);
 }
 
 gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int32_t* cu_seqlens,
@@ -386,7 +401,8 @@ gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, int64_t rows, const float* o,
 gdn_status gdn_device_error(int32_t* status, int32_t clear) {
   if (status == nullptr) return GDN_ERR_INVALID_ARG;
   *status = GDN_OK;
-  cudaError_t (*readers[])(int32_t*, bool) = {gdn::read_error_decode, gdn::read_error_conv,
+  cudaError_t (*readers[])(int32_t*, bool) = {gdn::read_error_decode, gdn::read_error_decode_mt,
+                                               gdn::read_error_conv,
                                                gdn::read_error_rmsnorm, gdn::read_error_prefill,
                                                gdn::read_error_prefill_tc,
                                                gdn::read_error_prefill_cp};

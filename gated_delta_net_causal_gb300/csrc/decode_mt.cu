@@ -1,0 +1,397 @@
+// Multi-token decode: T (1..8) consecutive tokens of every sequence in one
+// launch, each state read from and written to HBM once for the T tokens
+// instead of once per token (the "resident state" case of a decode step:
+// speculative or multi-token-prediction decode verifies several tokens of a
+// sequence at a time). Per token and value row j of V head h the step is the
+// one gdn_decode_step takes (ferrox-core gdn.rs, `delta_step`):
+//   S_j *= a_t;  p = S_j . k_t;  d = b_t (v_tj - p);  S_j += d k_t;
+//   o_tj = S_j . q_t / sqrt(D),
+// applied token after token to the row while it sits in registers. Every
+// token's arithmetic is written in the same order as in the one-token kernel
+// (decode.cu: the conv sum, the norms, the gates, both dot products from the
+// old row, the fused update and read-out), so a T-token call gives the same
+// bits as T successive gdn_decode_step calls.
+//
+// Structure (as in decode.cu): a persistent kernel, one CTA per SM, a work
+// item is one (sequence, K head) pair with its V heads; one producer warp
+// streams the item's state rows through a shared-memory ring with 1-D bulk
+// copies, eight consumer warps update the rows. Per item the consumer warps
+// (1) run the conv over the item's q, k and v channels for all T tokens from
+// the old conv state (and write the new one: this CTA alone owns those
+// channels), and the gates; barrier; (2) each warp takes the l2 norms of every
+// token's q and k; (3) the state pass, T tokens per row; barrier; (4) the
+// outputs of every (head, token) pair, one warp per pair. The per-item
+// buffers are single: barrier (1)->(2) of the next item orders them.
+//
+// Every wait is bounded; a wait that gives up records GDN_ERR_TIMEOUT and
+// raises a CTA-wide abort flag, after which no warp waits again.
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kMtCW = 8;                      // consumer warps
+constexpr int kMtThreads = 32 * (kMtCW + 1);  // + one producer warp
+constexpr int kMtTMax = 8;                    // tokens per sequence and call
+constexpr int kMtRPL = 2;                     // rows each lane updates per pass
+constexpr int kMtMaxStages = 16;
+
+template <int D, int REPMAX>
+struct MtGeom {
+  static constexpr int LPR = D / 16;  // lanes per row (16 columns per lane)
+  static constexpr int RPW = 32 / LPR;
+  static constexpr int WROWS = RPW * kMtRPL;
+  static constexpr int CHUNK_ROWS = WROWS * kMtCW < D ? WROWS * kMtCW : D;
+  static constexpr int CPH = D / CHUNK_ROWS;
+  static constexpr uint32_t SLOT_BYTES = CHUNK_ROWS * D * 4;
+  static constexpr int SLOT_FLOATS = CHUNK_ROWS * D;
+  // static shared memory: q, k [T][D], v and the outputs [REPMAX][T][D], plus
+  // gates, norm weight, per-warp norms and barriers (under 4 KB)
+  static constexpr int STATIC_BYTES = (2 + 2 * REPMAX) * kMtTMax * D * 4 + 4096;
+  static constexpr int RING_AVAIL = 227 * 1024 - STATIC_BYTES;
+  static constexpr int RING_CAP = RING_AVAIL < 192 * 1024 ? RING_AVAIL : 192 * 1024;
+  static constexpr int STAGES_RAW = RING_CAP / (int)SLOT_BYTES;
+  static constexpr int STAGES = STAGES_RAW < kMtMaxStages ? STAGES_RAW : kMtMaxStages;
+  static constexpr int RING_BYTES = STAGES * (int)SLOT_BYTES;
+  static_assert(STAGES >= 2, "ring too small");
+};
+
+__device__ __forceinline__ bool mt_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (*abort_flag) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  record_device_error(GDN_ERR_TIMEOUT);
+  *abort_flag = 1;
+  return false;
+}
+
+__device__ __forceinline__ void mt_consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kMtCW * 32) : "memory");
+}
+
+template <typename T, int D, int REPMAX>
+__global__ void __launch_bounds__(kMtThreads, 1)
+    decode_multi_kernel(const DecodeArgs p, const int num_items) {
+  using G = MtGeom<D, REPMAX>;
+  constexpr int LPR = G::LPR, RPW = G::RPW, STAGES = G::STAGES;
+  constexpr int NC = kMtCW * 32;
+  constexpr int PER = D / 32;  // output elements per lane
+
+  extern __shared__ __align__(128) float ring[];
+  __shared__ float sq[kMtTMax][D], sk[kMtTMax][D];
+  __shared__ float sv[REPMAX][kMtTMax][D], so[REPMAX][kMtTMax][D];
+  __shared__ float sgate[REPMAX][kMtTMax][2];
+  __shared__ float sinv[kMtCW][3][kMtTMax];  // per warp: 1/|q|, 1/|k|, k.q scale
+  __shared__ float snw[D];
+  __shared__ __align__(8) uint64_t full_bar[kMtMaxStages], empty_bar[kMtMaxStages];
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rep = p.rep, Hk = p.Hk, Hv = p.Hv, NT = p.tokens;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kMtCW);
+    }
+    s_abort = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == kMtCW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t k = 0;
+      for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+        const int b = item / Hk, kh = item - (item / Hk) * Hk;
+        for (int r = 0; r < rep; ++r) {
+          const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+          const float* gS = p.state + ((size_t)b * Hv + h) * (size_t)(D * D);
+          for (int c = 0; c < G::CPH; ++c, ++k) {
+            const int slot = (int)(k % STAGES);
+            if (k >= (uint32_t)STAGES &&
+                !mt_wait(&empty_bar[slot], ((k / STAGES) - 1) & 1, abort_flag))
+              return;
+            mbar_arrive_expect_tx(&full_bar[slot], G::SLOT_BYTES);
+            bulk_load(ring + slot * G::SLOT_FLOATS, gS + (size_t)c * G::SLOT_FLOATS,
+                      G::SLOT_BYTES, &full_bar[slot]);
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const size_t C = (size_t)p.C;
+  const int qk_f = Hk * D;
+  const T* w = static_cast<const T*>(p.conv_w);
+  const int sub = lane % LPR, rq = lane / LPR;
+  if (p.z != nullptr)
+    for (int j = tid; j < D; j += NC) snw[j] = p.norm_w[j];
+
+  uint32_t k = 0;
+  for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
+    const int b = item / Hk, kh = item - (item / Hk) * Hk;
+    const T* xb = static_cast<const T*>(p.mixed_qkv) + (size_t)b * NT * C;
+    T* cst = static_cast<T*>(p.conv_state) + (size_t)b * C * 3;
+
+    // (1) conv + SiLU of the item's channels [q of kh | k of kh | v of each
+    // head] for every token, rolling the 3-wide window through the tokens
+    const int nch = (2 + rep) * D;
+    for (int idx = tid; idx < nch; idx += NC) {
+      const int which = idx / D, i = idx - which * D;
+      int c;
+      float* dst;
+      if (which < 2) {
+        c = which * qk_f + kh * D + i;
+        dst = which == 0 ? &sq[0][i] : &sk[0][i];
+      } else {
+        const int r = which - 2;
+        const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+        c = 2 * qk_f + h * D + i;
+        dst = &sv[r][0][i];
+      }
+      T* cp = cst + (size_t)c * 3;
+      T a0 = cp[0], a1 = cp[1], a2 = cp[2];
+      T xv[kMtTMax];
+#pragma unroll
+      for (int t = 0; t < kMtTMax; ++t) xv[t] = t < NT ? xb[(size_t)t * C + c] : T();
+      const float w0 = to_f32(w[(size_t)c * 4 + 0]), w1 = to_f32(w[(size_t)c * 4 + 1]);
+      const float w2 = to_f32(w[(size_t)c * 4 + 2]), w3 = to_f32(w[(size_t)c * 4 + 3]);
+#pragma unroll
+      for (int t = 0; t < kMtTMax; ++t) {
+        if (t < NT) {
+          float acc = w0 * to_f32(a0);
+          acc += w1 * to_f32(a1);
+          acc += w2 * to_f32(a2);
+          acc += w3 * to_f32(xv[t]);
+          dst[t * D] = silu_f(acc);
+          a0 = a1;
+          a1 = a2;
+          a2 = xv[t];
+        }
+      }
+      if (!*abort_flag) {
+        cp[0] = a0;
+        cp[1] = a1;
+        cp[2] = a2;
+      }
+    }
+    for (int j = tid; j < rep * NT; j += NC) {
+      const int r = j / NT, t = j - (j / NT) * NT;
+      const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+      const size_t gi = ((size_t)b * NT + t) * Hv + h;
+      sgate[r][t][0] = expf(gate_g(p.decay, p.decay_param[h], p.dt_bias[h],
+                                   to_f32(static_cast<const T*>(p.a)[gi])));
+      sgate[r][t][1] = sigmoid_f(to_f32(static_cast<const T*>(p.b)[gi]));
+    }
+    mt_consumer_sync();
+
+    // (2) l2 norms of every token's q and k and their product, each warp over
+    // all D, kept per warp
+    for (int t = 0; t < NT; ++t) {
+      float qq = 0.f, kk = 0.f, qkr = 0.f;
+#pragma unroll
+      for (int i = lane; i < D; i += 32) {
+        const float qv = sq[t][i], kv = sk[t][i];
+        qq = fmaf(qv, qv, qq);
+        kk = fmaf(kv, kv, kk);
+        qkr = fmaf(qv, kv, qkr);
+      }
+      qq = group_sum<32>(qq);
+      kk = group_sum<32>(kk);
+      qkr = group_sum<32>(qkr);
+      const float inv_q = 1.f / sqrtf(qq + p.l2_eps);
+      const float inv_k = 1.f / sqrtf(kk + p.l2_eps);
+      if (lane == 0) {
+        sinv[warp][0][t] = inv_q;
+        sinv[warp][1][t] = inv_k;
+        sinv[warp][2][t] = qkr * inv_q * inv_k * p.scale;
+      }
+    }
+    __syncwarp();
+
+    // (3) the state pass: each row read once from the ring, T token steps in
+    // registers, written back once
+    for (int r = 0; r < rep; ++r) {
+      const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+      float* gS = p.state + ((size_t)b * Hv + h) * (size_t)(D * D);
+      for (int c = 0; c < G::CPH; ++c, ++k) {
+        const int slot = (int)(k % STAGES);
+        const bool ready = mt_wait(&full_bar[slot], (k / STAGES) & 1, abort_flag);
+        if (ready && warp * G::WROWS < G::CHUNK_ROWS) {
+          float4 s4[kMtRPL][4];
+          int rowv[kMtRPL];
+#pragma unroll
+          for (int u = 0; u < kMtRPL; ++u) {
+            const int rl = warp * G::WROWS + u * RPW + rq;
+            rowv[u] = c * G::CHUNK_ROWS + rl;
+            const float* srow = ring + slot * G::SLOT_FLOATS + rl * D;
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+              s4[u][m] = *reinterpret_cast<const float4*>(srow + 4 * sub + 4 * LPR * m);
+          }
+          for (int t = 0; t < NT; ++t) {
+            const float sqs = sinv[warp][0][t] * p.scale;
+            const float inv_k = sinv[warp][1][t];
+            const float kq = sinv[warp][2][t];
+            float kr[16], qr[16];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int col = 4 * sub + 4 * LPR * m + e;
+                kr[4 * m + e] = sk[t][col] * inv_k;
+                qr[4 * m + e] = sq[t][col] * sqs;
+              }
+            }
+            float pk[kMtRPL], pq[kMtRPL];
+#pragma unroll
+            for (int u = 0; u < kMtRPL; ++u) {
+              float pk4[4], pq4[4];
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                pk4[m] = s4[u][m].x * kr[4 * m + 0];
+                pq4[m] = s4[u][m].x * qr[4 * m + 0];
+                pk4[m] = fmaf(s4[u][m].y, kr[4 * m + 1], pk4[m]);
+                pq4[m] = fmaf(s4[u][m].y, qr[4 * m + 1], pq4[m]);
+                pk4[m] = fmaf(s4[u][m].z, kr[4 * m + 2], pk4[m]);
+                pq4[m] = fmaf(s4[u][m].z, qr[4 * m + 2], pq4[m]);
+                pk4[m] = fmaf(s4[u][m].w, kr[4 * m + 3], pk4[m]);
+                pq4[m] = fmaf(s4[u][m].w, qr[4 * m + 3], pq4[m]);
+              }
+              pk[u] = (pk4[0] + pk4[1]) + (pk4[2] + pk4[3]);
+              pq[u] = (pq4[0] + pq4[1]) + (pq4[2] + pq4[3]);
+            }
+#pragma unroll
+            for (int o = LPR / 2; o > 0; o >>= 1) {
+#pragma unroll
+              for (int u = 0; u < kMtRPL; ++u) {
+                pk[u] += __shfl_xor_sync(0xffffffffu, pk[u], o);
+                pq[u] += __shfl_xor_sync(0xffffffffu, pq[u], o);
+              }
+            }
+            const float alpha = sgate[r][t][0], beta = sgate[r][t][1];
+#pragma unroll
+            for (int u = 0; u < kMtRPL; ++u) {
+              const int row = rowv[u];
+              const float d = beta * (sv[r][t][row] - alpha * pk[u]);
+              const float o = fmaf(alpha, pq[u], d * kq);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                s4[u][m].x = fmaf(d, kr[4 * m + 0], alpha * s4[u][m].x);
+                s4[u][m].y = fmaf(d, kr[4 * m + 1], alpha * s4[u][m].y);
+                s4[u][m].z = fmaf(d, kr[4 * m + 2], alpha * s4[u][m].z);
+                s4[u][m].w = fmaf(d, kr[4 * m + 3], alpha * s4[u][m].w);
+              }
+              if (sub == 0) so[r][t][row] = o;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kMtRPL; ++u) {
+            float* grow = gS + (size_t)rowv[u] * D;
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+              __stcs(reinterpret_cast<float4*>(grow + 4 * sub + 4 * LPR * m), s4[u][m]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+      }
+    }
+    mt_consumer_sync();
+
+    // (4) outputs: one warp per (head, token) pair
+    if (!*abort_flag) {
+      for (int pr = warp; pr < rep * NT; pr += kMtCW) {
+        const int r = pr / NT, t = pr - (pr / NT) * NT;
+        const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+        const size_t obase = (((size_t)b * NT + t) * Hv + h) * D + lane * PER;
+        float ov[PER];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) ov[e] = so[r][t][lane * PER + e];
+        if (p.core_out != nullptr) {
+#pragma unroll
+          for (int e = 0; e < PER; ++e) p.core_out[obase + e] = ov[e];
+        }
+        if (p.z != nullptr) {
+          float ss = 0.f;
+#pragma unroll
+          for (int e = 0; e < PER; ++e) ss += ov[e] * ov[e];
+          ss = group_sum<32>(ss);
+          const float inv = 1.f / sqrtf(ss / (float)D + p.rms_eps);
+          const T* zr = static_cast<const T*>(p.z) + obase;
+          T* outr = static_cast<T*>(p.out) + obase;
+#pragma unroll
+          for (int e = 0; e < PER; ++e)
+            outr[e] = from_f32<T>(ov[e] * inv * snw[lane * PER + e] * silu_f(to_f32(zr[e])));
+        }
+      }
+    }
+  }
+}
+
+int mt_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <typename T, int D, int REPMAX>
+cudaError_t launch_mt_t(const DecodeArgs& p, int32_t batch, cudaStream_t stream) {
+  auto kern = decode_multi_kernel<T, D, REPMAX>;
+  const int smem = MtGeom<D, REPMAX>::RING_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int items = batch * p.Hk;
+  const int grid = items < mt_sm_count() ? items : mt_sm_count();
+  kern<<<grid, kMtThreads, smem, stream>>>(p, items);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_mt_r(const DecodeArgs& p, int32_t batch, cudaStream_t stream) {
+  if (p.rep <= 2) return launch_mt_t<T, D, 2>(p, batch, stream);
+  if (p.rep <= 4) return launch_mt_t<T, D, 4>(p, batch, stream);
+  return launch_mt_t<T, D, 8>(p, batch, stream);
+}
+
+template <typename T>
+cudaError_t launch_mt_d(const DecodeArgs& p, int32_t D, int32_t batch, cudaStream_t stream) {
+  switch (D) {
+    case 32: return launch_mt_r<T, 32>(p, batch, stream);
+    case 64: return launch_mt_r<T, 64>(p, batch, stream);
+    case 128: return launch_mt_r<T, 128>(p, batch, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_multi(const DecodeArgs& p, int32_t dtype, int32_t D, int32_t batch,
+                                cudaStream_t stream) {
+  if (p.tokens < 1 || p.tokens > kMtTMax) return cudaErrorInvalidValue;
+  switch (dtype) {
+    case GDN_F16: return launch_mt_d<__half>(p, D, batch, stream);
+    case GDN_BF16: return launch_mt_d<__nv_bfloat16>(p, D, batch, stream);
+    case GDN_F32: return launch_mt_d<float>(p, D, batch, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gdn
+
+GDN_DEFINE_ERROR_READER(decode_mt)

@@ -26,6 +26,9 @@ struct DecodeArgs {
   // conv_state[slots[b]] (slots == nullptr: slot b); num_slots bounds it
   const int32_t* slots;
   int32_t num_slots;
+  // tokens per sequence (the multi-token kernel; the one-token kernel takes 1):
+  // activations [B][tokens][...], outputs [B][tokens][Hv][D]
+  int32_t tokens;
   int32_t Hk, Hv, rep, map, decay, C;
   float l2_eps, rms_eps, scale;
 };
@@ -78,6 +81,8 @@ struct PrefillArgs {
 // status (cudaSuccess when everything was enqueued).
 cudaError_t launch_decode(const DecodeArgs& p, int32_t dtype, int32_t D, int32_t batch,
                           cudaStream_t stream);
+cudaError_t launch_decode_multi(const DecodeArgs& p, int32_t dtype, int32_t D, int32_t batch,
+                                cudaStream_t stream);
 cudaError_t launch_conv(const ConvArgs& p, int32_t dtype, cudaStream_t stream);
 cudaError_t launch_rmsnorm(const RmsNormArgs& p, int32_t dtype, int32_t D, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& p, int32_t dtype, int32_t D, cudaStream_t stream);
@@ -91,6 +96,7 @@ cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_
 
 // Device error words, one per kernel translation unit.
 cudaError_t read_error_decode(int32_t* status, bool clear);
+cudaError_t read_error_decode_mt(int32_t* status, bool clear);
 cudaError_t read_error_conv(int32_t* status, bool clear);
 cudaError_t read_error_rmsnorm(int32_t* status, bool clear);
 cudaError_t read_error_prefill(int32_t* status, bool clear);

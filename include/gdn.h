@@ -149,6 +149,36 @@ gdn_status gdn_decode_step(const gdn_dims* dims, int32_t batch, const void* mixe
                            void* out, void* stream);
 
 /*
+ * Multi-token decode: `tokens` consecutive tokens of each of `batch`
+ * sequences in one call, with the state of each (sequence, V head) read
+ * from and written to memory once for all of them instead of once per
+ * token (speculative or multi-token-prediction decode). The result is that
+ * of `tokens` successive gdn_decode_step calls, token 0 first, each fed the
+ * row of every activation that belongs to that token; the arithmetic of each
+ * token is ordered as in gdn_decode_step, so the two agree bit for bit.
+ * The pages' decode step is one token (gdn.rs `delta_step`); applying it to
+ * a block of tokens with the state held on chip is this library's own
+ * reading of a decode over several tokens.
+ *
+ * tokens       T in 1..8 (T = 1 is gdn_decode_step); T < 1 is
+ *              GDN_ERR_INVALID_ARG, T > 8 GDN_ERR_UNSUPPORTED.
+ * mixed_qkv    [B][T][C] io dtype, pre-conv (row b*T + t is token t of
+ *              sequence b).
+ * a, b         [B][T][Hv] io dtype.
+ * core_out     [B][T][Hv][D] fp32, or NULL.
+ * z, out       [B][T][Hv][D] io dtype (fused gated RMSNorm), or NULL.
+ * conv_state   [B][C][3], state [B][Hv][D][D]: in place, as in
+ *              gdn_decode_step; afterwards they hold the state after token
+ *              T-1.
+ * Every other argument, and every error, is as in gdn_decode_step.
+ */
+gdn_status gdn_decode_multi(const gdn_dims* dims, int32_t batch, int32_t tokens,
+                            const void* mixed_qkv, const void* a, const void* b,
+                            const float* decay_param, const float* dt_bias, const void* conv_w,
+                            void* conv_state, float* state, float* core_out, const void* z,
+                            const float* norm_w, void* out, void* stream);
+
+/*
  * gdn_decode_step over a pool of state slots: batch row b reads and updates
  * state[state_slots[b]] and conv_state[state_slots[b]] of a pool of
  * num_slots sequences, so a serving loop can batch whichever sequences are

@@ -138,6 +138,27 @@ def test_decode_slots_rejects_bad_arguments(lib):
 
 
 @no_device
+def test_decode_multi_rejects_bad_arguments(lib):
+    ok = gdn.dims(16, 32, 128)
+
+    def call(batch=2, tokens=4, **ptrs):
+        p = dict(x=0x10000, a=0x2000000, b=0x3000000, dp=0x100000, dt=0x110000, w=0x120000,
+                 cs=0x4000000, st=0x10000000, core=0x70000000)
+        p.update(ptrs)
+        return lib.gdn_decode_multi(ctypes.byref(ok), batch, tokens,
+                                    *[VP(p[k]) if p[k] is not None else None for k in
+                                      ("x", "a", "b", "dp", "dt", "w", "cs", "st", "core")],
+                                    None, None, None, None)
+    assert call(tokens=0) == 1
+    assert call(tokens=9) == 3  # more than 8 tokens per call
+    assert call(batch=0) == 0  # nothing to do, nothing launched
+    assert call(x=None) == 1
+    # the activations span B*T rows: 2 x 4 x 8192 bf16 = 128 KiB from 0x10000,
+    # so a core output at 0x28000 overlaps them (with one token it would not)
+    assert call(core=0x28000) == 4
+
+
+@no_device
 def test_conv_and_prefill_and_norm_reject_bad_arguments(lib):
     d = gdn.dims(2, 4, 32)
     f = lib.gdn_conv_update
