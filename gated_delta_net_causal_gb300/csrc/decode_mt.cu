@@ -12,8 +12,11 @@
 // old row, the fused update and read-out), so a T-token call gives the same
 // bits as T successive gdn_decode_step calls.
 //
-// Structure (as in decode.cu): a persistent kernel, one CTA per SM, a work
-// item is one (sequence, K head) pair with its V heads; one producer warp
+// Structure (as in decode.cu): a persistent kernel, a work item is one
+// (sequence, K head) pair with its V heads. Two CTAs share each SM where
+// their shared memory fits (up to four V heads per K head), so one CTA's
+// per-item prologue and output loads overlap the other's state stream. One
+// producer warp
 // streams the item's state rows through a shared-memory ring with 1-D bulk
 // copies, eight consumer warps update the rows. Per item the consumer warps
 // (1) run the conv over the item's q, k and v channels for all T tokens from
@@ -49,7 +52,9 @@ struct MtGeom {
   // static shared memory: q, k [T][D], v and the outputs [REPMAX][T][D], plus
   // gates, norm weight, per-warp norms and barriers (under 4 KB)
   static constexpr int STATIC_BYTES = (2 + 2 * REPMAX) * kMtTMax * D * 4 + 4096;
-  static constexpr int RING_AVAIL = 227 * 1024 - STATIC_BYTES;
+  // two CTAs per SM (112 KB each) while that leaves a ring of two 32 KB slots
+  static constexpr int CTAS_PER_SM = REPMAX <= 4 ? 2 : 1;
+  static constexpr int RING_AVAIL = (CTAS_PER_SM == 2 ? 112 : 227) * 1024 - STATIC_BYTES;
   static constexpr int RING_CAP = RING_AVAIL < 192 * 1024 ? RING_AVAIL : 192 * 1024;
   static constexpr int STAGES_RAW = RING_CAP / (int)SLOT_BYTES;
   static constexpr int STAGES = STAGES_RAW < kMtMaxStages ? STAGES_RAW : kMtMaxStages;
@@ -72,7 +77,7 @@ __device__ __forceinline__ void mt_consumer_sync() {
 }
 
 template <typename T, int D, int REPMAX>
-__global__ void __launch_bounds__(kMtThreads, 1)
+__global__ void __launch_bounds__(kMtThreads, 2)
     decode_multi_kernel(const DecodeArgs p, const int num_items) {
   using G = MtGeom<D, REPMAX>;
   constexpr int LPR = G::LPR, RPW = G::RPW, STAGES = G::STAGES;
@@ -356,8 +361,17 @@ cudaError_t launch_mt_t(const DecodeArgs& p, int32_t batch, cudaStream_t stream)
   const int smem = MtGeom<D, REPMAX>::RING_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  // resident CTAs per SM as the runtime computes them (asked once per variant)
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kMtThreads, smem);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
+  }
   const int items = batch * p.Hk;
-  const int grid = items < mt_sm_count() ? items : mt_sm_count();
+  const int slots = mt_sm_count() * per_sm;
+  const int grid = items < slots ? items : slots;
   kern<<<grid, kMtThreads, smem, stream>>>(p, items);
   return cudaGetLastError();
 }
