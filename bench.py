@@ -350,8 +350,8 @@ def run_gpu(args, ws, rank, local):
     prefill = run_prefill(args, peaks, ws) if not args.no_prefill else None
     varlen = run_varlen(args, ws) if not args.no_prefill else None
     multilayer = run_multilayer(args, ws, peaks) if not args.no_multilayer else None
-    slot_dec = run_slot_decode(args, ws, peaks) if not args.no_multilayer else None
-    multi_dec = run_multi_decode(args, ws, peaks) if not args.no_multilayer else None
+    slot_dec = run_slot_decode(args, ws, peaks) if not args.no_extra else None
+    multi_dec = run_multi_decode(args, ws, peaks) if not args.no_extra else None
     clk = clocks.stop()
     if clk is not None:
         clk["window"] = "decode warm-up through the prefill blocks (brackets the timed steps)"
@@ -839,7 +839,9 @@ def main():
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-multilayer", action="store_true")
+    ap.add_argument("--no-multilayer", action="store_true", help="skip the 48-layer decode block")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the state-slot and multi-token decode blocks")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
