@@ -153,10 +153,13 @@ def _dist():
 
 
 def _barrier_max(value: float, ws: int) -> float:
+    """The maximum of `value` over all ranks (the slowest rank's time), after
+    a barrier; the value itself with one process."""
     if ws == 1:
         return value
     import torch.distributed as dist
-    t = torch.tensor([value], device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], device=dev, dtype=torch.float64)
     dist.barrier()
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
@@ -165,8 +168,11 @@ def _barrier_max(value: float, ws: int) -> float:
 # --------------------------------------------------------------------- GPU arm
 
 def _decode_setup(batch: int, sets: int, rank: int):
+    """Rank r runs its own `batch` sequences (global sequences r*batch ..
+    (r+1)*batch - 1, drawn from the rank's own seed): the sequences are
+    sharded across ranks with no exchange."""
     import gated_delta_net_causal_gb300 as gdn
-    wl = gi.workload_batched_decode(batch=batch, sets=sets)
+    wl = gi.workload_batched_decode(batch=batch, sets=sets, shard=rank)
     shape, w = wl["shape"], wl["weights"]
     d = gdn.dims(16, 32, 128, map=shape.map, decay=shape.decay, io_dtype=torch.bfloat16)
     dev = {k: getattr(w, k).cuda() for k in ("conv_w", "decay_param", "dt_bias", "norm_w")}

@@ -194,12 +194,15 @@ def workload_single_layer_b1(dtype: str = "f16", map: int = GROUPED,
                 state=delta_state(g, shape, 1, uniform_half_width=0.025))
 
 
-def workload_batched_decode(batch: int = 64, sets: int = 16) -> Dict:
+def workload_batched_decode(batch: int = 64, sets: int = 16, shard: int = 0) -> Dict:
     """B=64 decode, Hk=16, Hv=32, D=128, Tiled, negative-rate, bf16 inputs
     ~N(0,1), fp32 state ~N(0,0.02), conv state ~N(0,0.1); ``sets`` distinct
-    per-step input sets that a long run cycles through."""
+    per-step input sets that a long run cycles through. ``shard`` r > 0 draws
+    another batch of sequences from its own seed (one per process when the
+    sequences are split across processes); shard 0 is the single-process
+    workload."""
     shape = Shape(16, 32, 128, map=TILED, decay=NEGATIVE_RATE, dtype="bf16")
-    g = rng(SEED_BASE + 2)
+    g = rng(SEED_BASE + 2 + 7919 * shard)
     w = layer_weights(g, shape)
     steps = [step_inputs(g, shape, batch) for _ in range(sets)]
     return dict(shape=shape, weights=w, steps=steps, batch=batch,
