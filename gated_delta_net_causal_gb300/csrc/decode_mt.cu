@@ -361,14 +361,16 @@ cudaError_t launch_mt_t(const DecodeArgs& p, int32_t batch, cudaStream_t stream)
   const int smem = MtGeom<D, REPMAX>::RING_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  // resident CTAs per SM as the runtime computes them (asked once per variant)
-  static int per_sm = 0;
-  if (per_sm == 0) {
+  // resident CTAs per SM as the runtime computes them, asked once per variant
+  // (after the shared-memory attribute above; initialised thread-safely)
+  static const int per_sm = [&] {
     int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kMtThreads, smem);
-    if (e != cudaSuccess) return e;
-    per_sm = n > 0 ? n : 1;
-  }
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kMtThreads, smem) != cudaSuccess) {
+      cudaGetLastError();
+      return 1;
+    }
+    return n > 0 ? n : 1;
+  }();
   const int items = batch * p.Hk;
   const int slots = mt_sm_count() * per_sm;
   const int grid = items < slots ? items : slots;
