@@ -90,6 +90,12 @@ def lib():
             L.gdn_oracle_delta_chunked.restype = None
             L.gdn_oracle_delta_chunked.argtypes = [_I32, _I32, _I32, _INT, _I64, _I32, _D, _D, _D,
                                                    _D, _D, _D, _D]
+            L.gdn_oracle_delta_affine.restype = None
+            L.gdn_oracle_delta_affine.argtypes = [_I32, _I32, _I32, _INT, _I64, _I32, _D, _D, _D,
+                                                  _D, _D, _D, _D]
+            L.gdn_oracle_chunk_factors.restype = None
+            L.gdn_oracle_chunk_factors.argtypes = [_I32, _I32, _I32, _INT, _I64, _I32, _I32, _D,
+                                                   _D, _D, _D, _D, _D, _D, _D, _D]
             L.gdn_oracle_delta_bruteforce.restype = _INT
             L.gdn_oracle_delta_bruteforce.argtypes = [_I32, _I32, _I32, _INT, _I64, _D, _D, _D,
                                                       _D, _D, _D, _D]
@@ -192,6 +198,28 @@ def delta_chunked(q, k, v, g, beta, S, map_: int, chunk: int = 64):
     return _delta_common(lib().gdn_oracle_delta_chunked, q, k, v, g, beta, S, map_, int(chunk))
 
 
+def delta_affine(q, k, v, g, beta, S, map_: int, chunk: int = 64):
+    """O9, O4 carried chunk by chunk as affine maps of the chunk-start state:
+    o = X S^T + Y, then S <- S M + N (factors from chunk_factors)."""
+    return _delta_common(lib().gdn_oracle_delta_affine, q, k, v, g, beta, S, map_, int(chunk))
+
+
+def chunk_factors(q, k, v, g, beta, map_: int, h: int, t0: int, L: int):
+    """O9's per-chunk factors for V head h over tokens [t0, t0 + L): returns
+    (M [D][D], N [D][D], X [L][D], Y [L][D]) with S_end = S0 M + N and the
+    chunk's outputs X S0^T + Y (S0 = the state before token t0)."""
+    q, k, v, g, beta = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta)
+    T, Hk, D = q.shape
+    Hv = v.shape[1]
+    if not (0 <= t0 and 1 <= L and t0 + L <= T and 0 <= h < Hv):
+        raise ValueError("chunk outside the sequence")
+    M, N = np.zeros((D, D)), np.zeros((D, D))
+    X, Y = np.zeros((L, D)), np.zeros((L, D))
+    lib().gdn_oracle_chunk_factors(Hk, Hv, D, map_, int(t0), int(L), int(h), _p(q), _p(k),
+                                   _p(v), _p(g), _p(beta), _p(M), _p(N), _p(X), _p(Y))
+    return M, N, X, Y
+
+
 def delta_bruteforce(q, k, v, g, beta, S, map_: int):
     """O8, explicit matrix products in long double (D <= 8)."""
     return _delta_common(lib().gdn_oracle_delta_bruteforce, q, k, v, g, beta, S, map_)
@@ -246,5 +274,6 @@ def prefill_core(Hk: int, Hv: int, D: int, map_: int, q, k, v, g, beta, S, cu_se
 
 
 __all__ = ["build", "lib", "sigmoid", "silu", "softplus", "k_head", "conv", "conv_varlen",
-           "l2norm", "gates", "delta", "delta_chunked", "delta_bruteforce", "gated_rmsnorm",
+           "l2norm", "gates", "delta", "delta_chunked", "delta_affine", "chunk_factors",
+           "delta_bruteforce", "gated_rmsnorm",
            "segment", "prefill_core", "GROUPED", "TILED", "LOG_RATE", "NEGATIVE_RATE"]

@@ -369,6 +369,146 @@ void gdn_oracle_delta_chunked(int32_t Hk, int32_t Hv, int32_t D, int map, int64_
     free(S0);
 }
 
+/* ------------------------------------------------------------------- O9 */
+
+/* One chunk of the O7 summation written as an affine map of its start state
+ * (our derivation from the chunk form above; the pages name the carry stage of
+ * the chunked kernel, gated_delta_attention_tests.rs `run_chunked_core`, and
+ * print no formula for it). With U, W, c as in O7, E = diag(e^{c_L - c_s}) and
+ * P[t][s] = e^{c_t - c_s} (q_t . k_s) for s <= t:
+ *   S_L = S0 M + N,   M = e^{c_L} I - W^T E K   (D x D, key by key)
+ *                     N = U^T E K                 (D x D, value by key)
+ *   o   = X S0^T + Y, X = scale (diag(e^{c}) Q - P W)   (L x D)
+ *                     Y = scale P U                     (L x D)
+ * None of M, N, X, Y depends on S0. This function computes them for the L
+ * tokens starting at token t0 of V head h (q, k, v, g, beta laid out as for
+ * gdn_oracle_delta); M, N are D*D, X, Y are L*D, row-major. */
+void gdn_oracle_chunk_factors(int32_t Hk, int32_t Hv, int32_t D, int map, int64_t t0,
+                              int32_t L, int32_t h, const double* q, const double* k,
+                              const double* v, const double* g, const double* beta, double* M,
+                              double* N, double* X, double* Y) {
+    const double scale = 1.0 / sqrt((double)D);
+    const int32_t kh = gdn_oracle_k_head(map, h, Hk, Hv);
+    double* cg = (double*)malloc(sizeof(double) * L);
+    double* A = (double*)malloc(sizeof(double) * L * L);
+    double* Tm = (double*)malloc(sizeof(double) * L * L);
+    double* P = (double*)malloc(sizeof(double) * L * L);
+    double* U = (double*)malloc(sizeof(double) * L * D);
+    double* W = (double*)malloc(sizeof(double) * L * D);
+#define KV(t) (k + ((t0 + (t)) * Hk + kh) * D)
+#define QV(t) (q + ((t0 + (t)) * Hk + kh) * D)
+#define VV(t) (v + ((t0 + (t)) * Hv + h) * D)
+#define GI(t) ((t0 + (t)) * Hv + h)
+    double run = 0.0;
+    for (int32_t t = 0; t < L; ++t) {
+        run += g[GI(t)];
+        cg[t] = run;
+    }
+    for (int32_t t = 0; t < L; ++t)
+        for (int32_t s = 0; s < L; ++s) {
+            double kk = 0.0, qk = 0.0;
+            for (int32_t i = 0; i < D; ++i) {
+                kk += KV(t)[i] * KV(s)[i];
+                qk += QV(t)[i] * KV(s)[i];
+            }
+            A[t * L + s] = s < t ? beta[GI(t)] * exp(cg[t] - cg[s]) * kk : 0.0;
+            P[t * L + s] = s <= t ? exp(cg[t] - cg[s]) * qk : 0.0;
+        }
+    for (int32_t s = 0; s < L; ++s)
+        for (int32_t t = 0; t < L; ++t) {
+            if (t < s) {
+                Tm[t * L + s] = 0.0;
+                continue;
+            }
+            double val = (t == s) ? 1.0 : 0.0;
+            for (int32_t r = s; r < t; ++r) val -= A[t * L + r] * Tm[r * L + s];
+            Tm[t * L + s] = val;
+        }
+    for (int32_t t = 0; t < L; ++t)
+        for (int32_t c = 0; c < D; ++c) {
+            double u = 0.0, w = 0.0;
+            for (int32_t s = 0; s <= t; ++s) {
+                u += Tm[t * L + s] * beta[GI(s)] * VV(s)[c];
+                w += Tm[t * L + s] * beta[GI(s)] * exp(cg[s]) * KV(s)[c];
+            }
+            U[t * D + c] = u;
+            W[t * D + c] = w;
+        }
+    /* M[a][i] = e^{c_L} [a == i] - sum_s W[s][a] e^{c_L - c_s} k_s[i];
+     * N[j][i] = sum_s U[s][j] e^{c_L - c_s} k_s[i] */
+    for (int32_t a = 0; a < D; ++a)
+        for (int32_t i = 0; i < D; ++i) {
+            double m = (a == i) ? exp(cg[L - 1]) : 0.0, n = 0.0;
+            for (int32_t s = 0; s < L; ++s) {
+                const double e = exp(cg[L - 1] - cg[s]) * KV(s)[i];
+                m -= W[s * D + a] * e;
+                n += U[s * D + a] * e;
+            }
+            M[a * D + i] = m;
+            N[a * D + i] = n;
+        }
+    /* X[t][i] = scale (e^{c_t} q_t[i] - sum_s P[t][s] W[s][i]);
+     * Y[t][j] = scale sum_s P[t][s] U[s][j] */
+    for (int32_t t = 0; t < L; ++t)
+        for (int32_t i = 0; i < D; ++i) {
+            double x = exp(cg[t]) * QV(t)[i], y = 0.0;
+            for (int32_t s = 0; s <= t; ++s) {
+                x -= P[t * L + s] * W[s * D + i];
+                y += P[t * L + s] * U[s * D + i];
+            }
+            X[t * D + i] = scale * x;
+            Y[t * D + i] = scale * y;
+        }
+#undef KV
+#undef QV
+#undef VV
+#undef GI
+    free(cg);
+    free(A);
+    free(Tm);
+    free(P);
+    free(U);
+    free(W);
+}
+
+/* The recurrence of O4 carried chunk by chunk through the affine maps of
+ * gdn_oracle_chunk_factors: per chunk o = X S^T + Y, then S <- S M + N. Same
+ * arguments as gdn_oracle_delta_chunked. */
+void gdn_oracle_delta_affine(int32_t Hk, int32_t Hv, int32_t D, int map, int64_t T, int32_t Cn,
+                             const double* q, const double* k, const double* v, const double* g,
+                             const double* beta, double* S, double* o) {
+    double* M = (double*)malloc(sizeof(double) * D * D);
+    double* N = (double*)malloc(sizeof(double) * D * D);
+    double* X = (double*)malloc(sizeof(double) * Cn * D);
+    double* Y = (double*)malloc(sizeof(double) * Cn * D);
+    double* S0 = (double*)malloc(sizeof(double) * D * D);
+    for (int32_t h = 0; h < Hv; ++h) {
+        double* Sh = S + (int64_t)h * D * D;
+        for (int64_t t0 = 0; t0 < T; t0 += Cn) {
+            const int32_t L = (int32_t)((T - t0) < Cn ? (T - t0) : Cn);
+            gdn_oracle_chunk_factors(Hk, Hv, D, map, t0, L, h, q, k, v, g, beta, M, N, X, Y);
+            memcpy(S0, Sh, sizeof(double) * D * D);
+            for (int32_t t = 0; t < L; ++t)
+                for (int32_t j = 0; j < D; ++j) {
+                    double acc = Y[t * D + j];
+                    for (int32_t i = 0; i < D; ++i) acc += X[t * D + i] * S0[j * D + i];
+                    o[((t0 + t) * Hv + h) * D + j] = acc;
+                }
+            for (int32_t j = 0; j < D; ++j)
+                for (int32_t i = 0; i < D; ++i) {
+                    double acc = N[j * D + i];
+                    for (int32_t a = 0; a < D; ++a) acc += S0[j * D + a] * M[a * D + i];
+                    Sh[j * D + i] = acc;
+                }
+        }
+    }
+    free(M);
+    free(N);
+    free(X);
+    free(Y);
+    free(S0);
+}
+
 /* ------------------------------------------------------------------- O8 */
 
 #define GDN_ORACLE_BF_MAXD 8

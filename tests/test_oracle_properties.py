@@ -194,3 +194,56 @@ def test_read_out_scale():
     v = np.array([[[1.0, -2.0, 3.0, 0.5]]])
     o, _ = oracle.delta(k, k, v, np.zeros((1, 1)), np.ones((1, 1)), np.zeros((1, D, D)), 0)
     assert np.max(np.abs(o - v / 2.0)) < 1e-15
+
+
+# ------------------------------------------------ O9: the chunk as an affine map
+@pytest.mark.parametrize("chunk", [1, 7, 64, 145])
+@pytest.mark.parametrize("g_scale", [0.02, 0.5, 8.0])
+def test_affine_chunk_map_equals_recurrence(chunk, g_scale):
+    T = 145
+    q, k, v, g, beta, S = _rand_case(15, T, 2, 4, 16, g_scale=g_scale)
+    for mp in (oracle.GROUPED, oracle.TILED):
+        o, S1 = oracle.delta(q, k, v, g, beta, S, mp)
+        oa, Sa = oracle.delta_affine(q, k, v, g, beta, S, mp, chunk)
+        assert np.max(np.abs(oa - o)) < 1e-12 * max(1.0, np.max(np.abs(o)))
+        assert np.max(np.abs(Sa - S1)) < 1e-12 * max(1.0, np.max(np.abs(S1)))
+
+
+def test_affine_chunk_map_underflowing_decay():
+    T = 70
+    q, k, v, g, beta, S = _rand_case(16, T, 1, 2, 8)
+    g = -np.random.default_rng(1).uniform(0, 50, size=(T, 2))
+    o, S1 = oracle.delta(q, k, v, g, beta, S, oracle.GROUPED)
+    oa, Sa = oracle.delta_affine(q, k, v, g, beta, S, oracle.GROUPED, 64)
+    assert np.all(np.isfinite(oa)) and np.all(np.isfinite(Sa))
+    assert np.max(np.abs(oa - o)) < 1e-12 and np.max(np.abs(Sa - S1)) < 1e-12
+
+
+@pytest.mark.parametrize("mp", [oracle.GROUPED, oracle.TILED])
+def test_chunk_factors_read_off_the_recurrence(mp):
+    """Each factor, pinned to the token recurrence (O4) run on the chunk's
+    tokens from chosen start states: S0 = 0 gives S_end = N and o = Y; S0 =
+    e_a e_b^T (a one at value row a, key column b) adds row b of M to row a of
+    S_end and column b of X to column a of o."""
+    T, Hk, Hv, D = 9, 2, 4, 8
+    q, k, v, g, beta, _ = _rand_case(17, T, Hk, Hv, D, g_scale=0.7)
+    t0, L, h = 2, 6, 3
+    M, N, X, Y = oracle.chunk_factors(q, k, v, g, beta, mp, h, t0, L)
+    sl = slice(t0, t0 + L)
+
+    def run(S0h):
+        S = np.zeros((Hv, D, D))
+        S[h] = S0h
+        o, S1 = oracle.delta(q[sl], k[sl], v[sl], g[sl], beta[sl], S, mp)
+        return o[:, h, :], S1[h]
+
+    o0, s0 = run(np.zeros((D, D)))
+    assert np.max(np.abs(s0 - N)) < 1e-12 and np.max(np.abs(o0 - Y)) < 1e-12
+    for a, b in [(0, 0), (5, 2), (7, 7), (1, 6)]:
+        E = np.zeros((D, D))
+        E[a, b] = 1.0
+        o1, s1 = run(E)
+        assert np.max(np.abs((s1 - s0)[a] - M[b])) < 1e-12
+        others = np.delete(s1 - s0, a, axis=0)
+        assert np.max(np.abs(others)) < 1e-12  # no other row moves
+        assert np.max(np.abs((o1 - o0)[:, a] - X[:, b])) < 1e-12
