@@ -1,8 +1,9 @@
 """GB300 gated delta-net core: a thin Python binding over libgdn.so.
 
 Each function takes torch CUDA tensors, checks only what marshalling needs
-(device, dtype, contiguity), and calls the C-ABI entry point of the same name
-on the current torch CUDA stream. Every step of the computation runs in the
+(device, dtype, contiguity, and that every tensor holds the elements the call
+touches, since the C ABI sees only pointers), and calls the C-ABI entry point
+of the same name on the current torch CUDA stream. Every step of the computation runs in the
 library's CUDA kernels; there is no CPU or PyTorch fallback. If libgdn.so is
 missing the import of the library raises.
 
@@ -118,6 +119,28 @@ def _ptr(t: Optional[torch.Tensor], name: str, dtype=None) -> Optional[int]:
     return t.data_ptr()
 
 
+def _shape(d: GdnDims):
+    Hk, Hv, D = d.n_k_heads, d.n_v_heads, d.head_dim
+    return Hk, Hv, D, (2 * Hk + Hv) * D
+
+
+def _need(t, name: str, n: int):
+    """The C ABI sees only pointers: a tensor handed to a call must hold at
+    least the elements the call touches, or a kernel would read or write past
+    it. Checked here, before anything reaches the library."""
+    if isinstance(t, torch.Tensor) and t.numel() < n:
+        raise ValueError(f"{name} holds {t.numel()} elements; the call uses {n}")
+
+
+def _need_rows(t, name: str, rows: int, width: int):
+    """A token-strided operand: at least `rows` rows, each `width` contiguous
+    elements from the row's start."""
+    if t.dim() < 2 or t.shape[0] < rows:
+        raise ValueError(f"{name} must have at least {rows} rows")
+    if rows > 0 and (not t[0].is_contiguous() or t[0].numel() < width):
+        raise ValueError(f"{name}: each row must hold {width} contiguous elements")
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -135,6 +158,10 @@ def gdn_conv_update(d: GdnDims, cu_seqlens: torch.Tensor, x: torch.Tensor, conv_
     io = _io(d)
     n = cu_seqlens.numel() - 1
     total = x.shape[0] if x.dim() > 0 else 0
+    _, _, _, C = _shape(d)
+    for t, name, cnt in ((x, "x", total * C), (y, "y", total * C), (conv_w, "conv_w", C * 4),
+                         (conv_state, "conv_state", max(n, 0) * C * 3)):
+        _need(t, name, cnt)
     _check(library().gdn_conv_update(
         ctypes.byref(d), n, _ptr(cu_seqlens, "cu_seqlens", torch.int32), total,
         _ptr(x, "x", io), _ptr(conv_w, "conv_w", io), _ptr(conv_state, "conv_state", io),
@@ -142,10 +169,26 @@ def gdn_conv_update(d: GdnDims, cu_seqlens: torch.Tensor, x: torch.Tensor, conv_
     return y
 
 
+def _check_decode_sizes(d, batch, tokens, slots, mixed_qkv, a, b, decay_param, dt_bias, conv_w,
+                        conv_state, state, core_out, z, norm_w, out):
+    _, Hv, D, C = _shape(d)
+    rows = batch * tokens
+    for t, name, cnt in ((mixed_qkv, "mixed_qkv", rows * C), (a, "a", rows * Hv),
+                         (b, "b", rows * Hv), (decay_param, "decay_param", Hv),
+                         (dt_bias, "dt_bias", Hv), (conv_w, "conv_w", C * 4),
+                         (conv_state, "conv_state", slots * C * 3),
+                         (state, "state", slots * Hv * D * D),
+                         (core_out, "core_out", rows * Hv * D), (z, "z", rows * Hv * D),
+                         (norm_w, "norm_w", D), (out, "out", rows * Hv * D)):
+        _need(t, name, cnt)
+
+
 def gdn_decode_step(d: GdnDims, mixed_qkv, a, b, decay_param, dt_bias, conv_w, conv_state,
                     state, core_out=None, z=None, norm_w=None, out=None, stream=None):
     io = _io(d)
     batch = mixed_qkv.shape[0]
+    _check_decode_sizes(d, batch, 1, batch, mixed_qkv, a, b, decay_param, dt_bias, conv_w,
+                        conv_state, state, core_out, z, norm_w, out)
     f32 = torch.float32
     _check(library().gdn_decode_step(
         ctypes.byref(d), batch, _ptr(mixed_qkv, "mixed_qkv", io), _ptr(a, "a", io),
@@ -164,6 +207,8 @@ def gdn_decode_multi(d: GdnDims, mixed_qkv, a, b, decay_param, dt_bias, conv_w, 
     if mixed_qkv.dim() != 3:
         raise ValueError("mixed_qkv must be [B][T][C]")
     batch, tokens = mixed_qkv.shape[0], mixed_qkv.shape[1]
+    _check_decode_sizes(d, batch, tokens, batch, mixed_qkv, a, b, decay_param, dt_bias, conv_w,
+                        conv_state, state, core_out, z, norm_w, out)
     f32 = torch.float32
     _check(library().gdn_decode_multi(
         ctypes.byref(d), batch, tokens, _ptr(mixed_qkv, "mixed_qkv", io), _ptr(a, "a", io),
@@ -186,6 +231,8 @@ def gdn_decode_step_slots(d: GdnDims, state_slots, mixed_qkv, a, b, decay_param,
         raise ValueError("state_slots must hold one entry per batch row")
     if conv_state.shape[0] != state.shape[0]:
         raise ValueError("state and conv_state must hold the same number of slots")
+    _check_decode_sizes(d, batch, 1, state.shape[0], mixed_qkv, a, b, decay_param, dt_bias,
+                        conv_w, conv_state, state, core_out, z, norm_w, out)
     f32 = torch.float32
     _check(library().gdn_decode_step_slots(
         ctypes.byref(d), batch, _ptr(state_slots, "state_slots", torch.int32), state.shape[0],
@@ -221,6 +268,20 @@ def gdn_prefill_workspace_size(d: GdnDims, num_seqs: int, total_tokens: int,
     return n.value
 
 
+def _check_prefill_sizes(d, cu_seqlens, q, k, v, a, b, decay_param, dt_bias, state, core_out, z,
+                         norm_w, out):
+    Hk, Hv, D, _ = _shape(d)
+    T, n = q.shape[0], max(cu_seqlens.numel() - 1, 0)
+    _need_rows(q, "q", T, Hk * D)
+    _need_rows(k, "k", T, Hk * D)
+    _need_rows(v, "v", T, Hv * D)
+    for t, name, cnt in ((a, "a", T * Hv), (b, "b", T * Hv), (decay_param, "decay_param", Hv),
+                         (dt_bias, "dt_bias", Hv), (state, "state", n * Hv * D * D),
+                         (core_out, "core_out", T * Hv * D), (z, "z", T * Hv * D),
+                         (norm_w, "norm_w", D), (out, "out", T * Hv * D)):
+        _need(t, name, cnt)
+
+
 def gdn_prefill_chunked(d: GdnDims, cu_seqlens, q, k, v, a, b, decay_param, dt_bias, state,
                         core_out=None, z=None, norm_w=None, out=None, flags: int = 0,
                         workspace="auto", stream=None):
@@ -235,6 +296,8 @@ def gdn_prefill_chunked(d: GdnDims, cu_seqlens, q, k, v, a, b, decay_param, dt_b
     io = _io(d)
     f32 = torch.float32
     gate_dt = f32 if (flags & GDN_GATES_PRECOMPUTED) else io
+    _check_prefill_sizes(d, cu_seqlens, q, k, v, a, b, decay_param, dt_bias, state, core_out, z,
+                         norm_w, out)
     total = q.shape[0]
     n = cu_seqlens.numel() - 1
     ws_ptr, ws_bytes = None, 0
@@ -275,6 +338,8 @@ def gdn_prefill_chunked_static(d: GdnDims, cu_seqlens, q, k, v, a, b, decay_para
     io = _io(d)
     f32 = torch.float32
     gate_dt = f32 if (flags & GDN_GATES_PRECOMPUTED) else io
+    _check_prefill_sizes(d, cu_seqlens, q, k, v, a, b, decay_param, dt_bias, state, core_out, z,
+                         norm_w, out)
     _check(library().gdn_prefill_chunked_static(
         ctypes.byref(d), cu_seqlens.numel() - 1, _ptr(cu_seqlens, "cu_seqlens", torch.int32),
         q.shape[0], _base_ptr(q, "q", io), _token_stride(q, "q"), _base_ptr(k, "k", io),
@@ -289,6 +354,9 @@ def gdn_prefill_chunked_static(d: GdnDims, cu_seqlens, q, k, v, a, b, decay_para
 def gdn_gated_rmsnorm(d: GdnDims, o, z, norm_w, y, stream=None):
     io = _io(d)
     rows = o.numel() // d.head_dim
+    for t, name in ((z, "z"), (y, "y")):
+        _need(t, name, rows * d.head_dim)
+    _need(norm_w, "norm_w", d.head_dim)
     _check(library().gdn_gated_rmsnorm(
         ctypes.byref(d), rows, _ptr(o, "o", torch.float32), _ptr(z, "z", io),
         _ptr(norm_w, "norm_w", torch.float32), _ptr(y, "y", io), _stream(stream)),

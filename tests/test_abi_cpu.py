@@ -216,3 +216,67 @@ def test_binding_fails_loudly_on_cpu_tensors(lib):
     t = torch.zeros(4, 8)
     with pytest.raises(ValueError):
         gdn.gdn_gated_rmsnorm(d, t, t, torch.zeros(32), t)
+
+
+def test_binding_checks_every_tensor_size_before_the_call(lib):
+    """The C ABI sees only pointers: an undersized tensor must be caught in
+    the binding (a kernel would otherwise read or write past it). Correctly
+    sized CPU tensors get past these checks and fail on the device check."""
+    f32 = torch.float32
+    d = gdn.dims(2, 4, 32, io_dtype=f32)  # C = (2*2 + 4) * 32 = 256
+    Z = torch.zeros
+
+    def dec(**over):
+        t = dict(x=Z(2, 256), a=Z(2, 4), b=Z(2, 4), dp=Z(4), dt=Z(4), w=Z(256, 4),
+                 cs=Z(2, 256, 3), st=Z(2, 4, 32, 32), core=Z(2, 4, 32))
+        t.update(over)
+        gdn.gdn_decode_step(d, t["x"], t["a"], t["b"], t["dp"], t["dt"], t["w"], t["cs"],
+                            t["st"], core_out=t["core"])
+
+    for name, small in (("a", Z(1, 4)), ("b", Z(2, 3)), ("dp", Z(3)), ("w", Z(255, 4)),
+                        ("cs", Z(1, 256, 3)), ("st", Z(1, 4, 32, 32)), ("core", Z(2, 4, 31))):
+        with pytest.raises(ValueError, match="elements"):
+            dec(**{name: small})
+    with pytest.raises(ValueError, match="CUDA"):
+        dec()
+
+    def multi(**over):
+        t = dict(x=Z(2, 3, 256), a=Z(2, 3, 4), b=Z(2, 3, 4), st=Z(2, 4, 32, 32),
+                 core=Z(2, 3, 4, 32))
+        t.update(over)
+        gdn.gdn_decode_multi(d, t["x"], t["a"], t["b"], Z(4), Z(4), Z(256, 4), Z(2, 256, 3),
+                             t["st"], core_out=t["core"])
+
+    for name, small in (("a", Z(2, 2, 4)), ("core", Z(2, 2, 4, 32)), ("st", Z(1, 4, 32, 32))):
+        with pytest.raises(ValueError, match="elements"):
+            multi(**{name: small})
+    with pytest.raises(ValueError, match="CUDA"):
+        multi()
+
+    slots = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(ValueError, match="elements"):  # z of 1 row for 2
+        gdn.gdn_decode_step_slots(d, slots, Z(2, 256), Z(2, 4), Z(2, 4), Z(4), Z(4), Z(256, 4),
+                                  Z(5, 256, 3), Z(5, 4, 32, 32), z=Z(1, 4, 32), norm_w=Z(32),
+                                  out=Z(2, 4, 32))
+
+    def pre(**over):
+        T = 10
+        t = dict(q=Z(T, 64), k=Z(T, 64), v=Z(T, 128), a=Z(T, 4), st=Z(2, 4, 32, 32),
+                 core=Z(T, 4, 32))
+        t.update(over)
+        cu = torch.tensor([0, 4, T], dtype=torch.int32)
+        gdn.gdn_prefill_chunked(d, cu, t["q"], t["k"], t["v"], t["a"], Z(T, 4), Z(4), Z(4),
+                                t["st"], core_out=t["core"], workspace=None)
+
+    for name, small in (("k", Z(9, 64)), ("v", Z(10, 96)), ("a", Z(9, 4)),
+                        ("st", Z(1, 4, 32, 32)), ("core", Z(9, 4, 32))):
+        with pytest.raises(ValueError, match="rows|elements"):
+            pre(**{name: small})
+    with pytest.raises(ValueError, match="CUDA"):
+        pre()
+
+    cu = torch.tensor([0, 3], dtype=torch.int32)
+    with pytest.raises(ValueError, match="elements"):
+        gdn.gdn_conv_update(d, cu, Z(3, 256), Z(256, 4), Z(1, 256, 3), Z(2, 256))
+    with pytest.raises(ValueError, match="elements"):
+        gdn.gdn_gated_rmsnorm(d, Z(4, 32), Z(3, 32), Z(32), Z(4, 32))
