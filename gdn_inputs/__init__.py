@@ -212,6 +212,34 @@ def workload_single_layer_b1(dtype: str = "f16", map: int = GROUPED,
                 state=delta_state(g, shape, 1, uniform_half_width=0.025))
 
 
+def workload_single_layer_sin(map: int = GROUPED, decay: int = LOG_RATE) -> Dict:
+    """The batch-1, 4-token layer on the deterministic fill of the Metal
+    conformance test (ferrum-kernels gated_delta_attention_tests.rs, the
+    conformance setup: ``half_values`` / ``float_values``, sin(i f) a in
+    float32): mixed_qkv (f 0.017, a 0.21), a (0.071, 0.18), b (0.053, 0.24),
+    z (0.029, 0.31), conv weight (0.011, 0.16) and conv state (0.023, 0.04)
+    in f16, the delta state (0.007, 0.025) in f32, laid out as this
+    library's arrays; A_log_h = -1.7 + 0.07 h (its negative rate -exp(A_log)
+    in float32), dt_bias_h = -0.25 + 0.04 h, norm w_j = 0.82 + 0.013 j."""
+    shape = Shape(16, 32, 128, map=map, decay=decay, dtype="f16")
+    T, C, Hv, D = 4, shape.qkv_features, shape.n_v_heads, shape.head_dim
+
+    def h16(n, f, a, *dims):
+        return to_dtype(sin_values(n, f, a), "f16").view(*dims)
+    x = StepInputs(mixed_qkv=h16(T * C, 0.017, 0.21, T, C), a=h16(T * Hv, 0.071, 0.18, T, Hv),
+                   b=h16(T * Hv, 0.053, 0.24, T, Hv), z=h16(T * Hv * D, 0.029, 0.31, T, Hv * D))
+    idx = np.arange(Hv, dtype=np.float32)
+    log_rates = np.float32(-1.7) + idx * np.float32(0.07)
+    param = log_rates if decay == LOG_RATE else -np.exp(log_rates)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    w = Weights(conv_w=h16(C * 4, 0.011, 0.16, C, 4), decay_param=f32(param),
+                dt_bias=f32(np.float32(-0.25) + idx * np.float32(0.04)),
+                norm_w=f32(np.float32(0.82) + np.arange(D, dtype=np.float32) * np.float32(0.013)))
+    state = f32(sin_values(Hv * D * D, 0.007, 0.025)).view(1, Hv, D, D)
+    return dict(shape=shape, weights=w, inputs=x, conv_state=h16(C * 3, 0.023, 0.04, 1, C, 3),
+                state=state)
+
+
 def workload_batched_decode(batch: int = 64, sets: int = 16, shard: int = 0) -> Dict:
     """B=64 decode, Hk=16, Hv=32, D=128, Tiled, negative-rate, bf16 inputs
     ~N(0,1), fp32 state ~N(0,0.02), conv state ~N(0,0.1); ``sets`` distinct

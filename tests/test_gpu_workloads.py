@@ -18,13 +18,18 @@ pytestmark = pytest.mark.gpu
 
 # ------------------------------------------------------------ single layer, B=1
 
+@pytest.mark.parametrize("source", ["seeded", "sin_fill"])
 @pytest.mark.parametrize("mp,dec", [(gi.GROUPED, gi.LOG_RATE), (gi.TILED, gi.NEGATIVE_RATE)])
-def test_single_layer_b1_four_tokens_and_split(mp, dec):
+def test_single_layer_b1_four_tokens_and_split(mp, dec, source):
     """(i) four tokens decoded one at a time; (ii) the first three as one
     segment (conv update + chunked prefill, one partial chunk) then one decode
     step. (i) at the decode bounds, (ii) at the chunk bounds, against the
-    oracle and against each other."""
-    wl = gi.workload_single_layer_b1(dtype="f16", map=mp, decay=dec)
+    oracle and against each other. On the seeded inputs and, as a
+    cross-check, on the Metal conformance test's deterministic sin fill."""
+    if source == "seeded":
+        wl = gi.workload_single_layer_b1(dtype="f16", map=mp, decay=dec)
+    else:
+        wl = gi.workload_single_layer_sin(map=mp, decay=dec)
     shape, w, x = wl["shape"], wl["weights"], wl["inputs"]
     D, Hv, Hk, C = 128, 32, 16, shape.qkv_features
     # oracle over the whole 4-token segment

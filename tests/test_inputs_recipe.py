@@ -92,3 +92,25 @@ def test_varlen_lengths_as_drawn():
     lengths = gi.varlen_lengths(gi.SEED_BASE + 5, 8, 512, 8192)
     assert lengths == [8110, 2965, 6963, 3562, 4169, 3929, 2191, 2593]
     assert sum(lengths) == 34482
+
+
+def test_single_layer_sin_fill():
+    """The deterministic fill: value i of each array is sin(i f) a, computed in
+    float32 and rounded to f16 (the state stays float32)."""
+    import math
+    for decay in (gi.LOG_RATE, gi.NEGATIVE_RATE):
+        wl = gi.workload_single_layer_sin(decay=decay)
+        x, w = wl["inputs"], wl["weights"]
+        assert tuple(x.mixed_qkv.shape) == (4, 8192) and x.mixed_qkv.dtype == torch.float16
+        flat = x.mixed_qkv.reshape(-1)
+        for i in (0, 1, 8193, 32767):
+            ref = np.float16(np.float32(math.sin(np.float32(i) * np.float32(0.017))) *
+                             np.float32(0.21))
+            assert abs(float(flat[i]) - float(ref)) <= 2.0 ** -24 + abs(float(ref)) * 2.0 ** -10
+        assert tuple(wl["state"].shape) == (1, 32, 128, 128) and wl["state"].dtype == torch.float32
+        s1 = float(wl["state"].reshape(-1)[1])
+        assert abs(s1 - math.sin(0.007) * 0.025) < 1e-8
+        lr = -1.7 + 0.07 * np.arange(32)
+        want = lr if decay == gi.LOG_RATE else -np.exp(lr)
+        assert np.allclose(w.decay_param.numpy(), want, rtol=1e-6, atol=1e-6)
+        assert tuple(wl["conv_state"].shape) == (1, 8192, 3)
