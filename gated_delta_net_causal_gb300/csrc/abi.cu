@@ -164,7 +164,7 @@ const char* gdn_status_string(int32_t status) {
   }
 }
 
-int32_t gdn_version(void) { return 200; }
+int32_t gdn_version(void) { return 300; }
 
 int64_t gdn_qkv_features(const gdn_dims* dims) {
   if (check_dims(dims) != GDN_OK) return -1;

@@ -83,7 +83,8 @@ typedef struct gdn_dims {
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* gdn_status_string(int32_t status);
 
-/* ABI version: major * 10000 + minor * 100 + patch. */
+/* ABI version: major * 10000 + minor * 100 + patch. 0.3.0 added
+ * gdn_decode_multi and gdn_decode_step_slots. */
 int32_t gdn_version(void);
 
 /* Channels of the packed pre-conv activation: C = 2*Hk*D + Hv*D, laid out
