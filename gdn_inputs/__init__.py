@@ -36,27 +36,26 @@ def rng(seed: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(seed))
 
 
-def _round_to_odd_f32(x: np.ndarray) -> np.ndarray:
+def _round_to_odd_f32(x: torch.Tensor) -> torch.Tensor:
     """float64 -> float32 rounded to odd: truncate toward zero, then set the
     last mantissa bit when anything was dropped. A second rounding (to
     nearest even) of the result to a format at least two bits narrower gives
     exactly the once-rounded float64 value (the round-to-odd theorem), so the
     16-bit conversions below round once although they pass through float32."""
-    f = x.astype(np.float32)
-    away = np.abs(f.astype(np.float64)) > np.abs(x)
-    f = np.where(away, np.nextafter(f, np.float32(0)), f).astype(np.float32)
-    inexact = f.astype(np.float64) != x
-    bits = f.view(np.uint32) | inexact.astype(np.uint32)
-    return bits.view(np.float32)
+    f = x.to(torch.float32)
+    away = f.to(torch.float64).abs() > x.abs()
+    f = torch.where(away, torch.nextafter(f, torch.zeros_like(f)), f)
+    inexact = (f.to(torch.float64) != x).to(torch.int32)
+    return (f.view(torch.int32) | inexact).view(torch.float32)
 
 
 def to_dtype(x: np.ndarray, dtype: str) -> torch.Tensor:
     """Round float64 values once, to nearest with ties to even, to the storage
     dtype (finite values in the float32 range)."""
-    x = np.ascontiguousarray(x, dtype=np.float64)
+    x = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64))
     if dtype == "f32":
-        return torch.from_numpy(x).to(torch.float32)
-    return torch.from_numpy(_round_to_odd_f32(x)).to(DTYPES[dtype])
+        return x.to(torch.float32)
+    return _round_to_odd_f32(x).to(DTYPES[dtype])
 
 
 def as_f64(t: torch.Tensor) -> np.ndarray:
