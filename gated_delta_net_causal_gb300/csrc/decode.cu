@@ -64,13 +64,7 @@ struct DecGeom {
 
 // Bounded wait that also gives up as soon as another warp has aborted.
 __device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (*abort_flag) return false;
-    if (mbar_try_wait(bar, parity)) return true;
-  }
-  record_device_error(GDN_ERR_TIMEOUT);
-  *abort_flag = 1;
-  return false;
+  return mbar_wait_bounded(bar, parity, abort_flag);
 }
 
 __device__ __forceinline__ void consumer_sync() {

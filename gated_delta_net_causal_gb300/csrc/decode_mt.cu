@@ -63,13 +63,7 @@ struct MtGeom {
 };
 
 __device__ __forceinline__ bool mt_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (*abort_flag) return false;
-    if (mbar_try_wait(bar, parity)) return true;
-  }
-  record_device_error(GDN_ERR_TIMEOUT);
-  *abort_flag = 1;
-  return false;
+  return mbar_wait_bounded(bar, parity, abort_flag);
 }
 
 __device__ __forceinline__ void mt_consumer_sync() {

@@ -76,9 +76,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Spin limit for every bounded wait: a wait that gives up records
-// GDN_ERR_TIMEOUT in the device error word and the kernel returns.
-constexpr uint32_t kSpinLimit = 1u << 24;
+// Every wait on another thread's progress is bounded in time: after
+// kWaitLimitNs of the global timer it records GDN_ERR_TIMEOUT in the device
+// error word and gives up, and the kernel runs to its end.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 // One error word per translation unit (read back by the host through
 // gdn_device_error); the first recorded status wins.
@@ -118,14 +125,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait on the phase with the given parity. Returns false (and records
-// GDN_ERR_TIMEOUT) if it never completes.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+// Bounded wait on the phase with the given parity. Gives up (false) when
+// *abort_flag is set by another thread, or after limit_ns, recording
+// GDN_ERR_TIMEOUT and raising *abort_flag so the other waiters follow.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort_flag,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (abort_flag != nullptr && *abort_flag) return false;
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15) == 0 && global_ns() - t0 > limit_ns) {
+      record_device_error(GDN_ERR_TIMEOUT);
+      if (abort_flag != nullptr) *abort_flag = 1;
+      return false;
+    }
   }
-  record_device_error(GDN_ERR_TIMEOUT);
-  return false;
+}
+// Bounded wait without an abort flag.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_bounded(bar, parity, nullptr);
 }
 
 // ------------------------------------------------- PTX: bulk async copies

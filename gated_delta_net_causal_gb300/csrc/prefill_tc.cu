@@ -83,10 +83,7 @@ __device__ __forceinline__ int64_t clamp_cu_tc(const int32_t* cu, int n, int64_t
 }
 
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  record_device_error(GDN_ERR_TIMEOUT);
-  return false;
+  return mbar_wait(bar, parity);
 }
 
 template <typename T>
