@@ -3,7 +3,9 @@ and the tolerance checks."""
 
 from __future__ import annotations
 
-from typing import Optional
+import os
+from concurrent.futures import ThreadPoolExecutor
+from typing import Callable, Iterable, List, Optional
 
 import numpy as np
 import torch
@@ -150,3 +152,11 @@ class DecodeRunner:
                                  self.conv_state, self.state, core_out=core_out, z=z,
                                  norm_w=self.w["norm_w"] if norm else None, out=out)
         return core_out, out
+
+
+def parallel_map(fn: Callable, items: Iterable) -> List:
+    """fn over items on the host's cores: the oracle runs in C through ctypes,
+    which releases the interpreter lock, so threads run it in parallel."""
+    items = list(items)
+    with ThreadPoolExecutor(max_workers=min(len(items), os.cpu_count() or 4) or 1) as ex:
+        return list(ex.map(fn, items))

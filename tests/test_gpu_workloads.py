@@ -11,7 +11,7 @@ import gdn_inputs as gi
 import oracle
 from tests.gpu_helpers import (CHUNK_OUT_ABS, CHUNK_STATE_ABS, DECODE_OUT_ABS, DECODE_STATE_REL,
                                DecodeRunner, F64, assert_abs, assert_gated, assert_lowp,
-                               assert_state_rel, cuda, decode_reference)
+                               assert_state_rel, cuda, decode_reference, parallel_map)
 
 pytestmark = pytest.mark.gpu
 
@@ -161,12 +161,13 @@ def _head_channels(shape, h):
                            2 * qk + np.arange(h * D, (h + 1) * D)])
 
 
-def test_varlen_prefill_then_decode_sampled():
+def test_varlen_prefill_then_decode():
     """8 sequences (lengths U[512,8192] as drawn) packed by cu_seqlens, each
     resuming from a prior state and conv state: conv update, chunked prefill
-    with the fused norm, then 16 batched decode steps. Sampled (sequence,
-    head) pairs are recomputed by the oracle as one reduced segment (their
-    three channel groups, one K head, one V head) over prefill + decode."""
+    with the fused norm, then 16 batched decode steps. One V head of every
+    sequence (and a second one of the longest) is recomputed by the oracle as
+    one reduced segment (its three channel groups, one K head, one V head)
+    over prefill + decode; the fused norm is checked on every output row."""
     wl = gi.workload_varlen()
     shape, w, x = wl["shape"], wl["weights"], wl["inputs"]
     lengths, cu = wl["lengths"], wl["cu_seqlens"]
@@ -191,12 +192,14 @@ def test_varlen_prefill_then_decode_sampled():
     torch.cuda.synchronize()
     core_h = core.cpu()
     dec_h = torch.stack([c.cpu() for c in dec_core])  # [16][N][Hv][D]
-    # sampled (sequence, head) pairs: the longest and the shortest sequence
-    order = np.argsort(lengths)
-    pairs = [(int(order[-1]), 0), (int(order[-1]), 63), (int(order[0]), 17), (3, 40)]
+    # one V head per sequence (heads spread over the 64, the longest sequence
+    # also with a second head), each recomputed by the oracle in parallel
+    pairs = [(n, (17 * n + 5) % Hv) for n in range(N)] + [(int(np.argmax(lengths)), 63)]
     X = F64(x.mixed_qkv)
     A, Bb, Z = F64(x.a), F64(x.b), F64(x.z).reshape(T, Hv, D)
-    for n, h in pairs:
+
+    def recompute(pair):
+        n, h = pair
         s0, s1 = int(cu[n]), int(cu[n + 1])
         ch = _head_channels(shape, h)
         xs_n = np.concatenate([X[s0:s1][:, ch]] + [F64(wl["decode"][s].mixed_qkv)[n:n + 1][:, ch]
@@ -205,17 +208,24 @@ def test_varlen_prefill_then_decode_sampled():
                                                     for s in range(16)])
         b_n = np.concatenate([Bb[s0:s1, h:h + 1]] + [F64(wl["decode"][s].b)[n:n + 1, h:h + 1]
                                                      for s in range(16)])
-        rc, _, rcs, rS = oracle.segment(
+        return oracle.segment(
             1, 1, D, 0, shape.decay, xs_n, a_n, b_n, None, F64(w.conv_w)[ch],
             F64(w.decay_param)[h:h + 1], F64(w.dt_bias)[h:h + 1], F64(w.norm_w),
             F64(wl["conv_state"])[n][ch], F64(wl["state"])[n][h:h + 1])
+
+    refs = parallel_map(recompute, pairs)
+    Sd_h, csd_h = Sd.cpu(), F64(csd.cpu())
+    for (n, h), (rc, _, rcs, rS) in zip(pairs, refs):
+        s0, s1 = int(cu[n]), int(cu[n + 1])
+        ch = _head_channels(shape, h)
         L = s1 - s0
         tag = f"seq {n} (len {L}) head {h}"
         assert_abs(core_h[s0:s1, h], rc[:L, 0], CHUNK_OUT_ABS, tag + " prefill output")
         assert_abs(dec_h[:, n, h], rc[L:, 0], CHUNK_OUT_ABS, tag + " decode output")
-        assert_abs(Sd.cpu()[n, h:h + 1], rS, CHUNK_STATE_ABS, tag + " final state")
-        assert np.array_equal(F64(csd.cpu())[n][ch], rcs), tag + " conv state"
-    # the fused norm of the prefill against the oracle's norm of the kernel's core
-    ry = oracle.gated_rmsnorm(F64(core_h[:256]), Z[:256], F64(w.norm_w), 1e-6)
-    assert_lowp(out.cpu()[:256], ry, "bf16", "varlen fused norm")
+        assert_abs(Sd_h[n, h:h + 1], rS, CHUNK_STATE_ABS, tag + " final state")
+        assert np.array_equal(csd_h[n][ch], rcs), tag + " conv state"
+    # the fused norm of the whole prefill against the oracle's norm of the
+    # kernel's core output
+    ry = oracle.gated_rmsnorm(F64(core_h), Z, F64(w.norm_w), 1e-6)
+    assert_lowp(out.cpu(), ry, "bf16", "varlen fused norm")
     assert gdn.gdn_device_error() == 0
