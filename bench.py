@@ -9,9 +9,13 @@ place, and the gated RMSNorm epilogue):
 Metric: state GB/s = 2 * B * Hv * D^2 * 4 bytes / step time.
 
 A second block measures chunked prefill (one sequence of T=4096, Hk=16, Hv=32,
-D=128, Grouped, bf16 raw q/k/v/z/a/b, fused gated RMSNorm) in tokens/s, and a
-third the whole path on the varlen workload (conv update over 8 packed
-sequences, chunked prefill with the fused norm, 16 decode steps) in tokens/s.
+D=128, Grouped, bf16 raw q/k/v/z/a/b, fused gated RMSNorm) in tokens/s, with
+its tensor roofline, the same call end to end from host buffers, and the
+oracle's rate on the host cores; a third the whole path on the varlen workload
+(conv update over 8 packed sequences, chunked prefill with the fused norm, 16
+decode steps) in tokens/s, with the prefill call alone against its roofline;
+a fourth the batch-1 layer's latency (four decode steps, one multi-token call,
+the 3 + 1 split through conv update and chunked prefill).
 
 Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on
 the launching stream; a 512 MiB buffer is overwritten between timed steps so
@@ -354,7 +358,8 @@ def run_gpu(args, ws, rank, local):
 
     # chunked prefill block and the varlen whole-path block
     prefill = run_prefill(args, peaks, ws) if not args.no_prefill else None
-    varlen = run_varlen(args, ws) if not args.no_prefill else None
+    varlen = run_varlen(args, ws, peaks) if not args.no_prefill else None
+    batch1 = run_batch1(args, ws) if not args.no_prefill else None
     multilayer = run_multilayer(args, ws, peaks) if not args.no_multilayer else None
     slot_dec = run_slot_decode(args, ws, peaks) if not args.no_extra else None
     multi_dec = run_multi_decode(args, ws, peaks) if not args.no_extra else None
@@ -423,6 +428,8 @@ def run_gpu(args, ws, rank, local):
         line["prefill"] = prefill
     if varlen is not None:
         line["varlen_path"] = varlen
+    if batch1 is not None:
+        line["batch1_layer"] = batch1
     if multilayer is not None:
         line["multilayer_decode"] = multilayer
     if slot_dec is not None:
@@ -471,11 +478,37 @@ def run_prefill(args, peaks, ws):
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1) * 1e-3)
     t = _barrier_max(statistics.mean(times), ws)
+
+    # end to end through the C ABI with host buffers: the call's inputs (q, k,
+    # v, a, b, z) copied from pinned host memory, the call, the gated output
+    # copied back, a host sync; the state stays resident
+    hin = {"q": wl["q"].view(T, -1).pin_memory(), "k": wl["k"].view(T, -1).pin_memory(),
+           "v": wl["v"].view(T, -1).pin_memory(), "a": wl["a"].pin_memory(),
+           "b": wl["b"].pin_memory(), "z": wl["z"].pin_memory()}
+    dbuf = {nm: torch.empty_like(tt, device="cuda") for nm, tt in hin.items()}
+    out_host = torch.empty((T, 32, 128), dtype=torch.bfloat16).pin_memory()
+    h2d = sum(tt.numel() * tt.element_size() for tt in hin.values())
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_times = []
+    for i in range(max(3, min(args.steps, 10)) + 2):
+        state.copy_(s0)
+        flush.fill_(float(i))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for nm in dbuf:
+            dbuf[nm].copy_(hin[nm], non_blocking=True)
+        gdn.gdn_prefill_chunked(d, cu, dbuf["q"], dbuf["k"], dbuf["v"], dbuf["a"], dbuf["b"], dp, dt,
+                                state, core_out=None, z=dbuf["z"], norm_w=nw, out=out,
+                                workspace=wsb)
+        out_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_times.append(time.perf_counter() - t0)
+    t_e2e = _barrier_max(statistics.mean(e2e_times[2:]), ws)
     Hk, Hv, D, Cc = 16, 32, 128, 64
     flop_per_token = Hv * (6 * D * D + 6 * Cc * D + Cc * Cc / 3) + Hk * 4 * Cc * D
     flops = flop_per_token * T
     byts = T * (2 * Hk * D + 2 * Hv * D) * 2 + T * Hv * D * 2 + 2 * Hv * D * D * 4 + 4 * T * Hv * 2
-    return {"workload": PREFILL_WORKLOAD, "value": round(ws * T / t, 1), "unit": "tokens/s",
+    res = {"workload": PREFILL_WORKLOAD, "value": round(ws * T / t, 1), "unit": "tokens/s",
             "ms_per_call": round(t * 1e3, 4), "calls": n, "launches_per_call": 3,
             "roofline": {"bound": "tensor", "achieved": round(flops / t / 1e12, 3),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -488,11 +521,19 @@ def run_prefill(args, peaks, ws):
                          "algorithmic_flops_per_call": flops,
                          "algorithmic_bytes_per_call": byts,
                          "hbm_frac": round(byts / t / 1e9 / peaks["hbm_gbs"], 4),
-                         "timed": "the whole call (chunk index, prep, carry launches)",
-                         "kernel": "cp_prep_kernel + cp_chain_kernel"}}
+                         "timed": "the whole call (chunk index, prep, chain launches)",
+                         "kernel": "cp_prep_kernel + cp_chain_kernel"},
+           "e2e": {"value": round(ws * T / t_e2e, 1), "unit": "tokens/s",
+                   "ms_per_call": round(t_e2e * 1e3, 4), "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h,
+                   "issue": "H2D of q, k, v, a, b, z from pinned memory, the gdn_prefill_chunked "
+                            "call, D2H of the gated output, host sync; eager, per call"}}
+    if not args.no_cpu_baseline and ws == 1:
+        res["cpu_baseline"] = cpu_baseline_prefill(wl, seconds=min(args.cpu_seconds, 15.0))
+    return res
 
 
-def run_varlen(args, ws):
+def run_varlen(args, ws, peaks):
     """The whole hot path on the varlen workload: conv update over 8 packed
     sequences (lengths U[512,8192] as drawn, 34,482 tokens), chunked prefill
     with the fused gated norm continuing from their states, then 16 batched
@@ -546,10 +587,125 @@ def run_varlen(args, ws):
         times.append(e0.elapsed_time(e1) * 1e-3)
     t = _barrier_max(statistics.mean(times), ws)
     tokens = T + 16 * N
+
+    # the prefill call alone (the core of the path), on the conv output of the
+    # first pass, the states reset before each call
+    def pre():
+        gdn.gdn_prefill_chunked(d, cu, y[:, :qk], y[:, qk:2 * qk], y[:, 2 * qk:], a, b, dp, dt,
+                                st, z=z, norm_w=nw, out=out, workspace=wsb)
+
+    ptimes = []
+    for _ in range(4):
+        st.copy_(s0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pre()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ptimes.append(e0.elapsed_time(e1) * 1e-3)
+    tp = _barrier_max(statistics.mean(ptimes[1:]), ws)
+    Cc = 64
+    flops = T * (Hv * (6 * D * D + 6 * Cc * D + Cc * Cc / 3) + Hk * 4 * Cc * D)
+    byts = (T * (2 * Hk * D + 2 * Hv * D) * 2 + T * Hv * D * 2 + 2 * N * Hv * D * D * 4
+            + 2 * T * Hv * 2)
     return {"workload": "varlen: 8 sequences (34,482 tokens) conv update + chunked prefill with "
                         "fused norm + 16 decode steps, Hk=16 Hv=64 D=128, Tiled, bf16",
             "value": round(ws * tokens / t, 1), "unit": "tokens/s", "ms_per_pass": round(t * 1e3, 4),
-            "launches_per_pass": 2 + 3 + 16}
+            "launches_per_pass": 2 + 3 + 16,
+            "prefill_core": {"value": round(ws * T / tp, 1), "unit": "tokens/s",
+                             "ms_per_call": round(tp * 1e3, 4),
+                             "roofline": {"bound": "tensor", "achieved": round(flops / tp / 1e12, 3),
+                                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                          "frac": round(flops / tp / 1e12 / peaks["bf16_tflops"], 5),
+                                          "algorithmic_flops_per_call": flops,
+                                          "algorithmic_bytes_per_call": byts,
+                                          "hbm_frac": round(byts / tp / 1e9 / peaks["hbm_gbs"], 4),
+                                          "peak_source": peaks["source"]},
+                             "timed": "the gdn_prefill_chunked call alone (index, prep, chain), "
+                                      "fused norm, states reset before each of 3 timed calls"}}
+
+
+def run_batch1(args, ws):
+    """The batch-1 layer (Hk=16, Hv=32, D=128, Grouped, log-rate, f16, the
+    seeded inputs of the parity test): four tokens through gdn_decode_step one
+    at a time, the same four as one gdn_decode_multi call, and the 3 + 1 split
+    (conv update + chunked prefill on three tokens, then one decode step).
+    Latency per pass, with the states reset before each pass; eager launches
+    and, for the four steps, one CUDA graph."""
+    import gated_delta_net_causal_gb300 as gdn
+    wl = gi.workload_single_layer_b1(dtype="f16")
+    shape, w, x = wl["shape"], wl["weights"], wl["inputs"]
+    Hk, Hv, D = 16, 32, 128
+    C = shape.qkv_features
+    d = gdn.dims(Hk, Hv, D, map=shape.map, decay=shape.decay, io_dtype=torch.float16)
+    xs, a, b = x.mixed_qkv.cuda(), x.a.cuda(), x.b.cuda()
+    z = x.z.cuda().view(4, Hv, D)
+    cw, dp, dt, nw = (getattr(w, n).cuda() for n in ("conv_w", "decay_param", "dt_bias", "norm_w"))
+    cs0, s0 = wl["conv_state"].cuda(), wl["state"].cuda()
+    cs, st = cs0.clone(), s0.clone()
+    out = torch.empty((4, Hv, D), device="cuda", dtype=torch.float16)
+    y3 = torch.empty((3, C), device="cuda", dtype=torch.float16)
+    cu3 = gi.cu_seqlens([3]).cuda()
+    qk = Hk * D
+    stream = torch.cuda.current_stream()
+
+    def four():
+        for t in range(4):
+            gdn.gdn_decode_step(d, xs[t:t + 1], a[t:t + 1], b[t:t + 1], dp, dt, cw, cs, st,
+                                z=z[t:t + 1], norm_w=nw, out=out[t:t + 1])
+
+    def multi():
+        gdn.gdn_decode_multi(d, xs.view(1, 4, C), a.view(1, 4, Hv), b.view(1, 4, Hv), dp, dt, cw,
+                             cs, st, z=z.view(1, 4, Hv, D), norm_w=nw, out=out.view(1, 4, Hv, D))
+
+    def split():
+        gdn.gdn_conv_update(d, cu3, xs[:3], cw, cs, y3)
+        gdn.gdn_prefill_chunked(d, cu3, y3[:, :qk], y3[:, qk:2 * qk], y3[:, 2 * qk:], a[:3], b[:3],
+                                dp, dt, st, z=z[:3], norm_w=nw, out=out[:3])
+        gdn.gdn_decode_step(d, xs[3:], a[3:], b[3:], dp, dt, cw, cs, st, z=z[3:], norm_w=nw,
+                            out=out[3:])
+
+    def timed(fn, reps=20):
+        for _ in range(3):
+            cs.copy_(cs0)
+            st.copy_(s0)
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            cs.copy_(cs0)
+            st.copy_(s0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        return statistics.median(ts)
+
+    t_four, t_multi, t_split = timed(four), timed(multi), timed(split)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            four()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    t_graph = timed(g.replay)
+    state_bytes = 2 * Hv * D * D * 4
+    return {"workload": "batch-1 layer, 4 tokens: Hk=16 Hv=32 D=128, Grouped, log-rate, f16 "
+                        "activations, fp32 state, fused gated norm",
+            "unit": "us",
+            "four_decode_steps_us": round(_barrier_max(t_four, ws) * 1e6, 2),
+            "four_decode_steps_graph_us": round(_barrier_max(t_graph, ws) * 1e6, 2),
+            "decode_multi_4_tokens_us": round(_barrier_max(t_multi, ws) * 1e6, 2),
+            "split_3_plus_1_us": round(_barrier_max(t_split, ws) * 1e6, 2),
+            "us_per_token_graph": round(_barrier_max(t_graph, ws) * 1e6 / 4, 2),
+            "state_bytes_per_token": state_bytes,
+            "timing": "median of 20 passes between CUDA events, states reset before each; the "
+                      "split pass is conv update + chunked prefill (3 tokens, the single-pass "
+                      "kernel for f16) + one decode step"}
 
 
 def run_multilayer(args, ws, peaks):
@@ -819,6 +975,49 @@ def cpu_baseline_decode(seconds: float = 15.0, threads: int = None):
             "cores": len(seqs), "kind": "oracle",
             "sample": f"{i} decode steps x {len(seqs)} of the 64 sequences (fp64 oracle, "
                       f"one sequence per thread), {el:.1f} s"}
+
+
+def cpu_baseline_prefill(wl, seconds: float = 15.0, threads: int = None):
+    """The oracle (as it stands) on the T=4096 prefill workload: the l2 norms,
+    gates and the token recurrence of every V head over the first tokens of
+    the sequence (one head per host thread, ctypes releases the GIL inside the
+    C oracle), repeated over growing token counts until about `seconds` have
+    passed; the rate is tokens of the whole layer (all 32 V heads) per
+    second."""
+    import concurrent.futures as cf
+    import oracle
+    F = gi.as_f64
+    shape, w = wl["shape"], wl["weights"]
+    threads = threads or min(os.cpu_count() or 1, 32)
+    gg, bb = oracle.gates(F(wl["a"]), F(wl["b"]), F(w.decay_param), F(w.dt_bias), shape.decay)
+    q = oracle.l2norm(F(wl["q"]))
+    k = oracle.l2norm(F(wl["k"]))
+    v = F(wl["v"])
+    S0 = F(wl["state"])[0]
+    Hk, Hv = shape.n_k_heads, shape.n_v_heads
+
+    def head(args_):
+        h, T_s = args_
+        kh = oracle.k_head(shape.map, h, Hk, Hv)
+        oracle.delta(q[:T_s, kh:kh + 1], k[:T_s, kh:kh + 1], v[:T_s, h:h + 1], gg[:T_s, h:h + 1],
+                     bb[:T_s, h:h + 1], S0[h:h + 1], 0)
+
+    oracle.lib()
+    tokens = 0
+    T_s = 256
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        while True:
+            list(ex.map(head, [(h, T_s) for h in range(Hv)]))
+            tokens += T_s
+            if time.perf_counter() - t0 >= seconds:
+                break
+            T_s = min(2 * T_s, 4096)
+    el = time.perf_counter() - t0
+    return {"value": round(tokens / el, 2), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"the token recurrence of all {Hv} V heads over {tokens} tokens in total "
+                      f"(prefixes of the T=4096 sequence, fp64 oracle, one head per thread), "
+                      f"{el:.1f} s"}
 
 
 def run_reference(args, ws, rank):

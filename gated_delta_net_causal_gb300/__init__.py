@@ -327,7 +327,7 @@ def gdn_prefill_chunked(d: GdnDims, cu_seqlens, q, k, v, a, b, decay_param, dt_b
     return core_out, out
 
 
-GDN_STATIC_SCRATCH_BYTES = 192 << 20
+GDN_STATIC_SCRATCH_BYTES = 96 << 20
 
 
 def gdn_prefill_chunked_static(d: GdnDims, cu_seqlens, q, k, v, a, b, decay_param, dt_bias,

@@ -360,11 +360,11 @@ gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
   if (dims->head_dim != 128 || dims->io_dtype != GDN_BF16 || (flags & GDN_PREFILL_CUDA_CORES) ||
       dims->n_v_heads > 8 * dims->n_k_heads || num_seqs == 0 || total_tokens == 0)
     return GDN_OK;
-  // (T + 63 N) / 64 chunk slots of 73 KB per V head and 16 KB per K head
-  // (1168 and 256 bytes per token), plus the chunk index
+  // (T + 63 N) / 64 chunk slots of 25 KB per V head and 16 KB per K head,
+  // plus the chunk index
   int64_t tmp = 0;
   if (!mul_ok(total_tokens + 63 * (int64_t)num_seqs,
-              (int64_t)dims->n_v_heads * 1168 + (int64_t)dims->n_k_heads * 256 + 400, &tmp))
+              (int64_t)dims->n_v_heads * 400 + (int64_t)dims->n_k_heads * 256 + 400, &tmp))
     return GDN_ERR_EXTENT;
   *bytes = gdn::prefill_cp_workspace_bytes(num_seqs, total_tokens, dims->n_k_heads,
                                            dims->n_v_heads);

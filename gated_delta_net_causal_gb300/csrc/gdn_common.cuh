@@ -128,10 +128,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait on the phase with the given parity. Gives up (false) when
 // *abort_flag is set by another thread, or after limit_ns, recording
 // GDN_ERR_TIMEOUT and raising *abort_flag so the other waiters follow.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort_flag,
-                                                  uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+// (The loop lives in a function of its own so that a wait that completes
+// at once costs the caller no registers.)
+__device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                            uint64_t limit_ns) {
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (abort_flag != nullptr && *abort_flag) return false;
@@ -142,6 +142,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort_flag,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, limit_ns);
 }
 // Bounded wait without an abort flag.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {

@@ -2,38 +2,34 @@
 // bf16 activations, chunk 64, three launches over a caller-provided
 // workspace.
 //
-// The chunk algebra (the recurrence of ferrox-core gdn.rs summed chunk-wise;
-// the stages of ferrum-kernels gated_delta_attention_tests.rs
-// `run_chunked_core`) is split by what depends on the state. Within a chunk
-// of L tokens from state S (rows j = value, columns i = key), with c the
-// chunk-local cumulative decay, G_t = e^{c_t}, raw k, q and their l2 scales
-// rk_t, rq_t (rq includes 1/sqrt(D)):
+// The chunk algebra is the one of the single-pass kernel (the recurrence of
+// ferrox-core gdn.rs summed chunk-wise; the stages of ferrum-kernels
+// gated_delta_attention_tests.rs `run_chunked_core`), split by what depends on
+// the state. Within a chunk of L tokens from state S (rows j = value, columns
+// i = key), with c the chunk-local cumulative decay, G_t = e^{c_t}, raw k, q
+// and their l2 scales rk_t, rq_t (rq includes 1/sqrt(D)):
 //
 //   state-free, every chunk at once (cp_prep_kernel, one CTA per chunk and
 //   K head, looping over the V heads that read it):
 //     A   = beta_t e^{c_t-c_s} rk_t rk_s (k_t . k_s)            (s < t)
-//     Tb  = (I + A)^{-1} diag(beta)                              (hi + lo bf16)
-//     U   = Tb V,  W = Tb diag(G rk) K       (tensor cores)      -> fp32, hi + lo bf16
+//     Tb  = (I + A)^{-1} diag(beta)                              -> hi + lo bf16
 //     P   = e^{c_t-c_s} rq_t rk_s (q_t . k_s)                    (s <= t) -> bf16
-//     dk_t = e^{c_{L-1}-c_t} rk_t,  gq_t = G_t rq_t,  G_{L-1}
-//   the scan, one CTA per (V head, sequence), chunk after chunk
-//   (cp_scan_kernel; the fp32 state lives in TMEM as an MMA accumulator):
-//     Dm^T = U^T - S W^T            (the chunk's delta-rule corrections d_t)
+//     ak_t = G_t rk_t,  dk_t = e^{c_{L-1}-c_t} rk_t,  gq_t = G_t rq_t,  G_{L-1}
+//   the carry, one CTA per (V head, sequence), chunk after chunk
+//   (cp_chain_kernel; the state lives in TMEM as an fp32 accumulator):
+//     KS^T = S K^T                  R^T[j][s] = v_s[j] - ak_s KS^T[j][s]
+//     Dm^T = R^T Tb^T               (the chunk's delta-rule corrections d_t)
 //     S    = G_{L-1} S + (Dm diag(dk))^T K
 //     O^T  = S Q^T diag(gq) + Dm^T P^T, then the gated RMSNorm over j.
-// Only the two products of the middle line depend on the previous chunk, so
-// each chunk costs two dependent MMA groups; S Q^T and Dm^T P^T are issued
-// off that chain.
 //
-// Every product that carries the state forward keeps fp32 accuracy on bf16
-// tensor cores by splitting each fp32 factor as x = hi + lo (two bf16 values,
-// about 16 significant bits together): S W^T uses S_hi W_hi + S_hi W_lo +
-// S_lo W_hi, the update Dm'_hi K + Dm'_lo K, and U and W both halves of Tb
-// (raw k and v are exact in bf16). The two output products use the hi parts
-// only.
+// Every product that carries the state forward (S K^T, R Tb^T, Dm^T K) keeps
+// fp32 accuracy on bf16 tensor cores by splitting the fp32 factor as
+// x = hi + lo (two bf16 values, about 16 significant bits together): S and
+// Dm' are split, raw k is exact in bf16, and R Tb^T uses hi*hi + hi*lo +
+// lo*hi. The two output products (S Q^T, Dm P^T) use the hi parts only.
 //
-// Because the scan CTA owns all 128 value rows of its head, the gated RMSNorm
-// of each output row is a reduction inside the CTA: no cluster.
+// Because the carry CTA owns all 128 value rows of its head, the gated
+// RMSNorm of each output row is a reduction inside the CTA: no cluster.
 #include <cuda.h>
 #include <string.h>
 
@@ -48,6 +44,8 @@ namespace {
 constexpr int kC = 64;   // chunk
 constexpr int kD = 128;  // head_dim
 constexpr int kPrepThreads = 256;
+constexpr int kCarryThreads = 256;  // warps 0-7: the state carry (two threads per value row)
+constexpr int kChainThreads = 512;  // warps 8-15: output and gated norm
 constexpr int kAStride = kC + 1;    // padded row pitch of the fp32 A matrix
 constexpr int kMaxRep = 8;          // V heads per K head on this path
 
@@ -55,9 +53,7 @@ constexpr int kMaxRep = 8;          // V heads per K head on this path
 
 struct CpWork {
   int32_t* cs;         // [N+1] first chunk slot of each sequence
-  __nv_bfloat16* tw;   // [G*Hv*64][64]: P (row-major per slot)
-  float* u;            // [G*Hv][128 j][64 t]: U^T = (Tb V)^T per slot (columns t >= L zero)
-  __nv_bfloat16* wm;   // [G*Hv][2][64 t][128 i]: W hi, W lo per slot (rows t >= L zero)
+  __nv_bfloat16* tw;   // [3][G*Hv*64][64]: Tb hi, Tb lo, P (row-major per slot)
   __nv_bfloat16* kt;   // [G*Hk*128][64]: raw k transposed, rows t >= L zero
   float* vec;          // [G*Hv][4][64]: ak, dk, gq, {G_{L-1}, 0...}
   int64_t G;           // chunk slots
@@ -65,7 +61,7 @@ struct CpWork {
 
 struct CpLayout {
   int64_t G;
-  size_t off_tm, off_u, off_wm, off_kt, off_vec, total;
+  size_t off_tm, off_kt, off_vec, total;
 };
 
 CpLayout cp_layout(int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
@@ -73,9 +69,7 @@ CpLayout cp_layout(int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
   // sum over sequences of ceil(len/64) <= (T + 63 N) / 64
   l.G = T > 0 ? (T + 63 * (int64_t)N) / kC : 0;
   l.off_tm = ((size_t)4 * ((size_t)N + 1) + 1023) / 1024 * 1024;
-  l.off_u = l.off_tm + (size_t)l.G * Hv * kC * kC * 2;
-  l.off_wm = l.off_u + (size_t)l.G * Hv * kD * kC * 4;
-  l.off_kt = l.off_wm + (size_t)l.G * Hv * 2 * kD * kC * 2;
+  l.off_kt = l.off_tm + (size_t)3 * l.G * Hv * kC * kC * 2;
   l.off_vec = l.off_kt + (size_t)l.G * Hk * kD * kC * 2;
   l.total = l.off_vec + (size_t)l.G * Hv * 4 * kC * 4;
   return l;
@@ -179,33 +173,25 @@ __global__ void __launch_bounds__(1024) cp_index_kernel(const PrefillArgs p, con
 
 // ------------------------------------------------------------------ prep
 
-// The k rows of the k/q tile stay until W has been formed from them; the q
-// rows are dead once the grams and l2 scales are taken, and then hold the V
-// tile of the V head in hand. A and Tm sit after the tile; the raw gate
-// inputs overlay Tm until the gates are taken. Once the inverse is complete,
-// the hi/lo tiles of Tb diag(G rk) (B of W) overlay A and those of Tb (B of
-// U) overlay Tm.
+// The k and q tile is dead once the grams have completed and K^T and the l2
+// scales are taken from it; the per-V-head matrices then reuse its space.
 constexpr uint32_t P_OFF_KQ = 0;       // bf16 [128][128 i] SW128 (TMA): rows 0-63 k, 64-127 q
-constexpr uint32_t P_OFF_A = 32768;    // fp32 [64][65]; later bf16 [2][64 t][64 s] SW128
-constexpr uint32_t P_OFF_T = 50176;    // fp32 [64][64] Tm (products in its upper triangle); 1024-aligned
-constexpr uint32_t P_SMEM = 66560 + 1024;
-constexpr uint32_t P_TMEM_COLS = 128;  // grams 0-63, U^T and W 64-127
-// swizzled operand tiles start on 1024-byte boundaries
-static_assert(P_OFF_KQ % 1024 == 0 && P_OFF_A % 1024 == 0 && P_OFF_T % 1024 == 0, "tile alignment");
+constexpr uint32_t P_OFF_A = 0;        // fp32 [64][65]
+constexpr uint32_t P_OFF_T = 16640;    // fp32 [64][64] Tm (products in its upper triangle)
+constexpr uint32_t P_SMEM = 33024 + 1024;
 
-__global__ void __launch_bounds__(kPrepThreads, 3)
+__global__ void __launch_bounds__(kPrepThreads, 4)
     cp_prep_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+                   const __grid_constant__ CUtensorMap tm_k) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(16) float sinvk[kC], sinvq[kC];
-  // per V head: beta, the chunk-local cumulative decay c and G = e^c
-  __shared__ __align__(16) float sbeta[kMaxRep][kC], sc[kMaxRep][kC], sgam[kMaxRep][kC];
-  // raw gate inputs (in the Tm space until the first inverse)
-  float (*sga)[kC] = reinterpret_cast<float (*)[kC]>(sm + P_OFF_T);
-  float (*sgb)[kC] = reinterpret_cast<float (*)[kC]>(sm + P_OFF_T + kMaxRep * kC * 4);
+  // raw gate inputs, then per V head: beta, the chunk-local cumulative decay
+  // c and G = e^c
+  __shared__ __align__(16) float sga[kMaxRep][kC], sgb[kMaxRep][kC], sbeta[kMaxRep][kC],
+      sc[kMaxRep][kC], sgam[kMaxRep][kC];
   __shared__ uint32_t s_tmem;
-  __shared__ __align__(8) uint64_t bar_ld, bar_gp, bar_w, bar_v;
+  __shared__ __align__(8) uint64_t bar_ld, bar_gp;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int qd = warp & 3;
@@ -228,14 +214,12 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
   const bool pregate = (p.flags & GDN_GATES_PRECOMPUTED) != 0;
 
   if (warp == 0) {
-    tc::tmem_alloc(&s_tmem, P_TMEM_COLS);
+    tc::tmem_alloc(&s_tmem, 64);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
     mbar_init(&bar_ld, 1);
     mbar_init(&bar_gp, 1);
-    mbar_init(&bar_w, 1);
-    mbar_init(&bar_v, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(&bar_ld, 32768u);
     tc::tma_load_2d(sm + P_OFF_KQ, &tm_k, kh * kD, (int)c0, &bar_ld);
@@ -307,8 +291,8 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
       sinvq[srow] = live ? (prenorm ? 1.f : 1.f / sqrtf(qq + p.l2_eps)) * p.scale : 0.f;
     }
   }
-  // K^T of this chunk and K head for the scan's state update (its K-major B
-  // operand): thread pair (i, half) gathers 32 rows t of column i
+  // K^T of this chunk and K head for the carry's state update: thread pair
+  // (i, half) gathers 32 rows t of column i
   {
     const int i = tid >> 1, th = tid & 1;
     const uint32_t col = (uint32_t)((i >> 6) * 16384 + (i & 7) * 2);
@@ -334,7 +318,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
   if (__syncthreads_or(to)) {
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tb, P_TMEM_COLS);
+    if (warp == 0) tc::tmem_dealloc(tb, 64);
     return;
   }
   tc::fence_after_sync();
@@ -379,14 +363,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
 
   float* Ap = reinterpret_cast<float*>(sm + P_OFF_A);
   float* Tp = reinterpret_cast<float*>(sm + P_OFF_T);
-  // the V tile of V head r into the q rows (j halves 16 KB apart)
-  auto load_v = [&](int r) {
-    const int h = p.map == GDN_MAP_GROUPED ? kh * p.rep + r : kh + r * p.Hk;
-    mbar_arrive_expect_tx(&bar_v, 16384u);
-    tc::tma_load_2d(sm + P_OFF_KQ + 8192, &tm_v, h * kD, (int)c0, &bar_v);
-    tc::tma_load_2d(sm + P_OFF_KQ + 24576, &tm_v, h * kD + 64, (int)c0, &bar_v);
-  };
-  if (tid == 0) load_v(0);
+  const size_t HvG = (size_t)w.G * p.Hv;
   for (int r = 0; r < p.rep; ++r) {
     const int h = p.map == GDN_MAP_GROUPED ? kh * p.rep + r : kh + r * p.Hk;
     const size_t slot = (size_t)g * p.Hv + h;
@@ -406,33 +383,31 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
       constexpr float kLog2e = 1.4426950408889634f;
       const float ct = sc[r][t] * kLog2e;
       // e^{c_t - c_s} (<= 1 for s <= t) times rk_s for this thread's 32
-      // columns s, from 16-byte loads of the per-token vectors
-      float dks[32];
+      // columns s, four at a time from 16-byte loads of the per-token vectors
+      float pr[32];
 #pragma unroll
       for (int m4 = 0; m4 < 8; ++m4) {
         const float4 c4 = *reinterpret_cast<const float4*>(&sc[r][32 * hc + 4 * m4]);
         const float4 k4 = *reinterpret_cast<const float4*>(&sinvk[32 * hc + 4 * m4]);
-        dks[4 * m4] = exp2f(ct - c4.x * kLog2e) * k4.x;
-        dks[4 * m4 + 1] = exp2f(ct - c4.y * kLog2e) * k4.y;
-        dks[4 * m4 + 2] = exp2f(ct - c4.z * kLog2e) * k4.z;
-        dks[4 * m4 + 3] = exp2f(ct - c4.w * kLog2e) * k4.w;
+        const float cv[4] = {c4.x, c4.y, c4.z, c4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = 4 * m4 + u, s = 32 * hc + e;
+          pr[e] = (live && s <= t) ? exp2f(ct - cv[u] * kLog2e) * kv[u] * gv[e] : 0.f;
+        }
       }
       if (is_a) {
         const float bk = sbeta[r][t] * sinvk[t];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int s = 32 * hc + e;
-          Ap[t * kAStride + s] = (live && s < t) ? bk * dks[e] * gv[e] : 0.f;
+          Ap[t * kAStride + s] = s < t ? bk * pr[e] : 0.f;
         }
       } else {
         const float iqt = sinvq[t];
-        float pr[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int s = 32 * hc + e;
-          pr[e] = (live && s <= t) ? dks[e] * gv[e] * iqt : 0.f;
-        }
-        uint4* dst = reinterpret_cast<uint4*>(w.tw + (slot * kC + t) * kC + 32 * hc);
+        for (int e = 0; e < 32; ++e) pr[e] *= iqt;
+        uint4* dst = reinterpret_cast<uint4*>(w.tw + ((2 * HvG + slot) * kC + t) * kC + 32 * hc);
 #pragma unroll
         for (int m = 0; m < 4; ++m)
           dst[m] = make_uint4(pack_bf16(pr[8 * m], pr[8 * m + 1]), pack_bf16(pr[8 * m + 2], pr[8 * m + 3]),
@@ -537,45 +512,25 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
       *reinterpret_cast<float2*>(Tp + (32 + r0 + 1) * kC + c0) = make_float2(-y10, -y11);
       __syncthreads();
     }
-    // Tb = Tm diag(beta) and Tb diag(ak) (ak = G rk) as hi + lo bf16 tiles
-    // (K-major, zero above the diagonal): Tb over Tm once every thread has
-    // read its row of Tm, Tb diag(ak) over the dead A; 16 consecutive
-    // elements of one row per thread
+    // Tb = Tm diag(beta) as hi + lo bf16, zero above the diagonal; 16
+    // consecutive elements of one row per thread
     {
       const int e0 = 16 * tid, tr = e0 >> 6, u0 = e0 & 63;
-      float x[16], xa[16];
+      float x[16];
 #pragma unroll
-      for (int m4 = 0; m4 < 4; ++m4) {
-        const float4 t4 = *reinterpret_cast<const float4*>(Tp + tr * kC + u0 + 4 * m4);
-        const float4 b4 = *reinterpret_cast<const float4*>(&sbeta[r][u0 + 4 * m4]);
-        const float4 g4 = *reinterpret_cast<const float4*>(&sgam[r][u0 + 4 * m4]);
-        const float4 k4 = *reinterpret_cast<const float4*>(&sinvk[u0 + 4 * m4]);
-        const float tv[4] = {t4.x, t4.y, t4.z, t4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
-        const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int m = 4 * m4 + e;
-          x[m] = u0 + m <= tr ? tv[e] * bv[e] : 0.f;
-          xa[m] = x[m] * (gv[e] * kv[e]);
-        }
+      for (int m = 0; m < 16; ++m) {
+        const int s = u0 + m;
+        x[m] = s <= tr ? Tp[tr * kC + s] * sbeta[r][s] : 0.f;
       }
-      const int c16 = u0 >> 3;
       uint4 h0, l0, h1, l1;
-      split8(xa, h0, l0);
-      split8(xa + 8, h1, l1);
-      unsigned char* ba = sm + P_OFF_A;
-      *reinterpret_cast<uint4*>(ba + sw_chunk(tr, c16, kC)) = h0;
-      *reinterpret_cast<uint4*>(ba + sw_chunk(tr, c16 + 1, kC)) = h1;
-      *reinterpret_cast<uint4*>(ba + 8192 + sw_chunk(tr, c16, kC)) = l0;
-      *reinterpret_cast<uint4*>(ba + 8192 + sw_chunk(tr, c16 + 1, kC)) = l1;
       split8(x, h0, l0);
       split8(x + 8, h1, l1);
-      __syncthreads();  // Tm has been read
-      unsigned char* bu = sm + P_OFF_T;
-      *reinterpret_cast<uint4*>(bu + sw_chunk(tr, c16, kC)) = h0;
-      *reinterpret_cast<uint4*>(bu + sw_chunk(tr, c16 + 1, kC)) = h1;
-      *reinterpret_cast<uint4*>(bu + 8192 + sw_chunk(tr, c16, kC)) = l0;
-      *reinterpret_cast<uint4*>(bu + 8192 + sw_chunk(tr, c16 + 1, kC)) = l1;
+      uint4* dh = reinterpret_cast<uint4*>(w.tw + slot * (kC * kC) + e0);
+      uint4* dl = reinterpret_cast<uint4*>(w.tw + (HvG + slot) * (kC * kC) + e0);
+      dh[0] = h0;
+      dh[1] = h1;
+      dl[0] = l0;
+      dl[1] = l1;
     }
     if (tid < kC) {
       const int t = tid;
@@ -586,204 +541,86 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
       vv[2 * kC + t] = live ? sgam[r][t] * sinvq[t] : 0.f;
       vv[3 * kC + t] = t == 0 ? sgam[r][L - 1] : 0.f;
     }
-    // U^T = (Tb V)^T on the tensor cores: A = the V tile read MN-major (j
-    // along M, the two j halves 16 KB apart), B = the Tb tiles over Tm; the
-    // hi and lo products accumulate into TMEM columns 64-127, and row j
-    // (lane j) goes to the workspace as fp32
-    fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    {
-      bool bad = false;
-      if (tid == 0) {
-        bad = !mbar_wait(&bar_v, (uint32_t)(r & 1));
-        if (!bad) {
-          tc::fence_after_sync();
-          const uint32_t id = tc::idesc(tc::kBF16, 128, 64) | tc::kAMajorMN;
-          const uint32_t av = smem_u32(sm + P_OFF_KQ + 8192);
-          const uint64_t dbh = tc::sdesc_sw128(smem_u32(sm + P_OFF_T));
-          const uint64_t dbl = tc::sdesc_sw128(smem_u32(sm + P_OFF_T + 8192));
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const uint64_t da = tc::sdesc_mn(av + 2048u * s, 16384u);
-            tc::mma_f16(tb + 64, da, tc::sdesc_at(dbh, kC, s), id, s > 0);
-            tc::mma_f16(tb + 64, da, tc::sdesc_at(dbl, kC, s), id, true);
-          }
-          tc::mma_commit(&bar_w);
-        }
-      }
-      if (__syncthreads_or(bad) || __syncthreads_or(!mbar_wait(&bar_w, (uint32_t)((3 * r) & 1)))) {
-        tc::fence_before_sync();
-        __syncthreads();
-        if (warp == 0) tc::tmem_dealloc(tb, P_TMEM_COLS);
-        return;
-      }
-      tc::fence_after_sync();
-      const int j = tid & 127, hc = tid >> 7;
-      float x[32];
-      tc::tmem_ld16(tq + 64 + 32 * hc, *reinterpret_cast<float(*)[16]>(x));
-      tc::tmem_ld16(tq + 64 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(x + 16));
-      tc::tmem_wait_ld();
-      float4* du = reinterpret_cast<float4*>(w.u + (slot * kD + j) * kC + 32 * hc);
-#pragma unroll
-      for (int m = 0; m < 8; ++m) du[m] = make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
-      tc::fence_before_sync();
-      __syncthreads();  // every thread has its U columns; the V tile is free
-    }
-    // W = Tb diag(G rk) K on the tensor cores, rows t contiguous in i (the
-    // scan's K-major B operand): A = [hi; lo] tiles of Tb diag(ak) stacked as
-    // 128 rows (over the dead A), B = the k rows of the k/q tile read
-    // MN-major, one 64-wide i half at a time into TMEM columns 64-127. Row
-    // t' of the result is hi_t' K (t' < 64) or lo_{t'-64} K: the lo rows go
-    // through shared memory (over the dead Tb tiles, 16-byte chunks
-    // XOR-swizzled by row) and are added to the hi rows, which split the sum
-    // as hi + lo bf16.
-    auto issue_w = [&](int half) {
-      tc::fence_after_sync();
-      const uint32_t id = tc::idesc(tc::kBF16, 128, 64) | tc::kBMajorMN;
-      const uint64_t da = tc::sdesc_sw128(smem_u32(sm + P_OFF_A));
-      const uint32_t bk = smem_u32(sm + P_OFF_KQ) + 16384u * half;
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        tc::mma_f16(tb + 64, tc::sdesc_at(da, 128, s), tc::sdesc_mn(bk + 2048u * s, 16384u), id, s > 0);
-      tc::mma_commit(&bar_w);
-    };
-    if (tid == 0) {
-      issue_w(0);
-      if (r + 1 < p.rep) load_v(r + 1);
-    }
-    float* xb = Tp;  // [64][64] fp32 exchange of the lo rows
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      if (__syncthreads_or(!mbar_wait(&bar_w, (uint32_t)((3 * r + 1 + half) & 1)))) {
-        tc::fence_before_sync();
-        __syncthreads();
-        if (warp == 0) tc::tmem_dealloc(tb, P_TMEM_COLS);
-        return;
-      }
-      tc::fence_after_sync();
-      const int row = tid & 127, hc = tid >> 7;
-      float x[32];
-      tc::tmem_ld16(tq + 64 + 32 * hc, *reinterpret_cast<float(*)[16]>(x));
-      tc::tmem_ld16(tq + 64 + 32 * hc + 16, *reinterpret_cast<float(*)[16]>(x + 16));
-      tc::tmem_wait_ld();
-      tc::fence_before_sync();
-      __syncthreads();  // every thread has its columns: the next half may overwrite them
-      if (tid == 0 && half == 0) issue_w(1);
-      if (row >= kC) {
-        const int tr = row - kC;
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-          *reinterpret_cast<float4*>(xb + tr * kC + 4 * ((8 * hc + m) ^ (tr & 7))) =
-              make_float4(x[4 * m], x[4 * m + 1], x[4 * m + 2], x[4 * m + 3]);
-      }
-      __syncthreads();
-      if (row < kC) {
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const float4 lo4 = *reinterpret_cast<const float4*>(xb + row * kC + 4 * ((8 * hc + m) ^ (row & 7)));
-          x[4 * m] += lo4.x;
-          x[4 * m + 1] += lo4.y;
-          x[4 * m + 2] += lo4.z;
-          x[4 * m + 3] += lo4.w;
-        }
-        uint4* dh = reinterpret_cast<uint4*>(w.wm + ((slot * 2) * kC + row) * kD + 64 * half + 32 * hc);
-        uint4* dl = reinterpret_cast<uint4*>(w.wm + ((slot * 2 + 1) * kC + row) * kD + 64 * half + 32 * hc);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          uint4 hv, lv;
-          split8(x + 8 * m, hv, lv);
-          dh[m] = hv;
-          dl[m] = lv;
-        }
-      }
-      __syncthreads();  // the exchange buffer is reused by the next half
-    }
-    tc::fence_before_sync();
-    __syncthreads();  // A, Tm and the W columns are rewritten for the next V head
+    __syncthreads();  // A and Tm are rewritten for the next V head
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tb, P_TMEM_COLS);
+  if (warp == 0) tc::tmem_dealloc(tb, 64);
 }
 
-// ------------------------------------------------------------------ scan
+// ----------------------------------------------------------------- carry
 
-// Shared memory (byte offsets from a 1024-aligned base). The per-chunk
-// workspace tiles are double-buffered by chunk parity and loaded a chunk
-// ahead; V, K and Q are single tiles reloaded as soon as their MMA completes.
-constexpr uint32_t ST_U = 0;           // fp32 [2][128 j][32 t] SW128 (two t halves): U^T
-constexpr uint32_t ST_WHI = 32768;     // bf16 [64 t][128 i] SW128 (two i halves): W hi, K-major B
-constexpr uint32_t ST_WLO = 49152;     // W lo
-constexpr uint32_t ST_VEC = 65536;     // fp32 [4][64]: ak, dk, gq, {G_{L-1}}
-constexpr uint32_t ST_BYTES = 66560;   // one stage
-constexpr uint32_t SO_P = 2 * ST_BYTES;        // bf16 [64 t][64 s] SW128: P (K-major B of Dm^T P^T)
-constexpr uint32_t SO_K = SO_P + 8192;         // bf16 [128 i][64 t] SW128: k transposed, K-major B of the update
-constexpr uint32_t SO_Q = SO_K + 16384;        // bf16 [64 t][128 i] two i halves: K-major B of S Q^T
-constexpr uint32_t SO_DL = SO_Q + 16384;       // bf16 [128 j][64 t] SW128: Dm' lo, K-major A
-constexpr uint32_t SO_Z = SO_DL + 16384;       // bf16 [2][64 t][128 j] row-major: z (TMA), then out
-constexpr uint32_t S_SMEM = SO_Z + 32768 + 1024;
-static_assert(ST_U % 1024 == 0 && ST_WHI % 1024 == 0 && ST_WLO % 1024 == 0 && ST_BYTES % 1024 == 0 &&
-                  SO_P % 1024 == 0 && SO_K % 1024 == 0 && SO_Q % 1024 == 0 && SO_DL % 1024 == 0 &&
-                  SO_Z % 1024 == 0,
-              "tile alignment");
+// shared memory (byte offsets from a 1024-aligned base)
+constexpr uint32_t C_OFF_KQ = 0;         // bf16 [128][128 i] SW128 (TMA): rows 0-63 k, 64-127 q
+constexpr uint32_t C_OFF_KT = 32768;     // bf16 [2][128 i][64 t] SW128 (TMA, k transposed by prep)
+constexpr uint32_t C_OFF_TB = 65536;     // bf16 [2][128][64 s] SW128 (TMA): rows 0-63 Tb hi, 64-127 lo
+constexpr uint32_t C_OFF_P = 98304;      // bf16 [2][64 t][64 s] SW128 (TMA): P
+constexpr uint32_t C_OFF_V = 114688;     // bf16 [64 s][128 j] row-major (TMA)
+constexpr uint32_t C_OFF_VEC = 131072;   // fp32 [2][4][64] (bulk copy), by chunk parity
+constexpr uint32_t C_OFF_Z = 133120;     // bf16 [2][64 t][128 j] row-major: z (TMA), then out
+constexpr uint32_t C_SMEM = 165888 + 1024;
+// K^T, Tb and P are double-buffered by chunk parity and loaded a chunk ahead,
+// together with k and q, on one barrier per parity
+constexpr uint32_t kInBytes = 32768 + 16384 + 16384 + 8192;
 
-// TMEM columns. A operands are packed bf16 pairs (row j in lane j, K
-// elements 2c, 2c+1 in column c). A region is rewritten only after an MMA
-// commit or a barrier of its readers covers the previous contents.
-constexpr uint32_t TS_HI = 0;    // S hi (64): A of S W^T and S Q^T
-constexpr uint32_t TS_LO = 64;   // S lo (64)
-constexpr uint32_t TS_Y = 128;   // fp32 -S W^T (64); Dm^T = U^T + this
-constexpr uint32_t TS_S = 192;   // fp32 S (128): the state accumulator, pre-scaled by G_{L-1}
-constexpr uint32_t TS_DH = 320;  // (dk Dm)^T hi (32): A of the update
-constexpr uint32_t TS_DM = 352;  // Dm^T hi (32): A of Dm^T P^T
-constexpr uint32_t TS_OQ = 384;  // fp32 S Q^T (64)
-constexpr uint32_t TS_DP = 448;  // fp32 Dm^T P^T (64)
+// TMEM columns. A operands of the MMAs live in TMEM as packed bf16 pairs
+// (row j in lane j, K elements 2c, 2c+1 in column c). Each region is
+// rewritten only after every reader of its previous contents is known to be
+// done (an MMA commit or a wait on the reading threads' barrier).
+constexpr uint32_t TM_S = 0;      // fp32 S (128): the state accumulator
+constexpr uint32_t TM_X = 128;    // S hi (64) | S lo (64); fp32 [R_hi Tb^T | R_hi Tb_lo^T] after (3)
+constexpr uint32_t TM_XLO = 192;
+constexpr uint32_t TM_Z = 256;    // R^T hi (32) | lo (32); (dk Dm)^T hi | lo after (4)
+constexpr uint32_t TM_ZLO = 288;
+constexpr uint32_t TM_Y = 320;    // fp32 [KS | OQ] (128); Dm^T P^T over the KS half
+constexpr uint32_t TM_W = 448;    // Dm^T hi (32), A operand of Dm^T P^T
+constexpr uint32_t TM_COLS = 512;
 
-constexpr int kScanThreads = 576;  // warp 0 loads, warp 1 MMAs, 2-9 state, 10-17 output
-constexpr int kOutThreads = 256;
+constexpr int kIssueWarp = 16;                 // every MMA (a converged warp, one elected lane)
+constexpr int kLoadWarp = 17;                  // the carry's TMA loads (lane 0)
+constexpr int kOutThreads = 256;               // warps 8-15
+constexpr int kChainAll = kChainThreads + 64;  // + the issue and load warps
 
 // Bounded wait that gives up at once when another role has given up.
 __device__ __forceinline__ bool chain_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   return mbar_wait_bounded(bar, parity, abort_flag);
 }
 
-// A warp hands TMEM (and shared-memory) operands it wrote to the MMA warp.
-__device__ __forceinline__ void warp_done(uint64_t* bar, int lane) {
+// A carry warp hands one K slice of an A operand it wrote to the issue warp.
+__device__ __forceinline__ void slice_done(uint64_t* bar, int lane) {
   tc::tmem_wait_st();
-  fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncwarp();
   if (lane == 0) mbar_arrive(bar);
 }
 
-// Per chunk c, the MMA warp's order (each group waits for its operands):
-//   (a) Y = -(S_hi W_hi^T + S_hi W_lo^T + S_lo W_hi^T), in two K halves as
-//       the state copies arrive (conv1(c-1) has read Y by then)
-//   (o) OQ = S_hi Q^T                               once the output warps read OQ(c-1)
-//   (c) S += Dm'_hi K + Dm'_lo K, in two K halves   as conv1(c) writes Dm'
-//   (p) DP = Dm_hi P^T                              once the output warps read DP(c-1)
-// The state warps: conv1(c) after (a): Dm^T = U^T + Y, Dm' = Dm diag(dk) as
-// hi (TMEM) + lo (shared memory), Dm_hi (TMEM); conv2(c) after (c): the new
-// state's hi/lo copies, the accumulator rescaled by the next chunk's
-// G_{L-1}. Only (a) -> conv1 -> (c) -> conv2 -> (a) is a dependent chain;
-// (o), (p) and the output warps' gated norm run beside it.
-__global__ void __launch_bounds__(kScanThreads, 1)
-    cp_scan_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_u,
-                   const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_wm,
-                   const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_z,
-                   const __grid_constant__ CUtensorMap tm_o) {
+// Per chunk k (the issue warp's order; the carry warps hand over each K slice
+// of an operand as soon as it is in TMEM, so the MMAs on slice s run while
+// slice s+1 is computed):
+//   (1) [KS | OQ] = S_hi [k; q]^T + S_lo k^T, K = i in two slices (bar_sc)
+//   (2) R^T = V^T - diag(ak) KS^T -> hi/lo, K = s in two slices (bar_r)
+//   (3) [R_hi Tb^T | R_hi Tb_lo^T] (+ R_lo Tb^T onto the first half)
+//   (4) Dm^T = sum of the halves; (dk Dm)^T hi/lo and Dm^T hi (bar_d)
+//   (5) S += (dk Dm)^T K (hi, lo), on the accumulator pre-scaled by G_{L-1};
+//       Dm^T P^T over the KS half, for the output only
+//   (6) the new state: hi/lo copies (next chunk's (1)), accumulator rescaled
+// The load warp issues a buffer's next load once its last reader is done:
+//   K, Q, and Tb, P, K^T of chunk k+1 (into the buffers of chunk k-1), all on
+//   bar_in[(k+1) & 1], after (1) completes (its commit covers chunk k-1's
+//   (3) and (5));  V after every slice of (2);  vec two chunks ahead after
+//   every slice of (4)
+// The output group reads OQ after (1) and Dm^T P^T after (5), then releases
+// the [KS | OQ] columns (bar_oe) for chunk k+1's (1).
+__global__ void __launch_bounds__(kChainAll, 1)
+    cp_chain_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_z,
+                    const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_o) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) uint64_t bar_st[2], bar_p, bar_k, bar_q, bar_z[2];
-  __shared__ __align__(8) uint64_t bar_a, bar_oq, bar_cc, bar_dp, bar_fin;
-  // bar_s[q]: the state copies of column batch q (k-steps {0,1,4,5} / {2,3,6,7});
-  // bar_c1[b]: the corrections of token batch b (k-steps {0,2} / {1,3})
-  __shared__ __align__(8) uint64_t bar_s[2], bar_c1[2], bar_oqe, bar_dpe;
-  // per stage slot (so no waiter can fall two phases behind): the stage's
-  // MMAs have completed, the output warps have copied its gq
-  __shared__ __align__(8) uint64_t bar_sf[2], bar_gq[2];
+  __shared__ __align__(8) uint64_t bar_in[2], bar_v, bar_m1, bar_m3, bar_m5;
+  __shared__ __align__(8) uint64_t bar_vec[2], bar_of, bar_oe, bar_fin, bar_z[2];
+  __shared__ __align__(8) uint64_t bar_sc[2], bar_r[2], bar_d[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ float spart[4][kC];
@@ -803,32 +640,28 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   int64_t seq_s, seq_e;
   seq_range(p, n, seq_s, seq_e);
   const bool fused = p.z != nullptr;
+  const size_t HvG = (size_t)w.G * p.Hv;
 
   if (warp == 0) {
-    tc::tmem_alloc(&s_tmem, 512);
+    tc::tmem_alloc(&s_tmem, TM_COLS);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
+    mbar_init(&bar_v, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar_st[b], 1);
+      mbar_init(&bar_in[b], 1);
+      mbar_init(&bar_vec[b], 1);
       mbar_init(&bar_z[b], 1);
-      mbar_init(&bar_sf[b], 1);
-      mbar_init(&bar_gq[b], 8);
+      mbar_init(&bar_sc[b], kCarryThreads / 32);
+      mbar_init(&bar_r[b], kCarryThreads / 32);
+      mbar_init(&bar_d[b], kCarryThreads / 32);
     }
-    mbar_init(&bar_p, 1);
-    mbar_init(&bar_k, 1);
-    mbar_init(&bar_q, 1);
-    mbar_init(&bar_a, 1);
-    mbar_init(&bar_oq, 1);
-    mbar_init(&bar_cc, 1);
-    mbar_init(&bar_dp, 1);
+    mbar_init(&bar_m1, 1);
+    mbar_init(&bar_m3, 1);
+    mbar_init(&bar_m5, 1);
+    mbar_init(&bar_of, 1);
+    mbar_init(&bar_oe, kOutThreads);
     mbar_init(&bar_fin, 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar_s[b], 8);
-      mbar_init(&bar_c1[b], 8);
-    }
-    mbar_init(&bar_oqe, 8);
-    mbar_init(&bar_dpe, 8);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -837,312 +670,354 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   tc::fence_after_sync();
   const uint32_t tb = s_tmem;
   volatile int* abort_flag = &s_abort;
-  auto chunk_c0 = [&](int c) { return seq_s + (int64_t)kC * c; };
-  auto slot_of = [&](int c) { return (size_t)(kb + c) * p.Hv + h; };
-  auto stage = [&](int c) { return sm + (uint32_t)(c & 1) * ST_BYTES; };
+  auto chunk_c0 = [&](int k) { return seq_s + (int64_t)kC * k; };
+  auto slot_of = [&](int k) { return (size_t)(kb + k) * p.Hv + h; };
 
-  // the loader's copies in flight, for the exit path
-  uint32_t n_st0 = 0, n_st1 = 0, n_p = 0, n_k = 0, n_q = 0;
-  const bool loader = warp == 0 && lane == 0;
+  // the load warp's loads; the counts let the exit path wait for copies in
+  // flight
+  uint32_t n_in0 = 0, n_in1 = 0, n_v = 0, n_vec0 = 0, n_vec1 = 0;
+  const bool loader = warp == kLoadWarp && lane == 0;
 
-  if (warp == 0) {
-    // ================================================ loads (lane 0)
-    if (loader) {
-      auto load_stage = [&](int c) {
-        uint64_t* bar = &bar_st[c & 1];
-        if (c & 1) ++n_st1; else ++n_st0;
-        mbar_arrive_expect_tx(bar, ST_BYTES);
-        unsigned char* st = stage(c);
-        const size_t slot = slot_of(c);
-        tc::tma_load_2d(st + ST_U, &tm_u, 0, (int)(slot * kD), bar);
-        tc::tma_load_2d(st + ST_U + 16384, &tm_u, 32, (int)(slot * kD), bar);
-        tc::tma_load_2d(st + ST_WHI, &tm_wm, 0, (int)(slot * 2 * kC), bar);
-        tc::tma_load_2d(st + ST_WHI + 8192, &tm_wm, 64, (int)(slot * 2 * kC), bar);
-        tc::tma_load_2d(st + ST_WLO, &tm_wm, 0, (int)(slot * 2 * kC + kC), bar);
-        tc::tma_load_2d(st + ST_WLO + 8192, &tm_wm, 64, (int)(slot * 2 * kC + kC), bar);
-        bulk_load(st + ST_VEC, w.vec + slot * (4 * kC), 1024u, bar);
-      };
-      auto load_p = [&](int c) {
-        ++n_p;
-        mbar_arrive_expect_tx(&bar_p, 8192u);
-        tc::tma_load_2d(sm + SO_P, &tm_w, 0, (int)(slot_of(c) * kC), &bar_p);
-      };
-      auto load_kt = [&](int c) {
-        ++n_k;
-        mbar_arrive_expect_tx(&bar_k, 16384u);
-        tc::tma_load_2d(sm + SO_K, &tm_kt, 0, (int)(((kb + c) * p.Hk + kh) * kD), &bar_k);
-      };
-      auto load_q = [&](int c) {
-        ++n_q;
-        mbar_arrive_expect_tx(&bar_q, 16384u);
-        const int y = (int)chunk_c0(c);
-        tc::tma_load_2d(sm + SO_Q, &tm_q, kh * kD, y, &bar_q);
-        tc::tma_load_2d(sm + SO_Q + 8192, &tm_q, kh * kD + 64, y, &bar_q);
-      };
-      load_stage(0);
-      if (nch > 1) load_stage(1);
-      load_kt(0);
-      load_q(0);
-      load_p(0);
-      for (int c = 0; c < nch; ++c) {
-        const uint32_t ph = (uint32_t)(c & 1);
-        const bool more = c + 1 < nch;
-        if (!chain_wait(&bar_oq, ph, abort_flag)) break;
-        if (more) load_q(c + 1);
-        if (!chain_wait(&bar_cc, ph, abort_flag)) break;
-        if (more) load_kt(c + 1);
-        // stage c is free once its MMAs completed and the output warps have
-        // copied its gq; P once (p) completed
-        const uint32_t sp = (uint32_t)((c >> 1) & 1);
-        if (!chain_wait(&bar_sf[c & 1], sp, abort_flag)) break;
-        if (more) load_p(c + 1);
-        if (!chain_wait(&bar_gq[c & 1], sp, abort_flag)) break;
-        if (c + 2 < nch) load_stage(c + 2);
-      }
+  if (loader) {
+    // the MMA operands of chunk k on bar_in[k & 1]: the expected bytes are
+    // posted once per phase, the copies may land before or after
+    auto arm_in = [&](int k) {
+      if (k & 1) ++n_in1; else ++n_in0;
+      mbar_arrive_expect_tx(&bar_in[k & 1], kInBytes);
+    };
+    auto load_kq = [&](int k) {
+      uint64_t* bar = &bar_in[k & 1];
+      const int y = (int)chunk_c0(k);
+      tc::tma_load_2d(sm + C_OFF_KQ, &tm_k, kh * kD, y, bar);
+      tc::tma_load_2d(sm + C_OFF_KQ + 16384, &tm_k, kh * kD + 64, y, bar);
+      tc::tma_load_2d(sm + C_OFF_KQ + 8192, &tm_q, kh * kD, y, bar);
+      tc::tma_load_2d(sm + C_OFF_KQ + 24576, &tm_q, kh * kD + 64, y, bar);
+    };
+    auto load_tbpk = [&](int k) {
+      uint64_t* bar = &bar_in[k & 1];
+      const int b = k & 1;
+      const size_t slot = slot_of(k);
+      tc::tma_load_2d(sm + C_OFF_TB + b * 16384, &tm_w, 0, (int)(slot * kC), bar);
+      tc::tma_load_2d(sm + C_OFF_TB + b * 16384 + 8192, &tm_w, 0, (int)((HvG + slot) * kC), bar);
+      tc::tma_load_2d(sm + C_OFF_P + b * 8192, &tm_w, 0, (int)((2 * HvG + slot) * kC), bar);
+      tc::tma_load_2d(sm + C_OFF_KT + b * 16384, &tm_kt, 0, (int)(((kb + k) * p.Hk + kh) * kD), bar);
+    };
+    auto load_v = [&](int k) {
+      ++n_v;
+      mbar_arrive_expect_tx(&bar_v, 16384u);
+      tc::tma_load_2d(sm + C_OFF_V, &tm_v, h * kD, (int)chunk_c0(k), &bar_v);
+    };
+    auto load_vec = [&](int k) {
+      uint64_t* bar = &bar_vec[k & 1];
+      if (k & 1) ++n_vec1; else ++n_vec0;
+      mbar_arrive_expect_tx(bar, 1024u);
+      bulk_load(sm + C_OFF_VEC + (k & 1) * 1024, w.vec + slot_of(k) * (4 * kC), 1024u, bar);
+    };
+    arm_in(0);
+    load_kq(0);
+    load_tbpk(0);
+    load_v(0);
+    load_vec(0);
+    if (nch > 1) {
+      arm_in(1);
+      load_tbpk(1);
+      load_vec(1);
     }
-  } else if (warp == 1) {
-    // ================================================ MMA issue (one warp)
-    const uint32_t id_a = tc::idesc(tc::kBF16, 128, 64) | tc::kNegB;
-    const uint32_t id_o = tc::idesc(tc::kBF16, 128, 64);
-    const uint32_t id_c = tc::idesc(tc::kBF16, 128, 128);
-    const uint64_t d_q = tc::sdesc_sw128(smem_u32(sm + SO_Q));
-    const uint64_t d_kt = tc::sdesc_sw128(smem_u32(sm + SO_K));
-    const uint64_t d_dl = tc::sdesc_sw128(smem_u32(sm + SO_DL));
-    const uint64_t d_p = tc::sdesc_sw128(smem_u32(sm + SO_P));
-    bool ok = true;
-    for (int c = 0; c < nch && ok; ++c) {
-      const uint32_t ph = (uint32_t)(c & 1), pp = (uint32_t)((c + 1) & 1);
-      unsigned char* st = stage(c);
-      const uint64_t d_wh = tc::sdesc_sw128(smem_u32(st + ST_WHI));
-      const uint64_t d_wl = tc::sdesc_sw128(smem_u32(st + ST_WLO));
-      // (a), in two halves as the state copies arrive
+    for (int k = 0; k < nch; ++k) {
+      const uint32_t ph = (uint32_t)(k & 1);
+      const bool more = k + 1 < nch;
+      if (!chain_wait(&bar_m1, ph, abort_flag)) break;
+      if (more) {
+        if (k >= 1) {
+          arm_in(k + 1);
+          load_tbpk(k + 1);  // into chunk k-1's buffers
+        }
+        load_kq(k + 1);
+      }
+      if (!chain_wait(&bar_r[1], ph, abort_flag)) break;
+      if (more) load_v(k + 1);  // every slice of (2) has read V
+      if (!chain_wait(&bar_d[1], ph, abort_flag)) break;
+      if (k + 2 < nch) load_vec(k + 2);  // every slice of (4) has read these vectors
+    }
+  } else if (warp == kIssueWarp) {
+    const uint32_t id64 = tc::idesc(tc::kBF16, 128, 64), id128 = tc::idesc(tc::kBF16, 128, 128);
+    const uint64_t d_kq = tc::sdesc_sw128(smem_u32(sm + C_OFF_KQ)),
+                   d_kt = tc::sdesc_sw128(smem_u32(sm + C_OFF_KT)),
+                   d_tb = tc::sdesc_sw128(smem_u32(sm + C_OFF_TB)),
+                   d_p = tc::sdesc_sw128(smem_u32(sm + C_OFF_P));
+    for (int k = 0; k < nch; ++k) {
+      const uint32_t ph = (uint32_t)(k & 1);
+      bool ok = chain_wait(&bar_in[k & 1], (uint32_t)((k >> 1) & 1), abort_flag);
+      if (ok && k >= 1) ok = chain_wait(&bar_oe, (uint32_t)((k - 1) & 1), abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      // (1) slice s of the state copies covers k-steps 2s, 2s+1, 4+2s, 5+2s
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        ok = (q > 0 || chain_wait(&bar_st[c & 1], (uint32_t)((c >> 1) & 1), abort_flag)) &&
-             chain_wait(&bar_s[q], ph, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) break;
+      for (int s = 0; s < 2; ++s) {
+        ok = __all_sync(0xffffffffu, chain_wait(&bar_sc[s], ph, abort_flag));
+        if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int s = 2 * q + (e & 1) + 4 * (e >> 1);
-          const uint64_t bh = tc::sdesc_at(d_wh, kC, s), bl = tc::sdesc_at(d_wl, kC, s);
-          tc::mma_f16_ts_elect(tb + TS_Y, tb + TS_HI + 8 * s, bh, id_a, s > 0);
-          tc::mma_f16_ts_elect(tb + TS_Y, tb + TS_HI + 8 * s, bl, id_a, true);
-          tc::mma_f16_ts_elect(tb + TS_Y, tb + TS_LO + 8 * s, bh, id_a, true);
+          const int ks = 2 * s + (e & 1) + 4 * (e >> 1);
+          tc::mma_f16_ts_elect(tb + TM_Y, tb + TM_X + 8 * ks, tc::sdesc_at(d_kq, 128, ks), id128, ks > 0);
+          tc::mma_f16_ts_elect(tb + TM_Y, tb + TM_XLO + 8 * ks, tc::sdesc_at(d_kq, 128, ks), id64, true);
         }
       }
       if (!ok) break;
-      tc::mma_commit_elect(&bar_a);
-      // (o)
-      ok = chain_wait(&bar_q, ph, abort_flag) && (c == 0 || chain_wait(&bar_oqe, pp, abort_flag));
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc::fence_after_sync();
+      tc::mma_commit_elect(&bar_m1);
+      // (3) slice s of R covers k-steps s and 2 + s; B = [Tb hi; Tb lo]
+      // (N=128) for R hi, Tb hi (N=64) for R lo
+      const uint64_t dtb = d_tb + (uint64_t)((k & 1) * 16384 >> 4);
 #pragma unroll
-      for (int s = 0; s < 8; ++s)
-        tc::mma_f16_ts_elect(tb + TS_OQ, tb + TS_HI + 8 * s, tc::sdesc_at(d_q, kC, s), id_o, s > 0);
-      tc::mma_commit_elect(&bar_oq);
-      // (c), in two halves as the corrections arrive
-      ok = chain_wait(&bar_k, ph, abort_flag);
-#pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        ok = ok && chain_wait(&bar_c1[b], ph, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) break;
+      for (int s = 0; s < 2; ++s) {
+        ok = __all_sync(0xffffffffu, chain_wait(&bar_r[s], ph, abort_flag));
+        if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int s = b + 2 * e;
-          const uint64_t bk = tc::sdesc_at(d_kt, 128, s);
-          tc::mma_f16_ts_elect(tb + TS_S, tb + TS_DH + 8 * s, bk, id_c, true);
-          tc::mma_f16_elect(tb + TS_S, tc::sdesc_at(d_dl, 128, s), bk, id_c, true);
+          const int ks = s + 2 * e;
+          tc::mma_f16_ts_elect(tb + TM_X, tb + TM_Z + 8 * ks, tc::sdesc_at(dtb, 128, ks), id128, ks > 0);
+          tc::mma_f16_ts_elect(tb + TM_X, tb + TM_ZLO + 8 * ks, tc::sdesc_at(dtb, 64, ks), id64, true);
         }
       }
       if (!ok) break;
-      tc::mma_commit_elect(&bar_cc);
-      // (p)
-      ok = chain_wait(&bar_p, ph, abort_flag) && (c == 0 || chain_wait(&bar_dpe, pp, abort_flag));
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc::fence_after_sync();
+      tc::mma_commit_elect(&bar_m3);
+      // (5) slice s of Dm covers k-steps s and 2 + s
+      const uint64_t dkt = d_kt + (uint64_t)((k & 1) * 16384 >> 4);
+      const uint64_t dp = d_p + (uint64_t)((k & 1) * 8192 >> 4);
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
-        tc::mma_f16_ts_elect(tb + TS_DP, tb + TS_DM + 8 * s, tc::sdesc_at(d_p, kC, s), id_o, s > 0);
-      tc::mma_commit_elect(&bar_dp);
-      tc::mma_commit_elect(&bar_sf[c & 1]);
+      for (int s = 0; s < 2; ++s) {
+        ok = __all_sync(0xffffffffu, chain_wait(&bar_d[s], ph, abort_flag));
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int ks = s + 2 * e;
+          tc::mma_f16_ts_elect(tb + TM_S, tb + TM_Z + 8 * ks, tc::sdesc_at(dkt, 128, ks), id128, true);
+          tc::mma_f16_ts_elect(tb + TM_S, tb + TM_ZLO + 8 * ks, tc::sdesc_at(dkt, 128, ks), id128, true);
+        }
+        if (s == 0) {
+          tc::mma_f16_ts_elect(tb + TM_Y, tb + TM_W, tc::sdesc_at(dp, 64, 0), id64, false);
+          tc::mma_f16_ts_elect(tb + TM_Y, tb + TM_W + 16, tc::sdesc_at(dp, 64, 2), id64, true);
+        }
+      }
+      if (!ok) break;
+      tc::mma_commit_elect(&bar_m5);
+      tc::mma_f16_ts_elect(tb + TM_Y, tb + TM_W + 8, tc::sdesc_at(dp, 64, 1), id64, true);
+      tc::mma_f16_ts_elect(tb + TM_Y, tb + TM_W + 24, tc::sdesc_at(dp, 64, 3), id64, true);
+      tc::mma_commit_elect(&bar_of);  // OQ and Dm^T P^T of this chunk
     }
-  } else if (warp < 10) {
-    // ============================ state warps: thread (j, hf) owns value row j
-    // (TMEM lane j), state columns i in [64 hf, 64 hf + 64) and tokens t in
-    // [32 hf, 32 hf + 32) of the per-chunk corrections
-    const int q4 = warp & 3, hf = (warp - 2) >> 2;
-    const int j = 32 * q4 + lane;
-    const uint32_t tl = tb + ((uint32_t)(32 * q4) << 16);
-    float* gS = p.state + (((size_t)n * p.Hv + h) * kD + j) * kD + 64 * hf;
+  } else if (tid < kCarryThreads) {
+    // ============================ carry group: thread (j, ch) owns value row j
+    // (TMEM lane j) and half ch of the columns of each per-row phase
+    const int j = tid & 127, ch = tid >> 7;
+    const uint32_t tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
+    float* gS = p.state + (((size_t)n * p.Hv + h) * kD + j) * kD + 64 * ch;
 
-    // the state -> its hi/lo copies and the accumulator rescaled by `gl`
-    // (or, after the last chunk, the state to memory); 32 columns at a time,
-    // every TMEM load of a batch issued before one wait
-    auto pass_state = [&](bool from_memory, bool last, float gl) {
+    // 64 fp32 state values (this thread's half row) -> hi/lo A operands in
+    // TMEM, one 32-wide K slice at a time, then the accumulator rescaled by gl
+    auto store_state = [&](float (&v)[kC], float gl) {
 #pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
-        float v[32];
-        if (from_memory) {
-          const float4* src = reinterpret_cast<const float4*>(gS + 32 * qq);
+      for (int s = 0; s < 2; ++s) {
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const float4 f = src[m];
-            v[4 * m] = f.x;
-            v[4 * m + 1] = f.y;
-            v[4 * m + 2] = f.z;
-            v[4 * m + 3] = f.w;
-          }
-        } else {
-          tc::tmem_ld16(tl + TS_S + 64 * hf + 32 * qq, *reinterpret_cast<float(*)[16]>(v));
-          tc::tmem_ld16(tl + TS_S + 64 * hf + 32 * qq + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-          tc::tmem_wait_ld();
-        }
-        if (last) {
-          float4* dst = reinterpret_cast<float4*>(gS + 32 * qq);
-#pragma unroll
-          for (int m = 0; m < 8; ++m) dst[m] = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
-          continue;
-        }
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int q = 0; q < 2; ++q) {
           uint32_t hw[8], lw[8];
 #pragma unroll
           for (int m = 0; m < 8; ++m) {
-            const float a0 = v[16 * hh + 2 * m], a1 = v[16 * hh + 2 * m + 1];
+            const float a0 = v[32 * s + 16 * q + 2 * m], a1 = v[32 * s + 16 * q + 2 * m + 1];
             const __nv_bfloat162 hv = __floats2bfloat162_rn(a0, a1);
             hw[m] = *reinterpret_cast<const uint32_t*>(&hv);
             lw[m] = pack_bf16(a0 - __low2float(hv), a1 - __high2float(hv));
           }
-          tc::tmem_st8u(tl + TS_HI + 32 * hf + 16 * qq + 8 * hh, hw);
-          tc::tmem_st8u(tl + TS_LO + 32 * hf + 16 * qq + 8 * hh, lw);
+          tc::tmem_st8u(tl + TM_X + 32 * ch + 16 * s + 8 * q, hw);
+          tc::tmem_st8u(tl + TM_XLO + 32 * ch + 16 * s + 8 * q, lw);
         }
-#pragma unroll
-        for (int m = 0; m < 32; ++m) v[m] *= gl;
-        warp_done(&bar_s[qq], lane);
-        tc::tmem_st16(tl + TS_S + 64 * hf + 32 * qq, *reinterpret_cast<const float(*)[16]>(v));
-        tc::tmem_st16(tl + TS_S + 64 * hf + 32 * qq + 16, *reinterpret_cast<const float(*)[16]>(v + 16));
+        slice_done(&bar_sc[s], lane);
       }
+#pragma unroll
+      for (int e = 0; e < kC; ++e) v[e] *= gl;
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        tc::tmem_st16(tl + TM_S + 64 * ch + 16 * m, *reinterpret_cast<const float(*)[16]>(v + 16 * m));
     };
 
-    bool to = !chain_wait(&bar_st[0], 0, abort_flag);
+    bool to = !chain_wait(&bar_vec[0], 0, abort_flag);
     to = __any_sync(0xffffffffu, to);
-    if (!to) pass_state(true, false, reinterpret_cast<const float*>(sm + ST_VEC)[3 * kC]);
+    if (!to) {
+      float v[kC];
+      const float4* src = reinterpret_cast<const float4*>(gS);
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float4 f = src[m];
+        v[4 * m] = f.x;
+        v[4 * m + 1] = f.y;
+        v[4 * m + 2] = f.z;
+        v[4 * m + 3] = f.w;
+      }
+      store_state(v, reinterpret_cast<const float*>(sm + C_OFF_VEC)[3 * kC]);
+    }
 
-    for (int c = 0; c < nch && !to; ++c) {
-      const uint32_t ph = (uint32_t)(c & 1);
-      const bool more = c + 1 < nch;
-      const float* vec = reinterpret_cast<const float*>(stage(c) + ST_VEC);
-      // conv1: Dm^T = U^T + Y; (dk Dm)^T hi -> TMEM, lo -> shared memory;
-      // Dm^T hi -> TMEM
-      to = !chain_wait(&bar_st[c & 1], (uint32_t)((c >> 1) & 1), abort_flag) ||
-           !chain_wait(&bar_a, ph, abort_flag);
+    for (int k = 0; k < nch && !to; ++k) {
+      const uint32_t ph = (uint32_t)(k & 1);
+      const int64_t c0 = chunk_c0(k);
+      const int L = (int)((seq_e - c0) < kC ? (seq_e - c0) : kC);
+      const float* vec = reinterpret_cast<const float*>(sm + C_OFF_VEC + (k & 1) * 1024);
+      const bool more = k + 1 < nch;
+
+      // (2) R^T = V^T - diag(ak) KS^T (columns s >= L zero); this thread's
+      // 32 columns s = 32 ch .., two slices of 16
+      // (V and the vectors landed long before (1) completes: checked first)
+      to = !chain_wait(&bar_v, ph, abort_flag) ||
+           !chain_wait(&bar_vec[k & 1], (uint32_t)((k >> 1) & 1), abort_flag) ||
+           !chain_wait(&bar_m1, ph, abort_flag);
       if (__any_sync(0xffffffffu, to)) break;
       tc::fence_after_sync();
+      {
+        const __nv_bfloat16* vt = reinterpret_cast<const __nv_bfloat16*>(sm + C_OFF_V) + j;
+        float ks[32];
 #pragma unroll
-      for (int bt = 0; bt < 2; ++bt) {
-        const int t0 = 32 * hf + 16 * bt;
-        float y[16], dk[16];
-        tc::tmem_ld16(tl + TS_Y + t0, y);
-        const unsigned char* ur = stage(c) + ST_U + hf * 16384 + (j >> 3) * 1024 + (j & 7) * 128;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float4 d4 = reinterpret_cast<const float4*>(vec + kC + t0)[m];
-          dk[4 * m] = d4.x;
-          dk[4 * m + 1] = d4.y;
-          dk[4 * m + 2] = d4.z;
-          dk[4 * m + 3] = d4.w;
-        }
-        float uv[16];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float4 u4 = *reinterpret_cast<const float4*>(ur + (((4 * bt + m) ^ (j & 7)) << 4));
-          uv[4 * m] = u4.x;
-          uv[4 * m + 1] = u4.y;
-          uv[4 * m + 2] = u4.z;
-          uv[4 * m + 3] = u4.w;
-        }
+        for (int m = 0; m < 2; ++m)
+          tc::tmem_ld16(tl + TM_Y + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(ks + 16 * m));
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int m = 0; m < 16; ++m) y[m] += uv[m];
-        uint32_t dh[8], dm[8], dl[8];
+        for (int s = 0; s < 2; ++s) {
+          uint32_t hw[8], lw[8];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const float x0 = y[2 * m] * dk[2 * m], x1 = y[2 * m + 1] * dk[2 * m + 1];
-          const __nv_bfloat162 hv = __floats2bfloat162_rn(x0, x1);
-          dh[m] = *reinterpret_cast<const uint32_t*>(&hv);
-          dl[m] = pack_bf16(x0 - __low2float(hv), x1 - __high2float(hv));
-          dm[m] = pack_bf16(y[2 * m], y[2 * m + 1]);
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 a4 = reinterpret_cast<const float4*>(vec)[8 * ch + 4 * s + e4];
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+            float r[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int e = 16 * s + 4 * e4 + u, t = 32 * ch + e;
+              const float x = __bfloat162float(vt[t * kD]) - av[u] * ks[e];
+              r[u] = t < L ? x : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const __nv_bfloat162 hv = __floats2bfloat162_rn(r[2 * u], r[2 * u + 1]);
+              hw[2 * e4 + u] = *reinterpret_cast<const uint32_t*>(&hv);
+              lw[2 * e4 + u] = pack_bf16(r[2 * u] - __low2float(hv), r[2 * u + 1] - __high2float(hv));
+            }
+          }
+          tc::tmem_st8u(tl + TM_Z + 16 * ch + 8 * s, hw);
+          tc::tmem_st8u(tl + TM_ZLO + 16 * ch + 8 * s, lw);
+          slice_done(&bar_r[s], lane);
         }
-        tc::tmem_st8u(tl + TS_DH + t0 / 2, dh);
-        tc::tmem_st8u(tl + TS_DM + t0 / 2, dm);
-        *reinterpret_cast<uint4*>(sm + SO_DL + sw_chunk(j, t0 / 8, 128)) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
-        *reinterpret_cast<uint4*>(sm + SO_DL + sw_chunk(j, t0 / 8 + 1, 128)) = make_uint4(dl[4], dl[5], dl[6], dl[7]);
-        warp_done(&bar_c1[bt], lane);
       }
-      // conv2: the new state; the next chunk's G_{L-1} from its stage
-      to = (more && !chain_wait(&bar_st[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1), abort_flag)) ||
-           !chain_wait(&bar_cc, ph, abort_flag);
+
+      // (4) Dm^T = [R Tb^T halves summed]; (dk Dm)^T hi/lo into R's columns
+      // and Dm^T hi for the output; this thread's 32 columns t, two slices
+      to = !chain_wait(&bar_m3, ph, abort_flag);
       if (__any_sync(0xffffffffu, to)) break;
       tc::fence_after_sync();
-      pass_state(false, !more, more ? reinterpret_cast<const float*>(stage(c + 1) + ST_VEC)[3 * kC] : 1.f);
+      {
+        float dm[32];
+        {
+          float db[32];
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            tc::tmem_ld16(tl + TM_X + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(dm + 16 * m));
+            tc::tmem_ld16(tl + TM_XLO + 32 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(db + 16 * m));
+          }
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) dm[e] += db[e];
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          uint32_t hw[8], lw[8], dw[8];
+#pragma unroll
+          for (int m = 0; m < 8; ++m) dw[m] = pack_bf16(dm[16 * s + 2 * m], dm[16 * s + 2 * m + 1]);
+          tc::tmem_st8u(tl + TM_W + 16 * ch + 8 * s, dw);
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 d4 = reinterpret_cast<const float4*>(vec + kC)[8 * ch + 4 * s + e4];
+            const int e = 16 * s + 4 * e4;
+            const float x0 = d4.x * dm[e], x1 = d4.y * dm[e + 1];
+            const float x2 = d4.z * dm[e + 2], x3 = d4.w * dm[e + 3];
+            const __nv_bfloat162 h01 = __floats2bfloat162_rn(x0, x1), h23 = __floats2bfloat162_rn(x2, x3);
+            hw[2 * e4] = *reinterpret_cast<const uint32_t*>(&h01);
+            hw[2 * e4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+            lw[2 * e4] = pack_bf16(x0 - __low2float(h01), x1 - __high2float(h01));
+            lw[2 * e4 + 1] = pack_bf16(x2 - __low2float(h23), x3 - __high2float(h23));
+          }
+          tc::tmem_st8u(tl + TM_Z + 16 * ch + 8 * s, hw);
+          tc::tmem_st8u(tl + TM_ZLO + 16 * ch + 8 * s, lw);
+          slice_done(&bar_d[s], lane);
+        }
+      }
+
+      // (6) the new state: operand copies and the next chunk's decay in TMEM;
+      // after the last chunk, back to global memory
+      to = more && !chain_wait(&bar_vec[(k + 1) & 1], (uint32_t)(((k + 1) >> 1) & 1), abort_flag);
+      to = to || !chain_wait(&bar_m5, ph, abort_flag);
+      if (__any_sync(0xffffffffu, to)) break;
+      tc::fence_after_sync();
+      {
+        float v[kC];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          tc::tmem_ld16(tl + TM_S + 64 * ch + 16 * m, *reinterpret_cast<float(*)[16]>(v + 16 * m));
+        tc::tmem_wait_ld();
+        if (!more) {
+          float4* dst = reinterpret_cast<float4*>(gS);
+#pragma unroll
+          for (int m = 0; m < 16; ++m)
+            dst[m] = make_float4(v[4 * m], v[4 * m + 1], v[4 * m + 2], v[4 * m + 3]);
+        } else {
+          store_state(v, reinterpret_cast<const float*>(sm + C_OFF_VEC + ((k + 1) & 1) * 1024)[3 * kC]);
+        }
+      }
     }
     tc::tmem_wait_st();
     tc::fence_before_sync();
-  } else {
-    // ============================ output warps: thread (j, hf) owns output
-    // column j = 32 (warp % 4) + lane for the 32 tokens t0 = 32 hf ... With
-    // the fused norm, the per-token sums of squares are reduce-scattered
-    // across lanes, z arrives by TMA into a row-major tile (two, by chunk
-    // parity) that the gated result overwrites in place, and a full chunk
-    // leaves as one 2-D TMA store.
-    const int u = tid - 320, q4 = warp & 3, hf = (warp - 10) >> 2;
-    const int j = 32 * q4 + lane, t0 = 32 * hf;
+  } else if (tid < kChainThreads) {
+    // ============================ output group: 8 warps; thread (j, half)
+    // owns output column j = 32 (warp % 4) + lane for the 32 rows of its half.
+    // OQ is read once (1) completes and Dm^T P^T once (5) completes; then
+    // TMEM is released to the next chunk. With the fused norm, the per-row
+    // sums of squares are reduce-scattered across lanes, z arrives by TMA into
+    // a row-major tile (two, by chunk parity) that the gated result overwrites
+    // in place, and each live row leaves as one 256-byte bulk store.
+    const int u = tid - kCarryThreads, q4 = warp & 3, half = (warp - 8) >> 2;
+    const int j = 32 * q4 + lane, t0 = 32 * half;
     const uint32_t tl = tb + ((uint32_t)(32 * q4) << 16);
     const float nwj = fused ? p.norm_w[j] : 0.f;
     uint32_t n_z0 = 0, n_z1 = 0;
     bool stored = false;
-    auto load_z = [&](int c) {
-      if (c & 1) ++n_z1; else ++n_z0;
-      mbar_arrive_expect_tx(&bar_z[c & 1], 16384u);
-      tc::tma_load_2d(sm + SO_Z + (c & 1) * 16384, &tm_z, h * kD, (int)chunk_c0(c), &bar_z[c & 1]);
+    auto load_z = [&](int k) {
+      if (k & 1) ++n_z1; else ++n_z0;
+      mbar_arrive_expect_tx(&bar_z[k & 1], 16384u);
+      tc::tma_load_2d(sm + C_OFF_Z + (k & 1) * 16384, &tm_z, h * kD, (int)chunk_c0(k), &bar_z[k & 1]);
     };
     if (fused && u == 0) {
       load_z(0);
       if (nch > 1) load_z(1);
     }
     bool to = false;  // a bounded wait gave up (agreed on at the next barrier)
-    for (int c = 0; c < nch; ++c) {
-      const int64_t c0 = chunk_c0(c);
+    for (int k = 0; k < nch; ++k) {
+      const int64_t c0 = chunk_c0(k);
       const int L = (int)((seq_e - c0) < kC ? (seq_e - c0) : kC);
-      const float* vec = reinterpret_cast<const float*>(stage(c) + ST_VEC);
-      __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(sm + SO_Z + (c & 1) * 16384);
+      const float* gq = sgq[k & 1] + t0;
+      __nv_bfloat16* zb = reinterpret_cast<__nv_bfloat16*>(sm + C_OFF_Z + (k & 1) * 16384);
+      if (u < kC) sgq[k & 1][u] = __ldg(w.vec + slot_of(k) * (4 * kC) + 2 * kC + u);
       float a[2][16], b[2][16];
-      to |= !chain_wait(&bar_st[c & 1], (uint32_t)((c >> 1) & 1), abort_flag) ||
-            !chain_wait(&bar_oq, (uint32_t)(c & 1), abort_flag);
-      if (bar_or(2, kOutThreads, to)) break;
-      tc::fence_after_sync();
+      to |= !chain_wait(&bar_m1, (uint32_t)(k & 1), abort_flag);
+      if (!__any_sync(0xffffffffu, to)) {
+        tc::fence_after_sync();
 #pragma unroll
-      for (int m = 0; m < 2; ++m) tc::tmem_ld16(tl + TS_OQ + t0 + 16 * m, a[m]);
-      tc::tmem_wait_ld();
-      if (u < kC) sgq[c & 1][u] = vec[2 * kC + u];
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bar_oqe);       // OQ(c) read
-        mbar_arrive(&bar_gq[c & 1]);  // and gq(c) copied: stage c may be reloaded
+        for (int m = 0; m < 2; ++m) tc::tmem_ld16(tl + TM_Y + 64 + t0 + 16 * m, a[m]);
+        tc::tmem_wait_ld();
       }
-      to |= !chain_wait(&bar_dp, (uint32_t)(c & 1), abort_flag);
+      to |= !chain_wait(&bar_of, (uint32_t)(k & 1), abort_flag);
       if (bar_or(2, kOutThreads, to)) break;
       tc::fence_after_sync();
 #pragma unroll
-      for (int m = 0; m < 2; ++m) tc::tmem_ld16(tl + TS_DP + t0 + 16 * m, b[m]);
+      for (int m = 0; m < 2; ++m) tc::tmem_ld16(tl + TM_Y + t0 + 16 * m, b[m]);
       tc::tmem_wait_ld();
       tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_dpe);
-      const float* gq = sgq[c & 1] + t0;
+      mbar_arrive(&bar_oe);  // this chunk's output accumulators are free
       float o[32];
 #pragma unroll
       for (int m = 0; m < 2; ++m)
@@ -1174,8 +1049,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
       }
 #pragma unroll
-      for (int stp = 1; stp < 5; ++stp) {
-        const int m = 16 >> stp, hv = 16 >> stp;
+      for (int st = 1; st < 5; ++st) {
+        const int m = 16 >> st, hv = 16 >> st;
         const bool up = (lane & m) != 0;
 #pragma unroll
         for (int i = 0; i < hv; ++i) {
@@ -1189,31 +1064,31 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       if (u < kC)
         sinv[u] = 1.f / sqrtf((spart[0][u] + spart[1][u] + spart[2][u] + spart[3][u]) / (float)kD +
                               p.rms_eps);
-      // z of chunk c+1 into the tile chunk c-1 was stored from. Only a
-      // sequence's last chunk can be partial, so chunk c-1 was full and left
+      // z of chunk k+1 into the tile chunk k-1 was stored from. Only a
+      // sequence's last chunk can be partial, so chunk k-1 was full and left
       // as thread 0's one tile store: its own wait covers the reload.
-      if (u == 0 && c >= 1 && c + 1 < nch) {
+      if (u == 0 && k >= 1 && k + 1 < nch) {
         bulk_wait_read_all();
-        load_z(c + 1);
+        load_z(k + 1);
       }
-      to |= !chain_wait(&bar_z[c & 1], (uint32_t)((c >> 1) & 1), abort_flag);
+      to |= !chain_wait(&bar_z[k & 1], (uint32_t)((k >> 1) & 1), abort_flag);
       bar_named(2, kOutThreads);
       // the gated result over z, in place (rows >= L hold finite values that
       // are never stored), 16 rows at a time: all loads, then the math, then
       // all stores
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+      for (int hf = 0; hf < 2; ++hf) {
         float zf[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) zf[e] = __bfloat162float(zb[(t0 + 16 * hh + e) * kD + j]);
+        for (int e = 0; e < 16; ++e) zf[e] = __bfloat162float(zb[(t0 + 16 * hf + e) * kD + j]);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int t = t0 + 16 * hh + e;
+          const int t = t0 + 16 * hf + e;
           const float gate = __fdividef(zf[e], 1.f + __expf(-zf[e]));
-          zf[e] = o[16 * hh + e] * sinv[t] * nwj * gate;
+          zf[e] = o[16 * hf + e] * sinv[t] * nwj * gate;
         }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) zb[(t0 + 16 * hh + e) * kD + j] = __float2bfloat16_rn(zf[e]);
+        for (int e = 0; e < 16; ++e) zb[(t0 + 16 * hf + e) * kD + j] = __float2bfloat16_rn(zf[e]);
       }
       fence_proxy_async_smem();
       bar_named(2, kOutThreads);
@@ -1245,23 +1120,23 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   // bounded wait gave up)
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kIssueWarp) {
     tc::fence_after_sync();
     tc::mma_commit_elect(&bar_fin);
     mbar_wait(&bar_fin, 0);
     tc::fence_before_sync();
   }
   if (loader) {
-    if (n_st0) mbar_wait(&bar_st[0], (n_st0 - 1) & 1);
-    if (n_st1) mbar_wait(&bar_st[1], (n_st1 - 1) & 1);
-    if (n_p) mbar_wait(&bar_p, (n_p - 1) & 1);
-    if (n_k) mbar_wait(&bar_k, (n_k - 1) & 1);
-    if (n_q) mbar_wait(&bar_q, (n_q - 1) & 1);
+    if (n_in0) mbar_wait(&bar_in[0], (n_in0 - 1) & 1);
+    if (n_in1) mbar_wait(&bar_in[1], (n_in1 - 1) & 1);
+    if (n_v) mbar_wait(&bar_v, (n_v - 1) & 1);
+    if (n_vec0) mbar_wait(&bar_vec[0], (n_vec0 - 1) & 1);
+    if (n_vec1) mbar_wait(&bar_vec[1], (n_vec1 - 1) & 1);
   }
   __syncthreads();
   if (warp == 0) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tb, 512);
+    tc::tmem_dealloc(tb, TM_COLS);
   }
 }
 
@@ -1275,8 +1150,7 @@ bool prefill_cp_supported(const PrefillArgs& p, int32_t dtype, int32_t D) {
   if (D != kD || dtype != GDN_BF16 || p.rep > kMaxRep) return false;
   if (p.T >= ((int64_t)1 << 31)) return false;  // TMA row coordinates are int32
   const CpLayout l = cp_layout(p.N, p.T, p.Hk, p.Hv);
-  if ((double)l.G * p.Hv * kD >= 2147483647.0) return false;
-  if ((double)l.G * p.Hv * 2 * kC >= 2147483647.0) return false;
+  if ((double)l.G * p.Hv * kC * 3 >= 2147483647.0) return false;
   if ((double)l.G * p.Hk * kD >= 2147483647.0) return false;
   return tc::encode_fn() != nullptr;
 }
@@ -1287,25 +1161,22 @@ cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_
   CpWork w{};
   w.cs = static_cast<int32_t*>(workspace);
   w.tw = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(workspace) + l.off_tm);
-  w.u = reinterpret_cast<float*>(static_cast<char*>(workspace) + l.off_u);
-  w.wm = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(workspace) + l.off_wm);
   w.kt = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(workspace) + l.off_kt);
   w.vec = reinterpret_cast<float*>(static_cast<char*>(workspace) + l.off_vec);
   w.G = l.G;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
-  CUtensorMap mq, mk, mv, mw, mu, mwm, mkt, mz, mo;
+  CUtensorMap mq, mk, mv, mw, mz, mkt, mo;
   memset(&mz, 0, sizeof(mz));
   memset(&mo, 0, sizeof(mo));
   const int64_t qkc = (int64_t)p.Hk * kD, vc = (int64_t)p.Hv * kD;
-  if (!tc::make_map_2d(&mq, p.q, p.T, qkc, p.q_stride, 2, bf, 64, 64, sw) ||
-      !tc::make_map_2d(&mk, p.k, p.T, qkc, p.k_stride, 2, bf, 64, 64, sw) ||
-      !tc::make_map_2d(&mv, p.v, p.T, vc, p.v_stride, 2, bf, 64, 64, sw) ||
-      !tc::make_map_2d(&mw, w.tw, l.G * p.Hv * kC, kC, kC, 2, bf, 64, 64, sw) ||
-      !tc::make_map_2d(&mu, w.u, l.G * p.Hv * kD, kC, kC, 4, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 32, 128,
-                       sw) ||
-      !tc::make_map_2d(&mwm, w.wm, l.G * p.Hv * 2 * kC, kD, kD, 2, bf, 64, 64, sw) ||
-      !tc::make_map_2d(&mkt, w.kt, l.G * p.Hk * kD, kC, kC, 2, bf, 64, 128, sw))
+  if (!tc::make_map_2d(&mq, p.q, p.T, qkc, p.q_stride, 2, bf, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::make_map_2d(&mk, p.k, p.T, qkc, p.k_stride, 2, bf, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::make_map_2d(&mv, p.v, p.T, vc, p.v_stride, 2, bf, kD, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !tc::make_map_2d(&mw, w.tw, 3 * l.G * p.Hv * kC, kC, kC, 2, bf, 64, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!tc::make_map_2d(&mkt, w.kt, l.G * p.Hk * kD, kC, kC, 2, bf, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (p.z != nullptr &&
       (!tc::make_map_2d(&mz, p.z, p.T, vc, vc, 2, bf, kD, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
@@ -1316,13 +1187,13 @@ cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(cp_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
   if (e != cudaSuccess) return e;
-  cp_prep_kernel<<<dim3((unsigned)l.G, (unsigned)p.Hk), kPrepThreads, P_SMEM, stream>>>(p, w, mq, mk, mv);
+  cp_prep_kernel<<<dim3((unsigned)l.G, (unsigned)p.Hk), kPrepThreads, P_SMEM, stream>>>(p, w, mq, mk);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(cp_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
+  e = cudaFuncSetAttribute(cp_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
-  cp_scan_kernel<<<dim3((unsigned)p.Hv, (unsigned)p.N), kScanThreads, S_SMEM, stream>>>(p, w, mq, mk, mu, mw,
-                                                                                        mwm, mkt, mz, mo);
+  cp_chain_kernel<<<dim3((unsigned)p.Hv, (unsigned)p.N), kChainAll, C_SMEM, stream>>>(p, w, mq, mk,
+                                                                                         mv, mw, mz, mkt, mo);
   return cudaGetLastError();
 }
 

@@ -59,24 +59,7 @@ __device__ __forceinline__ uint64_t sdesc_at(uint64_t base, int rows, int s) {
   return base + (uint64_t)(((s >> 2) * rows * 128 + (s & 3) * 32) >> 4);
 }
 
-// Shared-memory descriptor for an MN-major SW128 tile: 64-element atoms
-// along M (or N), `lbo` bytes apart, whose rows are consecutive K indices
-// (128 B each, 1024 B per 8-row group, 16-byte chunks XOR-swizzled by the
-// row as in the K-major form). K-step s (16 rows) starts 2048 s bytes in.
-__device__ __forceinline__ uint64_t sdesc_mn(uint32_t smem_addr, uint32_t lbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((smem_addr & 0x3FFFF) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-  d |= (uint64_t)(1024 >> 4) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
 enum : uint32_t { kF16 = 0, kBF16 = 1, kTF32 = 2 };
-// Instruction-descriptor flags: B negated (bit 14), A MN-major (bit 15),
-// B MN-major (bit 16).
-enum : uint32_t { kNegB = 1u << 14, kAMajorMN = 1u << 15, kBMajorMN = 1u << 16 };
 
 // Instruction descriptor for kind::f16 / kind::tf32 with fp32 accumulation,
 // both operands K-major: D format (bits 4-5) = F32, A/B formats in bits 7-9 /
@@ -157,17 +140,6 @@ __device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tme
       "setp.ne.b32 p, %4, 0;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(id), "r"((uint32_t)accumulate)
-      : "memory");
-}
-// mma_f16 issued by one elected lane of a converged warp.
-__device__ __forceinline__ void mma_f16_elect(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
-                                              bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e, p;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(id), "r"((uint32_t)accumulate)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {

@@ -239,11 +239,10 @@ gdn_status gdn_decode_step_slots(const gdn_dims* dims, int32_t batch, const int3
  *  - head_dim 128, bf16, Hv/Hk <= 8, a workspace: the chunk-parallel
  *    tensor-core path.
  *    Every chunk's state-free factors (the K and QK grams, (I+A)^-1 diag(beta),
- *    W = (I+A)^-1 diag(beta G) K, the masked decayed QK^T) are computed at once
- *    into the workspace, then one CTA per (V head, sequence) scans its chunks
- *    with the fp32 state as a TMEM accumulator: per chunk the corrections
- *    V^T Tb^T - S W^T and the update S <- G S + Dm'^T K; products that carry
- *    the state use bf16 hi+lo splits of their fp32 factors.
+ *    the masked decayed QK^T) are computed at once into the workspace, then
+ *    one CTA per (V head, sequence) carries the state through its chunks with
+ *    the fp32 state as a TMEM accumulator; products that carry the state use
+ *    bf16 hi+lo splits of their fp32 factors.
  *  - head_dim 128, f16/bf16, no workspace (or f16): a single-pass tensor-core
  *    kernel (one cluster of four CTAs per V head and sequence, every chunk
  *    stage in sequence; tf32 hi+lo splits for the state-carrying products).
@@ -261,16 +260,16 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int
 /*
  * Bytes of workspace gdn_prefill_chunked can use for these sizes and flags
  * (0 when no workspace path applies: head_dim != 128, io dtype not bf16,
- * more than 8 V heads per K head, or GDN_PREFILL_CUDA_CORES): per 64-token
- * chunk slot ((T + 63 N) / 64 of them) 73 KB per V head and 16 KB per K head,
- * plus 4 (N + 1) bytes rounded up to 1 KB. Writes the size to *bytes; GDN_ERR_INVALID_ARG /
+ * more than 8 V heads per K head, or GDN_PREFILL_CUDA_CORES): per 64-token chunk slot ((T + 63 N) / 64 of
+ * them) 25 KB per V head and 16 KB per K head, plus 4 (N + 1) bytes rounded
+ * up to 1 KB. Writes the size to *bytes; GDN_ERR_INVALID_ARG /
  * GDN_ERR_EXTENT for invalid dims or sizes.
  */
 gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
                                       int64_t total_tokens, int32_t flags, int64_t* bytes);
 
 /* Size of the static device scratch behind gdn_prefill_chunked_static. */
-#define GDN_STATIC_SCRATCH_BYTES (192u << 20)
+#define GDN_STATIC_SCRATCH_BYTES (96u << 20)
 
 /*
  * gdn_prefill_chunked without a workspace argument that still takes the
@@ -283,7 +282,7 @@ gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
  * Arguments, results and errors are those of gdn_prefill_chunked, plus:
  *  - GDN_ERR_EXTENT, checked first, when gdn_prefill_workspace_size for
  *    these sizes exceeds GDN_STATIC_SCRATCH_BYTES (e.g. more than about
- *    4,700 tokens in one sequence at Hk=16, Hv=32; 2,400 at Hk=16, Hv=64);
+ *    5,900 tokens at Hk=16, Hv=32; 3,400 at Hk=16, Hv=64);
  *  - where no workspace path applies (f16, head_dim != 128,
  *    GDN_PREFILL_CUDA_CORES) it is gdn_prefill_chunked with workspace NULL.
  *

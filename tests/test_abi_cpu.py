@@ -52,8 +52,8 @@ def test_status_strings_and_version(lib):
 
 def test_prefill_workspace_size(lib):
     d = gdn.dims(16, 32, 128, io_dtype=torch.bfloat16)
-    # (T + 63 N) / 64 chunk slots x (Hv x 73 KB + Hk x 16 KB), after the 1 KB index
-    per_slot = 32 * 74752 + 16 * 16384
+    # (T + 63 N) / 64 chunk slots x (Hv x 25 KB + Hk x 16 KB), after the 1 KB index
+    per_slot = 32 * 25600 + 16 * 16384
     assert gdn.gdn_prefill_workspace_size(d, 1, 4096) == 1024 + 64 * per_slot
     assert gdn.gdn_prefill_workspace_size(d, 8, 34482) == 1024 + (34482 + 63 * 8) // 64 * per_slot
     assert gdn.gdn_prefill_workspace_size(d, 1, 0) == 0

@@ -229,9 +229,8 @@ def test_eight_v_heads_per_k_head(mp):
 def test_workspace_size_and_too_small_workspace():
     d = gdn.dims(16, 32, 128, io_dtype=torch.bfloat16)
     n = gdn.gdn_prefill_workspace_size(d, 1, 4096)
-    # 64 chunk slots x (32 V heads x 73 KB (P, U^T fp32, W hi, W lo, scale
-    # vectors) + 16 K heads x 16 KB (k transposed)) + the 1 KB index
-    assert n == 1024 + 64 * (32 * (8192 + 32768 + 2 * 16384 + 1024) + 16 * 16384)
+    # 64 chunk slots x (32 V heads x 25 KB + 16 K heads x 16 KB) + the 1 KB index
+    assert n == 1024 + 64 * (32 * (3 * 8192 + 1024) + 16 * 16384)
     assert gdn.gdn_prefill_workspace_size(d, 1, 4096, gdn.GDN_PREFILL_CUDA_CORES) == 0
     assert gdn.gdn_prefill_workspace_size(gdn.dims(16, 32, 128, io_dtype=torch.float16), 1,
                                           4096) == 0
