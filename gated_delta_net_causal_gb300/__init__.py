@@ -25,6 +25,7 @@ GDN_MAP_GROUPED, GDN_MAP_TILED = 0, 1
 GDN_DECAY_LOG_RATE, GDN_DECAY_NEGATIVE_RATE = 0, 1
 GDN_F16, GDN_BF16, GDN_F32 = 0, 1, 2
 GDN_QK_PRENORMALIZED, GDN_GATES_PRECOMPUTED, GDN_PREFILL_CUDA_CORES = 1, 2, 4
+GDN_PREFILL_CARRY_WHOLE, GDN_PREFILL_CARRY_SLICED = 8, 16
 
 _TORCH_TO_GDN = {torch.float16: GDN_F16, torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}
 _GDN_TO_TORCH = {v: k for k, v in _TORCH_TO_GDN.items()}
@@ -327,7 +328,7 @@ def gdn_prefill_chunked(d: GdnDims, cu_seqlens, q, k, v, a, b, decay_param, dt_b
     return core_out, out
 
 
-GDN_STATIC_SCRATCH_BYTES = 96 << 20
+GDN_STATIC_SCRATCH_BYTES = 160 << 20
 
 
 def gdn_prefill_chunked_static(d: GdnDims, cu_seqlens, q, k, v, a, b, decay_param, dt_bias,
@@ -383,4 +384,5 @@ __all__ = ["GdnDims", "GdnError", "dims", "library", "status_string", "gdn_conv_
            "gdn_prefill_chunked_static", "GDN_STATIC_SCRATCH_BYTES", "gdn_gated_rmsnorm", "gdn_device_error",
            "gdn_qkv_features", "gdn_version", "GDN_MAP_GROUPED", "GDN_MAP_TILED",
            "GDN_DECAY_LOG_RATE", "GDN_DECAY_NEGATIVE_RATE", "GDN_F16", "GDN_BF16", "GDN_F32",
-           "GDN_QK_PRENORMALIZED", "GDN_GATES_PRECOMPUTED", "GDN_PREFILL_CUDA_CORES", "LIB_PATH"]
+           "GDN_QK_PRENORMALIZED", "GDN_GATES_PRECOMPUTED", "GDN_PREFILL_CUDA_CORES",
+           "GDN_PREFILL_CARRY_WHOLE", "GDN_PREFILL_CARRY_SLICED", "LIB_PATH"]

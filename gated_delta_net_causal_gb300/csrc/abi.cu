@@ -148,6 +148,15 @@ gdn_status decode_impl(const gdn_dims* dims, int32_t batch, int32_t tokens, cons
 
 }  // namespace
 
+// gdn_prefill_chunked flags: known bits only, and not both carry choices
+static bool prefill_flags_valid(int32_t flags) {
+  constexpr int32_t known = GDN_QK_PRENORMALIZED | GDN_GATES_PRECOMPUTED | GDN_PREFILL_CUDA_CORES |
+                            GDN_PREFILL_CARRY_WHOLE | GDN_PREFILL_CARRY_SLICED;
+  if ((flags & ~known) != 0) return false;
+  return (flags & (GDN_PREFILL_CARRY_WHOLE | GDN_PREFILL_CARRY_SLICED)) !=
+         (GDN_PREFILL_CARRY_WHOLE | GDN_PREFILL_CARRY_SLICED);
+}
+
 extern "C" {
 
 const char* gdn_status_string(int32_t status) {
@@ -251,8 +260,7 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int
   if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
   if (num_seqs == 0 && total_tokens > 0) return GDN_ERR_INVALID_ARG;
   if (num_seqs > kMaxGridY) return GDN_ERR_EXTENT;
-  if ((flags & ~(GDN_QK_PRENORMALIZED | GDN_GATES_PRECOMPUTED | GDN_PREFILL_CUDA_CORES)) != 0)
-    return GDN_ERR_INVALID_ARG;
+  if (!prefill_flags_valid(flags)) return GDN_ERR_INVALID_ARG;
   if (num_seqs == 0) return GDN_OK;
   const bool pregate = (flags & GDN_GATES_PRECOMPUTED) != 0;
   if (!cu_seqlens || !state) return GDN_ERR_INVALID_ARG;
@@ -355,16 +363,16 @@ gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
   if (st != GDN_OK) return st;
   if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
   if (num_seqs > kMaxGridY) return GDN_ERR_EXTENT;
-  if ((flags & ~(GDN_QK_PRENORMALIZED | GDN_GATES_PRECOMPUTED | GDN_PREFILL_CUDA_CORES)) != 0)
-    return GDN_ERR_INVALID_ARG;
+  if (!prefill_flags_valid(flags)) return GDN_ERR_INVALID_ARG;
   if (dims->head_dim != 128 || dims->io_dtype != GDN_BF16 || (flags & GDN_PREFILL_CUDA_CORES) ||
       dims->n_v_heads > 8 * dims->n_k_heads || num_seqs == 0 || total_tokens == 0)
     return GDN_OK;
   // (T + 63 N) / 64 chunk slots of 25 KB per V head and 16 KB per K head,
-  // plus the chunk index
+  // plus the chunk index, plus T Hv 512 bytes for few (V head, sequence)
+  // pairs (bounded here by 512 bytes per chunk-slot token and V head)
   int64_t tmp = 0;
   if (!mul_ok(total_tokens + 63 * (int64_t)num_seqs,
-              (int64_t)dims->n_v_heads * 400 + (int64_t)dims->n_k_heads * 256 + 400, &tmp))
+              (int64_t)dims->n_v_heads * 912 + (int64_t)dims->n_k_heads * 256 + 400, &tmp))
     return GDN_ERR_EXTENT;
   *bytes = gdn::prefill_cp_workspace_bytes(num_seqs, total_tokens, dims->n_k_heads,
                                            dims->n_v_heads);

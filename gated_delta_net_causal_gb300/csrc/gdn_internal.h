@@ -92,6 +92,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs& p, int32_t dtype, cudaStream_t 
 // chunk-parallel tensor-core prefill (head_dim 128, bf16) over a workspace
 int64_t prefill_cp_workspace_bytes(int32_t N, int64_t T, int32_t Hk, int32_t Hv);
 bool prefill_cp_supported(const PrefillArgs& p, int32_t dtype, int32_t D);
+// whether launch_prefill_cp carries the state with the sliced kernel
+bool prefill_cp_sliced(const PrefillArgs& p);
 cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_t stream);
 
 // Device error words, one per kernel translation unit.

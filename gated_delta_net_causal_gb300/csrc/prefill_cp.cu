@@ -48,6 +48,9 @@ constexpr int kCarryThreads = 256;  // warps 0-7: the state carry (two threads p
 constexpr int kChainThreads = 512;  // warps 8-15: output and gated norm
 constexpr int kAStride = kC + 1;    // padded row pitch of the fp32 A matrix
 constexpr int kMaxRep = 8;          // V heads per K head on this path
+// (V head, sequence) pairs up to which the sliced carry (four CTAs each) is
+// chosen, and the workspace holds an fp32 core output for its separate norm
+constexpr int64_t kSlMaxChains = 64;
 
 // ---------------------------------------------------------------- workspace
 
@@ -61,7 +64,7 @@ struct CpWork {
 
 struct CpLayout {
   int64_t G;
-  size_t off_tm, off_kt, off_vec, total;
+  size_t off_tm, off_kt, off_vec, off_o, total;  // off_o 0: no core-output region
 };
 
 CpLayout cp_layout(int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
@@ -72,6 +75,12 @@ CpLayout cp_layout(int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
   l.off_kt = l.off_tm + (size_t)3 * l.G * Hv * kC * kC * 2;
   l.off_vec = l.off_kt + (size_t)l.G * Hk * kD * kC * 2;
   l.total = l.off_vec + (size_t)l.G * Hv * 4 * kC * 4;
+  // few (V head, sequence) pairs: [T][Hv][128] fp32 for the sliced carry's
+  // core output, normalised by a separate pass when no core_out is given
+  if (l.G > 0 && (int64_t)Hv * N <= kSlMaxChains) {
+    l.off_o = (l.total + 255) / 256 * 256;
+    l.total = l.off_o + (size_t)T * Hv * kD * 4;
+  }
   return l;
 }
 
@@ -1140,6 +1149,665 @@ __global__ void __launch_bounds__(kChainAll, 1)
   }
 }
 
+
+// ---------------------------------------------------------- sliced carry
+//
+// The carry with the 128 value rows of each (V head, sequence) split over a
+// cluster of four CTAs, 32 rows j each. Given a chunk's state-free factors,
+// row j of the state evolves on its own, so the CTAs share nothing but the
+// gated RMSNorm's per-token sums of squares. Against cp_chain_kernel the
+// orientation is turned around: the MMA M dimension runs over tokens (or key
+// columns i) and this CTA's 32 value rows are N, so the state slice S_J is a
+// B operand in shared memory (bf16 hi and lo, [32 j][128 i]) and its fp32
+// copy lives transposed in TMEM (lane i, column j). Per chunk:
+//   (1) [KS | QS] (lane t, column j) = [k; q] (S_hi + S_lo)_J^T
+//   (2) R = V_J - diag(ak) KS -> hi/lo B tiles [64 s][32 j] (rows t >= L zero)
+//   (3) [X | Y] = [Tb hi; Tb lo] (R_hi + R_lo): Dm = X + Y, X in lanes 0-63,
+//       Y in lanes 64-127 (no exchange between lane quadrants)
+//   (4) (dk X) hi/lo, (dk Y) hi, X hi, Y hi -> B tiles
+//   (5) S_J^T += K^T (dk Dm) on the accumulator pre-scaled by G_{L-1} (three
+//       partial accumulators, one per B tile, summed by (6));
+//       P (X_hi + Y_hi) into lanes 64-127 of its own columns (A is a
+//       128-row window whose rows 64-127 are P; the first half is unused)
+//   (6) the new S_J hi/lo tiles and the accumulator rescaled
+// and O = gq QS + P Dm, then the gated RMSNorm with the sums of squares of
+// each token's row exchanged over the cluster. Each phase is a quarter of
+// the per-thread work of the unsliced carry, which is latency-bound at the
+// sizes where there are few (V head, sequence) pairs to spread over the SMs.
+
+constexpr int kSl = 32;             // value rows per CTA
+constexpr int kSlCta = kD / kSl;    // CTAs per cluster
+constexpr int kSlThreads = 384;     // warps 0-7 carry, 8 MMA, 9 loads, 10-11 output
+constexpr int kSlIssueWarp = 8;
+constexpr int kSlLoadWarp = 9;
+constexpr int kSlOutThreads = 64;   // warps 10-11: one token row t each
+
+// shared memory (byte offsets from a 1024-aligned base); the per-chunk
+// inputs are double-buffered by chunk parity b
+constexpr uint32_t L_KQ = 0;             // bf16 [2][128 rows: k t | q t][128 i] SW128 (TMA)
+constexpr uint32_t L_TB = 65536;         // bf16 [2][128 rows: Tb hi | Tb lo][64 s] SW128 (TMA)
+constexpr uint32_t L_KT = 98304;         // bf16 [2][128 i][64 t] SW128 (TMA)
+constexpr uint32_t L_P = 131072;         // bf16 [2][64 t][64 s] SW128 (TMA)
+constexpr uint32_t L_V = 147456;         // bf16 [2][64 t][32 j] row-major (TMA)
+constexpr uint32_t L_Z = 155648;         // bf16 [2][64 t][32 j] row-major: z (TMA)
+constexpr uint32_t L_VEC = 163840;       // fp32 [2][4][64]: ak, dk, gq, {G_{L-1}}
+constexpr uint32_t L_SH = 165888;        // bf16 [128 i][32 j] MN-major SW64: S hi
+constexpr uint32_t L_SL = L_SH + 8192;   // S lo
+constexpr uint32_t L_RH = L_SL + 8192;   // bf16 [64 s][32 j] MN-major SW64: R hi
+constexpr uint32_t L_RL = L_RH + 4096;   // R lo
+constexpr uint32_t L_DXH = L_RL + 4096;  // (dk X) hi
+constexpr uint32_t L_DXL = L_DXH + 4096; // (dk X) lo
+constexpr uint32_t L_DYH = L_DXL + 4096; // (dk Y) hi
+constexpr uint32_t L_XH = L_DYH + 4096;  // X hi
+constexpr uint32_t L_YH = L_XH + 4096;   // Y hi
+constexpr uint32_t L_O = L_YH + 4096;    // bf16 [2][64 t][32 j] row-major: the gated output (TMA store)
+constexpr uint32_t L_SMEM = L_O + 8192 + 1024;
+static_assert(L_SH % 1024 == 0 && L_RH % 1024 == 0 && L_YH % 1024 == 0 && L_VEC + 2048 <= L_SH,
+              "tile alignment");
+static_assert(L_P >= 8192 && L_SMEM <= 232448, "P window and shared memory budget");
+constexpr uint32_t kSlInBytes = 32768 + 16384 + 16384 + 8192;  // KQ, Tb, K^T, P
+constexpr uint32_t kSlVBytes = 4096 + 1024;                    // V_J, vectors
+constexpr uint32_t kNormBytes = (kSlCta - 1) * kC * 4;          // the peers' sums of squares
+
+// TMEM columns (lane = MMA row). Each product of a hi/lo pair of B tiles is
+// one MMA over both (N = 64 or 96, the tiles adjacent in shared memory), its
+// parts in adjacent 32-column groups that the reader adds.
+// The two that the output warps read are double-buffered by chunk parity b,
+// so that the output of chunk k may finish while chunk k + 1 runs.
+constexpr uint32_t T_KQS = 0;    // fp32 [2][KS (lanes 0-63) | QS (64-127)] x {S hi, S lo} (2 x 64)
+constexpr uint32_t T_XY = 128;   // fp32 [X | Y] x {R hi, R lo} (64)
+constexpr uint32_t T_S = 192;    // fp32 S_J^T (lane i) as three partial accumulators (96)
+constexpr uint32_t T_PD = 288;   // fp32 [2] P Dm in lanes 64-127, x {X hi, Y hi} (2 x 64)
+constexpr uint32_t T_SL_COLS = 512;
+
+// The B operands of the sliced carry are MN-major with 64-byte swizzling:
+// value row j (N, 32 of them) is contiguous, K index k picks a 64-byte row,
+// eight K rows form a 512-byte atom, and the 16-byte group c of value rows
+// 8c..8c+7 sits at group c ^ ((k % 8) / 2) of its row. A thread that holds
+// 16 value rows at one K index stores them as two 16-byte words per tile.
+__device__ __forceinline__ uint32_t mn64_group(int k, int c) {
+  return (uint32_t)((k >> 3) * 512 + (k & 7) * 64 + ((c ^ ((k & 7) >> 1)) << 4));
+}
+// Descriptor of such tiles side by side along N, `lbo` bytes apart.
+__device__ __forceinline__ uint64_t sdesc_mn64(uint32_t smem_addr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)(lbo >> 4) << 16;   // leading byte offset: between 32-row MN atoms
+  d |= (uint64_t)(512 >> 4) << 32;   // stride byte offset: between 8-row K groups
+  d |= (uint64_t)1 << 46;            // descriptor version
+  d |= (uint64_t)4 << 61;            // SWIZZLE_64B
+  return d;
+}
+// k-step s (16 K rows) of such a tile
+__device__ __forceinline__ uint64_t sdesc_mn64_at(uint64_t base, int s) {
+  return base + (uint64_t)((s * 1024) >> 4);
+}
+// x (value rows jl..jl+15 at K index k) rounded to bf16 into one tile
+__device__ __forceinline__ void put16(unsigned char* sm, uint32_t tile, int k, int jl, const float* x) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const float* y = x + 8 * c;
+    *reinterpret_cast<uint4*>(sm + tile + mn64_group(k, (jl >> 3) + c)) =
+        make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+  }
+}
+// x split into bf16 hi parts (tile th) and the rounded remainders (tile tl)
+__device__ __forceinline__ void put16_hilo(unsigned char* sm, uint32_t th, uint32_t tl, int k, int jl,
+                                           const float* x) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint4 hi, lo;
+    split8(x + 8 * c, hi, lo);
+    const uint32_t o = mn64_group(k, (jl >> 3) + c);
+    *reinterpret_cast<uint4*>(sm + th + o) = hi;
+    *reinterpret_cast<uint4*>(sm + tl + o) = lo;
+  }
+}
+// Bounded wait for the roles off the critical path (output, loads): between
+// polls the thread sleeps, so that it takes no issue slots from the carry
+// warps that share its SM sub-partition. `abort_flag` may be null (the wait
+// then ends only on completion or the time limit).
+__device__ __noinline__ bool wait_sleepy_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    __nanosleep(100);
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      record_device_error(GDN_ERR_TIMEOUT);
+      if (abort_flag != nullptr) *abort_flag = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool wait_sleepy(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_try_wait(bar, parity) || wait_sleepy_slow(bar, parity, abort_flag);
+}
+
+// A warp hands shared-memory (and TMEM) operands it wrote to the MMA warp.
+__device__ __forceinline__ void operands_done(uint64_t* bar, int lane) {
+  fence_proxy_async_smem();
+  tc::tmem_wait_st();
+  tc::fence_before_sync();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+__global__ void __cluster_dims__(kSlCta, 1, 1) __launch_bounds__(kSlThreads, 1)
+    cp_slice_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_z,
+                    const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_o) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t bar_in[2], bar_v[2], bar_z[2], bar_nm[2], bar_free[2], bar_q[2];
+  __shared__ __align__(8) uint64_t bar_m1, bar_m3, bar_m5, bar_oe[2], bar_fin;
+  __shared__ __align__(8) uint64_t bar_s[4], bar_r[2], bar_d[4];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ float snorm[2][kSlCta][kC];  // per token: the four slices' sums of squares
+  __shared__ float snw[kSl];              // this slice's gated-norm weights
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x / kSlCta, n = blockIdx.y;
+  const uint32_t rank = cluster_ctarank();
+  const int j0 = kSl * (int)rank;
+  const int kh = k_head_of(p.map, h, p.Hk, p.rep);
+  const int64_t kb = w.cs[n], ke = w.cs[n + 1];
+  // (both exits are taken by every CTA of the cluster, before any access to
+  // another CTA's shared memory)
+  if (ke <= kb) return;  // empty sequence: the state is left as it is
+  if (ke > w.G) {
+    if (tid == 0 && rank == 0) record_device_error(GDN_ERR_INVALID_ARG);
+    return;
+  }
+  const int nch = (int)(ke - kb);
+  int64_t seq_s, seq_e;
+  seq_range(p, n, seq_s, seq_e);
+  const bool fused = p.z != nullptr;
+  const size_t HvG = (size_t)w.G * p.Hv;
+
+  if (warp == 0) {
+    tc::tmem_alloc(&s_tmem, T_SL_COLS);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_in[b], 1);
+      mbar_init(&bar_v[b], 1);
+      mbar_init(&bar_z[b], 1);
+      mbar_init(&bar_nm[b], 1);
+      mbar_init(&bar_q[b], 1);
+      mbar_init(&bar_free[b], 1);
+      mbar_init(&bar_r[b], 2);
+    }
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&bar_s[q], 2);
+      mbar_init(&bar_d[q], 2);
+    }
+    mbar_init(&bar_m1, 1);
+    mbar_init(&bar_m3, 1);
+    mbar_init(&bar_m5, 1);
+    mbar_init(&bar_fin, 1);
+    mbar_init(&bar_oe[0], 2);
+    mbar_init(&bar_oe[1], 2);
+    s_abort = 0;
+    fence_mbar_init();
+    if (fused) {
+      for (int e = 0; e < kSl; ++e) snw[e] = p.norm_w[j0 + e];
+      // the norm exchange of chunks 0 and 1 (re-armed after each use): the
+      // three peers' 64 sums each
+      mbar_arrive_expect_tx(&bar_nm[0], kNormBytes);
+      mbar_arrive_expect_tx(&bar_nm[1], kNormBytes);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  // every CTA's barriers exist before a peer can signal them
+  cluster_arrive_release();
+  cluster_wait_acquire();
+  tc::fence_after_sync();
+  const uint32_t tb = s_tmem;
+  volatile int* abort_flag = &s_abort;
+  auto chunk_c0 = [&](int k) { return seq_s + (int64_t)kC * k; };
+  auto slot_of = [&](int k) { return (size_t)(kb + k) * p.Hv + h; };
+
+  uint32_t n_in0 = 0, n_in1 = 0;  // loads issued per buffer (the exit path waits for them)
+  const bool loader = warp == kSlLoadWarp && lane == 0;
+
+  if (loader) {
+    // chunk k's inputs into buffer k & 1; chunk k + 2 follows once the last
+    // MMA reading chunk k's buffer has completed (bar_free)
+    auto load = [&](int k) {
+      const int b = k & 1;
+      if (b) ++n_in1; else ++n_in0;
+      uint64_t* bi = &bar_in[b];
+      uint64_t* bv = &bar_v[b];
+      mbar_arrive_expect_tx(bi, kSlInBytes);
+      mbar_arrive_expect_tx(bv, kSlVBytes);
+      const int y = (int)chunk_c0(k);
+      unsigned char* kq = sm + L_KQ + b * 32768;
+      tc::tma_load_2d(kq, &tm_k, kh * kD, y, bi);
+      tc::tma_load_2d(kq + 16384, &tm_k, kh * kD + 64, y, bi);
+      tc::tma_load_2d(kq + 8192, &tm_q, kh * kD, y, bi);
+      tc::tma_load_2d(kq + 24576, &tm_q, kh * kD + 64, y, bi);
+      const size_t slot = slot_of(k);
+      tc::tma_load_2d(sm + L_TB + b * 16384, &tm_w, 0, (int)(slot * kC), bi);
+      tc::tma_load_2d(sm + L_TB + b * 16384 + 8192, &tm_w, 0, (int)((HvG + slot) * kC), bi);
+      tc::tma_load_2d(sm + L_P + b * 8192, &tm_w, 0, (int)((2 * HvG + slot) * kC), bi);
+      tc::tma_load_2d(sm + L_KT + b * 16384, &tm_kt, 0, (int)(((kb + k) * p.Hk + kh) * kD), bi);
+      tc::tma_load_2d(sm + L_V + b * 4096, &tm_v, h * kD + j0, y, bv);
+      bulk_load(sm + L_VEC + b * 1024, w.vec + slot * (4 * kC), 1024u, bv);
+    };
+    load(0);
+    if (nch > 1) load(1);
+    for (int k = 0; k + 2 < nch; ++k) {
+      if (!wait_sleepy(&bar_free[k & 1], (uint32_t)((k >> 1) & 1), abort_flag)) break;
+      load(k + 2);
+    }
+  } else if (warp == kSlIssueWarp) {
+    // A K-major (TMA tiles), B MN-major (bit 16): [S hi | S lo], [R hi | R lo],
+    // [X hi | Y hi] (N = 64) and [(dk X) hi | (dk X) lo | (dk Y) hi] (N = 96)
+    const uint32_t id64 = tc::idesc(tc::kBF16, 128, 2 * kSl) | (1u << 16);
+    const uint32_t id96 = tc::idesc(tc::kBF16, 128, 3 * kSl) | (1u << 16);
+    const uint64_t d_kq = tc::sdesc_sw128(smem_u32(sm + L_KQ)), d_tb = tc::sdesc_sw128(smem_u32(sm + L_TB)),
+                   d_kt = tc::sdesc_sw128(smem_u32(sm + L_KT)),
+                   d_pw = tc::sdesc_sw128(smem_u32(sm + L_P - 8192)),
+                   d_s = sdesc_mn64(smem_u32(sm + L_SH), L_SL - L_SH),
+                   d_r = sdesc_mn64(smem_u32(sm + L_RH), L_RL - L_RH),
+                   d_d = sdesc_mn64(smem_u32(sm + L_DXH), L_DXL - L_DXH),
+                   d_xy = sdesc_mn64(smem_u32(sm + L_XH), L_YH - L_XH);
+    for (int k = 0; k < nch; ++k) {
+      const uint32_t ph = (uint32_t)(k & 1);
+      const int b = k & 1;
+      bool ok = chain_wait(&bar_in[b], (uint32_t)((k >> 1) & 1), abort_flag);
+      // the output columns of buffer b are free once chunk k - 2's are read
+      if (ok && k >= 2) ok = chain_wait(&bar_oe[b], (uint32_t)(((k - 2) >> 1) & 1), abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const uint32_t t_kqs = tb + T_KQS + 64 * b, t_pd = tb + T_PD + 64 * b;
+      const uint64_t akq = d_kq + (uint64_t)((b * 32768) >> 4), atb = d_tb + (uint64_t)((b * 16384) >> 4),
+                     akt = d_kt + (uint64_t)((b * 16384) >> 4), apw = d_pw + (uint64_t)((b * 8192) >> 4);
+      // (1) quadrant q of the state copies holds K = i of k-steps 2q, 2q + 1
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        ok = __all_sync(0xffffffffu, chain_wait(&bar_s[q], ph, abort_flag));
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int ks = 2 * q + e;
+          tc::mma_f16_elect(t_kqs, tc::sdesc_at(akq, 128, ks), sdesc_mn64_at(d_s, ks), id64, ks > 0);
+        }
+      }
+      if (!ok) break;
+      tc::mma_commit_elect(&bar_m1);    // the carry's (2)
+      tc::mma_commit_elect(&bar_q[b]);  // the output's QS (a barrier per buffer: the output
+                                        // warps may be a chunk behind)
+      // (3) R rows t of quadrant q (0, 1) are K = s of k-steps 2q, 2q + 1
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        ok = __all_sync(0xffffffffu, chain_wait(&bar_r[q], ph, abort_flag));
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int ks = 2 * q + e;
+          tc::mma_f16_elect(tb + T_XY, tc::sdesc_at(atb, 128, ks), sdesc_mn64_at(d_r, ks), id64, ks > 0);
+        }
+      }
+      if (!ok) break;
+      tc::mma_commit_elect(&bar_m3);
+      // (5) rows t = 32h.. of dk X come from quadrant h, of dk Y from
+      // quadrant 2 + h: k-steps 2h, 2h + 1 once both are in
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        ok = __all_sync(0xffffffffu, chain_wait(&bar_d[hh], ph, abort_flag) &&
+                                         chain_wait(&bar_d[2 + hh], ph, abort_flag));
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int ks = 2 * hh + e;
+          tc::mma_f16_elect(tb + T_S, tc::sdesc_at(akt, 128, ks), sdesc_mn64_at(d_d, ks), id96, true);
+        }
+      }
+      if (!ok) break;
+      tc::mma_commit_elect(&bar_m5);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc::mma_f16_elect(t_pd, tc::sdesc_at(apw, 128, ks), sdesc_mn64_at(d_xy, ks), id64, ks > 0);
+      tc::mma_commit_elect(&bar_free[b]);  // the loader's reuse of buffer b, the output's P Dm
+    }
+  } else if (warp < 8) {
+    // ============ carry: warp (q, hf) = (warp % 4, warp / 4) reads TMEM lanes
+    // 32q.. and handles this CTA's value rows jl = 16 hf .. 16 hf + 15
+    const int q = warp & 3, jl = 16 * (warp >> 2);
+    const uint32_t tl = tb + ((uint32_t)(32 * q) << 16);
+    const int i = 32 * q + lane;  // key column (state lane)
+    float* gS = p.state + (((size_t)n * p.Hv + h) * kD + j0 + jl) * kD + i;  // row e at gS[e * kD]
+
+    // the state's 16 values -> hi/lo B tiles, then the accumulator: the
+    // first partial holds the state rescaled by gl, the other two restart
+    // from zero
+    auto store_state = [&](float (&v)[16], float gl) {
+      put16_hilo(sm, L_SH, L_SL, i, jl, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] *= gl;
+      tc::tmem_st16(tl + T_S + jl, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = 0.f;
+      tc::tmem_st16(tl + T_S + kSl + jl, v);
+      tc::tmem_st16(tl + T_S + 2 * kSl + jl, v);
+      operands_done(&bar_s[q], lane);
+    };
+
+    bool to = !chain_wait(&bar_v[0], 0, abort_flag);
+    to = __any_sync(0xffffffffu, to);
+    if (!to) {
+      float v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = gS[(size_t)e * kD];
+      store_state(v, reinterpret_cast<const float*>(sm + L_VEC)[3 * kC]);
+    }
+    for (int k = 0; k < nch && !to; ++k) {
+      const uint32_t ph = (uint32_t)(k & 1);
+      const int b = k & 1;
+      const int64_t c0 = chunk_c0(k);
+      const int L = (int)((seq_e - c0) < kC ? (seq_e - c0) : kC);
+      const float* vec = reinterpret_cast<const float*>(sm + L_VEC + b * 1024);
+      const bool more = k + 1 < nch;
+      to = !chain_wait(&bar_v[b], (uint32_t)((k >> 1) & 1), abort_flag);
+      if (q < 2) {
+        // (2) R rows t = 32q + lane (V and the vectors landed long before
+        // (1) completes: checked first)
+        to = to || !chain_wait(&bar_m1, ph, abort_flag);
+        if (__any_sync(0xffffffffu, to)) break;
+        tc::fence_after_sync();
+        const int t = i;
+        float ks[16], ks2[16];
+        tc::tmem_ld16(tl + T_KQS + 64 * b + jl, ks);
+        tc::tmem_ld16(tl + T_KQS + 64 * b + kSl + jl, ks2);
+        const uint4* vp = reinterpret_cast<const uint4*>(sm + L_V + b * 4096 + t * (kSl * 2) + jl * 2);
+        const uint4 va = vp[0], vb = vp[1];
+        const float ak = vec[t];
+        tc::tmem_wait_ld();
+        const uint32_t vw[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+        const bool live = t < L;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ks[e] += ks2[e];
+        float r[16];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&vw[m]);
+          r[2 * m] = live ? __low2float(v2) - ak * ks[2 * m] : 0.f;
+          r[2 * m + 1] = live ? __high2float(v2) - ak * ks[2 * m + 1] : 0.f;
+        }
+        put16_hilo(sm, L_RH, L_RL, t, jl, r);
+        operands_done(&bar_r[q], lane);
+      }
+      // (4) X (quadrants 0, 1) or Y (2, 3) of rows t = 32 (q % 2) + lane
+      to = to || !chain_wait(&bar_m3, ph, abort_flag);
+      if (__any_sync(0xffffffffu, to)) break;
+      tc::fence_after_sync();
+      {
+        const int t = 32 * (q & 1) + lane;
+        float x[16], x2[16];
+        tc::tmem_ld16(tl + T_XY + jl, x);
+        tc::tmem_ld16(tl + T_XY + kSl + jl, x2);
+        const float dk = vec[kC + t];
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] += x2[e];
+        put16(sm, q < 2 ? L_XH : L_YH, t, jl, x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] *= dk;
+        if (q < 2)
+          put16_hilo(sm, L_DXH, L_DXL, t, jl, x);
+        else
+          put16(sm, L_DYH, t, jl, x);
+        operands_done(&bar_d[q], lane);
+      }
+      // (6) the new state: operand copies and the next chunk's decay; after
+      // the last chunk, back to global memory
+      to = !chain_wait(&bar_m5, ph, abort_flag);
+      if (more) to = to || !chain_wait(&bar_v[(k + 1) & 1], (uint32_t)(((k + 1) >> 1) & 1), abort_flag);
+      if (__any_sync(0xffffffffu, to)) break;
+      tc::fence_after_sync();
+      float v[16], v1[16], v2[16];
+      tc::tmem_ld16(tl + T_S + jl, v);
+      tc::tmem_ld16(tl + T_S + kSl + jl, v1);
+      tc::tmem_ld16(tl + T_S + 2 * kSl + jl, v2);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] += v1[e] + v2[e];
+      if (!more) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) gS[(size_t)e * kD] = v[e];
+      } else {
+        store_state(v, reinterpret_cast<const float*>(sm + L_VEC + ((k + 1) & 1) * 1024)[3 * kC]);
+      }
+    }
+    tc::tmem_wait_st();
+    tc::fence_before_sync();
+  } else if (warp >= 10) {
+    // ============ output: thread u owns token row t = u (TMEM lane 64 + t)
+    // and this CTA's 32 columns j. QS is read once (1) completes and P Dm
+    // once its MMAs do; then TMEM is released to the next chunk but one. With
+    // the fused norm each row's sum of squares goes to all four CTAs
+    // (distributed shared memory), z arrives by TMA two chunks ahead into a
+    // row-major tile (two, by chunk parity), and the gated result leaves from
+    // a staging tile of its own (two), a full chunk as one tile store.
+    const int u = tid - 10 * 32, t = u;
+    const uint32_t tl = tb + ((uint32_t)(32 * (warp & 3)) << 16);
+    uint32_t n_z0 = 0, n_z1 = 0;
+    bool stored = false;
+    auto load_z = [&](int k) {
+      if (k & 1) ++n_z1; else ++n_z0;
+      mbar_arrive_expect_tx(&bar_z[k & 1], 4096u);
+      tc::tma_load_2d(sm + L_Z + (k & 1) * 4096, &tm_z, h * kD + j0, (int)chunk_c0(k), &bar_z[k & 1]);
+    };
+    if (fused && u == 0) {
+      load_z(0);
+      if (nch > 1) load_z(1);
+    }
+    // A bounded wait that gave up stops the stores but, with the fused norm,
+    // not the exchange: every CTA sends its sums for every chunk and takes
+    // its peers' before it goes on, so no copy into a CTA's shared memory is
+    // in flight when it exits (unless a peer stops answering altogether, when
+    // the time limit ends the wait).
+    bool to = false;  // a bounded wait gave up (agreed on at the chunk's barrier)
+    for (int k = 0; k < nch; ++k) {
+      const int b = k & 1;
+      const int64_t c0 = chunk_c0(k);
+      const int L = (int)((seq_e - c0) < kC ? (seq_e - c0) : kC);
+      const float gq = __ldg(w.vec + slot_of(k) * (4 * kC) + 2 * kC + t);
+      // QS (its S hi and S lo parts summed) once (1) completes
+      float a[32], o[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = 0.f;
+      to |= !wait_sleepy(&bar_q[b], (uint32_t)((k >> 1) & 1), abort_flag);
+      if (!__any_sync(0xffffffffu, to)) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float x[16], y[16];
+          tc::tmem_ld16(tl + T_KQS + 64 * b + 16 * hh, x);
+          tc::tmem_ld16(tl + T_KQS + 64 * b + kSl + 16 * hh, y);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) a[16 * hh + e] = x[e] + y[e];
+        }
+      }
+      // then gq QS + P (X hi + Y hi)
+      to |= !wait_sleepy(&bar_free[b], (uint32_t)((k >> 1) & 1), abort_flag);
+      if (!__any_sync(0xffffffffu, to)) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float x[16], y[16];
+          tc::tmem_ld16(tl + T_PD + 64 * b + 16 * hh, x);
+          tc::tmem_ld16(tl + T_PD + 64 * b + kSl + 16 * hh, y);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[16 * hh + e] = fmaf(gq, a[16 * hh + e], x[e] + y[e]);
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_oe[b]);  // this chunk's output accumulators are free
+      if (fused) {
+        // this slice's sum of squares of row t to the other three CTAs (an
+        // asynchronous store that completes on the receiver's mbarrier), and
+        // into this CTA's own slot
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ss = fmaf(o[e], o[e], ss);
+        const uint32_t slot = smem_u32(&snorm[b][rank][t]), nb = smem_u32(&bar_nm[b]);
+#pragma unroll
+        for (uint32_t r = 0; r < (uint32_t)kSlCta; ++r) {
+          if (r == rank)
+            snorm[b][rank][t] = ss;
+          else
+            st_async_cluster_f32(map_shared_rank(slot, r), ss, map_shared_rank(nb, r));
+        }
+      }
+      if (p.core_out != nullptr && t < L && !to) {
+        float4* cg = reinterpret_cast<float4*>(p.core_out + ((c0 + t) * p.Hv + h) * kD + j0);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) cg[m] = make_float4(o[4 * m], o[4 * m + 1], o[4 * m + 2], o[4 * m + 3]);
+      }
+      if (!fused) {
+        if (bar_or(3, kSlOutThreads, to)) break;
+        continue;
+      }
+      // the gate nw silu(z) while the peers' sums are on their way
+      if (!to) to = !wait_sleepy(&bar_z[b], (uint32_t)((k >> 1) & 1), abort_flag);
+      const uint4* zr = reinterpret_cast<const uint4*>(sm + L_Z + b * 4096 + t * (kSl * 2));
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint4 zw = zr[m];
+        const uint32_t zz[4] = {zw.x, zw.y, zw.z, zw.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const __nv_bfloat162 z2 = *reinterpret_cast<const __nv_bfloat162*>(&zz[c]);
+          const int e = 8 * m + 2 * c;
+          const float z0 = __low2float(z2), z1 = __high2float(z2);
+          o[e] *= snw[e] * __fdividef(z0, 1.f + __expf(-z0));
+          o[e + 1] *= snw[e + 1] * __fdividef(z1, 1.f + __expf(-z1));
+        }
+      }
+      // the peers' sums (a wait limited by time only: see above; all 64 rows
+      // agree on giving up)
+      const bool lost = !wait_sleepy(&bar_nm[b], (uint32_t)((k >> 1) & 1), nullptr);
+      if (bar_or(4, kSlOutThreads, lost)) {
+        *abort_flag = 1;
+        break;
+      }
+      float tot = 0.f;
+#pragma unroll
+      for (int r = 0; r < kSlCta; ++r) tot += snorm[b][r][t];
+      // (a peer writes this buffer again only after every row here has sent
+      // chunk k + 1's sums, i.e. after these reads)
+      if (u == 0 && k + 2 < nch) mbar_arrive_expect_tx(&bar_nm[b], kNormBytes);
+      const float rs = 1.f / sqrtf(tot / (float)kD + p.rms_eps);
+      // (the staging tile b was last stored from two chunks ago; thread 0
+      // waited for that store's reads before the previous chunk's barrier)
+      uint4* orow = reinterpret_cast<uint4*>(sm + L_O + b * 4096 + t * (kSl * 2));
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        orow[m] = make_uint4(pack_bf16(o[8 * m] * rs, o[8 * m + 1] * rs), pack_bf16(o[8 * m + 2] * rs, o[8 * m + 3] * rs),
+                             pack_bf16(o[8 * m + 4] * rs, o[8 * m + 5] * rs),
+                             pack_bf16(o[8 * m + 6] * rs, o[8 * m + 7] * rs));
+      fence_proxy_async_smem();
+      // the previous chunk's store has read its staging tile (rewritten next
+      // chunk) before this barrier
+      if (u == 0 && stored) bulk_wait_read_all();
+      to = bar_or(3, kSlOutThreads, to);
+      if (to) continue;  // no more stores or loads; the exchange goes on
+      const __nv_bfloat16* ob = reinterpret_cast<const __nv_bfloat16*>(sm + L_O + b * 4096);
+      if (L == kC) {
+        // a full chunk leaves as one tile
+        if (u == 0) {
+          tc::tma_store_2d(&tm_o, h * kD + j0, (int)c0, ob);
+          bulk_commit();
+          stored = true;
+        }
+      } else if (t < L) {
+        // the sequence's last chunk: row by row, so no row of the next
+        // sequence is written
+        bulk_store(static_cast<__nv_bfloat16*>(p.out) + ((c0 + t) * p.Hv + h) * kD + j0, ob + t * kSl,
+                   (uint32_t)(kSl * 2));
+        bulk_commit();
+        stored = true;
+      }
+      // every row has read z of chunk k: chunk k + 2's into its tile
+      if (u == 0 && k + 2 < nch) load_z(k + 2);
+    }
+    if (stored) bulk_wait_all();
+    if (u == 0) {
+      if (n_z0) mbar_wait(&bar_z[0], (n_z0 - 1) & 1);
+      if (n_z1) mbar_wait(&bar_z[1], (n_z1 - 1) & 1);
+    }
+  }
+
+  // drain: every copy and MMA this CTA issued has completed, and every CTA
+  // of the cluster is done writing into its peers' shared memory, before
+  // TMEM is released and the CTA exits
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kSlIssueWarp) {
+    tc::fence_after_sync();
+    tc::mma_commit_elect(&bar_fin);
+    mbar_wait(&bar_fin, 0);
+    tc::fence_before_sync();
+  }
+  if (loader) {
+    if (n_in0) {
+      mbar_wait(&bar_in[0], (n_in0 - 1) & 1);
+      mbar_wait(&bar_v[0], (n_in0 - 1) & 1);
+    }
+    if (n_in1) {
+      mbar_wait(&bar_in[1], (n_in1 - 1) & 1);
+      mbar_wait(&bar_v[1], (n_in1 - 1) & 1);
+    }
+  }
+  __syncthreads();
+  cluster_arrive_release();
+  cluster_wait_acquire();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tb, T_SL_COLS);
+  }
+}
+
+// ------------------------------------------------------- separate norm
+
+// The gated RMSNorm of the sliced carry's fp32 core output (the same formula
+// as the fused epilogues): rows (t, h) of the tokens the sequences cover,
+// [cu_seqlens[0], cu_seqlens[N]); one warp per row, four columns per lane.
+// Runs after the carry on the same stream.
+__global__ void __launch_bounds__(256) cp_norm_kernel(const PrefillArgs p, const float* __restrict__ o) {
+  int64_t lo = p.cu_seqlens[0], hi = p.cu_seqlens[p.N];
+  lo = lo < 0 ? 0 : (lo > p.T ? p.T : lo);
+  hi = hi < lo ? lo : (hi > p.T ? p.T : hi);
+  const int lane = threadIdx.x & 31;
+  const int64_t rows_end = hi * p.Hv;
+  const int64_t stride = (int64_t)gridDim.x * 8;
+  const float4 w = *reinterpret_cast<const float4*>(p.norm_w + 4 * lane);
+  for (int64_t row = lo * p.Hv + (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows_end; row += stride) {
+    const float4 v = *reinterpret_cast<const float4*>(o + row * kD + 4 * lane);
+    const uint2 zw = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.z) + row * kD + 4 * lane);
+    const __nv_bfloat162 z01 = *reinterpret_cast<const __nv_bfloat162*>(&zw.x);
+    const __nv_bfloat162 z23 = *reinterpret_cast<const __nv_bfloat162*>(&zw.y);
+    const float ss = group_sum<32>(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+    const float inv = 1.f / sqrtf(ss / (float)kD + p.rms_eps);
+    uint2 out;
+    out.x = pack_bf16(v.x * inv * w.x * silu_f(__low2float(z01)), v.y * inv * w.y * silu_f(__high2float(z01)));
+    out.y = pack_bf16(v.z * inv * w.z * silu_f(__low2float(z23)), v.w * inv * w.w * silu_f(__high2float(z23)));
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + row * kD + 4 * lane) = out;
+  }
+}
+
 }  // namespace
 
 int64_t prefill_cp_workspace_bytes(int32_t N, int64_t T, int32_t Hk, int32_t Hv) {
@@ -1153,6 +1821,19 @@ bool prefill_cp_supported(const PrefillArgs& p, int32_t dtype, int32_t D) {
   if ((double)l.G * p.Hv * kC * 3 >= 2147483647.0) return false;
   if ((double)l.G * p.Hk * kD >= 2147483647.0) return false;
   return tc::encode_fn() != nullptr;
+}
+
+bool prefill_cp_sliced(const PrefillArgs& p) {
+  if (p.flags & GDN_PREFILL_CARRY_SLICED) return true;
+  if (p.flags & GDN_PREFILL_CARRY_WHOLE) return false;
+  // four CTAs per (V head, sequence) pay where the whole-row carries would
+  // leave most SMs idle: at most two waves of sliced CTAs
+  if ((int64_t)p.Hv * p.N > kSlMaxChains) return false;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  return (int64_t)kSlCta * p.Hv * p.N <= 2 * (int64_t)sms;
 }
 
 cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_t stream) {
@@ -1190,6 +1871,38 @@ cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_
   cp_prep_kernel<<<dim3((unsigned)l.G, (unsigned)p.Hk), kPrepThreads, P_SMEM, stream>>>(p, w, mq, mk);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (prefill_cp_sliced(p)) {
+    // With the gated norm, the carry writes the fp32 core output (core_out,
+    // else the workspace's region for it) and a separate pass normalises it:
+    // the norm's work in the carry's output warps slows the carry's own
+    // phases on the SMs it shares. Without such a buffer (the sliced carry
+    // forced for many pairs), the carry's output warps apply it themselves.
+    PrefillArgs ps = p;
+    const bool defer = p.z != nullptr && (p.core_out != nullptr || l.off_o != 0);
+    if (defer) {
+      ps.z = nullptr;
+      if (ps.core_out == nullptr) ps.core_out = reinterpret_cast<float*>(static_cast<char*>(workspace) + l.off_o);
+    }
+    CUtensorMap mv32, mz32, mo32;
+    memset(&mz32, 0, sizeof(mz32));
+    memset(&mo32, 0, sizeof(mo32));
+    if (!tc::make_map_2d(&mv32, p.v, p.T, vc, p.v_stride, 2, bf, kSl, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    if (ps.z != nullptr &&
+        (!tc::make_map_2d(&mz32, p.z, p.T, vc, vc, 2, bf, kSl, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+         !tc::make_map_2d(&mo32, p.out, p.T, vc, vc, 2, bf, kSl, 64, CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(cp_slice_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L_SMEM);
+    if (e != cudaSuccess) return e;
+    cp_slice_kernel<<<dim3((unsigned)(kSlCta * p.Hv), (unsigned)p.N), kSlThreads, L_SMEM, stream>>>(
+        ps, w, mq, mk, mv32, mw, mz32, mkt, mo32);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !defer) return e;
+    const int64_t rows = p.T * p.Hv;
+    const int64_t blocks = (rows + 7) / 8 < 4096 ? (rows + 7) / 8 : 4096;
+    cp_norm_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, ps.core_out);
+    return cudaGetLastError();
+  }
   e = cudaFuncSetAttribute(cp_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
   cp_chain_kernel<<<dim3((unsigned)p.Hv, (unsigned)p.N), kChainAll, C_SMEM, stream>>>(p, w, mq, mk,

@@ -65,8 +65,14 @@ typedef enum gdn_dtype { GDN_F16 = 0, GDN_BF16 = 1, GDN_F32 = 2 } gdn_dtype;
 enum {
   GDN_QK_PRENORMALIZED = 1,  /* q and k are already l2-normalised: skip it */
   GDN_GATES_PRECOMPUTED = 2, /* a holds g and b holds beta, both fp32 [T][Hv] */
-  GDN_PREFILL_CUDA_CORES = 4 /* use the fp32 CUDA-core chunk kernel even where a
-                                tensor-core one applies (head_dim 128, f16/bf16) */
+  GDN_PREFILL_CUDA_CORES = 4, /* use the fp32 CUDA-core chunk kernel even where a
+                                 tensor-core one applies (head_dim 128, f16/bf16) */
+  /* On the chunk-parallel path, the carry kernel: by default the sliced one
+     (four CTAs per V head and sequence) when 4 Hv N is at most two waves of
+     the device's SMs, else one CTA per V head and sequence. These force
+     either (not both); other paths ignore them. */
+  GDN_PREFILL_CARRY_WHOLE = 8,
+  GDN_PREFILL_CARRY_SLICED = 16
 };
 
 typedef struct gdn_dims {
@@ -262,14 +268,16 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int
  * (0 when no workspace path applies: head_dim != 128, io dtype not bf16,
  * more than 8 V heads per K head, or GDN_PREFILL_CUDA_CORES): per 64-token chunk slot ((T + 63 N) / 64 of
  * them) 25 KB per V head and 16 KB per K head, plus 4 (N + 1) bytes rounded
- * up to 1 KB. Writes the size to *bytes; GDN_ERR_INVALID_ARG /
- * GDN_ERR_EXTENT for invalid dims or sizes.
+ * up to 1 KB; and where Hv N <= 64 (the sliced carry), T Hv 512 bytes more
+ * at a 256-byte boundary, for the fp32 core output that its separate gated
+ * norm reads when core_out is NULL. Writes the size to *bytes;
+ * GDN_ERR_INVALID_ARG / GDN_ERR_EXTENT for invalid dims or sizes.
  */
 gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
                                       int64_t total_tokens, int32_t flags, int64_t* bytes);
 
 /* Size of the static device scratch behind gdn_prefill_chunked_static. */
-#define GDN_STATIC_SCRATCH_BYTES (96u << 20)
+#define GDN_STATIC_SCRATCH_BYTES (160u << 20)
 
 /*
  * gdn_prefill_chunked without a workspace argument that still takes the
@@ -281,8 +289,8 @@ gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
  *
  * Arguments, results and errors are those of gdn_prefill_chunked, plus:
  *  - GDN_ERR_EXTENT, checked first, when gdn_prefill_workspace_size for
- *    these sizes exceeds GDN_STATIC_SCRATCH_BYTES (e.g. more than about
- *    5,900 tokens at Hk=16, Hv=32; 3,400 at Hk=16, Hv=64);
+ *    these sizes exceeds GDN_STATIC_SCRATCH_BYTES (e.g. more than 5,025
+ *    tokens in one sequence at Hk=16, Hv=32; 2,683 at Hk=16, Hv=64);
  *  - where no workspace path applies (f16, head_dim != 128,
  *    GDN_PREFILL_CUDA_CORES) it is gdn_prefill_chunked with workspace NULL.
  *

@@ -54,7 +54,8 @@ def test_prefill_workspace_size(lib):
     d = gdn.dims(16, 32, 128, io_dtype=torch.bfloat16)
     # (T + 63 N) / 64 chunk slots x (Hv x 25 KB + Hk x 16 KB), after the 1 KB index
     per_slot = 32 * 25600 + 16 * 16384
-    assert gdn.gdn_prefill_workspace_size(d, 1, 4096) == 1024 + 64 * per_slot
+    # one sequence (Hv N <= 64): plus the sliced carry's fp32 core output
+    assert gdn.gdn_prefill_workspace_size(d, 1, 4096) == 1024 + 64 * per_slot + 4096 * 32 * 512
     assert gdn.gdn_prefill_workspace_size(d, 8, 34482) == 1024 + (34482 + 63 * 8) // 64 * per_slot
     assert gdn.gdn_prefill_workspace_size(d, 1, 0) == 0
     assert gdn.gdn_prefill_workspace_size(d, 1, 4096, gdn.GDN_PREFILL_CUDA_CORES) == 0
@@ -66,6 +67,11 @@ def test_prefill_workspace_size(lib):
         gdn.gdn_prefill_workspace_size(d, -1, 10)
     with pytest.raises(gdn.GdnError):
         gdn.gdn_prefill_workspace_size(d, 1, 10, 64)  # unknown flag
+    # the carry choice does not change the workspace; both at once is refused
+    for carry in (gdn.GDN_PREFILL_CARRY_WHOLE, gdn.GDN_PREFILL_CARRY_SLICED):
+        assert gdn.gdn_prefill_workspace_size(d, 1, 4096, carry) == 1024 + 64 * per_slot + 4096 * 32 * 512
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_prefill_workspace_size(d, 1, 10, gdn.GDN_PREFILL_CARRY_WHOLE | gdn.GDN_PREFILL_CARRY_SLICED)
 
 
 def test_qkv_features(lib):
@@ -183,7 +189,10 @@ def test_conv_and_prefill_and_norm_reject_bad_arguments(lib):
     args[5] = 68  # q stride not a multiple of 16 bytes
     assert pf(*args) == 5
     args = list(base)
-    args[14] = 8  # unknown flag
+    args[14] = 32  # unknown flag
+    assert pf(*args) == 1
+    args = list(base)
+    args[14] = gdn.GDN_PREFILL_CARRY_WHOLE | gdn.GDN_PREFILL_CARRY_SLICED  # both carry kernels
     assert pf(*args) == 1
     args = list(base)
     args[16] = VP(0x100000)  # core_out aliases the state
@@ -280,3 +289,12 @@ def test_binding_checks_every_tensor_size_before_the_call(lib):
         gdn.gdn_conv_update(d, cu, Z(3, 256), Z(256, 4), Z(1, 256, 3), Z(2, 256))
     with pytest.raises(ValueError, match="elements"):
         gdn.gdn_gated_rmsnorm(d, Z(4, 32), Z(3, 32), Z(32), Z(4, 32))
+
+
+def test_binding_static_scratch_size_matches_the_header():
+    """The binding's GDN_STATIC_SCRATCH_BYTES is the header's."""
+    with open(os.path.join(ROOT, "include", "gdn.h")) as f:
+        text = f.read()
+    m = re.search(r"#define GDN_STATIC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    assert m is not None
+    assert gdn.GDN_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))

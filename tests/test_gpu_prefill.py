@@ -8,7 +8,7 @@ import torch
 import gated_delta_net_causal_gb300 as gdn
 import gdn_inputs as gi
 import oracle
-from tests.gpu_helpers import (CHUNK_OUT_ABS, CHUNK_STATE_ABS, F64, assert_abs, assert_lowp,
+from tests.gpu_helpers import (CHUNK_OUT_ABS, CHUNK_STATE_ABS, F64, assert_abs, assert_gated, assert_lowp,
                                cuda, parallel_map)
 
 pytestmark = pytest.mark.gpu
@@ -46,9 +46,13 @@ def _page_chunk_inputs(T, Hk, Hv, D):
     return t(q), t(k), t(v), t(g.reshape(T, Hv)), t(beta.reshape(T, Hv)), t(S0)
 
 
-# workspace argument per path: the chunk-parallel kernels (a workspace) or the
-# single-pass kernel (none); both are tensor-core paths for bf16 at D=128
-PATHS = {"parallel": "auto", "single": None}
+# (workspace argument, extra flags) per path: the chunk-parallel kernels (a
+# workspace) with the sliced carry (four CTAs per V head and sequence) or the
+# whole-row carry forced, or the single-pass kernel (no workspace); all are
+# tensor-core paths for bf16 at D=128
+PATHS = {"sliced": ("auto", gdn.GDN_PREFILL_CARRY_SLICED),
+         "whole": ("auto", gdn.GDN_PREFILL_CARRY_WHOLE),
+         "single": (None, 0)}
 
 
 def _run_prefill(d, cu, q, k, v, a, b, state, flags, dp=None, dt=None, z=None, nw=None,
@@ -77,15 +81,15 @@ def test_page_chunk_case_and_split_continuity(hk, hv, d, mp, io, path):
     untouched (the Metal chunk test's shapes and fill). fp32 activations run
     the CUDA-core kernel; bf16 at head_dim 128 a tensor-core one (chunk-
     parallel with a workspace, single-pass without)."""
-    if path == "single" and not (io == "bf16" and d == 128):
+    if path != "sliced" and not (io == "bf16" and d == 128):
         pytest.skip("the workspace only selects a kernel for bf16 at head_dim 128")
-    ws = PATHS[path]
+    ws, carry = PATHS[path]
     T = 145
     q, k, v, g, beta, S0 = _page_chunk_inputs(T, hk, hv, d)
     if io == "bf16":
         q, k, v = (x.to(torch.bfloat16) for x in (q, k, v))
     dims = gdn.dims(hk, hv, d, map=mp, io_dtype=gi.DTYPES[io])
-    flags = gdn.GDN_QK_PRENORMALIZED | gdn.GDN_GATES_PRECOMPUTED
+    flags = gdn.GDN_QK_PRENORMALIZED | gdn.GDN_GATES_PRECOMPUTED | carry
     ro, rS = oracle.delta(F64(q), F64(k), F64(v), F64(g), F64(beta), F64(S0)[0], mp)
 
     buf, state = _guarded_state(S0)
@@ -133,7 +137,7 @@ def _oracle_prefill(shape, w, q, k, v, a, b, S0, cu):
 @pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("mp,dec", [(gi.GROUPED, gi.LOG_RATE), (gi.TILED, gi.NEGATIVE_RATE)])
 def test_varlen_raw_inputs_with_fused_norm(dtype, d, mp, dec, path):
-    if path == "single" and not (dtype == "bf16" and d == 128):
+    if path != "sliced" and not (dtype == "bf16" and d == 128):
         pytest.skip("the workspace only selects a kernel for bf16 at head_dim 128")
     lengths = [1, 63, 64, 65, 130, 0, 7]
     shape = gi.Shape(2, 4, d, map=mp, decay=dec, dtype=dtype)
@@ -141,8 +145,8 @@ def test_varlen_raw_inputs_with_fused_norm(dtype, d, mp, dec, path):
     cu = gi.cu_seqlens(lengths)
     dims = gdn.dims(2, 4, d, map=mp, decay=dec, io_dtype=gi.DTYPES[dtype])
     state = cuda(S0)
-    core, out = _run_prefill(dims, cu, q, k, v, a, b, state, 0, dp=w.decay_param, dt=w.dt_bias,
-                             z=cuda(z), nw=cuda(w.norm_w), workspace=PATHS[path])
+    core, out = _run_prefill(dims, cu, q, k, v, a, b, state, PATHS[path][1], dp=w.decay_param,
+                             dt=w.dt_bias, z=cuda(z), nw=cuda(w.norm_w), workspace=PATHS[path][0])
     ro, rS = _oracle_prefill(shape, w, q, k, v, a, b, S0, cu)
     assert_abs(core.cpu(), ro, CHUNK_OUT_ABS, "varlen output")
     assert_abs(state.cpu(), rS, CHUNK_STATE_ABS, "varlen state")
@@ -155,16 +159,18 @@ def test_varlen_raw_inputs_with_fused_norm(dtype, d, mp, dec, path):
 
 @pytest.mark.parametrize("lengths", [[64], [1], [200, 0, 63], [129, 65, 1, 300]])
 def test_tensor_core_kernels_match_cuda_core_kernel(lengths):
-    """The three chunk kernels on the same bf16 inputs (head_dim 128): the
-    chunk-parallel and single-pass tensor-core ones and the fp32 CUDA-core
-    one, each within the chunk bounds of the oracle and of each other."""
+    """The chunk kernels on the same bf16 inputs (head_dim 128): the
+    chunk-parallel path with either carry kernel, the single-pass tensor-core
+    kernel and the fp32 CUDA-core one, each within the chunk bounds of the
+    oracle and of each other."""
     shape = gi.Shape(2, 8, 128, map=gi.TILED, decay=gi.LOG_RATE, dtype="bf16")
     w, q, k, v, z, a, b, S0 = _raw_case(900 + len(lengths), shape, lengths)
     cu = gi.cu_seqlens(lengths)
     dims = gdn.dims(2, 8, 128, map=gi.TILED, io_dtype=torch.bfloat16)
     ro, rS = _oracle_prefill(shape, w, q, k, v, a, b, S0, cu)
     runs = {}
-    for name, flags, ws in (("parallel", 0, "auto"), ("single", 0, None),
+    for name, flags, ws in (("sliced", gdn.GDN_PREFILL_CARRY_SLICED, "auto"),
+                            ("whole", gdn.GDN_PREFILL_CARRY_WHOLE, "auto"), ("single", 0, None),
                             ("cuda cores", gdn.GDN_PREFILL_CUDA_CORES, None)):
         st = cuda(S0)
         c, o = _run_prefill(dims, cu, q, k, v, a, b, st, flags, dp=w.decay_param, dt=w.dt_bias,
@@ -174,8 +180,37 @@ def test_tensor_core_kernels_match_cuda_core_kernel(lengths):
         ry = oracle.gated_rmsnorm(F64(c.cpu()), F64(z), F64(w.norm_w), 1e-6)
         assert_lowp(o.cpu(), ry, "bf16", f"{name} fused norm")
         runs[name] = c.cpu()
-    assert_abs(runs["parallel"], F64(runs["cuda cores"]), CHUNK_OUT_ABS, "parallel vs cuda cores")
+    assert_abs(runs["sliced"], F64(runs["cuda cores"]), CHUNK_OUT_ABS, "sliced vs cuda cores")
+    assert_abs(runs["whole"], F64(runs["cuda cores"]), CHUNK_OUT_ABS, "whole vs cuda cores")
     assert_abs(runs["single"], F64(runs["cuda cores"]), CHUNK_OUT_ABS, "single vs cuda cores")
+    assert gdn.gdn_device_error() == 0
+
+
+@pytest.mark.parametrize("lengths,forced", [([130, 0, 63], False), ([40] * 9, True)])
+def test_sliced_carry_gated_output_without_core_out(lengths, forced):
+    """The sliced carry asked for the gated output only (core_out NULL). For
+    few (V head, sequence) pairs (3 x 8 = 24) the norm is a separate pass
+    over the workspace's fp32 core output; with the sliced carry forced for
+    more pairs (9 x 8 = 72) the carry's output warps apply it, the per-row
+    sums of squares exchanged over the cluster. Both end to end against the
+    oracle with the chunked output bound carried through the norm, and the
+    states at the chunked bound."""
+    shape = gi.Shape(2, 8, 128, map=gi.TILED, decay=gi.LOG_RATE, dtype="bf16")
+    w, q, k, v, z, a, b, S0 = _raw_case(950 + len(lengths), shape, lengths)
+    cu = gi.cu_seqlens(lengths)
+    dims = gdn.dims(2, 8, 128, map=gi.TILED, io_dtype=torch.bfloat16)
+    T = q.shape[0]
+    state = cuda(S0)
+    out = torch.full((T, 8, 128), float("nan"), device="cuda", dtype=torch.bfloat16)
+    gdn.gdn_prefill_chunked(dims, cuda(cu), cuda(q).reshape(T, -1), cuda(k).reshape(T, -1),
+                            cuda(v).reshape(T, -1), cuda(a), cuda(b), cuda(w.decay_param),
+                            cuda(w.dt_bias), state, z=cuda(z), norm_w=cuda(w.norm_w), out=out,
+                            flags=gdn.GDN_PREFILL_CARRY_SLICED if forced else 0)
+    torch.cuda.synchronize()
+    ro, rS = _oracle_prefill(shape, w, q, k, v, a, b, S0, cu)
+    ry = oracle.gated_rmsnorm(ro, F64(z), F64(w.norm_w), 1e-6)
+    assert_gated(out.cpu(), ry, ro, z, w.norm_w, "bf16", "sliced gated output", eps_o=CHUNK_OUT_ABS)
+    assert_abs(state.cpu(), rS, CHUNK_STATE_ABS, "sliced state")
     assert gdn.gdn_device_error() == 0
 
 
@@ -230,7 +265,7 @@ def test_workspace_size_and_too_small_workspace():
     d = gdn.dims(16, 32, 128, io_dtype=torch.bfloat16)
     n = gdn.gdn_prefill_workspace_size(d, 1, 4096)
     # 64 chunk slots x (32 V heads x 25 KB + 16 K heads x 16 KB) + the 1 KB index
-    assert n == 1024 + 64 * (32 * (3 * 8192 + 1024) + 16 * 16384)
+    assert n == 1024 + 64 * (32 * (3 * 8192 + 1024) + 16 * 16384) + 4096 * 32 * 128 * 4
     assert gdn.gdn_prefill_workspace_size(d, 1, 4096, gdn.GDN_PREFILL_CUDA_CORES) == 0
     assert gdn.gdn_prefill_workspace_size(gdn.dims(16, 32, 128, io_dtype=torch.float16), 1,
                                           4096) == 0
@@ -305,8 +340,8 @@ def test_prefill_t4096_all_heads(random_state, path):
     dims = gdn.dims(16, 32, 128, map=shape.map, decay=shape.decay, io_dtype=torch.bfloat16)
     state = cuda(wl["state"])
     core, out = _run_prefill(dims, wl["cu_seqlens"], wl["q"], wl["k"], wl["v"], wl["a"],
-                             wl["b"], state, 0, dp=w.decay_param, dt=w.dt_bias,
-                             z=cuda(wl["z"]), nw=cuda(w.norm_w), workspace=PATHS[path])
+                             wl["b"], state, PATHS[path][1], dp=w.decay_param, dt=w.dt_bias,
+                             z=cuda(wl["z"]), nw=cuda(w.norm_w), workspace=PATHS[path][0])
     _check_all_heads(shape, w, wl["q"], wl["k"], wl["v"], wl["a"], wl["b"], F64(wl["state"])[0],
                      core, state, "T=4096")
     ry = oracle.gated_rmsnorm(F64(core.cpu()), F64(wl["z"]), F64(w.norm_w), 1e-6)
@@ -332,8 +367,8 @@ def test_prefill_t4096_long_memory(path):
     dims = gdn.dims(16, 32, 128, map=shape.map, decay=shape.decay, io_dtype=torch.bfloat16)
     state = cuda(wl["state"])
     core, out = _run_prefill(dims, wl["cu_seqlens"], wl["q"], wl["k"], wl["v"], wl["a"],
-                             wl["b"], state, 0, dp=dp, dt=w.dt_bias, z=cuda(wl["z"]),
-                             nw=cuda(w.norm_w), workspace=PATHS[path])
+                             wl["b"], state, PATHS[path][1], dp=dp, dt=w.dt_bias,
+                             z=cuda(wl["z"]), nw=cuda(w.norm_w), workspace=PATHS[path][0])
 
     class _W:  # the workload's weights with the long-memory decay parameter
         decay_param, dt_bias, norm_w = dp, w.dt_bias, w.norm_w
