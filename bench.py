@@ -199,6 +199,9 @@ def _decode_call(gdn, d, dev, inp, state, cstate, out):
 def run_gpu(args, ws, rank, local):
     torch.cuda.set_device(local)
     peaks = _peaks()
+    if args.prefill_only:
+        line = {"metric": "chunked prefill tokens/s", "prefill": run_prefill(args, peaks, ws)}
+        return line if rank == 0 else None
     batch = args.batch
     gdn, d, dev, steps, host, state, cstate, out, shape = _decode_setup(batch, 16, rank)
     flush = torch.empty(512 * 1024 * 1024 // 4, device="cuda", dtype=torch.float32)
@@ -458,26 +461,35 @@ def run_prefill(args, peaks, ws):
     flush = torch.empty(512 * 1024 * 1024 // 4, device="cuda", dtype=torch.float32)
     stream = torch.cuda.current_stream()
 
-    def call():
+    def call(flags=0):
         gdn.gdn_prefill_chunked(d, cu, q, k, v, a, b, dp, dt, state, core_out=None, z=z,
-                                norm_w=nw, out=out, workspace=wsb)
+                                norm_w=nw, out=out, workspace=wsb, flags=flags)
 
-    for _ in range(3):
-        state.copy_(s0)
-        call()
-    torch.cuda.synchronize()
-    n = max(3, min(args.steps, 20))
-    times = []
-    for i in range(n):
-        state.copy_(s0)
-        flush.fill_(float(i))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        call()
-        e1.record(stream)
+    def timed(flags, n):
+        for _ in range(3):
+            state.copy_(s0)
+            call(flags)
         torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1) * 1e-3)
-    t = _barrier_max(statistics.mean(times), ws)
+        times = []
+        for i in range(n):
+            state.copy_(s0)
+            flush.fill_(float(i))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call(flags)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e-3)
+        return _barrier_max(statistics.mean(times), ws)
+
+    n = max(3, min(args.steps, 20))
+    t = timed(0, n)
+    # the library's default carry for one sequence of 32 V heads: the sliced
+    # one (4 CTAs per V head) when Hv N <= 64 and 4 Hv N <= 2 x SMs, its
+    # gated norm then a separate pass; the whole-row carry timed beside it
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    sliced = 32 * 1 <= 64 and 4 * 32 <= 2 * sms
+    t_whole = timed(gdn.GDN_PREFILL_CARRY_WHOLE, n)
 
     # end to end through the C ABI with host buffers: the call's inputs (q, k,
     # v, a, b, z) copied from pinned host memory, the call, the gated output
@@ -509,20 +521,24 @@ def run_prefill(args, peaks, ws):
     flops = flop_per_token * T
     byts = T * (2 * Hk * D + 2 * Hv * D) * 2 + T * Hv * D * 2 + 2 * Hv * D * D * 4 + 4 * T * Hv * 2
     res = {"workload": PREFILL_WORKLOAD, "value": round(ws * T / t, 1), "unit": "tokens/s",
-            "ms_per_call": round(t * 1e3, 4), "calls": n, "launches_per_call": 3,
+            "ms_per_call": round(t * 1e3, 4), "calls": n, "launches_per_call": 4 if sliced else 3,
+            "carry": ("sliced: cp_slice_kernel, 4 CTAs per V head, then cp_norm_kernel" if sliced
+                      else "whole rows: cp_chain_kernel, 1 CTA per V head"),
+            "whole_row_carry_ms_per_call": round(t_whole * 1e3, 4),
             "roofline": {"bound": "tensor", "achieved": round(flops / t / 1e12, 3),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(flops / t / 1e12 / peaks["bf16_tflops"], 5),
                          "traffic": _profile_traffic("prefill_cp_t4096.txt",
                                                      _kernel_hash("prefill_cp.cu", "tc_common.cuh",
                                                                   "gdn_common.cuh")),
-                         "traffic_unit": "bytes per call (all three launches)",
+                         "traffic_unit": "bytes per call (all launches)",
                          "peak_source": peaks["source"],
                          "algorithmic_flops_per_call": flops,
                          "algorithmic_bytes_per_call": byts,
                          "hbm_frac": round(byts / t / 1e9 / peaks["hbm_gbs"], 4),
-                         "timed": "the whole call (chunk index, prep, chain launches)",
-                         "kernel": "cp_prep_kernel + cp_chain_kernel"},
+                         "timed": "the whole call (chunk index, prep, carry, norm launches)",
+                         "kernel": ("cp_prep_kernel + cp_slice_kernel + cp_norm_kernel" if sliced
+                                    else "cp_prep_kernel + cp_chain_kernel")},
            "e2e": {"value": round(ws * T / t_e2e, 1), "unit": "tokens/s",
                    "ms_per_call": round(t_e2e * 1e3, 4), "h2d_bytes_per_step": h2d,
                    "d2h_bytes_per_step": d2h,
@@ -1048,6 +1064,9 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the state-slot and multi-token decode blocks")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="run only the T=4096 chunked-prefill block (a process of about 1.5 GB "
+                         "on the device, for profiler captures of the prefill kernels)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     ws, rank, local = _dist()

@@ -1784,27 +1784,47 @@ __global__ void __cluster_dims__(kSlCta, 1, 1) __launch_bounds__(kSlThreads, 1)
 
 // The gated RMSNorm of the sliced carry's fp32 core output (the same formula
 // as the fused epilogues): rows (t, h) of the tokens the sequences cover,
-// [cu_seqlens[0], cu_seqlens[N]); one warp per row, four columns per lane.
-// Runs after the carry on the same stream.
+// [cu_seqlens[0], cu_seqlens[N]). A warp takes four rows, each lane the same
+// four columns of each (one coalesced 512-byte row per load), all eight
+// loads issued before the reductions. Runs after the carry on the same
+// stream.
+constexpr int kNormRowsPerWarp = 4;
+constexpr int kNormRowsPerBlock = 8 * kNormRowsPerWarp;  // 256 threads
 __global__ void __launch_bounds__(256) cp_norm_kernel(const PrefillArgs p, const float* __restrict__ o) {
   int64_t lo = p.cu_seqlens[0], hi = p.cu_seqlens[p.N];
   lo = lo < 0 ? 0 : (lo > p.T ? p.T : lo);
   hi = hi < lo ? lo : (hi > p.T ? p.T : hi);
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, c0 = 4 * lane;
   const int64_t rows_end = hi * p.Hv;
-  const int64_t stride = (int64_t)gridDim.x * 8;
-  const float4 w = *reinterpret_cast<const float4*>(p.norm_w + 4 * lane);
-  for (int64_t row = lo * p.Hv + (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows_end; row += stride) {
-    const float4 v = *reinterpret_cast<const float4*>(o + row * kD + 4 * lane);
-    const uint2 zw = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.z) + row * kD + 4 * lane);
-    const __nv_bfloat162 z01 = *reinterpret_cast<const __nv_bfloat162*>(&zw.x);
-    const __nv_bfloat162 z23 = *reinterpret_cast<const __nv_bfloat162*>(&zw.y);
-    const float ss = group_sum<32>(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
-    const float inv = 1.f / sqrtf(ss / (float)kD + p.rms_eps);
-    uint2 out;
-    out.x = pack_bf16(v.x * inv * w.x * silu_f(__low2float(z01)), v.y * inv * w.y * silu_f(__high2float(z01)));
-    out.y = pack_bf16(v.z * inv * w.z * silu_f(__low2float(z23)), v.w * inv * w.w * silu_f(__high2float(z23)));
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + row * kD + 4 * lane) = out;
+  const int64_t stride = (int64_t)gridDim.x * kNormRowsPerBlock;
+  const float4 w = *reinterpret_cast<const float4*>(p.norm_w + c0);
+  for (int64_t r0 = lo * p.Hv + (int64_t)blockIdx.x * kNormRowsPerBlock + kNormRowsPerWarp * (threadIdx.x >> 5);
+       r0 < rows_end; r0 += stride) {
+    float4 v[kNormRowsPerWarp];
+    uint2 zw[kNormRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kNormRowsPerWarp; ++r) {
+      v[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+      zw[r] = make_uint2(0u, 0u);
+      if (r0 + r < rows_end) {  // (uniform across the warp)
+        v[r] = *reinterpret_cast<const float4*>(o + (r0 + r) * kD + c0);
+        zw[r] = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.z) + (r0 + r) * kD + c0);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kNormRowsPerWarp; ++r) {
+      const float ss = group_sum<32>(v[r].x * v[r].x + v[r].y * v[r].y + v[r].z * v[r].z + v[r].w * v[r].w);
+      const float inv = 1.f / sqrtf(ss / (float)kD + p.rms_eps);
+      const __nv_bfloat162 z01 = *reinterpret_cast<const __nv_bfloat162*>(&zw[r].x);
+      const __nv_bfloat162 z23 = *reinterpret_cast<const __nv_bfloat162*>(&zw[r].y);
+      uint2 y;
+      y.x = pack_bf16(v[r].x * inv * w.x * silu_fast(__low2float(z01)),
+                      v[r].y * inv * w.y * silu_fast(__high2float(z01)));
+      y.y = pack_bf16(v[r].z * inv * w.z * silu_fast(__low2float(z23)),
+                      v[r].w * inv * w.w * silu_fast(__high2float(z23)));
+      if (r0 + r < rows_end)
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + (r0 + r) * kD + c0) = y;
+    }
   }
 }
 
@@ -1899,7 +1919,8 @@ cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_
     e = cudaGetLastError();
     if (e != cudaSuccess || !defer) return e;
     const int64_t rows = p.T * p.Hv;
-    const int64_t blocks = (rows + 7) / 8 < 4096 ? (rows + 7) / 8 : 4096;
+    const int64_t need = (rows + kNormRowsPerBlock - 1) / kNormRowsPerBlock;
+    const int64_t blocks = need < 65536 ? need : 65536;
     cp_norm_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, ps.core_out);
     return cudaGetLastError();
   }

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(256) gated_rmsnorm_kernel(const RmsNormArgs p)
   const float inv = 1.f / sqrtf(ss / (float)D + p.eps);
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
-    const float v = ov[e] * inv * p.norm_w[lane * PER + e] * silu_f(to_f32(z[e]));
+    const float v = ov[e] * inv * p.norm_w[lane * PER + e] * silu_fast(to_f32(z[e]));
     y[e] = from_f32<T>(v);
   }
 }
