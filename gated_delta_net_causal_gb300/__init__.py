@@ -93,6 +93,8 @@ def library() -> ctypes.CDLL:
         L.gdn_gated_rmsnorm.argtypes = [pd, i64, vp, vp, vp, vp, vp]
         L.gdn_device_error.restype = ctypes.c_int
         L.gdn_device_error.argtypes = [ctypes.POINTER(i32), i32]
+        L.gdn_selftest_wait_timeout.restype = ctypes.c_int
+        L.gdn_selftest_wait_timeout.argtypes = [i64, vp, vp]
         _lib = L
     return _lib
 
@@ -371,6 +373,15 @@ def gdn_device_error(clear: bool = True) -> int:
     return st.value
 
 
+def gdn_selftest_wait_timeout(limit_ns: int, gave_up: torch.Tensor, stream=None):
+    """A device-side bounded wait made to give up after limit_ns; gave_up is a
+    CUDA int32 tensor of one element, set to 1 by the kernel."""
+    if gave_up.numel() != 1:
+        raise ValueError("gave_up must have one element")
+    _check(library().gdn_selftest_wait_timeout(int(limit_ns), _ptr(gave_up, "gave_up", torch.int32),
+                                               _stream(stream)), "gdn_selftest_wait_timeout")
+
+
 def gdn_qkv_features(d: GdnDims) -> int:
     return int(library().gdn_qkv_features(ctypes.byref(d)))
 
@@ -382,6 +393,7 @@ def gdn_version() -> int:
 __all__ = ["GdnDims", "GdnError", "dims", "library", "status_string", "gdn_conv_update",
            "gdn_decode_step", "gdn_decode_multi", "gdn_decode_step_slots", "gdn_prefill_chunked", "gdn_prefill_workspace_size",
            "gdn_prefill_chunked_static", "GDN_STATIC_SCRATCH_BYTES", "gdn_gated_rmsnorm", "gdn_device_error",
+           "gdn_selftest_wait_timeout",
            "gdn_qkv_features", "gdn_version", "GDN_MAP_GROUPED", "GDN_MAP_TILED",
            "GDN_DECAY_LOG_RATE", "GDN_DECAY_NEGATIVE_RATE", "GDN_F16", "GDN_BF16", "GDN_F32",
            "GDN_QK_PRENORMALIZED", "GDN_GATES_PRECOMPUTED", "GDN_PREFILL_CUDA_CORES",

@@ -406,6 +406,11 @@ gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, int64_t rows, const float* o,
       gdn::launch_rmsnorm(p, dims->io_dtype, dims->head_dim, static_cast<cudaStream_t>(stream)));
 }
 
+gdn_status gdn_selftest_wait_timeout(int64_t limit_ns, int32_t* gave_up, void* stream) {
+  if (gave_up == nullptr || limit_ns < 1000 || limit_ns > 10000000000LL) return GDN_ERR_INVALID_ARG;
+  return cuda_status(gdn::launch_wait_timeout((uint64_t)limit_ns, gave_up, static_cast<cudaStream_t>(stream)));
+}
+
 gdn_status gdn_device_error(int32_t* status, int32_t clear) {
   if (status == nullptr) return GDN_ERR_INVALID_ARG;
   *status = GDN_OK;
@@ -413,7 +418,7 @@ gdn_status gdn_device_error(int32_t* status, int32_t clear) {
                                                gdn::read_error_conv,
                                                gdn::read_error_rmsnorm, gdn::read_error_prefill,
                                                gdn::read_error_prefill_tc,
-                                               gdn::read_error_prefill_cp};
+                                               gdn::read_error_prefill_cp, gdn::read_error_diag};
   for (auto rd : readers) {
     int32_t v = 0;
     if (rd(&v, clear != 0) != cudaSuccess) return GDN_ERR_CUDA;

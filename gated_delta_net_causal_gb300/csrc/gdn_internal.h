@@ -104,6 +104,9 @@ cudaError_t read_error_rmsnorm(int32_t* status, bool clear);
 cudaError_t read_error_prefill(int32_t* status, bool clear);
 cudaError_t read_error_prefill_tc(int32_t* status, bool clear);
 cudaError_t read_error_prefill_cp(int32_t* status, bool clear);
+cudaError_t read_error_diag(int32_t* status, bool clear);
+// diag.cu: one warp's bounded wait on an mbarrier nothing arrives on
+cudaError_t launch_wait_timeout(uint64_t limit_ns, int32_t* gave_up, cudaStream_t stream);
 
 }  // namespace gdn
 

@@ -1,11 +1,10 @@
 // gdn_prefill_chunked_static: the chunk-parallel prefill over a scratch
 // buffer that the library reserves statically, so that the call itself
 // allocates nothing and needs no workspace from the caller. One buffer per
-// device, shared by all calls (see include/gdn.h for the ordering rule).
+// CUDA context, shared by all calls (see include/gdn.h for the ordering
+// rule).
 #include <cuda_runtime.h>
 #include <stdint.h>
-
-#include <mutex>
 
 #include "gdn.h"
 
@@ -13,22 +12,14 @@ namespace {
 
 __device__ __align__(256) unsigned char g_prefill_scratch[GDN_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of this device's scratch, looked up once per device.
+// Device address of the scratch in the current context. Looked up on every
+// call (cheap, and it allocates nothing): the address belongs to the module
+// as loaded in the current context, so a cached value would go stale after
+// cudaDeviceReset or under another context on the same device.
 gdn_status scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess) return GDN_ERR_CUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess) return GDN_ERR_CUDA;
+  *out = p;
   return GDN_OK;
 }
 

@@ -282,10 +282,12 @@ gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
 /*
  * gdn_prefill_chunked without a workspace argument that still takes the
  * chunk-parallel path: it runs over a scratch buffer of
- * GDN_STATIC_SCRATCH_BYTES that the library reserves statically on each
- * device (when the library's kernels first load there), so the call
- * allocates nothing. The pages have no counterpart to this call; it serves
- * callers that cannot hand out device memory.
+ * GDN_STATIC_SCRATCH_BYTES that the library reserves statically in each
+ * CUDA context (when the library's kernels first load there), so the call
+ * allocates nothing. Its address is looked up in the calling thread's
+ * current context on every call, so it stays valid across cudaDeviceReset
+ * and under several contexts on one device. The pages have no counterpart
+ * to this call; it serves callers that cannot hand out device memory.
  *
  * Arguments, results and errors are those of gdn_prefill_chunked, plus:
  *  - GDN_ERR_EXTENT, checked first, when gdn_prefill_workspace_size for
@@ -294,7 +296,7 @@ gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
  *  - where no workspace path applies (f16, head_dim != 128,
  *    GDN_PREFILL_CUDA_CORES) it is gdn_prefill_chunked with workspace NULL.
  *
- * Races: the scratch is one buffer per device shared by every call of this
+ * Races: the scratch is one buffer per context shared by every call of this
  * function. Two calls whose executions can overlap in time (on different
  * streams without an event between them, or issued from host threads
  * without ordering) write it concurrently and corrupt each other's output
@@ -327,6 +329,18 @@ gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, int64_t rows, const float* o,
  * *status and, when clear != 0, resets it to GDN_OK.
  */
 gdn_status gdn_device_error(int32_t* status, int32_t clear);
+
+/*
+ * Self-test of the device-side give-up path: one warp waits on an mbarrier
+ * that nothing ever arrives on, with a time limit of limit_ns (1 us .. 10 s)
+ * instead of the library's usual 2 s, gives up, records GDN_ERR_TIMEOUT in
+ * the device error word (gdn_device_error) and exits; nothing faults or
+ * hangs and the context stays usable. gave_up is a device int32 written 1
+ * by the kernel when its wait gave up (0 if the wait had completed). No
+ * counterpart on the pages. GDN_ERR_INVALID_ARG for a limit out of range or
+ * a NULL gave_up.
+ */
+gdn_status gdn_selftest_wait_timeout(int64_t limit_ns, int32_t* gave_up, void* stream);
 
 #ifdef __cplusplus
 }

@@ -10,10 +10,11 @@
  * brute-force check), single-threaded, in the order the method is stated:
  *
  *   O1  causal depthwise conv (kernel 4, 3-wide rolling state) + SiLU
- *       -- ferrum-kernels gated_delta_attention_tests.rs, `cpu_segment`
- *          conv loop and conv-state update; libmir-metal decode/mod.rs,
- *          `convolve` (history concatenated before the input, depthwise
- *          conv1d, last kernel-1 inputs kept).
+ *       -- page "ferrum-kernels gated_delta_attention_tests.rs" (the Metal
+ *          conformance tests), section `cpu_segment`: the conv and the
+ *          conv-state update; page "libmir-metal decode/mod.rs", section
+ *          `convolve`: history concatenated before the input, depthwise
+ *          conv1d, the last kernel-1 inputs kept.
  *   O2  per-head l2 normalisation of q and k
  *       -- gated_delta_attention_tests.rs `cpu_segment` / `normalize_rows`:
  *          x * (sum x^2 + eps)^(-1/2);  ferrox-core gdn.rs `l2_normalize`:
@@ -83,34 +84,30 @@ int gdn_oracle_k_head(int map, int h, int n_k_heads, int n_v_heads) {
 /* ------------------------------------------------------------------- O1 */
 
 /* One sequence of T tokens. x [T][C], w [C][4], state [C][3] in/out,
- * y [T][C] = silu(conv). The state afterwards holds the last three raw
- * inputs (taken from the old state when T < 3). */
+ * y [T][C] = silu(conv). Written from the definition: per channel, the
+ * input sequence is the three kept inputs followed by the T new ones,
+ * u = [state | x] (3 + T values); output t is the SiLU of the 4-tap window
+ * of u that ends at the current token, sum_j w[j] u[t + j] (tap 3 on x_t),
+ * and the new state is the last three entries of u. */
 void gdn_oracle_conv(int64_t T, int32_t C, const double* x, const double* w, double* state,
                      double* y) {
-    for (int64_t t = 0; t < T; ++t) {
-        for (int32_t c = 0; c < C; ++c) {
+    const int64_t n = GDN_ORACLE_CONV_STATE + T;
+    double* u = (double*)malloc((size_t)n * sizeof(double));
+    if (u == NULL) abort();
+    for (int32_t c = 0; c < C; ++c) {
+        for (int p = 0; p < GDN_ORACLE_CONV_STATE; ++p)
+            u[p] = state[(int64_t)c * GDN_ORACLE_CONV_STATE + p];
+        for (int64_t t = 0; t < T; ++t) u[GDN_ORACLE_CONV_STATE + t] = x[t * C + c];
+        const double* wc = w + (int64_t)c * GDN_ORACLE_CONV_WIDTH;
+        for (int64_t t = 0; t < T; ++t) {
             double acc = 0.0;
-            for (int j = 0; j < GDN_ORACLE_CONV_WIDTH; ++j) {
-                int64_t src = t + j - GDN_ORACLE_CONV_STATE; /* token this tap reads */
-                double xv = src >= 0 ? x[src * C + c]
-                                     : state[(int64_t)c * GDN_ORACLE_CONV_STATE +
-                                             (GDN_ORACLE_CONV_STATE + src)];
-                acc += w[(int64_t)c * GDN_ORACLE_CONV_WIDTH + j] * xv;
-            }
+            for (int j = 0; j < GDN_ORACLE_CONV_WIDTH; ++j) acc += wc[j] * u[t + j];
             y[t * C + c] = gdn_oracle_silu(acc);
         }
-    }
-    for (int32_t c = 0; c < C; ++c) {
-        double next[GDN_ORACLE_CONV_STATE];
-        for (int p = 0; p < GDN_ORACLE_CONV_STATE; ++p) {
-            int64_t src = T + p - GDN_ORACLE_CONV_STATE;
-            next[p] = src >= 0 ? x[src * C + c]
-                               : state[(int64_t)c * GDN_ORACLE_CONV_STATE +
-                                       (GDN_ORACLE_CONV_STATE + src)];
-        }
         for (int p = 0; p < GDN_ORACLE_CONV_STATE; ++p)
-            state[(int64_t)c * GDN_ORACLE_CONV_STATE + p] = next[p];
+            state[(int64_t)c * GDN_ORACLE_CONV_STATE + p] = u[n - GDN_ORACLE_CONV_STATE + p];
     }
+    free(u);
 }
 
 /* ------------------------------------------------------------------- O2 */

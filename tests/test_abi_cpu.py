@@ -298,3 +298,14 @@ def test_binding_static_scratch_size_matches_the_header():
     m = re.search(r"#define GDN_STATIC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
     assert m is not None
     assert gdn.GDN_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_selftest_wait_timeout_rejects_bad_arguments(lib):
+    """Checked on the host before any launch: the limit's range and the
+    output pointer."""
+    f = lib.gdn_selftest_wait_timeout
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int64, VP, VP]
+    assert f(999, VP(0x1000), None) == 1
+    assert f(10_000_000_001, VP(0x1000), None) == 1
+    assert f(1_000_000, None, None) == 1

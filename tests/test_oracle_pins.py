@@ -67,6 +67,23 @@ def test_l2_normalize_example():
         assert np.max(np.abs(y2 - np.array([c["expected"]]))) <= max(c["tolerance"], 1e-12)
 
 
+def test_l2_normalize_many_rows_against_numpy():
+    """O2 over a (5, 3, 7) array, rows of different scales, against
+    numpy.linalg.norm row by row: a row-indexing or stride mistake in either
+    form fails here (the page's example has a single row)."""
+    rng = np.random.default_rng(20261203)
+    x = rng.normal(size=(5, 3, 7)) * rng.uniform(0.01, 100.0, size=(5, 3, 1))
+    x[2, 1] = 0.0  # an all-zero row
+    n = np.linalg.norm(x, axis=-1, keepdims=True)
+    eps = 1e-6
+    assert np.allclose(oracle.l2norm(x, eps, clamped=True), x / np.maximum(n, eps), rtol=1e-14, atol=0)
+    assert np.allclose(oracle.l2norm(x, eps, clamped=False), x / np.sqrt(n * n + eps), rtol=1e-14, atol=0)
+    # every nonzero row has unit norm up to the eps term
+    y = oracle.l2norm(x, 0.0, clamped=True)
+    norms = np.linalg.norm(y, axis=-1)
+    assert np.allclose(np.delete(norms.ravel(), 2 * 3 + 1), 1.0, rtol=1e-14)
+
+
 # -------------------------------------------------------------- closed forms
 
 def test_sigmoid_softplus_silu_closed_forms():

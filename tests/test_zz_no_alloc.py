@@ -96,3 +96,36 @@ def test_static_scratch_serial_calls_on_one_stream():
     torch.cuda.synchronize()
     assert torch.equal(core_one.cpu(), core_two.cpu())
     assert torch.equal(st_one.cpu(), st_two.cpu())
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("T", [4096, 5025])
+def test_static_scratch_full_size_bit_for_bit(T):
+    """The 4096-token single-sequence workload (Hk=16, Hv=32, bf16, fused
+    norm) and the longest sequence whose workspace still fits the static
+    scratch (5,025 tokens, within 2 % of its size): the static-scratch call
+    equals the workspace call bit for bit, so the scratch's far end (the
+    carry's core-output region) is addressed the same way."""
+    wl = gi.workload_prefill(T, random_state=True)
+    shape, w = wl["shape"], wl["weights"]
+    d = gdn.dims(16, 32, 128, map=shape.map, decay=shape.decay, io_dtype=torch.bfloat16)
+    need = gdn.gdn_prefill_workspace_size(d, 1, T)
+    assert need <= gdn.GDN_STATIC_SCRATCH_BYTES
+    if T == 5025:
+        assert need > 0.98 * gdn.GDN_STATIC_SCRATCH_BYTES
+        assert gdn.gdn_prefill_workspace_size(d, 1, T + 1) > gdn.GDN_STATIC_SCRATCH_BYTES
+    cu = cuda(wl["cu_seqlens"])
+    q, k, v = (cuda(wl[n]).reshape(T, -1) for n in ("q", "k", "v"))
+    a, b, z = cuda(wl["a"]), cuda(wl["b"]), cuda(wl["z"])
+    args = [cuda(w.decay_param), cuda(w.dt_bias)]
+    res = []
+    for fn in (gdn.gdn_prefill_chunked, gdn.gdn_prefill_chunked_static):
+        st = cuda(wl["state"])
+        out = torch.full((T, 32, 128), float("nan"), device="cuda", dtype=torch.bfloat16)
+        fn(d, cu, q, k, v, a, b, *args, st, z=z, norm_w=cuda(w.norm_w), out=out)
+        torch.cuda.synchronize()
+        res.append((out.cpu(), st.cpu()))
+    for x, y in zip(*res):
+        assert torch.equal(x, y)
+    assert not torch.isnan(res[0][0].float()).any()
+    assert gdn.gdn_device_error() == 0
