@@ -95,6 +95,15 @@ def library() -> ctypes.CDLL:
         L.gdn_device_error.argtypes = [ctypes.POINTER(i32), i32]
         L.gdn_selftest_wait_timeout.restype = ctypes.c_int
         L.gdn_selftest_wait_timeout.argtypes = [i64, vp, vp]
+        L.gdn_linear.restype = ctypes.c_int
+        L.gdn_linear.argtypes = [i32, i32, i32, vp, i64, vp, vp, vp, i64, vp, i64, vp]
+        L.gdn_linear_workspace_size.restype = ctypes.c_int
+        L.gdn_linear_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(i64)]
+        L.gdn_decode_layer.restype = ctypes.c_int
+        L.gdn_decode_layer.argtypes = [pd, i32, i32, vp, ctypes.POINTER(GdnLayerWeights), vp, vp, vp, vp,
+                                       i64, vp]
+        L.gdn_decode_layer_workspace_size.restype = ctypes.c_int
+        L.gdn_decode_layer_workspace_size.argtypes = [pd, i32, i32, ctypes.POINTER(i64)]
         _lib = L
     return _lib
 
@@ -373,6 +382,88 @@ def gdn_device_error(clear: bool = True) -> int:
     return st.value
 
 
+class GdnLayerWeights(ctypes.Structure):
+    """gdn_layer_weights: device pointers of one layer's weights."""
+    _fields_ = [("w_in", ctypes.c_void_p), ("b_in", ctypes.c_void_p), ("w_out", ctypes.c_void_p),
+                ("b_out", ctypes.c_void_p), ("conv_w", ctypes.c_void_p), ("decay_param", ctypes.c_void_p),
+                ("dt_bias", ctypes.c_void_p), ("norm_w", ctypes.c_void_p)]
+
+
+def gdn_linear_workspace_size(M: int, N: int, K: int) -> int:
+    n = ctypes.c_int64(0)
+    _check(library().gdn_linear_workspace_size(int(M), int(N), int(K), ctypes.byref(n)),
+           "gdn_linear_workspace_size")
+    return n.value
+
+
+def gdn_linear(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, bias: Optional[torch.Tensor] = None,
+               workspace="auto", stream=None) -> torch.Tensor:
+    """y[M][N] = x[M][K] w[N][K]^T (+ bias), bf16 (rows of x and y may be
+    strided)."""
+    bf = torch.bfloat16
+    if x.dim() != 2 or w.dim() != 2 or y.dim() != 2:
+        raise ValueError("x, w and y must be 2-D")
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or y.shape[0] != M or y.shape[1] != N:
+        raise ValueError(f"shapes: x {tuple(x.shape)}, w {tuple(w.shape)}, y {tuple(y.shape)}")
+    for t, name in ((x, "x"), (y, "y")):
+        if t.dtype != bf or not t.is_cuda or t.stride(1) != 1:
+            raise ValueError(f"{name} must be a CUDA bf16 tensor with unit column stride")
+    _need(bias, "bias", N)
+    need = gdn_linear_workspace_size(M, N, K)
+    if isinstance(workspace, str) and workspace == "auto":
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _need(workspace, "workspace", need)
+    _check(library().gdn_linear(int(M), int(N), int(K), x.data_ptr(), int(x.stride(0)), _ptr(w, "w", bf),
+                                _ptr(bias, "bias", torch.float32), y.data_ptr(), int(y.stride(0)),
+                                _ptr(workspace, "workspace", torch.uint8), int(workspace.numel()),
+                                _stream(stream)), "gdn_linear")
+    return y
+
+
+def gdn_decode_layer_workspace_size(d: GdnDims, hidden: int, batch: int) -> int:
+    n = ctypes.c_int64(0)
+    _check(library().gdn_decode_layer_workspace_size(ctypes.byref(d), int(hidden), int(batch),
+                                                     ctypes.byref(n)), "gdn_decode_layer_workspace_size")
+    return n.value
+
+
+def gdn_decode_layer(d: GdnDims, x: torch.Tensor, w_in, w_out, conv_w, decay_param, dt_bias, norm_w,
+                     conv_state, state, y, b_in=None, b_out=None, workspace="auto", stream=None):
+    """One decode step of a whole layer: x [batch][hidden] -> y [batch][hidden]
+    (bf16), conv_state and state updated in place."""
+    bf, f32 = torch.bfloat16, torch.float32
+    Hk, Hv, D, C = _shape(d)
+    batch, hidden = x.shape
+    n_in = (C + Hv * D + 2 * Hv + 63) // 64 * 64
+    _need(w_in, "w_in", n_in * hidden)
+    _need(b_in, "b_in", n_in)
+    _need(w_out, "w_out", hidden * Hv * D)
+    _need(b_out, "b_out", hidden)
+    _need(conv_w, "conv_w", C * 4)
+    for t, name in ((decay_param, "decay_param"), (dt_bias, "dt_bias")):
+        _need(t, name, Hv)
+    _need(norm_w, "norm_w", D)
+    _need(conv_state, "conv_state", batch * C * 3)
+    _need(state, "state", batch * Hv * D * D)
+    _need(y, "y", batch * hidden)
+    need = gdn_decode_layer_workspace_size(d, hidden, batch)
+    if isinstance(workspace, str) and workspace == "auto":
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _need(workspace, "workspace", need)
+    wts = GdnLayerWeights(_ptr(w_in, "w_in", bf), _ptr(b_in, "b_in", f32), _ptr(w_out, "w_out", bf),
+                          _ptr(b_out, "b_out", f32), _ptr(conv_w, "conv_w", bf),
+                          _ptr(decay_param, "decay_param", f32), _ptr(dt_bias, "dt_bias", f32),
+                          _ptr(norm_w, "norm_w", f32))
+    _check(library().gdn_decode_layer(ctypes.byref(d), int(hidden), int(batch), _ptr(x, "x", bf),
+                                      ctypes.byref(wts), _ptr(conv_state, "conv_state", bf),
+                                      _ptr(state, "state", f32), _ptr(y, "y", bf),
+                                      _ptr(workspace, "workspace", torch.uint8), int(workspace.numel()),
+                                      _stream(stream)), "gdn_decode_layer")
+    return y
+
+
 def gdn_selftest_wait_timeout(limit_ns: int, gave_up: torch.Tensor, stream=None):
     """A device-side bounded wait made to give up after limit_ns; gave_up is a
     CUDA int32 tensor of one element, set to 1 by the kernel."""
@@ -393,7 +484,8 @@ def gdn_version() -> int:
 __all__ = ["GdnDims", "GdnError", "dims", "library", "status_string", "gdn_conv_update",
            "gdn_decode_step", "gdn_decode_multi", "gdn_decode_step_slots", "gdn_prefill_chunked", "gdn_prefill_workspace_size",
            "gdn_prefill_chunked_static", "GDN_STATIC_SCRATCH_BYTES", "gdn_gated_rmsnorm", "gdn_device_error",
-           "gdn_selftest_wait_timeout",
+           "gdn_selftest_wait_timeout", "gdn_linear", "gdn_linear_workspace_size", "gdn_decode_layer",
+           "gdn_decode_layer_workspace_size", "GdnLayerWeights",
            "gdn_qkv_features", "gdn_version", "GDN_MAP_GROUPED", "GDN_MAP_TILED",
            "GDN_DECAY_LOG_RATE", "GDN_DECAY_NEGATIVE_RATE", "GDN_F16", "GDN_BF16", "GDN_F32",
            "GDN_QK_PRENORMALIZED", "GDN_GATES_PRECOMPUTED", "GDN_PREFILL_CUDA_CORES",

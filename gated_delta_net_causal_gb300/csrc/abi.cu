@@ -406,6 +406,175 @@ gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, int64_t rows, const float* o,
       gdn::launch_rmsnorm(p, dims->io_dtype, dims->head_dim, static_cast<cudaStream_t>(stream)));
 }
 
+gdn_status gdn_linear_workspace_size(int32_t M, int32_t N, int32_t K, int64_t* bytes) {
+  if (bytes == nullptr) return GDN_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (M < 1 || M > 128 || N < 64 || N % 64 != 0 || K < 64 || K % 64 != 0) return GDN_ERR_INVALID_ARG;
+  *bytes = gdn::linear_workspace_bytes(M, N, K);
+  return GDN_OK;
+}
+
+gdn_status gdn_linear(int32_t M, int32_t N, int32_t K, const void* x, int64_t x_stride, const void* w,
+                      const float* bias, void* y, int64_t y_stride, void* workspace,
+                      int64_t workspace_bytes, void* stream) {
+  int64_t need = 0;
+  gdn_status st = gdn_linear_workspace_size(M, N, K, &need);
+  if (st != GDN_OK) return st;
+  if (!x || !w || !y || !workspace) return GDN_ERR_INVALID_ARG;
+  if (x_stride < K || x_stride % 8 != 0 || y_stride < N || y_stride % 8 != 0) return GDN_ERR_INVALID_ARG;
+  if (workspace_bytes < need) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)))
+    return GDN_ERR_ALIGN;
+  const Range ry = range_of(y, ((int64_t)(M - 1) * y_stride + N) * 2), rw = range_of(workspace, need);
+  const Range ins[] = {range_of(x, ((int64_t)(M - 1) * x_stride + K) * 2), range_of(w, (int64_t)N * K * 2),
+                       range_of(bias, bias ? (int64_t)N * 4 : 0), rw};
+  for (const Range& in : ins)
+    if (overlap(ry, in)) return GDN_ERR_ALIAS;
+  for (int i = 0; i < 3; ++i)
+    if (overlap(rw, ins[i])) return GDN_ERR_ALIAS;
+  if (!gdn::linear_supported()) return GDN_ERR_UNSUPPORTED;
+  gdn::LinearArgs p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.bias = bias;
+  p.route.count = 1;
+  p.route.start[0] = 0;
+  p.route.start[1] = N;
+  p.route.ld[0] = y_stride;
+  p.route.dst[0] = y;
+  return cuda_status(gdn::launch_linear(p, x, x_stride, w, workspace, static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+
+struct LayerLayout {
+  int64_t C, vw, n_in;  // qkv features, value width Hv D, padded input-projection rows
+  size_t off_qkv, off_z, off_b, off_a, off_y, off_lin, total;
+};
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+gdn_status layer_layout(const gdn_dims* d, int32_t hidden, int32_t batch, LayerLayout* l) {
+  gdn_status st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (d->io_dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  if (hidden < 64 || hidden % 64 != 0 || batch < 1 || batch > 128) return GDN_ERR_INVALID_ARG;
+  const int64_t Hv = d->n_v_heads, D = d->head_dim;
+  if ((Hv * D) % 64 != 0 || Hv % 8 != 0) return GDN_ERR_UNSUPPORTED;
+  l->C = qkv_features(d);
+  l->vw = Hv * D;
+  l->n_in = (l->C + l->vw + 2 * Hv + 63) / 64 * 64;
+  if (l->n_in > INT32_MAX / 2 || (int64_t)hidden * l->n_in > INT32_MAX) return GDN_ERR_EXTENT;
+  size_t off = 0;
+  l->off_qkv = off;
+  off = align256(off + (size_t)batch * l->C * 2);
+  l->off_z = off;
+  off = align256(off + (size_t)batch * l->vw * 2);
+  l->off_b = off;
+  off = align256(off + (size_t)batch * Hv * 2);
+  l->off_a = off;
+  off = align256(off + (size_t)batch * Hv * 2);
+  l->off_y = off;
+  off = align256(off + (size_t)batch * l->vw * 2);
+  l->off_lin = off;
+  const int64_t lin_in = gdn::linear_workspace_bytes(batch, (int32_t)l->n_in, hidden);
+  const int64_t lin_out = gdn::linear_workspace_bytes(batch, hidden, (int32_t)l->vw);
+  l->total = off + (size_t)(lin_in > lin_out ? lin_in : lin_out);
+  return GDN_OK;
+}
+
+}  // namespace
+
+gdn_status gdn_decode_layer_workspace_size(const gdn_dims* dims, int32_t hidden, int32_t batch,
+                                           int64_t* bytes) {
+  if (bytes == nullptr) return GDN_ERR_INVALID_ARG;
+  *bytes = 0;
+  LayerLayout l{};
+  gdn_status st = layer_layout(dims, hidden, batch, &l);
+  if (st != GDN_OK) return st;
+  *bytes = (int64_t)l.total;
+  return GDN_OK;
+}
+
+gdn_status gdn_decode_layer(const gdn_dims* dims, int32_t hidden, int32_t batch, const void* x,
+                            const gdn_layer_weights* w, void* conv_state, float* state, void* y,
+                            void* workspace, int64_t workspace_bytes, void* stream) {
+  LayerLayout l{};
+  gdn_status st = layer_layout(dims, hidden, batch, &l);
+  if (st != GDN_OK) return st;
+  if (!x || !w || !y || !workspace || !w->w_in || !w->w_out) return GDN_ERR_INVALID_ARG;
+  if (workspace_bytes < (int64_t)l.total) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(w->w_in) || !aligned16(w->w_out) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      (w->b_in && (reinterpret_cast<uintptr_t>(w->b_in) & 3u)) ||
+      (w->b_out && (reinterpret_cast<uintptr_t>(w->b_out) & 3u)))
+    return GDN_ERR_ALIGN;
+  const int64_t Hv = dims->n_v_heads, D = dims->head_dim;
+  // the caller's buffers against the workspace and each other
+  const Range rws = range_of(workspace, (int64_t)l.total);
+  const Range ry = range_of(y, (int64_t)batch * hidden * 2);
+  const Range rx = range_of(x, (int64_t)batch * hidden * 2);
+  const Range rs = range_of(state, (int64_t)batch * Hv * D * D * 4);
+  const Range rc = range_of(conv_state, (int64_t)batch * l.C * 3 * 2);
+  const Range weights_r[] = {range_of(w->w_in, l.n_in * hidden * 2), range_of(w->b_in, w->b_in ? l.n_in * 4 : 0),
+                             range_of(w->w_out, (int64_t)hidden * l.vw * 2),
+                             range_of(w->b_out, w->b_out ? (int64_t)hidden * 4 : 0),
+                             range_of(w->conv_w, l.C * 4 * 2), range_of(w->decay_param, Hv * 4),
+                             range_of(w->dt_bias, Hv * 4), range_of(w->norm_w, D * 4)};
+  for (const Range& a : {rws, ry, rs, rc}) {
+    if (overlap(a, rx)) return GDN_ERR_ALIAS;
+    for (const Range& b : weights_r)
+      if (overlap(a, b)) return GDN_ERR_ALIAS;
+  }
+  if (overlap(rws, ry) || overlap(rws, rs) || overlap(rws, rc) || overlap(ry, rs) || overlap(ry, rc))
+    return GDN_ERR_ALIAS;
+  if (!gdn::linear_supported()) return GDN_ERR_UNSUPPORTED;
+  char* ws = static_cast<char*>(workspace);
+  void *qkv = ws + l.off_qkv, *z = ws + l.off_z, *bb = ws + l.off_b, *aa = ws + l.off_a, *yc = ws + l.off_y;
+  void* lin = ws + l.off_lin;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // (1) the fused input projection: qkv | z | b | a
+  gdn::LinearArgs pin{};
+  pin.M = batch;
+  pin.N = (int32_t)l.n_in;
+  pin.K = hidden;
+  pin.bias = w->b_in;
+  pin.route.count = 4;
+  pin.route.start[0] = 0;
+  pin.route.start[1] = (int32_t)l.C;
+  pin.route.start[2] = (int32_t)(l.C + l.vw);
+  pin.route.start[3] = (int32_t)(l.C + l.vw + Hv);
+  pin.route.start[4] = (int32_t)(l.C + l.vw + 2 * Hv);
+  pin.route.ld[0] = l.C;
+  pin.route.ld[1] = l.vw;
+  pin.route.ld[2] = Hv;
+  pin.route.ld[3] = Hv;
+  pin.route.dst[0] = qkv;
+  pin.route.dst[1] = z;
+  pin.route.dst[2] = bb;
+  pin.route.dst[3] = aa;
+  st = cuda_status(gdn::launch_linear(pin, x, hidden, w->w_in, lin, s));
+  if (st != GDN_OK) return st;
+  // (2) the core with its fused gated RMSNorm
+  st = decode_impl(dims, batch, 1, nullptr, batch, qkv, aa, bb, w->decay_param, w->dt_bias, w->conv_w,
+                   conv_state, state, nullptr, z, w->norm_w, yc, stream);
+  if (st != GDN_OK) return st;
+  // (3) the output projection
+  gdn::LinearArgs pout{};
+  pout.M = batch;
+  pout.N = hidden;
+  pout.K = (int32_t)l.vw;
+  pout.bias = w->b_out;
+  pout.route.count = 1;
+  pout.route.start[0] = 0;
+  pout.route.start[1] = hidden;
+  pout.route.ld[0] = hidden;
+  pout.route.dst[0] = y;
+  return cuda_status(gdn::launch_linear(pout, yc, l.vw, w->w_out, lin, s));
+}
+
 gdn_status gdn_selftest_wait_timeout(int64_t limit_ns, int32_t* gave_up, void* stream) {
   if (gave_up == nullptr || limit_ns < 1000 || limit_ns > 10000000000LL) return GDN_ERR_INVALID_ARG;
   return cuda_status(gdn::launch_wait_timeout((uint64_t)limit_ns, gave_up, static_cast<cudaStream_t>(stream)));
@@ -418,7 +587,8 @@ gdn_status gdn_device_error(int32_t* status, int32_t clear) {
                                                gdn::read_error_conv,
                                                gdn::read_error_rmsnorm, gdn::read_error_prefill,
                                                gdn::read_error_prefill_tc,
-                                               gdn::read_error_prefill_cp, gdn::read_error_diag};
+                                               gdn::read_error_prefill_cp, gdn::read_error_diag,
+                                               gdn::read_error_linear};
   for (auto rd : readers) {
     int32_t v = 0;
     if (rd(&v, clear != 0) != cudaSuccess) return GDN_ERR_CUDA;

@@ -33,6 +33,26 @@ struct DecodeArgs {
   float l2_eps, rms_eps, scale;
 };
 
+// Linear layer y = x W^T (+ bias) (linear.cu): output column n goes to
+// destination r with start[r] <= n < start[r + 1] (r < count), at
+// dst[r] + m * ld[r] + (n - start[r]); columns at or past start[count] are
+// not written. Starts, strides and destination addresses are multiples of 8
+// elements.
+constexpr int kLinearRoutes = 4;
+struct LinearRoute {
+  int32_t count;
+  int32_t start[kLinearRoutes + 1];
+  int64_t ld[kLinearRoutes];
+  void* dst[kLinearRoutes];
+};
+struct LinearArgs {
+  int32_t M, N, K, splits;  // splits is chosen by launch_linear
+  const float* bias;        // [N] or null
+  float* acc;               // split-K partial slices [splits][M][N] (set by launch_linear)
+  uint32_t* tickets;        // split-K tickets [N / 64] (set by launch_linear)
+  LinearRoute route;
+};
+
 struct ConvArgs {
   const int32_t* cu_seqlens;
   int32_t N;
@@ -105,6 +125,12 @@ cudaError_t read_error_prefill(int32_t* status, bool clear);
 cudaError_t read_error_prefill_tc(int32_t* status, bool clear);
 cudaError_t read_error_prefill_cp(int32_t* status, bool clear);
 cudaError_t read_error_diag(int32_t* status, bool clear);
+cudaError_t read_error_linear(int32_t* status, bool clear);
+// linear.cu: M <= 128, N and K multiples of 64, bf16
+int64_t linear_workspace_bytes(int32_t M, int32_t N, int32_t K);
+bool linear_supported();
+cudaError_t launch_linear(LinearArgs p, const void* x, int64_t x_stride, const void* w, void* workspace,
+                          cudaStream_t stream);
 // diag.cu: one warp's bounded wait on an mbarrier nothing arrives on
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int32_t* gave_up, cudaStream_t stream);
 

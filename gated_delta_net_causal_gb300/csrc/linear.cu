@@ -1,0 +1,251 @@
+// Linear layer y = x W^T (+ bias) on the 5th-generation tensor cores: the
+// projections around the core in a decode step (libmir-metal decode/mod.rs,
+// `build`: the qkv, gate, beta and alpha projections of the input and the
+// output projection, each a `Linear::forward`, matmul then bias).
+//
+// x [M][K] bf16 with M <= 128 rows (the batch), W [N][K] bf16 (one row per
+// output feature), fp32 accumulation in TMEM, bf16 out. At decode batch
+// sizes the work is bound by streaming W once: each CTA takes a band of 64
+// output features and streams its W rows (and the few x rows) through a TMA
+// ring, the x tile padded to the MMA's 128 rows by the tensor map's zero
+// fill. The output columns may be routed to up to four destinations (the
+// fused input projection writes qkv | z | b | a from one launch).
+//
+// Split-K for narrow outputs (few bands): grid.y splits the K steps; each
+// CTA stores its fp32 partial sums in a slice of its own, then takes a
+// ticket; the last CTA of a band (no CTA ever waits for another) adds the
+// slices in split order (so the result does not depend on which CTA ran
+// first), the bias, rounds and stores. The tickets are zeroed on the stream
+// before the launch.
+#include <cuda.h>
+#include <string.h>
+
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+#include "tc_common.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kLBM = 128;  // MMA rows (batch rows, zero-padded)
+constexpr int kLBN = 64;   // output features per CTA
+constexpr int kLBK = 64;   // K per stage (one 128-byte swizzle atom of bf16)
+constexpr int kLStages = 4;
+constexpr uint32_t kLATile = kLBM * kLBK * 2;    // 16 KB
+constexpr uint32_t kLWTile = kLBN * kLBK * 2;    // 8 KB
+constexpr uint32_t kLStage = kLATile + kLWTile;  // 24 KB, a multiple of 1024
+constexpr uint32_t kLSmem = kLStages * kLStage + 1024;
+constexpr int kLThreads = 128;  // warp 0 lane 0 loads, warp 1 issues MMAs, all four store
+constexpr int kLMaxSplits = 16;
+
+__global__ void __launch_bounds__(kLThreads, 2)
+    linear_kernel(const LinearArgs p, const __grid_constant__ CUtensorMap tm_x,
+                  const __grid_constant__ CUtensorMap tm_w) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t full[kLStages], empty[kLStages], done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort, s_last;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int band = blockIdx.x, n0 = band * kLBN;
+  const int nk = p.K / kLBK;
+  const int k_begin = (int)((int64_t)blockIdx.y * nk / p.splits);
+  const int k_end = (int)((int64_t)(blockIdx.y + 1) * nk / p.splits);
+
+  if (warp == 0) {
+    tc::tmem_alloc(&s_tmem, kLBN);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kLStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tb = s_tmem;
+  volatile int* abort_flag = &s_abort;
+  uint32_t n_loads = 0;
+
+  if (warp == 0 && lane == 0) {
+    // producer: stage i % S holds K step k_begin + i
+    for (int i = 0; k_begin + i < k_end; ++i) {
+      const int s = i % kLStages;
+      if (i >= kLStages && !mbar_wait_bounded(&empty[s], ((i / kLStages) - 1) & 1, abort_flag)) break;
+      mbar_arrive_expect_tx(&full[s], kLStage);
+      ++n_loads;
+      const int kx = (k_begin + i) * kLBK;
+      tc::tma_load_2d(sm + s * kLStage, &tm_x, kx, 0, &full[s]);
+      tc::tma_load_2d(sm + s * kLStage + kLATile, &tm_w, kx, n0, &full[s]);
+    }
+  } else if (warp == 1) {
+    const uint32_t id = tc::idesc(tc::kBF16, kLBM, kLBN);
+    const uint64_t d0 = tc::sdesc_sw128(smem_u32(sm));
+    bool ok = true;
+    for (int i = 0; k_begin + i < k_end; ++i) {
+      const int s = i % kLStages;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (i / kLStages) & 1, abort_flag));
+      if (!ok) break;
+      tc::fence_after_sync();
+      const uint64_t da = d0 + (uint64_t)((s * kLStage) >> 4);
+      const uint64_t dw = d0 + (uint64_t)((s * kLStage + kLATile) >> 4);
+#pragma unroll
+      for (int ks = 0; ks < kLBK / 16; ++ks)
+        tc::mma_f16_elect(tb, tc::sdesc_at(da, kLBM, ks), tc::sdesc_at(dw, kLBN, ks), id, i > 0 || ks > 0);
+      tc::mma_commit_elect(&empty[s]);
+    }
+    tc::mma_commit_elect(&done);
+  }
+
+  // epilogue: thread (warp w, lane) holds row m = 32 w + lane of the
+  // accumulator (TMEM lane m), 64 columns
+  const bool ok = mbar_wait_bounded(&done, 0, abort_flag) && !*abort_flag;
+  tc::fence_after_sync();
+  const int m = 32 * warp + lane;
+  float v[kLBN];
+  if (__all_sync(0xffffffffu, ok)) {
+#pragma unroll
+    for (int c = 0; c < kLBN / 16; ++c)
+      tc::tmem_ld16(tb + ((uint32_t)(32 * warp) << 16) + 16 * c, *reinterpret_cast<float(*)[16]>(v + 16 * c));
+    tc::tmem_wait_ld();
+  } else {
+#pragma unroll
+    for (int e = 0; e < kLBN; ++e) v[e] = 0.f;
+  }
+  bool final_rows = p.splits == 1;
+  if (p.splits > 1) {
+    // partial sums into this split's slice, then a ticket; the band's last
+    // CTA adds the slices back (past its own fence), in split order
+    const size_t slice = (size_t)p.M * p.N;
+    if (m < p.M) {
+      float4* prow = reinterpret_cast<float4*>(p.acc + blockIdx.y * slice + (size_t)m * p.N + n0);
+#pragma unroll
+      for (int c = 0; c < kLBN / 4; ++c) prow[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(p.tickets + band, 1u) == (unsigned)(p.splits - 1);
+    __syncthreads();
+    final_rows = s_last != 0;
+    if (final_rows) {
+      __threadfence();
+      if (m < p.M) {
+#pragma unroll
+        for (int e = 0; e < kLBN; ++e) v[e] = 0.f;
+        for (int sp = 0; sp < p.splits; ++sp) {
+          const float4* prow = reinterpret_cast<const float4*>(p.acc + sp * slice + (size_t)m * p.N + n0);
+#pragma unroll
+          for (int c = 0; c < kLBN / 4; ++c) {
+            const float4 a4 = __ldcg(prow + c);
+            v[4 * c] += a4.x;
+            v[4 * c + 1] += a4.y;
+            v[4 * c + 2] += a4.z;
+            v[4 * c + 3] += a4.w;
+          }
+        }
+      }
+    }
+  }
+  if (final_rows && m < p.M && !*abort_flag) {
+    // bias, one rounding, and the destination of each 8-column group
+#pragma unroll
+    for (int g8 = 0; g8 < kLBN / 8; ++g8) {
+      const int n = n0 + 8 * g8;
+      if (n >= p.route.start[p.route.count]) continue;  // padding columns
+      int r = 0;
+#pragma unroll
+      for (int q = 1; q < kLinearRoutes; ++q)
+        if (q < p.route.count && n >= p.route.start[q]) r = q;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = v[8 * g8 + e] + (p.bias != nullptr ? __ldg(p.bias + n + e) : 0.f);
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.route.dst[r]) + (size_t)m * p.route.ld[r] +
+                           (n - p.route.start[r]);
+      *reinterpret_cast<uint4*>(dst) = make_uint4(
+          (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[0])) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[1])) << 16),
+          (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[2])) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[3])) << 16),
+          (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[4])) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[5])) << 16),
+          (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[6])) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[7])) << 16));
+    }
+  }
+
+  // drain: every load this CTA issued has landed (the last one into each
+  // stage) and its MMAs completed, before TMEM is released
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0 && lane == 0) {
+    for (uint32_t s = 0; s < (uint32_t)kLStages && s < n_loads; ++s) {
+      const uint32_t uses = (n_loads - s + kLStages - 1) / kLStages;  // loads into stage s
+      mbar_wait(&full[s], (uses - 1) & 1);
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tb, kLBN);
+  }
+}
+
+int sm_count_linear() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+}  // namespace
+
+static int max_splits(int32_t K) {
+  const int half = K / kLBK / 2;  // each split at least two K steps
+  return half < 1 ? 1 : (half < kLMaxSplits ? half : kLMaxSplits);
+}
+
+int64_t linear_workspace_bytes(int32_t M, int32_t N, int32_t K) {
+  // the split-K partial slices and one ticket per band, 256-byte aligned
+  return ((int64_t)max_splits(K) * M * N * 4 + 255) / 256 * 256 + ((int64_t)(N / kLBN) * 4 + 255) / 256 * 256;
+}
+
+bool linear_supported() { return tc::encode_fn() != nullptr; }
+
+cudaError_t launch_linear(LinearArgs p, const void* x, int64_t x_stride, const void* w, void* workspace,
+                          cudaStream_t stream) {
+  if (p.M == 0 || p.N == 0) return cudaSuccess;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap mx, mw;
+  if (!tc::make_map_2d(&mx, x, p.M, p.K, x_stride, 2, bf, kLBK, kLBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::make_map_2d(&mw, w, p.N, p.K, p.K, 2, bf, kLBK, kLBN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  const int bands = p.N / kLBN;
+  // as many K splits as keep two CTAs per SM busy (each at least two K
+  // steps, at most kLMaxSplits)
+  int splits = (2 * sm_count_linear()) / bands;
+  if (splits > max_splits(p.K)) splits = max_splits(p.K);
+  if (splits < 1) splits = 1;
+  p.splits = splits;
+  if (splits > 1) {
+    const size_t part_bytes = ((size_t)max_splits(p.K) * p.M * p.N * 4 + 255) / 256 * 256;
+    p.acc = static_cast<float*>(workspace);
+    p.tickets = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + part_bytes);
+    cudaError_t e = cudaMemsetAsync(p.tickets, 0, (size_t)bands * 4, stream);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLSmem);
+  if (e != cudaSuccess) return e;
+  linear_kernel<<<dim3((unsigned)bands, (unsigned)splits), kLThreads, kLSmem, stream>>>(p, mx, mw);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn
+
+GDN_DEFINE_ERROR_READER(linear)

@@ -324,6 +324,91 @@ gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, int64_t rows, const float* o,
                              const float* norm_w, void* y, void* stream);
 
 /*
+ * Linear layer y = x W^T (+ bias), bf16 in and out, fp32 accumulation, on
+ * the tensor cores: the projections around the core in a decode layer.
+ * -- libmir-metal decode/mod.rs, `Linear::forward` (matmul, then bias) and
+ *    `build` (the qkv, gate, beta, alpha and output projections).
+ *
+ * M            rows of x and y, 1 <= M <= 128 (the decode batch).
+ * N, K         output and input features, positive multiples of 64.
+ * x            [M][x_stride] bf16, row m at x + m * x_stride (x_stride >= K,
+ *              a multiple of 8); 16-byte aligned.
+ * w            [N][K] bf16 row-major (one row per output feature); 16-byte
+ *              aligned.
+ * bias         [N] fp32 added before the one rounding to bf16, or NULL.
+ * y            [M][y_stride] bf16 (y_stride >= N, a multiple of 8); must not
+ *              overlap x, w, bias or the workspace.
+ * workspace    device scratch of gdn_linear_workspace_size bytes, 256-byte
+ *              aligned, contents irrelevant (the part that needs it is
+ *              zeroed on the stream by the call).
+ *
+ * Errors: GDN_ERR_INVALID_ARG (sizes, NULL pointers, strides),
+ * GDN_ERR_ALIGN, GDN_ERR_ALIAS, GDN_ERR_UNSUPPORTED (no TMA encoder in the
+ * driver), GDN_ERR_CUDA.
+ */
+gdn_status gdn_linear(int32_t M, int32_t N, int32_t K, const void* x, int64_t x_stride,
+                      const void* w, const float* bias, void* y, int64_t y_stride,
+                      void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Workspace bytes gdn_linear needs for M, N, K: fp32 [M][N] partial sums
+ * for each of up to min(16, K / 128) K splits and one 4-byte ticket per 64
+ * output features, each part rounded up to 256 bytes. The result does not
+ * depend on the order in which the splits finish. */
+gdn_status gdn_linear_workspace_size(int32_t M, int32_t N, int32_t K, int64_t* bytes);
+
+/*
+ * Weights of one layer for gdn_decode_layer. With C = (2 Hk + Hv) D and
+ * N_in = C + Hv D + 2 Hv rounded up to a multiple of 64:
+ * w_in         [N_in][hidden] bf16: rows 0..C-1 the qkv projection, the next
+ *              Hv D rows the gate (z) projection, then Hv rows the beta (b)
+ *              and Hv rows the alpha (a) projection; padding rows unused.
+ * b_in         [N_in] fp32 bias of those rows, or NULL.
+ * w_out        [hidden][Hv D] bf16, the output projection; b_out [hidden]
+ *              fp32 or NULL.
+ * conv_w, decay_param, dt_bias, norm_w  as in gdn_decode_step.
+ */
+typedef struct gdn_layer_weights {
+  const void* w_in;
+  const float* b_in;
+  const void* w_out;
+  const float* b_out;
+  const void* conv_w;
+  const float* decay_param;
+  const float* dt_bias;
+  const float* norm_w;
+} gdn_layer_weights;
+
+/*
+ * One decode step of a whole gated delta-net layer for a batch of
+ * sequences, one token each: the fused input projection (qkv | z | b | a in
+ * one gdn_linear launch), gdn_decode_step with its fused gated RMSNorm, and
+ * the output projection. Three kernel launches (plus the split-K zeroing of
+ * the output projection's accumulator).
+ * -- libmir-metal decode/mod.rs, `build`: qkv projection -> `convolve` ->
+ *    `split_qkv` -> gate/beta/alpha projections -> `recurrence` ->
+ *    `rms_norm` -> `precise_gate` -> output projection.
+ *
+ * dims         io_dtype GDN_BF16; Hv D a multiple of 64; Hv/Hk <= 8.
+ * hidden       model width, a positive multiple of 64.
+ * batch        1 <= batch <= 128.
+ * x            [batch][hidden] bf16 layer input.
+ * conv_state   [batch][C][3] bf16, state [batch][Hv][D][D] fp32, in place.
+ * y            [batch][hidden] bf16 layer output.
+ * workspace    gdn_decode_layer_workspace_size bytes, 256-byte aligned, not
+ *              overlapping any other argument; contents irrelevant.
+ * Errors as gdn_linear and gdn_decode_step.
+ */
+gdn_status gdn_decode_layer(const gdn_dims* dims, int32_t hidden, int32_t batch, const void* x,
+                            const gdn_layer_weights* weights, void* conv_state, float* state,
+                            void* y, void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Workspace bytes of gdn_decode_layer: the projections' bf16 outputs (qkv,
+ * z, b, a and the gated core output, [batch] rows each) and gdn_linear's
+ * workspace for the larger of its two calls, each rounded up to 256 bytes. */
+gdn_status gdn_decode_layer_workspace_size(const gdn_dims* dims, int32_t hidden, int32_t batch,
+                                           int64_t* bytes);
+
+/*
  * Device-side error word: kernels whose bounded waits give up record a
  * status here instead of hanging. Reads it (synchronising the device) into
  * *status and, when clear != 0, resets it to GDN_OK.

@@ -273,7 +273,53 @@ def prefill_core(Hk: int, Hv: int, D: int, map_: int, q, k, v, g, beta, S, cu_se
     return o, S
 
 
+def round_bf16(x) -> np.ndarray:
+    """Round to the nearest bf16 value (ties to even), via float32: the cast
+    the page's Linear applies to its output (`astype` to the input dtype)."""
+    f = np.ascontiguousarray(_f64(x), dtype=np.float64).astype(np.float32)
+    bits = f.view(np.uint32).astype(np.uint64)
+    rounded = (bits + 0x7FFF + ((bits >> 16) & 1)) & 0xFFFF0000
+    return rounded.astype(np.uint32).view(np.float32).astype(np.float64).reshape(np.shape(x))
+
+
+def linear(x, w, bias=None, round_out: bool = True) -> np.ndarray:
+    """y = x w^T (+ bias), the page's `Linear::forward` (libmir-metal
+    decode/mod.rs): a matmul in fp64 (a library routine), the bias, then one
+    rounding to bf16 (reading: the bias joins before the single cast)."""
+    y = _f64(x) @ _f64(w).T
+    if bias is not None:
+        y = y + _f64(bias)
+    return round_bf16(y) if round_out else y
+
+
+def decode_layer(Hk: int, Hv: int, D: int, map_: int, decay: int, x, w_in, b_in, w_out, b_out, conv_w,
+                 decay_param, dt_bias, norm_w, conv_state, S, l2_eps: float = 1e-6,
+                 rms_eps: float = 1e-6):
+    """One decode step of a layer, in the page's order (libmir-metal
+    decode/mod.rs, `build`): the qkv, gate, beta and alpha projections of
+    the input x [B][hidden] (rows of w_in: qkv | z | b | a), each rounded to
+    bf16; per sequence the core (O6 with its gated RMSNorm), its output
+    rounded to bf16; the output projection, rounded to bf16. Returns
+    (y [B][hidden], conv_state, S, y_core [B][Hv][D])."""
+    x = _f64(x)
+    B = x.shape[0]
+    C = (2 * Hk + Hv) * D
+    vw = Hv * D
+    proj = linear(x, w_in[:C + vw + 2 * Hv], None if b_in is None else _f64(b_in)[:C + vw + 2 * Hv])
+    qkv, z = proj[:, :C], proj[:, C:C + vw]
+    bb, aa = proj[:, C + vw:C + vw + Hv], proj[:, C + vw + Hv:C + vw + 2 * Hv]
+    cs, St = _f64(conv_state).copy(), _f64(S).copy()
+    yc = np.zeros((B, Hv, D))
+    for n in range(B):
+        _, y, cs[n], St[n] = segment(Hk, Hv, D, map_, decay, qkv[n:n + 1], aa[n:n + 1], bb[n:n + 1],
+                                     z[n:n + 1], conv_w, decay_param, dt_bias, norm_w, cs[n], St[n],
+                                     l2_eps=l2_eps, rms_eps=rms_eps)
+        yc[n] = round_bf16(y[0])
+    out = linear(yc.reshape(B, vw), w_out, b_out)
+    return out, cs, St, yc
+
+
 __all__ = ["build", "lib", "sigmoid", "silu", "softplus", "k_head", "conv", "conv_varlen",
            "l2norm", "gates", "delta", "delta_chunked", "delta_affine", "chunk_factors",
            "delta_bruteforce", "gated_rmsnorm",
-           "segment", "prefill_core", "GROUPED", "TILED", "LOG_RATE", "NEGATIVE_RATE"]
+           "segment", "prefill_core", "round_bf16", "linear", "decode_layer", "GROUPED", "TILED", "LOG_RATE", "NEGATIVE_RATE"]

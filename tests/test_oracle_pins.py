@@ -221,3 +221,64 @@ def test_segment_composes_the_steps():
     assert np.array_equal(core, o)
     assert np.array_equal(S1, Sr)
     assert np.array_equal(y, oracle.gated_rmsnorm(o, z, nw))
+
+
+# ------------------------------------------------------------- decode layer
+
+def test_round_bf16_against_torch_and_ties():
+    """round_bf16 agrees with torch's own float -> bfloat16 conversion (a
+    library routine) on random values of every scale, and rounds the exact
+    ties to even."""
+    import torch
+    rng = np.random.default_rng(7)
+    x = rng.normal(size=4000) * np.exp(rng.uniform(-30, 30, size=4000))
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.round_bf16(x), ref)
+    one_ulp = 2.0 ** -7
+    assert oracle.round_bf16(1.0 + one_ulp / 2) == 1.0                   # tie, even below
+    assert oracle.round_bf16(1.0 + 1.5 * one_ulp) == 1.0 + 2 * one_ulp   # tie, even above
+    assert oracle.round_bf16(1.0 + 0.75 * one_ulp) == 1.0 + one_ulp
+
+
+def test_linear_against_a_brute_force_sum():
+    """linear = an fsum triple loop (bias added, one rounding) on small
+    random shapes; without rounding it is the exact fp64 sum of products."""
+    rng = np.random.default_rng(11)
+    x = oracle.round_bf16(rng.normal(size=(3, 20)))
+    w = oracle.round_bf16(rng.normal(size=(7, 20)))
+    bias = rng.normal(size=7)
+    exact = np.array([[math.fsum([x[m, k] * w[n, k] for k in range(20)] + [bias[n]]) for n in range(7)]
+                      for m in range(3)])
+    assert np.allclose(oracle.linear(x, w, bias, round_out=False), exact, rtol=1e-15, atol=1e-15)
+    assert np.array_equal(oracle.linear(x, w, bias), oracle.round_bf16(exact))
+
+
+def test_decode_layer_with_selection_weights_is_the_segment():
+    """With input weights that copy given bf16 values of qkv, z, b, a out of
+    the input (one 1 per row) and an output projection that copies the gated
+    core output, the layer is O6 (already pinned) plus the bf16 roundings."""
+    Hk, Hv, D = 2, 4, 32
+    C, vw = (2 * Hk + Hv) * D, Hv * D
+    n = C + vw + 2 * Hv
+    hidden = n
+    rng = np.random.default_rng(5)
+    B = 2
+    x = oracle.round_bf16(rng.normal(size=(B, hidden)) * 0.5)
+    w_in = np.eye(n)  # row r picks input feature r
+    w_out = np.zeros((vw, vw))
+    w_out[np.arange(vw), np.arange(vw)] = 1.0
+    conv_w = rng.normal(size=(C, 4)) * 0.3
+    dp, dt = rng.normal(size=Hv) * 0.2 - 1.0, rng.normal(size=Hv) * 0.1
+    nw = rng.normal(size=D) * 0.1 + 1.0
+    cs0 = rng.normal(size=(B, C, 3)) * 0.1
+    S0 = rng.normal(size=(B, Hv, D, D)) * 0.02
+    out, cs, S, yc = oracle.decode_layer(Hk, Hv, D, oracle.GROUPED, oracle.LOG_RATE, x, w_in, None, w_out,
+                                         None, conv_w, dp, dt, nw, cs0, S0)
+    for b in range(B):
+        core, y, cs_b, S_b = oracle.segment(Hk, Hv, D, oracle.GROUPED, oracle.LOG_RATE, x[b:b + 1, :C],
+                                            x[b:b + 1, C + vw + Hv:C + vw + 2 * Hv],
+                                            x[b:b + 1, C + vw:C + vw + Hv], x[b:b + 1, C:C + vw], conv_w, dp,
+                                            dt, nw, cs0[b], S0[b])
+        assert np.array_equal(yc[b], oracle.round_bf16(y[0]))
+        assert np.array_equal(out[b], oracle.round_bf16(yc[b].reshape(-1)))
+        assert np.array_equal(cs[b], cs_b) and np.array_equal(S[b], S_b)
