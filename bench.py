@@ -363,6 +363,7 @@ def run_gpu(args, ws, rank, local):
     prefill = run_prefill(args, peaks, ws) if not args.no_prefill else None
     varlen = run_varlen(args, ws, peaks) if not args.no_prefill else None
     batch1 = run_batch1(args, ws) if not args.no_prefill else None
+    layer = run_decode_layer(args, ws, peaks) if not args.no_extra else None
     multilayer = run_multilayer(args, ws, peaks) if not args.no_multilayer else None
     slot_dec = run_slot_decode(args, ws, peaks) if not args.no_extra else None
     multi_dec = run_multi_decode(args, ws, peaks) if not args.no_extra else None
@@ -433,6 +434,8 @@ def run_gpu(args, ws, rank, local):
         line["varlen_path"] = varlen
     if batch1 is not None:
         line["batch1_layer"] = batch1
+    if layer is not None:
+        line["decode_layer"] = layer
     if multilayer is not None:
         line["multilayer_decode"] = multilayer
     if slot_dec is not None:
@@ -722,6 +725,100 @@ def run_batch1(args, ws):
             "timing": "median of 20 passes between CUDA events, states reset before each; the "
                       "split pass is conv update + chunked prefill (3 tokens, the single-pass "
                       "kernel for f16) + one decode step"}
+
+
+def run_decode_layer(args, ws, peaks):
+    """The whole decode layer on synthetic bf16 weights (gdn_decode_layer:
+    fused input projection, decode step with gated RMSNorm, output
+    projection): Hk=16, Hv=32, D=128, hidden 2048, Grouped, log-rate, at
+    B=64 and B=1. Weight and state sets are cycled so that each step's
+    bytes are not in L2 from the step before (sets x (weights + state) >=
+    256 MB); the K steps run as one CUDA graph. The two projections are also
+    timed alone (gdn_linear, same cycling) for their weight-streaming rate."""
+    import gated_delta_net_causal_gb300 as gdn
+    Hk, Hv, D, hidden = 16, 32, 128, 2048
+    shape = gi.Shape(Hk, Hv, D, map=gi.GROUPED, decay=gi.LOG_RATE, dtype="bf16")
+    C, vw = shape.qkv_features, Hv * D
+    n_in = (C + vw + 2 * Hv + 63) // 64 * 64
+    d = gdn.dims(Hk, Hv, D, map=shape.map, decay=shape.decay, io_dtype=torch.bfloat16)
+    g = gi.rng(gi.SEED_BASE + 77)
+    wts = gi.layer_weights(g, shape)
+    cw, dp, dt, nw = (getattr(wts, n).cuda() for n in ("conv_w", "decay_param", "dt_bias", "norm_w"))
+    w_bytes = (n_in * hidden + hidden * vw) * 2
+    stream = torch.cuda.current_stream()
+    res = {"workload": "decode layer on synthetic bf16 weights: hidden 2048, Hk=16 Hv=32 D=128, "
+                       "Grouped, log-rate; fused qkv|z|b|a projection, decode step with gated "
+                       "RMSNorm, output projection",
+           "unit": "us per layer step", "weight_bytes": w_bytes}
+    for B in (64, 1):
+        state_b = B * Hv * D * D * 4
+        nsets = max(2, -(-256 * 2**20 // (w_bytes + state_b)))
+        sets = []
+        for _ in range(nsets):
+            sets.append(dict(
+                w_in=gi.to_dtype(gi.normal(g, (n_in, hidden), hidden ** -0.5), "bf16").cuda(),
+                w_out=gi.to_dtype(gi.normal(g, (hidden, vw), vw ** -0.5), "bf16").cuda(),
+                cs=gi.to_dtype(gi.normal(g, (B, C, 3), 0.1), "bf16").cuda(),
+                st=gi.delta_state(g, shape, B, std=0.02).cuda()))
+        xs = [gi.to_dtype(gi.normal(g, (B, hidden), 1.0), "bf16").cuda() for _ in range(4)]
+        y = torch.empty((B, hidden), device="cuda", dtype=torch.bfloat16)
+        wsb = torch.empty(gdn.gdn_decode_layer_workspace_size(d, hidden, B), device="cuda",
+                          dtype=torch.uint8)
+        lin_ws = torch.empty(max(gdn.gdn_linear_workspace_size(B, n_in, hidden),
+                                 gdn.gdn_linear_workspace_size(B, hidden, vw)), device="cuda",
+                             dtype=torch.uint8)
+        proj = torch.empty((B, n_in), device="cuda", dtype=torch.bfloat16)
+        yc = torch.empty((B, vw), device="cuda", dtype=torch.bfloat16)
+
+        def step(i):
+            st = sets[i % nsets]
+            gdn.gdn_decode_layer(d, xs[i % 4], st["w_in"], st["w_out"], cw, dp, dt, nw, st["cs"],
+                                 st["st"], y, workspace=wsb)
+
+        def lin_in(i):
+            gdn.gdn_linear(xs[i % 4], sets[i % nsets]["w_in"], proj, workspace=lin_ws)
+
+        def lin_out(i):
+            gdn.gdn_linear(yc, sets[i % nsets]["w_out"], y, workspace=lin_ws)
+
+        def graph_time(fn, k=16):
+            for i in range(3):
+                fn(i)
+            torch.cuda.synchronize()
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(gr, stream=side):
+                    for i in range(k):
+                        fn(i)
+            stream.wait_stream(side)
+            gr.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gr.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return _barrier_max(e0.elapsed_time(e1) * 1e-3 / k, ws)
+
+        t_layer = graph_time(step)
+        t_in, t_out = graph_time(lin_in), graph_time(lin_out)
+        step_bytes = w_bytes + 2 * state_b + 2 * B * C * 3 * 2
+        res[f"B{B}"] = {
+            "us_per_step": round(t_layer * 1e6, 2),
+            "bytes_per_step": step_bytes,
+            "gbs": round(step_bytes / t_layer / 1e9, 1),
+            "hbm_frac": round(step_bytes / t_layer / 1e9 / peaks["hbm_gbs"], 4),
+            "in_projection_us": round(t_in * 1e6, 2),
+            "in_projection_weight_gbs": round(n_in * hidden * 2 / t_in / 1e9, 1),
+            "out_projection_us": round(t_out * 1e6, 2),
+            "out_projection_weight_gbs": round(hidden * vw * 2 / t_out / 1e9, 1),
+            "launches_per_step": 4, "weight_sets_cycled": nsets,
+            "timing": "16 consecutive steps as one CUDA graph replay between two CUDA events"}
+        del sets, wsb, lin_ws
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_multilayer(args, ws, peaks):

@@ -46,7 +46,7 @@ struct LinearRoute {
   void* dst[kLinearRoutes];
 };
 struct LinearArgs {
-  int32_t M, N, K, splits;  // splits is chosen by launch_linear
+  int32_t M, N, K, splits, stages;  // splits and stages are chosen by launch_linear
   const float* bias;        // [N] or null
   float* acc;               // split-K partial slices [splits][M][N] (set by launch_linear)
   uint32_t* tickets;        // split-K tickets [N / 64] (set by launch_linear)

@@ -6,9 +6,10 @@
 // x [M][K] bf16 with M <= 128 rows (the batch), W [N][K] bf16 (one row per
 // output feature), fp32 accumulation in TMEM, bf16 out. At decode batch
 // sizes the work is bound by streaming W once: each CTA takes a band of 64
-// output features and streams its W rows (and the few x rows) through a TMA
-// ring, the x tile padded to the MMA's 128 rows by the tensor map's zero
-// fill. The output columns may be routed to up to four destinations (the
+// output features and streams its W rows (and the M rows of x) through a TMA
+// ring. The MMA always spans 128 rows; rows past M of the x tile hold
+// whatever the buffer held and only reach accumulator rows that are never
+// stored. The output columns may be routed to up to four destinations (the
 // fused input projection writes qkv | z | b | a from one launch).
 //
 // Split-K for narrow outputs (few bands): grid.y splits the K steps; each
@@ -27,38 +28,45 @@
 namespace gdn {
 namespace {
 
-constexpr int kLBM = 128;  // MMA rows (batch rows, zero-padded)
+constexpr int kLBM = 128;  // MMA rows (batch rows; the x tile holds M of them)
 constexpr int kLBN = 64;   // output features per CTA
 constexpr int kLBK = 64;   // K per stage (one 128-byte swizzle atom of bf16)
-constexpr int kLStages = 4;
-constexpr uint32_t kLATile = kLBM * kLBK * 2;    // 16 KB
-constexpr uint32_t kLWTile = kLBN * kLBK * 2;    // 8 KB
-constexpr uint32_t kLStage = kLATile + kLWTile;  // 24 KB, a multiple of 1024
-constexpr uint32_t kLSmem = kLStages * kLStage + 1024;
+constexpr uint32_t kLWTile = kLBN * kLBK * 2;  // 8 KB
+// A stage is the x tile (M rounded up to 8 rows of 128 bytes, so a multiple
+// of 1024 bytes) then the W tile; as many stages as fit in 96 KB, two CTAs
+// per SM. The MMA reads 128 rows of x from
+// each stage's start, so the allocation ends 128 x 128 bytes past the last
+// stage's start at least (the rows past M it reads are never used).
+constexpr int kLMaxStages = 12;
+constexpr uint32_t kLStageBudget = 96 * 1024;
+constexpr int kLCtasPerSm = 2;
 constexpr int kLThreads = 128;  // warp 0 lane 0 loads, warp 1 issues MMAs, all four store
 constexpr int kLMaxSplits = 16;
 
-__global__ void __launch_bounds__(kLThreads, 2)
+__global__ void __launch_bounds__(kLThreads, kLCtasPerSm)
     linear_kernel(const LinearArgs p, const __grid_constant__ CUtensorMap tm_x,
                   const __grid_constant__ CUtensorMap tm_w) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) uint64_t full[kLStages], empty[kLStages], done;
+  __shared__ __align__(8) uint64_t full[kLMaxStages], empty[kLMaxStages], done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort, s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int band = blockIdx.x, n0 = band * kLBN;
+  const int stages = p.stages;
+  const uint32_t x_tile = (uint32_t)((p.M + 7) / 8) * 1024, stage_bytes = x_tile + kLWTile;
   const int nk = p.K / kLBK;
   const int k_begin = (int)((int64_t)blockIdx.y * nk / p.splits);
   const int k_end = (int)((int64_t)(blockIdx.y + 1) * nk / p.splits);
+  const int k_len = k_end - k_begin;
 
   if (warp == 0) {
     tc::tmem_alloc(&s_tmem, kLBN);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int s = 0; s < kLStages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -75,26 +83,26 @@ __global__ void __launch_bounds__(kLThreads, 2)
 
   if (warp == 0 && lane == 0) {
     // producer: stage i % S holds K step k_begin + i
-    for (int i = 0; k_begin + i < k_end; ++i) {
-      const int s = i % kLStages;
-      if (i >= kLStages && !mbar_wait_bounded(&empty[s], ((i / kLStages) - 1) & 1, abort_flag)) break;
-      mbar_arrive_expect_tx(&full[s], kLStage);
+    for (int i = 0; i < k_len; ++i) {
+      const int s = i % stages;
+      if (i >= stages && !mbar_wait_bounded(&empty[s], ((i / stages) - 1) & 1, abort_flag)) break;
+      mbar_arrive_expect_tx(&full[s], (uint32_t)p.M * (kLBK * 2) + kLWTile);
       ++n_loads;
       const int kx = (k_begin + i) * kLBK;
-      tc::tma_load_2d(sm + s * kLStage, &tm_x, kx, 0, &full[s]);
-      tc::tma_load_2d(sm + s * kLStage + kLATile, &tm_w, kx, n0, &full[s]);
+      tc::tma_load_2d(sm + s * stage_bytes, &tm_x, kx, 0, &full[s]);
+      tc::tma_load_2d(sm + s * stage_bytes + x_tile, &tm_w, kx, n0, &full[s]);
     }
   } else if (warp == 1) {
     const uint32_t id = tc::idesc(tc::kBF16, kLBM, kLBN);
     const uint64_t d0 = tc::sdesc_sw128(smem_u32(sm));
     bool ok = true;
-    for (int i = 0; k_begin + i < k_end; ++i) {
-      const int s = i % kLStages;
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (i / kLStages) & 1, abort_flag));
+    for (int i = 0; i < k_len; ++i) {
+      const int s = i % stages;
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (i / stages) & 1, abort_flag));
       if (!ok) break;
       tc::fence_after_sync();
-      const uint64_t da = d0 + (uint64_t)((s * kLStage) >> 4);
-      const uint64_t dw = d0 + (uint64_t)((s * kLStage + kLATile) >> 4);
+      const uint64_t da = d0 + (uint64_t)((s * stage_bytes) >> 4);
+      const uint64_t dw = d0 + (uint64_t)((s * stage_bytes + x_tile) >> 4);
 #pragma unroll
       for (int ks = 0; ks < kLBK / 16; ++ks)
         tc::mma_f16_elect(tb, tc::sdesc_at(da, kLBM, ks), tc::sdesc_at(dw, kLBN, ks), id, i > 0 || ks > 0);
@@ -118,10 +126,34 @@ __global__ void __launch_bounds__(kLThreads, 2)
 #pragma unroll
     for (int e = 0; e < kLBN; ++e) v[e] = 0.f;
   }
-  bool final_rows = p.splits == 1;
-  if (p.splits > 1) {
+  // bias, one rounding, and the destination of an 8-column group of row m
+  auto store8 = [&](int m, int g8, const float* x8) {
+    const int n = n0 + 8 * g8;
+    if (n >= p.route.start[p.route.count]) return;  // padding columns
+    int r = 0;
+#pragma unroll
+    for (int q = 1; q < kLinearRoutes; ++q)
+      if (q < p.route.count && n >= p.route.start[q]) r = q;
+    uint32_t w4[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float b0 = p.bias != nullptr ? __ldg(p.bias + n + 2 * e) : 0.f;
+      const float b1 = p.bias != nullptr ? __ldg(p.bias + n + 2 * e + 1) : 0.f;
+      w4[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x8[2 * e] + b0)) |
+              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x8[2 * e + 1] + b1)) << 16);
+    }
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.route.dst[r]) + (size_t)m * p.route.ld[r] +
+                         (n - p.route.start[r]);
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  };
+  if (p.splits == 1) {
+    if (m < p.M && !*abort_flag)
+#pragma unroll
+      for (int g8 = 0; g8 < kLBN / 8; ++g8) store8(m, g8, v + 8 * g8);
+  } else {
     // partial sums into this split's slice, then a ticket; the band's last
-    // CTA adds the slices back (past its own fence), in split order
+    // CTA adds the slices (past its own fence) in split order, every thread
+    // taking (row, 8-column group) units
     const size_t slice = (size_t)p.M * p.N;
     if (m < p.M) {
       float4* prow = reinterpret_cast<float4*>(p.acc + blockIdx.y * slice + (size_t)m * p.N + n0);
@@ -132,50 +164,23 @@ __global__ void __launch_bounds__(kLThreads, 2)
     __syncthreads();
     if (tid == 0) s_last = atomicAdd(p.tickets + band, 1u) == (unsigned)(p.splits - 1);
     __syncthreads();
-    final_rows = s_last != 0;
-    if (final_rows) {
+    if (s_last && !*abort_flag) {
       __threadfence();
-      if (m < p.M) {
+      for (int u = tid; u < p.M * (kLBN / 8); u += kLThreads) {
+        const int um = u >> 3, g8 = u & 7;
+        const float* base = p.acc + (size_t)um * p.N + n0 + 8 * g8;
+        float x8[8];
 #pragma unroll
-        for (int e = 0; e < kLBN; ++e) v[e] = 0.f;
+        for (int e = 0; e < 8; ++e) x8[e] = 0.f;
+#pragma unroll 4
         for (int sp = 0; sp < p.splits; ++sp) {
-          const float4* prow = reinterpret_cast<const float4*>(p.acc + sp * slice + (size_t)m * p.N + n0);
-#pragma unroll
-          for (int c = 0; c < kLBN / 4; ++c) {
-            const float4 a4 = __ldcg(prow + c);
-            v[4 * c] += a4.x;
-            v[4 * c + 1] += a4.y;
-            v[4 * c + 2] += a4.z;
-            v[4 * c + 3] += a4.w;
-          }
+          const float4 a0 = __ldcg(reinterpret_cast<const float4*>(base + sp * slice));
+          const float4 a1 = __ldcg(reinterpret_cast<const float4*>(base + sp * slice) + 1);
+          x8[0] += a0.x, x8[1] += a0.y, x8[2] += a0.z, x8[3] += a0.w;
+          x8[4] += a1.x, x8[5] += a1.y, x8[6] += a1.z, x8[7] += a1.w;
         }
+        store8(um, g8, x8);
       }
-    }
-  }
-  if (final_rows && m < p.M && !*abort_flag) {
-    // bias, one rounding, and the destination of each 8-column group
-#pragma unroll
-    for (int g8 = 0; g8 < kLBN / 8; ++g8) {
-      const int n = n0 + 8 * g8;
-      if (n >= p.route.start[p.route.count]) continue;  // padding columns
-      int r = 0;
-#pragma unroll
-      for (int q = 1; q < kLinearRoutes; ++q)
-        if (q < p.route.count && n >= p.route.start[q]) r = q;
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = v[8 * g8 + e] + (p.bias != nullptr ? __ldg(p.bias + n + e) : 0.f);
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.route.dst[r]) + (size_t)m * p.route.ld[r] +
-                           (n - p.route.start[r]);
-      *reinterpret_cast<uint4*>(dst) = make_uint4(
-          (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[0])) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[1])) << 16),
-          (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[2])) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[3])) << 16),
-          (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[4])) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[5])) << 16),
-          (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[6])) |
-              ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[7])) << 16));
     }
   }
 
@@ -184,8 +189,8 @@ __global__ void __launch_bounds__(kLThreads, 2)
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0 && lane == 0) {
-    for (uint32_t s = 0; s < (uint32_t)kLStages && s < n_loads; ++s) {
-      const uint32_t uses = (n_loads - s + kLStages - 1) / kLStages;  // loads into stage s
+    for (uint32_t s = 0; s < (uint32_t)stages && s < n_loads; ++s) {
+      const uint32_t uses = (n_loads - s + stages - 1) / stages;  // loads into stage s
       mbar_wait(&full[s], (uses - 1) & 1);
     }
   }
@@ -223,13 +228,14 @@ cudaError_t launch_linear(LinearArgs p, const void* x, int64_t x_stride, const v
   if (p.M == 0 || p.N == 0) return cudaSuccess;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap mx, mw;
-  if (!tc::make_map_2d(&mx, x, p.M, p.K, x_stride, 2, bf, kLBK, kLBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc::make_map_2d(&mw, w, p.N, p.K, p.K, 2, bf, kLBK, kLBN, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!tc::make_map_2d(&mx, x, p.M, p.K, x_stride, 2, bf, kLBK, (uint32_t)p.M, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::make_map_2d(&mw, w, p.N, p.K, p.K, 2, bf, kLBK, kLBN, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
     return cudaErrorInvalidValue;
   const int bands = p.N / kLBN;
-  // as many K splits as keep two CTAs per SM busy (each at least two K
-  // steps, at most kLMaxSplits)
-  int splits = (2 * sm_count_linear()) / bands;
+  // as many K splits as keep every CTA slot of the SMs busy in one wave
+  // (each split at least two K steps, at most kLMaxSplits)
+  int splits = (kLCtasPerSm * sm_count_linear()) / bands;
   if (splits > max_splits(p.K)) splits = max_splits(p.K);
   if (splits < 1) splits = 1;
   p.splits = splits;
@@ -240,9 +246,14 @@ cudaError_t launch_linear(LinearArgs p, const void* x, int64_t x_stride, const v
     cudaError_t e = cudaMemsetAsync(p.tickets, 0, (size_t)bands * 4, stream);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kLSmem);
+  const uint32_t stage_bytes = (uint32_t)((p.M + 7) / 8) * 1024 + kLWTile;
+  int stages = (int)(kLStageBudget / stage_bytes);
+  p.stages = stages < kLMaxStages ? (stages < 2 ? 2 : stages) : kLMaxStages;
+  const uint32_t x_tile = stage_bytes - kLWTile;
+  const uint32_t smem = (uint32_t)p.stages * stage_bytes + (kLBM * 128 - (x_tile < kLBM * 128 ? x_tile : kLBM * 128)) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  linear_kernel<<<dim3((unsigned)bands, (unsigned)splits), kLThreads, kLSmem, stream>>>(p, mx, mw);
+  linear_kernel<<<dim3((unsigned)bands, (unsigned)splits), kLThreads, smem, stream>>>(p, mx, mw);
   return cudaGetLastError();
 }
 

@@ -278,7 +278,8 @@ inline EncodeTiledFn encode_fn() {
 // elements read as zero.
 inline bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
                         int64_t stride, uint32_t esize, CUtensorMapDataType dt, uint32_t box_cols,
-                        uint32_t box_rows, CUtensorMapSwizzle sw) {
+                        uint32_t box_rows, CUtensorMapSwizzle sw,
+                        CUtensorMapL2promotion l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_128B) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)(rows > 0 ? rows : 1)};
@@ -286,7 +287,7 @@ inline bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t 
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
