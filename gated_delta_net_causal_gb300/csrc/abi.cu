@@ -77,7 +77,8 @@ gdn_status decode_impl(const gdn_dims* dims, int32_t batch, int32_t tokens, cons
   if (tokens > 8 || (tokens > 1 && slots != nullptr)) return GDN_ERR_UNSUPPORTED;
   if (batch > kMaxGridY) return GDN_ERR_EXTENT;
   const int rep = dims->n_v_heads / dims->n_k_heads;
-  if (rep > 8) return GDN_ERR_UNSUPPORTED;
+  // one token: up to 16 V heads per K head; several tokens: up to 8
+  if (rep > (tokens > 1 ? 8 : 16)) return GDN_ERR_UNSUPPORTED;
   if (batch == 0) return GDN_OK;
   if (!mixed_qkv || !a || !b || !decay_param || !dt_bias || !conv_w || !conv_state || !state)
     return GDN_ERR_INVALID_ARG;
@@ -365,7 +366,7 @@ gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int32_t num_seqs,
   if (num_seqs > kMaxGridY) return GDN_ERR_EXTENT;
   if (!prefill_flags_valid(flags)) return GDN_ERR_INVALID_ARG;
   if (dims->head_dim != 128 || dims->io_dtype != GDN_BF16 || (flags & GDN_PREFILL_CUDA_CORES) ||
-      dims->n_v_heads > 8 * dims->n_k_heads || num_seqs == 0 || total_tokens == 0)
+      dims->n_v_heads > 16 * dims->n_k_heads || num_seqs == 0 || total_tokens == 0)
     return GDN_OK;
   // (T + 63 N) / 64 chunk slots of 25 KB per V head and 16 KB per K head,
   // plus the chunk index, plus T Hv 512 bytes for few (V head, sequence)

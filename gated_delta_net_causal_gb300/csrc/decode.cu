@@ -45,10 +45,12 @@ namespace gdn {
 constexpr int kDecCW = 8;                      // consumer warps
 constexpr int kDecThreads = 32 * (kDecCW + 1);  // + one producer warp
 constexpr int kDecMaxStages = 16;              // ring slots (upper bound)
-constexpr int kDecRingBytes = 192 * 1024;      // shared-memory ring
+// shared-memory ring: 192 KB, or 160 KB where the per-item buffers for 16 V
+// heads per K head (about 35 KB of static shared memory) take the rest
+constexpr int dec_ring_bytes(int repmax) { return repmax > 8 ? 160 * 1024 : 192 * 1024; }
 constexpr int kDecRPL = 2;                     // rows each lane updates per pass
 
-template <int D>
+template <int D, int REPMAX>
 struct DecGeom {
   static constexpr int LPR = D / 16;                       // lanes per row
   static constexpr int RPW = 32 / LPR;                     // rows per warp, per row slot
@@ -57,7 +59,7 @@ struct DecGeom {
   static constexpr int CPH = D / CHUNK_ROWS;               // chunks per head
   static constexpr uint32_t SLOT_BYTES = CHUNK_ROWS * D * 4;
   static constexpr int SLOT_FLOATS = CHUNK_ROWS * D;
-  static constexpr int STAGES_RAW = kDecRingBytes / (int)SLOT_BYTES;
+  static constexpr int STAGES_RAW = dec_ring_bytes(REPMAX) / (int)SLOT_BYTES;
   static constexpr int STAGES = STAGES_RAW < kDecMaxStages ? STAGES_RAW : kDecMaxStages;
   static constexpr int RING_BYTES = STAGES * (int)SLOT_BYTES;
 };
@@ -74,7 +76,7 @@ __device__ __forceinline__ void consumer_sync() {
 template <typename T, int D, int REPMAX, bool SLOTS>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_step_kernel(const DecodeArgs p, const int num_items) {
-  using G = DecGeom<D>;
+  using G = DecGeom<D, REPMAX>;
   constexpr int LPR = G::LPR, RPW = G::RPW;
   constexpr int kDecStages = G::STAGES;
   constexpr int kDecMaxRep = REPMAX;
@@ -152,8 +154,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   T pcs0[NIT], pcs1[NIT], pcs2[NIT], pcx[NIT], pcw[NIT][4];
   int pchan[NIT];
   float pga = 0.f, pgb = 0.f, pgp = 0.f, pgd = 0.f;
-  constexpr int PER = D / 32;  // output elements per lane (warp r writes head r)
-  T pz[PER];
+  constexpr int PER = D / 32;  // output elements per lane
+  // warp w writes the outputs of heads w, w + kDecCW, ... (one head each up
+  // to eight heads per K head, two for sixteen)
+  constexpr int HPW = (kDecMaxRep + kDecCW - 1) / kDecCW;
+  T pz[HPW][PER];
   if (p.z != nullptr)
     for (int j = tid; j < D; j += NC) snw[j] = p.norm_w[j];
   auto prefetch = [&](int item) {
@@ -198,11 +203,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       pgp = p.decay_param[h];
       pgd = p.dt_bias[h];
     }
-    if (item < num_items && p.z != nullptr && warp < rep) {
-      const int h = p.map == GDN_MAP_TILED ? kh + warp * Hk : kh * rep + warp;
-      const T* zr = static_cast<const T*>(p.z) + ((size_t)b * Hv + h) * D + lane * PER;
 #pragma unroll
-      for (int e = 0; e < PER; ++e) pz[e] = zr[e];
+    for (int hw = 0; hw < HPW; ++hw) {
+      const int r = warp + hw * kDecCW;
+      if (item < num_items && p.z != nullptr && r < rep) {
+        const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+        const T* zr = static_cast<const T*>(p.z) + ((size_t)b * Hv + h) * D + lane * PER;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) pz[hw][e] = zr[e];
+      }
     }
   };
   prefetch(blockIdx.x);
@@ -211,37 +220,43 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   // head r) are written after every warp has finished its state pass, i.e.
   // past the next item's first barrier, so they overlap the next item's
   // stream instead of holding every warp at a barrier of their own.
-  auto write_outputs = [&](int it, int pb, const T (&zz)[PER]) {
-    if (warp >= rep || *abort_flag) return;
+  auto write_outputs = [&](int it, int pb, const T (&zz)[HPW][PER]) {
+    if (*abort_flag) return;
     const int b = it / Hk, kh = it - (it / Hk) * Hk;
-    const int r = warp;
-    const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
-    const size_t obase = ((size_t)b * Hv + h) * D + lane * PER;
-    float ov[PER];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) ov[e] = so[pb][r][lane * PER + e];
-    if (p.core_out != nullptr) {
+    for (int hw = 0; hw < HPW; ++hw) {
+      const int r = warp + hw * kDecCW;
+      if (r >= rep) break;
+      const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+      const size_t obase = ((size_t)b * Hv + h) * D + lane * PER;
+      float ov[PER];
 #pragma unroll
-      for (int e = 0; e < PER; ++e) p.core_out[obase + e] = ov[e];
-    }
-    if (p.z != nullptr) {
-      float ss = 0.f;
+      for (int e = 0; e < PER; ++e) ov[e] = so[pb][r][lane * PER + e];
+      if (p.core_out != nullptr) {
 #pragma unroll
-      for (int e = 0; e < PER; ++e) ss += ov[e] * ov[e];
-      ss = group_sum<32>(ss);
-      const float inv = 1.f / sqrtf(ss / (float)D + p.rms_eps);
-      T* outr = static_cast<T*>(p.out) + obase;
+        for (int e = 0; e < PER; ++e) p.core_out[obase + e] = ov[e];
+      }
+      if (p.z != nullptr) {
+        float ss = 0.f;
 #pragma unroll
-      for (int e = 0; e < PER; ++e)
-        outr[e] = from_f32<T>(ov[e] * inv * snw[lane * PER + e] * silu_f(to_f32(zz[e])));
+        for (int e = 0; e < PER; ++e) ss += ov[e] * ov[e];
+        ss = group_sum<32>(ss);
+        const float inv = 1.f / sqrtf(ss / (float)D + p.rms_eps);
+        T* outr = static_cast<T*>(p.out) + obase;
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+          outr[e] = from_f32<T>(ov[e] * inv * snw[lane * PER + e] * silu_f(to_f32(zz[hw][e])));
+      }
     }
   };
 
   uint32_t k = 0;
   int prev_item = -1, prev_buf = 0;
-  T zp[PER];  // z of the previous item, for its outputs
+  T zp[HPW][PER];  // z of the previous item, for its outputs
 #pragma unroll
-  for (int e = 0; e < PER; ++e) zp[e] = T();
+  for (int hw = 0; hw < HPW; ++hw)
+#pragma unroll
+    for (int e = 0; e < PER; ++e) zp[hw][e] = T();
   for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
     const int b = item / Hk, kh = item - (item / Hk) * Hk;
     const int sb = slot_of(b);  // the producer skipped this row's state too if < 0
@@ -252,9 +267,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     T cs1[NIT], cs2[NIT], cx[NIT];
     int chan[NIT];
     float y[NIT];
-    T zc[PER];
+    T zc[HPW][PER];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) zc[e] = pz[e];
+    for (int hw = 0; hw < HPW; ++hw)
+#pragma unroll
+      for (int e = 0; e < PER; ++e) zc[hw][e] = pz[hw][e];
     // conv + SiLU for this item from the prefetched registers: channels
     // [q of kh | k of kh | v of each head]
 #pragma unroll
@@ -300,7 +317,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     consumer_sync();
     if (prev_item >= 0) write_outputs(prev_item, prev_buf, zp);
 #pragma unroll
-    for (int e = 0; e < PER; ++e) zp[e] = zc[e];
+    for (int hw = 0; hw < HPW; ++hw)
+#pragma unroll
+      for (int e = 0; e < PER; ++e) zp[hw][e] = zc[hw][e];
     prev_item = item;
     prev_buf = buf;
 
@@ -439,7 +458,7 @@ template <typename T, int D, int REPMAX>
 static cudaError_t launch_decode_t(const DecodeArgs& p, int32_t batch, cudaStream_t stream) {
   auto kern = p.slots != nullptr ? decode_step_kernel<T, D, REPMAX, true>
                                  : decode_step_kernel<T, D, REPMAX, false>;
-  const int smem = DecGeom<D>::RING_BYTES;
+  const int smem = DecGeom<D, REPMAX>::RING_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int items = batch * p.Hk;
@@ -449,12 +468,13 @@ static cudaError_t launch_decode_t(const DecodeArgs& p, int32_t batch, cudaStrea
 }
 
 // The per-item register and shared buffers are sized for REPMAX V heads per
-// K head: 2, 4 or 8.
+// K head: 2, 4, 8 or 16.
 template <typename T, int D>
 static cudaError_t launch_decode_r(const DecodeArgs& p, int32_t batch, cudaStream_t stream) {
   if (p.rep <= 2) return launch_decode_t<T, D, 2>(p, batch, stream);
   if (p.rep <= 4) return launch_decode_t<T, D, 4>(p, batch, stream);
-  return launch_decode_t<T, D, 8>(p, batch, stream);
+  if (p.rep <= 8) return launch_decode_t<T, D, 8>(p, batch, stream);
+  return launch_decode_t<T, D, 16>(p, batch, stream);
 }
 
 template <typename T>

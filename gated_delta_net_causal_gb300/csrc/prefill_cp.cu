@@ -47,7 +47,7 @@ constexpr int kPrepThreads = 256;
 constexpr int kCarryThreads = 256;  // warps 0-7: the state carry (two threads per value row)
 constexpr int kChainThreads = 512;  // warps 8-15: output and gated norm
 constexpr int kAStride = kC + 1;    // padded row pitch of the fp32 A matrix
-constexpr int kMaxRep = 8;          // V heads per K head on this path
+constexpr int kMaxRep = 16;         // V heads per K head on this path
 // (V head, sequence) pairs up to which the sliced carry (four CTAs each) is
 // chosen, and the workspace holds an fp32 core output for its separate norm
 constexpr int64_t kSlMaxChains = 64;

@@ -147,7 +147,7 @@ gdn_status gdn_conv_update(const gdn_dims* dims, int32_t num_seqs, const int32_t
  * z            [B][Hv][D] io dtype output-gate input, or NULL (no norm).
  * norm_w       [D] fp32 RMSNorm weight (shared by all heads); needed with z.
  * out          [B][Hv][D] io dtype gated-RMSNorm output; needed with z.
- * At least one of core_out and (z, out) must be given. Hv/Hk <= 8.
+ * At least one of core_out and (z, out) must be given. Hv/Hk <= 16.
  */
 gdn_status gdn_decode_step(const gdn_dims* dims, int32_t batch, const void* mixed_qkv,
                            const void* a, const void* b, const float* decay_param,
@@ -177,7 +177,9 @@ gdn_status gdn_decode_step(const gdn_dims* dims, int32_t batch, const void* mixe
  * conv_state   [B][C][3], state [B][Hv][D][D]: in place, as in
  *              gdn_decode_step; afterwards they hold the state after token
  *              T-1.
- * Every other argument, and every error, is as in gdn_decode_step.
+ * Every other argument, and every error, is as in gdn_decode_step, except
+ * that T > 1 takes at most 8 V heads per K head (GDN_ERR_UNSUPPORTED
+ * beyond).
  */
 gdn_status gdn_decode_multi(const gdn_dims* dims, int32_t batch, int32_t tokens,
                             const void* mixed_qkv, const void* a, const void* b,
@@ -242,7 +244,7 @@ gdn_status gdn_decode_step_slots(const gdn_dims* dims, int32_t batch, const int3
  *              garbage afterwards. May be NULL (workspace_bytes ignored).
  *
  * Which kernels run (all on the given stream):
- *  - head_dim 128, bf16, Hv/Hk <= 8, a workspace: the chunk-parallel
+ *  - head_dim 128, bf16, Hv/Hk <= 16, a workspace: the chunk-parallel
  *    tensor-core path.
  *    Every chunk's state-free factors (the K and QK grams, (I+A)^-1 diag(beta),
  *    the masked decayed QK^T) are computed at once into the workspace, then
@@ -266,7 +268,7 @@ gdn_status gdn_prefill_chunked(const gdn_dims* dims, int32_t num_seqs, const int
 /*
  * Bytes of workspace gdn_prefill_chunked can use for these sizes and flags
  * (0 when no workspace path applies: head_dim != 128, io dtype not bf16,
- * more than 8 V heads per K head, or GDN_PREFILL_CUDA_CORES): per 64-token chunk slot ((T + 63 N) / 64 of
+ * more than 16 V heads per K head, or GDN_PREFILL_CUDA_CORES): per 64-token chunk slot ((T + 63 N) / 64 of
  * them) 25 KB per V head and 16 KB per K head, plus 4 (N + 1) bytes rounded
  * up to 1 KB; and where Hv N <= 64 (the sliced carry), T Hv 512 bytes more
  * at a 256-byte boundary, for the fp32 core output that its separate gated
@@ -388,7 +390,7 @@ typedef struct gdn_layer_weights {
  *    `split_qkv` -> gate/beta/alpha projections -> `recurrence` ->
  *    `rms_norm` -> `precise_gate` -> output projection.
  *
- * dims         io_dtype GDN_BF16; Hv D a multiple of 64; Hv/Hk <= 8.
+ * dims         io_dtype GDN_BF16; Hv D a multiple of 64; Hv/Hk <= 16.
  * hidden       model width, a positive multiple of 64.
  * batch        1 <= batch <= 128.
  * x            [batch][hidden] bf16 layer input.

@@ -104,7 +104,7 @@ def test_decode_rejects_bad_arguments(lib):
     assert _decode(lib, gdn.dims(16, 32, 80)) == 3  # head_dim 80 unsupported
     assert _decode(lib, gdn.dims(16, 32, 128, map=7)) == 1
     assert _decode(lib, gdn.dims(16, 32, 128, decay=5)) == 1
-    assert _decode(lib, gdn.dims(1, 16, 128)) == 3  # 16 V heads per K head > 8
+    assert _decode(lib, gdn.dims(1, 32, 128)) == 3  # 32 V heads per K head > 16
     assert _decode(lib, ok, batch=-1) == 1
     assert _decode(lib, ok, batch=70000) == 2  # grid y limit
     assert _decode(lib, ok, batch=0) == 0  # nothing to do, nothing launched
@@ -162,6 +162,13 @@ def test_decode_multi_rejects_bad_arguments(lib):
     # the activations span B*T rows: 2 x 4 x 8192 bf16 = 128 KiB from 0x10000,
     # so a core output at 0x28000 overlaps them (with one token it would not)
     assert call(core=0x28000) == 4
+    # more than 8 V heads per K head: one token runs, several do not
+    wide = gdn.dims(1, 16, 128)
+    args = [VP(a) for a in (0x10000, 0x2000000, 0x3000000, 0x100000, 0x110000, 0x120000, 0x4000000,
+                            0x10000000, 0x70000000)] + [None] * 4
+    assert lib.gdn_decode_multi(ctypes.byref(wide), 2, 2, *args) == 3
+    args[8] = VP(0x10000)  # (the core output on the activations: refused on the host)
+    assert lib.gdn_decode_multi(ctypes.byref(wide), 2, 1, *args) == 4
 
 
 @no_device

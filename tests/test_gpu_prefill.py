@@ -238,26 +238,27 @@ def test_many_short_sequences_chunk_index():
     assert gdn.gdn_device_error() == 0
 
 
+@pytest.mark.parametrize("rep", [8, 16])
 @pytest.mark.parametrize("mp", [gi.GROUPED, gi.TILED])
-def test_eight_v_heads_per_k_head(mp):
-    """The widest head ratio the chunk-parallel path takes (Hv/Hk = 8: one
-    prep CTA builds eight V heads' factors from one K head's grams), with
-    sequences that end inside a chunk and one that is empty."""
+def test_many_v_heads_per_k_head(mp, rep):
+    """The widest head ratios the chunk-parallel path takes (Hv/Hk = 8 and
+    16: one prep CTA builds every V head's factors from one K head's
+    grams), with sequences that end inside a chunk and one that is empty."""
     lengths = [150, 0, 64, 9]
-    shape = gi.Shape(1, 8, 128, map=mp, decay=gi.NEGATIVE_RATE, dtype="bf16")
-    w, q, k, v, z, a, b, S0 = _raw_case(7000 + mp, shape, lengths)
+    shape = gi.Shape(1, rep, 128, map=mp, decay=gi.NEGATIVE_RATE, dtype="bf16")
+    w, q, k, v, z, a, b, S0 = _raw_case(7000 + mp + rep, shape, lengths)
     cu = gi.cu_seqlens(lengths)
-    dims = gdn.dims(1, 8, 128, map=mp, decay=gi.NEGATIVE_RATE, io_dtype=torch.bfloat16)
+    dims = gdn.dims(1, rep, 128, map=mp, decay=gi.NEGATIVE_RATE, io_dtype=torch.bfloat16)
     assert gdn.gdn_prefill_workspace_size(dims, len(lengths), sum(lengths)) > 0
     state = cuda(S0)
     core, out = _run_prefill(dims, cu, q, k, v, a, b, state, 0, dp=w.decay_param, dt=w.dt_bias,
                              z=cuda(z), nw=cuda(w.norm_w))
     ro, rS = _oracle_prefill(shape, w, q, k, v, a, b, S0, cu)
-    assert_abs(core.cpu(), ro, CHUNK_OUT_ABS, "Hv/Hk=8 output")
-    assert_abs(state.cpu(), rS, CHUNK_STATE_ABS, "Hv/Hk=8 state")
+    assert_abs(core.cpu(), ro, CHUNK_OUT_ABS, f"Hv/Hk={rep} output")
+    assert_abs(state.cpu(), rS, CHUNK_STATE_ABS, f"Hv/Hk={rep} state")
     assert torch.equal(state.cpu()[1], S0[1])
     ry = oracle.gated_rmsnorm(F64(core.cpu()), F64(z), F64(w.norm_w), 1e-6)
-    assert_lowp(out.cpu(), ry, "bf16", "Hv/Hk=8 fused norm")
+    assert_lowp(out.cpu(), ry, "bf16", f"Hv/Hk={rep} fused norm")
     assert gdn.gdn_device_error() == 0
 
 
