@@ -51,7 +51,8 @@ gdn_status check_dims(const gdn_dims* d) {
   if (!(d->l2_eps >= 0.f) || !isfinite(d->l2_eps)) return GDN_ERR_INVALID_ARG;
   if (!(d->rms_eps >= 0.f) || !isfinite(d->rms_eps)) return GDN_ERR_INVALID_ARG;
   if (d->head_dim < 1) return GDN_ERR_INVALID_ARG;
-  if (d->head_dim != 32 && d->head_dim != 64 && d->head_dim != 128) return GDN_ERR_UNSUPPORTED;
+  if (d->head_dim != 32 && d->head_dim != 64 && d->head_dim != 96 && d->head_dim != 128)
+    return GDN_ERR_UNSUPPORTED;
   if (d->n_v_heads > kMaxGridY) return GDN_ERR_EXTENT;
   const int64_t C = (2 * (int64_t)d->n_k_heads + d->n_v_heads) * d->head_dim;
   if (C > INT32_MAX / 4) return GDN_ERR_EXTENT;

@@ -50,11 +50,17 @@ constexpr int kDecMaxStages = 16;              // ring slots (upper bound)
 constexpr int dec_ring_bytes(int repmax) { return repmax > 8 ? 160 * 1024 : 192 * 1024; }
 constexpr int kDecRPL = 2;                     // rows each lane updates per pass
 
+// Each row is handled by LPR lanes, each lane taking NV4 groups of four
+// columns (group m of lane sub at column 4 sub + 4 LPR m): 16 columns per
+// lane at D = 32, 64, 128; at D = 96 eight lanes of 12 columns, and three
+// rows per lane per pass so that one 96-row chunk is a whole head.
 template <int D, int REPMAX>
 struct DecGeom {
-  static constexpr int LPR = D / 16;                       // lanes per row
+  static constexpr int LPR = D == 96 ? 8 : D / 16;         // lanes per row
+  static constexpr int NV4 = D / (4 * LPR);                // float4 groups per lane
+  static constexpr int RPL = D == 96 ? 3 : kDecRPL;        // rows each lane updates per pass
   static constexpr int RPW = 32 / LPR;                     // rows per warp, per row slot
-  static constexpr int WROWS = RPW * kDecRPL;              // rows per warp pass
+  static constexpr int WROWS = RPW * RPL;                  // rows per warp pass
   static constexpr int CHUNK_ROWS = WROWS * kDecCW < D ? WROWS * kDecCW : D;
   static constexpr int CPH = D / CHUNK_ROWS;               // chunks per head
   static constexpr uint32_t SLOT_BYTES = CHUNK_ROWS * D * 4;
@@ -338,11 +344,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const float inv_q = 1.f / sqrtf(qq + p.l2_eps);
     const float inv_k = 1.f / sqrtf(kk + p.l2_eps);
     const float kq = qkr * inv_q * inv_k * p.scale;
-    float kr[16], qr[16];
+    constexpr int NV4 = G::NV4, RPL = G::RPL;
+    float kr[4 * NV4], qr[4 * NV4];
     {
       const float sqs = inv_q * p.scale;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
+      for (int m = 0; m < NV4; ++m) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int col = 4 * sub + 4 * LPR * m + e;
@@ -368,23 +375,23 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int slot = (int)(k % kDecStages);
         const bool ready = dec_wait(&full_bar[slot], (k / kDecStages) & 1, abort_flag);
         if (ready && warp * G::WROWS < G::CHUNK_ROWS) {
-          float4 s4[kDecRPL][4];
-          int rowv[kDecRPL];
+          float4 s4[RPL][NV4];
+          int rowv[RPL];
 #pragma unroll
-          for (int u = 0; u < kDecRPL; ++u) {
+          for (int u = 0; u < RPL; ++u) {
             const int rl = warp * G::WROWS + u * RPW + rq;  // row within the chunk
             rowv[u] = c * G::CHUNK_ROWS + rl;
             const float* srow = ring + slot * G::SLOT_FLOATS + rl * D;
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int m = 0; m < NV4; ++m)
               s4[u][m] = *reinterpret_cast<const float4*>(srow + 4 * sub + 4 * LPR * m);
           }
-          float pk[kDecRPL], pq[kDecRPL];
+          float pk[RPL], pq[RPL];
 #pragma unroll
-          for (int u = 0; u < kDecRPL; ++u) {
-            float pk4[4], pq4[4];
+          for (int u = 0; u < RPL; ++u) {
+            float pk4[NV4], pq4[NV4];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
+            for (int m = 0; m < NV4; ++m) {
               pk4[m] = s4[u][m].x * kr[4 * m + 0];
               pq4[m] = s4[u][m].x * qr[4 * m + 0];
               pk4[m] = fmaf(s4[u][m].y, kr[4 * m + 1], pk4[m]);
@@ -394,25 +401,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
               pk4[m] = fmaf(s4[u][m].w, kr[4 * m + 3], pk4[m]);
               pq4[m] = fmaf(s4[u][m].w, qr[4 * m + 3], pq4[m]);
             }
-            pk[u] = (pk4[0] + pk4[1]) + (pk4[2] + pk4[3]);
-            pq[u] = (pq4[0] + pq4[1]) + (pq4[2] + pq4[3]);
+            pk[u] = sum_groups<NV4>(pk4);
+            pq[u] = sum_groups<NV4>(pq4);
           }
 #pragma unroll
           for (int o = LPR / 2; o > 0; o >>= 1) {
 #pragma unroll
-            for (int u = 0; u < kDecRPL; ++u) {
+            for (int u = 0; u < RPL; ++u) {
               pk[u] += __shfl_xor_sync(0xffffffffu, pk[u], o);
               pq[u] += __shfl_xor_sync(0xffffffffu, pq[u], o);
             }
           }
 #pragma unroll
-          for (int u = 0; u < kDecRPL; ++u) {
+          for (int u = 0; u < RPL; ++u) {
             const int row = rowv[u];
             const float d = beta * (sv[buf][r][row] - alpha * pk[u]);
             const float o = fmaf(alpha, pq[u], d * kq);
             float* grow = gS + (size_t)row * D;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
+            for (int m = 0; m < NV4; ++m) {
               float4 n4;
               n4.x = fmaf(d, kr[4 * m + 0], alpha * s4[u][m].x);
               n4.y = fmaf(d, kr[4 * m + 1], alpha * s4[u][m].y);
@@ -483,6 +490,7 @@ static cudaError_t launch_decode_d(const DecodeArgs& p, int32_t D, int32_t batch
   switch (D) {
     case 32: return launch_decode_r<T, 32>(p, batch, stream);
     case 64: return launch_decode_r<T, 64>(p, batch, stream);
+    case 96: return launch_decode_r<T, 96>(p, batch, stream);
     case 128: return launch_decode_r<T, 128>(p, batch, stream);
     default: return cudaErrorInvalidValue;
   }

@@ -40,11 +40,17 @@ constexpr int kMtTMax = 8;                    // tokens per sequence and call
 constexpr int kMtRPL = 2;                     // rows each lane updates per pass
 constexpr int kMtMaxStages = 16;
 
+// The lane geometry of the one-token decode kernel (decode.cu): LPR lanes
+// per row, NV4 groups of four columns per lane (16 columns at D = 32, 64,
+// 128; eight lanes of 12 at D = 96, three rows per lane so that a chunk is a
+// whole 96-row head).
 template <int D, int REPMAX>
 struct MtGeom {
-  static constexpr int LPR = D / 16;  // lanes per row (16 columns per lane)
+  static constexpr int LPR = D == 96 ? 8 : D / 16;  // lanes per row
+  static constexpr int NV4 = D / (4 * LPR);
+  static constexpr int RPL = D == 96 ? 3 : kMtRPL;
   static constexpr int RPW = 32 / LPR;
-  static constexpr int WROWS = RPW * kMtRPL;
+  static constexpr int WROWS = RPW * RPL;
   static constexpr int CHUNK_ROWS = WROWS * kMtCW < D ? WROWS * kMtCW : D;
   static constexpr int CPH = D / CHUNK_ROWS;
   static constexpr uint32_t SLOT_BYTES = CHUNK_ROWS * D * 4;
@@ -74,7 +80,7 @@ template <typename T, int D, int REPMAX>
 __global__ void __launch_bounds__(kMtThreads, 2)
     decode_multi_kernel(const DecodeArgs p, const int num_items) {
   using G = MtGeom<D, REPMAX>;
-  constexpr int LPR = G::LPR, RPW = G::RPW, STAGES = G::STAGES;
+  constexpr int LPR = G::LPR, RPW = G::RPW, STAGES = G::STAGES, NV4 = G::NV4, RPL = G::RPL;
   constexpr int NC = kMtCW * 32;
   constexpr int PER = D / 32;  // output elements per lane
 
@@ -225,24 +231,24 @@ __global__ void __launch_bounds__(kMtThreads, 2)
         const int slot = (int)(k % STAGES);
         const bool ready = mt_wait(&full_bar[slot], (k / STAGES) & 1, abort_flag);
         if (ready && warp * G::WROWS < G::CHUNK_ROWS) {
-          float4 s4[kMtRPL][4];
-          int rowv[kMtRPL];
+          float4 s4[RPL][NV4];
+          int rowv[RPL];
 #pragma unroll
-          for (int u = 0; u < kMtRPL; ++u) {
+          for (int u = 0; u < RPL; ++u) {
             const int rl = warp * G::WROWS + u * RPW + rq;
             rowv[u] = c * G::CHUNK_ROWS + rl;
             const float* srow = ring + slot * G::SLOT_FLOATS + rl * D;
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int m = 0; m < NV4; ++m)
               s4[u][m] = *reinterpret_cast<const float4*>(srow + 4 * sub + 4 * LPR * m);
           }
           for (int t = 0; t < NT; ++t) {
             const float sqs = sinv[warp][0][t] * p.scale;
             const float inv_k = sinv[warp][1][t];
             const float kq = sinv[warp][2][t];
-            float kr[16], qr[16];
+            float kr[4 * NV4], qr[4 * NV4];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
+            for (int m = 0; m < NV4; ++m) {
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int col = 4 * sub + 4 * LPR * m + e;
@@ -250,12 +256,12 @@ __global__ void __launch_bounds__(kMtThreads, 2)
                 qr[4 * m + e] = sq[t][col] * sqs;
               }
             }
-            float pk[kMtRPL], pq[kMtRPL];
+            float pk[RPL], pq[RPL];
 #pragma unroll
-            for (int u = 0; u < kMtRPL; ++u) {
-              float pk4[4], pq4[4];
+            for (int u = 0; u < RPL; ++u) {
+              float pk4[NV4], pq4[NV4];
 #pragma unroll
-              for (int m = 0; m < 4; ++m) {
+              for (int m = 0; m < NV4; ++m) {
                 pk4[m] = s4[u][m].x * kr[4 * m + 0];
                 pq4[m] = s4[u][m].x * qr[4 * m + 0];
                 pk4[m] = fmaf(s4[u][m].y, kr[4 * m + 1], pk4[m]);
@@ -265,25 +271,25 @@ __global__ void __launch_bounds__(kMtThreads, 2)
                 pk4[m] = fmaf(s4[u][m].w, kr[4 * m + 3], pk4[m]);
                 pq4[m] = fmaf(s4[u][m].w, qr[4 * m + 3], pq4[m]);
               }
-              pk[u] = (pk4[0] + pk4[1]) + (pk4[2] + pk4[3]);
-              pq[u] = (pq4[0] + pq4[1]) + (pq4[2] + pq4[3]);
+              pk[u] = sum_groups<NV4>(pk4);
+              pq[u] = sum_groups<NV4>(pq4);
             }
 #pragma unroll
             for (int o = LPR / 2; o > 0; o >>= 1) {
 #pragma unroll
-              for (int u = 0; u < kMtRPL; ++u) {
+              for (int u = 0; u < RPL; ++u) {
                 pk[u] += __shfl_xor_sync(0xffffffffu, pk[u], o);
                 pq[u] += __shfl_xor_sync(0xffffffffu, pq[u], o);
               }
             }
             const float alpha = sgate[r][t][0], beta = sgate[r][t][1];
 #pragma unroll
-            for (int u = 0; u < kMtRPL; ++u) {
+            for (int u = 0; u < RPL; ++u) {
               const int row = rowv[u];
               const float d = beta * (sv[r][t][row] - alpha * pk[u]);
               const float o = fmaf(alpha, pq[u], d * kq);
 #pragma unroll
-              for (int m = 0; m < 4; ++m) {
+              for (int m = 0; m < NV4; ++m) {
                 s4[u][m].x = fmaf(d, kr[4 * m + 0], alpha * s4[u][m].x);
                 s4[u][m].y = fmaf(d, kr[4 * m + 1], alpha * s4[u][m].y);
                 s4[u][m].z = fmaf(d, kr[4 * m + 2], alpha * s4[u][m].z);
@@ -293,10 +299,10 @@ __global__ void __launch_bounds__(kMtThreads, 2)
             }
           }
 #pragma unroll
-          for (int u = 0; u < kMtRPL; ++u) {
+          for (int u = 0; u < RPL; ++u) {
             float* grow = gS + (size_t)rowv[u] * D;
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int m = 0; m < NV4; ++m)
               __stcs(reinterpret_cast<float4*>(grow + 4 * sub + 4 * LPR * m), s4[u][m]);
           }
         }
@@ -384,6 +390,7 @@ cudaError_t launch_mt_d(const DecodeArgs& p, int32_t D, int32_t batch, cudaStrea
   switch (D) {
     case 32: return launch_mt_r<T, 32>(p, batch, stream);
     case 64: return launch_mt_r<T, 64>(p, batch, stream);
+    case 96: return launch_mt_r<T, 96>(p, batch, stream);
     case 128: return launch_mt_r<T, 128>(p, batch, stream);
     default: return cudaErrorInvalidValue;
   }

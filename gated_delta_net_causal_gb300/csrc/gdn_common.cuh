@@ -61,6 +61,15 @@ __device__ __forceinline__ float gate_g(int decay, float param, float dt_bias, f
   return rate * softplus_f(a + dt_bias);
 }
 
+// The per-lane partial sums of a decode row over its NV4 column groups, in
+// the one fixed order both decode kernels use (so they agree bit for bit).
+template <int NV4>
+__device__ __forceinline__ float sum_groups(const float (&a)[NV4]) {
+  static_assert(NV4 == 3 || NV4 == 4, "three or four column groups per lane");
+  if constexpr (NV4 == 4) return (a[0] + a[1]) + (a[2] + a[3]);
+  else return (a[0] + a[1]) + a[2];
+}
+
 __device__ __forceinline__ int k_head_of(int map, int h, int Hk, int rep) {
   return map == GDN_MAP_TILED ? (h % Hk) : (h / rep);
 }

@@ -311,6 +311,7 @@ static cudaError_t launch_prefill_d(const PrefillArgs& p, int32_t D, cudaStream_
   switch (D) {
     case 32: return launch_prefill_t<T, 32>(p, stream);
     case 64: return launch_prefill_t<T, 64>(p, stream);
+    case 96: return launch_prefill_t<T, 96>(p, stream);
     case 128: return launch_prefill_t<T, 128>(p, stream);
     default: return cudaErrorInvalidValue;
   }

@@ -38,6 +38,7 @@ static cudaError_t launch_rms_t(const RmsNormArgs& p, int32_t D, cudaStream_t st
   switch (D) {
     case 32: gated_rmsnorm_kernel<T, 32><<<(unsigned)grid, 256, 0, stream>>>(p); break;
     case 64: gated_rmsnorm_kernel<T, 64><<<(unsigned)grid, 256, 0, stream>>>(p); break;
+    case 96: gated_rmsnorm_kernel<T, 96><<<(unsigned)grid, 256, 0, stream>>>(p); break;
     case 128: gated_rmsnorm_kernel<T, 128><<<(unsigned)grid, 256, 0, stream>>>(p); break;
     default: return cudaErrorInvalidValue;
   }

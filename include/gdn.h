@@ -26,7 +26,7 @@
  *  - io dtype (gdn_dims.io_dtype) is the storage type of the activations,
  *    the conv weight and the conv state; the delta state, core outputs,
  *    decay parameters, dt_bias and the norm weight are always fp32.
- *  - Supported shapes: head_dim (Dk = Dv = D) in {32, 64, 128};
+ *  - Supported shapes: head_dim (Dk = Dv = D) in {32, 64, 96, 128};
  *    n_v_heads a multiple of n_k_heads; conv kernel width 4 (3-wide state).
  */
 #ifndef GDN_H_
@@ -78,7 +78,7 @@ enum {
 typedef struct gdn_dims {
   int32_t n_k_heads; /* Hk >= 1 */
   int32_t n_v_heads; /* Hv, a multiple of Hk */
-  int32_t head_dim;  /* D = Dk = Dv in {32, 64, 128} */
+  int32_t head_dim;  /* D = Dk = Dv in {32, 64, 96, 128} */
   int32_t map;       /* gdn_head_map */
   int32_t decay;     /* gdn_decay */
   int32_t io_dtype;  /* gdn_dtype */

@@ -48,7 +48,7 @@ def test_conv_update_large_batch_tail_tiles():
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
-@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("D", [32, 64, 96, 128])
 def test_gated_rmsnorm(dtype, D):
     g = gi.rng(D)
     rows = 1000 + D

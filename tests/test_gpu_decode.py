@@ -37,7 +37,8 @@ def _check_steps(shape, batch, steps, seed, with_norm=True, core=True):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("hk,hv,d", [(2, 4, 32), (2, 4, 64), (1, 2, 128), (4, 8, 128),
-                                     (2, 2, 128), (1, 8, 128), (1, 16, 128), (2, 32, 64)])
+                                     (2, 2, 128), (1, 8, 128), (1, 16, 128), (2, 32, 64),
+                                     (2, 4, 96), (1, 8, 96)])
 @pytest.mark.parametrize("mp,dec", [(gi.GROUPED, gi.LOG_RATE), (gi.TILED, gi.NEGATIVE_RATE)])
 def test_decode_small_shapes(dtype, hk, hv, d, mp, dec):
     shape = gi.Shape(hk, hv, d, map=mp, decay=dec, dtype=dtype)

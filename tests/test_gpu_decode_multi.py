@@ -73,7 +73,7 @@ def _run_steps(shape, w, cs0, S0, steps, core=True, norm=True):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("hk,hv,d", [(2, 4, 32), (2, 4, 64), (4, 8, 128), (2, 2, 128),
-                                     (1, 8, 128), (2, 8, 64)])
+                                     (1, 8, 128), (2, 8, 64), (2, 4, 96)])
 @pytest.mark.parametrize("T", [2, 5, 8])
 def test_multi_equals_successive_steps_bitwise(dtype, hk, hv, d, T):
     mp, dec = (gi.TILED, gi.NEGATIVE_RATE) if (hk + T) % 2 else (gi.GROUPED, gi.LOG_RATE)

@@ -134,7 +134,7 @@ def _oracle_prefill(shape, w, q, k, v, a, b, S0, cu):
 
 @pytest.mark.parametrize("path", list(PATHS))
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("d", [32, 64, 96, 128])
 @pytest.mark.parametrize("mp,dec", [(gi.GROUPED, gi.LOG_RATE), (gi.TILED, gi.NEGATIVE_RATE)])
 def test_varlen_raw_inputs_with_fused_norm(dtype, d, mp, dec, path):
     if path != "sliced" and not (dtype == "bf16" and d == 128):
