@@ -199,8 +199,14 @@ def _decode_call(gdn, d, dev, inp, state, cstate, out):
 def run_gpu(args, ws, rank, local):
     torch.cuda.set_device(local)
     peaks = _peaks()
-    if args.prefill_only:
-        line = {"metric": "chunked prefill tokens/s", "prefill": run_prefill(args, peaks, ws)}
+    only = "prefill" if args.prefill_only else args.only
+    if only:
+        blocks = {"prefill": lambda: run_prefill(args, peaks, ws),
+                  "varlen_path": lambda: run_varlen(args, ws, peaks),
+                  "decode_layer": lambda: run_decode_layer(args, ws, peaks),
+                  "multi_token_decode": lambda: run_multi_decode(args, ws, peaks),
+                  "slot_decode": lambda: run_slot_decode(args, ws, peaks)}
+        line = {"metric": f"the {only} block alone", only: blocks[only]()}
         return line if rank == 0 else None
     batch = args.batch
     gdn, d, dev, steps, host, state, cstate, out, shape = _decode_setup(batch, 16, rank)
@@ -623,6 +629,20 @@ def run_varlen(args, ws, peaks):
         torch.cuda.synchronize()
         ptimes.append(e0.elapsed_time(e1) * 1e-3)
     tp = _barrier_max(statistics.mean(ptimes[1:]), ws)
+
+    # the conv update alone (two launches: the outputs, then the state), the
+    # conv states reset before each call
+    ctimes = []
+    for _ in range(4):
+        cs.copy_(cs0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gdn.gdn_conv_update(d, cu, x, conv_w, cs, y)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ctimes.append(e0.elapsed_time(e1) * 1e-3)
+    tc = _barrier_max(statistics.mean(ctimes[1:]), ws)
+    cbytes = 2 * T * C * 2 + 2 * N * C * 3 * 2 + C * 4 * 2
     Cc = 64
     flops = T * (Hv * (6 * D * D + 6 * Cc * D + Cc * Cc / 3) + Hk * 4 * Cc * D)
     byts = (T * (2 * Hk * D + 2 * Hv * D) * 2 + T * Hv * D * 2 + 2 * N * Hv * D * D * 4
@@ -641,7 +661,16 @@ def run_varlen(args, ws, peaks):
                                           "hbm_frac": round(byts / tp / 1e9 / peaks["hbm_gbs"], 4),
                                           "peak_source": peaks["source"]},
                              "timed": "the gdn_prefill_chunked call alone (index, prep, chain), "
-                                      "fused norm, states reset before each of 3 timed calls"}}
+                                      "fused norm, states reset before each of 3 timed calls"},
+            "conv_update": {"us_per_call": round(tc * 1e6, 2),
+                            "roofline": {"bound": "hbm", "achieved": round(cbytes / tc / 1e9, 1),
+                                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                         "frac": round(cbytes / tc / 1e9 / peaks["hbm_gbs"], 4),
+                                         "algorithmic_bytes_per_call": cbytes,
+                                         "peak_source": peaks["source"]},
+                            "kernel": "conv_fwd_kernel + conv_state_kernel",
+                            "timed": "the gdn_conv_update call alone, conv states reset before "
+                                     "each of 3 timed calls"}}
 
 
 def run_batch1(args, ws):
@@ -1164,6 +1193,10 @@ def main():
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the T=4096 chunked-prefill block (a process of about 1.5 GB "
                          "on the device, for profiler captures of the prefill kernels)")
+    ap.add_argument("--only", default=None,
+                    choices=["prefill", "varlen_path", "decode_layer", "multi_token_decode",
+                             "slot_decode"],
+                    help="run only this block and print it (for profiler captures of its kernels)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     ws, rank, local = _dist()
