@@ -197,7 +197,7 @@ gdn_status gdn_conv_update(const gdn_dims* dims, int32_t num_seqs, const int32_t
   int64_t xel = 0, xbytes = 0, sel = 0, sbytes = 0;
   if (!mul_ok(total_tokens, C, &xel) || !mul_ok(xel, es, &xbytes)) return GDN_ERR_EXTENT;
   if (!mul_ok((int64_t)num_seqs, C * 3, &sel) || !mul_ok(sel, es, &sbytes)) return GDN_ERR_EXTENT;
-  if ((total_tokens + 63) / 64 > INT32_MAX) return GDN_ERR_EXTENT;
+  if (total_tokens > INT32_MAX - 64) return GDN_ERR_EXTENT;  // TMA row coordinates are int32
   if (!aligned16(cu_seqlens) || !aligned16(conv_w) || !aligned16(conv_state)) return GDN_ERR_ALIGN;
   if (total_tokens > 0 && (!aligned16(x) || !aligned16(y))) return GDN_ERR_ALIGN;
   if (total_tokens > 0) {

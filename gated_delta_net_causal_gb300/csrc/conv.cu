@@ -4,146 +4,260 @@
 // conv-state update; libmir-metal decode/mod.rs `convolve`).
 //
 // Two launches on the caller's stream:
-//  1. conv_fwd_kernel: y for every token. A thread owns 16 bytes of channels
-//     (8 for f16/bf16, 4 for f32) and 4 consecutive tokens; it loads the 7
-//     input rows its window needs once (16-byte vectors), converts its
-//     weights once, and when one sequence covers the whole window unpacks
-//     each row once into the accumulators of every token it is a tap of. Only
-//     windows that reach back past a sequence start take the per-token path
-//     that reads the OLD conv state for the (at most three) taps before the
-//     sequence's first token. The kernel is bound by instruction issue, not
-//     by HBM, so every per-element instruction counts.
+//  1. conv_fwd_kernel: y for every token, persistent, two CTAs per SM. The
+//     work is cut into tiles of 64 tokens x 512 bytes of channels. A load
+//     warp streams each tile's 67 input rows (three rows of history, then the
+//     64 tokens) into a three-stage shared-memory ring with one TMA copy per
+//     tile; rows before the first token or past the last read as zero. Eight
+//     compute warps take eight tokens each: a thread holds 16 bytes of
+//     channels, reads the 11 rows its window needs from shared memory once,
+//     and accumulates each row into the (at most four) tokens it is a tap of,
+//     two channels per paired fp32 FMA, taps in order 0..3 from zero; a token
+//     is stored as soon as its last tap is in. Only windows that reach back
+//     past a sequence start (or tiles past the end) take the per-token path
+//     that reads the OLD conv state for the taps before the sequence's first
+//     token.
 //  2. conv_state_kernel: the new conv state (last three raw inputs of each
 //     sequence). Running it after (1) in stream order is what makes the in-place
 //     state update race-free: (1) never sees a half-updated state.
+#include <cuda.h>
+
+#include <type_traits>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "tc_common.cuh"
 
 namespace gdn {
+namespace {
 
-constexpr int kConvTPT = 4;    // tokens per thread
-constexpr int kConvCV = 32;    // channel vectors per block
-constexpr int kConvTG = 8;     // token groups per block
+constexpr int kCvTok = 64;                               // output tokens per tile
+constexpr int kCvRows = kCvTok + 3;                      // input rows per tile
+constexpr int kCvRowBytes = 512;                         // channels per tile, in bytes
+constexpr uint32_t kCvStageBytes = kCvRows * kCvRowBytes;  // 34,304
+constexpr int kCvStages = 3;
+constexpr int kCvWarps = 8;                   // compute warps
+constexpr int kCvTpt = kCvTok / kCvWarps;     // tokens per thread
+constexpr int kCvThreads = (kCvWarps + 1) * 32;  // + the load warp
+constexpr int kCvCtasPerSm = 2;
+constexpr uint32_t kCvSmem = kCvStages * kCvStageBytes + 128;
 
 __device__ __forceinline__ int64_t clamp_cu(const int32_t* cu, int n, int64_t T) {
   int64_t v = cu[n];
   return v < 0 ? 0 : (v > T ? T : v);
 }
 
+// the last sequence n in [0, N) with start <= t
+__device__ __forceinline__ int seq_of(const int32_t* cu, int N, int64_t T, int64_t t) {
+  int lo = 0, hi = N - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (clamp_cu(cu, mid, T) <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// d = a * b + c on both lanes of a pair, one rounding each (paired fp32 FMA)
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// 16 bytes of channels as fp32 pairs (channels 2p, 2p + 1 in pair p)
 template <typename T>
-__device__ __forceinline__ void unpack16(const uint4& raw, float (&out)[16 / sizeof(T)]) {
-  const T* v = reinterpret_cast<const T*>(&raw);
+__device__ __forceinline__ void unpack_pairs(const uint4& raw, float2 (&x)[16 / sizeof(T) / 2]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  if constexpr (sizeof(T) == 4) {
+    x[0] = make_float2(__uint_as_float(w[0]), __uint_as_float(w[1]));
+    x[1] = make_float2(__uint_as_float(w[2]), __uint_as_float(w[3]));
+  } else if constexpr (std::is_same<T, __nv_bfloat16>::value) {
 #pragma unroll
-  for (int e = 0; e < (int)(16 / sizeof(T)); ++e) out[e] = to_f32(v[e]);
+    for (int p = 0; p < 4; ++p) x[p] = make_float2(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xffff0000u));
+  } else {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) x[p] = __half22float2(*reinterpret_cast<const __half2*>(&w[p]));
+  }
+}
+
+__device__ __forceinline__ float silu_conv(float a) {
+  // silu with the fast exponential and divide (~2^-21 relative error, far
+  // below one ulp of the 16-bit output)
+  return __fdividef(a, 1.f + __expf(-a));
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kConvCV* kConvTG) conv_fwd_kernel(const ConvArgs p) {
-  constexpr int VEC = 16 / (int)sizeof(T);
-  constexpr int NR = kConvTPT + 3;
-  const int cv = threadIdx.x % kConvCV, tg = threadIdx.x / kConvCV;
-  const int64_t c0 = ((int64_t)blockIdx.y * kConvCV + cv) * VEC;
-  const int64_t t0 = ((int64_t)blockIdx.x * kConvTG + tg) * kConvTPT;
-  const int64_t T_ = p.T, C = p.C;
-  if (c0 >= C || t0 >= T_) return;
-  const T* xp = static_cast<const T*>(p.x) + c0;
-  const T* st = static_cast<const T*>(p.conv_state);
-  T* y = static_cast<T*>(p.y);
-
-  uint4 xr[NR];
-#pragma unroll
-  for (int u = 0; u < NR; ++u) {
-    const int64_t tau = t0 - 3 + u;
-    xr[u] = (tau >= 0 && tau < T_) ? *reinterpret_cast<const uint4*>(xp + tau * C)
-                                    : make_uint4(0, 0, 0, 0);
-  }
-  float wf[VEC][4];
-  {
-    constexpr int WV = VEC * 4 * (int)sizeof(T) / 16;
-    uint4 wr[WV];
-    const uint4* wp = reinterpret_cast<const uint4*>(static_cast<const T*>(p.conv_w) + c0 * 4);
-#pragma unroll
-    for (int i = 0; i < WV; ++i) wr[i] = wp[i];
-    const T* wv = reinterpret_cast<const T*>(wr);
-#pragma unroll
-    for (int e = 0; e < VEC; ++e)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) wf[e][j] = to_f32(wv[e * 4 + j]);
-  }
-  int lo = 0, hi = p.N - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (clamp_cu(p.cu_seqlens, mid, T_) <= t0) lo = mid;
-    else hi = mid - 1;
-  }
-  int n = lo;
-  int64_t s_n = clamp_cu(p.cu_seqlens, n, T_);
-  int64_t s_next = n + 1 < p.N ? clamp_cu(p.cu_seqlens, n + 1, T_) : T_ + 1;
-
-  float acc[kConvTPT][VEC];
-#pragma unroll
-  for (int jj = 0; jj < kConvTPT; ++jj)
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) acc[jj][e] = 0.f;
-  if (s_n <= t0 - 3 && s_next > t0 + kConvTPT - 1) {
-    // one sequence covers the whole window: each row is unpacked once and
-    // feeds every output token it is a tap of
-#pragma unroll
-    for (int u = 0; u < NR; ++u) {
-      float xv[VEC];
-      unpack16<T>(xr[u], xv);
-#pragma unroll
-      for (int jj = 0; jj < kConvTPT; ++jj) {
-        const int j = u - jj;  // tap index of row u for token jj
-        if (j >= 0 && j < 4) {
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) acc[jj][e] = fmaf(wf[e][j], xv[e], acc[jj][e]);
-        }
-      }
-    }
+__device__ __forceinline__ uint4 pack_pairs(const float2 (&v)[16 / sizeof(T) / 2]) {
+  uint4 out;
+  uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+  if constexpr (sizeof(T) == 4) {
+    o[0] = __float_as_uint(silu_conv(v[0].x));
+    o[1] = __float_as_uint(silu_conv(v[0].y));
+    o[2] = __float_as_uint(silu_conv(v[1].x));
+    o[3] = __float_as_uint(silu_conv(v[1].y));
   } else {
 #pragma unroll
-    for (int jj = 0; jj < kConvTPT; ++jj) {
-      const int64_t t = t0 + jj;
-      if (t >= T_) break;
-      while (s_next <= t) {
-        ++n;
-        s_n = s_next;
-        s_next = n + 1 < p.N ? clamp_cu(p.cu_seqlens, n + 1, T_) : T_ + 1;
-      }
-      const int64_t s = s_n > t ? t : s_n;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int64_t tau = t + j - 3;
-        float xv[VEC];
-        if (tau >= s) {
-          unpack16<T>(xr[jj + j], xv);
-        } else {
-          const int slot = 3 + (int)(tau - s);
-          const T* sp = st + ((int64_t)n * C + c0) * 3 + slot;
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) xv[e] = to_f32(sp[e * 3]);
-        }
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) acc[jj][e] = fmaf(wf[e][j], xv[e], acc[jj][e]);
+    for (int p = 0; p < 4; ++p) {
+      const float a = silu_conv(v[p].x), b = silu_conv(v[p].y);
+      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        o[p] = *reinterpret_cast<const uint32_t*>(&h);
+      } else {
+        const __half2 h = __floats2half2_rn(a, b);
+        o[p] = *reinterpret_cast<const uint32_t*>(&h);
       }
     }
   }
-#pragma unroll
-  for (int jj = 0; jj < kConvTPT; ++jj) {
-    const int64_t t = t0 + jj;
-    if (t < T_) {
-      uint4 packed;
-      T* pv = reinterpret_cast<T*>(&packed);
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        const float a = acc[jj][e];
-        // silu with the fast exponential and divide (~2^-21 relative error,
-        // far below one ulp of the 16-bit output)
-        pv[e] = from_f32<T>(__fdividef(a, 1.f + __expf(-a)));
-      }
-      *reinterpret_cast<uint4*>(y + t * C + c0) = packed;
+  return out;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kCvThreads, kCvCtasPerSm)
+    conv_fwd_kernel(const ConvArgs p, const __grid_constant__ CUtensorMap tm_x, int64_t ntt,
+                    int64_t ntiles) {
+  constexpr int VEC = 16 / (int)sizeof(T);  // channels per thread
+  constexpr int NP = VEC / 2;               // channel pairs per thread
+  constexpr int CPT = kCvRowBytes / (int)sizeof(T);  // channels per tile
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  __shared__ __align__(8) uint64_t full[kCvStages], empty[kCvStages];
+  __shared__ int s_abort;
+  volatile int* abort_flag = &s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kCvStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kCvWarps);
     }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kCvWarps) {
+    // load warp: tile i of this CTA into stage i % S once its previous
+    // occupant is consumed
+    if (lane != 0) return;
+    int64_t issued = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++issued) {
+      const int s = (int)(issued % kCvStages);
+      if (issued >= kCvStages &&
+          !mbar_wait_bounded(&empty[s], (uint32_t)(((issued / kCvStages) - 1) & 1), abort_flag))
+        break;
+      const int64_t cb = tile / ntt, tt = tile - cb * ntt;
+      mbar_arrive_expect_tx(&full[s], kCvStageBytes);
+      tc::tma_load_2d(sm + s * kCvStageBytes, &tm_x, (int)(cb * CPT), (int)(tt * kCvTok - 3), &full[s]);
+    }
+    // no copy may land in shared memory after the CTA has exited: wait for
+    // the last S issued (each is the latest phase of its stage)
+    for (int64_t i = issued > kCvStages ? issued - kCvStages : 0; i < issued; ++i)
+      mbar_wait_bounded(&full[i % kCvStages], (uint32_t)((i / kCvStages) & 1), nullptr);
+    return;
+  }
+
+  const int64_t T_ = p.T, C = p.C;
+  const T* st = static_cast<const T*>(p.conv_state);
+  T* y = static_cast<T*>(p.y);
+  float2 w[NP][4];  // weights of this thread's channel pairs, by tap
+  int64_t cur_cb = -1;
+  int64_t k = 0;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+    const int s = (int)(k % kCvStages);
+    const int64_t cb = tile / ntt, tt = tile - cb * ntt;
+    const int64_t c0 = cb * CPT + (int64_t)lane * VEC;
+    const int64_t ta = tt * kCvTok + (int64_t)warp * kCvTpt;  // first output token of this thread
+    const bool live = c0 < C && ta < T_;
+    if (cb != cur_cb) {
+      cur_cb = cb;
+      if (c0 < C) {
+        const uint4* wp = reinterpret_cast<const uint4*>(static_cast<const T*>(p.conv_w) + c0 * 4);
+        constexpr int WV = VEC * 4 * (int)sizeof(T) / 16;
+        uint4 wr[WV];
+#pragma unroll
+        for (int i = 0; i < WV; ++i) wr[i] = wp[i];
+        const T* wv = reinterpret_cast<const T*>(wr);
+#pragma unroll
+        for (int q = 0; q < NP; ++q)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) w[q][j] = make_float2(to_f32(wv[(2 * q) * 4 + j]), to_f32(wv[(2 * q + 1) * 4 + j]));
+      }
+    }
+    // fast when the window of every token of this thread lies in one sequence
+    bool fast = false;
+    int n = 0;
+    if (live) {
+      const int64_t tl = ta + kCvTpt - 1 < T_ ? ta + kCvTpt - 1 : T_ - 1;
+      n = seq_of(p.cu_seqlens, p.N, T_, tl);
+      fast = ta + kCvTpt <= T_ && clamp_cu(p.cu_seqlens, n, T_) <= ta - 3;
+    }
+    const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((k / kCvStages) & 1), abort_flag);
+    if (__any_sync(0xffffffffu, !ok)) break;
+    // row u of this thread's window (token ta - 3 + u), its 16 bytes
+    const unsigned char* rows = sm + s * kCvStageBytes + warp * kCvTpt * kCvRowBytes + lane * 16;
+    if (live && fast) {
+      float2 acc[4][NP];  // the four tokens in flight, token jj in acc[jj % 4]
+#pragma unroll
+      for (int u = 0; u < kCvTpt + 3; ++u) {
+        float2 xv[NP];
+        unpack_pairs<T>(*reinterpret_cast<const uint4*>(rows + u * kCvRowBytes), xv);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int jj = u - j;  // the token this row is tap j of
+          if (jj >= 0 && jj < kCvTpt) {
+#pragma unroll
+            for (int q = 0; q < NP; ++q)
+              acc[jj & 3][q] = fma2(w[q][j], xv[q], j == 0 ? make_float2(0.f, 0.f) : acc[jj & 3][q]);
+          }
+        }
+        if (u >= 3) {
+          const int jj = u - 3;
+          *reinterpret_cast<uint4*>(y + (ta + jj) * C + c0) = pack_pairs<T>(acc[jj & 3]);
+        }
+      }
+    } else if (live) {
+      // per token; taps before the sequence's first token come from the old
+      // conv state
+      n = seq_of(p.cu_seqlens, p.N, T_, ta);
+      int64_t s_n = clamp_cu(p.cu_seqlens, n, T_);
+      int64_t s_next = n + 1 < p.N ? clamp_cu(p.cu_seqlens, n + 1, T_) : T_ + 1;
+      for (int jj = 0; jj < kCvTpt; ++jj) {
+        const int64_t t = ta + jj;
+        if (t >= T_) break;
+        while (s_next <= t) {
+          ++n;
+          s_n = s_next;
+          s_next = n + 1 < p.N ? clamp_cu(p.cu_seqlens, n + 1, T_) : T_ + 1;
+        }
+        const int64_t sq = s_n > t ? t : s_n;
+        float2 acc[NP];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t tau = t + j - 3;
+          float2 xv[NP];
+          if (tau >= sq) {
+            unpack_pairs<T>(*reinterpret_cast<const uint4*>(rows + (jj + j) * kCvRowBytes), xv);
+          } else {
+            const int slot = 3 + (int)(tau - sq);
+            const T* sp = st + ((int64_t)n * C + c0) * 3 + slot;
+#pragma unroll
+            for (int q = 0; q < NP; ++q) xv[q] = make_float2(to_f32(sp[(2 * q) * 3]), to_f32(sp[(2 * q + 1) * 3]));
+          }
+#pragma unroll
+          for (int q = 0; q < NP; ++q) acc[q] = fma2(w[q][j], xv[q], j == 0 ? make_float2(0.f, 0.f) : acc[q]);
+        }
+        *reinterpret_cast<uint4*>(y + t * C + c0) = pack_pairs<T>(acc);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
   }
 }
 
@@ -170,14 +284,32 @@ __global__ void __launch_bounds__(256) conv_state_kernel(const ConvArgs p) {
   for (int q = 0; q < 3; ++q) sp[q] = nw[q];
 }
 
+int conv_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
 template <typename T>
-static cudaError_t launch_conv_t(const ConvArgs& p, cudaStream_t stream) {
-  constexpr int VEC = 16 / (int)sizeof(T);
+cudaError_t launch_conv_t(const ConvArgs& p, CUtensorMapDataType dt, cudaStream_t stream) {
   if (p.T > 0) {
-    const int64_t gx = (p.T + kConvTG * kConvTPT - 1) / (kConvTG * kConvTPT);
-    const int64_t gy = (p.C / VEC + kConvCV - 1) / kConvCV;
-    conv_fwd_kernel<T><<<dim3((unsigned)gx, (unsigned)gy), kConvCV * kConvTG, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    CUtensorMap tm;
+    constexpr int CPT = kCvRowBytes / (int)sizeof(T);
+    if (!tc::make_map_2d(&tm, p.x, p.T, p.C, p.C, sizeof(T), dt, CPT, kCvRows,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    const int64_t ntt = (p.T + kCvTok - 1) / kCvTok;
+    const int64_t ncb = ((int64_t)p.C + CPT - 1) / CPT;
+    const int64_t ntiles = ntt * ncb;
+    const int64_t slots = (int64_t)kCvCtasPerSm * conv_sm_count();
+    const int grid = (int)(ntiles < slots ? ntiles : slots);
+    cudaError_t e = cudaFuncSetAttribute(conv_fwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kCvSmem);
+    if (e != cudaSuccess) return e;
+    conv_fwd_kernel<T><<<grid, kCvThreads, kCvSmem, stream>>>(p, tm, ntt, ntiles);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (p.N > 0) {
@@ -188,11 +320,13 @@ static cudaError_t launch_conv_t(const ConvArgs& p, cudaStream_t stream) {
   return cudaSuccess;
 }
 
+}  // namespace
+
 cudaError_t launch_conv(const ConvArgs& p, int32_t dtype, cudaStream_t stream) {
   switch (dtype) {
-    case GDN_F16: return launch_conv_t<__half>(p, stream);
-    case GDN_BF16: return launch_conv_t<__nv_bfloat16>(p, stream);
-    case GDN_F32: return launch_conv_t<float>(p, stream);
+    case GDN_F16: return launch_conv_t<__half>(p, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, stream);
+    case GDN_BF16: return launch_conv_t<__nv_bfloat16>(p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, stream);
+    case GDN_F32: return launch_conv_t<float>(p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, stream);
     default: return cudaErrorInvalidValue;
   }
 }

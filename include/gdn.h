@@ -113,6 +113,7 @@ int64_t gdn_qkv_features(const gdn_dims* dims);
  *   fewer than three tokens).
  *
  * num_seqs    N >= 0 sequences.
+ * total_tokens  0 <= T <= 2^31 - 65 (GDN_ERR_EXTENT beyond).
  * cu_seqlens  device int32 [N+1], cu[0] = 0, non-decreasing, cu[N] =
  *             total_tokens; sequence n owns tokens [cu[n], cu[n+1]). Values
  *             outside [0, total_tokens] are clamped on the device.

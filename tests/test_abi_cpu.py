@@ -184,6 +184,10 @@ def test_conv_and_prefill_and_norm_reject_bad_arguments(lib):
              VP(0x100000), None) == 5  # cu_seqlens misaligned
     assert f(ctypes.byref(d), 1, VP(0x100), 2 ** 62, VP(0x1000), VP(0x9000), VP(0xa000),
              VP(0x100000), None) == 2  # extent overflow
+    # the tiles' TMA row coordinates are int32: 2^31 - 65 tokens is the most
+    big = 1 << 44
+    assert f(ctypes.byref(d), 1, VP(0x100), 2 ** 31 - 64, VP(0x1000), VP(big), VP(big + 0x1000),
+             VP(2 * big), None) == 2
 
     pf = lib.gdn_prefill_chunked
     base = [ctypes.byref(d), 1, VP(0x100), 10, VP(0x1000), 128, VP(0x2000), 128, VP(0x3000), 128,
