@@ -1433,11 +1433,8 @@ __global__ void __cluster_dims__(kSlCta, 1, 1) __launch_bounds__(kSlThreads, 1)
         ok = __all_sync(0xffffffffu, chain_wait(&bar_s[q], ph, abort_flag));
         if (!ok) break;
         tc::fence_after_sync();
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int ks = 2 * q + e;
-          tc::mma_f16_elect(t_kqs, tc::sdesc_at(akq, 128, ks), sdesc_mn64_at(d_s, ks), id64, ks > 0);
-        }
+        tc::mma_f16_elect2(t_kqs, tc::sdesc_at(akq, 128, 2 * q), sdesc_mn64_at(d_s, 2 * q),
+                           tc::sdesc_at(akq, 128, 2 * q + 1), sdesc_mn64_at(d_s, 2 * q + 1), id64, q > 0);
       }
       if (!ok) break;
       tc::mma_commit_elect(&bar_m1);    // the carry's (2)
@@ -1449,11 +1446,8 @@ __global__ void __cluster_dims__(kSlCta, 1, 1) __launch_bounds__(kSlThreads, 1)
         ok = __all_sync(0xffffffffu, chain_wait(&bar_r[q], ph, abort_flag));
         if (!ok) break;
         tc::fence_after_sync();
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int ks = 2 * q + e;
-          tc::mma_f16_elect(tb + T_XY, tc::sdesc_at(atb, 128, ks), sdesc_mn64_at(d_r, ks), id64, ks > 0);
-        }
+        tc::mma_f16_elect2(tb + T_XY, tc::sdesc_at(atb, 128, 2 * q), sdesc_mn64_at(d_r, 2 * q),
+                           tc::sdesc_at(atb, 128, 2 * q + 1), sdesc_mn64_at(d_r, 2 * q + 1), id64, q > 0);
       }
       if (!ok) break;
       tc::mma_commit_elect(&bar_m3);
@@ -1465,17 +1459,15 @@ __global__ void __cluster_dims__(kSlCta, 1, 1) __launch_bounds__(kSlThreads, 1)
                                          chain_wait(&bar_d[2 + hh], ph, abort_flag));
         if (!ok) break;
         tc::fence_after_sync();
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int ks = 2 * hh + e;
-          tc::mma_f16_elect(tb + T_S, tc::sdesc_at(akt, 128, ks), sdesc_mn64_at(d_d, ks), id96, true);
-        }
+        tc::mma_f16_elect2(tb + T_S, tc::sdesc_at(akt, 128, 2 * hh), sdesc_mn64_at(d_d, 2 * hh),
+                           tc::sdesc_at(akt, 128, 2 * hh + 1), sdesc_mn64_at(d_d, 2 * hh + 1), id96, true);
       }
       if (!ok) break;
       tc::mma_commit_elect(&bar_m5);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        tc::mma_f16_elect(t_pd, tc::sdesc_at(apw, 128, ks), sdesc_mn64_at(d_xy, ks), id64, ks > 0);
+      for (int ks = 0; ks < 4; ks += 2)
+        tc::mma_f16_elect2(t_pd, tc::sdesc_at(apw, 128, ks), sdesc_mn64_at(d_xy, ks), tc::sdesc_at(apw, 128, ks + 1),
+                           sdesc_mn64_at(d_xy, ks + 1), id64, ks > 0);
       tc::mma_commit_elect(&bar_free[b]);  // the loader's reuse of buffer b, the output's P Dm
     }
   } else if (warp < 8) {
@@ -1655,6 +1647,11 @@ __global__ void __cluster_dims__(kSlCta, 1, 1) __launch_bounds__(kSlThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_oe[b]);  // this chunk's output accumulators are free
+      if (fused && p.core_out != nullptr && t < L && !to) {
+        float4* cg = reinterpret_cast<float4*>(p.core_out + ((c0 + t) * p.Hv + h) * kD + j0);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) cg[m] = make_float4(o[4 * m], o[4 * m + 1], o[4 * m + 2], o[4 * m + 3]);
+      }
       if (fused) {
         // this slice's sum of squares of row t to the other three CTAs (an
         // asynchronous store that completes on the receiver's mbarrier), and
@@ -1671,13 +1668,36 @@ __global__ void __cluster_dims__(kSlCta, 1, 1) __launch_bounds__(kSlThreads, 1)
             st_async_cluster_f32(map_shared_rank(slot, r), ss, map_shared_rank(nb, r));
         }
       }
-      if (p.core_out != nullptr && t < L && !to) {
-        float4* cg = reinterpret_cast<float4*>(p.core_out + ((c0 + t) * p.Hv + h) * kD + j0);
-#pragma unroll
-        for (int m = 0; m < 8; ++m) cg[m] = make_float4(o[4 * m], o[4 * m + 1], o[4 * m + 2], o[4 * m + 3]);
-      }
       if (!fused) {
+        // the core output: a full chunk leaves as one tile store from a
+        // staging tile (two, by chunk parity, in the z and output tiles'
+        // space, unused without the fused norm; 16-byte group m of row t at
+        // group m ^ (t % 8), the tensor map's 128-byte swizzle); a
+        // sequence's last, partial chunk by rows
+        const bool full_tile = L == kC;
+        if (p.core_out != nullptr && !to) {
+          if (full_tile) {
+            unsigned char* stg = sm + (b ? L_O : L_Z);
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+              *reinterpret_cast<float4*>(stg + t * 128 + ((m ^ (t & 7)) << 4)) =
+                  make_float4(o[4 * m], o[4 * m + 1], o[4 * m + 2], o[4 * m + 3]);
+            fence_proxy_async_smem();
+          } else if (t < L) {
+            float4* cg = reinterpret_cast<float4*>(p.core_out + ((c0 + t) * p.Hv + h) * kD + j0);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) cg[m] = make_float4(o[4 * m], o[4 * m + 1], o[4 * m + 2], o[4 * m + 3]);
+          }
+        }
+        // the previous chunk's tile store has read the other staging tile
+        // (written again next chunk) before the rows pass the barrier
+        if (u == 0 && stored) bulk_wait_read_all();
         if (bar_or(3, kSlOutThreads, to)) break;
+        if (u == 0 && full_tile && p.core_out != nullptr) {
+          tc::tma_store_2d(&tm_o, h * kD + j0, (int)c0, sm + (b ? L_O : L_Z));
+          bulk_commit();
+          stored = true;
+        }
         continue;
       }
       // the gate nw silu(z) while the peers' sums are on their way
@@ -1911,6 +1931,12 @@ cudaError_t launch_prefill_cp(const PrefillArgs& p, void* workspace, cudaStream_
     if (ps.z != nullptr &&
         (!tc::make_map_2d(&mz32, p.z, p.T, vc, vc, 2, bf, kSl, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
          !tc::make_map_2d(&mo32, p.out, p.T, vc, vc, 2, bf, kSl, 64, CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return cudaErrorInvalidValue;
+    // without the fused norm the output map is the fp32 core output's, in
+    // tiles of 64 tokens x 32 columns (128 bytes, swizzled)
+    if (ps.z == nullptr && ps.core_out != nullptr &&
+        !tc::make_map_2d(&mo32, ps.core_out, p.T, vc, vc, 4, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, kSl, 64,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(cp_slice_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L_SMEM);
     if (e != cudaSuccess) return e;

@@ -154,6 +154,19 @@ __device__ __forceinline__ void mma_f16_elect(uint32_t d_tmem, uint64_t a, uint6
       "l"(a), "l"(b), "r"(id), "r"((uint32_t)accumulate)
       : "memory");
 }
+// two consecutive k-steps into one accumulator (the second accumulates)
+// issued by one elected lane of a converged warp
+__device__ __forceinline__ void mma_f16_elect2(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint64_t a1,
+                                               uint64_t b1, uint32_t id, bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %5, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %5, 1;\n\t}" ::"r"(d_tmem),
+      "l"(a0), "l"(b0), "l"(a1), "l"(b1), "r"(id), "r"((uint32_t)accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
