@@ -58,20 +58,6 @@ __device__ __forceinline__ int seq_of(const int32_t* cu, int N, int64_t T, int64
   return lo;
 }
 
-// d = a * b + c on both lanes of a pair, one rounding each (paired fp32 FMA)
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rb, {%4, %5};\n\t"
-      "mov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-
 // 16 bytes of channels as fp32 pairs (channels 2p, 2p + 1 in pair p)
 template <typename T>
 __device__ __forceinline__ void unpack_pairs(const uint4& raw, float2 (&x)[16 / sizeof(T) / 2]) {

@@ -46,7 +46,7 @@ constexpr int kD = 128;  // head_dim
 constexpr int kPrepThreads = 256;
 constexpr int kCarryThreads = 256;  // warps 0-7: the state carry (two threads per value row)
 constexpr int kChainThreads = 512;  // warps 8-15: output and gated norm
-constexpr int kAStride = kC + 1;    // padded row pitch of the fp32 A matrix
+constexpr int kAStride = kC + 4;    // padded row pitch of the fp32 A matrix (16-byte rows)
 constexpr int kMaxRep = 16;         // V heads per K head on this path
 // (V head, sequence) pairs up to which the sliced carry (four CTAs each) is
 // chosen, and the workspace holds an fp32 core output for its separate norm
@@ -186,8 +186,8 @@ __global__ void __launch_bounds__(1024) cp_index_kernel(const PrefillArgs p, con
 // scales are taken from it; the per-V-head matrices then reuse its space.
 constexpr uint32_t P_OFF_KQ = 0;       // bf16 [128][128 i] SW128 (TMA): rows 0-63 k, 64-127 q
 constexpr uint32_t P_OFF_A = 0;        // fp32 [64][65]
-constexpr uint32_t P_OFF_T = 16640;    // fp32 [64][64] Tm (products in its upper triangle)
-constexpr uint32_t P_SMEM = 33024 + 1024;
+constexpr uint32_t P_OFF_T = kC * kAStride * 4;  // fp32 [64][64] Tm (products in its upper triangle)
+constexpr uint32_t P_SMEM = P_OFF_T + kC * kC * 4 + 1024;
 
 __global__ void __launch_bounds__(kPrepThreads, 4)
     cp_prep_kernel(const PrefillArgs p, const CpWork w, const __grid_constant__ CUtensorMap tm_q,
@@ -408,9 +408,11 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       if (is_a) {
         const float bk = sbeta[r][t] * sinvk[t];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int s = 32 * hc + e;
-          Ap[t * kAStride + s] = s < t ? bk * pr[e] : 0.f;
+        for (int m = 0; m < 8; ++m) {
+          const int s = 32 * hc + 4 * m;
+          *reinterpret_cast<float4*>(Ap + t * kAStride + s) =
+              make_float4(s < t ? bk * pr[4 * m] : 0.f, s + 1 < t ? bk * pr[4 * m + 1] : 0.f,
+                          s + 2 < t ? bk * pr[4 * m + 2] : 0.f, s + 3 < t ? bk * pr[4 * m + 3] : 0.f);
         }
       } else {
         const float iqt = sinvq[t];
@@ -435,9 +437,17 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
 #pragma unroll
       for (int m = 1; m < 16; ++m) {
         const float* arow = Ap + (b0 + m) * kAStride + b0;
+        float av[16];
+#pragma unroll
+        for (int q4 = 0; q4 < 16; q4 += 4) {
+          if (q4 < m) {
+            const float4 v = *reinterpret_cast<const float4*>(arow + q4);
+            av[q4] = v.x, av[q4 + 1] = v.y, av[q4 + 2] = v.z, av[q4 + 3] = v.w;
+          }
+        }
         float acc = 0.f;
 #pragma unroll
-        for (int q = 0; q < m; ++q) acc = fmaf(arow[q], x[q], acc);
+        for (int q = 0; q < m; ++q) acc = fmaf(av[q], x[q], acc);
         if (m > l) x[m] = -acc;
       }
       if (lane < 16) {
@@ -464,26 +474,28 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       // columns per thread; X at Tm[r][32 + 16 B + c]
       const int B = tid >> 7, u = tid & 127, r = u >> 3, c = (u & 7) * 2, o = 32 * B;
       const float* arow = Ap + (o + 16 + r) * kAStride + o;
-      float x0 = 0.f, x1 = 0.f;
+      float2 x = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float2 tv = *reinterpret_cast<const float2*>(Tp + (o + q) * kC + o + c);
-        const float av = arow[q];
-        x0 = fmaf(av, tv.x, x0);
-        x1 = fmaf(av, tv.y, x1);
+      for (int q4 = 0; q4 < 16; q4 += 4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(arow + q4);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          x = fma2(make_float2(av[u], av[u]), *reinterpret_cast<const float2*>(Tp + (o + q4 + u) * kC + o + c), x);
       }
-      *reinterpret_cast<float2*>(Tp + r * kC + 32 + 16 * B + c) = make_float2(x0, x1);
+      *reinterpret_cast<float2*>(Tp + r * kC + 32 + 16 * B + c) = x;
       __syncthreads();
       const float* trow = Tp + (o + 16 + r) * kC + o + 16;
-      float y0 = 0.f, y1 = 0.f;
+      float2 y = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float2 xv = *reinterpret_cast<const float2*>(Tp + q * kC + 32 + 16 * B + c);
-        const float tv = trow[q];
-        y0 = fmaf(tv, xv.x, y0);
-        y1 = fmaf(tv, xv.y, y1);
+      for (int q4 = 0; q4 < 16; q4 += 4) {
+        const float4 t4 = *reinterpret_cast<const float4*>(trow + q4);
+        const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          y = fma2(make_float2(tv[u], tv[u]), *reinterpret_cast<const float2*>(Tp + (q4 + u) * kC + 32 + 16 * B + c), y);
       }
-      *reinterpret_cast<float2*>(Tp + (o + 16 + r) * kC + o + c) = make_float2(-y0, -y1);
+      *reinterpret_cast<float2*>(Tp + (o + 16 + r) * kC + o + c) = make_float2(-y.x, -y.y);
       __syncthreads();
     }
     {
@@ -492,33 +504,39 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       const int r0 = (tid >> 4) * 2, c0 = (tid & 15) * 2;
       const float* a0 = Ap + (32 + r0) * kAStride;
       const float* a1 = a0 + kAStride;
-      float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+      float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const float2 tv = *reinterpret_cast<const float2*>(Tp + q * kC + c0);
-        const float av0 = a0[q], av1 = a1[q];
-        x00 = fmaf(av0, tv.x, x00);
-        x01 = fmaf(av0, tv.y, x01);
-        x10 = fmaf(av1, tv.x, x10);
-        x11 = fmaf(av1, tv.y, x11);
+      for (int q4 = 0; q4 < 32; q4 += 4) {
+        const float4 p0 = *reinterpret_cast<const float4*>(a0 + q4);
+        const float4 p1 = *reinterpret_cast<const float4*>(a1 + q4);
+        const float av0[4] = {p0.x, p0.y, p0.z, p0.w}, av1[4] = {p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 tv = *reinterpret_cast<const float2*>(Tp + (q4 + u) * kC + c0);
+          x0 = fma2(make_float2(av0[u], av0[u]), tv, x0);
+          x1 = fma2(make_float2(av1[u], av1[u]), tv, x1);
+        }
       }
-      *reinterpret_cast<float2*>(Tp + r0 * kC + 32 + c0) = make_float2(x00, x01);
-      *reinterpret_cast<float2*>(Tp + (r0 + 1) * kC + 32 + c0) = make_float2(x10, x11);
+      *reinterpret_cast<float2*>(Tp + r0 * kC + 32 + c0) = x0;
+      *reinterpret_cast<float2*>(Tp + (r0 + 1) * kC + 32 + c0) = x1;
       __syncthreads();
       const float* t0 = Tp + (32 + r0) * kC + 32;
       const float* t1 = t0 + kC;
-      float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+      float2 y0 = make_float2(0.f, 0.f), y1 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const float2 xv = *reinterpret_cast<const float2*>(Tp + q * kC + 32 + c0);
-        const float tv0 = t0[q], tv1 = t1[q];
-        y00 = fmaf(tv0, xv.x, y00);
-        y01 = fmaf(tv0, xv.y, y01);
-        y10 = fmaf(tv1, xv.x, y10);
-        y11 = fmaf(tv1, xv.y, y11);
+      for (int q4 = 0; q4 < 32; q4 += 4) {
+        const float4 p0 = *reinterpret_cast<const float4*>(t0 + q4);
+        const float4 p1 = *reinterpret_cast<const float4*>(t1 + q4);
+        const float tv0[4] = {p0.x, p0.y, p0.z, p0.w}, tv1[4] = {p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 xv = *reinterpret_cast<const float2*>(Tp + (q4 + u) * kC + 32 + c0);
+          y0 = fma2(make_float2(tv0[u], tv0[u]), xv, y0);
+          y1 = fma2(make_float2(tv1[u], tv1[u]), xv, y1);
+        }
       }
-      *reinterpret_cast<float2*>(Tp + (32 + r0) * kC + c0) = make_float2(-y00, -y01);
-      *reinterpret_cast<float2*>(Tp + (32 + r0 + 1) * kC + c0) = make_float2(-y10, -y11);
+      *reinterpret_cast<float2*>(Tp + (32 + r0) * kC + c0) = make_float2(-y0.x, -y0.y);
+      *reinterpret_cast<float2*>(Tp + (32 + r0 + 1) * kC + c0) = make_float2(-y1.x, -y1.y);
       __syncthreads();
     }
     // Tb = Tm diag(beta) as hi + lo bf16, zero above the diagonal; 16
@@ -527,9 +545,12 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       const int e0 = 16 * tid, tr = e0 >> 6, u0 = e0 & 63;
       float x[16];
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const int s = u0 + m;
-        x[m] = s <= tr ? Tp[tr * kC + s] * sbeta[r][s] : 0.f;
+      for (int m4 = 0; m4 < 16; m4 += 4) {
+        const float4 tv = *reinterpret_cast<const float4*>(Tp + tr * kC + u0 + m4);
+        const float4 bv = *reinterpret_cast<const float4*>(&sbeta[r][u0 + m4]);
+        const float t4[4] = {tv.x, tv.y, tv.z, tv.w}, b4[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[m4 + u] = u0 + m4 + u <= tr ? t4[u] * b4[u] : 0.f;
       }
       uint4 h0, l0, h1, l1;
       split8(x, h0, l0);
