@@ -474,31 +474,42 @@ def run_prefill(args, peaks, ws):
         gdn.gdn_prefill_chunked(d, cu, q, k, v, a, b, dp, dt, state, core_out=None, z=z,
                                 norm_w=nw, out=out, workspace=wsb, flags=flags)
 
-    def timed(flags, n):
+    def timed(flags, n, graph):
+        # graph: the call captured once as a CUDA graph (its tensor maps
+        # encoded at capture) and each timed call one replay, so the host's
+        # submission work is outside the events; else one eager call
         for _ in range(3):
             state.copy_(s0)
             call(flags)
         torch.cuda.synchronize()
+        run = lambda: call(flags)
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                call(flags)
+            torch.cuda.synchronize()
+            run = g.replay
         times = []
         for i in range(n):
             state.copy_(s0)
             flush.fill_(float(i))
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            call(flags)
+            run()
             e1.record(stream)
             torch.cuda.synchronize()
             times.append(e0.elapsed_time(e1) * 1e-3)
         return _barrier_max(statistics.mean(times), ws)
 
     n = max(3, min(args.steps, 20))
-    t = timed(0, n)
+    t = timed(0, n, True)
+    t_eager = timed(0, n, False)
     # the library's default carry for one sequence of 32 V heads: the sliced
     # one (4 CTAs per V head) when Hv N <= 64 and 4 Hv N <= 2 x SMs, its
     # gated norm then a separate pass; the whole-row carry timed beside it
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     sliced = 32 * 1 <= 64 and 4 * 32 <= 2 * sms
-    t_whole = timed(gdn.GDN_PREFILL_CARRY_WHOLE, n)
+    t_whole = timed(gdn.GDN_PREFILL_CARRY_WHOLE, n, True)
 
     # end to end through the C ABI with host buffers: the call's inputs (q, k,
     # v, a, b, z) copied from pinned host memory, the call, the gated output
@@ -534,6 +545,11 @@ def run_prefill(args, peaks, ws):
             "carry": ("sliced: cp_slice_kernel, 4 CTAs per V head, then cp_norm_kernel" if sliced
                       else "whole rows: cp_chain_kernel, 1 CTA per V head"),
             "whole_row_carry_ms_per_call": round(t_whole * 1e3, 4),
+            "eager_ms_per_call": round(t_eager * 1e3, 4),
+            "timing": "one call per timed region (state reset, 512 MiB overwritten before it): the "
+                      "call captured once as a CUDA graph and replayed between two CUDA events; "
+                      "eager_ms_per_call times the same call issued from the host between the "
+                      "events (host submission included)",
             "roofline": {"bound": "tensor", "achieved": round(flops / t / 1e12, 3),
                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(flops / t / 1e12 / peaks["bf16_tflops"], 5),
@@ -545,7 +561,8 @@ def run_prefill(args, peaks, ws):
                          "algorithmic_flops_per_call": flops,
                          "algorithmic_bytes_per_call": byts,
                          "hbm_frac": round(byts / t / 1e9 / peaks["hbm_gbs"], 4),
-                         "timed": "the whole call (chunk index, prep, carry, norm launches)",
+                         "timed": "the whole call (chunk index, prep, carry, norm launches), "
+                                  "graph replay",
                          "kernel": ("cp_prep_kernel + cp_slice_kernel + cp_norm_kernel" if sliced
                                     else "cp_prep_kernel + cp_chain_kernel")},
            "e2e": {"value": round(ws * T / t_e2e, 1), "unit": "tokens/s",
@@ -598,19 +615,34 @@ def run_varlen(args, ws, peaks):
         for (xd, ad, bd, zd) in dec:
             gdn.gdn_decode_step(d, xd, ad, bd, dp, dt, conv_w, cs, st, z=zd, norm_w=nw, out=dout)
 
-    path()
-    torch.cuda.synchronize()
-    times = []
-    for _ in range(3):
+    def graphed(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g.replay
+
+    def time_calls(run, reset, n):
+        times = []
+        for _ in range(n):
+            reset()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e-3)
+        return times
+
+    def reset_all():
         cs.copy_(cs0)
         st.copy_(s0)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        path()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        times.append(e0.elapsed_time(e1) * 1e-3)
-    t = _barrier_max(statistics.mean(times), ws)
+
+    path()
+    torch.cuda.synchronize()
+    t_eager = _barrier_max(statistics.mean(time_calls(path, reset_all, 3)), ws)
+    path_g = graphed(path)
+    t = _barrier_max(statistics.mean(time_calls(path_g, reset_all, 3)), ws)
     tokens = T + 16 * N
 
     # the prefill call alone (the core of the path), on the conv output of the
@@ -619,29 +651,13 @@ def run_varlen(args, ws, peaks):
         gdn.gdn_prefill_chunked(d, cu, y[:, :qk], y[:, qk:2 * qk], y[:, 2 * qk:], a, b, dp, dt,
                                 st, z=z, norm_w=nw, out=out, workspace=wsb)
 
-    ptimes = []
-    for _ in range(4):
-        st.copy_(s0)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        pre()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ptimes.append(e0.elapsed_time(e1) * 1e-3)
-    tp = _barrier_max(statistics.mean(ptimes[1:]), ws)
+    pre_g = graphed(pre)
+    tp = _barrier_max(statistics.mean(time_calls(pre_g, lambda: st.copy_(s0), 4)[1:]), ws)
 
     # the conv update alone (two launches: the outputs, then the state), the
     # conv states reset before each call
-    ctimes = []
-    for _ in range(4):
-        cs.copy_(cs0)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        gdn.gdn_conv_update(d, cu, x, conv_w, cs, y)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ctimes.append(e0.elapsed_time(e1) * 1e-3)
-    tc = _barrier_max(statistics.mean(ctimes[1:]), ws)
+    conv_g = graphed(lambda: gdn.gdn_conv_update(d, cu, x, conv_w, cs, y))
+    tc = _barrier_max(statistics.mean(time_calls(conv_g, lambda: cs.copy_(cs0), 4)[1:]), ws)
     cbytes = 2 * T * C * 2 + 2 * N * C * 3 * 2 + C * 4 * 2
     Cc = 64
     flops = T * (Hv * (6 * D * D + 6 * Cc * D + Cc * Cc / 3) + Hk * 4 * Cc * D)
@@ -650,6 +666,10 @@ def run_varlen(args, ws, peaks):
     return {"workload": "varlen: 8 sequences (34,482 tokens) conv update + chunked prefill with "
                         "fused norm + 16 decode steps, Hk=16 Hv=64 D=128, Tiled, bf16",
             "value": round(ws * tokens / t, 1), "unit": "tokens/s", "ms_per_pass": round(t * 1e3, 4),
+            "eager_ms_per_pass": round(t_eager * 1e3, 4),
+            "timing": "each pass, call or update captured once as a CUDA graph and replayed between "
+                      "two CUDA events, states reset before each; eager_ms_per_pass issues the pass "
+                      "from the host between the events",
             "launches_per_pass": 2 + 3 + 16,
             "prefill_core": {"value": round(ws * T / tp, 1), "unit": "tokens/s",
                              "ms_per_call": round(tp * 1e3, 4),
@@ -661,7 +681,7 @@ def run_varlen(args, ws, peaks):
                                           "hbm_frac": round(byts / tp / 1e9 / peaks["hbm_gbs"], 4),
                                           "peak_source": peaks["source"]},
                              "timed": "the gdn_prefill_chunked call alone (index, prep, chain), "
-                                      "fused norm, states reset before each of 3 timed calls"},
+                                      "fused norm, states reset before each of 3 timed replays"},
             "conv_update": {"us_per_call": round(tc * 1e6, 2),
                             "roofline": {"bound": "hbm", "achieved": round(cbytes / tc / 1e9, 1),
                                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -670,7 +690,7 @@ def run_varlen(args, ws, peaks):
                                          "peak_source": peaks["source"]},
                             "kernel": "conv_fwd_kernel + conv_state_kernel",
                             "timed": "the gdn_conv_update call alone, conv states reset before "
-                                     "each of 3 timed calls"}}
+                                     "each of 3 timed replays"}}
 
 
 def run_batch1(args, ws):
