@@ -345,17 +345,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const float inv_k = 1.f / sqrtf(kk + p.l2_eps);
     const float kq = qkr * inv_q * inv_k * p.scale;
     constexpr int NV4 = G::NV4, RPL = G::RPL;
-    float kr[4 * NV4], qr[4 * NV4];
+    float4 kr[NV4], qr[NV4];  // this lane's columns of the normalised k and scaled q
     {
       const float sqs = inv_q * p.scale;
 #pragma unroll
       for (int m = 0; m < NV4; ++m) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int col = 4 * sub + 4 * LPR * m + e;
-          kr[4 * m + e] = sk[buf][col] * inv_k;
-          qr[4 * m + e] = sq[buf][col] * sqs;
-        }
+        const int col = 4 * sub + 4 * LPR * m;
+        kr[m] = make_float4(sk[buf][col] * inv_k, sk[buf][col + 1] * inv_k, sk[buf][col + 2] * inv_k,
+                            sk[buf][col + 3] * inv_k);
+        qr[m] = make_float4(sq[buf][col] * sqs, sq[buf][col + 1] * sqs, sq[buf][col + 2] * sqs,
+                            sq[buf][col + 3] * sqs);
       }
     }
 
@@ -389,20 +388,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           float pk[RPL], pq[RPL];
 #pragma unroll
           for (int u = 0; u < RPL; ++u) {
-            float pk4[NV4], pq4[NV4];
-#pragma unroll
-            for (int m = 0; m < NV4; ++m) {
-              pk4[m] = s4[u][m].x * kr[4 * m + 0];
-              pq4[m] = s4[u][m].x * qr[4 * m + 0];
-              pk4[m] = fmaf(s4[u][m].y, kr[4 * m + 1], pk4[m]);
-              pq4[m] = fmaf(s4[u][m].y, qr[4 * m + 1], pq4[m]);
-              pk4[m] = fmaf(s4[u][m].z, kr[4 * m + 2], pk4[m]);
-              pq4[m] = fmaf(s4[u][m].z, qr[4 * m + 2], pq4[m]);
-              pk4[m] = fmaf(s4[u][m].w, kr[4 * m + 3], pk4[m]);
-              pq4[m] = fmaf(s4[u][m].w, qr[4 * m + 3], pq4[m]);
-            }
-            pk[u] = sum_groups<NV4>(pk4);
-            pq[u] = sum_groups<NV4>(pq4);
+            pk[u] = row_dot<NV4>(s4[u], kr);
+            pq[u] = row_dot<NV4>(s4[u], qr);
           }
 #pragma unroll
           for (int o = LPR / 2; o > 0; o >>= 1) {
@@ -418,15 +405,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             const float d = beta * (sv[buf][r][row] - alpha * pk[u]);
             const float o = fmaf(alpha, pq[u], d * kq);
             float* grow = gS + (size_t)row * D;
+            row_update<NV4>(s4[u], kr, alpha, d);
 #pragma unroll
-            for (int m = 0; m < NV4; ++m) {
-              float4 n4;
-              n4.x = fmaf(d, kr[4 * m + 0], alpha * s4[u][m].x);
-              n4.y = fmaf(d, kr[4 * m + 1], alpha * s4[u][m].y);
-              n4.z = fmaf(d, kr[4 * m + 2], alpha * s4[u][m].z);
-              n4.w = fmaf(d, kr[4 * m + 3], alpha * s4[u][m].w);
-              __stcs(reinterpret_cast<float4*>(grow + 4 * sub + 4 * LPR * m), n4);
-            }
+            for (int m = 0; m < NV4; ++m) __stcs(reinterpret_cast<float4*>(grow + 4 * sub + 4 * LPR * m), s4[u][m]);
             if (sub == 0) so[buf][r][row] = o;
           }
         }

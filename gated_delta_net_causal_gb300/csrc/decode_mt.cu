@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kMtThreads, 2)
   __shared__ float sq[kMtTMax][D], sk[kMtTMax][D];
   __shared__ float sv[REPMAX][kMtTMax][D], so[REPMAX][kMtTMax][D];
   __shared__ float sgate[REPMAX][kMtTMax][2];
-  __shared__ float sinv[kMtCW][3][kMtTMax];  // per warp: 1/|q|, 1/|k|, k.q scale
+  __shared__ float skq[kMtTMax];  // per token: k.q of the normalised vectors, scaled
   __shared__ float snw[D];
   __shared__ __align__(8) uint64_t full_bar[kMtMaxStages], empty_bar[kMtMaxStages];
   __shared__ int s_abort;
@@ -198,9 +198,11 @@ __global__ void __launch_bounds__(kMtThreads, 2)
     }
     mt_consumer_sync();
 
-    // (2) l2 norms of every token's q and k and their product, each warp over
-    // all D, kept per warp
-    for (int t = 0; t < NT; ++t) {
+    // (2) warp t: the l2 norms of token t's q and k and their product, then
+    // k normalised and q normalised and scaled, in place (the one-token
+    // kernel's arithmetic, token by token)
+    if (warp < NT) {
+      const int t = warp;
       float qq = 0.f, kk = 0.f, qkr = 0.f;
 #pragma unroll
       for (int i = lane; i < D; i += 32) {
@@ -214,13 +216,15 @@ __global__ void __launch_bounds__(kMtThreads, 2)
       qkr = group_sum<32>(qkr);
       const float inv_q = 1.f / sqrtf(qq + p.l2_eps);
       const float inv_k = 1.f / sqrtf(kk + p.l2_eps);
-      if (lane == 0) {
-        sinv[warp][0][t] = inv_q;
-        sinv[warp][1][t] = inv_k;
-        sinv[warp][2][t] = qkr * inv_q * inv_k * p.scale;
+      const float sqs = inv_q * p.scale;
+      if (lane == 0) skq[t] = qkr * inv_q * inv_k * p.scale;
+#pragma unroll
+      for (int i = lane; i < D; i += 32) {
+        sk[t][i] *= inv_k;
+        sq[t][i] *= sqs;
       }
     }
-    __syncwarp();
+    mt_consumer_sync();
 
     // (3) the state pass: each row read once from the ring, T token steps in
     // registers, written back once
@@ -243,36 +247,19 @@ __global__ void __launch_bounds__(kMtThreads, 2)
               s4[u][m] = *reinterpret_cast<const float4*>(srow + 4 * sub + 4 * LPR * m);
           }
           for (int t = 0; t < NT; ++t) {
-            const float sqs = sinv[warp][0][t] * p.scale;
-            const float inv_k = sinv[warp][1][t];
-            const float kq = sinv[warp][2][t];
-            float kr[4 * NV4], qr[4 * NV4];
+            const float kq = skq[t];
+            float4 kr[NV4], qr[NV4];
 #pragma unroll
             for (int m = 0; m < NV4; ++m) {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int col = 4 * sub + 4 * LPR * m + e;
-                kr[4 * m + e] = sk[t][col] * inv_k;
-                qr[4 * m + e] = sq[t][col] * sqs;
-              }
+              const int col = 4 * sub + 4 * LPR * m;
+              kr[m] = *reinterpret_cast<const float4*>(&sk[t][col]);
+              qr[m] = *reinterpret_cast<const float4*>(&sq[t][col]);
             }
             float pk[RPL], pq[RPL];
 #pragma unroll
             for (int u = 0; u < RPL; ++u) {
-              float pk4[NV4], pq4[NV4];
-#pragma unroll
-              for (int m = 0; m < NV4; ++m) {
-                pk4[m] = s4[u][m].x * kr[4 * m + 0];
-                pq4[m] = s4[u][m].x * qr[4 * m + 0];
-                pk4[m] = fmaf(s4[u][m].y, kr[4 * m + 1], pk4[m]);
-                pq4[m] = fmaf(s4[u][m].y, qr[4 * m + 1], pq4[m]);
-                pk4[m] = fmaf(s4[u][m].z, kr[4 * m + 2], pk4[m]);
-                pq4[m] = fmaf(s4[u][m].z, qr[4 * m + 2], pq4[m]);
-                pk4[m] = fmaf(s4[u][m].w, kr[4 * m + 3], pk4[m]);
-                pq4[m] = fmaf(s4[u][m].w, qr[4 * m + 3], pq4[m]);
-              }
-              pk[u] = sum_groups<NV4>(pk4);
-              pq[u] = sum_groups<NV4>(pq4);
+              pk[u] = row_dot<NV4>(s4[u], kr);
+              pq[u] = row_dot<NV4>(s4[u], qr);
             }
 #pragma unroll
             for (int o = LPR / 2; o > 0; o >>= 1) {
@@ -288,13 +275,7 @@ __global__ void __launch_bounds__(kMtThreads, 2)
               const int row = rowv[u];
               const float d = beta * (sv[r][t][row] - alpha * pk[u]);
               const float o = fmaf(alpha, pq[u], d * kq);
-#pragma unroll
-              for (int m = 0; m < NV4; ++m) {
-                s4[u][m].x = fmaf(d, kr[4 * m + 0], alpha * s4[u][m].x);
-                s4[u][m].y = fmaf(d, kr[4 * m + 1], alpha * s4[u][m].y);
-                s4[u][m].z = fmaf(d, kr[4 * m + 2], alpha * s4[u][m].z);
-                s4[u][m].w = fmaf(d, kr[4 * m + 3], alpha * s4[u][m].w);
-              }
+              row_update<NV4>(s4[u], kr, alpha, d);
               if (sub == 0) so[r][t][row] = o;
             }
           }

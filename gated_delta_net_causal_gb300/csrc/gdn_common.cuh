@@ -78,6 +78,35 @@ __device__ __forceinline__ float gate_g(int decay, float param, float dt_bias, f
 
 // The per-lane partial sums of a decode row over its NV4 column groups, in
 // the one fixed order both decode kernels use (so they agree bit for bit).
+// Dot product of a lane's share of a state row with the matching columns of
+// a vector, both as NV4 groups of four: lanes (x, y) and (z, w) of the
+// groups accumulate in one paired FMA chain, group after group, and the two
+// halves are added last. The one- and multi-token decode kernels both use
+// it, so they round identically.
+template <int NV4>
+__device__ __forceinline__ float row_dot(const float4 (&s)[NV4], const float4 (&v)[NV4]) {
+  float2 a = fma2(make_float2(s[0].x, s[0].y), make_float2(v[0].x, v[0].y), make_float2(0.f, 0.f));
+  float2 b = fma2(make_float2(s[0].z, s[0].w), make_float2(v[0].z, v[0].w), make_float2(0.f, 0.f));
+#pragma unroll
+  for (int m = 1; m < NV4; ++m) {
+    a = fma2(make_float2(s[m].x, s[m].y), make_float2(v[m].x, v[m].y), a);
+    b = fma2(make_float2(s[m].z, s[m].w), make_float2(v[m].z, v[m].w), b);
+  }
+  return (a.x + b.x) + (a.y + b.y);
+}
+// s <- alpha s + d v on a lane's groups (one rounding of alpha s, then one
+// FMA per element)
+template <int NV4>
+__device__ __forceinline__ void row_update(float4 (&s)[NV4], const float4 (&v)[NV4], float alpha, float d) {
+  const float2 al = make_float2(alpha, alpha), dd = make_float2(d, d), nz = make_float2(-0.f, -0.f);
+#pragma unroll
+  for (int m = 0; m < NV4; ++m) {
+    const float2 lo = fma2(dd, make_float2(v[m].x, v[m].y), fma2(al, make_float2(s[m].x, s[m].y), nz));
+    const float2 hi = fma2(dd, make_float2(v[m].z, v[m].w), fma2(al, make_float2(s[m].z, s[m].w), nz));
+    s[m] = make_float4(lo.x, lo.y, hi.x, hi.y);
+  }
+}
+
 template <int NV4>
 __device__ __forceinline__ float sum_groups(const float (&a)[NV4]) {
   static_assert(NV4 == 3 || NV4 == 4, "three or four column groups per lane");
