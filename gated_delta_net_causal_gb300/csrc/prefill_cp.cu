@@ -1499,11 +1499,16 @@ __global__ void __cluster_dims__(kSlCta, 1, 1) __launch_bounds__(kSlThreads, 1)
     const int i = 32 * q + lane;  // key column (state lane)
     float* gS = p.state + (((size_t)n * p.Hv + h) * kD + j0 + jl) * kD + i;  // row e at gS[e * kD]
 
-    // the state's 16 values -> hi/lo B tiles, then the accumulator: the
-    // first partial holds the state rescaled by gl, the other two restart
-    // from zero
+    // the state's 16 values -> hi/lo B tiles, handed to (1) at once, then
+    // the accumulator: the first partial holds the state rescaled by gl, the
+    // other two restart from zero. Only (5) reads the accumulator, after
+    // every carry warp's next hand-off, each of which waits for this warp's
+    // TMEM stores first.
     auto store_state = [&](float (&v)[16], float gl) {
       put16_hilo(sm, L_SH, L_SL, i, jl, v);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_s[q]);
 #pragma unroll
       for (int e = 0; e < 16; ++e) v[e] *= gl;
       tc::tmem_st16(tl + T_S + jl, v);
@@ -1511,7 +1516,6 @@ __global__ void __cluster_dims__(kSlCta, 1, 1) __launch_bounds__(kSlThreads, 1)
       for (int e = 0; e < 16; ++e) v[e] = 0.f;
       tc::tmem_st16(tl + T_S + kSl + jl, v);
       tc::tmem_st16(tl + T_S + 2 * kSl + jl, v);
-      operands_done(&bar_s[q], lane);
     };
 
     bool to = !chain_wait(&bar_v[0], 0, abort_flag);
