@@ -413,11 +413,12 @@ def gdn_linear(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, bias: Optional
     _need(bias, "bias", N)
     need = gdn_linear_workspace_size(M, N, K)
     if isinstance(workspace, str) and workspace == "auto":
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device) if need > 0 else None
     _need(workspace, "workspace", need)
+    ws_ptr = _ptr(workspace, "workspace", torch.uint8) if workspace is not None else None
     _check(library().gdn_linear(int(M), int(N), int(K), x.data_ptr(), int(x.stride(0)), _ptr(w, "w", bf),
                                 _ptr(bias, "bias", torch.float32), y.data_ptr(), int(y.stride(0)),
-                                _ptr(workspace, "workspace", torch.uint8), int(workspace.numel()),
+                                ws_ptr, int(workspace.numel()) if workspace is not None else 0,
                                 _stream(stream)), "gdn_linear")
     return y
 

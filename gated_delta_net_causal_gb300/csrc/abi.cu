@@ -422,10 +422,10 @@ gdn_status gdn_linear(int32_t M, int32_t N, int32_t K, const void* x, int64_t x_
   int64_t need = 0;
   gdn_status st = gdn_linear_workspace_size(M, N, K, &need);
   if (st != GDN_OK) return st;
-  if (!x || !w || !y || !workspace) return GDN_ERR_INVALID_ARG;
+  if (!x || !w || !y || (need > 0 && !workspace)) return GDN_ERR_INVALID_ARG;
   if (x_stride < K || x_stride % 8 != 0 || y_stride < N || y_stride % 8 != 0) return GDN_ERR_INVALID_ARG;
   if (workspace_bytes < need) return GDN_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) ||
       (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)))
     return GDN_ERR_ALIGN;
   const Range ry = range_of(y, ((int64_t)(M - 1) * y_stride + N) * 2), rw = range_of(workspace, need);

@@ -48,8 +48,6 @@ struct LinearRoute {
 struct LinearArgs {
   int32_t M, N, K, splits, stages;  // splits and stages are chosen by launch_linear
   const float* bias;        // [N] or null
-  float* acc;               // split-K partial slices [splits][M][N] (set by launch_linear)
-  uint32_t* tickets;        // split-K tickets [N / 64] (set by launch_linear)
   LinearRoute route;
 };
 

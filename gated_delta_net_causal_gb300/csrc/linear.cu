@@ -12,12 +12,12 @@
 // stored. The output columns may be routed to up to four destinations (the
 // fused input projection writes qkv | z | b | a from one launch).
 //
-// Split-K for narrow outputs (few bands): grid.y splits the K steps; each
-// CTA stores its fp32 partial sums in a slice of its own, then takes a
-// ticket; the last CTA of a band (no CTA ever waits for another) adds the
-// slices in split order (so the result does not depend on which CTA ran
-// first), the bias, rounds and stores. The tickets are zeroed on the stream
-// before the launch.
+// Split-K for narrow outputs (few bands): grid.y splits the K steps and
+// the splits of a band form one thread-block cluster (at most 8). Each CTA
+// keeps its fp32 partial tile in its own shared memory; the cluster adds the
+// tiles in split order over distributed shared memory (so the result does
+// not depend on which CTA ran first), adds the bias, rounds and stores. No
+// global scratch, fence or atomic is involved.
 #include <cuda.h>
 #include <string.h>
 
@@ -41,7 +41,7 @@ constexpr int kLMaxStages = 12;
 constexpr uint32_t kLStageBudget = 96 * 1024;
 constexpr int kLCtasPerSm = 2;
 constexpr int kLThreads = 128;  // warp 0 lane 0 loads, warp 1 issues MMAs, all four store
-constexpr int kLMaxSplits = 16;
+constexpr int kLMaxSplits = 8;  // the portable cluster size
 
 __global__ void __launch_bounds__(kLThreads, kLCtasPerSm)
     linear_kernel(const LinearArgs p, const __grid_constant__ CUtensorMap tm_x,
@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(kLThreads, kLCtasPerSm)
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) uint64_t full[kLMaxStages], empty[kLMaxStages], done;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_abort, s_last;
+  __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int band = blockIdx.x, n0 = band * kLBN;
@@ -151,37 +151,44 @@ __global__ void __launch_bounds__(kLThreads, kLCtasPerSm)
 #pragma unroll
       for (int g8 = 0; g8 < kLBN / 8; ++g8) store8(m, g8, v + 8 * g8);
   } else {
-    // partial sums into this split's slice, then a ticket; the band's last
-    // CTA adds the slices (past its own fence) in split order, every thread
-    // taking (row, 8-column group) units
-    const size_t slice = (size_t)p.M * p.N;
+    // the K splits of a band are one cluster. This split's fp32 partial tile
+    // goes into its own shared memory (the ring is idle: every load it
+    // issued was consumed by an MMA that has completed), 16-byte group c of
+    // row m at group c ^ (m % 16); after a cluster barrier every CTA sums
+    // its share of the (row, 8-column group) units over the cluster's tiles
+    // in rank order, so the result does not depend on which CTA ran first;
+    // a second barrier keeps each tile in place until its peers have read
+    // it. Every thread reaches both barriers, whatever happened before.
+    float* part = reinterpret_cast<float*>(sm);
     if (m < p.M) {
-      float4* prow = reinterpret_cast<float4*>(p.acc + blockIdx.y * slice + (size_t)m * p.N + n0);
 #pragma unroll
-      for (int c = 0; c < kLBN / 4; ++c) prow[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      for (int c = 0; c < kLBN / 4; ++c)
+        *reinterpret_cast<float4*>(part + m * kLBN + 4 * (c ^ (m & 15))) =
+            make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
     }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(p.tickets + band, 1u) == (unsigned)(p.splits - 1);
-    __syncthreads();
-    if (s_last && !*abort_flag) {
-      __threadfence();
-      for (int u = tid; u < p.M * (kLBN / 8); u += kLThreads) {
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    const int S = p.splits, rank = (int)cluster_ctarank();
+    const uint32_t base = smem_u32(part);
+    if (!*abort_flag) {
+      for (int u = rank * kLThreads + tid; u < p.M * (kLBN / 8); u += S * kLThreads) {
         const int um = u >> 3, g8 = u & 7;
-        const float* base = p.acc + (size_t)um * p.N + n0 + 8 * g8;
+        const uint32_t o0 = (uint32_t)(um * kLBN + 4 * ((2 * g8) ^ (um & 15))) * 4u;
+        const uint32_t o1 = (uint32_t)(um * kLBN + 4 * ((2 * g8 + 1) ^ (um & 15))) * 4u;
         float x8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) x8[e] = 0.f;
-#pragma unroll 4
-        for (int sp = 0; sp < p.splits; ++sp) {
-          const float4 a0 = __ldcg(reinterpret_cast<const float4*>(base + sp * slice));
-          const float4 a1 = __ldcg(reinterpret_cast<const float4*>(base + sp * slice) + 1);
+        for (int sp = 0; sp < S; ++sp) {
+          const float4 a0 = ld_shared_cluster_f32x4(map_shared_rank(base + o0, (uint32_t)sp));
+          const float4 a1 = ld_shared_cluster_f32x4(map_shared_rank(base + o1, (uint32_t)sp));
           x8[0] += a0.x, x8[1] += a0.y, x8[2] += a0.z, x8[3] += a0.w;
           x8[4] += a1.x, x8[5] += a1.y, x8[6] += a1.z, x8[7] += a1.w;
         }
         store8(um, g8, x8);
       }
     }
+    cluster_arrive_release();
+    cluster_wait_acquire();
   }
 
   // drain: every load this CTA issued has landed (the last one into each
@@ -216,14 +223,11 @@ static int max_splits(int32_t K) {
   return half < 1 ? 1 : (half < kLMaxSplits ? half : kLMaxSplits);
 }
 
-int64_t linear_workspace_bytes(int32_t M, int32_t N, int32_t K) {
-  // the split-K partial slices and one ticket per band, 256-byte aligned
-  return ((int64_t)max_splits(K) * M * N * 4 + 255) / 256 * 256 + ((int64_t)(N / kLBN) * 4 + 255) / 256 * 256;
-}
+int64_t linear_workspace_bytes(int32_t, int32_t, int32_t) { return 0; }
 
 bool linear_supported() { return tc::encode_fn() != nullptr; }
 
-cudaError_t launch_linear(LinearArgs p, const void* x, int64_t x_stride, const void* w, void* workspace,
+cudaError_t launch_linear(LinearArgs p, const void* x, int64_t x_stride, const void* w, void*,
                           cudaStream_t stream) {
   if (p.M == 0 || p.N == 0) return cudaSuccess;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -234,18 +238,11 @@ cudaError_t launch_linear(LinearArgs p, const void* x, int64_t x_stride, const v
     return cudaErrorInvalidValue;
   const int bands = p.N / kLBN;
   // as many K splits as keep every CTA slot of the SMs busy in one wave
-  // (each split at least two K steps, at most kLMaxSplits)
+  // (each split at least two K steps, at most one cluster of kLMaxSplits)
   int splits = (kLCtasPerSm * sm_count_linear()) / bands;
   if (splits > max_splits(p.K)) splits = max_splits(p.K);
   if (splits < 1) splits = 1;
   p.splits = splits;
-  if (splits > 1) {
-    const size_t part_bytes = ((size_t)max_splits(p.K) * p.M * p.N * 4 + 255) / 256 * 256;
-    p.acc = static_cast<float*>(workspace);
-    p.tickets = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + part_bytes);
-    cudaError_t e = cudaMemsetAsync(p.tickets, 0, (size_t)bands * 4, stream);
-    if (e != cudaSuccess) return e;
-  }
   const uint32_t stage_bytes = (uint32_t)((p.M + 7) / 8) * 1024 + kLWTile;
   int stages = (int)(kLStageBudget / stage_bytes);
   p.stages = stages < kLMaxStages ? (stages < 2 ? 2 : stages) : kLMaxStages;
@@ -253,7 +250,20 @@ cudaError_t launch_linear(LinearArgs p, const void* x, int64_t x_stride, const v
   const uint32_t smem = (uint32_t)p.stages * stage_bytes + (kLBM * 128 - (x_tile < kLBM * 128 ? x_tile : kLBM * 128)) + 1024;
   cudaError_t e = cudaFuncSetAttribute(linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  linear_kernel<<<dim3((unsigned)bands, (unsigned)splits), kLThreads, smem, stream>>>(p, mx, mw);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)bands, (unsigned)splits);
+  cfg.blockDim = dim3(kLThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)splits;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = splits > 1 ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, linear_kernel, p, mx, mw);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

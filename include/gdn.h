@@ -342,8 +342,10 @@ gdn_status gdn_gated_rmsnorm(const gdn_dims* dims, int64_t rows, const float* o,
  * y            [M][y_stride] bf16 (y_stride >= N, a multiple of 8); must not
  *              overlap x, w, bias or the workspace.
  * workspace    device scratch of gdn_linear_workspace_size bytes, 256-byte
- *              aligned, contents irrelevant (the part that needs it is
- *              zeroed on the stream by the call).
+ *              aligned; may be NULL when that size is 0 (it is 0 for every
+ *              shape this version accepts: narrow outputs split K over a
+ *              thread-block cluster that adds the partial sums in its own
+ *              shared memory, in split order).
  *
  * Errors: GDN_ERR_INVALID_ARG (sizes, NULL pointers, strides),
  * GDN_ERR_ALIGN, GDN_ERR_ALIAS, GDN_ERR_UNSUPPORTED (no TMA encoder in the
@@ -353,10 +355,9 @@ gdn_status gdn_linear(int32_t M, int32_t N, int32_t K, const void* x, int64_t x_
                       const void* w, const float* bias, void* y, int64_t y_stride,
                       void* workspace, int64_t workspace_bytes, void* stream);
 
-/* Workspace bytes gdn_linear needs for M, N, K: fp32 [M][N] partial sums
- * for each of up to min(16, K / 128) K splits and one 4-byte ticket per 64
- * output features, each part rounded up to 256 bytes. The result does not
- * depend on the order in which the splits finish. */
+/* Workspace bytes gdn_linear needs for M, N, K (0 in this version: the K
+ * splits of narrow outputs, at most min(8, K / 128), are summed in shared
+ * memory; the result does not depend on the order in which they finish). */
 gdn_status gdn_linear_workspace_size(int32_t M, int32_t N, int32_t K, int64_t* bytes);
 
 /*

@@ -320,3 +320,38 @@ def test_selftest_wait_timeout_rejects_bad_arguments(lib):
     assert f(999, VP(0x1000), None) == 1
     assert f(10_000_000_001, VP(0x1000), None) == 1
     assert f(1_000_000, None, None) == 1
+
+
+def test_linear_needs_no_workspace_and_rejects_bad_arguments(lib):
+    """gdn_linear: narrow outputs sum their K splits inside a thread-block
+    cluster, so the workspace size is 0 and NULL is accepted; sizes, strides
+    and alignment are checked before anything is launched."""
+    for mnk in ((1, 64, 64), (64, 2048, 4096), (128, 12352, 2048)):
+        assert gdn.gdn_linear_workspace_size(*mnk) == 0
+    f = lib.gdn_linear
+    ok = [64, 2048, 4096, VP(0x10000), 4096, VP(0x100000000), None, VP(0x200000000), 2048, None, 0, None]
+    bad = list(ok)
+    bad[0] = 0  # no rows
+    assert f(*bad) == 1
+    bad = list(ok)
+    bad[0] = 129  # more rows than one MMA
+    assert f(*bad) == 1
+    bad = list(ok)
+    bad[1] = 96  # N not a multiple of 64
+    assert f(*bad) == 1
+    bad = list(ok)
+    bad[4] = 4092  # x rows closer than K
+    assert f(*bad) == 1
+    bad = list(ok)
+    bad[3] = VP(0x10008)  # x not 16-byte aligned
+    assert f(*bad) == 5
+    bad = list(ok)
+    bad[7] = VP(0x10000 + 64)  # y overlapping x
+    assert f(*bad) == 4
+    d = gdn.dims(16, 32, 128)
+    # the decode layer's workspace: the activations between its three calls only
+    C, vw, Hv = (2 * 16 + 32) * 128, 32 * 128, 32
+    align = lambda n: (n + 255) // 256 * 256
+    B = 64
+    expect = (align(B * C * 2) + align(B * vw * 2) + 2 * align(B * Hv * 2) + align(B * vw * 2))
+    assert gdn.gdn_decode_layer_workspace_size(d, 2048, B) == expect
