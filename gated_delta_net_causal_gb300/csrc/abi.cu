@@ -71,7 +71,7 @@ gdn_status decode_impl(const gdn_dims* dims, int32_t batch, int32_t tokens, cons
                        int32_t num_slots, const void* mixed_qkv, const void* a, const void* b,
                        const float* decay_param, const float* dt_bias, const void* conv_w,
                        void* conv_state, float* state, float* core_out, const void* z,
-                       const float* norm_w, void* out, void* stream) {
+                       const float* norm_w, void* out, void* stream, bool overlap_prev = false) {
   gdn_status st = check_dims(dims);
   if (st != GDN_OK) return st;
   if (batch < 0 || num_slots < 0 || tokens < 1) return GDN_ERR_INVALID_ARG;
@@ -141,6 +141,7 @@ gdn_status decode_impl(const gdn_dims* dims, int32_t batch, int32_t tokens, cons
   p.l2_eps = dims->l2_eps;
   p.rms_eps = dims->rms_eps;
   p.scale = 1.0f / sqrtf((float)D);
+  p.overlap_prev = overlap_prev ? 1 : 0;
   if (tokens > 1)
     return cuda_status(gdn::launch_decode_multi(p, dims->io_dtype, dims->head_dim, batch,
                                                 static_cast<cudaStream_t>(stream)));
@@ -559,12 +560,17 @@ gdn_status gdn_decode_layer(const gdn_dims* dims, int32_t hidden, int32_t batch,
   pin.route.dst[3] = aa;
   st = cuda_status(gdn::launch_linear(pin, x, hidden, w->w_in, lin, s));
   if (st != GDN_OK) return st;
-  // (2) the core with its fused gated RMSNorm
+  // (2) the core with its fused gated RMSNorm, launched to overlap (1)'s
+  // tail: (1) writes only the projections in the workspace, so the state
+  // rows stream in while it drains and the activations are read after it
+  // has completed
   st = decode_impl(dims, batch, 1, nullptr, batch, qkv, aa, bb, w->decay_param, w->dt_bias, w->conv_w,
-                   conv_state, state, nullptr, z, w->norm_w, yc, stream);
+                   conv_state, state, nullptr, z, w->norm_w, yc, stream, true);
   if (st != GDN_OK) return st;
-  // (3) the output projection
+  // (3) the output projection, overlapping (2)'s tail the same way: its
+  // weight tiles load while (2) drains, its input after (2) has completed
   gdn::LinearArgs pout{};
+  pout.overlap_prev = 1;
   pout.M = batch;
   pout.N = hidden;
   pout.K = (int32_t)l.vw;

@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   }
   __syncthreads();
   volatile int* abort_flag = &s_abort;
+  grid_launch_dependents();
 
   // state slot of batch row b, or -1 for a padded or out-of-range row (the
   // plain call is compiled without the table: slot b, never -1)
@@ -149,6 +150,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
+  // The producer streams state rows at once; the consumers read the
+  // activations, which the preceding kernel may have written, only after it
+  // has completed (nothing to wait for without an overlapped launch).
+  grid_dependency_wait();
   const size_t C = (size_t)p.C;
   const int qk_f = Hk * D;
   const T* w = static_cast<const T*>(p.conv_w);
@@ -451,7 +456,18 @@ static cudaError_t launch_decode_t(const DecodeArgs& p, int32_t batch, cudaStrea
   if (e != cudaSuccess) return e;
   const int items = batch * p.Hk;
   const int grid = items < sm_count() ? items : sm_count();
-  kern<<<grid, kDecThreads, smem, stream>>>(p, items);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.overlap_prev ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, p, items);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -238,6 +238,20 @@ __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// ------------------------------------------- PTX: programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the preceding kernel on the stream still runs. grid_dependency_wait()
+// returns once that kernel has completed and its writes are visible to the
+// calling thread (at once when the launch carries no such dependency);
+// grid_launch_dependents() lets the next kernel of that kind start once every
+// CTA of this grid has called it or exited.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------ PTX: cluster
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release;" ::: "memory");

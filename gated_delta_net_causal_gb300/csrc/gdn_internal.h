@@ -31,6 +31,10 @@ struct DecodeArgs {
   int32_t tokens;
   int32_t Hk, Hv, rep, map, decay, C;
   float l2_eps, rms_eps, scale;
+  // launched to overlap the preceding kernel on the stream (programmatic
+  // dependent launch): set only where that kernel is known not to write the
+  // state, the conv state or any weight (inside gdn_decode_layer)
+  int32_t overlap_prev;
 };
 
 // Linear layer y = x W^T (+ bias) (linear.cu): output column n goes to
@@ -49,6 +53,9 @@ struct LinearArgs {
   int32_t M, N, K, splits, stages;  // splits and stages are chosen by launch_linear
   const float* bias;        // [N] or null
   LinearRoute route;
+  // launched to overlap the preceding kernel (programmatic dependent
+  // launch): set only where that kernel does not write w or the bias
+  int32_t overlap_prev;
 };
 
 struct ConvArgs {

@@ -80,12 +80,24 @@ __global__ void __launch_bounds__(kLThreads, kLCtasPerSm)
   const uint32_t tb = s_tmem;
   volatile int* abort_flag = &s_abort;
   uint32_t n_loads = 0;
+  grid_launch_dependents();
 
   if (warp == 0 && lane == 0) {
-    // producer: stage i % S holds K step k_begin + i
-    for (int i = 0; i < k_len; ++i) {
+    // producer: stage i % S holds K step k_begin + i. The first S stages'
+    // weight tiles go out before x, which the preceding kernel may have
+    // written, is read (after it has completed; at once without an
+    // overlapped launch)
+    const int first = k_len < stages ? k_len : stages;
+    for (int i = 0; i < first; ++i) {
+      mbar_arrive_expect_tx(&full[i], (uint32_t)p.M * (kLBK * 2) + kLWTile);
+      ++n_loads;
+      tc::tma_load_2d(sm + i * stage_bytes + x_tile, &tm_w, (k_begin + i) * kLBK, n0, &full[i]);
+    }
+    grid_dependency_wait();
+    for (int i = 0; i < first; ++i) tc::tma_load_2d(sm + i * stage_bytes, &tm_x, (k_begin + i) * kLBK, 0, &full[i]);
+    for (int i = first; i < k_len; ++i) {
       const int s = i % stages;
-      if (i >= stages && !mbar_wait_bounded(&empty[s], ((i / stages) - 1) & 1, abort_flag)) break;
+      if (!mbar_wait_bounded(&empty[s], ((i / stages) - 1) & 1, abort_flag)) break;
       mbar_arrive_expect_tx(&full[s], (uint32_t)p.M * (kLBK * 2) + kLWTile);
       ++n_loads;
       const int kx = (k_begin + i) * kLBK;
@@ -260,8 +272,16 @@ cudaError_t launch_linear(LinearArgs p, const void* x, int64_t x_stride, const v
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = (unsigned)splits;
   attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = splits > 1 ? 1 : 0;
+  cudaLaunchAttribute attr2[2];
+  int na = 0;
+  if (splits > 1) attr2[na++] = attr[0];
+  if (p.overlap_prev) {
+    attr2[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr2[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr2;
+  cfg.numAttrs = (unsigned)na;
   e = cudaLaunchKernelEx(&cfg, linear_kernel, p, mx, mw);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
