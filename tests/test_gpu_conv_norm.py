@@ -31,6 +31,25 @@ def test_conv_update_varlen(dtype, lengths):
         assert_lowp(y.cpu(), ry, dtype, f"conv y {lengths}", rel=1e-5)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("hk,hv,D", [(1, 1, 32), (1, 3, 64)])
+def test_conv_update_partial_channel_tile(dtype, hk, hv, D):
+    """Channel counts (96, 320) that leave the last 512-byte channel tile
+    partly empty, with sequences crossing the 64-token tiles."""
+    shape = gi.Shape(hk, hv, D, dtype=dtype)
+    lengths = [70, 3, 0, 130, 1]
+    data = gi.small_shape_inputs(50 + D + hv, shape, lengths)
+    x, w, cs = data["inputs"].mixed_qkv, data["weights"].conv_w, data["conv_state"]
+    d = gdn.dims(hk, hv, D, io_dtype=gi.DTYPES[dtype])
+    xs, csd = cuda(x), cuda(cs)
+    y = torch.full_like(xs, float("nan"))
+    gdn.gdn_conv_update(d, cuda(data["cu_seqlens"]), xs, cuda(w), csd, y)
+    torch.cuda.synchronize()
+    ry, rcs = oracle.conv_varlen(F64(x), F64(w), F64(cs), data["cu_seqlens"].numpy())
+    assert np.array_equal(F64(csd.cpu()), rcs), "conv state must be a bit copy"
+    assert_lowp(y.cpu(), ry, dtype, f"conv y C={(2 * hk + hv) * D}", rel=1e-5)
+
+
 def test_conv_update_large_batch_tail_tiles():
     """Many sequences and a token count that is not a multiple of the tile."""
     shape = gi.Shape(4, 8, 128, dtype="bf16")
