@@ -33,13 +33,17 @@ constexpr int kLBN = 64;   // output features per CTA
 constexpr int kLBK = 64;   // K per stage (one 128-byte swizzle atom of bf16)
 constexpr uint32_t kLWTile = kLBN * kLBK * 2;  // 8 KB
 // A stage is the x tile (M rounded up to 8 rows of 128 bytes, so a multiple
-// of 1024 bytes) then the W tile; as many stages as fit in 96 KB, two CTAs
-// per SM. The MMA reads 128 rows of x from
+// of 1024 bytes) then the W tile; as many stages as fit in the ring budget
+// below. The MMA reads 128 rows of x from
 // each stage's start, so the allocation ends 128 x 128 bytes past the last
 // stage's start at least (the rows past M it reads are never used).
 constexpr int kLMaxStages = 12;
-constexpr uint32_t kLStageBudget = 96 * 1024;
-constexpr int kLCtasPerSm = 2;
+// three CTAs per SM with a 64 KB ring from 32 rows of x up (more weight
+// streams in flight, K split over more CTAs), two with a 96 KB ring below
+// (a small x tile leaves the smaller ring too few bytes in flight)
+constexpr int kLCtasPerSm = 3;
+__host__ __device__ constexpr int linear_ctas_per_sm(int32_t M) { return M >= 32 ? 3 : 2; }
+__host__ __device__ constexpr uint32_t linear_stage_budget(int32_t M) { return M >= 32 ? 64 * 1024 : 96 * 1024; }
 constexpr int kLThreads = 128;  // warp 0 lane 0 loads, warp 1 issues MMAs, all four store
 constexpr int kLMaxSplits = 8;  // the portable cluster size
 
@@ -251,12 +255,12 @@ cudaError_t launch_linear(LinearArgs p, const void* x, int64_t x_stride, const v
   const int bands = p.N / kLBN;
   // as many K splits as keep every CTA slot of the SMs busy in one wave
   // (each split at least two K steps, at most one cluster of kLMaxSplits)
-  int splits = (kLCtasPerSm * sm_count_linear()) / bands;
+  int splits = (linear_ctas_per_sm(p.M) * sm_count_linear()) / bands;
   if (splits > max_splits(p.K)) splits = max_splits(p.K);
   if (splits < 1) splits = 1;
   p.splits = splits;
   const uint32_t stage_bytes = (uint32_t)((p.M + 7) / 8) * 1024 + kLWTile;
-  int stages = (int)(kLStageBudget / stage_bytes);
+  int stages = (int)(linear_stage_budget(p.M) / stage_bytes);
   p.stages = stages < kLMaxStages ? (stages < 2 ? 2 : stages) : kLMaxStages;
   const uint32_t x_tile = stage_bytes - kLWTile;
   const uint32_t smem = (uint32_t)p.stages * stage_bytes + (kLBM * 128 - (x_tile < kLBM * 128 ? x_tile : kLBM * 128)) + 1024;
