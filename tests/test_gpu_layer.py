@@ -36,11 +36,14 @@ def _assert_linear(y_gpu, x, w, bias, what):
 @pytest.mark.gpu
 @pytest.mark.parametrize("M,N,K,with_bias,pad", [(1, 128, 64, False, 0), (3, 192, 256, True, 8),
                                                   (64, 12352, 2048, False, 0), (64, 2048, 4096, True, 0),
-                                                  (128, 256, 512, False, 24), (17, 64, 1024, True, 0)])
+                                                  (128, 256, 512, False, 24), (17, 64, 1024, True, 0),
+                                                  (31, 2048, 4096, True, 0), (32, 2048, 4096, False, 8),
+                                                  (33, 12352, 2048, True, 0)])
 def test_linear_matches_the_oracle(M, N, K, with_bias, pad):
     """Shapes of the fused input projection (N=12352), the split-K output
-    projection (N=2048, K=4096), the MMA's full 128 rows, a single row, and
-    strided rows of x and y."""
+    projection (N=2048, K=4096), the MMA's full 128 rows, a single row,
+    strided rows of x and y, and row counts on both sides of the switch
+    between the two ring sizes (32 rows)."""
     g = gi.rng(100 + M + N + K)
     x = _bf(g, (M, K + pad), 1.0)
     w = _bf(g, (N, K), 1.0 / np.sqrt(K))
@@ -85,7 +88,8 @@ def _run_layer(d, hidden, w, t):
 @pytest.mark.gpu
 @pytest.mark.parametrize("Hk,Hv,D,hidden,B,biases", [(2, 8, 64, 128, 3, True),
                                                      (16, 32, 128, 2048, 64, False),
-                                                     (16, 32, 128, 2048, 1, True)])
+                                                     (16, 32, 128, 2048, 1, True),
+                                                     (4, 16, 96, 512, 32, True)])
 def test_decode_layer(Hk, Hv, D, hidden, B, biases):
     shape, w, t, C, vw, n_in = _layer_case(700 + B + Hk, Hk, Hv, D, hidden, B, biases)
     d = gdn.dims(Hk, Hv, D, map=shape.map, decay=shape.decay, io_dtype=BF)
