@@ -359,14 +359,15 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
     }
   }
   __syncthreads();
+  // (each thread finishes its own elements; sc[r][31] is not rewritten)
   for (int e = tid; e < p.rep * kC; e += kPrepThreads) {
     const int r = e >> 6, t = e & 63;
-    if (t >= 32) sc[r][t] += sc[r][31];
-  }
-  __syncthreads();
-  for (int e = tid; e < p.rep * kC; e += kPrepThreads) {
-    const int r = e >> 6, t = e & 63;
-    sgam[r][t] = expf(sc[r][t]);
+    float c = sc[r][t];
+    if (t >= 32) {
+      c += sc[r][31];
+      sc[r][t] = c;
+    }
+    sgam[r][t] = expf(c);
   }
   __syncthreads();
 
@@ -571,7 +572,10 @@ __global__ void __launch_bounds__(kPrepThreads, 4)
       vv[2 * kC + t] = live ? sgam[r][t] * sinvq[t] : 0.f;
       vv[3 * kC + t] = t == 0 ? sgam[r][L - 1] : 0.f;
     }
-    __syncthreads();  // A and Tm are rewritten for the next V head
+    // no barrier here: the next V head's A/P build writes only A (every
+    // read of it ended before the doubling's last barrier) and global P;
+    // Tm, which this head's Tb rows still read, is rewritten only past the
+    // barrier that ends that build
   }
   tc::fence_before_sync();
   __syncthreads();
