@@ -15,16 +15,20 @@
 // Structure (as in decode.cu): a persistent kernel, a work item is one
 // (sequence, K head) pair with its V heads. Two CTAs share each SM where
 // their shared memory fits (up to four V heads per K head), so one CTA's
-// per-item prologue and output loads overlap the other's state stream. One
-// producer warp
-// streams the item's state rows through a shared-memory ring with 1-D bulk
-// copies, eight consumer warps update the rows. Per item the consumer warps
-// (1) run the conv over the item's q, k and v channels for all T tokens from
-// the old conv state (and write the new one: this CTA alone owns those
-// channels), and the gates; barrier; (2) each warp takes the l2 norms of every
-// token's q and k; (3) the state pass, T tokens per row; barrier; (4) the
-// outputs of every (head, token) pair, one warp per pair. The per-item
-// buffers are single: barrier (1)->(2) of the next item orders them.
+// per-item prologue and outputs overlap the other's state stream. One
+// producer warp streams the item's state rows through a shared-memory ring
+// with 1-D bulk copies, eight consumer warps update the rows. Per item the
+// consumer warps (1) run the conv over the item's q, k and v channels for
+// all T tokens from the old conv state (and write the new one: this CTA
+// alone owns those channels), and the gates; barrier; (2) each warp takes
+// the l2 norms of every token's q and k; (3) the state pass, T tokens per
+// row; barrier; (4) the outputs of every (head, token) pair, one warp per
+// pair. The per-item buffers are single: barrier (1)->(2) of the next item
+// orders them. With 16-bit activations, where shared memory allows, the
+// item's conv inputs (old conv state, the T tokens' inputs) arrive by
+// asynchronous copies into a staging area during the previous item's state
+// pass, and its z rows during its own, so neither (1) nor (4) waits on
+// global memory.
 //
 // Every wait is bounded; a wait that gives up records GDN_ERR_TIMEOUT and
 // raises a CTA-wide abort flag, after which no warp waits again.
@@ -44,7 +48,7 @@ constexpr int kMtMaxStages = 16;
 // per row, NV4 groups of four columns per lane (16 columns at D = 32, 64,
 // 128; eight lanes of 12 at D = 96, three rows per lane so that a chunk is a
 // whole 96-row head).
-template <int D, int REPMAX>
+template <typename T, int D, int REPMAX>
 struct MtGeom {
   static constexpr int LPR = D == 96 ? 8 : D / 16;  // lanes per row
   static constexpr int NV4 = D / (4 * LPR);
@@ -61,12 +65,39 @@ struct MtGeom {
   // two CTAs per SM (112 KB each) while that leaves a ring of two 32 KB slots
   static constexpr int CTAS_PER_SM = REPMAX <= 4 ? 2 : 1;
   static constexpr int RING_AVAIL = (CTAS_PER_SM == 2 ? 112 : 227) * 1024 - STATIC_BYTES;
-  static constexpr int RING_CAP = RING_AVAIL < 192 * 1024 ? RING_AVAIL : 192 * 1024;
-  static constexpr int STAGES_RAW = RING_CAP / (int)SLOT_BYTES;
-  static constexpr int STAGES = STAGES_RAW < kMtMaxStages ? STAGES_RAW : kMtMaxStages;
+  static constexpr int stages_in(int bytes) {
+    return (bytes < 192 * 1024 ? bytes : 192 * 1024) / (int)SLOT_BYTES < kMtMaxStages
+               ? (bytes < 192 * 1024 ? bytes : 192 * 1024) / (int)SLOT_BYTES
+               : kMtMaxStages;
+  }
+  // Staging area (behind the ring) for the global inputs of an item's
+  // prologue and outputs: the conv state and the T tokens' inputs of its
+  // NCH channels, and its z rows. Used with 16-bit activations where it
+  // leaves the ring at least min(its plain depth, 4) stages.
+  static constexpr int NCH = (2 + REPMAX) * D;
+  static constexpr int STG_X = kMtTMax * NCH;            // elements: [T][NCH]
+  static constexpr int STG_CS = 3 * NCH;                 // [NCH][3]
+  static constexpr int STG_Z = REPMAX * kMtTMax * D;     // [REPMAX][T][D]
+  static constexpr int STG_BYTES = (STG_X + STG_CS + STG_Z) * (int)sizeof(T);
+  static constexpr int STAGES_PLAIN = stages_in(RING_AVAIL);
+  static constexpr int STAGES_STG = stages_in(RING_AVAIL - STG_BYTES);
+  static constexpr bool STAGED =
+      sizeof(T) == 2 && STAGES_STG >= (STAGES_PLAIN < 4 ? STAGES_PLAIN : 4);
+  static constexpr int STAGES = STAGED ? STAGES_STG : STAGES_PLAIN;
   static constexpr int RING_BYTES = STAGES * (int)SLOT_BYTES;
+  static constexpr int DYN_BYTES = RING_BYTES + (STAGED ? STG_BYTES : 0);
   static_assert(STAGES >= 2, "ring too small");
+  static_assert((D * sizeof(T)) % 16 == 0 && RING_BYTES % 16 == 0 && (STG_X * sizeof(T)) % 16 == 0 &&
+                    (STG_CS * sizeof(T)) % 16 == 0,
+                "16-byte copy granules");
 };
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ bool mt_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   return mbar_wait_bounded(bar, parity, abort_flag);
@@ -77,12 +108,13 @@ __device__ __forceinline__ void mt_consumer_sync() {
 }
 
 template <typename T, int D, int REPMAX>
-__global__ void __launch_bounds__(kMtThreads, 2)
+__global__ void __launch_bounds__(kMtThreads, MtGeom<T, D, REPMAX>::CTAS_PER_SM)
     decode_multi_kernel(const DecodeArgs p, const int num_items) {
-  using G = MtGeom<D, REPMAX>;
+  using G = MtGeom<T, D, REPMAX>;
   constexpr int LPR = G::LPR, RPW = G::RPW, STAGES = G::STAGES, NV4 = G::NV4, RPL = G::RPL;
   constexpr int NC = kMtCW * 32;
   constexpr int PER = D / 32;  // output elements per lane
+  static_assert(REPMAX * kMtTMax <= NC, "one (head, token) gate per consumer thread");
 
   extern __shared__ __align__(128) float ring[];
   __shared__ float sq[kMtTMax][D], sk[kMtTMax][D];
@@ -140,6 +172,58 @@ __global__ void __launch_bounds__(kMtThreads, 2)
   if (p.z != nullptr)
     for (int j = tid; j < D; j += NC) snw[j] = p.norm_w[j];
 
+  // first global channel of channel group g (q, k, then V head g - 2) of K head kh
+  auto group_base = [&](int g, int kh) -> int {
+    if (g < 2) return g * qk_f + kh * D;
+    const int h = p.map == GDN_MAP_TILED ? kh + (g - 2) * Hk : kh * rep + (g - 2);
+    return 2 * qk_f + h * D;
+  };
+  // The staging area (16-bit activations): [T][NCH] inputs and [NCH][3] conv
+  // state of the item's channels, [REPMAX][T][D] z. An item's conv inputs are
+  // copied in while the previous item streams its state, its z rows while
+  // its own state streams: every copy is issued after an item's first
+  // barrier and waited for before its third, so the barriers order them.
+  T* const stg_x = reinterpret_cast<T*>(reinterpret_cast<char*>(ring) + G::RING_BYTES);
+  T* const stg_cs = stg_x + G::STG_X;
+  T* const stg_z = stg_cs + G::STG_CS;
+  constexpr int GR = D * (int)sizeof(T) / 16;  // 16-byte granules of D elements
+  auto stage_conv = [&](int it) {
+    if (it >= num_items) return;
+    const int b = it / Hk, kh = it - (it / Hk) * Hk;
+    const char* xsrc = static_cast<const char*>(p.mixed_qkv) + (size_t)b * NT * C * sizeof(T);
+    const char* csrc = static_cast<const char*>(p.conv_state) + (size_t)b * C * 3 * sizeof(T);
+    const int ng = 2 + rep, n_cs = ng * 3 * GR, n_all = n_cs + NT * ng * GR;
+    for (int q = tid; q < n_all; q += NC) {
+      if (q < n_cs) {
+        const int g = q / (3 * GR), o = q - g * (3 * GR);
+        cp_async16(reinterpret_cast<char*>(stg_cs + g * 3 * D) + o * 16,
+                   csrc + (size_t)group_base(g, kh) * 3 * sizeof(T) + o * 16);
+      } else {
+        const int j = q - n_cs, t = j / (ng * GR), rr = j - t * (ng * GR);
+        const int g = rr / GR, o = rr - g * GR;
+        cp_async16(reinterpret_cast<char*>(stg_x + t * G::NCH + g * D) + o * 16,
+                   xsrc + ((size_t)t * C + group_base(g, kh)) * sizeof(T) + o * 16);
+      }
+    }
+  };
+  auto stage_z = [&](int it) {
+    if (p.z == nullptr) return;
+    const int b = it / Hk, kh = it - (it / Hk) * Hk;
+    for (int q = tid; q < rep * NT * GR; q += NC) {
+      const int pr = q / GR, o = q - pr * GR, r = pr / NT, t = pr - r * NT;
+      const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
+      cp_async16(reinterpret_cast<char*>(stg_z + (r * kMtTMax + t) * D) + o * 16,
+                 static_cast<const char*>(p.z) + (((size_t)b * NT + t) * Hv + h) * D * sizeof(T) +
+                     o * 16);
+    }
+  };
+  if constexpr (G::STAGED) {
+    stage_conv(blockIdx.x);
+    cp_async_commit();
+    cp_async_wait_all();
+    mt_consumer_sync();
+  }
+
   uint32_t k = 0;
   for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
     const int b = item / Hk, kh = item - (item / Hk) * Hk;
@@ -147,26 +231,41 @@ __global__ void __launch_bounds__(kMtThreads, 2)
     T* cst = static_cast<T*>(p.conv_state) + (size_t)b * C * 3;
 
     // (1) conv + SiLU of the item's channels [q of kh | k of kh | v of each
-    // head] for every token, rolling the 3-wide window through the tokens
+    // head] for every token, rolling the 3-wide window through the tokens,
+    // then the gates (their inputs loaded first, so they arrive during the
+    // conv)
+    float ga = 0.f, gb = 0.f, gp = 0.f, gd = 0.f;
+    const int gr = tid / NT, gt = tid - (tid / NT) * NT;  // this thread's (head, token) gate
+    const bool has_gate = tid < rep * NT;
+    if (has_gate) {
+      const int h = p.map == GDN_MAP_TILED ? kh + gr * Hk : kh * rep + gr;
+      const size_t gi = ((size_t)b * NT + gt) * Hv + h;
+      ga = to_f32(static_cast<const T*>(p.a)[gi]);
+      gb = to_f32(static_cast<const T*>(p.b)[gi]);
+      gp = p.decay_param[h];
+      gd = p.dt_bias[h];
+    }
     const int nch = (2 + rep) * D;
     for (int idx = tid; idx < nch; idx += NC) {
       const int which = idx / D, i = idx - which * D;
-      int c;
-      float* dst;
-      if (which < 2) {
-        c = which * qk_f + kh * D + i;
-        dst = which == 0 ? &sq[0][i] : &sk[0][i];
-      } else {
-        const int r = which - 2;
-        const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
-        c = 2 * qk_f + h * D + i;
-        dst = &sv[r][0][i];
-      }
+      const int c = group_base(which, kh) + i;
+      float* dst = which == 0 ? &sq[0][i] : which == 1 ? &sk[0][i] : &sv[which - 2][0][i];
       T* cp = cst + (size_t)c * 3;
-      T a0 = cp[0], a1 = cp[1], a2 = cp[2];
+      T a0, a1, a2;
       T xv[kMtTMax];
+      if constexpr (G::STAGED) {
+        a0 = stg_cs[idx * 3 + 0];
+        a1 = stg_cs[idx * 3 + 1];
+        a2 = stg_cs[idx * 3 + 2];
 #pragma unroll
-      for (int t = 0; t < kMtTMax; ++t) xv[t] = t < NT ? xb[(size_t)t * C + c] : T();
+        for (int t = 0; t < kMtTMax; ++t) xv[t] = t < NT ? stg_x[t * G::NCH + idx] : T();
+      } else {
+        a0 = cp[0];
+        a1 = cp[1];
+        a2 = cp[2];
+#pragma unroll
+        for (int t = 0; t < kMtTMax; ++t) xv[t] = t < NT ? xb[(size_t)t * C + c] : T();
+      }
       const float w0 = to_f32(w[(size_t)c * 4 + 0]), w1 = to_f32(w[(size_t)c * 4 + 1]);
       const float w2 = to_f32(w[(size_t)c * 4 + 2]), w3 = to_f32(w[(size_t)c * 4 + 3]);
 #pragma unroll
@@ -188,15 +287,16 @@ __global__ void __launch_bounds__(kMtThreads, 2)
         cp[2] = a2;
       }
     }
-    for (int j = tid; j < rep * NT; j += NC) {
-      const int r = j / NT, t = j - (j / NT) * NT;
-      const int h = p.map == GDN_MAP_TILED ? kh + r * Hk : kh * rep + r;
-      const size_t gi = ((size_t)b * NT + t) * Hv + h;
-      sgate[r][t][0] = expf(gate_g(p.decay, p.decay_param[h], p.dt_bias[h],
-                                   to_f32(static_cast<const T*>(p.a)[gi])));
-      sgate[r][t][1] = sigmoid_f(to_f32(static_cast<const T*>(p.b)[gi]));
+    if (has_gate) {
+      sgate[gr][gt][0] = expf(gate_g(p.decay, gp, gd, ga));
+      sgate[gr][gt][1] = sigmoid_f(gb);
     }
     mt_consumer_sync();
+    if constexpr (G::STAGED) {
+      stage_conv(item + gridDim.x);
+      stage_z(item);
+      cp_async_commit();
+    }
 
     // (2) warp t: the l2 norms of token t's q and k and their product, then
     // k normalised and q normalised and scaled, in place (the one-token
@@ -291,6 +391,7 @@ __global__ void __launch_bounds__(kMtThreads, 2)
         if (lane == 0) mbar_arrive(&empty_bar[slot]);
       }
     }
+    if constexpr (G::STAGED) cp_async_wait_all();  // the next item's inputs, this item's z
     mt_consumer_sync();
 
     // (4) outputs: one warp per (head, token) pair
@@ -312,7 +413,8 @@ __global__ void __launch_bounds__(kMtThreads, 2)
           for (int e = 0; e < PER; ++e) ss += ov[e] * ov[e];
           ss = group_sum<32>(ss);
           const float inv = 1.f / sqrtf(ss / (float)D + p.rms_eps);
-          const T* zr = static_cast<const T*>(p.z) + obase;
+          const T* zr = G::STAGED ? stg_z + (r * kMtTMax + t) * D + lane * PER
+                                  : static_cast<const T*>(p.z) + obase;
           T* outr = static_cast<T*>(p.out) + obase;
 #pragma unroll
           for (int e = 0; e < PER; ++e)
@@ -339,7 +441,7 @@ int mt_sm_count() {
 template <typename T, int D, int REPMAX>
 cudaError_t launch_mt_t(const DecodeArgs& p, int32_t batch, cudaStream_t stream) {
   auto kern = decode_multi_kernel<T, D, REPMAX>;
-  const int smem = MtGeom<D, REPMAX>::RING_BYTES;
+  const int smem = MtGeom<T, D, REPMAX>::DYN_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // resident CTAs per SM as the runtime computes them, asked once per variant
