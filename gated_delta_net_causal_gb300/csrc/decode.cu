@@ -155,9 +155,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
-  // The producer streams state rows at once; the consumers read the
-  // activations, which the preceding kernel may have written, only after it
-  // has completed (nothing to wait for without an overlapped launch).
+  // The consumers read the activations, which the preceding kernel may have
+  // written, only after it has completed (with overlap_prev the producer is
+  // already streaming state rows meanwhile).
   grid_dependency_wait();
   const size_t C = (size_t)p.C;
   const int qk_f = Hk * D;
