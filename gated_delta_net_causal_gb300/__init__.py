@@ -69,6 +69,8 @@ def library() -> ctypes.CDLL:
         L.gdn_status_string.argtypes = [i32]
         L.gdn_version.restype = i32
         L.gdn_version.argtypes = []
+        L.gdn_host_pointer.restype = ctypes.c_int
+        L.gdn_host_pointer.argtypes = [vp, ctypes.POINTER(vp)]
         L.gdn_qkv_features.restype = i64
         L.gdn_qkv_features.argtypes = [pd]
         L.gdn_conv_update.restype = ctypes.c_int
@@ -117,18 +119,29 @@ def _check(status: int, what: str):
         raise GdnError(status, f"{what}: {status_string(status)}")
 
 
-def _ptr(t: Optional[torch.Tensor], name: str, dtype=None) -> Optional[int]:
+def gdn_host_pointer(t: torch.Tensor) -> int:
+    """The device address of a pinned host tensor's data (gdn_host_pointer)."""
+    dev = ctypes.c_void_p()
+    _check(library().gdn_host_pointer(ctypes.c_void_p(t.data_ptr()), ctypes.byref(dev)),
+           "gdn_host_pointer")
+    return int(dev.value)
+
+
+def _ptr(t: Optional[torch.Tensor], name: str, dtype=None, host_ok: bool = False) -> Optional[int]:
+    """A tensor argument's device address. With host_ok a pinned host tensor
+    is accepted too and passed as its mapped device address (the kernel then
+    reads or writes it over the host link)."""
     if t is None:
         return None
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_cuda and not (host_ok and t.device.type == "cpu" and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or pinned host memory" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    return t.data_ptr()
+    return t.data_ptr() if t.is_cuda else gdn_host_pointer(t)
 
 
 def _shape(d: GdnDims):
@@ -197,17 +210,21 @@ def _check_decode_sizes(d, batch, tokens, slots, mixed_qkv, a, b, decay_param, d
 
 def gdn_decode_step(d: GdnDims, mixed_qkv, a, b, decay_param, dt_bias, conv_w, conv_state,
                     state, core_out=None, z=None, norm_w=None, out=None, stream=None):
+    """mixed_qkv, a, b, z, core_out and out may be pinned host tensors: the
+    kernel reads and writes them in place over the host link."""
     io = _io(d)
     batch = mixed_qkv.shape[0]
     _check_decode_sizes(d, batch, 1, batch, mixed_qkv, a, b, decay_param, dt_bias, conv_w,
                         conv_state, state, core_out, z, norm_w, out)
     f32 = torch.float32
     _check(library().gdn_decode_step(
-        ctypes.byref(d), batch, _ptr(mixed_qkv, "mixed_qkv", io), _ptr(a, "a", io),
-        _ptr(b, "b", io), _ptr(decay_param, "decay_param", f32), _ptr(dt_bias, "dt_bias", f32),
-        _ptr(conv_w, "conv_w", io), _ptr(conv_state, "conv_state", io),
-        _ptr(state, "state", f32), _ptr(core_out, "core_out", f32), _ptr(z, "z", io),
-        _ptr(norm_w, "norm_w", f32), _ptr(out, "out", io), _stream(stream)), "gdn_decode_step")
+        ctypes.byref(d), batch, _ptr(mixed_qkv, "mixed_qkv", io, True), _ptr(a, "a", io, True),
+        _ptr(b, "b", io, True), _ptr(decay_param, "decay_param", f32),
+        _ptr(dt_bias, "dt_bias", f32), _ptr(conv_w, "conv_w", io),
+        _ptr(conv_state, "conv_state", io), _ptr(state, "state", f32),
+        _ptr(core_out, "core_out", f32, True), _ptr(z, "z", io, True),
+        _ptr(norm_w, "norm_w", f32), _ptr(out, "out", io, True), _stream(stream)),
+        "gdn_decode_step")
     return core_out, out
 
 
@@ -487,7 +504,7 @@ __all__ = ["GdnDims", "GdnError", "dims", "library", "status_string", "gdn_conv_
            "gdn_prefill_chunked_static", "GDN_STATIC_SCRATCH_BYTES", "gdn_gated_rmsnorm", "gdn_device_error",
            "gdn_selftest_wait_timeout", "gdn_linear", "gdn_linear_workspace_size", "gdn_decode_layer",
            "gdn_decode_layer_workspace_size", "GdnLayerWeights",
-           "gdn_qkv_features", "gdn_version", "GDN_MAP_GROUPED", "GDN_MAP_TILED",
+           "gdn_qkv_features", "gdn_version", "gdn_host_pointer", "GDN_MAP_GROUPED", "GDN_MAP_TILED",
            "GDN_DECAY_LOG_RATE", "GDN_DECAY_NEGATIVE_RATE", "GDN_F16", "GDN_BF16", "GDN_F32",
            "GDN_QK_PRENORMALIZED", "GDN_GATES_PRECOMPUTED", "GDN_PREFILL_CUDA_CORES",
            "GDN_PREFILL_CARRY_WHOLE", "GDN_PREFILL_CARRY_SLICED", "LIB_PATH"]

@@ -176,7 +176,18 @@ const char* gdn_status_string(int32_t status) {
   }
 }
 
-int32_t gdn_version(void) { return 300; }
+int32_t gdn_version(void) { return 400; }
+
+gdn_status gdn_host_pointer(const void* host, void** device) {
+  if (host == nullptr || device == nullptr) return GDN_ERR_INVALID_ARG;
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, const_cast<void*>(host), 0) != cudaSuccess || d == nullptr) {
+    cudaGetLastError();  // not mapped: the error must not surface at the caller's next call
+    return GDN_ERR_INVALID_ARG;
+  }
+  *device = d;
+  return GDN_OK;
+}
 
 int64_t gdn_qkv_features(const gdn_dims* dims) {
   if (check_dims(dims) != GDN_OK) return -1;

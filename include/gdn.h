@@ -16,7 +16,9 @@
  * Conventions shared by every call:
  *  - Every pointer is a DEVICE pointer the caller owns (allocated with
  *    cudaMalloc or by a framework allocator); the library never allocates,
- *    frees or retains one past the call. All work is enqueued on `stream`
+ *    frees or retains one past the call. The one exception is noted at
+ *    gdn_decode_step: its activations and outputs may also be mapped pinned
+ *    host memory (gdn_host_pointer). All work is enqueued on `stream`
  *    (a cudaStream_t; NULL = the legacy default stream) and is asynchronous.
  *  - Arguments are validated on the host before anything is enqueued; on an
  *    error nothing is launched and the status says why. A failed launch
@@ -90,7 +92,8 @@ typedef struct gdn_dims {
 const char* gdn_status_string(int32_t status);
 
 /* ABI version: major * 10000 + minor * 100 + patch. 0.3.0 added
- * gdn_decode_multi and gdn_decode_step_slots. */
+ * gdn_decode_multi and gdn_decode_step_slots; 0.4.0 gdn_linear,
+ * gdn_decode_layer and gdn_host_pointer. */
 int32_t gdn_version(void);
 
 /* Channels of the packed pre-conv activation: C = 2*Hk*D + Hv*D, laid out
@@ -149,6 +152,12 @@ gdn_status gdn_conv_update(const gdn_dims* dims, int32_t num_seqs, const int32_t
  * norm_w       [D] fp32 RMSNorm weight (shared by all heads); needed with z.
  * out          [B][Hv][D] io dtype gated-RMSNorm output; needed with z.
  * At least one of core_out and (z, out) must be given. Hv/Hk <= 16.
+ * mixed_qkv, a, b, z, core_out and out may be device addresses of mapped
+ * pinned host memory (gdn_host_pointer): the kernel then reads the
+ * activations and writes the outputs in place over the host link, with no
+ * separate copy (on a coherent host link such as Grace's, the cheapest way
+ * to feed one serving step from the host). Every other pointer, of this and
+ * every other call, must be device memory.
  */
 gdn_status gdn_decode_step(const gdn_dims* dims, int32_t batch, const void* mixed_qkv,
                            const void* a, const void* b, const float* decay_param,
@@ -411,6 +420,16 @@ gdn_status gdn_decode_layer(const gdn_dims* dims, int32_t hidden, int32_t batch,
  * workspace for the larger of its two calls, each rounded up to 256 bytes. */
 gdn_status gdn_decode_layer_workspace_size(const gdn_dims* dims, int32_t hidden, int32_t batch,
                                            int64_t* bytes);
+
+/*
+ * The device address of pinned host memory (cudaHostAlloc, or page-locked
+ * by a framework's pinned allocator), for the arguments of gdn_decode_step
+ * that accept it. Writes *device and returns GDN_OK if the runtime reports
+ * host as mapped into the device's address space; GDN_ERR_INVALID_ARG for a
+ * NULL argument or memory that is not (pageable memory, device memory).
+ * Allocates nothing; the mapping lives as long as the allocation.
+ */
+gdn_status gdn_host_pointer(const void* host, void** device);
 
 /*
  * Device-side error word: kernels whose bounded waits give up record a

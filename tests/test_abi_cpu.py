@@ -355,3 +355,23 @@ def test_linear_needs_no_workspace_and_rejects_bad_arguments(lib):
     B = 64
     expect = (align(B * C * 2) + align(B * vw * 2) + 2 * align(B * Hv * 2) + align(B * vw * 2))
     assert gdn.gdn_decode_layer_workspace_size(d, 2048, B) == expect
+
+
+def test_host_pointer_rejects_null_and_the_binding_rejects_pageable_memory(lib):
+    """gdn_host_pointer checks its arguments before any CUDA call; the
+    binding takes pinned host memory only where the call allows it, and never
+    pageable memory."""
+    import torch
+    import gated_delta_net_causal_gb300 as gdn
+    out = ctypes.c_void_p()
+    assert lib.gdn_host_pointer(None, ctypes.byref(out)) == 1
+    buf = ctypes.create_string_buffer(64)
+    assert lib.gdn_host_pointer(ctypes.cast(buf, ctypes.c_void_p), None) == 1
+    d = gdn.dims(2, 4, 128, io_dtype=torch.bfloat16)
+    C = gdn.gdn_qkv_features(d)
+    bf, f32 = torch.bfloat16, torch.float32
+    args = (torch.zeros(2, C, dtype=bf), torch.zeros(2, 4, dtype=bf), torch.zeros(2, 4, dtype=bf),
+            torch.zeros(4), torch.zeros(4), torch.zeros(C, 4, dtype=bf),
+            torch.zeros(2, C, 3, dtype=bf), torch.zeros(2, 4, 128, 128, dtype=f32))
+    with pytest.raises(ValueError, match="pinned host memory"):
+        gdn.gdn_decode_step(d, *args, core_out=torch.zeros(2, 4, 128))

@@ -141,3 +141,34 @@ def test_decode_tagged_heads_read_the_mapped_k_head():
         torch.cuda.synchronize()
         rc, _, _, _ = decode_reference(shape, w, x, F64(cs), F64(S), with_norm=False)
         assert_abs(core, rc, DECODE_OUT_ABS, f"tagged heads map={mp}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_reads_and_writes_pinned_host_memory(dtype):
+    """Activations, z and both outputs in mapped pinned host memory (read and
+    written by the kernel over the host link): the same bits as the call on
+    device copies, for several steps in a row."""
+    import gated_delta_net_causal_gb300 as gdn
+    shape = gi.Shape(2, 4, 128, map=gi.TILED, decay=gi.NEGATIVE_RATE, dtype=dtype)
+    g = gi.rng(91)
+    w = gi.layer_weights(g, shape)
+    cs0, S0 = gi.conv_state(g, shape, 5), gi.delta_state(g, shape, 5)
+    dev = DecodeRunner(shape, w, cs0, S0)
+    host = DecodeRunner(shape, w, cs0, S0)
+    io = gi.DTYPES[dtype]
+    for step in range(3):
+        x = gi.step_inputs(g, shape, 5)
+        B, Hv, D = 5, shape.n_v_heads, shape.head_dim
+        pin = {k: getattr(x, k).contiguous().pin_memory() for k in ("mixed_qkv", "a", "b", "z")}
+        assert gdn.gdn_host_pointer(pin["a"]) != 0
+        core_h = torch.full((B, Hv, D), float("nan")).pin_memory()
+        out_h = torch.full((B, Hv, D), float("nan"), dtype=io).pin_memory()
+        gdn.gdn_decode_step(host.d, pin["mixed_qkv"], pin["a"], pin["b"], host.w["decay_param"],
+                            host.w["dt_bias"], host.w["conv_w"], host.conv_state, host.state,
+                            core_out=core_h, z=pin["z"].view(B, Hv, D), norm_w=host.w["norm_w"],
+                            out=out_h)
+        core_d, out_d = dev.step(x)
+        torch.cuda.synchronize()
+        assert torch.equal(core_h, core_d.cpu()), f"step {step}: core output"
+        assert torch.equal(out_h, out_d.cpu()), f"step {step}: gated output"
+        assert torch.equal(host.state, dev.state) and torch.equal(host.conv_state, dev.conv_state)
