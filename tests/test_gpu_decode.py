@@ -7,7 +7,7 @@ import torch
 import gdn_inputs as gi
 import oracle
 from tests.gpu_helpers import (DECODE_OUT_ABS, DECODE_STATE_REL, DecodeRunner, F64, assert_abs,
-                               assert_gated, assert_state_rel, decode_reference)
+                               assert_gated, assert_state_rel, cuda, decode_reference)
 
 pytestmark = pytest.mark.gpu
 
@@ -172,3 +172,64 @@ def test_decode_reads_and_writes_pinned_host_memory(dtype):
         assert torch.equal(core_h, core_d.cpu()), f"step {step}: core output"
         assert torch.equal(out_h, out_d.cpu()), f"step {step}: gated output"
         assert torch.equal(host.state, dev.state) and torch.equal(host.conv_state, dev.conv_state)
+
+
+# With decays near 1 the state keeps every step's rounding, so errors of
+# successive steps add: ten times the single-step state bound after 32 steps
+# (the fp32 rounding of 32 kept steps is a few 1e-6 of the state's largest
+# magnitude; a dropped decay moves it by about 3e-2 over those steps, a sign
+# error by its own size).
+LONG_STATE_REL = 10 * DECODE_STATE_REL
+
+
+@pytest.mark.parametrize("mp,dec", [(gi.GROUPED, gi.LOG_RATE), (gi.TILED, gi.NEGATIVE_RATE)])
+def test_decode_long_memory_many_steps(mp, dec):
+    """32 consecutive steps with decay rates of about 1e-3 per token
+    (A_log = ln U[5e-4, 2e-3], so the state carries across all of them):
+    every step's outputs against the oracle at the decode bounds, the state
+    within LONG_STATE_REL; then the same 32 tokens as four 8-token
+    gdn_decode_multi calls from the same start, against the same oracle."""
+    import gated_delta_net_causal_gb300 as gdn
+    shape = gi.Shape(2, 4, 128, map=mp, decay=dec, dtype="bf16")
+    B, steps = 3, 32
+    g = gi.rng(777)
+    a_log = np.log(g.uniform(5e-4, 2e-3, size=shape.n_v_heads))
+    w = gi.layer_weights(g, shape, a_log=a_log)
+    cs0 = gi.conv_state(g, shape, B, std=0.1)
+    S0 = gi.delta_state(g, shape, B, std=0.05)
+    xs = [gi.step_inputs(g, shape, B) for _ in range(steps)]
+    g_tok, _ = oracle.gates(F64(xs[0].a), F64(xs[0].b), F64(w.decay_param), F64(w.dt_bias), dec)
+    assert float(np.median(g_tok)) > -5e-3, "the case must have long memory"
+
+    run = DecodeRunner(shape, w, cs0, S0)
+    cs, S = F64(cs0), F64(S0)
+    refs = []
+    for step, x in enumerate(xs):
+        core_out, out = run.step(x)
+        torch.cuda.synchronize()
+        rc, ry, cs, S = decode_reference(shape, w, x, cs, S)
+        refs.append(rc)
+        tag = f"{shape} long-memory step {step}"
+        assert_abs(core_out, rc, DECODE_OUT_ABS, tag + " core")
+        assert_gated(out, ry, rc, x.z, w.norm_w, shape.dtype, tag + " gated norm",
+                     core_gpu=core_out)
+        assert_state_rel(run.state, S, LONG_STATE_REL, tag + " state")
+        assert np.array_equal(F64(run.conv_state.cpu()), cs), tag + " conv state (bitwise)"
+
+    multi = DecodeRunner(shape, w, cs0, S0)
+    Hv, D = shape.n_v_heads, shape.head_dim
+    for c in range(steps // 8):
+        blk = xs[8 * c:8 * c + 8]
+
+        def stack(name):
+            return cuda(torch.stack([getattr(s, name).reshape(B, -1) for s in blk], dim=1))
+        core = torch.full((B, 8, Hv, D), float("nan"), device="cuda")
+        gdn.gdn_decode_multi(multi.d, stack("mixed_qkv"), stack("a"), stack("b"),
+                             multi.w["decay_param"], multi.w["dt_bias"], multi.w["conv_w"],
+                             multi.conv_state, multi.state, core_out=core)
+        torch.cuda.synchronize()
+        for t in range(8):
+            assert_abs(core[:, t], refs[8 * c + t], DECODE_OUT_ABS, f"multi call {c} token {t}")
+    assert_state_rel(multi.state, S, LONG_STATE_REL, "multi-token long-memory state")
+    assert np.array_equal(F64(multi.conv_state.cpu()), cs), "multi-token conv state (bitwise)"
+    assert gdn.gdn_device_error() == 0
