@@ -395,8 +395,10 @@ typedef struct gdn_layer_weights {
  * One decode step of a whole gated delta-net layer for a batch of
  * sequences, one token each: the fused input projection (qkv | z | b | a in
  * one gdn_linear launch), gdn_decode_step with its fused gated RMSNorm, and
- * the output projection. Three kernel launches (plus the split-K zeroing of
- * the output projection's accumulator).
+ * the output projection. Three kernel launches; the second and third start
+ * while their predecessor inside the call drains (programmatic dependent
+ * launch), reading only what that predecessor does not write until it has
+ * completed.
  * -- libmir-metal decode/mod.rs, `build`: qkv projection -> `convolve` ->
  *    `split_qkv` -> gate/beta/alpha projections -> `recurrence` ->
  *    `rms_norm` -> `precise_gate` -> output projection.
