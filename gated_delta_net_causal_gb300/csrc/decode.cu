@@ -126,11 +126,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   if (warp == kDecCW) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      // Every launch may overlap its predecessor's tail (programmatic
-      // dependent launch): the state rows are read only once the preceding
-      // kernel, which may have written them, has completed, except where
-      // the caller knows it wrote no state (the decode layer's projection).
-      if (!p.overlap_prev) grid_dependency_wait();
       uint32_t k = 0;
       for (int item = blockIdx.x; item < num_items; item += gridDim.x) {
         const int b = item / Hk, kh = item - (item / Hk) * Hk;
@@ -155,9 +150,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
-  // The consumers read the activations, which the preceding kernel may have
-  // written, only after it has completed (with overlap_prev the producer is
-  // already streaming state rows meanwhile).
+  // The producer streams state rows at once; the consumers read the
+  // activations, which the preceding kernel may have written, only after it
+  // has completed (nothing to wait for without an overlapped launch).
   grid_dependency_wait();
   const size_t C = (size_t)p.C;
   const int qk_f = Hk * D;
@@ -470,7 +465,7 @@ static cudaError_t launch_decode_t(const DecodeArgs& p, int32_t batch, cudaStrea
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.overlap_prev ? 1 : 0;
   e = cudaLaunchKernelEx(&cfg, kern, p, items);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -31,11 +31,9 @@ struct DecodeArgs {
   int32_t tokens;
   int32_t Hk, Hv, rep, map, decay, C;
   float l2_eps, rms_eps, scale;
-  // The one-token kernel is always launched to overlap the preceding
-  // kernel's tail (programmatic dependent launch) and waits for it before
-  // touching memory; with overlap_prev its producer streams state rows
-  // before that wait: set only where the preceding kernel is known not to
-  // write the state, the conv state or any weight (inside gdn_decode_layer)
+  // launched to overlap the preceding kernel on the stream (programmatic
+  // dependent launch): set only where that kernel is known not to write the
+  // state, the conv state or any weight (inside gdn_decode_layer)
   int32_t overlap_prev;
 };
 
